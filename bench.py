@@ -1,0 +1,298 @@
+"""Benchmark of the exact, order-invariant softmax reduction on one GB300 (or N replicas).
+
+Metric: exact attention MACs/s on the long-context causal workload (B1 H16 S4096 D128
+bf16, 1% of K rows x8), MACs = B * Hq * P * 2D with P the unmasked (query, key) pairs.
+A step is one pass of the whole attention path through the C ABI: rowmax over all keys,
+exact accumulate (NUM/DEN digits, canonical), finalize to f32 - the kernels of det_attn.
+Inputs are resident in HBM when the timed region starts; L2 is flushed (a 512 MiB write)
+between timed steps, outside the per-step CUDA events.
+
+Under torchrun (N > 1) every rank runs its own independent problem of the same shape
+(weak scaling; the path partitions by (batch, head) with no exchange), the timed region
+is bracketed by barriers, and rank 0 reports total MACs / max time over ranks.
+
+--impl reference times the oracle (the exact C implementation, as it stands) on the host
+cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes as C
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "exact attention MACs/s (S=4096,D=128,bf16) and % of binding INT/FP64 pipe peak"
+UNIT = "MAC/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={q}", "--format=csv,noheader",
+                                       "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1].split()[0]))
+                smax.append(float(parts[2].split()[0]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample(w, Q, K, V, rows_per_head: int, nthreads: int):
+    """Time the oracle's fused pass on sampled query rows; returns (MACs, seconds, sample)."""
+    from oracle import native
+    native.build()
+    A = native.Attn(Q, K, V, w.causal, w.scale)
+    rng = np.random.default_rng(0)
+    rows = []
+    for h in range(w.Hq):
+        for i in rng.choice(w.S, size=rows_per_head, replace=False):
+            rows.append(h * w.S + int(i))
+    rows = np.asarray(rows, dtype=np.int64)
+    keys = (rows % w.S) + 1 if w.causal else np.full(len(rows), w.S)
+    macs = int(keys.sum()) * 2 * w.D
+    t0 = time.perf_counter()
+    A.forward_rows(rows=rows, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return macs, dt, f"{len(rows)} query rows ({rows_per_head} per head, seeded), all their keys"
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = W.c3()
+    Q, K, V = w.tensors("cpu")
+    cores = os.cpu_count() or 1
+    rows_per_head = args.ref_rows
+    vals = []
+    for s in range(args.warmup + args.steps):
+        macs, dt, sample = oracle_sample(w, Q, K, V, rows_per_head, cores)
+        if s >= args.warmup:
+            vals.append(macs / dt)
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "S": w.S, "D": w.D, "causal": True},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import bitwise_deterministic_shard_gb300 as da
+    da.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    w = W.c3()
+    if rank > 0:
+        w.seed = w.seed + 1000 * rank          # an independent problem per rank
+    Qh, Kh, Vh = w.tensors("cpu")
+    Q, K, V = Qh.to(dev), Kh.to(dev), Vh.to(dev)
+    P = da._Problem(Q, K, V, True, None)
+    L = da.lib()
+    ws = torch.empty(L.da_workspace_bytes(P.ref(), 1), dtype=torch.uint8, device=dev)
+    rows = w.B * w.Hq * w.S
+    m = torch.empty(rows, dtype=torch.float32, device=dev)
+    num = torch.empty(rows, 15, w.D, dtype=torch.int64, device=dev)
+    den = torch.empty(rows, 6, dtype=torch.int64, device=dev)
+    out = torch.empty(w.B, w.Hq, w.S, w.D, dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    sp = C.c_void_p(stream.cuda_stream)
+
+    def ptr(t):
+        return C.c_void_p(t.data_ptr())
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        assert L.da_rowmax(P.ref(), 0, w.S, ptr(m), sp) == 0
+        if ev:
+            ev[1].record(stream)
+        assert L.da_accumulate(P.ref(), ptr(m), 0, w.S, ptr(num), ptr(den), 0, sp) == 0
+        if ev:
+            ev[2].record(stream)
+        assert L.da_finalize(ptr(num), ptr(den), w.B, w.Hq, w.S, w.D, ptr(out), None, sp) == 0
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = Clocks(local_rank) if rank == 0 else None
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        step(evs[s])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t0
+    ck = clocks.stop() if clocks else None
+    k_rowmax = [e[0].elapsed_time(e[1]) for e in evs]
+    k_acc = [e[1].elapsed_time(e[2]) for e in evs]
+    k_fin = [e[2].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # --- end to end through the C ABI with host buffers (pinned), copies inside the region
+    Qp, Kp, Vp = Qh.pin_memory(), Kh.pin_memory(), Vh.pin_memory()
+    outp = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    Qe, Ke, Ve = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    Pe = da._Problem(Qe, Ke, Ve, True, None)
+
+    def e2e_step():
+        Qe.copy_(Qp, non_blocking=True)
+        Ke.copy_(Kp, non_blocking=True)
+        Ve.copy_(Vp, non_blocking=True)
+        assert L.da_det_attn(Pe.ref(), ptr(out), ptr(ws), ws.numel(), sp) == 0
+        outp.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    assert torch.equal(outp, out.cpu())
+    h2d = (Qh.numel() + Kh.numel() + Vh.numel()) * Qh.element_size()
+    d2h = out.numel() * 4
+
+    if rank != 0:
+        return
+    macs = w.attn_macs
+    value = macs * world / (ms * 1e-3)
+    e2e_val = macs * world / (statistics.mean(e2e_ms) * 1e-3)
+    # roofline of the dominant kernel (accumulate): integer multiply-add pipe
+    pk = _peaks()
+    sm_clock = (ck or {}).get("sm_mhz") or pk.get("clocks_under_load", {}).get("sm_mhz_median") or 1447.0
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    imadw_per_clk_sm = float(os.environ.get("DA_IMADWIDE_PER_CLK_SM", "32"))
+    peak = n_sm * imadw_per_clk_sm * sm_clock * 1e6 / 1e12           # T IMAD.WIDE / s at the sampled clock
+    acc_ms = statistics.mean(k_acc)
+    acc_ops = w.pairs * 4 * w.D                                       # D score + 3D PV multiply-adds per pair
+    achieved = acc_ops / (acc_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": True,
+                   "input_dtype": "bf16", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed between timed steps (512 MiB write, outside the step events)",
+                   "attn_macs_per_step": macs, "pairs_per_step": w.pairs},
+        "method_macs_per_s": w.pairs * 3 * w.D * world / (ms * 1e-3),
+        "kernels_ms": {"rowmax": statistics.mean(k_rowmax), "accumulate": acc_ms, "finalize": statistics.mean(k_fin)},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "T IMAD.WIDE/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "accumulate", "peak_basis": f"{n_sm} SMs x {imadw_per_clk_sm:g} IMAD.WIDE/clk/SM x "
+                                                           f"{sm_clock:g} MHz (sampled SM clock)"},
+        "clocks": ck,
+        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": statistics.mean(e2e_ms)},
+        "gpu_launches": 3 * args.steps,
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline:
+        macs_c, dt_c, sample = oracle_sample(w, Qh, Kh, Vh, args.ref_rows, os.cpu_count() or 1)
+        line["cpu_baseline"] = {"value": macs_c / dt_c, "unit": UNIT, "cores": os.cpu_count() or 1, "kind": "oracle",
+                                "sample": sample, "seconds": dt_c}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=16, help="oracle sample: query rows per head")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        torch.distributed.init_process_group("nccl")
+    elif world > 1:
+        torch.distributed.init_process_group("gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

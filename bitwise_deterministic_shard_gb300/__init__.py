@@ -1,0 +1,311 @@
+"""Python binding of libdetattn, the C ABI of the exact, order-invariant softmax reduction.
+
+Argument marshalling only: every step of the computation runs in the CUDA kernels behind
+include/detattn.h.  PyTorch supplies device memory and the current stream.  There is no
+CPU fallback: if the library is not built, or a tensor is not on a CUDA device, the call
+raises.
+
+Names follow the pages: det-attn ("API": det_attn, rowmax, accumulate, finalize,
+det_attn_sharded) and det-cross-entropy ("API": rowmax, denom_digits, finalize; here
+dce_rowmax, dce_denom_digits, dce_finalize).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdetattn.so")
+
+NUM_NDIG, DEN_NDIG = 15, 6
+NUM_E0, DEN_E0 = -320, -160
+STATUS_NONFINITE, STATUS_ROWMAX_VIOLATION, STATUS_DIGIT_HEADROOM, STATUS_BAD_TARGET = 1, 2, 4, 8
+
+
+class DetAttnError(RuntimeError):
+    pass
+
+
+class _Tensor(C.Structure):
+    _fields_ = [("ptr", C.c_void_p), ("dtype", C.c_int32), ("B", C.c_int64), ("H", C.c_int64), ("S", C.c_int64),
+                ("D", C.c_int64), ("stride", C.c_int64 * 4)]
+
+
+class _Desc(C.Structure):
+    _fields_ = [("q", _Tensor), ("k", _Tensor), ("v", _Tensor), ("causal", C.c_int32), ("scale", C.c_float),
+                ("dev_status", C.c_void_p)]
+
+
+class _Matrix(C.Structure):
+    _fields_ = [("ptr", C.c_void_p), ("dtype", C.c_int32), ("rows", C.c_int64), ("cols", C.c_int64),
+                ("row_stride", C.c_int64)]
+
+
+_lib = None
+_P, _I64, _I32 = C.c_void_p, C.c_int64, C.c_int
+
+
+def lib():
+    """The loaded libdetattn.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise DetAttnError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+        L = C.CDLL(LIB_PATH)
+        L.da_abi_version.restype = C.c_int
+        L.da_status_string.argtypes = [C.c_int]
+        L.da_status_string.restype = C.c_char_p
+        D = C.POINTER(_Desc)
+        M = C.POINTER(_Matrix)
+        L.da_rowmax.argtypes = [D, _I64, _I64, _P, _P]
+        L.da_accumulate.argtypes = [D, _P, _I64, _I64, _P, _P, _I32, _P]
+        L.da_compose_max.argtypes = [_P, _P, _I64, _P]
+        L.da_compose_add.argtypes = [_P, _P, _I64, _P]
+        L.da_normalize.argtypes = [_P, _I64, _I32, _I64, _P, _P]
+        L.da_finalize.argtypes = [_P, _P, _I64, _I64, _I64, _I64, _P, _P, _P]
+        L.da_workspace_bytes.argtypes = [D, _I32]
+        L.da_workspace_bytes.restype = C.c_size_t
+        L.da_det_attn.argtypes = [D, _P, _P, C.c_size_t, _P]
+        L.da_det_attn_sharded.argtypes = [D, _P, _I32, _P, _P, _P, C.c_size_t, _P]
+        L.dce_rowmax.argtypes = [M, _I64, _I64, _P, _P, _P]
+        L.dce_denom_digits.argtypes = [M, _P, _I64, _I64, _P, _I32, _P, _P]
+        L.dce_finalize.argtypes = [_P, M, _P, _P, _P, _P, _P, _P]
+        for f in ("da_rowmax", "da_accumulate", "da_compose_max", "da_compose_add", "da_normalize", "da_finalize",
+                  "da_det_attn", "da_det_attn_sharded", "dce_rowmax", "dce_denom_digits", "dce_finalize"):
+            getattr(L, f).restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise DetAttnError(f"{what}: {lib().da_status_string(code).decode()} (code {code})")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return 0
+    if t.dtype == torch.bfloat16:
+        return 1
+    raise DetAttnError(f"unsupported dtype {t.dtype}: f32 and bf16 only")
+
+
+def _cuda(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise DetAttnError(f"{name} must be a CUDA tensor (there is no CPU path)")
+
+
+def _tensor(t: torch.Tensor, name: str) -> _Tensor:
+    _cuda(t, name)
+    if t.dim() != 4:
+        raise DetAttnError(f"{name} must be [B, H, S, D]")
+    if t.stride(3) != 1:
+        t = t.contiguous()
+    x = _Tensor()
+    x.ptr = t.data_ptr()
+    x.dtype = _dtype_code(t)
+    x.B, x.H, x.S, x.D = t.shape
+    for i in range(4):
+        x.stride[i] = t.stride(i)
+    return x
+
+
+def _stream():
+    return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+class _Problem:
+    """Keeps the tensors alive while their descriptor is in use."""
+
+    def __init__(self, Q, K, V, causal, scale, status=None):
+        self.keep = [t if t.stride(3) == 1 else t.contiguous() for t in (Q, K, V)]
+        Q, K, V = self.keep
+        self.desc = _Desc()
+        self.desc.q, self.desc.k, self.desc.v = _tensor(Q, "Q"), _tensor(K, "K"), _tensor(V, "V")
+        self.desc.causal = 1 if causal else 0
+        self.desc.scale = math.nan if scale is None else float(scale)
+        self.desc.dev_status = None if status is None else status.data_ptr()
+        self.B, self.Hq, self.Sq, self.D = Q.shape
+        self.Skv = K.shape[2]
+        self.device = Q.device
+
+    def ref(self):
+        return C.byref(self.desc)
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed device status word for the `status=` arguments."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def read_status(status: torch.Tensor) -> int:
+    return int(status.item())
+
+
+def workspace_bytes(Q, K, V, causal=False, scale=None, nsplits=1) -> int:
+    P = _Problem(Q, K, V, causal, scale)
+    return int(lib().da_workspace_bytes(P.ref(), nsplits))
+
+
+def _workspace(P: _Problem, nsplits: int, ws):
+    need = int(lib().da_workspace_bytes(P.ref(), nsplits))
+    if ws is None or ws.numel() * ws.element_size() < need:
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=P.device)
+    return ws
+
+
+def det_attn(Q, K, V, causal=False, scale=None, out=None, workspace=None, status=None):
+    """Fused deterministic attention (det-attn "API": det_attn); f32 output [B, Hq, Sq, D]."""
+    P = _Problem(Q, K, V, causal, scale, status)
+    out = torch.empty(P.B, P.Hq, P.Sq, P.D, dtype=torch.float32, device=P.device) if out is None else out
+    ws = _workspace(P, 1, workspace)
+    _check(lib().da_det_attn(P.ref(), _ptr(out), _ptr(ws), ws.numel(), _stream()), "det_attn")
+    return out
+
+
+def det_attn_sharded(Q, K, V, kv_splits, causal=False, scale=None, order=None, out=None, workspace=None,
+                     status=None):
+    """KV-shard composition (det-attn "API": det_attn_sharded), bit-identical to det_attn
+    for any kv_splits and any visiting order."""
+    P = _Problem(Q, K, V, causal, scale, status)
+    n = len(kv_splits)
+    splits = (C.c_int64 * n)(*[int(x) for x in kv_splits])
+    ordv = None if order is None else (C.c_int32 * n)(*[int(x) for x in order])
+    out = torch.empty(P.B, P.Hq, P.Sq, P.D, dtype=torch.float32, device=P.device) if out is None else out
+    ws = _workspace(P, n, workspace)
+    _check(lib().da_det_attn_sharded(P.ref(), splits, n, ordv, _ptr(out), _ptr(ws), ws.numel(), _stream()),
+           "det_attn_sharded")
+    return out
+
+
+def rowmax(Q, K, kv_lo=0, kv_hi=None, causal=False, scale=None, out=None, status=None):
+    """Per-query rowmax over keys [kv_lo, kv_hi) (det-attn "API": rowmax); f32 [B, Hq, Sq].
+    Shards combine with compose_max (or torch.maximum)."""
+    P = _Problem(Q, K, K, causal, scale, status)
+    kv_hi = P.Skv if kv_hi is None else kv_hi
+    m = torch.empty(P.B, P.Hq, P.Sq, dtype=torch.float32, device=P.device) if out is None else out
+    _check(lib().da_rowmax(P.ref(), kv_lo, kv_hi, _ptr(m), _stream()), "rowmax")
+    return m
+
+
+def accumulate(Q, K, V, m, kv_lo=0, kv_hi=None, causal=False, scale=None, num=None, den=None, add_into=False,
+               status=None):
+    """Exact NUM/DEN digits of keys [kv_lo, kv_hi) with the global rowmax m (det-attn "API":
+    accumulate).  Returns (num int64 [B,Hq,Sq,15,D], den int64 [B,Hq,Sq,6]), canonical."""
+    P = _Problem(Q, K, V, causal, scale, status)
+    kv_hi = P.Skv if kv_hi is None else kv_hi
+    if num is None:
+        num = torch.empty(P.B, P.Hq, P.Sq, NUM_NDIG, P.D, dtype=torch.int64, device=P.device)
+    if den is None:
+        den = torch.empty(P.B, P.Hq, P.Sq, DEN_NDIG, dtype=torch.int64, device=P.device)
+    m = m.contiguous()
+    _check(lib().da_accumulate(P.ref(), _ptr(m), kv_lo, kv_hi, _ptr(num), _ptr(den), 1 if add_into else 0,
+                               _stream()), "accumulate")
+    return num, den
+
+
+def compose_max(dst, src):
+    """dst = max(dst, src) elementwise (shard rowmax composition), in place."""
+    _check(lib().da_compose_max(_ptr(dst), _ptr(src), dst.numel(), _stream()), "compose_max")
+    return dst
+
+
+def compose_add(dst, src):
+    """dst += src elementwise (int64 digit composition), in place."""
+    _check(lib().da_compose_add(_ptr(dst), _ptr(src), dst.numel(), _stream()), "compose_add")
+    return dst
+
+
+def normalize(digits, status=None):
+    """Canonical form, in place, of NUM [..., 15, D] or DEN [..., 6] digit arrays."""
+    if digits.shape[-1] == DEN_NDIG and (digits.dim() < 2 or digits.shape[-2] != NUM_NDIG):
+        nrows, ndig, inner = digits.numel() // DEN_NDIG, DEN_NDIG, 1
+    else:
+        ndig, inner = digits.shape[-2], digits.shape[-1]
+        nrows = digits.numel() // (ndig * inner)
+    _check(lib().da_normalize(_ptr(digits), nrows, ndig, inner, _ptr(status), _stream()), "normalize")
+    return digits
+
+
+def finalize(num, den, out=None, status=None):
+    """Digits -> f32 output (det-attn "API": finalize): RN32(RN64(RN64(NUM)/RN64(DEN)))."""
+    B, H, S, _, D = num.shape
+    out = torch.empty(B, H, S, D, dtype=torch.float32, device=num.device) if out is None else out
+    _check(lib().da_finalize(_ptr(num), _ptr(den), B, H, S, D, _ptr(out), _ptr(status), _stream()), "finalize")
+    return out
+
+
+def _matrix(x: torch.Tensor) -> tuple[_Matrix, torch.Tensor]:
+    _cuda(x, "logits")
+    if x.dim() != 2:
+        raise DetAttnError("logits must be [N, V]")
+    if x.stride(1) != 1:
+        x = x.contiguous()
+    m = _Matrix()
+    m.ptr = x.data_ptr()
+    m.dtype = _dtype_code(x)
+    m.rows, m.cols = x.shape
+    m.row_stride = x.stride(0)
+    return m, x
+
+
+def dce_rowmax(logits, v_lo=0, v_hi=None, out=None, status=None):
+    """Per-token max over the vocab range [v_lo, v_hi) (det-cross-entropy "API": rowmax)."""
+    M, keep = _matrix(logits)
+    v_hi = M.cols if v_hi is None else v_hi
+    m = torch.empty(M.rows, dtype=torch.float32, device=logits.device) if out is None else out
+    _check(lib().dce_rowmax(C.byref(M), v_lo, v_hi, _ptr(m), _ptr(status), _stream()), "dce_rowmax")
+    return m
+
+
+def dce_denom_digits(logits, m, v_lo=0, v_hi=None, den=None, add_into=False, status=None):
+    """Exact denominator digits over [v_lo, v_hi) with the global rowmax m
+    (det-cross-entropy "API": denom_digits); int64 [N, 6]."""
+    M, keep = _matrix(logits)
+    v_hi = M.cols if v_hi is None else v_hi
+    den = torch.empty(M.rows, DEN_NDIG, dtype=torch.int64, device=logits.device) if den is None else den
+    _check(lib().dce_denom_digits(C.byref(M), _ptr(m), v_lo, v_hi, _ptr(den), 1 if add_into else 0, _ptr(status),
+                                  _stream()), "dce_denom_digits")
+    return den
+
+
+def dce_finalize(den, logits, targets, m, status=None):
+    """(loss f32 [N], denom f64 [N]) from composed digits (det-cross-entropy "API": finalize)."""
+    M, keep = _matrix(logits)
+    loss = torch.empty(M.rows, dtype=torch.float32, device=logits.device)
+    denom = torch.empty(M.rows, dtype=torch.float64, device=logits.device)
+    targets = targets.to(torch.int64).contiguous()
+    _check(lib().dce_finalize(_ptr(den), C.byref(M), _ptr(targets), _ptr(m), _ptr(loss), _ptr(denom), _ptr(status),
+                              _stream()), "dce_finalize")
+    return loss, denom
+
+
+def dce_forward(logits, targets, splits=None, status=None):
+    """Vocab-sharded composition (det-cross-entropy "Usage"): rowmax by max, digits by add,
+    finalize.  Returns (loss, denom, m, den)."""
+    V = logits.shape[1]
+    splits = [V] if splits is None else list(splits)
+    bounds, lo = [], 0
+    for n in splits:
+        bounds.append((lo, lo + n))
+        lo += n
+    if lo != V:
+        raise DetAttnError("vocab splits must sum to V")
+    m = dce_rowmax(logits, *bounds[0], status=status)
+    if len(bounds) > 1:
+        tmp = torch.empty_like(m)
+        for a, b in bounds[1:]:
+            compose_max(m, dce_rowmax(logits, a, b, out=tmp, status=status))
+    den = None
+    for k, (a, b) in enumerate(bounds):
+        den = dce_denom_digits(logits, m, a, b, den=den, add_into=k > 0, status=status)
+    loss, denom = dce_finalize(den, logits, targets, m, status=status)
+    return loss, denom, m, den

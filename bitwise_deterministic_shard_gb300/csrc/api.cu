@@ -1,0 +1,287 @@
+// Host side of the C ABI declared in include/detattn.h: argument checks, workspace
+// layout, and the launch sequences of the fused and the KV-sharded paths (page
+// "det-attn", section "API"; page "det-cross-entropy", section "API").
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "../../include/detattn.h"
+#include "attn_kernels.h"
+
+using namespace detattn;
+
+namespace {
+
+constexpr int64_t kMaxS = (int64_t)1 << 30;
+
+int elem_size(int dtype) { return dtype == DA_F32 ? 4 : 2; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_tensor(const da_tensor& t) {
+  if (t.dtype != DA_F32 && t.dtype != DA_BF16) return DA_EDTYPE;
+  if (t.B < 0 || t.H < 1 || t.S < 0 || t.D < 1 || t.D > 256) return DA_ESHAPE;
+  if (t.S > kMaxS || t.B > 65535 || t.H > 65535) return DA_ESHAPE;   // grid.z / grid.y limits
+  if (t.stride[3] != 1) return DA_ESHAPE;
+  if (t.B * t.S > 0 && t.ptr == nullptr) return DA_EINVAL;
+  if (!aligned(t.ptr, elem_size(t.dtype))) return DA_EALIGN;
+  return DA_OK;
+}
+
+int check_desc(const da_attn_desc* d) {
+  if (!d) return DA_EINVAL;
+  int e;
+  if ((e = check_tensor(d->q)) || (e = check_tensor(d->k)) || (e = check_tensor(d->v))) return e;
+  if (d->q.dtype != d->k.dtype || d->q.dtype != d->v.dtype) return DA_EDTYPE;
+  if (d->k.B != d->q.B || d->v.B != d->q.B || d->k.D != d->q.D || d->v.D != d->q.D) return DA_ESHAPE;
+  if (d->v.H != d->k.H || d->v.S != d->k.S) return DA_ESHAPE;
+  if (d->q.H % d->k.H != 0) return DA_ESHAPE;
+  if (d->causal && d->q.S != d->k.S) return DA_EINVAL;
+  if (!std::isnan(d->scale) && !std::isfinite(d->scale)) return DA_EINVAL;
+  return DA_OK;
+}
+
+AttnArgs make_args(const da_attn_desc* d) {
+  AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = d->q.ptr; a.k = d->k.ptr; a.v = d->v.ptr;
+  for (int t = 0; t < 4; t++) { a.qs[t] = d->q.stride[t]; a.ks[t] = d->k.stride[t]; a.vs[t] = d->v.stride[t]; }
+  a.dtype = d->q.dtype;
+  a.B = (int)d->q.B; a.Hq = (int)d->q.H; a.Hkv = (int)d->k.H;
+  a.Sq = (int)d->q.S; a.Skv = (int)d->k.S; a.D = (int)d->q.D;
+  a.causal = d->causal ? 1 : 0;
+  a.scale32 = std::isnan(d->scale) ? (float)(1.0 / std::sqrt((double)d->q.D)) : d->scale;
+  a.status = d->dev_status;
+  return a;
+}
+
+int launched(cudaError_t e) { return e == cudaSuccess ? DA_OK : DA_ECUDA; }
+
+size_t round_up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct WsLayout {
+  size_t m, m2, num, den, total;
+};
+
+WsLayout ws_layout(const da_attn_desc* d, int nsplits) {
+  const size_t rows = (size_t)d->q.B * d->q.H * d->q.S;
+  WsLayout w;
+  w.m = 0;
+  w.m2 = round_up(rows * 4);
+  w.num = w.m2 + (nsplits > 1 ? round_up(rows * 4) : 0);
+  w.den = w.num + round_up(rows * DA_NUM_NDIG * (size_t)d->q.D * 8);
+  w.total = w.den + round_up(rows * DA_DEN_NDIG * 8);
+  return w;
+}
+
+int check_matrix(const da_matrix* x) {
+  if (!x) return DA_EINVAL;
+  if (x->dtype != DA_F32 && x->dtype != DA_BF16) return DA_EDTYPE;
+  if (x->rows < 0 || x->cols < 0 || x->row_stride < x->cols) return DA_ESHAPE;
+  if (x->rows > ((int64_t)1 << 31) - 1) return DA_ESHAPE;
+  if (x->rows * x->cols > 0 && !x->ptr) return DA_EINVAL;
+  if (!aligned(x->ptr, elem_size(x->dtype))) return DA_EALIGN;
+  return DA_OK;
+}
+
+DceArgs make_dce(const da_matrix* x) {
+  DceArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.x = x->ptr; a.dtype = x->dtype; a.N = x->rows; a.V = x->cols; a.rs = x->row_stride;
+  return a;
+}
+
+}  // namespace
+
+#define DA_EXPORT __attribute__((visibility("default")))
+
+extern "C" {
+
+DA_EXPORT int da_abi_version(void) { return 1; }
+
+DA_EXPORT const char* da_status_string(int code) {
+  switch (code) {
+    case DA_OK: return "ok";
+    case DA_EINVAL: return "invalid argument";
+    case DA_ESHAPE: return "inconsistent shape or stride";
+    case DA_EDTYPE: return "unsupported or mismatched dtype";
+    case DA_EALIGN: return "misaligned pointer";
+    case DA_EWORKSPACE: return "workspace missing or too small";
+    case DA_ECUDA: return "CUDA launch failed";
+    default: return "unknown status";
+  }
+}
+
+DA_EXPORT int da_rowmax(const da_attn_desc* desc, int64_t kv_lo, int64_t kv_hi, float* m, da_stream_t stream) {
+  int e = check_desc(desc);
+  if (e) return e;
+  if (kv_lo < 0 || kv_hi < kv_lo || kv_hi > desc->k.S) return DA_EINVAL;
+  if (desc->q.B * desc->q.S == 0) return DA_OK;
+  if (!m) return DA_EINVAL;
+  if (!aligned(m, 4)) return DA_EALIGN;
+  AttnArgs a = make_args(desc);
+  a.kv_lo = (int)kv_lo; a.kv_hi = (int)kv_hi; a.m_out = m;
+  return launched(launch_rowmax(a, (cudaStream_t)stream));
+}
+
+DA_EXPORT int da_accumulate(const da_attn_desc* desc, const float* m, int64_t kv_lo, int64_t kv_hi, int64_t* num,
+                  int64_t* den, int add_into, da_stream_t stream) {
+  int e = check_desc(desc);
+  if (e) return e;
+  if (kv_lo < 0 || kv_hi < kv_lo || kv_hi > desc->k.S) return DA_EINVAL;
+  if (desc->q.B * desc->q.S == 0) return DA_OK;
+  if (!m || !num || !den) return DA_EINVAL;
+  if (!aligned(m, 4) || !aligned(num, 8) || !aligned(den, 8)) return DA_EALIGN;
+  AttnArgs a = make_args(desc);
+  a.kv_lo = (int)kv_lo; a.kv_hi = (int)kv_hi;
+  a.m_in = m; a.num = (long long*)num; a.den = (long long*)den; a.add_into = add_into ? 1 : 0;
+  return launched(launch_accumulate(a, (cudaStream_t)stream));
+}
+
+DA_EXPORT int da_compose_max(float* dst, const float* src, int64_t n, da_stream_t stream) {
+  if (n < 0) return DA_EINVAL;
+  if (n == 0) return DA_OK;
+  if (!dst || !src) return DA_EINVAL;
+  if (!aligned(dst, 4) || !aligned(src, 4)) return DA_EALIGN;
+  return launched(launch_compose_max(dst, src, n, (cudaStream_t)stream));
+}
+
+DA_EXPORT int da_compose_add(int64_t* dst, const int64_t* src, int64_t n, da_stream_t stream) {
+  if (n < 0) return DA_EINVAL;
+  if (n == 0) return DA_OK;
+  if (!dst || !src) return DA_EINVAL;
+  if (!aligned(dst, 16) || !aligned(src, 16)) return DA_EALIGN;
+  return launched(launch_compose_add((long long*)dst, (const long long*)src, n, (cudaStream_t)stream));
+}
+
+DA_EXPORT int da_normalize(int64_t* digits, int64_t nrows, int ndig, int64_t inner, int32_t* dev_status, da_stream_t stream) {
+  if (nrows < 0 || inner < 1 || (ndig != DA_NUM_NDIG && ndig != DA_DEN_NDIG)) return DA_EINVAL;
+  if (nrows == 0) return DA_OK;
+  if (!digits) return DA_EINVAL;
+  if (!aligned(digits, 8)) return DA_EALIGN;
+  return launched(launch_normalize((long long*)digits, nrows, ndig, inner, dev_status, (cudaStream_t)stream));
+}
+
+DA_EXPORT int da_finalize(const int64_t* num, const int64_t* den, int64_t B, int64_t Hq, int64_t Sq, int64_t D, float* out,
+                int32_t* dev_status, da_stream_t stream) {
+  if (B < 0 || Hq < 0 || Sq < 0 || D < 1 || D > 256) return DA_ESHAPE;
+  const int64_t rows = B * Hq * Sq;
+  if (rows == 0) return DA_OK;
+  if (!num || !den || !out) return DA_EINVAL;
+  if (!aligned(num, 8) || !aligned(den, 8) || !aligned(out, 4)) return DA_EALIGN;
+  return launched(launch_finalize((const long long*)num, (const long long*)den, rows, (int)D, out, dev_status,
+                                  (cudaStream_t)stream));
+}
+
+DA_EXPORT size_t da_workspace_bytes(const da_attn_desc* desc, int nsplits) {
+  if (check_desc(desc)) return 0;
+  return ws_layout(desc, nsplits).total;
+}
+
+DA_EXPORT int da_det_attn(const da_attn_desc* desc, float* out, void* ws, size_t ws_bytes, da_stream_t stream) {
+  int e = check_desc(desc);
+  if (e) return e;
+  if (desc->q.B * desc->q.S == 0) return DA_OK;
+  if (!out) return DA_EINVAL;
+  WsLayout w = ws_layout(desc, 1);
+  if (!ws || ws_bytes < w.total) return DA_EWORKSPACE;
+  if (!aligned(ws, 256)) return DA_EALIGN;
+  char* base = (char*)ws;
+  float* m = (float*)(base + w.m);
+  int64_t* num = (int64_t*)(base + w.num);
+  int64_t* den = (int64_t*)(base + w.den);
+  if ((e = da_rowmax(desc, 0, desc->k.S, m, stream))) return e;
+  if ((e = da_accumulate(desc, m, 0, desc->k.S, num, den, 0, stream))) return e;
+  return da_finalize(num, den, desc->q.B, desc->q.H, desc->q.S, desc->q.D, out, desc->dev_status, stream);
+}
+
+DA_EXPORT int da_det_attn_sharded(const da_attn_desc* desc, const int64_t* kv_splits, int nsplits, const int32_t* order,
+                        float* out, void* ws, size_t ws_bytes, da_stream_t stream) {
+  int e = check_desc(desc);
+  if (e) return e;
+  if (nsplits < 1 || !kv_splits) return DA_EINVAL;
+  std::vector<int64_t> lo(nsplits), hi(nsplits);
+  int64_t acc = 0;
+  for (int k = 0; k < nsplits; k++) {
+    if (kv_splits[k] < 0) return DA_EINVAL;
+    lo[k] = acc;
+    acc += kv_splits[k];
+    hi[k] = acc;
+  }
+  if (acc != desc->k.S) return DA_EINVAL;
+  std::vector<int32_t> ord(nsplits);
+  std::vector<char> seen(nsplits, 0);
+  for (int k = 0; k < nsplits; k++) {
+    int32_t o = order ? order[k] : k;
+    if (o < 0 || o >= nsplits || seen[o]) return DA_EINVAL;
+    seen[o] = 1;
+    ord[k] = o;
+  }
+  if (desc->q.B * desc->q.S == 0) return DA_OK;
+  if (!out) return DA_EINVAL;
+  WsLayout w = ws_layout(desc, nsplits);
+  if (!ws || ws_bytes < w.total) return DA_EWORKSPACE;
+  if (!aligned(ws, 256)) return DA_EALIGN;
+  char* base = (char*)ws;
+  float* m = (float*)(base + w.m);
+  float* m2 = (float*)(base + w.m2);
+  int64_t* num = (int64_t*)(base + w.num);
+  int64_t* den = (int64_t*)(base + w.den);
+  const int64_t rows = desc->q.B * desc->q.H * desc->q.S;
+  // pass 1: shard rowmaxes composed by max (a max all-reduce across context-parallel ranks)
+  for (int k = 0; k < nsplits; k++) {
+    const int s = ord[k];
+    if ((e = da_rowmax(desc, lo[s], hi[s], k == 0 ? m : m2, stream))) return e;
+    if (k > 0 && (e = da_compose_max(m, m2, rows, stream))) return e;
+  }
+  // pass 2: shard digits with the global rowmax, composed by integer add (a sum reduce)
+  for (int k = 0; k < nsplits; k++) {
+    const int s = ord[k];
+    if ((e = da_accumulate(desc, m, lo[s], hi[s], num, den, k == 0 ? 0 : 1, stream))) return e;
+  }
+  return da_finalize(num, den, desc->q.B, desc->q.H, desc->q.S, desc->q.D, out, desc->dev_status, stream);
+}
+
+DA_EXPORT int dce_rowmax(const da_matrix* logits, int64_t v_lo, int64_t v_hi, float* m, int32_t* dev_status,
+               da_stream_t stream) {
+  int e = check_matrix(logits);
+  if (e) return e;
+  if (v_lo < 0 || v_hi < v_lo || v_hi > logits->cols) return DA_EINVAL;
+  if (logits->rows == 0) return DA_OK;
+  if (!m) return DA_EINVAL;
+  if (!aligned(m, 4)) return DA_EALIGN;
+  DceArgs a = make_dce(logits);
+  a.v_lo = v_lo; a.v_hi = v_hi; a.m_out = m; a.status = dev_status;
+  return launched(launch_dce_rowmax(a, (cudaStream_t)stream));
+}
+
+DA_EXPORT int dce_denom_digits(const da_matrix* logits, const float* m, int64_t v_lo, int64_t v_hi, int64_t* den,
+                     int add_into, int32_t* dev_status, da_stream_t stream) {
+  int e = check_matrix(logits);
+  if (e) return e;
+  if (v_lo < 0 || v_hi < v_lo || v_hi > logits->cols) return DA_EINVAL;
+  if (v_hi - v_lo > ((int64_t)1 << 31)) return DA_EINVAL;
+  if (logits->rows == 0) return DA_OK;
+  if (!m || !den) return DA_EINVAL;
+  if (!aligned(m, 4) || !aligned(den, 8)) return DA_EALIGN;
+  DceArgs a = make_dce(logits);
+  a.v_lo = v_lo; a.v_hi = v_hi; a.m_in = m; a.den = (long long*)den; a.add_into = add_into ? 1 : 0;
+  a.status = dev_status;
+  return launched(launch_dce_denom(a, (cudaStream_t)stream));
+}
+
+DA_EXPORT int dce_finalize(const int64_t* den, const da_matrix* logits, const int64_t* targets, const float* m, float* loss,
+                 double* denom, int32_t* dev_status, da_stream_t stream) {
+  int e = check_matrix(logits);
+  if (e) return e;
+  if (logits->rows == 0) return DA_OK;
+  if (!den || !targets || !m || !loss || !denom) return DA_EINVAL;
+  if (!aligned(den, 8) || !aligned(targets, 8) || !aligned(m, 4) || !aligned(loss, 4) || !aligned(denom, 8))
+    return DA_EALIGN;
+  DceArgs a = make_dce(logits);
+  a.den = (long long*)den; a.targets = targets; a.m_in = m; a.loss = loss; a.denom = denom; a.status = dev_status;
+  return launched(launch_dce_finalize(a, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,631 @@
+// det-attn kernels for sm_103a: rowmax (pass 1) and exact accumulate (pass 2).
+//
+// Page "det-attn", section "Method": rowmax_i = max_j (scale Q_i.K_j) is a max-reduce;
+// NUM_id = sum_j exp(s_ij - rowmax_i) V_jd and DEN_i = sum_j exp(s_ij - rowmax_i) are
+// exact integer sums in fixed bins, so any tiling, split or order gives the same bits.
+//
+// Exact score on the integer pipe.  Each Q/K row is turned, once per tile load, into a
+// fixed-point int32 vector X_d = x_d 2^-F_row with |X_d| < 2^26 (F_row from the row's
+// largest exponent); the dot is then sum_d Xq_d Xk_d, one 32x32->64 multiply-add per MAC,
+// exact in int64 (|sum| < 2^60 for D <= 256), and RN32(dot 2^(Fq+Fk)) is one correctly
+// rounded conversion.  A row whose elements do not all fit the 26-bit window (a spread of
+// more than 18 binades for bf16, most f32 rows) takes the exact Kulisch fallback for its
+// pairs.
+//
+// Exact PV.  The weight w in [0, 1] is held as W = w 2^92, three 31-bit limbs (exact for
+// w >= 2^-69); V is fixed point per column over the CTA's key range, |Vint| < 2^23.  Per
+// (i, d) three int64 accumulators take limb*Vint (< 2^54 each); every 256 keys the limbs
+// carry into a fourth word in shared memory.  Products the window cannot hold (w < 2^-69,
+// or a V element more than 15 binades below its column maximum) are added exactly with
+// int64 atomics into the output digits; integer addition commutes, so this stays
+// deterministic.  At the end each (i, d) is converted to canonical radix-2^32 digits.
+#include "numerics.cuh"
+#include "attn_kernels.h"
+
+namespace detattn {
+
+// ---------------------------------------------------------------------------------------
+// fixed-point conversion of one row (one warp): X_d = x_d * 2^-F, F = max(ex,1) - 152
+// ---------------------------------------------------------------------------------------
+template <int DT, int DP>
+__device__ __forceinline__ void convert_row_fixed(const typename In<DT>::T* src, int D, int* dst, int* F_out,
+                                                  unsigned char* fit_out, int& nf, int lane) {
+  constexpr int PER = DP / 32;
+  uint32_t bv[PER];
+  int emax = 1;
+#pragma unroll
+  for (int t = 0; t < PER; t++) {
+    int d = lane + 32 * t;
+    uint32_t u = (src != nullptr && d < D) ? In<DT>::bits(src, d) : 0u;
+    if (nonfinite_bits(u)) { nf |= ST_NONFINITE; u = 0u; }
+    bv[t] = u;
+    int ex = (int)((u >> 23) & 0xFFu);
+    emax = max(emax, ex);
+  }
+  emax = __reduce_max_sync(0xFFFFFFFFu, emax);
+  const int F = emax - 152;
+  bool ok = true;
+#pragma unroll
+  for (int t = 0; t < PER; t++) {
+    Split s = split_f32(bv[t]);
+    int sh = s.lsb - F;   // <= 2
+    int X;
+    if (s.mant == 0) {
+      X = 0;
+    } else if (sh >= 0) {
+      X = (int)(s.mant << sh);
+    } else if (sh > -32) {
+      X = (int)(s.mant >> (-sh));
+      ok = ok && ((s.mant & ((1u << (-sh)) - 1u)) == 0u);
+    } else {
+      X = 0;
+      ok = false;
+    }
+    dst[lane + 32 * t] = s.neg ? -X : X;
+  }
+  ok = __all_sync(0xFFFFFFFFu, ok);
+  if (lane == 0) {
+    *F_out = F;
+    *fit_out = ok ? 1 : 0;
+  }
+}
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xFF800000); }
+
+// =======================================================================================
+// K1: rowmax.  CTA = 64 query rows of one (b, h); 256 threads; each thread 4 rows x 4
+// keys of a 64-key tile.
+// =======================================================================================
+template <int DT, int DP>
+__global__ void __launch_bounds__(256) rowmax_kernel(const AttnArgs a) {
+  using T = typename In<DT>::T;
+  constexpr int BM = 64, BN = 64, LD = DP + 4;
+  extern __shared__ __align__(16) int smem_i[];
+  int* Qx = smem_i;
+  int* Kx = Qx + BM * LD;
+  __shared__ int Fq[BM], Fk[BN];
+  __shared__ unsigned char qfit[BM], kfit[BN];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.y, b = blockIdx.z, hk = h / (a.Hq / a.Hkv);
+  const int q0 = blockIdx.x * BM;
+  const T* qbase = (const T*)a.q + b * a.qs[0] + h * a.qs[1];
+  const T* kbase = (const T*)a.k + b * a.ks[0] + hk * a.ks[1];
+  int nf = 0;
+
+  for (int r = warp; r < BM; r += 8) {
+    int i = q0 + r;
+    convert_row_fixed<DT, DP>(i < a.Sq ? qbase + (int64_t)i * a.qs[2] : nullptr, a.D, Qx + r * LD, &Fq[r], &qfit[r], nf,
+                              lane);
+  }
+  int lo = a.kv_lo, hi = a.kv_hi;
+  if (a.causal) hi = min(hi, q0 + BM);
+  const int ty = tid >> 4, tx = tid & 15;
+  float rmax[4];
+#pragma unroll
+  for (int r = 0; r < 4; r++) rmax[r] = neg_inf();
+
+  for (int kt = lo; kt < hi; kt += BN) {
+    __syncthreads();
+    for (int r = warp; r < BN; r += 8) {
+      int j = kt + r;
+      convert_row_fixed<DT, DP>(j < hi ? kbase + (int64_t)j * a.ks[2] : nullptr, a.D, Kx + r * LD, &Fk[r], &kfit[r],
+                                nf, lane);
+    }
+    __syncthreads();
+    long long acc[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; r++)
+#pragma unroll
+      for (int c = 0; c < 4; c++) acc[r][c] = 0;
+#pragma unroll 2
+    for (int d = 0; d < DP; d += 4) {
+      int4 qv[4], kv[4];
+#pragma unroll
+      for (int r = 0; r < 4; r++) qv[r] = *reinterpret_cast<const int4*>(Qx + (ty * 4 + r) * LD + d);
+#pragma unroll
+      for (int c = 0; c < 4; c++) kv[c] = *reinterpret_cast<const int4*>(Kx + (tx + 16 * c) * LD + d);
+#pragma unroll
+      for (int r = 0; r < 4; r++)
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+          acc[r][c] += (long long)qv[r].x * kv[c].x;
+          acc[r][c] += (long long)qv[r].y * kv[c].y;
+          acc[r][c] += (long long)qv[r].z * kv[c].z;
+          acc[r][c] += (long long)qv[r].w * kv[c].w;
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; r++) {
+      const int rl = ty * 4 + r, i = q0 + rl;
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        const int cl = tx + 16 * c, j = kt + cl;
+        if (i < a.Sq && j < hi && (!a.causal || j <= i)) {
+          float dv = (qfit[rl] && kfit[cl])
+                         ? cr32_scaled(acc[r][c], Fq[rl] + Fk[cl])
+                         : exact_dot_slow<DT>(qbase + (int64_t)i * a.qs[2], kbase + (int64_t)j * a.ks[2], a.D);
+          float s = __fmul_rn(a.scale32, dv);
+          if (!(fabsf(s) <= 3.4028235e38f)) nf |= ST_NONFINITE;
+          if (s > rmax[r]) rmax[r] = s;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; r++) {
+    float v = rmax[r];
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    rmax[r] = v;
+  }
+  if (tx == 0) {
+#pragma unroll
+    for (int r = 0; r < 4; r++) {
+      int i = q0 + ty * 4 + r;
+      if (i < a.Sq) {
+        float v = rmax[r];
+        if (v == 0.0f) v = __int_as_float(0);   // -0 -> +0
+        a.m_out[((int64_t)b * a.Hq + h) * a.Sq + i] = v;
+      }
+    }
+  }
+  report(a.status, nf);
+}
+
+// =======================================================================================
+// K2: exact accumulate.
+// =======================================================================================
+template <int DP> struct AccCfg;
+template <> struct AccCfg<64>  { static constexpr int RP = 4, CP = 2; };
+template <> struct AccCfg<128> { static constexpr int RP = 4, CP = 4; };
+template <> struct AccCfg<256> { static constexpr int RP = 2, CP = 8; };
+
+template <int DP>
+struct AccLayout {
+  static constexpr int RP = AccCfg<DP>::RP, CP = AccCfg<DP>::CP;
+  static constexpr int BM = 8 * RP, BN = 64, LD = DP + 4;
+  static constexpr int SR = BM / 16;                     // score rows per thread
+  static constexpr size_t q_off = 0;                               // int32 [BM][LD]
+  static constexpr size_t k_off = q_off + sizeof(int) * BM * LD;   // int32 [BN][LD]
+  static constexpr size_t v_off = k_off + sizeof(int) * BN * LD;   // int32 [BN][LD]
+  static constexpr size_t w_off = v_off + sizeof(int) * BN * LD;   // int32 [3][BN][BM]
+  static constexpr size_t wf_off = w_off + sizeof(int) * 3 * BN * BM;  // float [BN][BM]
+  static constexpr size_t p3_off = wf_off + sizeof(float) * BN * BM;   // int64 [BM][DP]
+  static constexpr size_t vm_off = p3_off + sizeof(long long) * BM * DP;  // uint32 [BN][DP/32]
+  static constexpr size_t ps_off = vm_off + sizeof(uint32_t) * BN * (DP / 32);  // uint16 [BN*BM]
+  static constexpr size_t bytes = ps_off + sizeof(uint16_t) * BN * BM;
+  static_assert(sizeof(long long) * BM * DP * 3 <= wf_off, "epilogue staging must fit in the tile area");
+};
+
+// add a signed 64-bit X * 2^o into lazily carried radix-2^32 digits dg[]
+__device__ __forceinline__ void digits_add_i64(long long* dg, long long X, int o) {
+  unsigned long long lo = (unsigned long long)X & 0xFFFFFFFFull;
+  long long hi = X >> 32;
+  int k = o >> 5, r = o & 31;
+  unsigned long long u = lo << r;
+  dg[k] += (long long)(u & 0xFFFFFFFFull);
+  dg[k + 1] += (long long)(u >> 32);
+  long long v = hi * (1ll << r);
+  dg[k + 1] += (long long)((unsigned long long)v & 0xFFFFFFFFull);
+  dg[k + 2] += v >> 32;
+}
+
+template <int DT, int DP>
+__global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
+  using T = typename In<DT>::T;
+  using L = AccLayout<DP>;
+  constexpr int RP = L::RP, CP = L::CP, BM = L::BM, BN = L::BN, LD = L::LD, SR = L::SR, NW = DP / 32;
+  extern __shared__ __align__(16) unsigned char smem_b[];
+  int* Qx = reinterpret_cast<int*>(smem_b + L::q_off);
+  int* Kx = reinterpret_cast<int*>(smem_b + L::k_off);
+  int* Vx = reinterpret_cast<int*>(smem_b + L::v_off);
+  int* Wl = reinterpret_cast<int*>(smem_b + L::w_off);
+  float* Wf = reinterpret_cast<float*>(smem_b + L::wf_off);
+  long long* P3 = reinterpret_cast<long long*>(smem_b + L::p3_off);
+  uint32_t* vmask = reinterpret_cast<uint32_t*>(smem_b + L::vm_off);
+  uint16_t* plist = reinterpret_cast<uint16_t*>(smem_b + L::ps_off);
+  __shared__ int Fq[BM], Fk[BN], Fv[DP], Ev[DP];
+  __shared__ unsigned char qfit[BM], kfit[BN];
+  __shared__ float mrow[BM];
+  __shared__ long long denT[BM][3];
+  __shared__ int s_np, s_vany, s_zeroed;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.y, b = blockIdx.z, hk = h / (a.Hq / a.Hkv);
+  const int qt = gridDim.x - 1 - blockIdx.x;   // longest causal tiles first
+  const int q0 = qt * BM;
+  const T* qbase = (const T*)a.q + b * a.qs[0] + h * a.qs[1];
+  const T* kbase = (const T*)a.k + b * a.ks[0] + hk * a.ks[1];
+  const T* vbase = (const T*)a.v + b * a.vs[0] + hk * a.vs[1];
+  const int64_t rowbase = ((int64_t)b * a.Hq + h) * a.Sq;
+  long long* numb = a.num + rowbase * NUM_NDIG * a.D;
+  long long* denb = a.den + rowbase * DEN_NDIG;
+  const int nrows = min(BM, a.Sq - q0);
+  int nf = 0, viol = 0;
+
+  int lo = a.kv_lo, hi = a.kv_hi;
+  if (a.causal) hi = min(hi, q0 + BM);
+
+  // ---- set-up: Q tile, rowmax, per-column V exponent over [lo, hi) ----
+  for (int r = warp; r < BM; r += 8) {
+    int i = q0 + r;
+    convert_row_fixed<DT, DP>(i < a.Sq ? qbase + (int64_t)i * a.qs[2] : nullptr, a.D, Qx + r * LD, &Fq[r], &qfit[r], nf,
+                              lane);
+  }
+  for (int r = tid; r < BM; r += 256) mrow[r] = (q0 + r < a.Sq) ? a.m_in[rowbase + q0 + r] : 0.0f;
+  for (int d = tid; d < DP; d += 256) Ev[d] = 1;
+  for (int e = tid; e < BM * DP; e += 256) P3[e] = 0;
+  if (tid == 0) { s_zeroed = 0; }
+  __syncthreads();
+  {
+    constexpr int G = 256 / DP > 0 ? 256 / DP : 1;
+    const int d = tid % DP, g = tid / DP;
+    int em = 1;
+    if (d < a.D && g < G)
+      for (int j = lo + g; j < hi; j += G) {
+        uint32_t u = In<DT>::bits(vbase + (int64_t)j * a.vs[2], d);
+        int ex = (int)((u >> 23) & 0xFFu);
+        if (ex != 0xFF) em = max(em, ex);
+      }
+    if (g < G) atomicMax(&Ev[d], em);
+  }
+  __syncthreads();
+  for (int d = tid; d < DP; d += 256) Fv[d] = Ev[d] - 149;   // |Vint| < 2^23
+
+  // ---- accumulators ----
+  long long acc[RP][CP][3];
+#pragma unroll
+  for (int r = 0; r < RP; r++)
+#pragma unroll
+    for (int c = 0; c < CP; c++)
+#pragma unroll
+      for (int l = 0; l < 3; l++) acc[r][c][l] = 0;
+  long long den[SR][3];
+#pragma unroll
+  for (int r = 0; r < SR; r++)
+#pragma unroll
+    for (int l = 0; l < 3; l++) den[r][l] = 0;
+
+  const int ty = tid >> 4, tx = tid & 15;    // score layout: rows tx + 16r, keys ty + 16c
+  const int pr = warp, pc = lane;            // PV layout: rows pr*RP + r, cols pc*CP + c
+  int tiles_since_carry = 0;
+
+  auto carry_into_p3 = [&]() {
+#pragma unroll
+    for (int r = 0; r < RP; r++)
+#pragma unroll
+      for (int c = 0; c < CP; c++) {
+        long long c0 = acc[r][c][0] >> 31;
+        acc[r][c][0] -= c0 * (1ll << 31);
+        acc[r][c][1] += c0;
+        long long c1 = acc[r][c][1] >> 31;
+        acc[r][c][1] -= c1 * (1ll << 31);
+        acc[r][c][2] += c1;
+        long long c2 = acc[r][c][2] >> 31;
+        acc[r][c][2] -= c2 * (1ll << 31);
+        P3[(pr * RP + r) * DP + pc * CP + c] += c2;
+      }
+  };
+
+  for (int kt = lo; kt < hi; kt += BN) {
+    __syncthreads();   // previous tile fully consumed
+    // ---- K and V tiles ----
+    for (int r = warp; r < BN; r += 8) {
+      int j = kt + r;
+      convert_row_fixed<DT, DP>(j < hi ? kbase + (int64_t)j * a.ks[2] : nullptr, a.D, Kx + r * LD, &Fk[r], &kfit[r],
+                                nf, lane);
+      const T* vrow = j < hi ? vbase + (int64_t)j * a.vs[2] : nullptr;
+#pragma unroll
+      for (int t = 0; t < NW; t++) {
+        int d = lane + 32 * t;
+        uint32_t u = (vrow != nullptr && d < a.D) ? In<DT>::bits(vrow, d) : 0u;
+        bool fit = true;
+        int X = 0;
+        if (nonfinite_bits(u)) {
+          nf |= ST_NONFINITE;
+        } else {
+          Split s = split_f32(u);
+          if (s.mant) {
+            int sh = Fv[d] - s.lsb;   // >= 1
+            if (sh < 32) {
+              X = (int)(s.mant >> sh);
+              fit = (s.mant & ((1u << sh) - 1u)) == 0u;
+            } else {
+              fit = false;
+            }
+            if (!fit) X = 0;
+            if (s.neg) X = -X;
+          }
+        }
+        Vx[r * LD + d] = X;
+        uint32_t bad = __ballot_sync(0xFFFFFFFFu, !fit);
+        if (lane == 0) vmask[r * NW + t] = bad;
+      }
+    }
+    if (tid == 0) { s_np = 0; s_vany = 0; }
+    __syncthreads();
+    // ---- scores, weights ----
+    {
+      long long sacc[SR][4];
+#pragma unroll
+      for (int r = 0; r < SR; r++)
+#pragma unroll
+        for (int c = 0; c < 4; c++) sacc[r][c] = 0;
+#pragma unroll 2
+      for (int d = 0; d < DP; d += 4) {
+        int4 qv[SR], kv[4];
+#pragma unroll
+        for (int r = 0; r < SR; r++) qv[r] = *reinterpret_cast<const int4*>(Qx + (tx + 16 * r) * LD + d);
+#pragma unroll
+        for (int c = 0; c < 4; c++) kv[c] = *reinterpret_cast<const int4*>(Kx + (ty + 16 * c) * LD + d);
+#pragma unroll
+        for (int r = 0; r < SR; r++)
+#pragma unroll
+          for (int c = 0; c < 4; c++) {
+            sacc[r][c] += (long long)qv[r].x * kv[c].x;
+            sacc[r][c] += (long long)qv[r].y * kv[c].y;
+            sacc[r][c] += (long long)qv[r].z * kv[c].z;
+            sacc[r][c] += (long long)qv[r].w * kv[c].w;
+          }
+      }
+#pragma unroll
+      for (int r = 0; r < SR; r++) {
+        const int rl = tx + 16 * r, i = q0 + rl;
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+          const int cl = ty + 16 * c, j = kt + cl;
+          float w = 0.0f;
+          if (i < a.Sq && j < hi && (!a.causal || j <= i)) {
+            float dv = (qfit[rl] && kfit[cl])
+                           ? cr32_scaled(sacc[r][c], Fq[rl] + Fk[cl])
+                           : exact_dot_slow<DT>(qbase + (int64_t)i * a.qs[2], kbase + (int64_t)j * a.ks[2], a.D);
+            float s = __fmul_rn(a.scale32, dv);
+            float x = __fsub_rn(s, mrow[rl]);
+            if (x != x) { nf |= ST_NONFINITE; x = neg_inf(); }
+            if (x > 0.0f) { viol |= ST_VIOLATION; x = 0.0f; }
+            w = exp32_det(x);
+          }
+          uint32_t wb = __float_as_uint(w);
+          int ex = (int)(wb >> 23);
+          int l0 = 0, l1 = 0, l2 = 0;
+          if (wb != 0u) {
+            if (ex >= 58) {
+              unsigned __int128 W = ((unsigned __int128)((wb & 0x7FFFFFu) | 0x800000u)) << (ex - 58);
+              l0 = (int)((uint64_t)W & 0x7FFFFFFFull);
+              l1 = (int)((uint64_t)(W >> 31) & 0x7FFFFFFFull);
+              l2 = (int)(uint64_t)(W >> 62);
+              den[r][0] += l0;
+              den[r][1] += l1;
+              den[r][2] += l2;
+            } else {
+              int e = atomicAdd(&s_np, 1);
+              plist[e] = (uint16_t)(cl * BM + rl);
+            }
+          }
+          Wl[(0 * BN + cl) * BM + rl] = l0;
+          Wl[(1 * BN + cl) * BM + rl] = l1;
+          Wl[(2 * BN + cl) * BM + rl] = l2;
+          Wf[cl * BM + rl] = w;
+        }
+      }
+    }
+    if (lane == 0) {
+      bool any = false;
+      for (int e = warp; e < BN * NW; e += 8) any = any || (vmask[e] != 0u);
+      if (any) s_vany = 1;
+    }
+    __syncthreads();
+    // ---- exact PV on the integer pipe ----
+#pragma unroll 2
+    for (int j = 0; j < BN; j++) {
+      int wv[3][RP];
+      int vv[CP];
+#pragma unroll
+      for (int l = 0; l < 3; l++) {
+        const int* wp = Wl + (l * BN + j) * BM + pr * RP;
+        if constexpr (RP == 4) {
+          int4 t4 = *reinterpret_cast<const int4*>(wp);
+          wv[l][0] = t4.x; wv[l][1] = t4.y; wv[l][2] = t4.z; wv[l][3] = t4.w;
+        } else {
+          int2 t2 = *reinterpret_cast<const int2*>(wp);
+          wv[l][0] = t2.x; wv[l][1] = t2.y;
+        }
+      }
+      const int* vp = Vx + j * LD + pc * CP;
+      if constexpr (CP == 2) {
+        int2 t2 = *reinterpret_cast<const int2*>(vp);
+        vv[0] = t2.x; vv[1] = t2.y;
+      } else {
+#pragma unroll
+        for (int c4 = 0; c4 < CP; c4 += 4) {
+          int4 t4 = *reinterpret_cast<const int4*>(vp + c4);
+          vv[c4] = t4.x; vv[c4 + 1] = t4.y; vv[c4 + 2] = t4.z; vv[c4 + 3] = t4.w;
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < RP; r++)
+#pragma unroll
+        for (int c = 0; c < CP; c++)
+#pragma unroll
+          for (int l = 0; l < 3; l++) acc[r][c][l] += (long long)wv[l][r] * vv[c];
+    }
+    if (++tiles_since_carry == 4) {   // 256 keys: limb sums stay below 2^62
+      carry_into_p3();
+      tiles_since_carry = 0;
+    }
+    // ---- products outside the window: exact int64 atomics into the output digits ----
+    if (s_np > 0 || s_vany) {
+      if (!s_zeroed) {
+        if (!a.add_into) {
+          for (int64_t e = tid; e < (int64_t)nrows * NUM_NDIG * a.D; e += 256) numb[(int64_t)q0 * NUM_NDIG * a.D + e] = 0;
+          for (int e = tid; e < nrows * DEN_NDIG; e += 256) denb[(int64_t)q0 * DEN_NDIG + e] = 0;
+        }
+        __syncthreads();
+        if (tid == 0) s_zeroed = 1;
+      }
+      const int np = s_np;
+      for (int e = warp; e < np; e += 8) {
+        const int cl = plist[e] / BM, rl = plist[e] % BM;
+        const int i = q0 + rl, j = kt + cl;
+        Split sw = split_f32(__float_as_uint(Wf[cl * BM + rl]));
+        long long* nrow = numb + (int64_t)i * NUM_NDIG * a.D;
+        for (int d = lane; d < a.D; d += 32) {
+          uint32_t u = In<DT>::bits(vbase + (int64_t)j * a.vs[2], d);
+          if (nonfinite_bits(u)) continue;
+          Split sv = split_f32(u);
+          atomic_digits_add(nrow + d, a.D, NUM_E0, (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
+        }
+        if (lane == 0) atomic_digits_add(denb + (int64_t)i * DEN_NDIG, 1, DEN_E0, sw.mant, 0, sw.lsb);
+      }
+      if (s_vany) {
+        for (int e = tid; e < BN * NW; e += 256) {
+          uint32_t m = vmask[e];
+          const int cl = e / NW, t = e % NW, j = kt + cl;
+          while (m) {
+            const int bit = __ffs(m) - 1;
+            m &= m - 1;
+            const int d = t * 32 + bit;
+            Split sv = split_f32(In<DT>::bits(vbase + (int64_t)j * a.vs[2], d));
+            for (int rl = 0; rl < BM; rl++) {
+              uint32_t wb = __float_as_uint(Wf[cl * BM + rl]);
+              if (wb == 0u || (int)(wb >> 23) < 58) continue;   // zero, or already a pair spill
+              Split sw = split_f32(wb);
+              atomic_digits_add(numb + (int64_t)(q0 + rl) * NUM_NDIG * a.D + d, a.D, NUM_E0,
+                                (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ---- epilogue: canonical digits ----
+  carry_into_p3();
+  if (tid < BM * 3) (&denT[0][0])[tid] = 0;
+  __syncthreads();   // tiles consumed; the tile area becomes the staging area below
+#pragma unroll
+  for (int r = 0; r < SR; r++)
+#pragma unroll
+    for (int l = 0; l < 3; l++) atomicAdd((unsigned long long*)&denT[tx + 16 * r][l], (unsigned long long)den[r][l]);
+  long long* stage = reinterpret_cast<long long*>(smem_b);   // [BM][DP][3], fits in the Q/K/V/W tiles
+#pragma unroll
+  for (int r = 0; r < RP; r++)
+#pragma unroll
+    for (int c = 0; c < CP; c++)
+#pragma unroll
+      for (int l = 0; l < 3; l++) stage[((pr * RP + r) * DP + pc * CP + c) * 3 + l] = acc[r][c][l];
+  __syncthreads();   // staging, P3, denT and every spill atomic complete
+  const bool rmw = a.add_into || s_zeroed;
+  for (int e = tid; e < BM * DP; e += 256) {
+    const int rl = e / DP, d = e % DP, i = q0 + rl;
+    if (i >= a.Sq || d >= a.D) continue;
+    long long* nrow = numb + (int64_t)i * NUM_NDIG * a.D;
+    long long dg[NUM_NDIG + 3];
+#pragma unroll
+    for (int k = 0; k < NUM_NDIG + 3; k++) dg[k] = 0;
+    if (rmw)
+#pragma unroll
+      for (int k = 0; k < NUM_NDIG; k++) dg[k] = __ldcg(nrow + (int64_t)k * a.D + d);
+    const int off = Fv[d] - 92 - NUM_E0;   // bit position of the accumulator's unit
+    digits_add_i64(dg, stage[e * 3 + 0], off);
+    digits_add_i64(dg, stage[e * 3 + 1], off + 31);
+    digits_add_i64(dg, stage[e * 3 + 2], off + 62);
+    digits_add_i64(dg, P3[e], off + 93);
+    kul_carry(dg, NUM_NDIG + 3);
+    long long top = dg[NUM_NDIG + 2];
+    bool bad = false;
+    for (int k = NUM_NDIG + 1; k >= NUM_NDIG - 1; k--) {
+      if (top > (1ll << 30) || top < -(1ll << 30)) bad = true;
+      top = top * 4294967296ll + dg[k];
+    }
+    if (bad) nf |= ST_HEADROOM;
+#pragma unroll
+    for (int k = 0; k < NUM_NDIG - 1; k++) nrow[(int64_t)k * a.D + d] = dg[k];
+    nrow[(int64_t)(NUM_NDIG - 1) * a.D + d] = top;
+  }
+  for (int rl = tid; rl < nrows; rl += 256) {
+    long long* drow = denb + (int64_t)(q0 + rl) * DEN_NDIG;
+    long long dg[DEN_NDIG + 3];
+#pragma unroll
+    for (int k = 0; k < DEN_NDIG + 3; k++) dg[k] = 0;
+    if (rmw)
+#pragma unroll
+      for (int k = 0; k < DEN_NDIG; k++) dg[k] = __ldcg(drow + k);
+    const int off = -92 - DEN_E0;
+    digits_add_i64(dg, denT[rl][0], off);
+    digits_add_i64(dg, denT[rl][1], off + 31);
+    digits_add_i64(dg, denT[rl][2], off + 62);
+    kul_carry(dg, DEN_NDIG + 3);
+    long long top = dg[DEN_NDIG + 2];
+    bool bad = false;
+    for (int k = DEN_NDIG + 1; k >= DEN_NDIG - 1; k--) {
+      if (top > (1ll << 30) || top < -(1ll << 30)) bad = true;
+      top = top * 4294967296ll + dg[k];
+    }
+    if (bad) nf |= ST_HEADROOM;
+#pragma unroll
+    for (int k = 0; k < DEN_NDIG - 1; k++) drow[k] = dg[k];
+    drow[DEN_NDIG - 1] = top;
+  }
+  report(a.status, nf | viol);
+}
+
+// ---------------------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------------------
+template <int DT, int DP>
+static cudaError_t launch_rowmax_t(const AttnArgs& a, cudaStream_t st) {
+  constexpr int BM = 64, BN = 64, LD = DP + 4;
+  const size_t smem = sizeof(int) * (BM + BN) * LD;
+  cudaError_t e = cudaFuncSetAttribute(rowmax_kernel<DT, DP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Sq + BM - 1) / BM, a.Hq, a.B);
+  rowmax_kernel<DT, DP><<<grid, 256, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DT, int DP>
+static cudaError_t launch_accumulate_t(const AttnArgs& a, cudaStream_t st) {
+  using L = AccLayout<DP>;
+  const size_t smem = L::bytes;
+  cudaError_t e =
+      cudaFuncSetAttribute(accumulate_kernel<DT, DP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Sq + L::BM - 1) / L::BM, a.Hq, a.B);
+  accumulate_kernel<DT, DP><<<grid, 256, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+static int padded_d(int D) { return D <= 64 ? 64 : (D <= 128 ? 128 : 256); }
+
+cudaError_t launch_rowmax(const AttnArgs& a, cudaStream_t st) {
+  const int dp = padded_d(a.D);
+  if (a.dtype == 0) {
+    if (dp == 64) return launch_rowmax_t<0, 64>(a, st);
+    if (dp == 128) return launch_rowmax_t<0, 128>(a, st);
+    return launch_rowmax_t<0, 256>(a, st);
+  }
+  if (dp == 64) return launch_rowmax_t<1, 64>(a, st);
+  if (dp == 128) return launch_rowmax_t<1, 128>(a, st);
+  return launch_rowmax_t<1, 256>(a, st);
+}
+
+cudaError_t launch_accumulate(const AttnArgs& a, cudaStream_t st) {
+  const int dp = padded_d(a.D);
+  if (a.dtype == 0) {
+    if (dp == 64) return launch_accumulate_t<0, 64>(a, st);
+    if (dp == 128) return launch_accumulate_t<0, 128>(a, st);
+    return launch_accumulate_t<0, 256>(a, st);
+  }
+  if (dp == 64) return launch_accumulate_t<1, 64>(a, st);
+  if (dp == 128) return launch_accumulate_t<1, 128>(a, st);
+  return launch_accumulate_t<1, 256>(a, st);
+}
+
+int accumulate_rows_per_cta(int D) {
+  const int dp = padded_d(D);
+  return dp == 256 ? AccLayout<256>::BM : AccLayout<128>::BM;
+}
+
+}  // namespace detattn

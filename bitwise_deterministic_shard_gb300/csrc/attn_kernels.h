@@ -1,0 +1,54 @@
+// Internal kernel interface of libdetattn (not part of the C ABI).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace detattn {
+
+struct AttnArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  int64_t qs[4], ks[4], vs[4];   // element strides of [B, H, S, D]; qs[3] == ks[3] == vs[3] == 1
+  int dtype;                     // 0 = f32, 1 = bf16
+  int B, Hq, Hkv, Sq, Skv, D;
+  int causal;
+  float scale32;
+  int kv_lo, kv_hi;
+  float* m_out;                  // rowmax output [B, Hq, Sq]
+  const float* m_in;             // global rowmax input [B, Hq, Sq]
+  long long* num;                // [B, Hq, Sq, 15, D]
+  long long* den;                // [B, Hq, Sq, 6]
+  int add_into;
+  int* status;                   // device status word (may be null)
+};
+
+cudaError_t launch_rowmax(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_accumulate(const AttnArgs& a, cudaStream_t st);
+int accumulate_rows_per_cta(int D);
+
+cudaError_t launch_compose_max(float* dst, const float* src, int64_t n, cudaStream_t st);
+cudaError_t launch_compose_add(long long* dst, const long long* src, int64_t n, cudaStream_t st);
+cudaError_t launch_normalize(long long* dg, int64_t nrows, int ndig, int64_t inner, int* status, cudaStream_t st);
+cudaError_t launch_finalize(const long long* num, const long long* den, int64_t rows, int D, float* out, int* status,
+                            cudaStream_t st);
+
+struct DceArgs {
+  const void* x;
+  int dtype;
+  int64_t N, V, rs;     // rows, columns, row stride (elements)
+  int64_t v_lo, v_hi;
+  const float* m_in;
+  float* m_out;
+  long long* den;
+  int add_into;
+  const int64_t* targets;
+  float* loss;
+  double* denom;
+  int* status;
+};
+cudaError_t launch_dce_rowmax(const DceArgs& a, cudaStream_t st);
+cudaError_t launch_dce_denom(const DceArgs& a, cudaStream_t st);
+cudaError_t launch_dce_finalize(const DceArgs& a, cudaStream_t st);
+
+}  // namespace detattn

@@ -1,0 +1,277 @@
+// Device numerics of the order-invariant softmax reduction (sm_103a).
+//
+// Every floating-point step is an explicit round-to-nearest intrinsic (__fmul_rn,
+// __fmaf_rn, __fsub_rn, __ddiv_rn, ...), so nothing is contracted or reassociated by the
+// compiler; every sum of products is exact integer arithmetic.  The contract these
+// routines implement (page "det-attn", section "Method"; page "det-cross-entropy",
+// section "Method"):
+//   d_ij = RN32(sum_d q_id k_jd) (exact dot, one rounding), s_ij = RN32(scale32 * d_ij)
+//   w_ij = exp32_det(RN32(s_ij - m_i))
+//   digits: value = sum_k digit_k 2^(E0 + 32 k), digits 0..n-2 in [0, 2^32), top signed.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace detattn {
+
+constexpr int NUM_NDIG = 15, DEN_NDIG = 6;
+constexpr int NUM_E0 = -320, DEN_E0 = -160;
+enum : int { ST_NONFINITE = 1, ST_VIOLATION = 2, ST_HEADROOM = 4, ST_BAD_TARGET = 8 };
+
+// ---------------------------------------------------------------------------------------
+// element access: bf16 is the upper half of a binary32, so widening is exact
+// ---------------------------------------------------------------------------------------
+template <int DT> struct In;
+template <> struct In<0> {
+  using T = float;
+  __device__ __forceinline__ static uint32_t bits(const T* p, int64_t i) { return __float_as_uint(__ldg(p + i)); }
+};
+template <> struct In<1> {
+  using T = uint16_t;
+  __device__ __forceinline__ static uint32_t bits(const T* p, int64_t i) { return (uint32_t)__ldg(p + i) << 16; }
+};
+
+// binary32 bits -> |x| = mant * 2^lsb (mant < 2^24), sign
+struct Split {
+  uint32_t mant;
+  int lsb;
+  int neg;
+};
+__device__ __forceinline__ Split split_f32(uint32_t u) {
+  Split s;
+  uint32_t ex = (u >> 23) & 0xFFu, fr = u & 0x7FFFFFu;
+  s.neg = (int)(u >> 31);
+  s.mant = ex ? (fr | 0x800000u) : fr;
+  s.lsb = (ex ? (int)ex : 1) - 150;
+  return s;
+}
+__device__ __forceinline__ bool nonfinite_bits(uint32_t u) { return ((u >> 23) & 0xFFu) == 0xFFu; }
+
+// ---------------------------------------------------------------------------------------
+// exp32_det: Cody-Waite argument reduction (Cody & Waite, "Software Manual for the
+// Elementary Functions", 1980) and a degree-7 Taylor polynomial, every step one binary32
+// rounding.  Constants: RN32(log2 e); ln 2 to 16 significant bits; RN32(ln 2 - that);
+// RN32(1/n!) for n = 0..7.  Valid for x <= 0 (callers clamp); x < -104 gives +0.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float exp32_det(float x) {
+  if (x != x) return x;
+  if (x < -104.0f) return 0.0f;
+  const float L2E = 0x1.715476p+0f, C1 = 0x1.62e4p-1f, C2 = 0x1.7f7d1cp-20f;
+  float t = __fmul_rn(x, L2E);
+  int k = __float2int_rn(t);          // ties to even
+  float kf = __int2float_rn(k);       // exact
+  float r1 = __fmaf_rn(-kf, C1, x);   // exact (Cody-Waite)
+  float r = __fmaf_rn(-kf, C2, r1);
+  float p = 0x1.a01a02p-13f;
+  p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);
+  p = __fmaf_rn(p, r, 0x1.111112p-7f);
+  p = __fmaf_rn(p, r, 0x1.555556p-5f);
+  p = __fmaf_rn(p, r, 0x1.555556p-3f);
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  // RN32(p * 2^k) in one rounding: an exact normal pre-scale, then one multiply
+  if (k >= -126) return __fmul_rn(p, __uint_as_float((uint32_t)(k + 127) << 23));
+  return __fmul_rn(__fmul_rn(p, __uint_as_float((uint32_t)(k + 64 + 127) << 23)), 0x1p-64f);
+}
+
+// ---------------------------------------------------------------------------------------
+// Round an exact value to binary32 (ties to even, gradual underflow, overflow -> inf).
+// The value is (neg ? -1 : 1) * (W + t) * 2^lsb with W a 128-bit magnitude and t in
+// [0, 1) nonzero iff `sticky`.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float round_f32(unsigned __int128 W, bool sticky, int lsb, int neg) {
+  if (W == 0) return neg ? -0.0f : 0.0f;   // callers only pass sticky with W == 0 when the value underflows
+  uint64_t hi = (uint64_t)(W >> 64), lo = (uint64_t)W;
+  int tb = hi ? 127 - __clzll((long long)hi) : 63 - __clzll((long long)lo);  // top bit index
+  int e = tb + lsb;                        // 2^e <= |value| < 2^(e+1)
+  int q = (e > -126 ? e : -126) - 23;      // exponent of the last kept bit
+  int cut = q - lsb;                       // bit index in W of the last kept bit
+  uint64_t n;
+  bool rb, st = sticky;
+  if (cut <= 0) {
+    n = (uint64_t)W << (-cut);             // exact (W < 2^24 here)
+    rb = false;
+  } else {
+    int rpos = cut - 1;                    // index of the rounding bit
+    n = cut >= 128 ? 0 : (uint64_t)(W >> cut);
+    rb = rpos >= 128 ? false : (bool)((W >> rpos) & 1);
+    unsigned __int128 below = rpos >= 128 ? W : (W & ((((unsigned __int128)1) << rpos) - 1));
+    st = st || (below != 0);
+  }
+  if (rb && (st || (n & 1))) n++;
+  uint32_t bitsv;
+  if (n == 0) {
+    bitsv = 0;
+  } else if (n < 0x800000u) {              // subnormal (q == -149)
+    bitsv = (uint32_t)n;
+  } else {
+    if (n == 0x1000000u) { n = 0x800000u; q++; }
+    int be = q + 150;
+    bitsv = be >= 255 ? 0x7F800000u : (((uint32_t)be << 23) | ((uint32_t)n & 0x7FFFFFu));
+  }
+  return __uint_as_float(bitsv | (neg ? 0x80000000u : 0u));
+}
+
+// RN32(T * 2^F) for an integer T, |T| < 2^63.
+__device__ __forceinline__ float cr32_scaled(long long T, int F) {
+  if (T == 0) return 0.0f;
+  float f = __ll2float_rn(T);
+  uint32_t b = __float_as_uint(f);
+  int ne = (int)((b >> 23) & 0xFFu) + F;
+  if (ne >= 1 && ne <= 254) return __uint_as_float(b + ((uint32_t)F << 23));
+  if (ne > 254) return T < 0 ? -__int_as_float(0x7F800000) : __int_as_float(0x7F800000);
+  unsigned long long mag = T < 0 ? 0ull - (unsigned long long)T : (unsigned long long)T;
+  return round_f32((unsigned __int128)mag, false, F, T < 0);
+}
+
+// ---------------------------------------------------------------------------------------
+// Kulisch accumulator in radix 2^32 (int64 words with lazy carries); word k weighs
+// 2^(32k - 320).  Used by the exact fallback dot and by digit conversions.
+// ---------------------------------------------------------------------------------------
+constexpr int KW = 20;
+
+__device__ __forceinline__ void kul_add(long long* a, unsigned long long mag, int neg, int lsb) {
+  if (mag == 0) return;
+  int pos = lsb + 320;
+  int k = pos >> 5, sh = pos & 31;
+  unsigned long long lo = mag << sh;
+  unsigned long long hi = sh ? (mag >> (64 - sh)) : 0ull;
+  long long c0 = (long long)(lo & 0xFFFFFFFFull), c1 = (long long)(lo >> 32), c2 = (long long)hi;
+  if (neg) { a[k] -= c0; a[k + 1] -= c1; a[k + 2] -= c2; }
+  else     { a[k] += c0; a[k + 1] += c1; a[k + 2] += c2; }
+}
+
+__device__ __forceinline__ void kul_carry(long long* a, int n) {
+  for (int k = 0; k < n - 1; k++) {
+    long long c = a[k] >> 32;
+    a[k] -= c * 4294967296ll;
+    a[k + 1] += c;
+  }
+}
+
+// RN32 of a Kulisch value (words weigh 2^(32k + base))
+static __device__ __noinline__ float kul_round_f32(long long* a, int n, int base) {
+  kul_carry(a, n);
+  int neg = a[n - 1] < 0;
+  if (neg) {
+    for (int k = 0; k < n; k++) a[k] = -a[k];
+    kul_carry(a, n);
+  }
+  int top = -1;
+  for (int k = n - 1; k >= 0; k--)
+    if (a[k] != 0) { top = k; break; }
+  if (top < 0) return 0.0f;
+  unsigned __int128 W = 0;
+  bool sticky = false;
+  int lo = top - 2;
+  for (int k = top; k >= lo; k--) W = (W << 32) | (unsigned long long)(k >= 0 ? (uint32_t)a[k] : 0u);
+  for (int k = 0; k < lo; k++) sticky = sticky || (a[k] != 0);
+  return round_f32(W, sticky, 32 * lo + base, neg);
+}
+
+// Exact fallback score: d = RN32(sum_d q_d k_d) from the raw inputs, any finite values.
+template <int DT>
+__device__ float exact_dot_slow(const typename In<DT>::T* q, const typename In<DT>::T* k, int D) {
+  long long a[KW];
+#pragma unroll
+  for (int t = 0; t < KW; t++) a[t] = 0;
+  for (int d = 0; d < D; d++) {
+    uint32_t qb = In<DT>::bits(q, d), kb = In<DT>::bits(k, d);
+    if (nonfinite_bits(qb) || nonfinite_bits(kb)) continue;
+    Split sq = split_f32(qb), sk = split_f32(kb);
+    kul_add(a, (unsigned long long)sq.mant * sk.mant, sq.neg ^ sk.neg, sq.lsb + sk.lsb);
+  }
+  return kul_round_f32(a, KW, -320);
+}
+
+// ---------------------------------------------------------------------------------------
+// Round a digit array (radix 2^32 int64, word k weighs 2^(32k + base), any carries) to
+// binary64, ties to even.  Values here lie in [2^-320, 2^192): normal binary64 range.
+// ---------------------------------------------------------------------------------------
+template <int N>
+__device__ __forceinline__ double digits_rn64(long long (&a)[N], int base) {
+  kul_carry(a, N);
+  int neg = a[N - 1] < 0;
+  if (neg) {
+#pragma unroll
+    for (int k = 0; k < N; k++) a[k] = -a[k];
+    kul_carry(a, N);
+  }
+  int top = -1;
+#pragma unroll
+  for (int k = 0; k < N; k++)
+    if (a[k] != 0) top = k;
+  if (top < 0) return 0.0;
+  // 96-bit window from the top word, sticky for everything below
+  unsigned long long w2 = (uint32_t)a[top];
+  unsigned long long w1 = top >= 1 ? (uint32_t)a[top - 1] : 0u;
+  unsigned long long w0 = top >= 2 ? (uint32_t)a[top - 2] : 0u;
+  bool sticky = false;
+#pragma unroll
+  for (int k = 0; k < N; k++)
+    if (k < top - 2 && a[k] != 0) sticky = true;
+  int lz = __clzll((long long)w2) - 32;            // leading zeros of the 32-bit top word
+  unsigned __int128 W = ((unsigned __int128)w2 << 64) | ((unsigned __int128)w1 << 32) | w0;
+  W <<= lz;                                         // top bit now at bit 95
+  unsigned long long top64 = (unsigned long long)(W >> 32);
+  if ((uint32_t)W != 0) sticky = true;
+  if (sticky) top64 |= 1ull;                        // below the rounding position (bit 10)
+  double r = __ull2double_rn(top64);                // one rounding to 53 bits
+  int e = 32 * (top - 2) + base + 32 - lz;          // weight of top64's bit 0
+  // exact scaling by 2^e (result stays normal)
+  int e1 = e / 2, e2 = e - e1;
+  r = __dmul_rn(r, __longlong_as_double((long long)(e1 + 1023) << 52));
+  r = __dmul_rn(r, __longlong_as_double((long long)(e2 + 1023) << 52));
+  return neg ? -r : r;
+}
+
+// ---------------------------------------------------------------------------------------
+// log64_det: reduction to [sqrt(1/2), sqrt(2)], the atanh series log f = 2 sum
+// u^(2n+1)/(2n+1), u = (f-1)/(f+1), ten terms after the first, then + e ln 2 in two parts.
+// binary64, every operation one rounding, nothing fused.  For positive finite normal d.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ double log64_det(double d) {
+  long long b = __double_as_longlong(d);
+  int e = (int)((b >> 52) & 0x7FF) - 1023;
+  double f = __longlong_as_double((b & 0x000FFFFFFFFFFFFFll) | 0x3FF0000000000000ll);  // [1, 2)
+  if (f > 0x1.6a09e667f3bcdp+0) { f = __dmul_rn(f, 0.5); e += 1; }
+  double a = __dsub_rn(f, 1.0);
+  double bb = __dadd_rn(f, 1.0);
+  double u = __ddiv_rn(a, bb);
+  double u2 = __dmul_rn(u, u);
+  double p = __ddiv_rn(1.0, 21.0);
+#pragma unroll
+  for (int n = 9; n >= 1; n--) p = __dadd_rn(__dmul_rn(p, u2), __ddiv_rn(1.0, (double)(2 * n + 1)));
+  double t1 = __dmul_rn(u2, p);
+  double t2 = __dmul_rn(u, t1);
+  double lf = __dmul_rn(__dadd_rn(u, t2), 2.0);
+  double fe = (double)e;
+  double hi = __dmul_rn(fe, 0x1.62e42fefa38p-1);
+  double lo = __dmul_rn(fe, 0x1.ef35793c7673p-45);
+  return __dadd_rn(hi, __dadd_rn(lo, lf));
+}
+
+// ---------------------------------------------------------------------------------------
+// exact atomic digit adds (integer adds commute, so concurrent adds stay deterministic)
+// ---------------------------------------------------------------------------------------
+// add (neg ? -1 : 1) * mag * 2^lsb, mag < 2^49, into digits whose word k weighs
+// 2^(32k + e0), word stride `stride` (elements)
+__device__ __forceinline__ void atomic_digits_add(long long* dg, int64_t stride, int e0, unsigned long long mag, int neg,
+                                                  int lsb) {
+  if (mag == 0) return;
+  int pos = lsb - e0;
+  int k = pos >> 5, sh = pos & 31;
+  unsigned long long lo = mag << sh;
+  unsigned long long hi = sh ? (mag >> (64 - sh)) : 0ull;
+  unsigned long long c[3] = {lo & 0xFFFFFFFFull, lo >> 32, hi};
+#pragma unroll
+  for (int t = 0; t < 3; t++)
+    if (c[t]) atomicAdd((unsigned long long*)(dg + (int64_t)(k + t) * stride), neg ? (0ull - c[t]) : c[t]);
+}
+
+__device__ __forceinline__ void report(int* status, int bits) {
+  if (bits && status) atomicOr(status, bits);
+}
+
+}  // namespace detattn

@@ -1,0 +1,174 @@
+/*
+ * libdetattn: C ABI of the exact, order-invariant softmax reduction (sm_103a).
+ *
+ * Sources (page title, section):
+ *   "det-attn" - "API" (det_attn, rowmax, accumulate, finalize, det_attn_sharded),
+ *                "Method" (global rowmax by a max-reduce; exact Kulisch sums NUM/DEN of
+ *                signed int64 digits; KV shards compose by max and by digit add),
+ *                "Correctness" and "Requirements and limits" (causal / non-causal,
+ *                MHA / GQA, f32 / bf16 inputs, D <= 256, f32 output).
+ *   "det-cross-entropy" - "API" (rowmax, denom_digits, finalize), "Usage" (vocab shards
+ *                combine by max and by digit add), "Method".
+ *
+ * Numerical contract (every rounding is IEEE round-to-nearest-even with gradual underflow):
+ *   score     s_ij = RN32(scale32 * RN32(sum_d q_id k_jd))      (exact dot, rounded once)
+ *   rowmax    m_i  = max over valid keys j of s_ij; -0 -> +0; no valid key -> -inf
+ *   weight    w_ij = exp32_det(RN32(s_ij - m_i)), a fixed binary32 routine
+ *                    (Cody-Waite reduction + degree-7 Taylor polynomial)
+ *   digits    NUM_id = sum_j w_ij v_jd, DEN_i = sum_j w_ij, exactly, as
+ *             value = sum_k digit_k * 2^(E0 + 32 k); NUM: E0 = -320, 15 digits;
+ *             DEN: E0 = -160, 6 digits.  Canonical form: digits 0..n-2 in [0, 2^32),
+ *             the top digit signed.  Digit arrays compose by plain int64 addition (up to
+ *             2^31 canonical arrays without overflow) and normalize back to canonical form.
+ *   finalize  o_id = RN32(RN64(RN64(NUM_id) / RN64(DEN_i)))
+ *   DCE       m_i = max_v x_iv; den_i = sum_v exp32_det(RN32(x_iv - m_i)) (DEN format);
+ *             loss_i = RN32(RN64(log64_det(RN64(den_i)) + RN64(m_i - x_{i,t_i}))),
+ *             denom_i = RN64(den_i); log64_det is a fixed binary64 routine.
+ *
+ * Conventions for every entry point:
+ *   - Every device pointer is caller-owned device memory; the library allocates nothing
+ *     and keeps no state between calls.  Work is enqueued on `stream` (NULL = the legacy
+ *     default stream) and the call returns without synchronizing.
+ *   - Host-side argument checks happen before any launch; on failure nothing is enqueued
+ *     and a DA_E* code is returned.  A failed launch returns DA_ECUDA.
+ *   - Data-dependent conditions are OR-ed into the optional device word `dev_status`
+ *     (DA_STATUS_* bits); read it after synchronizing the stream.  Kernels never trap.
+ *     When a status bit is set the affected outputs are unspecified.
+ *   - Causal masking keeps key j for query i when j <= i (global positions, so it does
+ *     not depend on how the keys are split) and requires Sq == Skv.
+ *   - GQA: query head h reads key/value head h / (Hq / Hkv) (contiguous groups).
+ */
+#ifndef DETATTN_H
+#define DETATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* da_stream_t; /* a cudaStream_t */
+
+/* return codes */
+#define DA_OK 0
+#define DA_EINVAL 1      /* bad argument value (null pointer, range, scale, order) */
+#define DA_ESHAPE 2      /* inconsistent shapes or strides */
+#define DA_EDTYPE 3      /* unsupported or mismatched dtype */
+#define DA_EALIGN 4      /* pointer not aligned to its element type */
+#define DA_EWORKSPACE 5  /* workspace missing or too small */
+#define DA_ECUDA 6       /* a CUDA launch failed */
+
+/* device status bits */
+#define DA_STATUS_NONFINITE 1        /* a non-finite input, score or intermediate was met */
+#define DA_STATUS_ROWMAX_VIOLATION 2 /* a score above the supplied rowmax (weight clamped to 1) */
+#define DA_STATUS_DIGIT_HEADROOM 4   /* a digit sum left the representable range */
+#define DA_STATUS_BAD_TARGET 8       /* a target index outside [0, V) (its loss is NaN) */
+
+/* element types */
+#define DA_F32 0
+#define DA_BF16 1
+
+#define DA_NUM_NDIG 15
+#define DA_DEN_NDIG 6
+#define DA_NUM_E0 (-320)
+#define DA_DEN_E0 (-160)
+
+/* A [B, H, S, D] tensor view: element strides, stride[3] must be 1. */
+typedef struct {
+  const void* ptr;
+  int32_t dtype; /* DA_F32 or DA_BF16 */
+  int64_t B, H, S, D;
+  int64_t stride[4];
+} da_tensor;
+
+/* One attention problem.  q: [B, Hq, Sq, D]; k, v: [B, Hkv, Skv, D], same dtype;
+ * 1 <= D <= 256; Hq % Hkv == 0; scale: NaN selects RN32(1/sqrt(D)), otherwise finite. */
+typedef struct {
+  da_tensor q, k, v;
+  int32_t causal;
+  float scale;
+  int32_t* dev_status; /* optional device int32, OR-ed with DA_STATUS_* bits */
+} da_attn_desc;
+
+/* A [rows, cols] matrix view with a row stride in elements (columns contiguous). */
+typedef struct {
+  const void* ptr;
+  int32_t dtype;
+  int64_t rows, cols, row_stride;
+} da_matrix;
+
+/* ABI version (incremented on any incompatible change). */
+int da_abi_version(void);
+
+/* Static text for a DA_* return code. */
+const char* da_status_string(int code);
+
+/* det-attn "API", rowmax: m[b,h,i] = max over keys j in [kv_lo, kv_hi) (causal: j <= i)
+ * of s_ij.  m: device f32 [B, Hq, Sq], contiguous.  Rows with no valid key get -inf.
+ * Shards combine with da_compose_max. */
+int da_rowmax(const da_attn_desc* desc, int64_t kv_lo, int64_t kv_hi, float* m, da_stream_t stream);
+
+/* det-attn "API", accumulate: exact NUM/DEN digits over keys [kv_lo, kv_hi) with the
+ * GLOBAL rowmax m (device f32 [B, Hq, Sq]).  num: device int64 [B, Hq, Sq, 15, D];
+ * den: device int64 [B, Hq, Sq, 6], both contiguous.  add_into = 0 overwrites them with
+ * the canonical digits of this range; add_into = 1 adds this range's sums to the
+ * (canonical or plainly added) digits already there and leaves canonical digits.  A score
+ * above m sets DA_STATUS_ROWMAX_VIOLATION. */
+int da_accumulate(const da_attn_desc* desc, const float* m, int64_t kv_lo, int64_t kv_hi, int64_t* num,
+                  int64_t* den, int add_into, da_stream_t stream);
+
+/* det-attn "Method", shard composition: dst[i] = max(dst[i], src[i]) (f32, -0 -> +0). */
+int da_compose_max(float* dst, const float* src, int64_t n, da_stream_t stream);
+
+/* det-attn "Method", shard composition: dst[i] += src[i] (int64 digit add; exact). */
+int da_compose_add(int64_t* dst, const int64_t* src, int64_t n, da_stream_t stream);
+
+/* Canonical form of digit arrays laid out [nrows, ndig, inner] (NUM: ndig = 15,
+ * inner = D; DEN and cross-entropy: ndig = 6, inner = 1), in place.  ndig must be 15 or 6.
+ * A value outside the range sets DA_STATUS_DIGIT_HEADROOM. */
+int da_normalize(int64_t* digits, int64_t nrows, int ndig, int64_t inner, int32_t* dev_status, da_stream_t stream);
+
+/* det-attn "API", finalize: out[b,h,i,d] = RN32(RN64(RN64(NUM)/RN64(DEN))); accepts any
+ * non-overflowing digits (canonical or plainly added).  out: device f32 [B, Hq, Sq, D]. */
+int da_finalize(const int64_t* num, const int64_t* den, int64_t B, int64_t Hq, int64_t Sq, int64_t D, float* out,
+                int32_t* dev_status, da_stream_t stream);
+
+/* Bytes of workspace da_det_attn (nsplits <= 1) or da_det_attn_sharded needs. */
+size_t da_workspace_bytes(const da_attn_desc* desc, int nsplits);
+
+/* det-attn "API", det_attn: rowmax over all keys, accumulate, finalize.  out: device f32
+ * [B, Hq, Sq, D] contiguous; ws: device workspace of at least da_workspace_bytes(desc, 1). */
+int da_det_attn(const da_attn_desc* desc, float* out, void* ws, size_t ws_bytes, da_stream_t stream);
+
+/* det-attn "API", det_attn_sharded: the keys split into nsplits contiguous shards of
+ * kv_splits[k] keys (host array, sum = Skv, entries >= 0), visited in the order
+ * order[0..nsplits-1] (host array, a permutation; NULL = 0, 1, ...).  Rowmax of every
+ * shard composed by max, then the digits of every shard (with the global rowmax)
+ * composed by add, then finalize.  Bit-identical to da_det_attn for any split and order. */
+int da_det_attn_sharded(const da_attn_desc* desc, const int64_t* kv_splits, int nsplits, const int32_t* order,
+                        float* out, void* ws, size_t ws_bytes, da_stream_t stream);
+
+/* det-cross-entropy "API", rowmax: m[i] = max over v in [v_lo, v_hi) of logits[i, v];
+ * -0 -> +0; empty range -> -inf.  m: device f32 [rows]. */
+int dce_rowmax(const da_matrix* logits, int64_t v_lo, int64_t v_hi, float* m, int32_t* dev_status,
+               da_stream_t stream);
+
+/* det-cross-entropy "API", denom_digits: exact digits of sum over v in [v_lo, v_hi) of
+ * exp32_det(RN32(logits[i, v] - m[i])), m the GLOBAL rowmax (device f32 [rows]).
+ * den: device int64 [rows, 6]; add_into as for da_accumulate. */
+int dce_denom_digits(const da_matrix* logits, const float* m, int64_t v_lo, int64_t v_hi, int64_t* den,
+                     int add_into, int32_t* dev_status, da_stream_t stream);
+
+/* det-cross-entropy "API", finalize: loss[i] (device f32 [rows]) and denom[i] = RN64(den_i)
+ * (device f64 [rows]) from composed digits (any non-overflowing form), the full logits,
+ * targets (device int64 [rows]) and the global rowmax.  A target outside [0, cols) gives
+ * a NaN loss and DA_STATUS_BAD_TARGET. */
+int dce_finalize(const int64_t* den, const da_matrix* logits, const int64_t* targets, const float* m, float* loss,
+                 double* denom, int32_t* dev_status, da_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DETATTN_H */

@@ -1,0 +1,70 @@
+"""The C-ABI library loads without a GPU and exports every entry point that
+include/detattn.h declares (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "detattn.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char\s*\*|const char\s*\*)\s*\**\s*(\w+)\s*\(", txt, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    from bitwise_deterministic_shard_gb300 import build
+    return build.build()
+
+
+def test_header_declares_the_page_api():
+    names = _declared()
+    for n in ("da_rowmax", "da_accumulate", "da_finalize", "da_det_attn", "da_det_attn_sharded", "da_compose_max",
+              "da_compose_add", "da_normalize", "dce_rowmax", "dce_denom_digits", "dce_finalize"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(libpath):
+    lib = ctypes.CDLL(libpath)
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_host_only_calls(libpath):
+    lib = ctypes.CDLL(libpath)
+    lib.da_status_string.restype = ctypes.c_char_p
+    assert lib.da_abi_version() == 1
+    assert lib.da_status_string(0) == b"ok"
+    assert lib.da_status_string(5).startswith(b"workspace")
+
+
+def test_argument_checks_reject_before_any_launch(libpath):
+    """Host validation returns codes without touching a GPU (null / bad shapes)."""
+    import bitwise_deterministic_shard_gb300 as da
+    L = da.lib()
+    assert L.da_rowmax(None, 0, 0, None, None) == 1                        # null descriptor
+    d = da._Desc()
+    for t in (d.q, d.k, d.v):
+        t.ptr = 4096                                                        # never dereferenced: rejected first
+        t.dtype, t.B, t.H, t.S, t.D = 1, 1, 2, 8, 300                      # D > 256
+        t.stride[3] = 1
+    assert L.da_rowmax(ctypes.byref(d), 0, 8, None, None) == 2
+    for t in (d.q, d.k, d.v):
+        t.D = 64
+    d.k.H = d.v.H = 3                                                       # Hq % Hkv != 0
+    assert L.da_rowmax(ctypes.byref(d), 0, 8, None, None) == 2
+    d.k.H = d.v.H = 1
+    d.v.dtype = 0                                                           # mixed dtypes
+    assert L.da_rowmax(ctypes.byref(d), 0, 8, None, None) == 3
+    d.v.dtype = 1
+    d.causal, d.k.S, d.v.S = 1, 9, 9                                        # causal needs Sq == Skv
+    assert L.da_rowmax(ctypes.byref(d), 0, 9, None, None) == 1
+    d.causal = 0
+    assert L.da_rowmax(ctypes.byref(d), 5, 3, None, None) == 1             # kv_hi < kv_lo
+    assert L.da_det_attn_sharded(ctypes.byref(d), (ctypes.c_int64 * 2)(4, 4), 2, None, None, None, 0, None) == 1
+    assert L.da_normalize(None, 4, 7, 1, None, None) == 1                  # ndig must be 15 or 6

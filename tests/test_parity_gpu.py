@@ -1,0 +1,303 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle, bit for bit.
+
+The oracle (oracle/native.py, the exact C implementation; oracle/exact.py pins it) and
+the CUDA kernels share no code; both take their inputs from workloads/.  Every floating-
+point output is compared with torch.equal / bit patterns (the contract fixes every
+rounding, so the tolerance is zero); digits are compared exactly.  Sizes: small cases that
+span several tiles with ragged tails, every workload of the det-attn and det-cross-entropy
+pages at full size (sampled rows for the oracle where full rows would take minutes),
+and the edge cases (empty key ranges, one key, GQA, strided views, f32 and bf16).
+"""
+import itertools
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+cuda = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
+
+
+@pytest.fixture(scope="module")
+def da():
+    import bitwise_deterministic_shard_gb300 as m
+    m.lib()
+    return m
+
+
+@pytest.fixture(scope="module")
+def orc():
+    from oracle import native
+    native.build()
+    return native
+
+
+def _bits(x):
+    x = x.detach().cpu().contiguous() if isinstance(x, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(x))
+    return x.view(torch.int32) if x.dtype == torch.float32 else x
+
+
+def assert_bits_equal(a, b, what=""):
+    a, b = _bits(a), _bits(b)
+    if not torch.equal(a, b):
+        diff = (a != b).nonzero()
+        raise AssertionError(f"{what}: {diff.shape[0]} elements differ, first at {diff[:5].tolist()}")
+
+
+def flat_rows(B, H, S, rows_bhi):
+    return np.asarray([(b * H + h) * S + i for b, h, i in rows_bhi], dtype=np.int64)
+
+
+def run_full(da, Q, K, V, causal, scale=None, status=None):
+    dev = torch.device("cuda")
+    Qd, Kd, Vd = Q.to(dev), K.to(dev), V.to(dev)
+    m = da.rowmax(Qd, Kd, causal=causal, scale=scale, status=status)
+    num, den = da.accumulate(Qd, Kd, Vd, m, causal=causal, scale=scale, status=status)
+    out = da.finalize(num, den)
+    fused = da.det_attn(Qd, Kd, Vd, causal=causal, scale=scale, status=status)
+    torch.cuda.synchronize()
+    return m, num, den, out, fused
+
+
+CASES = [
+    # (B, Hq, Hkv, S, D, dtype, causal)
+    (1, 2, 2, 37, 8, torch.bfloat16, False),
+    (1, 2, 1, 130, 64, torch.bfloat16, True),
+    (2, 4, 2, 200, 128, torch.bfloat16, True),
+    (1, 3, 3, 97, 100, torch.bfloat16, False),
+    (1, 2, 2, 70, 256, torch.bfloat16, True),
+    (1, 2, 1, 90, 64, torch.float32, False),
+    (1, 2, 2, 66, 128, torch.float32, True),
+    (1, 1, 1, 1, 16, torch.bfloat16, False),
+    (1, 2, 2, 65, 200, torch.float32, False),
+]
+
+
+@cuda
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"B{c[0]}Hq{c[1]}Hkv{c[2]}S{c[3]}D{c[4]}{str(c[5])[6:]}{'c' if c[6] else ''}")
+def test_small_cases_match_oracle(da, orc, case):
+    B, Hq, Hkv, S, D, dt, causal = case
+    Q, K, V = W.random_attn(1000 + S + D, B, Hq, Hkv, S, D, dt, causal)
+    st = da.new_status()
+    m, num, den, out, fused = run_full(da, Q, K, V, causal, status=st)
+    assert da.read_status(st) == 0
+    A = orc.Attn(Q, K, V, causal)
+    m_o, num_o, den_o, out_o = A.forward_rows()
+    assert_bits_equal(m.reshape(-1), m_o, "rowmax")
+    assert torch.equal(den.cpu().reshape(-1, 6), torch.from_numpy(den_o)), "DEN digits"
+    assert torch.equal(num.cpu().reshape(-1, 15, D), torch.from_numpy(num_o)), "NUM digits"
+    assert_bits_equal(out.reshape(-1, D), out_o, "output")
+    assert_bits_equal(fused, out, "fused vs composed")
+
+
+@cuda
+def test_wide_exponent_inputs_take_the_exact_fallbacks(da, orc):
+    """Rows whose elements span more than the fixed-point window (the Kulisch score
+    fallback), tiny V elements and tiny weights (the atomic spill paths)."""
+    Q, K, V = W.random_attn(7, 1, 2, 2, 150, 64, torch.bfloat16, False, spread=60.0)
+    K = K.clone()
+    K[0, 0, 3] *= 2 ** 40      # a key far above the others: tiny weights for the rest
+    Qd, Kd, Vd = Q.cuda(), K.cuda(), V.cuda()
+    st = da.new_status()
+    out = da.det_attn(Qd, Kd, Vd, status=st)
+    torch.cuda.synchronize()
+    _, num_o, den_o, out_o = orc.Attn(Q, K, V).forward_rows()
+    assert da.read_status(st) & ~1 == 0
+    assert_bits_equal(out.reshape(-1, 64), out_o, "output")
+
+
+@cuda
+def test_c1_fused_and_all_24_orders(da, orc):
+    w = W.c1()
+    Q, K, V = w.tensors("cuda")
+    fused = da.det_attn(Q, K, V, causal=w.causal, scale=w.scale)
+    _, _, _, ref = orc.Attn(Q.cpu(), K.cpu(), V.cpu(), w.causal, w.scale).forward_rows()
+    assert_bits_equal(fused.reshape(-1, w.D), ref, "C1 fused vs oracle")
+    for sp, order in w.splits:
+        out = da.det_attn_sharded(Q, K, V, sp, causal=w.causal, scale=w.scale, order=order)
+        assert torch.equal(out, fused), order
+    # a physical permutation of the K/V blocks (allowed: non-causal)
+    perm = torch.cat([torch.arange(96, 128), torch.arange(0, 32), torch.arange(64, 96), torch.arange(32, 64)])
+    outp = da.det_attn(Q, K[:, :, perm], V[:, :, perm], causal=False, scale=w.scale)
+    assert torch.equal(outp, fused)
+
+
+@cuda
+def test_c2_gqa_causal_splits_and_oracle(da, orc):
+    w = W.c2()
+    Q, K, V = w.tensors("cuda")
+    fused = da.det_attn(Q, K, V, causal=True)
+    torch.cuda.synchronize()
+    _, _, _, ref = orc.Attn(Q.cpu(), K.cpu(), V.cpu(), True).forward_rows()
+    assert_bits_equal(fused.reshape(-1, w.D), ref, "C2 fused vs oracle")
+    for sp, order in w.splits:
+        out = da.det_attn_sharded(Q, K, V, sp, causal=True, order=order)
+        assert torch.equal(out, fused), (sp, order)
+
+
+@cuda
+def test_c3_ring_steps_and_sampled_oracle(da, orc):
+    w = W.c3()
+    Q, K, V = w.tensors("cuda")
+    st = da.new_status()
+    fused = da.det_attn(Q, K, V, causal=True, status=st)
+    torch.cuda.synchronize()
+    assert da.read_status(st) == 0
+    rng = random.Random(3)
+    rows = [(0, h, i) for h in range(w.Hq) for i in rng.sample(range(w.S), 8)] + [(0, 0, w.S - 1), (0, 15, 0)]
+    A = orc.Attn(Q.cpu(), K.cpu(), V.cpu(), True)
+    fl = flat_rows(1, w.Hq, w.S, rows)
+    _, _, _, ref = A.forward_rows(rows=fl)
+    got = fused.reshape(-1, w.D)[torch.from_numpy(fl).cuda()]
+    assert_bits_equal(got, ref, "C3 sampled rows vs oracle")
+    for sp, order in w.splits:
+        out = da.det_attn_sharded(Q, K, V, sp, causal=True, order=order)
+        assert torch.equal(out, fused), len(sp)
+
+
+@cuda
+def test_c3_shard_digits_compose_to_fused_digits(da):
+    """accumulate per shard into separate arrays + compose_add + normalize equals the
+    fused digits (det-attn "Method": an int64 add of digit arrays)."""
+    w = W.c3()
+    Q, K, V = w.tensors("cuda")
+    Q, K, V = Q[:, :4, :1024], K[:, :4, :1024], V[:, :4, :1024]
+    m = da.rowmax(Q, K, causal=True)
+    num0, den0 = da.accumulate(Q, K, V, m, causal=True)
+    parts = [da.accumulate(Q, K, V, m, lo, lo + 256, causal=True) for lo in (768, 0, 512, 256)]
+    num, den = parts[0][0].clone(), parts[0][1].clone()
+    for n_, d_ in parts[1:]:
+        da.compose_add(num, n_)
+        da.compose_add(den, d_)
+    da.normalize(num)
+    da.normalize(den)
+    assert torch.equal(num, num0) and torch.equal(den, den0)
+    ms = [da.rowmax(Q, K, lo, lo + 256, causal=True) for lo in (512, 0, 768, 256)]
+    mm = ms[0].clone()
+    for x in ms[1:]:
+        da.compose_max(mm, x)
+    assert torch.equal(mm, m)
+
+
+@cuda
+def test_repeat_runs_bitwise_identical(da):
+    w = W.c3()
+    Q, K, V = w.tensors("cuda")
+    a = da.det_attn(Q, K, V, causal=True)
+    b = da.det_attn(Q, K, V, causal=True)
+    assert torch.equal(a, b)
+
+
+@cuda
+def test_strided_nhd_views(da, orc):
+    """Q/K/V as [B, S, H, D] projections viewed as [B, H, S, D] (non-contiguous heads)."""
+    g = torch.Generator().manual_seed(44)
+    qkv = torch.randn(1, 77, 3, 4, 64, generator=g).to(torch.bfloat16)
+    Q, K, V = (qkv[:, :, t].transpose(1, 2) for t in range(3))
+    out = da.det_attn(Q.cuda(), K.cuda(), V.cuda())
+    _, _, _, ref = orc.Attn(Q, K, V).forward_rows()
+    assert_bits_equal(out.reshape(-1, 64), ref, "strided")
+
+
+@cuda
+def test_empty_and_edge_ranges(da, orc):
+    Q, K, V = W.random_attn(45, 1, 2, 2, 50, 32, torch.bfloat16, False)
+    Qd, Kd, Vd = Q.cuda(), K.cuda(), V.cuda()
+    m = da.rowmax(Qd, Kd, 10, 10)
+    assert torch.all(m == float("-inf"))
+    mfull = da.rowmax(Qd, Kd)
+    num, den = da.accumulate(Qd, Kd, Vd, mfull, 20, 20)
+    assert not num.any() and not den.any()
+    # a shard of one key
+    n1, d1 = da.accumulate(Qd, Kd, Vd, mfull, 49, 50)
+    A = orc.Attn(Q, K, V)
+    mo, _ = A.rowmax()
+    no, do, _ = A.accumulate(mo, 49, 50)
+    assert torch.equal(n1.cpu().reshape(-1, 15, 32), torch.from_numpy(no))
+    assert torch.equal(d1.cpu().reshape(-1, 6), torch.from_numpy(do))
+    # causal: a shard that lies entirely after some queries contributes nothing to them
+    Qc, Kc, Vc = W.random_attn(46, 1, 1, 1, 64, 16, torch.bfloat16, True)
+    mc = da.rowmax(Qc.cuda(), Kc.cuda(), 32, 64, causal=True)
+    assert torch.all(mc[0, 0, :32] == float("-inf"))
+    mo2, _ = orc.Attn(Qc, Kc, Vc, True).rowmax(32, 64)
+    assert_bits_equal(mc.reshape(-1), mo2, "causal shard rowmax")
+
+
+@cuda
+def test_status_bits(da):
+    Q, K, V = W.random_attn(47, 1, 1, 1, 40, 16, torch.bfloat16, False)
+    Qd, Kd, Vd = Q.cuda(), K.cuda(), V.cuda()
+    m = da.rowmax(Qd, Kd)
+    st = da.new_status()
+    da.accumulate(Qd, Kd, Vd, m - 1.0, status=st)
+    torch.cuda.synchronize()
+    assert da.read_status(st) & da.STATUS_ROWMAX_VIOLATION
+    st2 = da.new_status()
+    Qn = Qd.clone()
+    Qn[0, 0, 5, 3] = float("inf")
+    da.rowmax(Qn, Kd, status=st2)
+    torch.cuda.synchronize()
+    assert da.read_status(st2) & da.STATUS_NONFINITE
+
+
+@cuda
+def test_host_argument_errors(da):
+    Q, K, V = (t.cuda() for t in W.random_attn(48, 1, 2, 2, 16, 16, torch.bfloat16, True))
+    with pytest.raises(da.DetAttnError):
+        da.det_attn_sharded(Q, K, V, [8, 9], causal=True)        # splits do not sum to S
+    with pytest.raises(da.DetAttnError):
+        da.det_attn_sharded(Q, K, V, [8, 8], causal=True, order=[0, 0])
+    with pytest.raises(da.DetAttnError):
+        da.det_attn(Q, K[:, :, :8], V[:, :, :8], causal=True)   # causal needs Sq == Skv
+    with pytest.raises(da.DetAttnError):
+        da.det_attn(Q.cpu(), K, V)                               # no CPU path
+
+
+# ------------------------------------------------------------------------ cross-entropy
+
+@cuda
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_dce_small_matches_oracle(da, orc, dt):
+    g = torch.Generator().manual_seed(50)
+    x = (torch.randn(33, 1001, generator=g) * 3).to(dt)
+    t = torch.randint(0, 1001, (33,), generator=g)
+    for splits in ([1001], [500, 501], [1, 333, 667]):
+        loss, denom, m, den = da.dce_forward(x.cuda(), t.cuda(), splits=splits)
+        rl, rd, rm, rden, st = orc.DCE(x).forward(t.numpy(), splits=splits)
+        assert_bits_equal(m, rm, "m")
+        assert torch.equal(den.cpu(), torch.from_numpy(rden))
+        assert_bits_equal(loss, rl, "loss")
+        assert torch.equal(denom.cpu(), torch.from_numpy(rd))
+
+
+@cuda
+def test_c5_vocab_splits_and_oracle(da, orc):
+    w = W.c5()
+    x, t = w.tensors("cuda")
+    base = da.dce_forward(x, t)
+    for sp in w.splits[1:]:
+        got = da.dce_forward(x, t, splits=sp)
+        for a, b in zip(base, got):
+            assert torch.equal(a, b), len(sp)
+    rows = np.arange(0, w.N, 8, dtype=np.int64)
+    D = orc.DCE(x.cpu())
+    rl, rd, rm, rden, st = D.forward(t.cpu().numpy(), rows=rows)
+    assert_bits_equal(base[0][torch.from_numpy(rows).cuda()], rl, "C5 loss")
+    assert torch.equal(base[1][torch.from_numpy(rows).cuda()].cpu(), torch.from_numpy(rd))
+    ref = torch.nn.functional.cross_entropy(x.double(), t, reduction="none")
+    assert float((base[0].double() - ref).abs().max()) < 2e-6
+
+
+@cuda
+def test_dce_bad_target(da):
+    x = torch.randn(4, 100, device="cuda")
+    t = torch.tensor([0, 100, -1, 99], device="cuda")
+    st = da.new_status()
+    loss, denom, _, _ = da.dce_forward(x, t, status=st)
+    torch.cuda.synchronize()
+    assert da.read_status(st) & da.STATUS_BAD_TARGET
+    assert torch.isnan(loss[1]) and torch.isnan(loss[2]) and not torch.isnan(loss[0])
