@@ -309,3 +309,24 @@ def dce_forward(logits, targets, splits=None, status=None):
         den = dce_denom_digits(logits, m, a, b, den=den, add_into=k > 0, status=status)
     loss, denom = dce_finalize(den, logits, targets, m, status=status)
     return loss, denom, m, den
+
+
+STATIC_MAX_ROWS = 65536
+
+
+def dce_forward_static(logits, targets, status=None):
+    """Cross-entropy forward through the static-scratch entry point, for callers that
+    cannot allocate device memory for the intermediates (the rowmax and the denominator
+    digits live in a fixed device array of STATIC_MAX_ROWS rows inside the library; only
+    loss and denom are returned in new tensors here).  Equal bit for bit to dce_forward
+    without splits.  Calls that overlap on the GPU race on the shared array."""
+    L = lib()
+    f = L.dce_forward_static
+    f.argtypes = [C.POINTER(_Matrix), _P, _P, _P, _P, _P]
+    f.restype = C.c_int
+    M, keep = _matrix(logits)
+    loss = torch.empty(M.rows, dtype=torch.float32, device=logits.device)
+    denom = torch.empty(M.rows, dtype=torch.float64, device=logits.device)
+    targets = targets.to(torch.int64).contiguous()
+    _check(f(C.byref(M), _ptr(targets), _ptr(loss), _ptr(denom), _ptr(status), _stream()), "dce_forward_static")
+    return loss, denom

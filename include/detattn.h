@@ -167,6 +167,28 @@ int dce_denom_digits(const da_matrix* logits, const float* m, int64_t v_lo, int6
 int dce_finalize(const int64_t* den, const da_matrix* logits, const int64_t* targets, const float* m, float* loss,
                  double* denom, int32_t* dev_status, da_stream_t stream);
 
+/* Static-scratch variant of the cross-entropy forward, for callers that cannot allocate
+ * device memory: code that runs where cudaMalloc is not allowed or not wanted, such as a
+ * host framework whose device memory is owned by another allocator, an embedded runtime
+ * with a fixed memory budget, or a call site that must not trigger allocation.  The pages
+ * have no counterpart of this entry point; it computes what dce_rowmax over [0, cols),
+ * dce_denom_digits over [0, cols) and dce_finalize compute, bit for bit, but keeps the
+ * rowmax and the denominator digits in a file-scope device array of
+ * DA_STATIC_MAX_ROWS rows (3.25 MiB) instead of caller memory.  It calls no cudaMalloc,
+ * cudaFree or allocating library routine.
+ *   - The caller still passes logits, targets (device int64 [rows]), loss (device f32
+ *     [rows]) and denom (device f64 [rows]).
+ *   - rows > DA_STATIC_MAX_ROWS returns DA_EWORKSPACE (the static scratch is too small).
+ *   - Every GPU that loads the library holds the array until the process exits.  The
+ *     first call on a device looks up the array's device address (once per device, with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array: calls whose work overlaps on the GPU (different
+ *     streams, or several host threads) race on it.  Serialize them.  Each call overwrites
+ *     every scratch entry it reads, so no clearing is needed between calls. */
+#define DA_STATIC_MAX_ROWS 65536
+int dce_forward_static(const da_matrix* logits, const int64_t* targets, float* loss, double* denom,
+                       int32_t* dev_status, da_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
