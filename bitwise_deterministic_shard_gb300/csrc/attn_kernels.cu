@@ -20,6 +20,7 @@
 // int64 atomics into the output digits; integer addition commutes, so this stays
 // deterministic.  At the end each (i, d) is converted to canonical radix-2^32 digits.
 #include "numerics.cuh"
+#include "score_tc.cuh"
 #include "attn_kernels.h"
 
 namespace detattn {
@@ -73,103 +74,114 @@ __device__ __forceinline__ void convert_row_fixed(const typename In<DT>::T* src,
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xFF800000); }
 
 // =======================================================================================
-// K1: rowmax.  CTA = 64 query rows of one (b, h); 256 threads; each thread 4 rows x 4
-// keys of a 64-key tile.
+// K1: rowmax.  CTA = 64 query rows of one (b, h), 256 threads, 32-key tiles.  The exact
+// scores come from the tensor cores (score_tc.cuh); warp w owns query rows
+// 16 (w / 2) .. +15 and keys 16 (w % 2) .. +15 of each tile (two 16 x 8 MMA tiles).
 // =======================================================================================
+template <int DP>
+struct RowmaxLayout {
+  static constexpr int BM = 64, BN = 32, LDS = DP + 8;
+  static constexpr size_t q_bytes = sizeof(uint16_t) * NSLICE * BM * LDS;
+  static constexpr size_t bytes = q_bytes + sizeof(uint16_t) * NSLICE * BN * LDS;
+};
+
 template <int DT, int DP>
 __global__ void __launch_bounds__(256) rowmax_kernel(const AttnArgs a) {
   using T = typename In<DT>::T;
-  constexpr int BM = 64, BN = 64, LD = DP + 4;
-  extern __shared__ __align__(16) int smem_i[];
-  int* Qx = smem_i;
-  int* Kx = Qx + BM * LD;
+  using L = RowmaxLayout<DP>;
+  constexpr int BM = L::BM, BN = L::BN, LDS = L::LDS;
+  extern __shared__ __align__(16) unsigned char smem_r[];
+  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem_r);
+  uint16_t* Ks = reinterpret_cast<uint16_t*>(smem_r + L::q_bytes);
   __shared__ int Fq[BM], Fk[BN];
   __shared__ unsigned char qfit[BM], kfit[BN];
+  __shared__ float wmax[8][2][8];
+  __shared__ uint16_t flist[BM * BN];   // pairs outside the fixed-point window, this tile
+  __shared__ int fkey[BM];              // their row max, as order-preserving int keys
+  __shared__ int s_nfix;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
   const int h = blockIdx.y, b = blockIdx.z, hk = h / (a.Hq / a.Hkv);
-  const int q0 = blockIdx.x * BM;
   const T* qbase = (const T*)a.q + b * a.qs[0] + h * a.qs[1];
   const T* kbase = (const T*)a.k + b * a.ks[0] + hk * a.ks[1];
   int nf = 0;
+  // causal: CTA x takes query tiles x and T-1-x, so every CTA sees about the same keys
+  const int ntiles = (a.Sq + BM - 1) / BM;
+  const int npass = (a.causal && blockIdx.x != ntiles - 1 - blockIdx.x) ? 2 : 1;
+  for (int pass = 0; pass < npass; pass++) {
+  const int q0 = (pass == 0 ? ntiles - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
+  if (pass) __syncthreads();
 
   for (int r = warp; r < BM; r += 8) {
     int i = q0 + r;
-    convert_row_fixed<DT, DP>(i < a.Sq ? qbase + (int64_t)i * a.qs[2] : nullptr, a.D, Qx + r * LD, &Fq[r], &qfit[r], nf,
-                              lane);
+    convert_row_slices<DT, DP>(i < a.Sq ? qbase + (int64_t)i * a.qs[2] : nullptr, a.D, Qs + r * LDS, BM * LDS, &Fq[r],
+                               &qfit[r], nf, lane);
   }
+  for (int r = tid; r < BM; r += 256) fkey[r] = float_key(neg_inf());
   int lo = a.kv_lo, hi = a.kv_hi;
   if (a.causal) hi = min(hi, q0 + BM);
-  const int ty = tid >> 4, tx = tid & 15;
-  float rmax[4];
-#pragma unroll
-  for (int r = 0; r < 4; r++) rmax[r] = neg_inf();
+  const int r0 = 16 * (warp >> 1), nb = 16 * (warp & 1);
+  float rmax[2] = {neg_inf(), neg_inf()};   // rows r0 + g, r0 + g + 8
 
   for (int kt = lo; kt < hi; kt += BN) {
     __syncthreads();
+    if (tid == 0) s_nfix = 0;
     for (int r = warp; r < BN; r += 8) {
       int j = kt + r;
-      convert_row_fixed<DT, DP>(j < hi ? kbase + (int64_t)j * a.ks[2] : nullptr, a.D, Kx + r * LD, &Fk[r], &kfit[r],
-                                nf, lane);
+      convert_row_slices<DT, DP>(j < hi ? kbase + (int64_t)j * a.ks[2] : nullptr, a.D, Ks + r * LDS, BN * LDS,
+                                 &Fk[r], &kfit[r], nf, lane);
     }
     __syncthreads();
-    long long acc[4][4];
 #pragma unroll
-    for (int r = 0; r < 4; r++)
+    for (int nt = 0; nt < 2; nt++) {
+      const int n0 = nb + 8 * nt;
+      float acc[NDIAG][4];
+      score_tile_mma<DP>(acc, Qs, BM * LDS, Ks, BN * LDS, LDS, r0, n0, g, t);
 #pragma unroll
-      for (int c = 0; c < 4; c++) acc[r][c] = 0;
-#pragma unroll 2
-    for (int d = 0; d < DP; d += 4) {
-      int4 qv[4], kv[4];
-#pragma unroll
-      for (int r = 0; r < 4; r++) qv[r] = *reinterpret_cast<const int4*>(Qx + (ty * 4 + r) * LD + d);
-#pragma unroll
-      for (int c = 0; c < 4; c++) kv[c] = *reinterpret_cast<const int4*>(Kx + (tx + 16 * c) * LD + d);
-#pragma unroll
-      for (int r = 0; r < 4; r++)
-#pragma unroll
-        for (int c = 0; c < 4; c++) {
-          acc[r][c] += (long long)qv[r].x * kv[c].x;
-          acc[r][c] += (long long)qv[r].y * kv[c].y;
-          acc[r][c] += (long long)qv[r].z * kv[c].z;
-          acc[r][c] += (long long)qv[r].w * kv[c].w;
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < 4; r++) {
-      const int rl = ty * 4 + r, i = q0 + rl;
-#pragma unroll
-      for (int c = 0; c < 4; c++) {
-        const int cl = tx + 16 * c, j = kt + cl;
+      for (int e = 0; e < 4; e++) {
+        const int rl = r0 + g + 8 * (e >> 1), cl = n0 + 2 * t + (e & 1);
+        const int i = q0 + rl, j = kt + cl;
         if (i < a.Sq && j < hi && (!a.causal || j <= i)) {
-          float dv = (qfit[rl] && kfit[cl])
-                         ? cr32_scaled(acc[r][c], Fq[rl] + Fk[cl])
-                         : exact_dot_slow<DT>(qbase + (int64_t)i * a.qs[2], kbase + (int64_t)j * a.ks[2], a.D);
-          float s = __fmul_rn(a.scale32, dv);
-          if (!(fabsf(s) <= 3.4028235e38f)) nf |= ST_NONFINITE;
-          if (s > rmax[r]) rmax[r] = s;
+          if (qfit[rl] && kfit[cl]) {
+            float sc = __fmul_rn(a.scale32, cr32_scaled(combine_diag(acc, e), Fq[rl] + Fk[cl]));
+            if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
+            if (sc > rmax[e >> 1]) rmax[e >> 1] = sc;
+          } else {
+            flist[atomicAdd(&s_nfix, 1)] = (uint16_t)(cl * BM + rl);   // a row outside the window
+          }
         }
       }
     }
-  }
-#pragma unroll
-  for (int r = 0; r < 4; r++) {
-    float v = rmax[r];
-#pragma unroll
-    for (int o = 1; o < 16; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    rmax[r] = v;
-  }
-  if (tx == 0) {
-#pragma unroll
-    for (int r = 0; r < 4; r++) {
-      int i = q0 + ty * 4 + r;
-      if (i < a.Sq) {
-        float v = rmax[r];
-        if (v == 0.0f) v = __int_as_float(0);   // -0 -> +0
-        a.m_out[((int64_t)b * a.Hq + h) * a.Sq + i] = v;
-      }
+    __syncthreads();
+    for (int fe = warp; fe < s_nfix; fe += 8) {   // one warp per deferred pair
+      const int cl = flist[fe] / BM, rl = flist[fe] % BM;
+      float sc = __fmul_rn(a.scale32, exact_dot_warp<DT>(qbase + (int64_t)(q0 + rl) * a.qs[2],
+                                                        kbase + (int64_t)(kt + cl) * a.ks[2], a.D, lane));
+      if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
+      if (lane == 0 && sc == sc) atomicMax(&fkey[rl], float_key(sc));
     }
   }
+#pragma unroll
+  for (int hh = 0; hh < 2; hh++) {
+    float v = rmax[hh];
+    v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
+    v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
+    if (t == 0) wmax[warp][hh][g] = v;
+  }
+  __syncthreads();
+  if (tid < BM) {
+    const int rl = tid, mw = 2 * (rl / 16), hh = (rl % 16) / 8, gg = rl % 8;
+    const float v0 = wmax[mw][hh][gg], v1 = wmax[mw + 1][hh][gg], v2 = key_float(fkey[rl]);
+    float v = v1 > v0 ? v1 : v0;
+    v = v2 > v ? v2 : v;
+    const int i = q0 + rl;
+    if (i < a.Sq) {
+      if (v == 0.0f) v = __int_as_float(0);   // -0 -> +0
+      a.m_out[((int64_t)b * a.Hq + h) * a.Sq + i] = v;
+    }
+  }
+  }   // pass
   report(a.status, nf);
 }
 
@@ -184,18 +196,19 @@ template <> struct AccCfg<256> { static constexpr int RP = 2, CP = 8; };
 template <int DP>
 struct AccLayout {
   static constexpr int RP = AccCfg<DP>::RP, CP = AccCfg<DP>::CP;
-  static constexpr int BM = 8 * RP, BN = 64, LD = DP + 4;
-  static constexpr int SR = BM / 16;                     // score rows per thread
-  static constexpr size_t q_off = 0;                               // int32 [BM][LD]
-  static constexpr size_t k_off = q_off + sizeof(int) * BM * LD;   // int32 [BN][LD]
-  static constexpr size_t v_off = k_off + sizeof(int) * BN * LD;   // int32 [BN][LD]
-  static constexpr size_t w_off = v_off + sizeof(int) * BN * LD;   // int32 [3][BN][BM]
-  static constexpr size_t wf_off = w_off + sizeof(int) * 3 * BN * BM;  // float [BN][BM]
-  static constexpr size_t p3_off = wf_off + sizeof(float) * BN * BM;   // int64 [BM][DP]
-  static constexpr size_t vm_off = p3_off + sizeof(long long) * BM * DP;  // uint32 [BN][DP/32]
-  static constexpr size_t ps_off = vm_off + sizeof(uint32_t) * BN * (DP / 32);  // uint16 [BN*BM]
-  static constexpr size_t bytes = ps_off + sizeof(uint16_t) * BN * BM;
+  static constexpr int BM = 8 * RP, BN = DP == 256 ? 32 : 64, LD = DP + 4, LDS = DP + 8, LDW = BM + 4;
+  static constexpr size_t q_off = 0;                                          // bf16 [4][BM][LDS]
+  static constexpr size_t k_off = q_off + sizeof(uint16_t) * NSLICE * BM * LDS;  // bf16 [4][BN][LDS]
+  static constexpr size_t v_off = k_off + sizeof(uint16_t) * NSLICE * BN * LDS;  // int32 [BN][LD]
+  static constexpr size_t w_off = v_off + sizeof(int) * BN * LD;                 // int32 [3][BN][LDW]
+  static constexpr size_t wf_off = w_off + sizeof(int) * 3 * BN * LDW;           // float [BN][BM]
+  static constexpr size_t p3_off = wf_off + sizeof(float) * BN * BM;             // int64 [BM][DP]
+  static constexpr size_t vm_off = p3_off + sizeof(long long) * BM * DP;         // uint32 [BN][DP/32]
+  static constexpr size_t ps_off = vm_off + sizeof(uint32_t) * BN * (DP / 32);    // uint16 [BN*BM] tiny weights
+  static constexpr size_t ls_off = ps_off + sizeof(uint16_t) * BN * BM;           // uint16 [BN*BM] low limb set
+  static constexpr size_t bytes = ls_off + sizeof(uint16_t) * BN * BM;
   static_assert(sizeof(long long) * BM * DP * 3 <= wf_off, "epilogue staging must fit in the tile area");
+  static_assert(bytes <= 227 * 1024, "shared memory budget");
 };
 
 // add a signed 64-bit X * 2^o into lazily carried radix-2^32 digits dg[]
@@ -215,26 +228,33 @@ template <int DT, int DP>
 __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
   using T = typename In<DT>::T;
   using L = AccLayout<DP>;
-  constexpr int RP = L::RP, CP = L::CP, BM = L::BM, BN = L::BN, LD = L::LD, SR = L::SR, NW = DP / 32;
+  constexpr int RP = L::RP, CP = L::CP, BM = L::BM, BN = L::BN, LD = L::LD, LDS = L::LDS, LDW = L::LDW;
+  constexpr int NW = DP / 32, NT = (BM / 16) * (BN / 8);
   extern __shared__ __align__(16) unsigned char smem_b[];
-  int* Qx = reinterpret_cast<int*>(smem_b + L::q_off);
-  int* Kx = reinterpret_cast<int*>(smem_b + L::k_off);
+  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem_b + L::q_off);
+  uint16_t* Ks = reinterpret_cast<uint16_t*>(smem_b + L::k_off);
   int* Vx = reinterpret_cast<int*>(smem_b + L::v_off);
   int* Wl = reinterpret_cast<int*>(smem_b + L::w_off);
   float* Wf = reinterpret_cast<float*>(smem_b + L::wf_off);
   long long* P3 = reinterpret_cast<long long*>(smem_b + L::p3_off);
   uint32_t* vmask = reinterpret_cast<uint32_t*>(smem_b + L::vm_off);
   uint16_t* plist = reinterpret_cast<uint16_t*>(smem_b + L::ps_off);
+  uint16_t* llist = reinterpret_cast<uint16_t*>(smem_b + L::ls_off);
   __shared__ int Fq[BM], Fk[BN], Fv[DP], Ev[DP];
   __shared__ unsigned char qfit[BM], kfit[BN];
   __shared__ float mrow[BM];
   __shared__ long long denT[BM][3];
-  __shared__ int s_np, s_vany, s_zeroed;
+  __shared__ int s_np, s_nl, s_nfix, s_vany, s_zeroed;
+  __shared__ uint16_t flist[BM * BN];   // pairs outside the fixed-point window, this tile
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.y, b = blockIdx.z, hk = h / (a.Hq / a.Hkv);
-  const int qt = gridDim.x - 1 - blockIdx.x;   // longest causal tiles first
-  const int q0 = qt * BM;
+  // causal: CTA x takes query tiles x and T-1-x, so every CTA sees about the same keys
+  const int ntiles = (a.Sq + BM - 1) / BM;
+  const int npass = (a.causal && blockIdx.x != ntiles - 1 - blockIdx.x) ? 2 : 1;
+  for (int pass = 0; pass < npass; pass++) {
+  const int q0 = (pass == 0 ? ntiles - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
+  if (pass) __syncthreads();
   const T* qbase = (const T*)a.q + b * a.qs[0] + h * a.qs[1];
   const T* kbase = (const T*)a.k + b * a.ks[0] + hk * a.ks[1];
   const T* vbase = (const T*)a.v + b * a.vs[0] + hk * a.vs[1];
@@ -243,15 +263,14 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
   long long* denb = a.den + rowbase * DEN_NDIG;
   const int nrows = min(BM, a.Sq - q0);
   int nf = 0, viol = 0;
-
   int lo = a.kv_lo, hi = a.kv_hi;
   if (a.causal) hi = min(hi, q0 + BM);
 
   // ---- set-up: Q tile, rowmax, per-column V exponent over [lo, hi) ----
   for (int r = warp; r < BM; r += 8) {
     int i = q0 + r;
-    convert_row_fixed<DT, DP>(i < a.Sq ? qbase + (int64_t)i * a.qs[2] : nullptr, a.D, Qx + r * LD, &Fq[r], &qfit[r], nf,
-                              lane);
+    convert_row_slices<DT, DP>(i < a.Sq ? qbase + (int64_t)i * a.qs[2] : nullptr, a.D, Qs + r * LDS, BM * LDS, &Fq[r],
+                               &qfit[r], nf, lane);
   }
   for (int r = tid; r < BM; r += 256) mrow[r] = (q0 + r < a.Sq) ? a.m_in[rowbase + q0 + r] : 0.0f;
   for (int d = tid; d < DP; d += 256) Ev[d] = 1;
@@ -260,15 +279,15 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
   __syncthreads();
   {
     constexpr int G = 256 / DP > 0 ? 256 / DP : 1;
-    const int d = tid % DP, g = tid / DP;
+    const int d = tid % DP, grp = tid / DP;
     int em = 1;
-    if (d < a.D && g < G)
-      for (int j = lo + g; j < hi; j += G) {
+    if (d < a.D && grp < G)
+      for (int j = lo + grp; j < hi; j += G) {
         uint32_t u = In<DT>::bits(vbase + (int64_t)j * a.vs[2], d);
         int ex = (int)((u >> 23) & 0xFFu);
         if (ex != 0xFF) em = max(em, ex);
       }
-    if (g < G) atomicMax(&Ev[d], em);
+    if (grp < G) atomicMax(&Ev[d], em);
   }
   __syncthreads();
   for (int d = tid; d < DP; d += 256) Fv[d] = Ev[d] - 149;   // |Vint| < 2^23
@@ -281,13 +300,8 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
     for (int c = 0; c < CP; c++)
 #pragma unroll
       for (int l = 0; l < 3; l++) acc[r][c][l] = 0;
-  long long den[SR][3];
-#pragma unroll
-  for (int r = 0; r < SR; r++)
-#pragma unroll
-    for (int l = 0; l < 3; l++) den[r][l] = 0;
-
-  const int ty = tid >> 4, tx = tid & 15;    // score layout: rows tx + 16r, keys ty + 16c
+  if (tid < BM * 3) (&denT[0][0])[tid] = 0;
+  const int g = lane >> 2, t = lane & 3;     // MMA fragment coordinates
   const int pr = warp, pc = lane;            // PV layout: rows pr*RP + r, cols pc*CP + c
   int tiles_since_carry = 0;
 
@@ -308,17 +322,49 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
       }
   };
 
+  auto weight_of = [&](float sc, float m, int& nfl, int& vio) -> float {
+    float x = __fsub_rn(sc, m);
+    if (x != x) { nfl |= ST_NONFINITE; x = neg_inf(); }
+    if (x > 0.0f) { vio |= ST_VIOLATION; x = 0.0f; }
+    return exp32_det(x);
+  };
+  // weight w of pair (rl, cl) -> limbs of W = w 2^92 in the Wl planes, the float in Wf,
+  // its denominator limbs into dp; weights outside the limb window go to the lists
+  auto store_weight = [&](float w, int rl, int cl, long long (&dp)[3]) {
+    uint32_t wb = __float_as_uint(w);
+    int ex = (int)(wb >> 23);
+    int l0 = 0, l1 = 0, l2 = 0;
+    if (wb != 0u) {
+      if (ex >= 58) {
+        unsigned __int128 W = ((unsigned __int128)((wb & 0x7FFFFFu) | 0x800000u)) << (ex - 58);
+        l0 = (int)((uint64_t)W & 0x7FFFFFFFull);
+        l1 = (int)((uint64_t)(W >> 31) & 0x7FFFFFFFull);
+        l2 = (int)(uint64_t)(W >> 62);
+        if (l0 != 0) llist[atomicAdd(&s_nl, 1)] = (uint16_t)(cl * BM + rl);   // w < 2^-38 (rare)
+        dp[0] += l0;
+        dp[1] += l1;
+        dp[2] += l2;
+      } else {
+        plist[atomicAdd(&s_np, 1)] = (uint16_t)(cl * BM + rl);
+      }
+    }
+    Wl[(0 * BN + cl) * LDW + rl] = l0;
+    Wl[(1 * BN + cl) * LDW + rl] = l1;
+    Wl[(2 * BN + cl) * LDW + rl] = l2;
+    Wf[cl * BM + rl] = w;
+  };
+
   for (int kt = lo; kt < hi; kt += BN) {
     __syncthreads();   // previous tile fully consumed
     // ---- K and V tiles ----
     for (int r = warp; r < BN; r += 8) {
       int j = kt + r;
-      convert_row_fixed<DT, DP>(j < hi ? kbase + (int64_t)j * a.ks[2] : nullptr, a.D, Kx + r * LD, &Fk[r], &kfit[r],
-                                nf, lane);
+      convert_row_slices<DT, DP>(j < hi ? kbase + (int64_t)j * a.ks[2] : nullptr, a.D, Ks + r * LDS, BN * LDS,
+                                 &Fk[r], &kfit[r], nf, lane);
       const T* vrow = j < hi ? vbase + (int64_t)j * a.vs[2] : nullptr;
 #pragma unroll
-      for (int t = 0; t < NW; t++) {
-        int d = lane + 32 * t;
+      for (int tv = 0; tv < NW; tv++) {
+        int d = lane + 32 * tv;
         uint32_t u = (vrow != nullptr && d < a.D) ? In<DT>::bits(vrow, d) : 0u;
         bool fit = true;
         int X = 0;
@@ -340,75 +386,41 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
         }
         Vx[r * LD + d] = X;
         uint32_t bad = __ballot_sync(0xFFFFFFFFu, !fit);
-        if (lane == 0) vmask[r * NW + t] = bad;
+        if (lane == 0) vmask[r * NW + tv] = bad;
       }
     }
-    if (tid == 0) { s_np = 0; s_vany = 0; }
+    if (tid == 0) { s_np = 0; s_nl = 0; s_nfix = 0; s_vany = 0; }
     __syncthreads();
-    // ---- scores, weights ----
-    {
-      long long sacc[SR][4];
+    // ---- exact scores on the tensor cores, then weights ----
+    for (int ot = warp; ot < NT; ot += 8) {
+      const int r0 = 16 * (ot / (BN / 8)), n0 = 8 * (ot % (BN / 8));
+      float sacc[NDIAG][4];
+      score_tile_mma<DP>(sacc, Qs, BM * LDS, Ks, BN * LDS, LDS, r0, n0, g, t);
+      long long dpart[2][3] = {{0, 0, 0}, {0, 0, 0}};
 #pragma unroll
-      for (int r = 0; r < SR; r++)
-#pragma unroll
-        for (int c = 0; c < 4; c++) sacc[r][c] = 0;
-#pragma unroll 2
-      for (int d = 0; d < DP; d += 4) {
-        int4 qv[SR], kv[4];
-#pragma unroll
-        for (int r = 0; r < SR; r++) qv[r] = *reinterpret_cast<const int4*>(Qx + (tx + 16 * r) * LD + d);
-#pragma unroll
-        for (int c = 0; c < 4; c++) kv[c] = *reinterpret_cast<const int4*>(Kx + (ty + 16 * c) * LD + d);
-#pragma unroll
-        for (int r = 0; r < SR; r++)
-#pragma unroll
-          for (int c = 0; c < 4; c++) {
-            sacc[r][c] += (long long)qv[r].x * kv[c].x;
-            sacc[r][c] += (long long)qv[r].y * kv[c].y;
-            sacc[r][c] += (long long)qv[r].z * kv[c].z;
-            sacc[r][c] += (long long)qv[r].w * kv[c].w;
+      for (int e = 0; e < 4; e++) {
+        const int rl = r0 + g + 8 * (e >> 1), cl = n0 + 2 * t + (e & 1);
+        const int i = q0 + rl, j = kt + cl;
+        float w = 0.0f;
+        if (i < a.Sq && j < hi && (!a.causal || j <= i)) {
+          if (!(qfit[rl] && kfit[cl])) {   // a row outside the window: deferred to one warp below
+            flist[atomicAdd(&s_nfix, 1)] = (uint16_t)(cl * BM + rl);
+            continue;
           }
-      }
-#pragma unroll
-      for (int r = 0; r < SR; r++) {
-        const int rl = tx + 16 * r, i = q0 + rl;
-#pragma unroll
-        for (int c = 0; c < 4; c++) {
-          const int cl = ty + 16 * c, j = kt + cl;
-          float w = 0.0f;
-          if (i < a.Sq && j < hi && (!a.causal || j <= i)) {
-            float dv = (qfit[rl] && kfit[cl])
-                           ? cr32_scaled(sacc[r][c], Fq[rl] + Fk[cl])
-                           : exact_dot_slow<DT>(qbase + (int64_t)i * a.qs[2], kbase + (int64_t)j * a.ks[2], a.D);
-            float s = __fmul_rn(a.scale32, dv);
-            float x = __fsub_rn(s, mrow[rl]);
-            if (x != x) { nf |= ST_NONFINITE; x = neg_inf(); }
-            if (x > 0.0f) { viol |= ST_VIOLATION; x = 0.0f; }
-            w = exp32_det(x);
-          }
-          uint32_t wb = __float_as_uint(w);
-          int ex = (int)(wb >> 23);
-          int l0 = 0, l1 = 0, l2 = 0;
-          if (wb != 0u) {
-            if (ex >= 58) {
-              unsigned __int128 W = ((unsigned __int128)((wb & 0x7FFFFFu) | 0x800000u)) << (ex - 58);
-              l0 = (int)((uint64_t)W & 0x7FFFFFFFull);
-              l1 = (int)((uint64_t)(W >> 31) & 0x7FFFFFFFull);
-              l2 = (int)(uint64_t)(W >> 62);
-              den[r][0] += l0;
-              den[r][1] += l1;
-              den[r][2] += l2;
-            } else {
-              int e = atomicAdd(&s_np, 1);
-              plist[e] = (uint16_t)(cl * BM + rl);
-            }
-          }
-          Wl[(0 * BN + cl) * BM + rl] = l0;
-          Wl[(1 * BN + cl) * BM + rl] = l1;
-          Wl[(2 * BN + cl) * BM + rl] = l2;
-          Wf[cl * BM + rl] = w;
+          float sc = __fmul_rn(a.scale32, cr32_scaled(combine_diag(sacc, e), Fq[rl] + Fk[cl]));
+          w = weight_of(sc, mrow[rl], nf, viol);
         }
+        store_weight(w, rl, cl, dpart[e >> 1]);
       }
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++)
+#pragma unroll
+        for (int l = 0; l < 3; l++) {
+          long long v = dpart[hh][l];
+          v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+          v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+          if (t == 0 && v) atomicAdd((unsigned long long*)&denT[r0 + g + 8 * hh][l], (unsigned long long)v);
+        }
     }
     if (lane == 0) {
       bool any = false;
@@ -416,14 +428,29 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
       if (any) s_vany = 1;
     }
     __syncthreads();
-    // ---- exact PV on the integer pipe ----
+    if (s_nfix > 0) {   // deferred pairs: one warp each computes the exact score, then the weight
+      for (int fe = warp; fe < s_nfix; fe += 8) {
+        const int cl = flist[fe] / BM, rl = flist[fe] % BM;
+        const float sc = __fmul_rn(a.scale32, exact_dot_warp<DT>(qbase + (int64_t)(q0 + rl) * a.qs[2],
+                                                                kbase + (int64_t)(kt + cl) * a.ks[2], a.D, lane));
+        if (lane == 0) {
+          long long dp[3] = {0, 0, 0};
+          store_weight(weight_of(sc, mrow[rl], nf, viol), rl, cl, dp);
+#pragma unroll
+          for (int l = 0; l < 3; l++)
+            if (dp[l]) atomicAdd((unsigned long long*)&denT[rl][l], (unsigned long long)dp[l]);
+        }
+      }
+      __syncthreads();
+    }
+    // ---- exact PV on the integer pipe: limbs 1 and 2 of every weight ----
 #pragma unroll 2
     for (int j = 0; j < BN; j++) {
-      int wv[3][RP];
+      int wv[2][RP];
       int vv[CP];
 #pragma unroll
-      for (int l = 0; l < 3; l++) {
-        const int* wp = Wl + (l * BN + j) * BM + pr * RP;
+      for (int l = 0; l < 2; l++) {
+        const int* wp = Wl + ((l + 1) * BN + j) * LDW + pr * RP;
         if constexpr (RP == 4) {
           int4 t4 = *reinterpret_cast<const int4*>(wp);
           wv[l][0] = t4.x; wv[l][1] = t4.y; wv[l][2] = t4.z; wv[l][3] = t4.w;
@@ -448,9 +475,24 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
 #pragma unroll
         for (int c = 0; c < CP; c++)
 #pragma unroll
-          for (int l = 0; l < 3; l++) acc[r][c][l] += (long long)wv[l][r] * vv[c];
+          for (int l = 0; l < 2; l++) mad_wide(acc[r][c][l + 1], wv[l][r], vv[c]);
     }
-    if (++tiles_since_carry == 4) {   // 256 keys: limb sums stay below 2^62
+    // ---- limb 0 is nonzero only for weights below 2^-38: the listed pairs of this tile ----
+    {
+      const int nl = s_nl;
+      for (int e = 0; e < nl; e++) {
+        const int cl = llist[e] / BM, rl = llist[e] % BM;
+        if (rl / RP != pr) continue;   // another warp's row
+        const int w0 = Wl[(0 * BN + cl) * LDW + rl];
+        const int* vp = Vx + cl * LD + pc * CP;
+#pragma unroll
+        for (int r = 0; r < RP; r++)
+          if (rl == pr * RP + r)
+#pragma unroll
+            for (int c = 0; c < CP; c++) mad_wide(acc[r][c][0], w0, vp[c]);
+      }
+    }
+    if (++tiles_since_carry == 256 / BN) {   // 256 keys: limb sums stay below 2^62
       carry_into_p3();
       tiles_since_carry = 0;
     }
@@ -502,12 +544,7 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
 
   // ---- epilogue: canonical digits ----
   carry_into_p3();
-  if (tid < BM * 3) (&denT[0][0])[tid] = 0;
   __syncthreads();   // tiles consumed; the tile area becomes the staging area below
-#pragma unroll
-  for (int r = 0; r < SR; r++)
-#pragma unroll
-    for (int l = 0; l < 3; l++) atomicAdd((unsigned long long*)&denT[tx + 16 * r][l], (unsigned long long)den[r][l]);
   long long* stage = reinterpret_cast<long long*>(smem_b);   // [BM][DP][3], fits in the Q/K/V/W tiles
 #pragma unroll
   for (int r = 0; r < RP; r++)
@@ -569,6 +606,9 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
     drow[DEN_NDIG - 1] = top;
   }
   report(a.status, nf | viol);
+  nf = 0;
+  viol = 0;
+  }   // pass
 }
 
 // ---------------------------------------------------------------------------------------
@@ -576,11 +616,12 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
 // ---------------------------------------------------------------------------------------
 template <int DT, int DP>
 static cudaError_t launch_rowmax_t(const AttnArgs& a, cudaStream_t st) {
-  constexpr int BM = 64, BN = 64, LD = DP + 4;
-  const size_t smem = sizeof(int) * (BM + BN) * LD;
+  using L = RowmaxLayout<DP>;
+  const size_t smem = L::bytes;
   cudaError_t e = cudaFuncSetAttribute(rowmax_kernel<DT, DP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.Sq + BM - 1) / BM, a.Hq, a.B);
+  const int nt = (a.Sq + L::BM - 1) / L::BM;
+  dim3 grid(a.causal ? (nt + 1) / 2 : nt, a.Hq, a.B);
   rowmax_kernel<DT, DP><<<grid, 256, smem, st>>>(a);
   return cudaGetLastError();
 }
@@ -592,7 +633,8 @@ static cudaError_t launch_accumulate_t(const AttnArgs& a, cudaStream_t st) {
   cudaError_t e =
       cudaFuncSetAttribute(accumulate_kernel<DT, DP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.Sq + L::BM - 1) / L::BM, a.Hq, a.B);
+  const int nt = (a.Sq + L::BM - 1) / L::BM;
+  dim3 grid(a.causal ? (nt + 1) / 2 : nt, a.Hq, a.B);
   accumulate_kernel<DT, DP><<<grid, 256, smem, st>>>(a);
   return cudaGetLastError();
 }

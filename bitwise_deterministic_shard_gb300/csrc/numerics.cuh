@@ -56,10 +56,12 @@ __device__ __forceinline__ bool nonfinite_bits(uint32_t u) { return ((u >> 23) &
 __device__ __forceinline__ float exp32_det(float x) {
   if (x != x) return x;
   if (x < -104.0f) return 0.0f;
-  const float L2E = 0x1.715476p+0f, C1 = 0x1.62e4p-1f, C2 = 0x1.7f7d1cp-20f;
+  const float L2E = 0x1.715476p+0f, C1 = 0x1.62e4p-1f, C2 = 0x1.7f7d1cp-20f, MAGIC = 12582912.0f;  // 1.5 * 2^23
   float t = __fmul_rn(x, L2E);
-  int k = __float2int_rn(t);          // ties to even
-  float kf = __int2float_rn(k);       // exact
+  // k = rint(t), ties to even: |t| <= 151, so t + 1.5 * 2^23 rounds t to an integer exactly
+  float tr = __fadd_rn(t, MAGIC);
+  int k = __float_as_int(tr) - 0x4B400000;
+  float kf = __fsub_rn(tr, MAGIC);    // exact
   float r1 = __fmaf_rn(-kf, C1, x);   // exact (Cody-Waite)
   float r = __fmaf_rn(-kf, C2, r1);
   float p = 0x1.a01a02p-13f;
@@ -74,6 +76,10 @@ __device__ __forceinline__ float exp32_det(float x) {
   if (k >= -126) return __fmul_rn(p, __uint_as_float((uint32_t)(k + 127) << 23));
   return __fmul_rn(__fmul_rn(p, __uint_as_float((uint32_t)(k + 64 + 127) << 23)), 0x1p-64f);
 }
+
+// exact small-integer <-> binary32 conversions on the FP32/integer pipes (|v| <= 2^22)
+__device__ __forceinline__ int small_f2i(float f) { return __float_as_int(__fadd_rn(f, 12582912.0f)) - 0x4B400000; }
+__device__ __forceinline__ float small_i2f(int v) { return __fsub_rn(__int_as_float(0x4B400000 + v), 12582912.0f); }
 
 // ---------------------------------------------------------------------------------------
 // Round an exact value to binary32 (ties to even, gradual underflow, overflow -> inf).
@@ -113,16 +119,35 @@ __device__ __forceinline__ float round_f32(unsigned __int128 W, bool sticky, int
   return __uint_as_float(bitsv | (neg ? 0x80000000u : 0u));
 }
 
-// RN32(T * 2^F) for an integer T, |T| < 2^63.
+// RN32(T * 2^F) for an integer T, |T| < 2^63: integer operations only (the 64-bit
+// integer -> float conversion runs on the slow FP64 path of this GPU).
 __device__ __forceinline__ float cr32_scaled(long long T, int F) {
   if (T == 0) return 0.0f;
-  float f = __ll2float_rn(T);
-  uint32_t b = __float_as_uint(f);
-  int ne = (int)((b >> 23) & 0xFFu) + F;
-  if (ne >= 1 && ne <= 254) return __uint_as_float(b + ((uint32_t)F << 23));
-  if (ne > 254) return T < 0 ? -__int_as_float(0x7F800000) : __int_as_float(0x7F800000);
-  unsigned long long mag = T < 0 ? 0ull - (unsigned long long)T : (unsigned long long)T;
-  return round_f32((unsigned __int128)mag, false, F, T < 0);
+  const int neg = T < 0;
+  const unsigned long long mag = neg ? 0ull - (unsigned long long)T : (unsigned long long)T;
+  const int tb = 63 - __clzll((long long)mag);   // top bit index
+  const int e = tb + F;                           // 2^e <= |value| < 2^(e+1)
+  int q = (e > -126 ? e : -126) - 23;             // exponent of the last kept bit
+  const int sh = q - F;                           // low bits of mag to drop
+  unsigned long long n;
+  if (sh <= 0) {
+    n = mag << (-sh);                             // exact, n < 2^24
+  } else if (sh >= 64) {
+    n = 0;                                        // below half the smallest subnormal
+  } else {
+    n = mag >> sh;
+    const unsigned long long rem = mag & ((1ull << sh) - 1ull), half = 1ull << (sh - 1);
+    if (rem > half || (rem == half && (n & 1ull))) n++;
+  }
+  uint32_t bitsv;
+  if (n < 0x800000ull) {
+    bitsv = (uint32_t)n;                          // subnormal or zero (q == -149)
+  } else {
+    if (n == 0x1000000ull) { n = 0x800000ull; q++; }
+    const int be = q + 150;
+    bitsv = be >= 255 ? 0x7F800000u : (((uint32_t)be << 23) | ((uint32_t)n & 0x7FFFFFu));
+  }
+  return __uint_as_float(bitsv | (neg ? 0x80000000u : 0u));
 }
 
 // ---------------------------------------------------------------------------------------
@@ -183,6 +208,74 @@ __device__ float exact_dot_slow(const typename In<DT>::T* q, const typename In<D
     kul_add(a, (unsigned long long)sq.mant * sk.mant, sq.neg ^ sk.neg, sq.lsb + sk.lsb);
   }
   return kul_round_f32(a, KW, -320);
+}
+
+// ---------------------------------------------------------------------------------------
+// Exact score of one pair by one warp, for rows outside the 26-bit fixed-point window:
+// each row is taken as a 52-bit fixed point X = x 2^-Flo (Flo = row max exponent - 178),
+// split in two signed 26-bit limbs; lanes split D, the four limb-product sums are exact
+// int64s reduced across the warp, and the 128-bit total is rounded once.  A row whose
+// elements span even more than the 52-bit window takes the Kulisch fallback.  Every lane
+// returns the same value.
+// ---------------------------------------------------------------------------------------
+template <int DT>
+__device__ float exact_dot_warp(const typename In<DT>::T* q, const typename In<DT>::T* k, int D, int lane) {
+  int eq = 1, ek = 1;
+  for (int d = lane; d < D; d += 32) {
+    const uint32_t a = In<DT>::bits(q, d), b = In<DT>::bits(k, d);
+    if (!nonfinite_bits(a)) eq = max(eq, (int)((a >> 23) & 0xFFu));
+    if (!nonfinite_bits(b)) ek = max(ek, (int)((b >> 23) & 0xFFu));
+  }
+  eq = __reduce_max_sync(0xFFFFFFFFu, eq);
+  ek = __reduce_max_sync(0xFFFFFFFFu, ek);
+  const int Fq = eq - 178, Fk = ek - 178;   // |X| < 2^52
+  long long shh = 0, shl = 0, slh = 0, sll = 0;
+  bool ok = true;
+  for (int d = lane; d < D; d += 32) {
+    uint32_t a = In<DT>::bits(q, d), b = In<DT>::bits(k, d);
+    if (nonfinite_bits(a)) a = 0u;
+    if (nonfinite_bits(b)) b = 0u;
+    long long X[2];
+    const uint32_t uu[2] = {a, b};
+    const int FF[2] = {Fq, Fk};
+#pragma unroll
+    for (int z = 0; z < 2; z++) {
+      const Split s = split_f32(uu[z]);
+      const int sh = s.lsb - FF[z];   // <= 28
+      long long v = 0;
+      if (s.mant) {
+        if (sh >= 0) {
+          v = (long long)s.mant << sh;
+        } else if (sh > -32) {
+          v = (long long)(s.mant >> (-sh));
+          ok = ok && ((s.mant & ((1u << (-sh)) - 1u)) == 0u);
+        } else {
+          ok = false;
+        }
+        if (s.neg) v = -v;
+      }
+      X[z] = v;
+    }
+    const long long qh = X[0] >> 26, ql = X[0] - qh * (1ll << 26);   // ql in [0, 2^26)
+    const long long kh = X[1] >> 26, kl = X[1] - kh * (1ll << 26);
+    shh += qh * kh;
+    shl += qh * kl;
+    slh += ql * kh;
+    sll += ql * kl;
+  }
+  if (!__all_sync(0xFFFFFFFFu, ok)) return exact_dot_slow<DT>(q, k, D);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    shh += __shfl_xor_sync(0xFFFFFFFFu, shh, o);
+    shl += __shfl_xor_sync(0xFFFFFFFFu, shl, o);
+    slh += __shfl_xor_sync(0xFFFFFFFFu, slh, o);
+    sll += __shfl_xor_sync(0xFFFFFFFFu, sll, o);
+  }
+  const __int128 T = (__int128)shh * ((__int128)1 << 52) + (__int128)(shl + slh) * (1ll << 26) + (__int128)sll;
+  if (T == 0) return 0.0f;
+  const int neg = T < 0;
+  const unsigned __int128 mag = neg ? (unsigned __int128)(-T) : (unsigned __int128)T;
+  return round_f32(mag, false, Fq + Fk, neg);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -269,6 +362,18 @@ __device__ __forceinline__ void atomic_digits_add(long long* dg, int64_t stride,
   for (int t = 0; t < 3; t++)
     if (c[t]) atomicAdd((unsigned long long*)(dg + (int64_t)(k + t) * stride), neg ? (0ull - c[t]) : c[t]);
 }
+
+// acc += a * b exactly: one 32x32 -> 64-bit signed multiply-add (mad.wide.s32)
+__device__ __forceinline__ void mad_wide(long long& acc, int a, int b) {
+  asm("mad.wide.s32 %0, %1, %2, %0;" : "+l"(acc) : "r"(a), "r"(b));
+}
+
+// order-preserving int key of a binary32 (not NaN): key(a) < key(b) iff a < b, with -0 < +0
+__device__ __forceinline__ int float_key(float f) {
+  const int b = __float_as_int(f);
+  return b >= 0 ? b : (b ^ 0x7FFFFFFF);
+}
+__device__ __forceinline__ float key_float(int k) { return __int_as_float(k >= 0 ? k : (k ^ 0x7FFFFFFF)); }
 
 __device__ __forceinline__ void report(int* status, int bits) {
   if (bits && status) atomicOr(status, bits);

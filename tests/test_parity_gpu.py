@@ -111,6 +111,51 @@ def test_wide_exponent_inputs_take_the_exact_fallbacks(da, orc):
 
 
 @cuda
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows_outside_the_fast_window_match_oracle(da, orc, causal):
+    """Rows with one element 20 to 40 binades below the row maximum do not fit the 26-bit
+    fixed point of the tensor-core path; their pairs take the deferred one-warp exact dot
+    (52-bit window).  Every third Q and K row is made such a row."""
+    g = torch.Generator().manual_seed(70 + causal)
+    Q, K, V = (torch.randn(1, 2, 150, 128, generator=g) for _ in range(3))
+    for X in (Q, K):
+        for r in range(0, 150, 3):
+            X[:, :, r, r % 128] *= 2.0 ** -(20 + r % 21)
+    Q, K, V = Q.to(torch.bfloat16), K.to(torch.bfloat16), V.to(torch.bfloat16)
+    st = da.new_status()
+    m, num, den, out, fused = run_full(da, Q, K, V, causal, status=st)
+    assert da.read_status(st) == 0
+    m_o, num_o, den_o, out_o = orc.Attn(Q, K, V, causal).forward_rows()
+    assert_bits_equal(m.reshape(-1), m_o, "rowmax")
+    assert torch.equal(num.cpu().reshape(-1, 15, 128), torch.from_numpy(num_o)), "NUM digits"
+    assert torch.equal(den.cpu().reshape(-1, 6), torch.from_numpy(den_o)), "DEN digits"
+    assert_bits_equal(fused.reshape(-1, 128), out_o, "output")
+
+
+@cuda
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_extreme_digit_patterns_match_oracle(da, orc, D):
+    """Every element has all eight significand bits set, exponents spread to the edge of
+    the 26-bit fixed-point window: the tensor-core digit slices take their largest values,
+    so the diagonal sums reach the top of their exactness bound."""
+    g = torch.Generator().manual_seed(60 + D)
+
+    def draw(h, S):
+        e = torch.randint(-18, 1, (1, h, S, D), generator=g).float()
+        sign = torch.randint(0, 2, (1, h, S, D), generator=g).float() * 2 - 1
+        return (sign * (2.0 - 2.0 ** -7) * torch.exp2(e)).to(torch.bfloat16)
+
+    Q, K = draw(2, 70), draw(2, 70)
+    V = torch.randn(1, 2, 70, D, generator=g).to(torch.bfloat16)
+    out = da.det_attn(Q.cuda(), K.cuda(), V.cuda(), causal=True)
+    m = da.rowmax(Q.cuda(), K.cuda(), causal=True)
+    A = orc.Attn(Q, K, V, causal=True)
+    m_o, _, _, out_o = A.forward_rows()
+    assert_bits_equal(m.reshape(-1), m_o, "rowmax")
+    assert_bits_equal(out.reshape(-1, D), out_o, "output")
+
+
+@cuda
 def test_c1_fused_and_all_24_orders(da, orc):
     w = W.c1()
     Q, K, V = w.tensors("cuda")
