@@ -147,6 +147,7 @@ def run_ours(args, rank, world, local_rank):
     P = da._Problem(Q, K, V, True, None)
     L = da.lib()
     ws = torch.empty(L.da_workspace_bytes(P.ref(), 1), dtype=torch.uint8, device=dev)
+    kvws = torch.empty(L.da_kv_workspace_bytes(P.ref()), dtype=torch.uint8, device=dev)
     rows = w.B * w.Hq * w.S
     m = torch.empty(rows, dtype=torch.float32, device=dev)
     num = torch.empty(rows, 15, w.D, dtype=torch.int64, device=dev)
@@ -161,10 +162,10 @@ def run_ours(args, rank, world, local_rank):
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        assert L.da_rowmax(P.ref(), 0, w.S, ptr(m), sp) == 0
+        assert L.da_rowmax(P.ref(), 0, w.S, ptr(m), ptr(kvws), kvws.numel(), sp) == 0
         if ev:
             ev[1].record(stream)
-        assert L.da_accumulate(P.ref(), ptr(m), 0, w.S, ptr(num), ptr(den), 0, sp) == 0
+        assert L.da_accumulate(P.ref(), ptr(m), 0, w.S, ptr(num), ptr(den), 0, ptr(kvws), kvws.numel(), sp) == 0
         if ev:
             ev[2].record(stream)
         assert L.da_finalize(ptr(num), ptr(den), w.B, w.Hq, w.S, w.D, ptr(out), None, sp) == 0

@@ -61,8 +61,10 @@ def lib():
         L.da_status_string.restype = C.c_char_p
         D = C.POINTER(_Desc)
         M = C.POINTER(_Matrix)
-        L.da_rowmax.argtypes = [D, _I64, _I64, _P, _P]
-        L.da_accumulate.argtypes = [D, _P, _I64, _I64, _P, _P, _I32, _P]
+        L.da_kv_workspace_bytes.argtypes = [D]
+        L.da_kv_workspace_bytes.restype = C.c_size_t
+        L.da_rowmax.argtypes = [D, _I64, _I64, _P, _P, C.c_size_t, _P]
+        L.da_accumulate.argtypes = [D, _P, _I64, _I64, _P, _P, _I32, _P, C.c_size_t, _P]
         L.da_compose_max.argtypes = [_P, _P, _I64, _P]
         L.da_compose_add.argtypes = [_P, _P, _I64, _P]
         L.da_normalize.argtypes = [_P, _I64, _I32, _I64, _P, _P]
@@ -162,6 +164,13 @@ def _workspace(P: _Problem, nsplits: int, ws):
     return ws
 
 
+def _kv_workspace(P: _Problem, ws):
+    need = int(lib().da_kv_workspace_bytes(P.ref()))
+    if ws is None or ws.numel() * ws.element_size() < need:
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=P.device)
+    return ws
+
+
 def det_attn(Q, K, V, causal=False, scale=None, out=None, workspace=None, status=None):
     """Fused deterministic attention (det-attn "API": det_attn); f32 output [B, Hq, Sq, D]."""
     P = _Problem(Q, K, V, causal, scale, status)
@@ -186,18 +195,19 @@ def det_attn_sharded(Q, K, V, kv_splits, causal=False, scale=None, order=None, o
     return out
 
 
-def rowmax(Q, K, kv_lo=0, kv_hi=None, causal=False, scale=None, out=None, status=None):
+def rowmax(Q, K, kv_lo=0, kv_hi=None, causal=False, scale=None, out=None, status=None, workspace=None):
     """Per-query rowmax over keys [kv_lo, kv_hi) (det-attn "API": rowmax); f32 [B, Hq, Sq].
     Shards combine with compose_max (or torch.maximum)."""
     P = _Problem(Q, K, K, causal, scale, status)
     kv_hi = P.Skv if kv_hi is None else kv_hi
     m = torch.empty(P.B, P.Hq, P.Sq, dtype=torch.float32, device=P.device) if out is None else out
-    _check(lib().da_rowmax(P.ref(), kv_lo, kv_hi, _ptr(m), _stream()), "rowmax")
+    ws = _kv_workspace(P, workspace)
+    _check(lib().da_rowmax(P.ref(), kv_lo, kv_hi, _ptr(m), _ptr(ws), ws.numel(), _stream()), "rowmax")
     return m
 
 
 def accumulate(Q, K, V, m, kv_lo=0, kv_hi=None, causal=False, scale=None, num=None, den=None, add_into=False,
-               status=None):
+               status=None, workspace=None):
     """Exact NUM/DEN digits of keys [kv_lo, kv_hi) with the global rowmax m (det-attn "API":
     accumulate).  Returns (num int64 [B,Hq,Sq,15,D], den int64 [B,Hq,Sq,6]), canonical."""
     P = _Problem(Q, K, V, causal, scale, status)
@@ -207,8 +217,9 @@ def accumulate(Q, K, V, m, kv_lo=0, kv_hi=None, causal=False, scale=None, num=No
     if den is None:
         den = torch.empty(P.B, P.Hq, P.Sq, DEN_NDIG, dtype=torch.int64, device=P.device)
     m = m.contiguous()
+    ws = _kv_workspace(P, workspace)
     _check(lib().da_accumulate(P.ref(), _ptr(m), kv_lo, kv_hi, _ptr(num), _ptr(den), 1 if add_into else 0,
-                               _stream()), "accumulate")
+                               _ptr(ws), ws.numel(), _stream()), "accumulate")
     return num, den
 
 

@@ -61,8 +61,10 @@ int launched(cudaError_t e) { return e == cudaSuccess ? DA_OK : DA_ECUDA; }
 size_t round_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t m, m2, num, den, total;
+  size_t m, m2, num, den, kv, total;
 };
+
+size_t kv_bytes(const da_attn_desc* d) { return kv_prep_bytes((int)d->k.B, (int)d->k.H, (int)d->k.S, (int)d->k.D); }
 
 WsLayout ws_layout(const da_attn_desc* d, int nsplits) {
   const size_t rows = (size_t)d->q.B * d->q.H * d->q.S;
@@ -71,8 +73,15 @@ WsLayout ws_layout(const da_attn_desc* d, int nsplits) {
   w.m2 = round_up(rows * 4);
   w.num = w.m2 + (nsplits > 1 ? round_up(rows * 4) : 0);
   w.den = w.num + round_up(rows * DA_NUM_NDIG * (size_t)d->q.D * 8);
-  w.total = w.den + round_up(rows * DA_DEN_NDIG * 8);
+  w.kv = w.den + round_up(rows * DA_DEN_NDIG * 8);
+  w.total = w.kv + round_up(kv_bytes(d));
   return w;
+}
+
+int check_kv_ws(const da_attn_desc* d, void* ws, size_t ws_bytes) {
+  if (!ws || ws_bytes < kv_bytes(d)) return DA_EWORKSPACE;
+  if (!aligned(ws, 256)) return DA_EALIGN;
+  return DA_OK;
 }
 
 int check_matrix(const da_matrix* x) {
@@ -98,7 +107,7 @@ DceArgs make_dce(const da_matrix* x) {
 
 extern "C" {
 
-DA_EXPORT int da_abi_version(void) { return 1; }
+DA_EXPORT int da_abi_version(void) { return 2; }
 
 DA_EXPORT const char* da_status_string(int code) {
   switch (code) {
@@ -113,30 +122,44 @@ DA_EXPORT const char* da_status_string(int code) {
   }
 }
 
-DA_EXPORT int da_rowmax(const da_attn_desc* desc, int64_t kv_lo, int64_t kv_hi, float* m, da_stream_t stream) {
+DA_EXPORT size_t da_kv_workspace_bytes(const da_attn_desc* desc) {
+  if (check_desc(desc)) return 0;
+  return kv_bytes(desc);
+}
+
+DA_EXPORT int da_rowmax(const da_attn_desc* desc, int64_t kv_lo, int64_t kv_hi, float* m, void* ws, size_t ws_bytes,
+                        da_stream_t stream) {
   int e = check_desc(desc);
   if (e) return e;
   if (kv_lo < 0 || kv_hi < kv_lo || kv_hi > desc->k.S) return DA_EINVAL;
   if (desc->q.B * desc->q.S == 0) return DA_OK;
   if (!m) return DA_EINVAL;
   if (!aligned(m, 4)) return DA_EALIGN;
+  if ((e = check_kv_ws(desc, ws, ws_bytes))) return e;
   AttnArgs a = make_args(desc);
   a.kv_lo = (int)kv_lo; a.kv_hi = (int)kv_hi; a.m_out = m;
-  return launched(launch_rowmax(a, (cudaStream_t)stream));
+  KvPrep p = kv_prep_layout(ws, a.B, a.Hkv, a.Skv, a.D, 0);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (launch_kv_prep(a, p, st) != cudaSuccess) return DA_ECUDA;
+  return launched(launch_rowmax(a, p, st));
 }
 
 DA_EXPORT int da_accumulate(const da_attn_desc* desc, const float* m, int64_t kv_lo, int64_t kv_hi, int64_t* num,
-                  int64_t* den, int add_into, da_stream_t stream) {
+                            int64_t* den, int add_into, void* ws, size_t ws_bytes, da_stream_t stream) {
   int e = check_desc(desc);
   if (e) return e;
   if (kv_lo < 0 || kv_hi < kv_lo || kv_hi > desc->k.S) return DA_EINVAL;
   if (desc->q.B * desc->q.S == 0) return DA_OK;
   if (!m || !num || !den) return DA_EINVAL;
   if (!aligned(m, 4) || !aligned(num, 8) || !aligned(den, 8)) return DA_EALIGN;
+  if ((e = check_kv_ws(desc, ws, ws_bytes))) return e;
   AttnArgs a = make_args(desc);
   a.kv_lo = (int)kv_lo; a.kv_hi = (int)kv_hi;
   a.m_in = m; a.num = (long long*)num; a.den = (long long*)den; a.add_into = add_into ? 1 : 0;
-  return launched(launch_accumulate(a, (cudaStream_t)stream));
+  KvPrep p = kv_prep_layout(ws, a.B, a.Hkv, a.Skv, a.D, 1);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (launch_kv_prep(a, p, st) != cudaSuccess) return DA_ECUDA;
+  return launched(launch_accumulate(a, p, st));
 }
 
 DA_EXPORT int da_compose_max(float* dst, const float* src, int64_t n, da_stream_t stream) {
@@ -191,8 +214,10 @@ DA_EXPORT int da_det_attn(const da_attn_desc* desc, float* out, void* ws, size_t
   float* m = (float*)(base + w.m);
   int64_t* num = (int64_t*)(base + w.num);
   int64_t* den = (int64_t*)(base + w.den);
-  if ((e = da_rowmax(desc, 0, desc->k.S, m, stream))) return e;
-  if ((e = da_accumulate(desc, m, 0, desc->k.S, num, den, 0, stream))) return e;
+  void* kv = base + w.kv;
+  const size_t kvb = ws_bytes - w.kv;
+  if ((e = da_rowmax(desc, 0, desc->k.S, m, kv, kvb, stream))) return e;
+  if ((e = da_accumulate(desc, m, 0, desc->k.S, num, den, 0, kv, kvb, stream))) return e;
   return da_finalize(num, den, desc->q.B, desc->q.H, desc->q.S, desc->q.D, out, desc->dev_status, stream);
 }
 
@@ -228,17 +253,19 @@ DA_EXPORT int da_det_attn_sharded(const da_attn_desc* desc, const int64_t* kv_sp
   float* m2 = (float*)(base + w.m2);
   int64_t* num = (int64_t*)(base + w.num);
   int64_t* den = (int64_t*)(base + w.den);
+  void* kv = base + w.kv;
+  const size_t kvb = ws_bytes - w.kv;
   const int64_t rows = desc->q.B * desc->q.H * desc->q.S;
   // pass 1: shard rowmaxes composed by max (a max all-reduce across context-parallel ranks)
   for (int k = 0; k < nsplits; k++) {
     const int s = ord[k];
-    if ((e = da_rowmax(desc, lo[s], hi[s], k == 0 ? m : m2, stream))) return e;
+    if ((e = da_rowmax(desc, lo[s], hi[s], k == 0 ? m : m2, kv, kvb, stream))) return e;
     if (k > 0 && (e = da_compose_max(m, m2, rows, stream))) return e;
   }
   // pass 2: shard digits with the global rowmax, composed by integer add (a sum reduce)
   for (int k = 0; k < nsplits; k++) {
     const int s = ord[k];
-    if ((e = da_accumulate(desc, m, lo[s], hi[s], num, den, k == 0 ? 0 : 1, stream))) return e;
+    if ((e = da_accumulate(desc, m, lo[s], hi[s], num, den, k == 0 ? 0 : 1, kv, kvb, stream))) return e;
   }
   return da_finalize(num, den, desc->q.B, desc->q.H, desc->q.S, desc->q.D, out, desc->dev_status, stream);
 }

@@ -85,8 +85,29 @@ struct RowmaxLayout {
   static constexpr size_t bytes = q_bytes + sizeof(uint16_t) * NSLICE * BN * LDS;
 };
 
+// copy rows [kt, kt + nrow) of the prepared K slices into a smem slice tile; rows at or
+// past hi are zero-filled (their pairs are masked)
+template <int DP>
+__device__ __forceinline__ void load_k_tile(const KvPrep& p, int64_t rowbase, int kt, int hi, int nrow, uint16_t* Ks,
+                                            int LDS, int* Fk, unsigned char* kfit, int tid) {
+  constexpr int CH = DP / 8;   // 16-byte chunks per slice row
+  for (int c = tid; c < nrow * NSLICE * CH; c += 256) {
+    const int r = c / (NSLICE * CH), q = (c / CH) % NSLICE, x = c % CH;
+    const int j = kt + r;
+    const bool ok = j < hi;
+    const uint16_t* src = p.ksl + ((rowbase + (ok ? j : kt)) * NSLICE + q) * DP + 8 * x;
+    cp_async16(Ks + q * nrow * LDS + r * LDS + 8 * x, src, ok ? 16 : 0);
+  }
+  for (int r = tid; r < nrow; r += 256) {
+    const int j = kt + r;
+    const int mv = j < hi ? p.kmeta[rowbase + j] : (1024 - 151) | (1 << 16);
+    Fk[r] = (mv & 0xFFFF) - 1024;
+    kfit[r] = (unsigned char)(mv >> 16);
+  }
+}
+
 template <int DT, int DP>
-__global__ void __launch_bounds__(256) rowmax_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(256) rowmax_kernel(const AttnArgs a, const KvPrep p) {
   using T = typename In<DT>::T;
   using L = RowmaxLayout<DP>;
   constexpr int BM = L::BM, BN = L::BN, LDS = L::LDS;
@@ -124,14 +145,12 @@ __global__ void __launch_bounds__(256) rowmax_kernel(const AttnArgs a) {
   const int r0 = 16 * (warp >> 1), nb = 16 * (warp & 1);
   float rmax[2] = {neg_inf(), neg_inf()};   // rows r0 + g, r0 + g + 8
 
+  const int64_t krow0 = ((int64_t)b * a.Hkv + hk) * a.Skv;
   for (int kt = lo; kt < hi; kt += BN) {
     __syncthreads();
     if (tid == 0) s_nfix = 0;
-    for (int r = warp; r < BN; r += 8) {
-      int j = kt + r;
-      convert_row_slices<DT, DP>(j < hi ? kbase + (int64_t)j * a.ks[2] : nullptr, a.D, Ks + r * LDS, BN * LDS,
-                                 &Fk[r], &kfit[r], nf, lane);
-    }
+    load_k_tile<DP>(p, krow0, kt, hi, BN, Ks, LDS, Fk, kfit, tid);
+    cp_async_wait_all();
     __syncthreads();
 #pragma unroll
     for (int nt = 0; nt < 2; nt++) {
@@ -189,14 +208,15 @@ __global__ void __launch_bounds__(256) rowmax_kernel(const AttnArgs a) {
 // K2: exact accumulate.
 // =======================================================================================
 template <int DP> struct AccCfg;
-template <> struct AccCfg<64>  { static constexpr int RP = 4, CP = 2; };
-template <> struct AccCfg<128> { static constexpr int RP = 4, CP = 4; };
-template <> struct AccCfg<256> { static constexpr int RP = 2, CP = 8; };
+// RP x CP accumulators per thread; MINB CTAs per SM (register and shared-memory budget)
+template <> struct AccCfg<64>  { static constexpr int RP = 4, CP = 2, MINB = 2; };
+template <> struct AccCfg<128> { static constexpr int RP = 2, CP = 4, MINB = 2; };
+template <> struct AccCfg<256> { static constexpr int RP = 2, CP = 8, MINB = 1; };
 
 template <int DP>
 struct AccLayout {
   static constexpr int RP = AccCfg<DP>::RP, CP = AccCfg<DP>::CP;
-  static constexpr int BM = 8 * RP, BN = DP == 256 ? 32 : 64, LD = DP + 4, LDS = DP + 8, LDW = BM + 4;
+  static constexpr int BM = 8 * RP, BN = 32, LD = DP + 4, LDS = DP + 8, LDW = BM + 4;
   static constexpr size_t q_off = 0;                                          // bf16 [4][BM][LDS]
   static constexpr size_t k_off = q_off + sizeof(uint16_t) * NSLICE * BM * LDS;  // bf16 [4][BN][LDS]
   static constexpr size_t v_off = k_off + sizeof(uint16_t) * NSLICE * BN * LDS;  // int32 [BN][LD]
@@ -209,6 +229,7 @@ struct AccLayout {
   static constexpr size_t bytes = ls_off + sizeof(uint16_t) * BN * BM;
   static_assert(sizeof(long long) * BM * DP * 3 <= wf_off, "epilogue staging must fit in the tile area");
   static_assert(bytes <= 227 * 1024, "shared memory budget");
+  static_assert(AccCfg<DP>::MINB == 1 || bytes + 8 * 1024 <= 113 * 1024, "two CTAs per SM");
 };
 
 // add a signed 64-bit X * 2^o into lazily carried radix-2^32 digits dg[]
@@ -225,7 +246,7 @@ __device__ __forceinline__ void digits_add_i64(long long* dg, long long X, int o
 }
 
 template <int DT, int DP>
-__global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(256, AccCfg<DP>::MINB) accumulate_kernel(const AttnArgs a, const KvPrep p) {
   using T = typename In<DT>::T;
   using L = AccLayout<DP>;
   constexpr int RP = L::RP, CP = L::CP, BM = L::BM, BN = L::BN, LD = L::LD, LDS = L::LDS, LDW = L::LDW;
@@ -240,7 +261,7 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
   uint32_t* vmask = reinterpret_cast<uint32_t*>(smem_b + L::vm_off);
   uint16_t* plist = reinterpret_cast<uint16_t*>(smem_b + L::ps_off);
   uint16_t* llist = reinterpret_cast<uint16_t*>(smem_b + L::ls_off);
-  __shared__ int Fq[BM], Fk[BN], Fv[DP], Ev[DP];
+  __shared__ int Fq[BM], Fk[BN], Fv[DP];
   __shared__ unsigned char qfit[BM], kfit[BN];
   __shared__ float mrow[BM];
   __shared__ long long denT[BM][3];
@@ -273,24 +294,11 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
                                &qfit[r], nf, lane);
   }
   for (int r = tid; r < BM; r += 256) mrow[r] = (q0 + r < a.Sq) ? a.m_in[rowbase + q0 + r] : 0.0f;
-  for (int d = tid; d < DP; d += 256) Ev[d] = 1;
   for (int e = tid; e < BM * DP; e += 256) P3[e] = 0;
   if (tid == 0) { s_zeroed = 0; }
+  for (int d = tid; d < DP; d += 256)   // biased exponent in [1, 254]: |Vint| < 2^23, digit offsets in range
+    Fv[d] = min(max(p.vcol[((int64_t)b * a.Hkv + hk) * DP + d], 1), 254) - 149;
   __syncthreads();
-  {
-    constexpr int G = 256 / DP > 0 ? 256 / DP : 1;
-    const int d = tid % DP, grp = tid / DP;
-    int em = 1;
-    if (d < a.D && grp < G)
-      for (int j = lo + grp; j < hi; j += G) {
-        uint32_t u = In<DT>::bits(vbase + (int64_t)j * a.vs[2], d);
-        int ex = (int)((u >> 23) & 0xFFu);
-        if (ex != 0xFF) em = max(em, ex);
-      }
-    if (grp < G) atomicMax(&Ev[d], em);
-  }
-  __syncthreads();
-  for (int d = tid; d < DP; d += 256) Fv[d] = Ev[d] - 149;   // |Vint| < 2^23
 
   // ---- accumulators ----
   long long acc[RP][CP][3];
@@ -322,6 +330,7 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
       }
   };
 
+  const int64_t krow0 = ((int64_t)b * a.Hkv + hk) * a.Skv;
   auto weight_of = [&](float sc, float m, int& nfl, int& vio) -> float {
     float x = __fsub_rn(sc, m);
     if (x != x) { nfl |= ST_NONFINITE; x = neg_inf(); }
@@ -356,39 +365,18 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
 
   for (int kt = lo; kt < hi; kt += BN) {
     __syncthreads();   // previous tile fully consumed
-    // ---- K and V tiles ----
-    for (int r = warp; r < BN; r += 8) {
-      int j = kt + r;
-      convert_row_slices<DT, DP>(j < hi ? kbase + (int64_t)j * a.ks[2] : nullptr, a.D, Ks + r * LDS, BN * LDS,
-                                 &Fk[r], &kfit[r], nf, lane);
-      const T* vrow = j < hi ? vbase + (int64_t)j * a.vs[2] : nullptr;
-#pragma unroll
-      for (int tv = 0; tv < NW; tv++) {
-        int d = lane + 32 * tv;
-        uint32_t u = (vrow != nullptr && d < a.D) ? In<DT>::bits(vrow, d) : 0u;
-        bool fit = true;
-        int X = 0;
-        if (nonfinite_bits(u)) {
-          nf |= ST_NONFINITE;
-        } else {
-          Split s = split_f32(u);
-          if (s.mant) {
-            int sh = Fv[d] - s.lsb;   // >= 1
-            if (sh < 32) {
-              X = (int)(s.mant >> sh);
-              fit = (s.mant & ((1u << sh) - 1u)) == 0u;
-            } else {
-              fit = false;
-            }
-            if (!fit) X = 0;
-            if (s.neg) X = -X;
-          }
-        }
-        Vx[r * LD + d] = X;
-        uint32_t bad = __ballot_sync(0xFFFFFFFFu, !fit);
-        if (lane == 0) vmask[r * NW + tv] = bad;
-      }
+    // ---- K and V tiles: prepared rows, copied asynchronously ----
+    load_k_tile<DP>(p, krow0, kt, hi, BN, Ks, LDS, Fk, kfit, tid);
+    for (int c = tid; c < BN * (DP / 4); c += 256) {
+      const int r = c / (DP / 4), x = c % (DP / 4), j = kt + r;
+      const bool ok = j < hi;
+      cp_async16(Vx + r * LD + 4 * x, p.vint + (krow0 + (ok ? j : kt)) * DP + 4 * x, ok ? 16 : 0);
     }
+    for (int c = tid; c < BN * NW; c += 256) {
+      const int r = c / NW, j = kt + r;
+      vmask[c] = j < hi ? p.vbad[(krow0 + j) * NW + c % NW] : 0u;
+    }
+    cp_async_wait_all();
     if (tid == 0) { s_np = 0; s_nl = 0; s_nfix = 0; s_vany = 0; }
     __syncthreads();
     // ---- exact scores on the tensor cores, then weights ----
@@ -615,19 +603,19 @@ __global__ void __launch_bounds__(256, 1) accumulate_kernel(const AttnArgs a) {
 // launchers
 // ---------------------------------------------------------------------------------------
 template <int DT, int DP>
-static cudaError_t launch_rowmax_t(const AttnArgs& a, cudaStream_t st) {
+static cudaError_t launch_rowmax_t(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
   using L = RowmaxLayout<DP>;
   const size_t smem = L::bytes;
   cudaError_t e = cudaFuncSetAttribute(rowmax_kernel<DT, DP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int nt = (a.Sq + L::BM - 1) / L::BM;
   dim3 grid(a.causal ? (nt + 1) / 2 : nt, a.Hq, a.B);
-  rowmax_kernel<DT, DP><<<grid, 256, smem, st>>>(a);
+  rowmax_kernel<DT, DP><<<grid, 256, smem, st>>>(a, p);
   return cudaGetLastError();
 }
 
 template <int DT, int DP>
-static cudaError_t launch_accumulate_t(const AttnArgs& a, cudaStream_t st) {
+static cudaError_t launch_accumulate_t(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
   using L = AccLayout<DP>;
   const size_t smem = L::bytes;
   cudaError_t e =
@@ -635,34 +623,34 @@ static cudaError_t launch_accumulate_t(const AttnArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int nt = (a.Sq + L::BM - 1) / L::BM;
   dim3 grid(a.causal ? (nt + 1) / 2 : nt, a.Hq, a.B);
-  accumulate_kernel<DT, DP><<<grid, 256, smem, st>>>(a);
+  accumulate_kernel<DT, DP><<<grid, 256, smem, st>>>(a, p);
   return cudaGetLastError();
 }
 
 static int padded_d(int D) { return D <= 64 ? 64 : (D <= 128 ? 128 : 256); }
 
-cudaError_t launch_rowmax(const AttnArgs& a, cudaStream_t st) {
+cudaError_t launch_rowmax(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
   const int dp = padded_d(a.D);
   if (a.dtype == 0) {
-    if (dp == 64) return launch_rowmax_t<0, 64>(a, st);
-    if (dp == 128) return launch_rowmax_t<0, 128>(a, st);
-    return launch_rowmax_t<0, 256>(a, st);
+    if (dp == 64) return launch_rowmax_t<0, 64>(a, p, st);
+    if (dp == 128) return launch_rowmax_t<0, 128>(a, p, st);
+    return launch_rowmax_t<0, 256>(a, p, st);
   }
-  if (dp == 64) return launch_rowmax_t<1, 64>(a, st);
-  if (dp == 128) return launch_rowmax_t<1, 128>(a, st);
-  return launch_rowmax_t<1, 256>(a, st);
+  if (dp == 64) return launch_rowmax_t<1, 64>(a, p, st);
+  if (dp == 128) return launch_rowmax_t<1, 128>(a, p, st);
+  return launch_rowmax_t<1, 256>(a, p, st);
 }
 
-cudaError_t launch_accumulate(const AttnArgs& a, cudaStream_t st) {
+cudaError_t launch_accumulate(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
   const int dp = padded_d(a.D);
   if (a.dtype == 0) {
-    if (dp == 64) return launch_accumulate_t<0, 64>(a, st);
-    if (dp == 128) return launch_accumulate_t<0, 128>(a, st);
-    return launch_accumulate_t<0, 256>(a, st);
+    if (dp == 64) return launch_accumulate_t<0, 64>(a, p, st);
+    if (dp == 128) return launch_accumulate_t<0, 128>(a, p, st);
+    return launch_accumulate_t<0, 256>(a, p, st);
   }
-  if (dp == 64) return launch_accumulate_t<1, 64>(a, st);
-  if (dp == 128) return launch_accumulate_t<1, 128>(a, st);
-  return launch_accumulate_t<1, 256>(a, st);
+  if (dp == 64) return launch_accumulate_t<1, 64>(a, p, st);
+  if (dp == 128) return launch_accumulate_t<1, 128>(a, p, st);
+  return launch_accumulate_t<1, 256>(a, p, st);
 }
 
 int accumulate_rows_per_cta(int D) {

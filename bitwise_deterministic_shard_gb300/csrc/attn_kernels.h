@@ -23,8 +23,23 @@ struct AttnArgs {
   int* status;                   // device status word (may be null)
 };
 
-cudaError_t launch_rowmax(const AttnArgs& a, cudaStream_t st);
-cudaError_t launch_accumulate(const AttnArgs& a, cudaStream_t st);
+// Prepared keys/values of one call's key range (prep_kernels.cu), rows indexed as
+// (b * Hkv + hk) * Skv + j.
+struct KvPrep {
+  uint16_t* ksl;     // bf16 digit slices [rows][4][DP]
+  int* kmeta;        // [rows]: (F + 1024) | (fit << 16)
+  int* vcol;         // [B * Hkv][DP] largest V biased exponent per column over the range
+  int* vint;         // [rows][DP] V fixed point, |Vint| < 2^23
+  uint32_t* vbad;    // [rows][DP / 32] elements outside the V window
+  int DP;
+  int do_v;
+};
+size_t kv_prep_bytes(int B, int Hkv, int Skv, int D);
+KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v);
+cudaError_t launch_kv_prep(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
+
+cudaError_t launch_rowmax(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
+cudaError_t launch_accumulate(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
 int accumulate_rows_per_cta(int D);
 
 cudaError_t launch_compose_max(float* dst, const float* src, int64_t n, cudaStream_t st);

@@ -368,6 +368,15 @@ __device__ __forceinline__ void mad_wide(long long& acc, int a, int b) {
   asm("mad.wide.s32 %0, %1, %2, %0;" : "+l"(acc) : "r"(a), "r"(b));
 }
 
+// 16-byte asynchronous global -> shared copy (zero-filled when src_bytes == 0)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sa), "l"(gmem), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // order-preserving int key of a binary32 (not NaN): key(a) < key(b) iff a < b, with -0 < +0
 __device__ __forceinline__ int float_key(float f) {
   const int b = __float_as_int(f);

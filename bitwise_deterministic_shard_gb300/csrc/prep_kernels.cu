@@ -1,0 +1,136 @@
+// Key/value preparation for sm_103a: every K row of a call's key range becomes the four
+// bf16 digit slices of its 26-bit fixed point (score_tc.cuh) plus its window exponent and
+// fit flag; every V row becomes int32 fixed point against its column's largest exponent
+// over the range (|Vint| < 2^23) plus a bit mask of the elements that do not fit.  Done
+// once per call (O(S D) work), so the attention kernels copy ready tiles with cp.async
+// instead of converting each tile once per block of query rows.
+#include "numerics.cuh"
+#include "score_tc.cuh"
+#include "attn_kernels.h"
+
+namespace detattn {
+
+// column maxima of the V biased exponents over rows [lo, hi), atomically into vcol (zeroed)
+template <int DT>
+__global__ void __launch_bounds__(256) prep_vcol_kernel(const AttnArgs a, KvPrep p) {
+  using T = typename In<DT>::T;
+  const int hk = blockIdx.y, b = blockIdx.z;
+  const T* vbase = (const T*)a.v + b * a.vs[0] + hk * a.vs[1];
+  int* vcol = p.vcol + ((int64_t)b * a.Hkv + hk) * p.DP;
+  const int rows_per_block = 256;
+  const int j0 = a.kv_lo + blockIdx.x * rows_per_block, j1 = min(a.kv_hi, j0 + rows_per_block);
+  for (int d = threadIdx.x % 64; d < a.D; d += 64) {
+    int em = 0;
+    for (int j = j0 + threadIdx.x / 64; j < j1; j += 4) {
+      const uint32_t u = In<DT>::bits(vbase + (int64_t)j * a.vs[2], d);
+      const int ex = (int)((u >> 23) & 0xFFu);
+      if (ex != 0xFF) em = max(em, ex);
+    }
+    if (em) atomicMax(&vcol[d], em);
+  }
+}
+
+// one warp per key row: K slices + meta, and (if p.do_v) V fixed point + spill bits
+template <int DT, int DP>
+__global__ void __launch_bounds__(256) prep_kv_kernel(const AttnArgs a, KvPrep p) {
+  using T = typename In<DT>::T;
+  constexpr int NW = DP / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int hk = blockIdx.y, b = blockIdx.z;
+  const int j = a.kv_lo + blockIdx.x * 8 + warp;
+  if (j >= a.kv_hi) return;
+  const int64_t row = ((int64_t)b * a.Hkv + hk) * a.Skv + j;
+  int nf = 0;
+  {
+    const T* krow = (const T*)a.k + b * a.ks[0] + hk * a.ks[1] + (int64_t)j * a.ks[2];
+    __shared__ int Fk_s[8];
+    __shared__ unsigned char fit_s[8];
+    convert_row_slices<DT, DP>(krow, a.D, p.ksl + row * NSLICE * DP, DP, &Fk_s[warp], &fit_s[warp], nf, lane);
+    __syncwarp();
+    if (lane == 0) p.kmeta[row] = (Fk_s[warp] + 1024) | ((int)fit_s[warp] << 16);
+  }
+  if (p.do_v) {
+    const T* vrow = (const T*)a.v + b * a.vs[0] + hk * a.vs[1] + (int64_t)j * a.vs[2];
+    const int* vcol = p.vcol + ((int64_t)b * a.Hkv + hk) * DP;
+#pragma unroll
+    for (int tv = 0; tv < NW; tv++) {
+      const int d = lane + 32 * tv;
+      const uint32_t u = d < a.D ? In<DT>::bits(vrow, d) : 0u;
+      bool fit = true;
+      int X = 0;
+      if (nonfinite_bits(u)) {
+        nf |= ST_NONFINITE;
+      } else {
+        const Split s = split_f32(u);
+        if (s.mant) {
+          const int sh = (min(max(vcol[d], 1), 254) - 149) - s.lsb;   // >= 1
+          if (sh < 32) {
+            X = (int)(s.mant >> sh);
+            fit = (s.mant & ((1u << sh) - 1u)) == 0u;
+          } else {
+            fit = false;
+          }
+          if (!fit) X = 0;
+          if (s.neg) X = -X;
+        }
+      }
+      p.vint[row * DP + d] = X;
+      const uint32_t bad = __ballot_sync(0xFFFFFFFFu, !fit);
+      if (lane == 0) p.vbad[row * NW + tv] = bad;
+    }
+  }
+  report(a.status, nf);
+}
+
+size_t kv_prep_bytes(int B, int Hkv, int Skv, int D) {
+  const int dp = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
+  const size_t rows = (size_t)B * Hkv * Skv;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  return up(rows * NSLICE * dp * 2) + up(rows * 4) + up((size_t)B * Hkv * dp * 4) + up(rows * dp * 4) +
+         up(rows * (dp / 32) * 4);
+}
+
+KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v) {
+  const int dp = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
+  const size_t rows = (size_t)B * Hkv * Skv;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  char* c = (char*)ws;
+  KvPrep p;
+  p.DP = dp;
+  p.do_v = do_v;
+  p.ksl = (uint16_t*)c;
+  c += up(rows * NSLICE * dp * 2);
+  p.kmeta = (int*)c;
+  c += up(rows * 4);
+  p.vcol = (int*)c;
+  c += up((size_t)B * Hkv * dp * 4);
+  p.vint = (int*)c;
+  c += up(rows * dp * 4);
+  p.vbad = (uint32_t*)c;
+  return p;
+}
+
+template <int DT, int DP>
+static cudaError_t launch_prep_t(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
+  const int n = a.kv_hi - a.kv_lo;
+  if (p.do_v) {   // the column exponents are read even when the range is empty
+    cudaError_t e = cudaMemsetAsync(p.vcol, 0, sizeof(int) * (size_t)a.B * a.Hkv * DP, st);
+    if (e != cudaSuccess) return e;
+    if (n > 0) prep_vcol_kernel<DT><<<dim3((n + 255) / 256, a.Hkv, a.B), 256, 0, st>>>(a, p);
+  }
+  if (n > 0) prep_kv_kernel<DT, DP><<<dim3((n + 7) / 8, a.Hkv, a.B), 256, 0, st>>>(a, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_prep(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
+  if (a.dtype == 0) {
+    if (p.DP == 64) return launch_prep_t<0, 64>(a, p, st);
+    if (p.DP == 128) return launch_prep_t<0, 128>(a, p, st);
+    return launch_prep_t<0, 256>(a, p, st);
+  }
+  if (p.DP == 64) return launch_prep_t<1, 64>(a, p, st);
+  if (p.DP == 128) return launch_prep_t<1, 128>(a, p, st);
+  return launch_prep_t<1, 256>(a, p, st);
+}
+
+}  // namespace detattn

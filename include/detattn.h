@@ -104,19 +104,27 @@ int da_abi_version(void);
 /* Static text for a DA_* return code. */
 const char* da_status_string(int code);
 
+/* Bytes of the key/value workspace da_rowmax and da_accumulate need: each call first
+ * rewrites the keys (and values) of its range [kv_lo, kv_hi) there in the form its
+ * kernels read (fixed-point digit slices), once per call rather than once per block of
+ * query rows.  Device memory, 256-byte aligned, caller-owned; contents need no
+ * initialization and are not meaningful after the call. */
+size_t da_kv_workspace_bytes(const da_attn_desc* desc);
+
 /* det-attn "API", rowmax: m[b,h,i] = max over keys j in [kv_lo, kv_hi) (causal: j <= i)
  * of s_ij.  m: device f32 [B, Hq, Sq], contiguous.  Rows with no valid key get -inf.
- * Shards combine with da_compose_max. */
-int da_rowmax(const da_attn_desc* desc, int64_t kv_lo, int64_t kv_hi, float* m, da_stream_t stream);
+ * Shards combine with da_compose_max.  ws: at least da_kv_workspace_bytes(desc). */
+int da_rowmax(const da_attn_desc* desc, int64_t kv_lo, int64_t kv_hi, float* m, void* ws, size_t ws_bytes,
+              da_stream_t stream);
 
 /* det-attn "API", accumulate: exact NUM/DEN digits over keys [kv_lo, kv_hi) with the
  * GLOBAL rowmax m (device f32 [B, Hq, Sq]).  num: device int64 [B, Hq, Sq, 15, D];
  * den: device int64 [B, Hq, Sq, 6], both contiguous.  add_into = 0 overwrites them with
  * the canonical digits of this range; add_into = 1 adds this range's sums to the
  * (canonical or plainly added) digits already there and leaves canonical digits.  A score
- * above m sets DA_STATUS_ROWMAX_VIOLATION. */
+ * above m sets DA_STATUS_ROWMAX_VIOLATION.  ws: at least da_kv_workspace_bytes(desc). */
 int da_accumulate(const da_attn_desc* desc, const float* m, int64_t kv_lo, int64_t kv_hi, int64_t* num,
-                  int64_t* den, int add_into, da_stream_t stream);
+                  int64_t* den, int add_into, void* ws, size_t ws_bytes, da_stream_t stream);
 
 /* det-attn "Method", shard composition: dst[i] = max(dst[i], src[i]) (f32, -0 -> +0). */
 int da_compose_max(float* dst, const float* src, int64_t n, da_stream_t stream);

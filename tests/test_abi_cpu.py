@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(libpath):
 def test_host_only_calls(libpath):
     lib = ctypes.CDLL(libpath)
     lib.da_status_string.restype = ctypes.c_char_p
-    assert lib.da_abi_version() == 1
+    assert lib.da_abi_version() == 2
     assert lib.da_status_string(0) == b"ok"
     assert lib.da_status_string(5).startswith(b"workspace")
 
@@ -47,24 +47,28 @@ def test_argument_checks_reject_before_any_launch(libpath):
     """Host validation returns codes without touching a GPU (null / bad shapes)."""
     import bitwise_deterministic_shard_gb300 as da
     L = da.lib()
-    assert L.da_rowmax(None, 0, 0, None, None) == 1                        # null descriptor
+    R = lambda d, lo, hi: L.da_rowmax(d, lo, hi, None, None, 0, None)
+    assert R(None, 0, 0) == 1                                               # null descriptor
     d = da._Desc()
     for t in (d.q, d.k, d.v):
         t.ptr = 4096                                                        # never dereferenced: rejected first
         t.dtype, t.B, t.H, t.S, t.D = 1, 1, 2, 8, 300                      # D > 256
         t.stride[3] = 1
-    assert L.da_rowmax(ctypes.byref(d), 0, 8, None, None) == 2
+    assert R(ctypes.byref(d), 0, 8) == 2
     for t in (d.q, d.k, d.v):
         t.D = 64
     d.k.H = d.v.H = 3                                                       # Hq % Hkv != 0
-    assert L.da_rowmax(ctypes.byref(d), 0, 8, None, None) == 2
+    assert R(ctypes.byref(d), 0, 8) == 2
     d.k.H = d.v.H = 1
     d.v.dtype = 0                                                           # mixed dtypes
-    assert L.da_rowmax(ctypes.byref(d), 0, 8, None, None) == 3
+    assert R(ctypes.byref(d), 0, 8) == 3
     d.v.dtype = 1
     d.causal, d.k.S, d.v.S = 1, 9, 9                                        # causal needs Sq == Skv
-    assert L.da_rowmax(ctypes.byref(d), 0, 9, None, None) == 1
+    assert R(ctypes.byref(d), 0, 9) == 1
     d.causal = 0
-    assert L.da_rowmax(ctypes.byref(d), 5, 3, None, None) == 1             # kv_hi < kv_lo
+    assert R(ctypes.byref(d), 5, 3) == 1                                    # kv_hi < kv_lo
+    d.k.S = d.v.S = 8
+    assert R(ctypes.byref(d), 0, 8) == 1                                    # m is null
+    assert L.da_kv_workspace_bytes(ctypes.byref(d)) > 0
     assert L.da_det_attn_sharded(ctypes.byref(d), (ctypes.c_int64 * 2)(4, 4), 2, None, None, None, 0, None) == 1
     assert L.da_normalize(None, 4, 7, 1, None, None) == 1                  # ndig must be 15 or 6
