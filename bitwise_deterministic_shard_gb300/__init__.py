@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libdetattn.so")
 
 NUM_NDIG, DEN_NDIG = 15, 6
 NUM_E0, DEN_E0 = -320, -160
-STATUS_NONFINITE, STATUS_ROWMAX_VIOLATION, STATUS_DIGIT_HEADROOM, STATUS_BAD_TARGET = 1, 2, 4, 8
+STATUS_NONFINITE, STATUS_ROWMAX_VIOLATION, STATUS_DIGIT_HEADROOM, STATUS_BAD_TARGET, STATUS_TIMEOUT = 1, 2, 4, 8, 16
 
 
 class DetAttnError(RuntimeError):

@@ -21,6 +21,7 @@
 // deterministic.  At the end each (i, d) is converted to canonical radix-2^32 digits.
 #include "numerics.cuh"
 #include "score_tc.cuh"
+#include "tc5.cuh"
 #include "attn_kernels.h"
 
 namespace detattn {
@@ -73,18 +74,6 @@ __device__ __forceinline__ void convert_row_fixed(const typename In<DT>::T* src,
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xFF800000); }
 
-// =======================================================================================
-// K1: rowmax.  CTA = 64 query rows of one (b, h), 256 threads, 32-key tiles.  The exact
-// scores come from the tensor cores (score_tc.cuh); warp w owns query rows
-// 16 (w / 2) .. +15 and keys 16 (w % 2) .. +15 of each tile (two 16 x 8 MMA tiles).
-// =======================================================================================
-template <int DP>
-struct RowmaxLayout {
-  static constexpr int BM = 64, BN = 32, LDS = DP + 8;
-  static constexpr size_t q_bytes = sizeof(uint16_t) * NSLICE * BM * LDS;
-  static constexpr size_t bytes = q_bytes + sizeof(uint16_t) * NSLICE * BN * LDS;
-};
-
 // copy rows [kt, kt + nrow) of the prepared K slices into a smem slice tile; rows at or
 // past hi are zero-filled (their pairs are masked)
 template <int DP>
@@ -106,101 +95,284 @@ __device__ __forceinline__ void load_k_tile(const KvPrep& p, int64_t rowbase, in
   }
 }
 
+// =======================================================================================
+// K1: rowmax on the tensor cores (tcgen05).
+//
+// The exact scores of a 128-key x 32-row block come from S^T = K Q^T on the 5th-generation
+// tensor cores.  Per step of 16 dimensions, four MMAs of M = 128 keys x N = 128 x K = 16:
+// A = key slice sa (the keys' bf16 digit slice sa, streamed from the prepared operand tiles
+// by bulk copies into an 8-stage shared-memory ring), B = all four query slices stacked
+// along N (row n = 32 sb + query row, resident), D_sa in TMEM (128 f32 columns each).  So
+// D_sa[key][32 sb + row] = sum_d K_sa[key][d] Q_sb[row][d], an integer below 2^21; the seven
+// diagonal sums A_c = sum_{sa+sb=c} D_sa[32 sb + row] are formed exactly in f32 by the
+// epilogue (integers below 2^23), and the exact dot is sum_c 2^(7c) A_c.
+//
+// Roles (one CTA per SM): warp 16 lane 0 issues the bulk copies; warps 17 and 18 (lane 0)
+// issue the MMAs of alternate steps (a tcgen05.commit holds its thread until that thread's
+// MMAs are done, so the other issuer keeps the tensor pipe fed meanwhile).  Every MMA
+// accumulates: warps 0-15 read TMEM (warp w: keys 32 (w % 4) .. +31 as its lanes, query rows
+// 8 (w / 4) .. +7), zero what they read, release it, then score.
+//
+// Certified filter.  The diagonal sums are exact integers in f32, so T~ = Horner(A_c) in f32
+// and B~ = Horner(|A_c|) bound the exact dot T: |T~ - T| <= 2^-21.3 B~, hence
+// U = T~ + 2^-19 B~ (one fma) satisfies U >= T >= L = T~ - 2^-19 B~.  Both roundings of the
+// score (to f32, then times scale) are monotone, so RN32(scale * U 2^E) bounds the exact score
+// from above.  A pair whose bound does not exceed the row's running maximum (an exact score
+// already found for that row, shared in shared memory after every key tile) cannot change
+// the row maximum and skips the exact rounding;
+// all others take the exact path (int64 dot, cr32_scaled).  A pair outside the 26-bit
+// window is computed by its warp with the exact two-limb warp dot.  Every mbarrier wait is
+// bounded; a wait that gives up sets DA_STATUS_TIMEOUT and the CTA winds down, freeing its
+// TMEM.
+// =======================================================================================
+template <int DP>
+struct RowmaxTcLayout {
+  static constexpr int BM = 32, NDS = DP / 16, NST = 8, TCOLS = 512, NEPI = 16, NISS = 2;
+  static constexpr int LOADER = NEPI, ISS0 = NEPI + 1;
+  static constexpr int THREADS = 32 * (NEPI + 1 + NISS);
+  static_assert(NDS % NISS == 0, "issuers split the steps of a tile evenly");
+  static constexpr size_t q_step = (size_t)NSLICE * BM * 32;   // one B block: 4 slices x BM rows x 16 bf16
+  static constexpr size_t q_bytes = (size_t)NDS * q_step;
+  static constexpr size_t k_off = q_bytes;
+  static constexpr size_t bytes = k_off + (size_t)NST * KT_BLOCK;
+  static_assert(NSLICE * NSLICE * BM <= TCOLS, "TMEM columns");
+  static_assert(bytes <= 227 * 1024, "shared memory budget");
+};
+
+// exact int64 dot sum_c 2^(7c) A_c from the 7 diagonal sums (f32 integers, |A_c| <= 2^22);
+// the conversions' common offset is folded into one constant (arithmetic mod 2^64)
+__device__ __forceinline__ long long combine7(const float (&v)[NDIAG][8], int r) {
+  int raw[NDIAG];
+#pragma unroll
+  for (int c = 0; c < NDIAG; c++) raw[c] = __float_as_int(__fadd_rn(v[c][r], 12582912.0f));
+  const int hi = (raw[5] - 0x4B400000) + (raw[6] - 0x4B400000) * 128;   // |hi| < 2^29
+  long long acc = (long long)((unsigned long long)(long long)hi << 35);
+#pragma unroll
+  for (int c = 0; c < 5; c++) mad_wide(acc, raw[c], 1 << (7 * c));
+  return (long long)((unsigned long long)acc - 0x4B400000ull * 0x10204081ull);
+}
+
+// true when the score RN32(scale * RN32(T 2^E)) cannot exceed `bound` and is finite
+__device__ __forceinline__ bool score_below(const float (&v)[NDIAG][8], int r, int E, float scale, float bound) {
+  if (E < -126 || E > 127) return false;
+  float t = v[NDIAG - 1][r], m = fabsf(v[NDIAG - 1][r]);
+#pragma unroll
+  for (int c = NDIAG - 2; c >= 0; c--) {
+    t = fmaf(t, 128.0f, v[c][r]);
+    m = fmaf(m, 128.0f, fabsf(v[c][r]));
+  }
+  const float p2 = __int_as_float((E + 127) << 23);
+  const float s1 = __fmul_rn(__fmul_rn(fmaf(m, 0x1p-19f, t), p2), scale);
+  const float s2 = __fmul_rn(__fmul_rn(fmaf(m, -0x1p-19f, t), p2), scale);
+  return fmaxf(s1, s2) <= bound && fminf(s1, s2) >= -3.4028235e38f;
+}
+
 template <int DT, int DP>
-__global__ void __launch_bounds__(256) rowmax_kernel(const AttnArgs a, const KvPrep p) {
+__global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kernel(const AttnArgs a, const KvPrep p) {
   using T = typename In<DT>::T;
-  using L = RowmaxLayout<DP>;
-  constexpr int BM = L::BM, BN = L::BN, LDS = L::LDS;
-  extern __shared__ __align__(16) unsigned char smem_r[];
-  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem_r);
-  uint16_t* Ks = reinterpret_cast<uint16_t*>(smem_r + L::q_bytes);
-  __shared__ int Fq[BM], Fk[BN];
-  __shared__ unsigned char qfit[BM], kfit[BN];
-  __shared__ float wmax[8][2][8];
-  __shared__ uint16_t flist[BM * BN];   // pairs outside the fixed-point window, this tile
-  __shared__ int fkey[BM];              // their row max, as order-preserving int keys
-  __shared__ int s_nfix;
+  using L = RowmaxTcLayout<DP>;
+  constexpr int BM = L::BM, NDS = L::NDS, NST = L::NST, NEPI = L::NEPI, NISS = L::NISS;
+  constexpr int NQ = NSLICE * BM;   // MMA N: the stacked query slices
+  constexpr uint32_t IDESC = tc5::idesc_bf16(KTILE, NQ);
+  extern __shared__ __align__(1024) unsigned char smem_t[];
+  unsigned char* Qs = smem_t;
+  unsigned char* Kst = smem_t + L::k_off;
+  __shared__ __align__(8) uint64_t full[NST], empty[NST], tfull, tempty, fin;
+  __shared__ uint32_t tmem_s;
+  __shared__ int Fq[BM], rkey[BM];
+  __shared__ unsigned char qfit[BM];
+  __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, t = lane & 3;
   const int h = blockIdx.y, b = blockIdx.z, hk = h / (a.Hq / a.Hkv);
   const T* qbase = (const T*)a.q + b * a.qs[0] + h * a.qs[1];
   const T* kbase = (const T*)a.k + b * a.ks[0] + hk * a.ks[1];
-  int nf = 0;
-  // causal: CTA x takes query tiles x and T-1-x, so every CTA sees about the same keys
-  const int ntiles = (a.Sq + BM - 1) / BM;
-  const int npass = (a.causal && blockIdx.x != ntiles - 1 - blockIdx.x) ? 2 : 1;
-  for (int pass = 0; pass < npass; pass++) {
-  const int q0 = (pass == 0 ? ntiles - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
-  if (pass) __syncthreads();
-
-  for (int r = warp; r < BM; r += 8) {
-    int i = q0 + r;
-    convert_row_slices<DT, DP>(i < a.Sq ? qbase + (int64_t)i * a.qs[2] : nullptr, a.D, Qs + r * LDS, BM * LDS, &Fq[r],
-                               &qfit[r], nf, lane);
-  }
-  for (int r = tid; r < BM; r += 256) fkey[r] = float_key(neg_inf());
-  int lo = a.kv_lo, hi = a.kv_hi;
-  if (a.causal) hi = min(hi, q0 + BM);
-  const int r0 = 16 * (warp >> 1), nb = 16 * (warp & 1);
-  float rmax[2] = {neg_inf(), neg_inf()};   // rows r0 + g, r0 + g + 8
-
   const int64_t krow0 = ((int64_t)b * a.Hkv + hk) * a.Skv;
-  for (int kt = lo; kt < hi; kt += BN) {
-    __syncthreads();
-    if (tid == 0) s_nfix = 0;
-    load_k_tile<DP>(p, krow0, kt, hi, BN, Ks, LDS, Fk, kfit, tid);
-    cp_async_wait_all();
-    __syncthreads();
+  const unsigned char* ktc = p.ktc + (int64_t)(b * a.Hkv + hk) * p.ntk * NDS * KT_BLOCK;
+
+  if (warp == 0) tc5::tmem_alloc(&tmem_s, L::TCOLS);
+  if (tid == 0) {
+    for (int s = 0; s < NST; s++) {
+      tc5::mbar_init(&full[s], 1);
+      tc5::mbar_init(&empty[s], 1);
+    }
+    tc5::mbar_init(&tfull, NISS);
+    tc5::mbar_init(&tempty, NEPI);
+    tc5::mbar_init(&fin, NISS);
+    s_abort = 0;
+    tc5::mbar_fence_init();
+  }
+  tc5::fence_before();
+  __syncthreads();
+  tc5::fence_after();
+  const uint32_t tmem = tmem_s;
+  // every MMA accumulates: the epilogue warps keep their TMEM region zero between key tiles
+  const uint32_t lbase = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (warp >> 2) * 8;
+  if (warp < NEPI) {
 #pragma unroll
-    for (int nt = 0; nt < 2; nt++) {
-      const int n0 = nb + 8 * nt;
-      float acc[NDIAG][4];
-      score_tile_mma<DP>(acc, Qs, BM * LDS, Ks, BN * LDS, LDS, r0, n0, g, t);
+    for (int g = 0; g < NSLICE * NSLICE; g++) tc5::st_zero_x8(lbase + g * BM);
+    tc5::st_wait();
+  }
+  tc5::fence_before();
+  __syncthreads();
+  tc5::fence_after();
+
+  int nf = 0;
+  uint32_t g_base = 0, tcount = 0;   // ring steps of earlier passes; key tiles seen by this thread's role
+  const int ntq = (a.Sq + BM - 1) / BM;
+  const int npass = (a.causal && (int)blockIdx.x != ntq - 1 - (int)blockIdx.x) ? 2 : 1;
+  for (int pass = 0; pass < npass; pass++) {
+    const int q0 = (pass == 0 ? ntq - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
+    const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
+    const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
+    const uint32_t nsteps = (uint32_t)nkt * NDS;
+    // ---- query slices into the resident B operand ----
+    for (int r = warp; r < BM; r += L::THREADS / 32) {
+      const int i = q0 + r;
+      row_slices<DT, DP>(
+          i < a.Sq ? qbase + (int64_t)i * a.qs[2] : nullptr, a.D,
+          [&](int q, int d, uint16_t v) {
+            *reinterpret_cast<uint16_t*>(Qs + (d >> 4) * L::q_step + tc5::canon_off(q * BM + r, d & 15)) = v;
+          },
+          &Fq[r], &qfit[r], nf, lane);
+    }
+    for (int r = tid; r < BM; r += L::THREADS) rkey[r] = float_key(neg_inf());
+    tc5::fence_async_smem();
+    __syncthreads();
+
+    if (warp == L::LOADER) {   // ---------------- bulk copies of the key operand tiles ----------------
+      if (lane == 0)
+        for (uint32_t ls = 0; ls < nsteps && !s_abort; ls++) {
+          const uint32_t g_step = g_base + ls, st = g_step % NST;
+          if (g_step >= NST && !tc5::mbar_wait(&empty[st], ((g_step / NST) - 1) & 1, &s_abort, 64)) break;
+          tc5::mbar_expect_tx(&full[st], KT_BLOCK);
+          tc5::bulk_g2s(Kst + st * KT_BLOCK, ktc + (size_t)ls * KT_BLOCK, KT_BLOCK, &full[st]);
+        }
+    } else if (warp >= L::ISS0) {   // ---------------- MMA issuers: steps ii, ii + NISS, ... ----------------
+      if (lane == 0) {
+        const uint32_t ii = warp - L::ISS0;
+        for (uint32_t ls = ii; ls < nsteps && !s_abort; ls += NISS) {
+          const uint32_t g_step = g_base + ls, st = g_step % NST;
+          const int k = (int)(ls % NDS);
+          if (!tc5::mbar_wait(&full[st], (g_step / NST) & 1, &s_abort)) break;
+          if (k == (int)ii && tcount >= 1 && !tc5::mbar_wait(&tempty, (tcount - 1) & 1, &s_abort)) break;
+          tc5::fence_after();
+          const uint64_t ka = tc5::desc(tc5::smem_addr(Kst + st * KT_BLOCK));
+          const uint64_t qa = tc5::desc(tc5::smem_addr(Qs + k * L::q_step));
 #pragma unroll
-      for (int e = 0; e < 4; e++) {
-        const int rl = r0 + g + 8 * (e >> 1), cl = n0 + 2 * t + (e & 1);
-        const int i = q0 + rl, j = kt + cl;
-        if (i < a.Sq && j < hi && (!a.causal || j <= i)) {
-          if (qfit[rl] && kfit[cl]) {
-            float sc = __fmul_rn(a.scale32, cr32_scaled(combine_diag(acc, e), Fq[rl] + Fk[cl]));
-            if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
-            if (sc > rmax[e >> 1]) rmax[e >> 1] = sc;
-          } else {
-            flist[atomicAdd(&s_nfix, 1)] = (uint16_t)(cl * BM + rl);   // a row outside the window
+          for (int sa = 0; sa < NSLICE; sa++)   // descriptor start addresses advance in 16-byte units
+            tc5::mma_bf16(tmem + sa * NQ, ka + (uint64_t)(sa * KTILE * 2), qa, IDESC, 1u);
+          tc5::commit(&empty[st]);
+          if (k + NISS >= NDS) {   // this issuer's last step of the tile
+            tc5::commit(&tfull);
+            tcount++;
           }
         }
       }
-    }
-    __syncthreads();
-    for (int fe = warp; fe < s_nfix; fe += 8) {   // one warp per deferred pair
-      const int cl = flist[fe] / BM, rl = flist[fe] % BM;
-      float sc = __fmul_rn(a.scale32, exact_dot_warp<DT>(qbase + (int64_t)(q0 + rl) * a.qs[2],
-                                                        kbase + (int64_t)(kt + cl) * a.ks[2], a.D, lane));
-      if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
-      if (lane == 0 && sc == sc) atomicMax(&fkey[rl], float_key(sc));
-    }
-  }
+    } else {   // ---------------- epilogue: thread = key, 8 query rows ----------------
+      const int quarter = warp & 3, rg = warp >> 2;
+      const int jl = 32 * quarter + lane;
+      float mrun[8];
 #pragma unroll
-  for (int hh = 0; hh < 2; hh++) {
-    float v = rmax[hh];
-    v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
-    v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
-    if (t == 0) wmax[warp][hh][g] = v;
-  }
-  __syncthreads();
-  if (tid < BM) {
-    const int rl = tid, mw = 2 * (rl / 16), hh = (rl % 16) / 8, gg = rl % 8;
-    const float v0 = wmax[mw][hh][gg], v1 = wmax[mw + 1][hh][gg], v2 = key_float(fkey[rl]);
-    float v = v1 > v0 ? v1 : v0;
-    v = v2 > v ? v2 : v;
-    const int i = q0 + rl;
-    if (i < a.Sq) {
-      if (v == 0.0f) v = __int_as_float(0);   // -0 -> +0
-      a.m_out[((int64_t)b * a.Hq + h) * a.Sq + i] = v;
+      for (int r = 0; r < 8; r++) mrun[r] = neg_inf();
+      for (int t = 0; t < nkt; t++) {
+        const int j = a.kv_lo + t * KTILE + jl;
+        const bool vj = j < hi;
+        const int mv = vj ? p.kmeta[krow0 + j] : 0;
+        if (!tc5::mbar_wait(&tfull, tcount & 1, &s_abort, 128)) break;
+        tc5::fence_after();
+        float v[NDIAG][8];   // diagonal sums of this thread's 8 rows, exact
+#pragma unroll
+        for (int rr = 0; rr < 8; rr += 4) {
+          float d[NSLICE][NSLICE][4];
+#pragma unroll
+          for (int sa = 0; sa < NSLICE; sa++)
+#pragma unroll
+            for (int sb = 0; sb < NSLICE; sb++) tc5::ld_x4(lbase + sa * NQ + sb * BM + rr, d[sa][sb]);
+          tc5::ld_wait();
+#pragma unroll
+          for (int e = 0; e < 4; e++)
+#pragma unroll
+            for (int c = 0; c < NDIAG; c++) {
+              float acc = 0.0f;
+#pragma unroll
+              for (int sa = 0; sa < NSLICE; sa++)
+                if (c - sa >= 0 && c - sa < NSLICE) acc = __fadd_rn(acc, d[sa][c - sa][e]);
+              v[c][rr + e] = acc;
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < NSLICE * NSLICE; g++) tc5::st_zero_x8(lbase + g * BM);
+        tc5::st_wait();
+        tc5::fence_before();
+        __syncwarp();
+        if (lane == 0) tc5::mbar_arrive(&tempty);
+        tcount++;
+        float thr[8];   // the rows' running maxima so far (exact scores)
+#pragma unroll
+        for (int r = 0; r < 8; r++) thr[r] = fmaxf(mrun[r], key_float(rkey[rg * 8 + r]));
+        const int Fk = (mv & 0xFFFF) - 1024, kf = mv >> 16;
+        uint32_t defer = 0;   // rows whose pair with this key needs the exact fallback
+#pragma unroll
+        for (int r = 0; r < 8; r++) {
+          const int rl = rg * 8 + r, i = q0 + rl;
+          if (vj && i < a.Sq && (!a.causal || j <= i)) {
+            if (qfit[rl] && kf) {
+              const int E = Fq[rl] + Fk;
+              if (!score_below(v, r, E, a.scale32, thr[r])) {
+                const float sc = __fmul_rn(a.scale32, cr32_scaled(combine7(v, r), E));
+                if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
+                mrun[r] = sc > mrun[r] ? sc : mrun[r];
+              }
+            } else {
+              defer |= 1u << rl;
+            }
+          }
+        }
+        // deferred pairs of this warp, one at a time with the whole warp
+        for (uint32_t pend = __ballot_sync(0xFFFFFFFFu, defer != 0); pend; pend = __ballot_sync(0xFFFFFFFFu, defer != 0)) {
+          const int src = __ffs(pend) - 1;
+          const uint32_t dm = __shfl_sync(0xFFFFFFFFu, defer, src);
+          const int rl = __ffs(dm) - 1;
+          const int jj = a.kv_lo + t * KTILE + 32 * quarter + src;
+          const float sc = __fmul_rn(a.scale32, exact_dot_warp<DT>(qbase + (int64_t)(q0 + rl) * a.qs[2],
+                                                                  kbase + (int64_t)jj * a.ks[2], a.D, lane));
+          if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
+          if (lane == 0 && sc == sc) atomicMax(&rkey[rl], float_key(sc));
+          if (lane == src) defer &= defer - 1;
+        }
+#pragma unroll
+        for (int r = 0; r < 8; r++) {   // publish this tile's maxima
+          const int km = __reduce_max_sync(0xFFFFFFFFu, float_key(mrun[r]));
+          if (lane == 0 && key_float(km) > thr[r]) atomicMax(&rkey[rg * 8 + r], km);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 8; r++) {
+        const int kmax = __reduce_max_sync(0xFFFFFFFFu, float_key(mrun[r]));
+        if (lane == 0) atomicMax(&rkey[rg * 8 + r], kmax);
+      }
     }
-  }
+    g_base += nsteps;
+    __syncthreads();
+    if (tid < BM) {
+      const int i = q0 + tid;
+      float v = key_float(rkey[tid]);
+      if (i < a.Sq) {
+        if (v == 0.0f) v = __int_as_float(0);   // -0 -> +0
+        a.m_out[((int64_t)b * a.Hq + h) * a.Sq + i] = v;
+      }
+    }
   }   // pass
+  if (warp >= L::ISS0 && lane == 0) {   // every MMA issued has completed before TMEM is released
+    tc5::commit(&fin);
+    tc5::mbar_wait(&fin, 0, &s_abort);
+  }
+  tc5::fence_before();
+  __syncthreads();
+  tc5::fence_after();
+  if (warp == 0) tc5::tmem_dealloc(tmem, L::TCOLS);
+  if (s_abort) nf |= ST_TIMEOUT;
   report(a.status, nf);
 }
 
@@ -604,13 +776,13 @@ __global__ void __launch_bounds__(256, AccCfg<DP>::MINB) accumulate_kernel(const
 // ---------------------------------------------------------------------------------------
 template <int DT, int DP>
 static cudaError_t launch_rowmax_t(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
-  using L = RowmaxLayout<DP>;
+  using L = RowmaxTcLayout<DP>;
   const size_t smem = L::bytes;
-  cudaError_t e = cudaFuncSetAttribute(rowmax_kernel<DT, DP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(rowmax_tc_kernel<DT, DP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int nt = (a.Sq + L::BM - 1) / L::BM;
   dim3 grid(a.causal ? (nt + 1) / 2 : nt, a.Hq, a.B);
-  rowmax_kernel<DT, DP><<<grid, 256, smem, st>>>(a, p);
+  rowmax_tc_kernel<DT, DP><<<grid, L::THREADS, smem, st>>>(a, p);
   return cudaGetLastError();
 }
 

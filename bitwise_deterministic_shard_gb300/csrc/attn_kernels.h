@@ -27,6 +27,8 @@ struct AttnArgs {
 // (b * Hkv + hk) * Skv + j.
 struct KvPrep {
   uint16_t* ksl;     // bf16 digit slices [rows][4][DP]
+  unsigned char* ktc;   // the same slices as tensor-core operand tiles (below)
+  int ntk;           // key tiles of KTILE rows per (b, hk) in ktc
   int* kmeta;        // [rows]: (F + 1024) | (fit << 16)
   int* vcol;         // [B * Hkv][DP] largest V biased exponent per column over the range
   int* vint;         // [rows][DP] V fixed point, |Vint| < 2^23
@@ -34,6 +36,11 @@ struct KvPrep {
   int DP;
   int do_v;
 };
+// ktc: per (b, hk), key tiles of KTILE keys starting at the call's kv_lo; per tile, per
+// 16-wide step of d, one 16 KiB block = 4 slices x (KTILE x 16 bf16 in the canonical
+// K-major operand layout of tc5.cuh).  Rows past kv_hi are zero.
+constexpr int KTILE = 128;
+constexpr int KT_BLOCK = 4 * KTILE * 16 * 2;
 size_t kv_prep_bytes(int B, int Hkv, int Skv, int D);
 KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v);
 cudaError_t launch_kv_prep(const AttnArgs& a, const KvPrep& p, cudaStream_t st);

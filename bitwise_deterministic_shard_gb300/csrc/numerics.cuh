@@ -16,7 +16,7 @@ namespace detattn {
 
 constexpr int NUM_NDIG = 15, DEN_NDIG = 6;
 constexpr int NUM_E0 = -320, DEN_E0 = -160;
-enum : int { ST_NONFINITE = 1, ST_VIOLATION = 2, ST_HEADROOM = 4, ST_BAD_TARGET = 8 };
+enum : int { ST_NONFINITE = 1, ST_VIOLATION = 2, ST_HEADROOM = 4, ST_BAD_TARGET = 8, ST_TIMEOUT = 16 };
 
 // ---------------------------------------------------------------------------------------
 // element access: bf16 is the upper half of a binary32, so widening is exact

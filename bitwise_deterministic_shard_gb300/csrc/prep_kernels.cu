@@ -6,6 +6,7 @@
 // instead of converting each tile once per block of query rows.
 #include "numerics.cuh"
 #include "score_tc.cuh"
+#include "tc5.cuh"
 #include "attn_kernels.h"
 
 namespace detattn {
@@ -30,22 +31,37 @@ __global__ void __launch_bounds__(256) prep_vcol_kernel(const AttnArgs a, KvPrep
   }
 }
 
-// one warp per key row: K slices + meta, and (if p.do_v) V fixed point + spill bits
+// one warp per key row: K slices (both layouts) + meta, and (if p.do_v) V fixed point +
+// spill bits.  Rows in [kv_hi, end of the last key tile) only zero their operand tile rows.
 template <int DT, int DP>
 __global__ void __launch_bounds__(256) prep_kv_kernel(const AttnArgs a, KvPrep p) {
   using T = typename In<DT>::T;
-  constexpr int NW = DP / 32;
+  constexpr int NW = DP / 32, NDS = DP / 16;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int hk = blockIdx.y, b = blockIdx.z;
-  const int j = a.kv_lo + blockIdx.x * 8 + warp;
-  if (j >= a.kv_hi) return;
+  const int jr = blockIdx.x * 8 + warp, j = a.kv_lo + jr;
+  const int n = a.kv_hi - a.kv_lo;
+  if (jr >= ((n + KTILE - 1) / KTILE) * KTILE) return;
+  unsigned char* tile = p.ktc + ((int64_t)(b * a.Hkv + hk) * p.ntk + jr / KTILE) * NDS * KT_BLOCK;
+  const int rt = jr % KTILE;
+  auto store_tc = [&](int q, int d, uint16_t v) {
+    *reinterpret_cast<uint16_t*>(tile + (d >> 4) * KT_BLOCK + q * (KTILE * 32) + tc5::canon_off(rt, d & 15)) = v;
+  };
+  if (j >= a.kv_hi) {
+    for (int d = lane; d < DP; d += 32)
+#pragma unroll
+      for (int q = 0; q < NSLICE; q++) store_tc(q, d, 0);
+    return;
+  }
   const int64_t row = ((int64_t)b * a.Hkv + hk) * a.Skv + j;
   int nf = 0;
   {
     const T* krow = (const T*)a.k + b * a.ks[0] + hk * a.ks[1] + (int64_t)j * a.ks[2];
     __shared__ int Fk_s[8];
     __shared__ unsigned char fit_s[8];
-    convert_row_slices<DT, DP>(krow, a.D, p.ksl + row * NSLICE * DP, DP, &Fk_s[warp], &fit_s[warp], nf, lane);
+    uint16_t* ks = p.ksl + row * NSLICE * DP;
+    row_slices<DT, DP>(krow, a.D, [&](int q, int d, uint16_t v) { ks[q * DP + d] = v; store_tc(q, d, v); },
+                       &Fk_s[warp], &fit_s[warp], nf, lane);
     __syncwarp();
     if (lane == 0) p.kmeta[row] = (Fk_s[warp] + 1024) | ((int)fit_s[warp] << 16);
   }
@@ -82,12 +98,17 @@ __global__ void __launch_bounds__(256) prep_kv_kernel(const AttnArgs a, KvPrep p
   report(a.status, nf);
 }
 
+static size_t ktc_bytes(int B, int Hkv, int Skv, int dp) {
+  const size_t ntk = (size_t)(Skv + KTILE - 1) / KTILE;
+  return (size_t)B * Hkv * ntk * (dp / 16) * KT_BLOCK;
+}
+
 size_t kv_prep_bytes(int B, int Hkv, int Skv, int D) {
   const int dp = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
   const size_t rows = (size_t)B * Hkv * Skv;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   return up(rows * NSLICE * dp * 2) + up(rows * 4) + up((size_t)B * Hkv * dp * 4) + up(rows * dp * 4) +
-         up(rows * (dp / 32) * 4);
+         up(rows * (dp / 32) * 4) + up(ktc_bytes(B, Hkv, Skv, dp));
 }
 
 KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v) {
@@ -107,6 +128,9 @@ KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v) {
   p.vint = (int*)c;
   c += up(rows * dp * 4);
   p.vbad = (uint32_t*)c;
+  c += up(rows * (dp / 32) * 4);
+  p.ktc = (unsigned char*)c;
+  p.ntk = (Skv + KTILE - 1) / KTILE;
   return p;
 }
 
@@ -118,7 +142,8 @@ static cudaError_t launch_prep_t(const AttnArgs& a, const KvPrep& p, cudaStream_
     if (e != cudaSuccess) return e;
     if (n > 0) prep_vcol_kernel<DT><<<dim3((n + 255) / 256, a.Hkv, a.B), 256, 0, st>>>(a, p);
   }
-  if (n > 0) prep_kv_kernel<DT, DP><<<dim3((n + 7) / 8, a.Hkv, a.B), 256, 0, st>>>(a, p);
+  const int padded = ((n + KTILE - 1) / KTILE) * KTILE;
+  if (n > 0) prep_kv_kernel<DT, DP><<<dim3(padded / 8, a.Hkv, a.B), 256, 0, st>>>(a, p);
   return cudaGetLastError();
 }
 

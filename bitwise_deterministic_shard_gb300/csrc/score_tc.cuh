@@ -90,11 +90,12 @@ __device__ __forceinline__ long long combine_diag(const float (&acc)[NDIAG][4], 
   return T;
 }
 
-// Convert one row (one warp) to fixed point and store its four digit slices.
-// Returns through F_out / fit_out as convert_row_fixed does.
-template <int DT, int DP>
-__device__ __forceinline__ void convert_row_slices(const typename In<DT>::T* src, int D, uint16_t* dst, int plane,
-                                                   int* F_out, unsigned char* fit_out, int& nf, int lane) {
+// Convert one row (one warp) to fixed point and hand its four digit slices to
+// store(slice, d, bf16 bits) for d in [0, DP) (zeros past D).  F_out / fit_out receive the
+// row's window exponent and whether every element fits the 26-bit window.
+template <int DT, int DP, class Store>
+__device__ __forceinline__ void row_slices(const typename In<DT>::T* src, int D, Store store, int* F_out,
+                                           unsigned char* fit_out, int& nf, int lane) {
   constexpr int PER = DP / 32;
   uint32_t bv[PER];
   int emax = 1;
@@ -128,13 +129,20 @@ __device__ __forceinline__ void convert_row_slices(const typename In<DT>::T* src
     uint16_t sl[NSLICE];
     slice4(X, sl);
 #pragma unroll
-    for (int q = 0; q < NSLICE; q++) dst[q * plane + lane + 32 * t] = sl[q];
+    for (int q = 0; q < NSLICE; q++) store(q, lane + 32 * t, sl[q]);
   }
   ok = __all_sync(0xFFFFFFFFu, ok);
   if (lane == 0) {
     *F_out = F;
     *fit_out = ok ? 1 : 0;
   }
+}
+
+// the same, stored as slice planes dst[q * plane + d]
+template <int DT, int DP>
+__device__ __forceinline__ void convert_row_slices(const typename In<DT>::T* src, int D, uint16_t* dst, int plane,
+                                                   int* F_out, unsigned char* fit_out, int& nf, int lane) {
+  row_slices<DT, DP>(src, D, [&](int q, int d, uint16_t v) { dst[q * plane + d] = v; }, F_out, fit_out, nf, lane);
 }
 
 }  // namespace detattn

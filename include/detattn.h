@@ -64,6 +64,7 @@ typedef struct CUstream_st* da_stream_t; /* a cudaStream_t */
 #define DA_STATUS_ROWMAX_VIOLATION 2 /* a score above the supplied rowmax (weight clamped to 1) */
 #define DA_STATUS_DIGIT_HEADROOM 4   /* a digit sum left the representable range */
 #define DA_STATUS_BAD_TARGET 8       /* a target index outside [0, V) (its loss is NaN) */
+#define DA_STATUS_TIMEOUT 16         /* a bounded wait inside a kernel gave up; outputs unspecified */
 
 /* element types */
 #define DA_F32 0

@@ -205,6 +205,33 @@ def test_c3_ring_steps_and_sampled_oracle(da, orc):
 
 
 @cuda
+def test_c4_unequal_splits_and_sampled_oracle(da, orc):
+    """Large non-causal workload at full size (B1 H56 S37810 D128 bf16; S is no tile
+    multiple): the fused call, the 32 unequal random splits composed in a random order,
+    and sampled rows (4 per head plus the last row) against the oracle."""
+    w = W.c4()
+    Q, K, V = w.tensors("cuda")
+    st = da.new_status()
+    fused = da.det_attn(Q, K, V, status=st)
+    torch.cuda.synchronize()
+    assert da.read_status(st) == 0
+    (sp, order), = w.splits
+    assert sum(sp) == w.S and len(sp) == 32
+    out = da.det_attn_sharded(Q, K, V, sp, order=order, status=st)
+    torch.cuda.synchronize()
+    assert da.read_status(st) == 0
+    assert torch.equal(out, fused)
+    del out
+    rng = random.Random(4)
+    rows = [(0, h, i) for h in range(w.Hq) for i in rng.sample(range(w.S), 4)] + [(0, w.Hq - 1, w.S - 1)]
+    fl = flat_rows(1, w.Hq, w.S, rows)
+    A = orc.Attn(Q.cpu(), K.cpu(), V.cpu(), False)
+    _, _, _, ref = A.forward_rows(rows=fl)
+    got = fused.reshape(-1, w.D)[torch.from_numpy(fl).cuda()]
+    assert_bits_equal(got, ref, "C4 sampled rows vs oracle")
+
+
+@cuda
 def test_c3_shard_digits_compose_to_fused_digits(da):
     """accumulate per shard into separate arrays + compose_add + normalize equals the
     fused digits (det-attn "Method": an int64 add of digit arrays)."""
