@@ -72,7 +72,6 @@ __device__ __forceinline__ void convert_row_fixed(const typename In<DT>::T* src,
   }
 }
 
-__device__ __forceinline__ float neg_inf() { return __int_as_float(0xFF800000); }
 
 // copy rows [kt, kt + nrow) of the prepared K slices into a smem slice tile; rows at or
 // past hi are zero-filled (their pairs are masked)
@@ -279,7 +278,7 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
         const int j = a.kv_lo + t * KTILE + jl;
         const bool vj = j < hi;
         const int mv = vj ? p.kmeta[krow0 + j] : 0;
-        if (!tc5::mbar_wait(&tfull, tcount & 1, &s_abort, 128)) break;
+        if (!__all_sync(0xFFFFFFFFu, tc5::mbar_wait(&tfull, tcount & 1, &s_abort, 128))) break;   // warp-uniform
         tc5::fence_after();
         float v[NDIAG][8];   // diagonal sums of this thread's 8 rows, exact
 #pragma unroll
@@ -815,19 +814,8 @@ cudaError_t launch_rowmax(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
 
 cudaError_t launch_accumulate(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
   const int dp = padded_d(a.D);
-  if (a.dtype == 0) {
-    if (dp == 64) return launch_accumulate_t<0, 64>(a, p, st);
-    if (dp == 128) return launch_accumulate_t<0, 128>(a, p, st);
-    return launch_accumulate_t<0, 256>(a, p, st);
-  }
-  if (dp == 64) return launch_accumulate_t<1, 64>(a, p, st);
-  if (dp == 128) return launch_accumulate_t<1, 128>(a, p, st);
-  return launch_accumulate_t<1, 256>(a, p, st);
-}
-
-int accumulate_rows_per_cta(int D) {
-  const int dp = padded_d(D);
-  return dp == 256 ? AccLayout<256>::BM : AccLayout<128>::BM;
+  if (dp <= 128) return launch_accumulate_tc(a, p, st);
+  return a.dtype == 0 ? launch_accumulate_t<0, 256>(a, p, st) : launch_accumulate_t<1, 256>(a, p, st);
 }
 
 }  // namespace detattn

@@ -47,7 +47,7 @@ cudaError_t launch_kv_prep(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
 
 cudaError_t launch_rowmax(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
 cudaError_t launch_accumulate(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
-int accumulate_rows_per_cta(int D);
+cudaError_t launch_accumulate_tc(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // D <= 128
 
 cudaError_t launch_compose_max(float* dst, const float* src, int64_t n, cudaStream_t st);
 cudaError_t launch_compose_add(long long* dst, const long long* src, int64_t n, cudaStream_t st);

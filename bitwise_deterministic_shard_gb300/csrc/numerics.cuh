@@ -46,6 +46,7 @@ __device__ __forceinline__ Split split_f32(uint32_t u) {
   return s;
 }
 __device__ __forceinline__ bool nonfinite_bits(uint32_t u) { return ((u >> 23) & 0xFFu) == 0xFFu; }
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xFF800000); }
 
 // ---------------------------------------------------------------------------------------
 // exp32_det: Cody-Waite argument reduction (Cody & Waite, "Software Manual for the
