@@ -41,14 +41,14 @@ template <int DP>
 struct AccTcLayout {
   static constexpr int BM = 32, NDS = DP / 16, NST = 2, VCH = 16, NVB = 2, NCW = 16;
   static constexpr int KLOAD = NCW, ISSUER = NCW + 1, VLOAD = NCW + 2, THREADS = 32 * (NCW + 3);
-  static constexpr int RP = 2, CP = DP / 32, NW = DP / 32, LDW = BM + 2, NCH = KTILE / VCH;
+  static constexpr int RP = 2, CP = DP / 32, NW = DP / 32, LDW = KTILE + 4, NCH = KTILE / VCH;
   static constexpr int TCOLS = 512, BUF = 256;
   static constexpr size_t q_bytes = (size_t)NDS * NSLICE * BM * 32;   // B blocks [step][slice], BM x 16 bf16
   static constexpr size_t k_off = q_bytes;                              // NST key operand stages
   static constexpr size_t v_off = k_off + (size_t)NST * KT_BLOCK;       // NVB V chunks
   static constexpr size_t v_chunk = (size_t)VCH * DP * 4;               //   int32 [VCH][DP]
-  static constexpr size_t w_off = v_off + NVB * v_chunk;                // int32 [3][KTILE][LDW] weight limbs
-  static constexpr size_t wf_off = w_off + (size_t)3 * KTILE * LDW * 4; // float [KTILE][BM] weights
+  static constexpr size_t w_off = v_off + NVB * v_chunk;                // int32 [3][BM][LDW] weight limbs
+  static constexpr size_t wf_off = w_off + (size_t)3 * BM * LDW * 4;    // float [BM][KTILE] weights
   static constexpr size_t p3_off = wf_off + (size_t)KTILE * BM * 4;     // int64 [BM][DP] carried limbs
   static constexpr size_t ps_off = p3_off + (size_t)BM * DP * 8;        // uint16 pairs below 2^-69
   static constexpr int NBAD = 1024;                                     // listed V elements outside the window
@@ -78,41 +78,49 @@ __device__ __forceinline__ long long warp_sum31(int x) {
   return (long long)lo + ((long long)hi << 16);
 }
 
-// PV of one V chunk through limbs L0 .. L0 + NLB - 1: acc[r][c][l] += W_l(key, row) * Vint(key, col)
+// PV of one V chunk through limbs L0 .. L0 + NLB - 1: acc[r][c][l] += W_l(row, key) * Vint(key, col).
+// Limb planes are [limb][row][key] (row stride LDW); two keys per step, one 64-bit load per
+// (limb, row).
 template <int L0, int NLB, int RP, int CP, int DP, int LDW, int VCH>
 __device__ __forceinline__ void pv_chunk(long long (&acc)[RP][CP][3], const int* Wl, const int* vsl, int key0, int pr,
                                          int pc) {
-#pragma unroll 2
-  for (int jj = 0; jj < VCH; jj++) {
-    const int key = key0 + jj;
-    int wv[NLB][RP], vv[CP];
+#pragma unroll 1
+  for (int jj = 0; jj < VCH; jj += 2) {
+    int wv[NLB][RP][2], vv[2][CP];
 #pragma unroll
-    for (int l = 0; l < NLB; l++) {
-      const int2 t2 = *reinterpret_cast<const int2*>(Wl + ((L0 + l) * KTILE + key) * LDW + pr * RP);
-      wv[l][0] = t2.x;
-      wv[l][1] = t2.y;
-    }
-    const int* vp = vsl + jj * DP + pc * CP;
-    if constexpr (CP == 2) {
-      const int2 t2 = *reinterpret_cast<const int2*>(vp);
-      vv[0] = t2.x;
-      vv[1] = t2.y;
-    } else {
+    for (int l = 0; l < NLB; l++)
 #pragma unroll
-      for (int c4 = 0; c4 < CP; c4 += 4) {
-        const int4 t4 = *reinterpret_cast<const int4*>(vp + c4);
-        vv[c4] = t4.x;
-        vv[c4 + 1] = t4.y;
-        vv[c4 + 2] = t4.z;
-        vv[c4 + 3] = t4.w;
+      for (int r = 0; r < RP; r++) {
+        const int2 t2 = *reinterpret_cast<const int2*>(Wl + ((L0 + l) * (RP * 16) + pr * RP + r) * LDW + key0 + jj);
+        wv[l][r][0] = t2.x;
+        wv[l][r][1] = t2.y;
+      }
+#pragma unroll
+    for (int k2 = 0; k2 < 2; k2++) {
+      const int* vp = vsl + (jj + k2) * DP + pc * CP;
+      if constexpr (CP == 2) {
+        const int2 t2 = *reinterpret_cast<const int2*>(vp);
+        vv[k2][0] = t2.x;
+        vv[k2][1] = t2.y;
+      } else {
+#pragma unroll
+        for (int c4 = 0; c4 < CP; c4 += 4) {
+          const int4 t4 = *reinterpret_cast<const int4*>(vp + c4);
+          vv[k2][c4] = t4.x;
+          vv[k2][c4 + 1] = t4.y;
+          vv[k2][c4 + 2] = t4.z;
+          vv[k2][c4 + 3] = t4.w;
+        }
       }
     }
 #pragma unroll
-    for (int r = 0; r < RP; r++)
+    for (int k2 = 0; k2 < 2; k2++)
 #pragma unroll
-      for (int c = 0; c < CP; c++)
+      for (int r = 0; r < RP; r++)
 #pragma unroll
-        for (int l = 0; l < NLB; l++) mad_wide(acc[r][c][L0 + l], wv[l][r], vv[c]);
+        for (int c = 0; c < CP; c++)
+#pragma unroll
+          for (int l = 0; l < NLB; l++) mad_wide(acc[r][c][L0 + l], wv[l][r][k2], vv[k2][c]);
   }
 }
 
@@ -288,19 +296,26 @@ __global__ void __launch_bounds__(AccTcLayout<DP>::THREADS, 1) accumulate_tc_ker
         const int ex = (int)(wb >> 23);
         int l0 = 0, l1 = 0, l2 = 0;
         if (wb != 0u) {
-          if (ex >= 58) {
-            const unsigned __int128 W = ((unsigned __int128)((wb & 0x7FFFFFu) | 0x800000u)) << (ex - 58);
-            l0 = (int)((uint64_t)W & 0x7FFFFFFFull);
-            l1 = (int)((uint64_t)(W >> 31) & 0x7FFFFFFFull);
-            l2 = (int)(uint64_t)(W >> 62);
+          if (ex >= 58) {   // W = mant << (ex - 58) < 2^93, split into 31-bit limbs with 64-bit shifts
+            const uint64_t mant = (wb & 0x7FFFFFu) | 0x800000u;
+            const int sh = ex - 58;
+            if (sh <= 38) {
+              const uint64_t W = mant << sh;   // < 2^62
+              l0 = (int)(W & 0x7FFFFFFFull);
+              l1 = (int)(W >> 31);
+            } else {
+              const uint64_t W1 = mant << (sh - 31);   // W >> 31, exact: the low 31 bits of W are zero
+              l1 = (int)(W1 & 0x7FFFFFFFull);
+              l2 = (int)(W1 >> 31);
+            }
           } else {
             plist[atomicAdd(&s_np, 1)] = (uint16_t)(cl * BM + rl);             // w < 2^-69: exact atomics
           }
         }
-        Wl[(0 * KTILE + cl) * LDW + rl] = l0;
-        Wl[(1 * KTILE + cl) * LDW + rl] = l1;
-        Wl[(2 * KTILE + cl) * LDW + rl] = l2;
-        Wf[cl * BM + rl] = w;
+        Wl[(0 * BM + rl) * LDW + cl] = l0;
+        Wl[(1 * BM + rl) * LDW + cl] = l1;
+        Wl[(2 * BM + rl) * LDW + cl] = l2;
+        Wf[rl * KTILE + cl] = w;
         lb[0] = l0;
         lb[1] = l1;
         lb[2] = l2;
@@ -435,7 +450,7 @@ __global__ void __launch_bounds__(AccTcLayout<DP>::THREADS, 1) accumulate_tc_ker
           for (int e = warp; e < np; e += NCW) {
             const int cl = plist[e] / BM, rl = plist[e] % BM;
             const int i = q0 + rl, jj = kt + cl;
-            Split sw = split_f32(__float_as_uint(Wf[cl * BM + rl]));
+            Split sw = split_f32(__float_as_uint(Wf[rl * KTILE + cl]));
             long long* nrow = numb + (int64_t)i * NUM_NDIG * a.D;
             for (int d = lane; d < a.D; d += 32) {
               uint32_t u = In<DT>::bits(vbase + (int64_t)jj * a.vs[2], d);
@@ -450,7 +465,7 @@ __global__ void __launch_bounds__(AccTcLayout<DP>::THREADS, 1) accumulate_tc_ker
             const int rl = it % BM;
             const uint32_t ent = badl[it / BM];
             const int cl = (int)(ent >> 16), d = (int)(ent & 0xFFFFu);
-            const uint32_t wb = __float_as_uint(Wf[cl * BM + rl]);
+            const uint32_t wb = __float_as_uint(Wf[rl * KTILE + cl]);
             if (wb == 0u || (int)(wb >> 23) < 58) continue;   // zero, or already a pair spill
             const Split sv = split_f32(In<DT>::bits(vbase + (int64_t)(kt + cl) * a.vs[2], d));
             const Split sw = split_f32(wb);
@@ -470,7 +485,7 @@ __global__ void __launch_bounds__(AccTcLayout<DP>::THREADS, 1) accumulate_tc_ker
                 for (int q = 0; q < L::NBAD && !listed; q++) listed = badl[q] == (((uint32_t)cl << 16) | (uint32_t)d);
                 if (listed) continue;
                 for (int rl = 0; rl < BM; rl++) {
-                  uint32_t wb = __float_as_uint(Wf[cl * BM + rl]);
+                  uint32_t wb = __float_as_uint(Wf[rl * KTILE + cl]);
                   if (wb == 0u || (int)(wb >> 23) < 58) continue;   // zero, or already a pair spill
                   Split sw = split_f32(wb);
                   atomic_digits_add(numb + (int64_t)(q0 + rl) * NUM_NDIG * a.D + d, a.D, NUM_E0,
