@@ -1,19 +1,15 @@
-// det-attn kernels for sm_103a: rowmax (pass 1) and exact accumulate (pass 2).
+// det-attn kernels for sm_103a: rowmax (pass 1, tcgen05) and the exact accumulate for
+// D = 256 (pass 2; D <= 128 runs accumulate_tc.cu).
 //
 // Page "det-attn", section "Method": rowmax_i = max_j (scale Q_i.K_j) is a max-reduce;
 // NUM_id = sum_j exp(s_ij - rowmax_i) V_jd and DEN_i = sum_j exp(s_ij - rowmax_i) are
 // exact integer sums in fixed bins, so any tiling, split or order gives the same bits.
 //
-// Exact score on the integer pipe.  Each Q/K row is turned, once per tile load, into a
-// fixed-point int32 vector X_d = x_d 2^-F_row with |X_d| < 2^26 (F_row from the row's
-// largest exponent); the dot is then sum_d Xq_d Xk_d, one 32x32->64 multiply-add per MAC,
-// exact in int64 (|sum| < 2^60 for D <= 256), and RN32(dot 2^(Fq+Fk)) is one correctly
-// rounded conversion.  A row whose elements do not all fit the 26-bit window (a spread of
-// more than 18 binades for bf16, most f32 rows) takes the exact Kulisch fallback for its
-// pairs.
+// Exact scores come from integer-valued bf16 digit slices on the tensor cores (score_tc.cuh:
+// mma.sync in the D = 256 accumulate kernel; tc5.cuh: tcgen05 in rowmax), rounded once.
 //
 // Exact PV.  The weight w in [0, 1] is held as W = w 2^92, three 31-bit limbs (exact for
-// w >= 2^-69); V is fixed point per column over the CTA's key range, |Vint| < 2^23.  Per
+// w >= 2^-69); V is fixed point per column over the call's key range, |Vint| < 2^23.  Per
 // (i, d) three int64 accumulators take limb*Vint (< 2^54 each); every 256 keys the limbs
 // carry into a fourth word in shared memory.  Products the window cannot hold (w < 2^-69,
 // or a V element more than 15 binades below its column maximum) are added exactly with
@@ -25,74 +21,6 @@
 #include "attn_kernels.h"
 
 namespace detattn {
-
-// ---------------------------------------------------------------------------------------
-// fixed-point conversion of one row (one warp): X_d = x_d * 2^-F, F = max(ex,1) - 152
-// ---------------------------------------------------------------------------------------
-template <int DT, int DP>
-__device__ __forceinline__ void convert_row_fixed(const typename In<DT>::T* src, int D, int* dst, int* F_out,
-                                                  unsigned char* fit_out, int& nf, int lane) {
-  constexpr int PER = DP / 32;
-  uint32_t bv[PER];
-  int emax = 1;
-#pragma unroll
-  for (int t = 0; t < PER; t++) {
-    int d = lane + 32 * t;
-    uint32_t u = (src != nullptr && d < D) ? In<DT>::bits(src, d) : 0u;
-    if (nonfinite_bits(u)) { nf |= ST_NONFINITE; u = 0u; }
-    bv[t] = u;
-    int ex = (int)((u >> 23) & 0xFFu);
-    emax = max(emax, ex);
-  }
-  emax = __reduce_max_sync(0xFFFFFFFFu, emax);
-  const int F = emax - 152;
-  bool ok = true;
-#pragma unroll
-  for (int t = 0; t < PER; t++) {
-    Split s = split_f32(bv[t]);
-    int sh = s.lsb - F;   // <= 2
-    int X;
-    if (s.mant == 0) {
-      X = 0;
-    } else if (sh >= 0) {
-      X = (int)(s.mant << sh);
-    } else if (sh > -32) {
-      X = (int)(s.mant >> (-sh));
-      ok = ok && ((s.mant & ((1u << (-sh)) - 1u)) == 0u);
-    } else {
-      X = 0;
-      ok = false;
-    }
-    dst[lane + 32 * t] = s.neg ? -X : X;
-  }
-  ok = __all_sync(0xFFFFFFFFu, ok);
-  if (lane == 0) {
-    *F_out = F;
-    *fit_out = ok ? 1 : 0;
-  }
-}
-
-
-// copy rows [kt, kt + nrow) of the prepared K slices into a smem slice tile; rows at or
-// past hi are zero-filled (their pairs are masked)
-template <int DP>
-__device__ __forceinline__ void load_k_tile(const KvPrep& p, int64_t rowbase, int kt, int hi, int nrow, uint16_t* Ks,
-                                            int LDS, int* Fk, unsigned char* kfit, int tid) {
-  constexpr int CH = DP / 8;   // 16-byte chunks per slice row
-  for (int c = tid; c < nrow * NSLICE * CH; c += 256) {
-    const int r = c / (NSLICE * CH), q = (c / CH) % NSLICE, x = c % CH;
-    const int j = kt + r;
-    const bool ok = j < hi;
-    const uint16_t* src = p.ksl + ((rowbase + (ok ? j : kt)) * NSLICE + q) * DP + 8 * x;
-    cp_async16(Ks + q * nrow * LDS + r * LDS + 8 * x, src, ok ? 16 : 0);
-  }
-  for (int r = tid; r < nrow; r += 256) {
-    const int j = kt + r;
-    const int mv = j < hi ? p.kmeta[rowbase + j] : (1024 - 151) | (1 << 16);
-    Fk[r] = (mv & 0xFFFF) - 1024;
-    kfit[r] = (unsigned char)(mv >> 16);
-  }
-}
 
 // =======================================================================================
 // K1: rowmax on the tensor cores (tcgen05).
