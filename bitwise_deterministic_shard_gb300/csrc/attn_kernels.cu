@@ -22,6 +22,27 @@
 
 namespace detattn {
 
+// copy rows [kt, kt + nrow) of the prepared K slices into a smem slice tile; rows at or
+// past hi are zero-filled (their pairs are masked)
+template <int DP>
+__device__ __forceinline__ void load_k_tile(const KvPrep& p, int64_t rowbase, int kt, int hi, int nrow, uint16_t* Ks,
+                                            int LDS, int* Fk, unsigned char* kfit, int tid) {
+  constexpr int CH = DP / 8;   // 16-byte chunks per slice row
+  for (int c = tid; c < nrow * NSLICE * CH; c += 256) {
+    const int r = c / (NSLICE * CH), q = (c / CH) % NSLICE, x = c % CH;
+    const int j = kt + r;
+    const bool ok = j < hi;
+    const uint16_t* src = p.ksl + ((rowbase + (ok ? j : kt)) * NSLICE + q) * DP + 8 * x;
+    cp_async16(Ks + q * nrow * LDS + r * LDS + 8 * x, src, ok ? 16 : 0);
+  }
+  for (int r = tid; r < nrow; r += 256) {
+    const int j = kt + r;
+    const int mv = j < hi ? p.kmeta[rowbase + j] : (1024 - 151) | (1 << 16);
+    Fk[r] = (mv & 0xFFFF) - 1024;
+    kfit[r] = (unsigned char)(mv >> 16);
+  }
+}
+
 // =======================================================================================
 // K1: rowmax on the tensor cores (tcgen05).
 //
