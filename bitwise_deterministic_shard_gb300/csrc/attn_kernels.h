@@ -30,6 +30,7 @@ struct KvPrep {
   unsigned char* ktc;   // the same slices as tensor-core operand tiles (below)
   int ntk;           // key tiles of KTILE rows per (b, hk) in ktc
   int* kmeta;        // [rows]: (F + 1024) | (fit << 16)
+  unsigned char* vtc;   // DP == 128: V as tensor-core operand digit planes (below), else null
   int* vcol;         // [B * Hkv][DP] largest V biased exponent per column over the range
   int* vint;         // [rows][DP] V fixed point, |Vint| < 2^23
   uint32_t* vbad;    // [rows][DP / 32] elements outside the V window
@@ -41,6 +42,11 @@ struct KvPrep {
 // K-major operand layout of tc5.cuh).  Rows past kv_hi are zero.
 constexpr int KTILE = 128;
 constexpr int KT_BLOCK = 4 * KTILE * 16 * 2;
+// vtc (DP == 128): per (b, hk), blocks of 16 keys from kv_lo (padded to whole key tiles);
+// per block 3 planes = the balanced base-256 digits of Vint (each exact in bf16), each a
+// 128 (d) x 16 (keys) operand block in the canonical K-major layout of tc5.cuh.
+constexpr int VKEYS = 16;
+constexpr int VP_BLOCK = 3 * 128 * VKEYS * 2;
 size_t kv_prep_bytes(int B, int Hkv, int Skv, int D);
 KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v);
 cudaError_t launch_kv_prep(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
@@ -48,6 +54,8 @@ cudaError_t launch_kv_prep(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
 cudaError_t launch_rowmax(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
 cudaError_t launch_accumulate(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
 cudaError_t launch_accumulate_tc(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // D <= 128
+cudaError_t launch_accumulate_tp(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // 64 < D <= 128
+constexpr int ACC_TP_MAX_TILES = 4096;   // key tiles per pass the tensor-PV kernel's state holds exactly
 
 cudaError_t launch_compose_max(float* dst, const float* src, int64_t n, cudaStream_t st);
 cudaError_t launch_compose_add(long long* dst, const long long* src, int64_t n, cudaStream_t st);

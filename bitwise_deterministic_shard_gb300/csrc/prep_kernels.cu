@@ -47,10 +47,21 @@ __global__ void __launch_bounds__(256) prep_kv_kernel(const AttnArgs a, KvPrep p
   auto store_tc = [&](int q, int d, uint16_t v) {
     *reinterpret_cast<uint16_t*>(tile + (d >> 4) * KT_BLOCK + q * (KTILE * 32) + tc5::canon_off(rt, d & 15)) = v;
   };
+  unsigned char* vblk = (p.do_v && p.vtc != nullptr)
+                            ? p.vtc + ((int64_t)(b * a.Hkv + hk) * p.ntk * (KTILE / VKEYS) + jr / VKEYS) * VP_BLOCK
+                            : nullptr;
+  auto store_v = [&](int t, int d, int r) {   // digit t of Vint(key, d) into its operand plane
+    *reinterpret_cast<uint16_t*>(vblk + t * (VP_BLOCK / 3) + tc5::canon_off(d, jr % VKEYS)) =
+        (uint16_t)(__float_as_uint(small_i2f(r)) >> 16);
+  };
   if (j >= a.kv_hi) {
-    for (int d = lane; d < DP; d += 32)
+    for (int d = lane; d < DP; d += 32) {
 #pragma unroll
       for (int q = 0; q < NSLICE; q++) store_tc(q, d, 0);
+      if (vblk)
+#pragma unroll
+        for (int t = 0; t < 3; t++) store_v(t, d, 0);
+    }
     return;
   }
   const int64_t row = ((int64_t)b * a.Hkv + hk) * a.Skv + j;
@@ -91,11 +102,28 @@ __global__ void __launch_bounds__(256) prep_kv_kernel(const AttnArgs a, KvPrep p
         }
       }
       p.vint[row * DP + d] = X;
+      if (vblk) {   // balanced base-256 digits: X = r0 + 256 r1 + 65536 r2, |r_t| <= 128
+        int r0 = X & 255;
+        if (r0 >= 128) r0 -= 256;
+        const int X1 = (X - r0) >> 8;
+        int r1 = X1 & 255;
+        if (r1 >= 128) r1 -= 256;
+        const int r2 = (X1 - r1) >> 8;
+        store_v(0, d, r0);
+        store_v(1, d, r1);
+        store_v(2, d, r2);
+      }
       const uint32_t bad = __ballot_sync(0xFFFFFFFFu, !fit);
       if (lane == 0) p.vbad[row * NW + tv] = bad;
     }
   }
   report(a.status, nf);
+}
+
+static size_t vtc_bytes(int B, int Hkv, int Skv, int dp) {
+  if (dp != 128) return 0;
+  const size_t ntk = (size_t)(Skv + KTILE - 1) / KTILE;
+  return (size_t)B * Hkv * ntk * (KTILE / VKEYS) * VP_BLOCK;
 }
 
 static size_t ktc_bytes(int B, int Hkv, int Skv, int dp) {
@@ -108,7 +136,7 @@ size_t kv_prep_bytes(int B, int Hkv, int Skv, int D) {
   const size_t rows = (size_t)B * Hkv * Skv;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   return up(rows * NSLICE * dp * 2) + up(rows * 4) + up((size_t)B * Hkv * dp * 4) + up(rows * dp * 4) +
-         up(rows * (dp / 32) * 4) + up(ktc_bytes(B, Hkv, Skv, dp));
+         up(rows * (dp / 32) * 4) + up(ktc_bytes(B, Hkv, Skv, dp)) + up(vtc_bytes(B, Hkv, Skv, dp));
 }
 
 KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v) {
@@ -131,6 +159,8 @@ KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v) {
   c += up(rows * (dp / 32) * 4);
   p.ktc = (unsigned char*)c;
   p.ntk = (Skv + KTILE - 1) / KTILE;
+  c += up(ktc_bytes(B, Hkv, Skv, dp));
+  p.vtc = dp == 128 ? (unsigned char*)c : nullptr;
   return p;
 }
 

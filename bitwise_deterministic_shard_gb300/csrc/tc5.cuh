@@ -145,6 +145,10 @@ __device__ __forceinline__ void ld_x4(uint32_t taddr, float (&v)[4]) {
 __device__ __forceinline__ void st_zero_x8(uint32_t taddr) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1};" ::"r"(taddr), "r"(0u) : "memory");
 }
+// zero 4 consecutive 32-bit columns of this thread's TMEM lane
+__device__ __forceinline__ void st_zero_x4(uint32_t taddr) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%1,%1,%1};" ::"r"(taddr), "r"(0u) : "memory");
+}
 __device__ __forceinline__ void st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
