@@ -69,11 +69,18 @@ __device__ __forceinline__ void pv_block_mmas(uint32_t tmem, const unsigned char
   const uint64_t va = tc5::desc(tc5::smem_addr(vblk));
   const uint64_t wa = tc5::desc(tc5::smem_addr(wblk));
 #pragma unroll
-  for (int s = 0; s < L::NWP; s++)
+  for (int t = 0; t < L::NVP; t++)     // the A operand (V digit t) stays for ten MMAs in a row
 #pragma unroll
-    for (int t = 0; t < L::NVP; t++)   // descriptor start addresses advance in 16-byte units
+    for (int s = 0; s < L::NWP; s++)   // descriptor start addresses advance in 16-byte units
       tc5::mma_bf16(tmem + L::PV_COL + (s + t) * L::BM, va + (uint64_t)(t * (VP_BLOCK / 3) / 16),
                     wa + (uint64_t)(s * L::w_blk / 16), idesc, 1u);
+}
+
+// bf16 bits of an integer b in [0, 255] (exact: at most 8 significant bits)
+__device__ __forceinline__ uint16_t byte_bf16(uint32_t b) {
+  if (b == 0u) return 0;
+  const int e = 31 - __clz((int)b);
+  return (uint16_t)(((uint32_t)(e + 127) << 7) | ((b << (7 - e)) & 0x7Fu));
 }
 
 __device__ __forceinline__ void add_i64_at_tp(long long* dg, long long X, int o) {
@@ -86,12 +93,6 @@ __device__ __forceinline__ void add_i64_at_tp(long long* dg, long long X, int o)
   long long v = hi * (1ll << r);
   dg[k + 1] += (long long)((unsigned long long)v & 0xFFFFFFFFull);
   dg[k + 2] += v >> 32;
-}
-
-__device__ __forceinline__ long long warp_sum31_tp(int x) {
-  const unsigned lo = __reduce_add_sync(0xFFFFFFFFu, (unsigned)x & 0xFFFFu);
-  const unsigned hi = __reduce_add_sync(0xFFFFFFFFu, (unsigned)x >> 16);
-  return (long long)lo + ((long long)hi << 16);
 }
 
 template <int DT>
@@ -259,11 +260,11 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
       // PV state: this thread owns value column d = 32 quarter + lane and rows 4 rg .. 4 rg + 3;
       // acc[r][k] is radix-2^32 digit k (lazily carried) in units of 2^(Fv[d] - 79)
       const int dcol = 32 * quarter + lane;
-      long long acc[4][3];
+      long long acc[4][3], dsum[4][3];   // dsum: this thread's DEN limb sums for its 4 rows (all its keys)
 #pragma unroll
       for (int r = 0; r < 4; r++)
 #pragma unroll
-        for (int k = 0; k < 3; k++) acc[r][k] = 0;
+        for (int k = 0; k < 3; k++) acc[r][k] = dsum[r][k] = 0;
       auto weight_of = [&](float sc, float m) -> float {
         float x = __fsub_rn(sc, m);
         if (x != x) { nf |= ST_NONFINITE; x = neg_inf(); }
@@ -299,12 +300,11 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
             }
           }
         }
-        unsigned char* blk = wbuf + (size_t)(cl / VKEYS) * NWP * L::w_blk + tc5::canon_off(rl, cl % VKEYS);
+        if (x != 0u) {   // the buffer was zeroed: write the (at most four) digits W can have
+          unsigned char* blk = wbuf + (size_t)(cl / VKEYS) * NWP * L::w_blk + tc5::canon_off(rl, cl % VKEYS);
 #pragma unroll
-        for (int s = 0; s < NWP; s++) {
-          const int q = s - b0;
-          const uint32_t byte = (q >= 0 && q < 4) ? (x >> (8 * q)) & 255u : 0u;
-          *reinterpret_cast<uint16_t*>(blk + s * L::w_blk) = (uint16_t)(__float_as_uint((float)byte) >> 16);
+          for (int q = 0; q < 4; q++)
+            if (b0 + q < NWP) *reinterpret_cast<uint16_t*>(blk + (b0 + q) * L::w_blk) = byte_bf16((x >> (8 * q)) & 255u);
         }
         Wf[rl * KTILE + cl] = w;
       };
@@ -344,6 +344,8 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         const int mv = vj ? p.kmeta[krow0 + j] : 0;
         const int Fk = (mv & 0xFFFF) - 1024, kf = mv >> 16;
         if (tid == 0) { s_np = 0; s_nbad = 0; s_vany = 0; }
+        for (int e = tid; e < (int)(L::w_buf / 16); e += NCT)   // this buffer's previous PV reads are done
+          reinterpret_cast<uint4*>(wbuf)[e] = make_uint4(0u, 0u, 0u, 0u);
         tc5::bar_sync(1, NCT);
         for (int e = tid; e < KTILE * NW; e += NCT) {   // V elements outside the column window
           const int r = e / NW;
@@ -389,10 +391,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           int lb[3];
           store_weight(w, rl, dcol, wbuf, lb);
 #pragma unroll
-          for (int l = 0; l < 3; l++) {
-            const long long s = warp_sum31_tp(lb[l]);
-            if (lane == 0 && s) atomicAdd((unsigned long long*)&denT[rl][l], (unsigned long long)s);
-          }
+          for (int l = 0; l < 3; l++) dsum[e][l] += lb[l];
         }
         // pairs outside the fixed-point window: the whole warp computes each exact dot
         for (uint32_t pend = __ballot_sync(0xFFFFFFFFu, defer != 0); pend;
@@ -493,6 +492,15 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         tc5::bar_sync(1, NCT);   // tile consumed: float weights, lists and counters are free
       }
       if (nkt > 0) drain(tc + nkt - 1);
+#pragma unroll
+      for (int r = 0; r < 4; r++)   // DEN: the warp's keys of each of its rows, then the four key quarters
+#pragma unroll
+        for (int l = 0; l < 3; l++) {
+          long long v = dsum[r][l];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+          if (lane == 0 && v) atomicAdd((unsigned long long*)&denT[rg * 4 + r][l], (unsigned long long)v);
+        }
       // ---- epilogue: canonical digits ----
       tc5::bar_sync(1, NCT);   // denT and every spill atomic complete
       const bool rmw = a.add_into || s_zeroed;
