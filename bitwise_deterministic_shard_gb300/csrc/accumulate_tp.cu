@@ -7,12 +7,15 @@
 // CTA = 16 query rows of one (b, h), key tiles of 128 keys, one CTA per SM.
 //
 // Scores.  S^T = K Q^T from integer-valued bf16 digit slices (score_tc.cuh): per
-// 16-dimension step, 16 tcgen05 MMAs of M = 128 keys x N = 16 rows x K = 16 accumulate the
-// 7 diagonal sums A_c in TMEM (exact integers); two accumulator sets, so the next tile's
-// scores overlap this tile's weights.
+// 16-dimension step, 4 tcgen05 MMAs of M = 128 keys x N = 64 x K = 16, one per key slice sa,
+// with the four query slices stacked along N (n = 16 sb + row), so
+// D_sa[key][16 sb + row] = sum_d K_sa Q_sb (an integer below 2^21); the compute warps form
+// the seven diagonal sums A_c = sum_{sa+sb=c} D_sa exactly in f32 (integers below 2^23).
 //
 // PV.  Every weight w >= 2^-56 is held as W = w 2^79, an integer below 2^80, split into
-// ten base-256 digits (bytes, each exact in bf16); V is fixed point per column,
+// ten base-256 digits (bytes, each exact in bf16; the digit planes are MN-major, rows
+// contiguous, so a warp's stores for 32 keys of one row spread over the banks); V is fixed
+// point per column,
 // |Vint| < 2^23, split into three balanced base-256 digits (|digit| <= 128, prepared once
 // per call).  PV^T = V^T W^T runs on the tensor cores: per 16 keys, 30 MMAs of M = 128
 // value columns x N = 16 rows x K = 16 keys, weight digit s times V digit t accumulated
@@ -47,8 +50,10 @@ struct AccTpLayout {
   static constexpr int LOADW = NCW, SISS = NCW + 1, PISS0 = NCW + 2, THREADS = 32 * (NCW + 2 + NISS);
   static constexpr int NWP = 10, NVP = 3, NPD = NWP + NVP - 1, NKB = KTILE / VKEYS;
   static_assert(NKB % NISS == 0, "the PV issuers split a tile's key blocks evenly");
-  static constexpr int PV_COL = 0, SC_COL = NPD * BM, SC_BUF = NDIAG * BM, TCOLS = 512;   // TMEM columns
-  static constexpr size_t q_bytes = (size_t)NDS * NSLICE * BM * 32;    // B blocks [step][slice], 16 rows x 16 bf16
+  static constexpr int NQ = NSLICE * BM;                              // score MMA N: the stacked query slices
+  static constexpr int PV_COL = 0, SC_COL = 256, TCOLS = 512;         // TMEM: PV diagonals, score accumulators
+  static constexpr size_t q_step = (size_t)NQ * 32;                    // one B block: 64 rows (16 sb + r) x 16 bf16
+  static constexpr size_t q_bytes = (size_t)NDS * q_step;
   static constexpr size_t k_off = q_bytes;                             // NSK key operand steps
   static constexpr size_t v_off = k_off + (size_t)NSK * KT_BLOCK;      // NVB V digit blocks
   static constexpr size_t w_blk = (size_t)BM * VKEYS * 2;              // one weight digit block: 16 rows x 16 keys
@@ -58,7 +63,7 @@ struct AccTpLayout {
   static constexpr size_t ps_off = wf_off + (size_t)BM * KTILE * 4;    // uint16 pairs below 2^-56
   static constexpr size_t bytes = ps_off + (size_t)KTILE * BM * 2;
   static constexpr int NBAD = 1024;
-  static_assert(SC_COL + 2 * SC_BUF <= TCOLS, "TMEM columns");
+  static_assert(NPD * BM <= SC_COL && SC_COL + NSLICE * NQ <= TCOLS, "TMEM columns");
   static_assert(bytes <= 210 * 1024, "shared memory budget");
 };
 
@@ -102,8 +107,9 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   constexpr int DP = L::DP, BM = L::BM, NDS = L::NDS, NSK = L::NSK, NVB = L::NVB, NCW = L::NCW;
   constexpr int NKB = L::NKB, NWP = L::NWP, NISS = L::NISS, NW = DP / 32;
   constexpr int NCT = 32 * NCW;
-  constexpr uint32_t IDESC_S = tc5::idesc_bf16(KTILE, BM);   // scores: 128 keys x 16 rows
-  constexpr uint32_t IDESC_P = tc5::idesc_bf16(DP, BM);      // PV: 128 columns x 16 rows
+  constexpr int NQ = L::NQ;
+  constexpr uint32_t IDESC_S = tc5::idesc_bf16(KTILE, NQ);   // scores: 128 keys x (4 slices x 16 rows)
+  constexpr uint32_t IDESC_P = tc5::idesc_bf16(DP, BM, true);   // PV: 128 columns x 16 rows, weights MN-major
   extern __shared__ __align__(1024) unsigned char smem_p[];
   unsigned char* Qs = smem_p;
   unsigned char* Kst = smem_p + L::k_off;
@@ -111,8 +117,8 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   unsigned char* Wp = smem_p + L::w_off;
   float* Wf = reinterpret_cast<float*>(smem_p + L::wf_off);
   uint16_t* plist = reinterpret_cast<uint16_t*>(smem_p + L::ps_off);
-  __shared__ __align__(8) uint64_t kfull[NSK], kempty[NSK], sfull[2], sempty[2], vfull[NVB], vempty[NVB], wready[2],
-      pvdone, pvfree, fin;
+  __shared__ __align__(8) uint64_t kfull[NSK], kempty[NSK], sfull, sempty, vfull[NVB], vempty[NVB], wready[2], pvdone,
+      pvfree, fin;
   __shared__ uint32_t tmem_s;
   __shared__ int Fq[BM], Fv[DP];
   __shared__ unsigned char qfit[BM];
@@ -145,11 +151,9 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
       tc5::mbar_init(&vfull[s], 1);
       tc5::mbar_init(&vempty[s], 1);
     }
-    for (int s = 0; s < 2; s++) {
-      tc5::mbar_init(&sfull[s], 1);
-      tc5::mbar_init(&sempty[s], NCW);
-      tc5::mbar_init(&wready[s], NCW);
-    }
+    for (int s = 0; s < 2; s++) tc5::mbar_init(&wready[s], NCW);
+    tc5::mbar_init(&sfull, 1);
+    tc5::mbar_init(&sempty, NCW);
     tc5::mbar_init(&pvdone, NISS);
     tc5::mbar_init(&pvfree, NCW);
     tc5::mbar_init(&fin, 1 + NISS);   // the score issuer and the PV issuers
@@ -189,7 +193,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
       row_slices<DT, DP>(
           i < a.Sq ? qbase + (int64_t)i * a.qs[2] : nullptr, a.D,
           [&](int q, int d, uint16_t v) {
-            *reinterpret_cast<uint16_t*>(Qs + ((d >> 4) * NSLICE + q) * (BM * 32) + tc5::canon_off(r, d & 15)) = v;
+            *reinterpret_cast<uint16_t*>(Qs + (d >> 4) * L::q_step + tc5::canon_off(q * BM + r, d & 15)) = v;
           },
           &Fq[r], &qfit[r], nf, lane);
     }
@@ -218,25 +222,18 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
     } else if (warp == L::SISS) {   // ---------------- score MMAs ----------------
       if (lane == 0)
         for (int ls = 0; ls < nkt * NDS && !s_abort; ls++) {
-          const uint32_t g = tc * NDS + ls, st = g % NSK, tt = tc + ls / NDS, bsel = tt & 1;
+          const uint32_t g = tc * NDS + ls, st = g % NSK, tt = tc + ls / NDS;
           const int k = ls % NDS;
           if (!tc5::mbar_wait(&kfull[st], (g / NSK) & 1, &s_abort, 32)) break;
-          if (k == 0 && tt >= 2 && !tc5::mbar_wait(&sempty[bsel], ((tt >> 1) - 1) & 1, &s_abort, 64)) break;
+          if (k == 0 && tt >= 1 && !tc5::mbar_wait(&sempty, (tt - 1) & 1, &s_abort, 64)) break;
           tc5::fence_after();
           const uint64_t ka = tc5::desc(tc5::smem_addr(Kst + st * KT_BLOCK));
-          const uint64_t qa = tc5::desc(tc5::smem_addr(Qs + k * NSLICE * BM * 32));
-          const uint32_t dbase = tmem + L::SC_COL + bsel * L::SC_BUF;
+          const uint64_t qa = tc5::desc(tc5::smem_addr(Qs + k * L::q_step));
 #pragma unroll
-          for (int sa = 0; sa < NSLICE; sa++)
-#pragma unroll
-            for (int sb = 0; sb < NSLICE; sb++) {
-              const int c = sa + sb;
-              const uint32_t accum = (k > 0 || sa != (c > 3 ? c - 3 : 0)) ? 1u : 0u;
-              tc5::mma_bf16(dbase + c * BM, ka + (uint64_t)(sa * KTILE * 2), qa + (uint64_t)(sb * BM * 2), IDESC_S,
-                            accum);
-            }
+          for (int sa = 0; sa < NSLICE; sa++)   // descriptor start addresses advance in 16-byte units
+            tc5::mma_bf16(tmem + L::SC_COL + sa * NQ, ka + (uint64_t)(sa * KTILE * 2), qa, IDESC_S, k > 0 ? 1u : 0u);
           tc5::commit(&kempty[st]);
-          if (k == NDS - 1) tc5::commit(&sfull[bsel]);
+          if (k == NDS - 1) tc5::commit(&sfull);
         }
     } else if (warp >= L::PISS0) {   // ---------------- PV MMAs: key blocks ii, ii + NISS, ... ----------------
       if (lane == 0) {
@@ -260,11 +257,11 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
       // PV state: this thread owns value column d = 32 quarter + lane and rows 4 rg .. 4 rg + 3;
       // acc[r][k] is radix-2^32 digit k (lazily carried) in units of 2^(Fv[d] - 79)
       const int dcol = 32 * quarter + lane;
-      long long acc[4][3], dsum[4][3];   // dsum: this thread's DEN limb sums for its 4 rows (all its keys)
+      long long acc[4][3];
 #pragma unroll
       for (int r = 0; r < 4; r++)
 #pragma unroll
-        for (int k = 0; k < 3; k++) acc[r][k] = dsum[r][k] = 0;
+        for (int k = 0; k < 3; k++) acc[r][k] = 0;
       auto weight_of = [&](float sc, float m) -> float {
         float x = __fsub_rn(sc, m);
         if (x != x) { nf |= ST_NONFINITE; x = neg_inf(); }
@@ -301,7 +298,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           }
         }
         if (x != 0u) {   // the buffer was zeroed: write the (at most four) digits W can have
-          unsigned char* blk = wbuf + (size_t)(cl / VKEYS) * NWP * L::w_blk + tc5::canon_off(rl, cl % VKEYS);
+          unsigned char* blk = wbuf + (size_t)(cl / VKEYS) * NWP * L::w_blk + tc5::mn_off(rl, cl % VKEYS);
 #pragma unroll
           for (int q = 0; q < 4; q++)
             if (b0 + q < NWP) *reinterpret_cast<uint16_t*>(blk + (b0 + q) * L::w_blk) = byte_bf16((x >> (8 * q)) & 255u);
@@ -359,20 +356,39 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           }
         }
         // ---- weights of rows 4 rg .. 4 rg + 3 against this thread's key ----
-        const bool ok = __all_sync(0xFFFFFFFFu, tc5::mbar_wait(&sfull[bsel], (tt >> 1) & 1, &s_abort, 64));
+        const bool ok = __all_sync(0xFFFFFFFFu, tc5::mbar_wait(&sfull, tt & 1, &s_abort, 64));
         tc5::fence_after();
-        float v[NDIAG][4];
-        if (ok) {
+        float v[NDIAG][4];   // diagonal sums of this thread's 4 rows, exact
 #pragma unroll
-          for (int c = 0; c < NDIAG; c++) tc5::ld_x4(lane_base + L::SC_COL + bsel * L::SC_BUF + c * BM + rg * 4, v[c]);
-          tc5::ld_wait();
-        } else {
+        for (int rr = 0; rr < 4; rr += 2) {
+          float dd[NSLICE][NSLICE][2];
+          if (ok) {
 #pragma unroll
-          for (int c = 0; c < NDIAG; c++) v[c][0] = v[c][1] = v[c][2] = v[c][3] = 0.0f;
+            for (int sa = 0; sa < NSLICE; sa++)
+#pragma unroll
+              for (int sb = 0; sb < NSLICE; sb++)
+                tc5::ld_x2(lane_base + L::SC_COL + sa * NQ + sb * BM + rg * 4 + rr, dd[sa][sb][0], dd[sa][sb][1]);
+            tc5::ld_wait();
+          } else {
+#pragma unroll
+            for (int sa = 0; sa < NSLICE; sa++)
+#pragma unroll
+              for (int sb = 0; sb < NSLICE; sb++) dd[sa][sb][0] = dd[sa][sb][1] = 0.0f;
+          }
+#pragma unroll
+          for (int e = 0; e < 2; e++)
+#pragma unroll
+            for (int c = 0; c < NDIAG; c++) {
+              float sum = 0.0f;
+#pragma unroll
+              for (int sa = 0; sa < NSLICE; sa++)
+                if (c - sa >= 0 && c - sa < NSLICE) sum = __fadd_rn(sum, dd[sa][c - sa][e]);
+              v[c][rr + e] = sum;
+            }
         }
         tc5::fence_before();
         __syncwarp();
-        if (lane == 0) tc5::mbar_arrive(&sempty[bsel]);
+        if (lane == 0) tc5::mbar_arrive(&sempty);
         uint32_t defer = 0;
 #pragma unroll
         for (int e = 0; e < 4; e++) {
@@ -391,7 +407,12 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           int lb[3];
           store_weight(w, rl, dcol, wbuf, lb);
 #pragma unroll
-          for (int l = 0; l < 3; l++) dsum[e][l] += lb[l];
+          for (int l = 0; l < 3; l++) {   // DEN: exact warp sums of 31-bit limbs (two 16-bit halves)
+            const unsigned lo = __reduce_add_sync(0xFFFFFFFFu, (unsigned)lb[l] & 0xFFFFu);
+            const unsigned hi2 = __reduce_add_sync(0xFFFFFFFFu, (unsigned)lb[l] >> 16);
+            const long long sm = (long long)lo + ((long long)hi2 << 16);
+            if (lane == 0 && sm) atomicAdd((unsigned long long*)&denT[rl][l], (unsigned long long)sm);
+          }
         }
         // pairs outside the fixed-point window: the whole warp computes each exact dot
         for (uint32_t pend = __ballot_sync(0xFFFFFFFFu, defer != 0); pend;
@@ -492,15 +513,6 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         tc5::bar_sync(1, NCT);   // tile consumed: float weights, lists and counters are free
       }
       if (nkt > 0) drain(tc + nkt - 1);
-#pragma unroll
-      for (int r = 0; r < 4; r++)   // DEN: the warp's keys of each of its rows, then the four key quarters
-#pragma unroll
-        for (int l = 0; l < 3; l++) {
-          long long v = dsum[r][l];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-          if (lane == 0 && v) atomicAdd((unsigned long long*)&denT[rg * 4 + r][l], (unsigned long long)v);
-        }
       // ---- epilogue: canonical digits ----
       tc5::bar_sync(1, NCT);   // denT and every spill atomic complete
       const bool rmw = a.add_into || s_zeroed;

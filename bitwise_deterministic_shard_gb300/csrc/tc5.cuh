@@ -24,14 +24,23 @@ __device__ __forceinline__ int canon_off(int r, int k) {   // byte offset in an 
   return (r >> 3) * 256 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
 }
 
+// byte offset of element (n, k) in an N x 16 bf16 block stored MN-major (n contiguous in
+// 16-byte core-matrix rows): the descriptor's leading offset (128 B) steps 8 k's, its stride
+// offset (256 B) steps 8 n's; select it with the instruction descriptor's B-major bit
+__device__ __forceinline__ int mn_off(int n, int k) {
+  return (k >> 3) * 128 + (n >> 3) * 256 + (k & 7) * 16 + (n & 7) * 2;
+}
+
 __device__ __forceinline__ uint64_t desc(uint32_t saddr) {
   return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(256 >> 4) << 32) |
          ((uint64_t)1 << 46);
 }
 
-// kind::f16 instruction descriptor: f32 accumulator, bf16 A and B, both K-major, M x N
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+// kind::f16 instruction descriptor: f32 accumulator, bf16 A and B, A K-major, B K-major
+// (or MN-major with b_mn), M x N
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn ? (1u << 16) : 0u) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ uint64_t globaltimer() {
