@@ -8,36 +8,35 @@
 //
 // Scores.  S^T = K Q^T from integer-valued bf16 digit slices (score_tc.cuh): per
 // 16-dimension step, 4 tcgen05 MMAs of M = 128 keys x N = 64 x K = 16, one per key slice sa,
-// with the four query slices stacked along N (n = 16 sb + row), so
-// D_sa[key][16 sb + row] = sum_d K_sa Q_sb (an integer below 2^21); the compute warps form
-// the seven diagonal sums A_c = sum_{sa+sb=c} D_sa exactly in f32 (integers below 2^23).
+// with the four query slices stacked along N (n = 16 sb + row).  The MMA of key slice sa
+// writes its accumulator at TMEM column offset 16 sa, so column 16 sb + row lands on
+// 16 (sa + sb) + row: the tensor core itself forms the seven diagonal sums
+// A_c = sum_{sa+sb=c} sum_d K_sa Q_sb (integers below 2^22, exact in f32).
 //
 // PV.  Every weight w >= 2^-56 is held as W = w 2^79, an integer below 2^80, split into
-// ten base-256 digits (bytes, each exact in bf16; the digit planes are MN-major, rows
-// contiguous, so a warp's stores for 32 keys of one row spread over the banks); V is fixed
-// point per column,
-// |Vint| < 2^23, split into three balanced base-256 digits (|digit| <= 128, prepared once
-// per call).  PV^T = V^T W^T runs on the tensor cores: per 16 keys, 30 MMAs of M = 128
-// value columns x N = 16 rows x K = 16 keys, weight digit s times V digit t accumulated
-// into the diagonal sum P_c, c = s + t (12 f32 accumulators of 16 TMEM columns).  A
-// product is at most 255 * 128, a diagonal has at most 3 of them per key, so over one
-// 128-key tile every partial sum is an integer below 128 * 3 * 32640 < 2^24: exact.  After
-// each tile the compute warps fold sum_c P_c 2^(8c) into three radix-2^32 int64 digits per
-// (row, column) in registers and zero the accumulators.  The weight digit planes are
+// ten base-256 digits W_s (bytes, exact in f16); V is fixed point per column, |Vint| < 2^23,
+// split into three balanced base-256 digits V_t (|V_t| <= 128, prepared once per call).
+// The ten weight digit planes of a 16-key block lie next to each other along N (n = 16 s +
+// row, MN-major), so one MMA of M = 128 value columns x N = 160 x K = 16 multiplies V digit
+// t by all ten; written at column offset 16 t it adds V_t W_s into the diagonal sum
+// P_c (c = s + t) at column 16 c + row.  Three MMAs per 16 keys, plus one with an all-ones
+// A operand whose rows all receive DEN's digit sums sum_k W_s.  A product is at most
+// 255 * 128 and a diagonal holds at most 3 per key, so over one 128-key tile every partial
+// sum is an integer below 128 * 3 * 32640 < 2^24: exact.  After each tile the compute warps
+// fold sum_c P_c 2^(8c) into three radix-2^32 int64 digits per (row, column) and the DEN
+// planes into int32 sums, then zero the accumulators.  The weight digit planes are
 // double-buffered, so the PV MMAs of one tile run while the next tile's weights are
 // computed.  Products outside the window (w < 2^-56, or a V element below its column
-// window) are added with exact int64 atomics into the output digits, one (element, row)
-// product per thread.
+// window) are added with exact int64 atomics into the output digits.
 //
 // Roles: warp 16 copies (lane 0: key operand steps, 2-stage ring; lane 1: V digit blocks,
-// 3-stage ring), warp 17 lane 0 issues the score MMAs, warps 18 and 19 (lane 0) issue the PV
-// MMAs of alternate 16-key blocks (a tcgen05.commit holds its thread until that thread's
-// MMAs are done; every PV MMA accumulates onto TMEM the compute warps zero after reading, so
-// the two need no ordering).  Warps 0-15 compute weights, write the weight digit planes and
-// drain the PV accumulators.  Every mbarrier wait is bounded; one that gives up sets
-// DA_STATUS_TIMEOUT, and a failed wait in the compute warps only skips work so every named
-// barrier is still passed.  The three int64 state digits stay exact for up to
-// ACC_TP_MAX_TILES key tiles per pass; longer key ranges take the integer-pipe kernel.
+// 3-stage ring), warp 17 lane 0 issues the score MMAs, warp 18 lane 0 the PV and DEN MMAs.
+// Warps 0-15 read the score diagonals, compute weights, write the weight digit planes and
+// drain the PV accumulators; each zeroes the TMEM it read before releasing it, so every MMA
+// accumulates.  Every mbarrier wait is bounded; one that gives up sets DA_STATUS_TIMEOUT,
+// and a failed wait in the compute warps only skips work so every named barrier is still
+// passed.  The three int64 state digits stay exact for up to ACC_TP_MAX_TILES key tiles per
+// pass; longer key ranges take the integer-pipe kernel.
 #include "numerics.cuh"
 #include "score_tc.cuh"
 #include "tc5.cuh"
@@ -46,46 +45,49 @@
 namespace detattn {
 
 struct AccTpLayout {
-  static constexpr int DP = 128, BM = 16, NDS = DP / 16, NSK = 2, NVB = 3, NCW = 16, NISS = 2;
-  static constexpr int LOADW = NCW, SISS = NCW + 1, PISS0 = NCW + 2, THREADS = 32 * (NCW + 2 + NISS);
+  static constexpr int DP = 128, BM = 16, NDS = DP / 16, NSK = 2, NVB = 3, NCW = 16;
+  static constexpr int LOADW = NCW, SISS = NCW + 1, PISS = NCW + 2, THREADS = 32 * (NCW + 3);
   static constexpr int NWP = 10, NVP = 3, NPD = NWP + NVP - 1, NKB = KTILE / VKEYS;
-  static_assert(NKB % NISS == 0, "the PV issuers split a tile's key blocks evenly");
   static constexpr int NQ = NSLICE * BM;                              // score MMA N: the stacked query slices
-  static constexpr int PV_COL = 0, SC_COL = 256, TCOLS = 512;         // TMEM: PV diagonals, score accumulators
+  static constexpr int NW16 = NWP * BM;                               // PV MMA N: the stacked weight digits
+  // TMEM columns: PV diagonals P_c at 16 c, DEN digit sums at 16 s, score diagonals at 16 c
+  static constexpr int PV_COL = 0, DEN_COL = PV_COL + NPD * BM, SC_COL = DEN_COL + NWP * BM, TCOLS = 512;
   static constexpr size_t q_step = (size_t)NQ * 32;                    // one B block: 64 rows (16 sb + r) x 16 bf16
   static constexpr size_t q_bytes = (size_t)NDS * q_step;
   static constexpr size_t k_off = q_bytes;                             // NSK key operand steps
   static constexpr size_t v_off = k_off + (size_t)NSK * KT_BLOCK;      // NVB V digit blocks
-  static constexpr size_t w_blk = (size_t)BM * VKEYS * 2;              // one weight digit block: 16 rows x 16 keys
+  static constexpr size_t w_blk = (size_t)BM * VKEYS * 2;              // one weight digit plane: 16 rows x 16 keys
   static constexpr size_t w_buf = (size_t)NKB * NWP * w_blk;           // one tile's weight digit planes [kb][s]
   static constexpr size_t w_off = v_off + (size_t)NVB * VP_BLOCK;      // two buffers
-  static constexpr size_t wf_off = w_off + 2 * w_buf;                  // float [BM][KTILE] weights
+  static constexpr size_t one_off = w_off + 2 * w_buf;                 // 128 x 16 f16 ones (DEN's A operand)
+  static constexpr size_t wf_off = one_off + (size_t)DP * 16 * 2;      // float [KTILE][BM] weights
   static constexpr size_t ps_off = wf_off + (size_t)BM * KTILE * 4;    // uint16 pairs below 2^-56
   static constexpr size_t bytes = ps_off + (size_t)KTILE * BM * 2;
   static constexpr int NBAD = 1024;
-  static_assert(NPD * BM <= SC_COL && SC_COL + NSLICE * NQ <= TCOLS, "TMEM columns");
+  static_assert(SC_COL + NDIAG * BM <= TCOLS, "TMEM columns");
+  static_assert(NW16 <= 256 && NW16 % 16 == 0, "one PV MMA covers every weight digit");
+  static_assert(KTILE * (DP / 32) == 32 * NCW, "one V-bad word per compute thread");
   static_assert(bytes <= 210 * 1024, "shared memory budget");
 };
 
-// the 30 PV products of one 16-key block: weight digit s (B) times V digit t (A) into P_{s+t}
+// one 16-key block: V digit t (A) times the ten stacked weight digits (B) into P_{s+t}, and
+// the ones block times the weight digits into the DEN sums
 __device__ __forceinline__ void pv_block_mmas(uint32_t tmem, const unsigned char* vblk, const unsigned char* wblk,
-                                              uint32_t idesc) {
+                                              uint64_t ones, uint32_t idesc) {
   using L = AccTpLayout;
   const uint64_t va = tc5::desc(tc5::smem_addr(vblk));
   const uint64_t wa = tc5::desc(tc5::smem_addr(wblk));
 #pragma unroll
-  for (int t = 0; t < L::NVP; t++)     // the A operand (V digit t) stays for ten MMAs in a row
-#pragma unroll
-    for (int s = 0; s < L::NWP; s++)   // descriptor start addresses advance in 16-byte units
-      tc5::mma_bf16(tmem + L::PV_COL + (s + t) * L::BM, va + (uint64_t)(t * (VP_BLOCK / 3) / 16),
-                    wa + (uint64_t)(s * L::w_blk / 16), idesc, 1u);
+  for (int t = 0; t < L::NVP; t++)   // descriptor start addresses advance in 16-byte units
+    tc5::mma_bf16(tmem + L::PV_COL + t * L::BM, va + (uint64_t)(t * (VP_BLOCK / 3) / 16), wa, idesc, 1u);
+  tc5::mma_bf16(tmem + L::DEN_COL, ones, wa, idesc, 1u);
 }
 
-// bf16 bits of an integer b in [0, 255] (exact: at most 8 significant bits)
-__device__ __forceinline__ uint16_t byte_bf16(uint32_t b) {
-  if (b == 0u) return 0;
-  const int e = 31 - __clz((int)b);
-  return (uint16_t)(((uint32_t)(e + 127) << 7) | ((b << (7 - e)) & 0x7Fu));
+// two f16 values b0, b1 in [0, 255] from the pattern (0x64 b1 0x64 b0): (1024 + b) - 1024
+__device__ __forceinline__ uint32_t f16_pair_from_biased(uint32_t h) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64006400u));
+  return r;
 }
 
 __device__ __forceinline__ void add_i64_at_tp(long long* dg, long long X, int o) {
@@ -105,11 +107,11 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   using T = typename In<DT>::T;
   using L = AccTpLayout;
   constexpr int DP = L::DP, BM = L::BM, NDS = L::NDS, NSK = L::NSK, NVB = L::NVB, NCW = L::NCW;
-  constexpr int NKB = L::NKB, NWP = L::NWP, NISS = L::NISS, NW = DP / 32;
+  constexpr int NKB = L::NKB, NWP = L::NWP, NW = DP / 32;
   constexpr int NCT = 32 * NCW;
   constexpr int NQ = L::NQ;
-  constexpr uint32_t IDESC_S = tc5::idesc_bf16(KTILE, NQ);   // scores: 128 keys x (4 slices x 16 rows)
-  constexpr uint32_t IDESC_P = tc5::idesc_bf16(DP, BM, true);   // PV: 128 columns x 16 rows, weights MN-major
+  constexpr uint32_t IDESC_S = tc5::idesc_bf16(KTILE, NQ);        // scores: 128 keys x (4 slices x 16 rows)
+  constexpr uint32_t IDESC_P = tc5::idesc_f16(DP, L::NW16, true);   // PV: 128 columns x (10 digits x 16 rows)
   extern __shared__ __align__(1024) unsigned char smem_p[];
   unsigned char* Qs = smem_p;
   unsigned char* Kst = smem_p + L::k_off;
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   __shared__ long long denT[BM][3];
   __shared__ uint32_t vmask[KTILE * NW];
   __shared__ uint32_t badl[L::NBAD];
-  __shared__ int s_np, s_nbad, s_vany, s_zeroed;
+  __shared__ int s_np[2], s_nbad[2], s_vany[2], s_zeroed;   // per tile parity
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -154,24 +156,30 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
     for (int s = 0; s < 2; s++) tc5::mbar_init(&wready[s], NCW);
     tc5::mbar_init(&sfull, 1);
     tc5::mbar_init(&sempty, NCW);
-    tc5::mbar_init(&pvdone, NISS);
+    tc5::mbar_init(&pvdone, 1);
     tc5::mbar_init(&pvfree, NCW);
-    tc5::mbar_init(&fin, 1 + NISS);   // the score issuer and the PV issuers
+    tc5::mbar_init(&fin, 2);   // the score issuer and the PV issuer
     s_abort = 0;
     tc5::mbar_fence_init();
   }
   for (int d = tid; d < DP; d += L::THREADS)   // biased exponent in [1, 254]: |Vint| < 2^23, digit offsets in range
     Fv[d] = min(max(p.vcol[((int64_t)b * a.Hkv + hk) * DP + d], 1), 254) - 149;
+  for (int e = tid; e < DP * 16 / 2; e += L::THREADS)   // f16 1.0 pairs: DEN's all-ones A operand
+    reinterpret_cast<uint32_t*>(smem_p + L::one_off)[e] = 0x3C003C00u;
   tc5::fence_before();
   __syncthreads();
   tc5::fence_after();
   const uint32_t tmem = tmem_s;
-  // the PV accumulators start at zero; the compute warps zero what they drain
+  // every accumulator starts at zero; the compute warps zero what they read
   const int quarter = warp & 3, rg = warp >> 2;   // compute warp: TMEM lanes 32 quarter .., rows 4 rg .. 4 rg + 3
   const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
   if (warp < NCW) {
 #pragma unroll
     for (int c = 0; c < L::NPD; c++) tc5::st_zero_x4(lane_base + L::PV_COL + c * BM + rg * 4);
+#pragma unroll
+    for (int c = 0; c < NWP; c++) tc5::st_zero_x4(lane_base + L::DEN_COL + c * BM + rg * 4);
+#pragma unroll
+    for (int c = 0; c < NDIAG; c++) tc5::st_zero_x4(lane_base + L::SC_COL + c * BM + rg * 4);
     tc5::st_wait();
   }
   tc5::fence_before();
@@ -199,6 +207,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
     }
     for (int r = tid; r < BM; r += L::THREADS) mrow[r] = (q0 + r < a.Sq) ? a.m_in[rowbase + q0 + r] : 0.0f;
     for (int e = tid; e < BM * 3; e += L::THREADS) (&denT[0][0])[e] = 0;
+    if (tid < 2) { s_np[tid] = 0; s_nbad[tid] = 0; s_vany[tid] = 0; }
     if (tid == 0) s_zeroed = 0;
     tc5::fence_async_smem();
     __syncthreads();
@@ -231,31 +240,32 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           const uint64_t qa = tc5::desc(tc5::smem_addr(Qs + k * L::q_step));
 #pragma unroll
           for (int sa = 0; sa < NSLICE; sa++)   // descriptor start addresses advance in 16-byte units
-            tc5::mma_bf16(tmem + L::SC_COL + sa * NQ, ka + (uint64_t)(sa * KTILE * 2), qa, IDESC_S, k > 0 ? 1u : 0u);
+            tc5::mma_bf16(tmem + L::SC_COL + sa * BM, ka + (uint64_t)(sa * KTILE * 2), qa, IDESC_S, 1u);
           tc5::commit(&kempty[st]);
           if (k == NDS - 1) tc5::commit(&sfull);
         }
-    } else if (warp >= L::PISS0) {   // ---------------- PV MMAs: key blocks ii, ii + NISS, ... ----------------
+    } else if (warp == L::PISS) {   // ---------------- PV and DEN MMAs ----------------
       if (lane == 0) {
-        const int ii = warp - L::PISS0;
+        const uint64_t ones = tc5::desc(tc5::smem_addr(smem_p + L::one_off));
         for (int t = 0; t < nkt && !s_abort; t++) {
           const uint32_t tt = tc + t, bsel = tt & 1;
           if (!tc5::mbar_wait(&wready[bsel], (tt >> 1) & 1, &s_abort, 64)) break;   // weight digits of tile tt
           if (tt >= 1 && !tc5::mbar_wait(&pvfree, (tt - 1) & 1, &s_abort, 64)) break;   // accumulators drained
           tc5::fence_after();
-          for (int kb = ii; kb < NKB && !s_abort; kb += NISS) {
+          for (int kb = 0; kb < NKB && !s_abort; kb++) {
             const uint32_t g = tt * NKB + kb, sl = g % NVB;
             if (!tc5::mbar_wait(&vfull[sl], (g / NVB) & 1, &s_abort, 32)) break;
             tc5::fence_after();
-            pv_block_mmas(tmem, Vst + sl * VP_BLOCK, Wp + bsel * L::w_buf + (size_t)kb * NWP * L::w_blk, IDESC_P);
+            pv_block_mmas(tmem, Vst + sl * VP_BLOCK, Wp + bsel * L::w_buf + (size_t)kb * NWP * L::w_blk, ones, IDESC_P);
             tc5::commit(&vempty[sl]);
           }
           tc5::commit(&pvdone);
         }
       }
     } else {   // ---------------- compute warps ----------------
-      // PV state: this thread owns value column d = 32 quarter + lane and rows 4 rg .. 4 rg + 3;
-      // acc[r][k] is radix-2^32 digit k (lazily carried) in units of 2^(Fv[d] - 79)
+      // Weight phase: this thread's key is TMEM lane dcol (rows 4 rg .. 4 rg + 3).  Drain: it
+      // owns value column d = dcol; acc[r][k] is radix-2^32 digit k (lazily carried) in units
+      // of 2^(Fv[d] - 79).
       const int dcol = 32 * quarter + lane;
       long long acc[4][3];
 #pragma unroll
@@ -268,48 +278,17 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         if (x > 0.0f) { viol |= ST_VIOLATION; x = 0.0f; }
         return exp32_det(x);
       };
-      // weight of pair (row rl, key cl) -> digit planes of buffer wbuf, float plane, spill list, DEN limbs
-      auto store_weight = [&](float w, int rl, int cl, unsigned char* wbuf, int (&lb)[3]) {
-        const uint32_t wb = __float_as_uint(w);
-        const int ex = (int)(wb >> 23);
-        uint32_t x = 0;
-        int b0 = 0;
-        lb[0] = lb[1] = lb[2] = 0;
-        if (wb != 0u) {
-          const uint64_t mant = (wb & 0x7FFFFFu) | 0x800000u;
-          if (ex >= 71) {   // W = mant << (ex - 71) < 2^80: four bytes starting at byte b0
-            const int sh = ex - 71;
-            b0 = sh >> 3;
-            x = (uint32_t)(mant << (sh & 7));
-          } else {
-            plist[atomicAdd(&s_np, 1)] = (uint16_t)(cl * BM + rl);   // w < 2^-56: exact atomics
-          }
-          if (ex >= 58) {   // DEN limbs of w 2^92 (31 bits each)
-            const int sh = ex - 58;
-            if (sh <= 38) {
-              const uint64_t W = mant << sh;
-              lb[0] = (int)(W & 0x7FFFFFFFull);
-              lb[1] = (int)(W >> 31);
-            } else {
-              const uint64_t W1 = mant << (sh - 31);
-              lb[1] = (int)(W1 & 0x7FFFFFFFull);
-              lb[2] = (int)(W1 >> 31);
-            }
-          }
-        }
-        if (x != 0u) {   // the buffer was zeroed: write the (at most four) digits W can have
-          unsigned char* blk = wbuf + (size_t)(cl / VKEYS) * NWP * L::w_blk + tc5::mn_off(rl, cl % VKEYS);
-#pragma unroll
-          for (int q = 0; q < 4; q++)
-            if (b0 + q < NWP) *reinterpret_cast<uint16_t*>(blk + (b0 + q) * L::w_blk) = byte_bf16((x >> (8 * q)) & 255u);
-        }
-        Wf[rl * KTILE + cl] = w;
-      };
-      // fold the PV accumulators of one tile into the integer digits, zero them, release them
-      auto drain = [&](uint32_t tt) {
-        const bool ok = __all_sync(0xFFFFFFFFu, tc5::mbar_wait(&pvdone, tt & 1, &s_abort, 64));
+      // lane 0 waits, the warp follows
+      auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        bool ok = true;
+        if (lane == 0) ok = tc5::mbar_wait(bar, parity, &s_abort, 64);
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
         tc5::fence_after();
-        if (ok) {
+        return ok;
+      };
+      // fold the PV and DEN accumulators of one tile into the integer sums, zero them, release them
+      auto drain = [&](uint32_t tt) {
+        if (warp_wait(&pvdone, tt & 1)) {
 #pragma unroll
           for (int g3 = 0; g3 < 3; g3++) {   // diagonals 4 g3 .. 4 g3 + 3 -> digit g3
             float pv[4][4];
@@ -324,119 +303,166 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
               acc[r][g3] += s;
             }
           }
+          // DEN: this warp folds planes quarter + 4 k (every lane holds the same sums); plane
+          // s weighs 2^(8 s) = 2^(32 k + 8 quarter) in units of 2^-79
+          float dv[3][4];
+#pragma unroll
+          for (int k = 0; k < 3; k++)
+            if (quarter + 4 * k < NWP) tc5::ld_x4(lane_base + L::DEN_COL + (quarter + 4 * k) * BM + rg * 4, dv[k]);
+          tc5::ld_wait();
+          if (lane == 0)
+#pragma unroll
+            for (int k = 0; k < 3; k++)
+              if (quarter + 4 * k < NWP)
+#pragma unroll
+                for (int r = 0; r < 4; r++) {
+                  const int sv = __float2int_rn(dv[k][r]);   // < 2^15
+                  if (sv) atomicAdd((unsigned long long*)&denT[rg * 4 + r][k], (unsigned long long)sv << (8 * quarter));
+                }
 #pragma unroll
           for (int c = 0; c < L::NPD; c++) tc5::st_zero_x4(lane_base + L::PV_COL + c * BM + rg * 4);
+#pragma unroll
+          for (int c = 0; c < NWP; c++) tc5::st_zero_x4(lane_base + L::DEN_COL + c * BM + rg * 4);
           tc5::st_wait();
         }
         tc5::fence_before();
         __syncwarp();
         if (lane == 0) tc5::mbar_arrive(&pvfree);
       };
+      // key meta of this thread's key and V-bad word tid of tile t (zeros past the range)
+      auto tile_meta = [&](int t, int& mv, uint32_t& vb) {
+        mv = 0;
+        vb = 0u;
+        if (t < nkt) {
+          const int kt = a.kv_lo + t * KTILE, r = tid / NW;
+          if (kt + dcol < hi) mv = p.kmeta[krow0 + kt + dcol];
+          if (kt + r < hi) vb = p.vbad[(krow0 + kt + r) * NW + tid % NW];
+        }
+      };
+      int mv_n;
+      uint32_t vb_n;
+      tile_meta(0, mv_n, vb_n);
       for (int t = 0; t < nkt; t++) {
-        const int kt = a.kv_lo + t * KTILE;
+        const int kt = a.kv_lo + t * KTILE, cp = t & 1;
         const uint32_t tt = tc + t, bsel = tt & 1;
         unsigned char* wbuf = Wp + bsel * L::w_buf;
-        const int j = kt + dcol;   // this thread's key in the weight phase (TMEM lane = key)
+        const int j = kt + dcol;
         const bool vj = j < hi;
-        const int mv = vj ? p.kmeta[krow0 + j] : 0;
+        const int mv = mv_n;
+        const uint32_t vb = vb_n;
+        tile_meta(t + 1, mv_n, vb_n);   // the next tile's, in flight meanwhile
         const int Fk = (mv & 0xFFFF) - 1024, kf = mv >> 16;
-        if (tid == 0) { s_np = 0; s_nbad = 0; s_vany = 0; }
-        for (int e = tid; e < (int)(L::w_buf / 16); e += NCT)   // this buffer's previous PV reads are done
-          reinterpret_cast<uint4*>(wbuf)[e] = make_uint4(0u, 0u, 0u, 0u);
-        tc5::bar_sync(1, NCT);
-        for (int e = tid; e < KTILE * NW; e += NCT) {   // V elements outside the column window
-          const int r = e / NW;
-          uint32_t m = (kt + r < hi) ? p.vbad[(krow0 + kt + r) * NW + e % NW] : 0u;
-          vmask[e] = m;
-          if (m) s_vany = 1;
+        if (tid == 0) { s_np[cp ^ 1] = 0; s_nbad[cp ^ 1] = 0; s_vany[cp ^ 1] = 0; }   // the next tile's counters
+        {   // V elements outside the column window (key tid / NW, word tid % NW)
+          uint32_t m = vb;
+          vmask[tid] = m;
+          if (m) s_vany[cp] = 1;
           while (m) {
-            const int bit = __ffs(m) - 1, slot = atomicAdd(&s_nbad, 1);
+            const int bit = __ffs(m) - 1, slot = atomicAdd(&s_nbad[cp], 1);
             m &= m - 1;
-            if (slot < L::NBAD) badl[slot] = ((uint32_t)r << 16) | (uint32_t)((e % NW) * 32 + bit);
+            if (slot < L::NBAD) badl[slot] = ((uint32_t)(tid / NW) << 16) | (uint32_t)((tid % NW) * 32 + bit);
           }
         }
-        // ---- weights of rows 4 rg .. 4 rg + 3 against this thread's key ----
-        const bool ok = __all_sync(0xFFFFFFFFu, tc5::mbar_wait(&sfull, tt & 1, &s_abort, 64));
-        tc5::fence_after();
-        float v[NDIAG][4];   // diagonal sums of this thread's 4 rows, exact
+        // ---- score diagonals of rows 4 rg .. 4 rg + 3 against this thread's key ----
+        const bool ok = warp_wait(&sfull, tt & 1);
+        float v[NDIAG][4];
+        if (ok) {
 #pragma unroll
-        for (int rr = 0; rr < 4; rr += 2) {
-          float dd[NSLICE][NSLICE][2];
-          if (ok) {
+          for (int c = 0; c < NDIAG; c++) tc5::ld_x4(lane_base + L::SC_COL + c * BM + rg * 4, v[c]);
+          tc5::ld_wait();
 #pragma unroll
-            for (int sa = 0; sa < NSLICE; sa++)
+          for (int c = 0; c < NDIAG; c++) tc5::st_zero_x4(lane_base + L::SC_COL + c * BM + rg * 4);
+          tc5::st_wait();
+        } else {
 #pragma unroll
-              for (int sb = 0; sb < NSLICE; sb++)
-                tc5::ld_x2(lane_base + L::SC_COL + sa * NQ + sb * BM + rg * 4 + rr, dd[sa][sb][0], dd[sa][sb][1]);
-            tc5::ld_wait();
-          } else {
+          for (int c = 0; c < NDIAG; c++)
 #pragma unroll
-            for (int sa = 0; sa < NSLICE; sa++)
-#pragma unroll
-              for (int sb = 0; sb < NSLICE; sb++) dd[sa][sb][0] = dd[sa][sb][1] = 0.0f;
-          }
-#pragma unroll
-          for (int e = 0; e < 2; e++)
-#pragma unroll
-            for (int c = 0; c < NDIAG; c++) {
-              float sum = 0.0f;
-#pragma unroll
-              for (int sa = 0; sa < NSLICE; sa++)
-                if (c - sa >= 0 && c - sa < NSLICE) sum = __fadd_rn(sum, dd[sa][c - sa][e]);
-              v[c][rr + e] = sum;
-            }
+            for (int e = 0; e < 4; e++) v[c][e] = 0.0f;
         }
         tc5::fence_before();
         __syncwarp();
         if (lane == 0) tc5::mbar_arrive(&sempty);
+        // ---- weights ----
+        float w[4];
         uint32_t defer = 0;
 #pragma unroll
         for (int e = 0; e < 4; e++) {
           const int rl = rg * 4 + e, i = q0 + rl;
-          float w = 0.0f;
+          w[e] = 0.0f;
           if (ok && vj && i < a.Sq && (!a.causal || j <= i)) {
-            if (qfit[rl] && kf) {
-              long long Tsum = 0;
-#pragma unroll
-              for (int c = NDIAG - 1; c >= 0; c--) Tsum = Tsum * 128 + small_f2i(v[c][e]);
-              w = weight_of(__fmul_rn(a.scale32, cr32_scaled(Tsum, Fq[rl] + Fk)), mrow[rl]);
-            } else {
+            if (qfit[rl] && kf)
+              w[e] = weight_of(__fmul_rn(a.scale32, cr32_scaled(combine_diag(v, e), Fq[rl] + Fk)), mrow[rl]);
+            else
               defer |= 1u << e;   // the exact fallback below fills this pair
-            }
-          }
-          int lb[3];
-          store_weight(w, rl, dcol, wbuf, lb);
-#pragma unroll
-          for (int l = 0; l < 3; l++) {   // DEN: exact warp sums of 31-bit limbs (two 16-bit halves)
-            const unsigned lo = __reduce_add_sync(0xFFFFFFFFu, (unsigned)lb[l] & 0xFFFFu);
-            const unsigned hi2 = __reduce_add_sync(0xFFFFFFFFu, (unsigned)lb[l] >> 16);
-            const long long sm = (long long)lo + ((long long)hi2 << 16);
-            if (lane == 0 && sm) atomicAdd((unsigned long long*)&denT[rl][l], (unsigned long long)sm);
           }
         }
         // pairs outside the fixed-point window: the whole warp computes each exact dot
         for (uint32_t pend = __ballot_sync(0xFFFFFFFFu, defer != 0); pend;
              pend = __ballot_sync(0xFFFFFFFFu, defer != 0)) {
           const int src = __ffs(pend) - 1;
-          const uint32_t dm = __shfl_sync(0xFFFFFFFFu, defer, src);
-          const int rl = rg * 4 + __ffs(dm) - 1, cl = 32 * quarter + src;
+          const int e0 = __ffs(__shfl_sync(0xFFFFFFFFu, defer, src)) - 1;
+          const int rl = rg * 4 + e0, cl = 32 * quarter + src;
           const float sc = __fmul_rn(a.scale32, exact_dot_warp<DT>(qbase + (int64_t)(q0 + rl) * a.qs[2],
                                                                   kbase + (int64_t)(kt + cl) * a.ks[2], a.D, lane));
-          if (lane == 0) {
-            int lb[3];
-            store_weight(weight_of(sc, mrow[rl]), rl, cl, wbuf, lb);
+          const float wd = weight_of(sc, mrow[rl]);
+          if (lane == src) {
 #pragma unroll
-            for (int l = 0; l < 3; l++)
-              if (lb[l]) atomicAdd((unsigned long long*)&denT[rl][l], (unsigned long long)lb[l]);
+            for (int e = 0; e < 4; e++)
+              if (e == e0) w[e] = wd;
+            defer &= defer - 1;
           }
-          if (lane == src) defer &= defer - 1;
+        }
+        // ---- weight digits: W = w 2^79 = x 2^(8 b0), x < 2^32; words[e][q] = bytes 4q .. 4q + 3 of W ----
+        uint32_t words[4][3];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const uint32_t wb = __float_as_uint(w[e]);   // 0 <= w <= 1
+          const int ex = (int)(wb >> 23);
+          uint32_t x = 0;
+          int b0 = 0;
+          if (ex >= 71) {
+            const int sh = ex - 71;   // <= 56
+            b0 = sh >> 3;
+            x = ((wb & 0x7FFFFFu) | 0x800000u) << (sh & 7);
+          } else if (wb != 0u) {
+            plist[atomicAdd(&s_np[cp], 1)] = (uint16_t)(dcol * BM + rg * 4 + e);   // w < 2^-56: exact atomics
+          }
+          const uint64_t y = (uint64_t)x << (8 * (b0 & 3));
+          const uint32_t lo = (uint32_t)y, hw = (uint32_t)(y >> 32);
+          const bool low = b0 < 4;
+          words[e][0] = low ? lo : 0u;
+          words[e][1] = low ? hw : lo;
+          words[e][2] = low ? 0u : hw;
+        }
+        *reinterpret_cast<float4*>(Wf + dcol * BM + rg * 4) = make_float4(w[0], w[1], w[2], w[3]);
+        {   // plane s of this key's 4 rows: 4 f16 values, contiguous in the MN-major block (one 8-byte store)
+          unsigned char* wdst = wbuf + (size_t)(dcol / VKEYS) * NWP * L::w_blk + tc5::mn_off(rg * 4, dcol % VKEYS);
+#pragma unroll
+          for (int q = 0; q < 3; q++) {
+            const uint32_t a01[2] = {__byte_perm(words[0][q], words[1][q], 0x5140),    // bytes 0, 1 of rows 0, 1
+                                     __byte_perm(words[0][q], words[1][q], 0x7362)};   // bytes 2, 3
+            const uint32_t a23[2] = {__byte_perm(words[2][q], words[3][q], 0x5140),
+                                     __byte_perm(words[2][q], words[3][q], 0x7362)};
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+              const int s = 4 * q + k;
+              if (s < NWP) {
+                const uint32_t sel = (k & 1) ? 0x4342u : 0x4140u;   // (0x64, byte of row 1, 0x64, byte of row 0)
+                const uint32_t h01 = f16_pair_from_biased(__byte_perm(a01[k >> 1], 0x64646464u, sel));
+                const uint32_t h23 = f16_pair_from_biased(__byte_perm(a23[k >> 1], 0x64646464u, sel));
+                *reinterpret_cast<uint2*>(wdst + s * L::w_blk) = make_uint2(h01, h23);
+              }
+            }
+          }
         }
         tc5::fence_async_smem();   // the weight digit planes are read by the tensor cores
         __syncwarp();
         if (lane == 0) tc5::mbar_arrive(&wready[bsel]);
+        // ---- the previous tile's PV products are done by now (or soon): fold them in ----
+        if (t >= 1) drain(tt - 1);
         // ---- products outside the window: exact int64 atomics into the output digits ----
         tc5::bar_sync(1, NCT);   // lists, spill counters and the float weights complete
-        if (s_np > 0 || s_vany) {
+        if (s_np[cp] > 0 || s_vany[cp]) {
           if (!s_zeroed) {
             if (!a.add_into) {
               for (int64_t e = tid; e < (int64_t)nrows * NUM_NDIG * a.D; e += NCT)
@@ -446,11 +472,11 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
             tc5::bar_sync(1, NCT);
             if (tid == 0) s_zeroed = 1;
           }
-          const int np = s_np;
+          const int np = s_np[cp];
           for (int e = warp; e < np; e += NCW) {
             const int cl = plist[e] / BM, rl = plist[e] % BM;
             const int i = q0 + rl, jj = kt + cl;
-            const uint32_t wb = __float_as_uint(Wf[rl * KTILE + cl]);
+            const uint32_t wb = __float_as_uint(Wf[cl * BM + rl]);
             const Split sw = split_f32(wb);
             long long* nrow = numb + (int64_t)i * NUM_NDIG * a.D;
             for (int d = lane; d < a.D; d += 32) {
@@ -459,15 +485,14 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
               Split sv = split_f32(u);
               atomic_digits_add(nrow + d, a.D, NUM_E0, (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
             }
-            if (lane == 0 && (int)(wb >> 23) < 58)   // the DEN limbs cover w >= 2^-69 only
-              atomic_digits_add(denb + (int64_t)i * DEN_NDIG, 1, DEN_E0, sw.mant, 0, sw.lsb);
+            if (lane == 0) atomic_digits_add(denb + (int64_t)i * DEN_NDIG, 1, DEN_E0, sw.mant, 0, sw.lsb);
           }
-          const int nbad = s_nbad;
+          const int nbad = s_nbad[cp];
           for (int it = tid; it < min(nbad, L::NBAD) * BM; it += NCT) {   // one (element, row) product each
             const int rl = it % BM;
             const uint32_t ent = badl[it / BM];
             const int cl = (int)(ent >> 16), d = (int)(ent & 0xFFFFu);
-            const uint32_t wb = __float_as_uint(Wf[rl * KTILE + cl]);
+            const uint32_t wb = __float_as_uint(Wf[cl * BM + rl]);
             if (wb == 0u || (int)(wb >> 23) < 71) continue;   // zero, or already a pair spill
             const Split sv = split_f32(In<DT>::bits(vbase + (int64_t)(kt + cl) * a.vs[2], d));
             const Split sw = split_f32(wb);
@@ -487,7 +512,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
                 if (listed) continue;
                 Split sv = split_f32(In<DT>::bits(vbase + (int64_t)jj * a.vs[2], d));
                 for (int rl = 0; rl < BM; rl++) {
-                  uint32_t wb = __float_as_uint(Wf[rl * KTILE + cl]);
+                  uint32_t wb = __float_as_uint(Wf[cl * BM + rl]);
                   if (wb == 0u || (int)(wb >> 23) < 71) continue;
                   Split sw = split_f32(wb);
                   atomic_digits_add(numb + (int64_t)(q0 + rl) * NUM_NDIG * a.D + d, a.D, NUM_E0,
@@ -497,8 +522,6 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
             }
           }
         }
-        // ---- the previous tile's PV products are done by now (or soon): fold them in ----
-        if (t >= 1) drain(tt - 1);
         if ((t & 1023) == 1023) {   // carry the lower digits up
 #pragma unroll
           for (int r = 0; r < 4; r++) {
@@ -510,7 +533,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
             acc[r][2] += c1;
           }
         }
-        tc5::bar_sync(1, NCT);   // tile consumed: float weights, lists and counters are free
+        tc5::bar_sync(1, NCT);   // tile consumed: float weights, lists and V masks are free
       }
       if (nkt > 0) drain(tc + nkt - 1);
       // ---- epilogue: canonical digits ----
@@ -552,10 +575,10 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         if (rmw)
 #pragma unroll
           for (int k = 0; k < DEN_NDIG; k++) dg[k] = __ldcg(drow + k);
-        const int off = -92 - DEN_E0;
+        const int off = -79 - DEN_E0;   // W units
         add_i64_at_tp(dg, denT[rl][0], off);
-        add_i64_at_tp(dg, denT[rl][1], off + 31);
-        add_i64_at_tp(dg, denT[rl][2], off + 62);
+        add_i64_at_tp(dg, denT[rl][1], off + 32);
+        add_i64_at_tp(dg, denT[rl][2], off + 64);
         kul_carry(dg, DEN_NDIG + 3);
         long long top = dg[DEN_NDIG + 2];
         bool bad = false;
@@ -572,7 +595,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
     tc += nkt;
     __syncthreads();
   }   // pass
-  if ((warp == L::SISS || warp >= L::PISS0) && lane == 0) {   // every MMA has completed before TMEM is released
+  if ((warp == L::SISS || warp == L::PISS) && lane == 0) {   // every MMA has completed before TMEM is released
     tc5::commit(&fin);
     tc5::mbar_wait(&fin, 0, &s_abort);
   }

@@ -87,19 +87,6 @@ struct RowmaxTcLayout {
   static_assert(bytes <= 227 * 1024, "shared memory budget");
 };
 
-// exact int64 dot sum_c 2^(7c) A_c from the 7 diagonal sums (f32 integers, |A_c| <= 2^22);
-// the conversions' common offset is folded into one constant (arithmetic mod 2^64)
-__device__ __forceinline__ long long combine7(const float (&v)[NDIAG][8], int r) {
-  int raw[NDIAG];
-#pragma unroll
-  for (int c = 0; c < NDIAG; c++) raw[c] = __float_as_int(__fadd_rn(v[c][r], 12582912.0f));
-  const int hi = (raw[5] - 0x4B400000) + (raw[6] - 0x4B400000) * 128;   // |hi| < 2^29
-  long long acc = (long long)((unsigned long long)(long long)hi << 35);
-#pragma unroll
-  for (int c = 0; c < 5; c++) mad_wide(acc, raw[c], 1 << (7 * c));
-  return (long long)((unsigned long long)acc - 0x4B400000ull * 0x10204081ull);
-}
-
 // true when the score RN32(scale * RN32(T 2^E)) cannot exceed `bound` and is finite
 __device__ __forceinline__ bool score_below(const float (&v)[NDIAG][8], int r, int E, float scale, float bound) {
   if (E < -126 || E > 127) return false;
@@ -268,7 +255,7 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
             if (qfit[rl] && kf) {
               const int E = Fq[rl] + Fk;
               if (!score_below(v, r, E, a.scale32, thr[r])) {
-                const float sc = __fmul_rn(a.scale32, cr32_scaled(combine7(v, r), E));
+                const float sc = __fmul_rn(a.scale32, cr32_scaled(combine_diag(v, r), E));
                 if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
                 mrun[r] = sc > mrun[r] ? sc : mrun[r];
               }

@@ -43,7 +43,7 @@ struct KvPrep {
 constexpr int KTILE = 128;
 constexpr int KT_BLOCK = 4 * KTILE * 16 * 2;
 // vtc (DP == 128): per (b, hk), blocks of 16 keys from kv_lo (padded to whole key tiles);
-// per block 3 planes = the balanced base-256 digits of Vint (each exact in bf16), each a
+// per block 3 planes = the balanced base-256 digits of Vint (each exact in f16), each a
 // 128 (d) x 16 (keys) operand block in the canonical K-major layout of tc5.cuh.
 constexpr int VKEYS = 16;
 constexpr int VP_BLOCK = 3 * 128 * VKEYS * 2;

@@ -4,6 +4,7 @@
 // over the range (|Vint| < 2^23) plus a bit mask of the elements that do not fit.  Done
 // once per call (O(S D) work), so the attention kernels copy ready tiles with cp.async
 // instead of converting each tile once per block of query rows.
+#include <cuda_fp16.h>
 #include "numerics.cuh"
 #include "score_tc.cuh"
 #include "tc5.cuh"
@@ -50,9 +51,9 @@ __global__ void __launch_bounds__(256) prep_kv_kernel(const AttnArgs a, KvPrep p
   unsigned char* vblk = (p.do_v && p.vtc != nullptr)
                             ? p.vtc + ((int64_t)(b * a.Hkv + hk) * p.ntk * (KTILE / VKEYS) + jr / VKEYS) * VP_BLOCK
                             : nullptr;
-  auto store_v = [&](int t, int d, int r) {   // digit t of Vint(key, d) into its operand plane
+  auto store_v = [&](int t, int d, int r) {   // digit t of Vint(key, d) into its operand plane (f16, exact)
     *reinterpret_cast<uint16_t*>(vblk + t * (VP_BLOCK / 3) + tc5::canon_off(d, jr % VKEYS)) =
-        (uint16_t)(__float_as_uint(small_i2f(r)) >> 16);
+        __half_as_ushort(__int2half_rn(r));
   };
   if (j >= a.kv_hi) {
     for (int d = lane; d < DP; d += 32) {

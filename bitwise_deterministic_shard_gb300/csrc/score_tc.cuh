@@ -82,12 +82,19 @@ __device__ __forceinline__ void score_tile_mma(float (&acc)[NDIAG][4], const uin
   }
 }
 
-// exact int64 dot from the 7 diagonal sums of one output element
-__device__ __forceinline__ long long combine_diag(const float (&acc)[NDIAG][4], int e) {
-  long long T = 0;
+// exact int64 dot sum_c 2^(7c) A_c from the 7 diagonal sums of output element e (f32
+// integers, |A_c| <= 2^22): v + 1.5 2^23 puts A_c in the low bits of the float's pattern,
+// and the patterns' common offset is folded into one constant (arithmetic mod 2^64)
+template <int N>
+__device__ __forceinline__ long long combine_diag(const float (&acc)[NDIAG][N], int e) {
+  int raw[NDIAG];
 #pragma unroll
-  for (int c = NDIAG - 1; c >= 0; c--) T = T * 128 + small_f2i(acc[c][e]);   // |A_c| <= 2^22
-  return T;
+  for (int c = 0; c < NDIAG; c++) raw[c] = __float_as_int(__fadd_rn(acc[c][e], 12582912.0f));
+  const int hi = (raw[5] - 0x4B400000) + (raw[6] - 0x4B400000) * 128;   // |hi| < 2^30
+  long long T = (long long)((unsigned long long)(long long)hi << 35);
+#pragma unroll
+  for (int c = 0; c < 5; c++) mad_wide(T, raw[c], 1 << (7 * c));
+  return (long long)((unsigned long long)T - 0x4B400000ull * 0x10204081ull);
 }
 
 // Convert one row (one warp) to fixed point and hand its four digit slices to

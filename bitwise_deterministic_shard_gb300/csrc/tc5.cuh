@@ -1,5 +1,5 @@
-// Blackwell (sm_103a) primitives for the tensor-core score engine: TMEM allocation,
-// tcgen05.mma (kind::f16, bf16 operands, f32 accumulators in TMEM), tcgen05.ld,
+// Blackwell (sm_103a) primitives for the tensor-core kernels: TMEM allocation,
+// tcgen05.mma (kind::f16, bf16 or f16 operands, f32 accumulators in TMEM), tcgen05.ld,
 // mbarriers and bulk global->shared copies.
 //
 // Operand layout (shared memory, no swizzle, K-major).  An R x 16 bf16 block stores
@@ -41,6 +41,10 @@ __device__ __forceinline__ uint64_t desc(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn = false) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn ? (1u << 16) : 0u) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(m >> 4) << 24);
+}
+// the same with f16 A and B
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool b_mn = false) {
+  return (1u << 4) | (b_mn ? (1u << 16) : 0u) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -111,7 +115,8 @@ __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::be
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, M x N x 16
+// D[tmem] (+)= A[smem] * B[smem]^T, M x N x 16 (kind::f16: the instruction descriptor names
+// the operand type, bf16 or f16)
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
