@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(AccTcLayout<DP>::THREADS, 1) accumulate_tc_ker
         // a failed wait only skips work: every compute warp still passes every barrier below
         const bool live = __all_sync(0xFFFFFFFFu, tc5::mbar_wait(&tfull[bsel], (tc >> 1) & 1, &s_abort, 64));
         tc5::fence_after();
-        const int Fk = (mv & 0xFFFF) - 1024, kf = mv >> 16;
+        const int Fk = kmeta_F(mv), kf = kmeta_fit(mv);
         const uint32_t tbase = tmem + ((uint32_t)(32 * quarter) << 16) + bsel * L::BUF + rg * 8;
         uint32_t defer = 0;
 #pragma unroll

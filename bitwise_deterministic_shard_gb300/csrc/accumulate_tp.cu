@@ -29,7 +29,7 @@
 // computed.  Products outside the window (w < 2^-56, or a V element below its column
 // window) are added with exact int64 atomics into the output digits.
 //
-// Roles: warp 16 copies (lane 0: key operand steps, 2-stage ring; lane 1: V digit blocks,
+// Roles: warp 16 copies (lane 0: key operand steps, 4-stage ring; lane 1: V digit blocks,
 // 3-stage ring), warp 17 lane 0 issues the score MMAs, warp 18 lane 0 the PV and DEN MMAs.
 // Warps 0-15 read the score diagonals, compute weights, write the weight digit planes and
 // drain the PV accumulators; each zeroes the TMEM it read before releasing it, so every MMA
@@ -45,7 +45,7 @@
 namespace detattn {
 
 struct AccTpLayout {
-  static constexpr int DP = 128, BM = 16, NDS = DP / 16, NSK = 2, NVB = 3, NCW = 16;
+  static constexpr int DP = 128, BM = 16, NDS = DP / 16, NSK = 4, NVB = 3, NCW = 16;
   static constexpr int LOADW = NCW, SISS = NCW + 1, PISS = NCW + 2, THREADS = 32 * (NCW + 3);
   static constexpr int NWP = 10, NVP = 3, NPD = NWP + NVP - 1, NKB = KTILE / VKEYS;
   static constexpr int NQ = NSLICE * BM;                              // score MMA N: the stacked query slices
@@ -67,7 +67,7 @@ struct AccTpLayout {
   static_assert(SC_COL + NDIAG * BM <= TCOLS, "TMEM columns");
   static_assert(NW16 <= 256 && NW16 % 16 == 0, "one PV MMA covers every weight digit");
   static_assert(KTILE * (DP / 32) == 32 * NCW, "one V-bad word per compute thread");
-  static_assert(bytes <= 210 * 1024, "shared memory budget");
+  static_assert(bytes <= 213 * 1024, "shared memory budget (plus about 8 KB static)");
 };
 
 // one 16-key block: V digit t (A) times the ten stacked weight digits (B) into P_{s+t}, and
@@ -123,7 +123,8 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
       pvfree, fin;
   __shared__ uint32_t tmem_s;
   __shared__ int Fq[BM], Fv[DP];
-  __shared__ unsigned char qfit[BM];
+  __shared__ unsigned char qfit[BM], qlon[BM];
+  __shared__ int2 qlo[BM][NLO];
   __shared__ float mrow[BM];
   __shared__ long long denT[BM][3];
   __shared__ uint32_t vmask[KTILE * NW];
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           [&](int q, int d, uint16_t v) {
             *reinterpret_cast<uint16_t*>(Qs + (d >> 4) * L::q_step + tc5::canon_off(q * BM + r, d & 15)) = v;
           },
-          &Fq[r], &qfit[r], nf, lane);
+          &Fq[r], &qfit[r], nf, lane, qlo[r], &qlon[r]);
     }
     for (int r = tid; r < BM; r += L::THREADS) mrow[r] = (q0 + r < a.Sq) ? a.m_in[rowbase + q0 + r] : 0.0f;
     for (int e = tid; e < BM * 3; e += L::THREADS) (&denT[0][0])[e] = 0;
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         const int mv = mv_n;
         const uint32_t vb = vb_n;
         tile_meta(t + 1, mv_n, vb_n);   // the next tile's, in flight meanwhile
-        const int Fk = (mv & 0xFFFF) - 1024, kf = mv >> 16;
+        const int Fk = kmeta_F(mv), kf = kmeta_fit(mv);
         if (tid == 0) { s_np[cp ^ 1] = 0; s_nbad[cp ^ 1] = 0; s_vany[cp ^ 1] = 0; }   // the next tile's counters
         {   // V elements outside the column window (key tid / NW, word tid % NW)
           uint32_t m = vb;
@@ -390,27 +391,34 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           const int rl = rg * 4 + e, i = q0 + rl;
           w[e] = 0.0f;
           if (ok && vj && i < a.Sq && (!a.causal || j <= i)) {
-            if (qfit[rl] && kf)
+            if (qfit[rl] && kf) {
               w[e] = weight_of(__fmul_rn(a.scale32, cr32_scaled(combine_diag(v, e), Fq[rl] + Fk)), mrow[rl]);
-            else
-              defer |= 1u << e;   // the exact fallback below fills this pair
+            } else if (qlon[rl] != LO_DEEP && kmeta_lon(mv) != KLO_DEEP) {   // truncated dot + low limbs
+              const float dot = dot_lo<DT>(combine_diag(v, e), qbase + (int64_t)i * a.qs[2], Fq[rl], qlo[rl], qlon[rl],
+                                           kbase + (int64_t)j * a.ks[2], Fk, p.klo + (krow0 + j) * NLO, kmeta_lon(mv));
+              w[e] = weight_of(__fmul_rn(a.scale32, dot), mrow[rl]);
+            } else {
+              defer |= 1u << e;   // a deep row: the general exact dot below fills this pair
+            }
           }
         }
-        // pairs outside the fixed-point window: the whole warp computes each exact dot
-        for (uint32_t pend = __ballot_sync(0xFFFFFFFFu, defer != 0); pend;
-             pend = __ballot_sync(0xFFFFFFFFu, defer != 0)) {
-          const int src = __ffs(pend) - 1;
-          const int e0 = __ffs(__shfl_sync(0xFFFFFFFFu, defer, src)) - 1;
-          const int rl = rg * 4 + e0, cl = 32 * quarter + src;
-          const float sc = __fmul_rn(a.scale32, exact_dot_warp<DT>(qbase + (int64_t)(q0 + rl) * a.qs[2],
-                                                                  kbase + (int64_t)(kt + cl) * a.ks[2], a.D, lane));
-          const float wd = weight_of(sc, mrow[rl]);
-          if (lane == src) {
+        // pairs with a deep row: each thread computes its own exactly
+        if (defer) {
+          const T* krow = kbase + (int64_t)j * a.ks[2];
 #pragma unroll
-            for (int e = 0; e < 4; e++)
-              if (e == e0) w[e] = wd;
-            defer &= defer - 1;
-          }
+          for (int e = 0; e < 4; e++)
+            if ((defer >> e) & 1u) {
+              const int rl = rg * 4 + e;
+              const T* qrow = qbase + (int64_t)(q0 + rl) * a.qs[2];
+              float dot;
+              if (!qfit[rl] && kf)
+                dot = exact_dot_lane<DT, true, false>(qrow, Fq[rl], krow, Fk, a.D);
+              else if (qfit[rl])
+                dot = exact_dot_lane<DT, false, true>(qrow, Fq[rl], krow, Fk, a.D);
+              else
+                dot = exact_dot_lane<DT, true, true>(qrow, Fq[rl], krow, Fk, a.D);
+              w[e] = weight_of(__fmul_rn(a.scale32, dot), mrow[rl]);
+            }
         }
         // ---- weight digits: W = w 2^79 = x 2^(8 b0), x < 2^32; words[e][q] = bytes 4q .. 4q + 3 of W ----
         uint32_t words[4][3];

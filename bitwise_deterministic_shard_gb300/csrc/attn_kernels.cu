@@ -38,8 +38,8 @@ __device__ __forceinline__ void load_k_tile(const KvPrep& p, int64_t rowbase, in
   for (int r = tid; r < nrow; r += 256) {
     const int j = kt + r;
     const int mv = j < hi ? p.kmeta[rowbase + j] : (1024 - 151) | (1 << 16);
-    Fk[r] = (mv & 0xFFFF) - 1024;
-    kfit[r] = (unsigned char)(mv >> 16);
+    Fk[r] = kmeta_F(mv);
+    kfit[r] = (unsigned char)kmeta_fit(mv);
   }
 }
 
@@ -115,6 +115,8 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
   __shared__ __align__(8) uint64_t full[NST], empty[NST], tfull, tempty, fin;
   __shared__ uint32_t tmem_s;
   __shared__ int Fq[BM], rkey[BM];
+  __shared__ unsigned char qlon[BM];
+  __shared__ int2 qlo[BM][NLO];
   __shared__ unsigned char qfit[BM];
   __shared__ volatile int s_abort;
 
@@ -169,7 +171,7 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
           [&](int q, int d, uint16_t v) {
             *reinterpret_cast<uint16_t*>(Qs + (d >> 4) * L::q_step + tc5::canon_off(q * BM + r, d & 15)) = v;
           },
-          &Fq[r], &qfit[r], nf, lane);
+          &Fq[r], &qfit[r], nf, lane, qlo[r], &qlon[r]);
     }
     for (int r = tid; r < BM; r += L::THREADS) rkey[r] = float_key(neg_inf());
     tc5::fence_async_smem();
@@ -246,7 +248,7 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
         float thr[8];   // the rows' running maxima so far (exact scores)
 #pragma unroll
         for (int r = 0; r < 8; r++) thr[r] = fmaxf(mrun[r], key_float(rkey[rg * 8 + r]));
-        const int Fk = (mv & 0xFFFF) - 1024, kf = mv >> 16;
+        const int Fk = kmeta_F(mv), kf = kmeta_fit(mv);
         uint32_t defer = 0;   // rows whose pair with this key needs the exact fallback
 #pragma unroll
         for (int r = 0; r < 8; r++) {
@@ -259,8 +261,14 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
                 if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
                 mrun[r] = sc > mrun[r] ? sc : mrun[r];
               }
+            } else if (qlon[rl] != LO_DEEP && kmeta_lon(mv) != KLO_DEEP) {   // truncated dot + low limbs
+              const float sc = __fmul_rn(
+                  a.scale32, dot_lo<DT>(combine_diag(v, r), qbase + (int64_t)i * a.qs[2], Fq[rl], qlo[rl], qlon[rl],
+                                        kbase + (int64_t)j * a.ks[2], Fk, p.klo + (krow0 + j) * NLO, kmeta_lon(mv)));
+              if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
+              mrun[r] = sc > mrun[r] ? sc : mrun[r];
             } else {
-              defer |= 1u << rl;
+              defer |= 1u << rl;   // a deep row: the warp's exact dot below
             }
           }
         }

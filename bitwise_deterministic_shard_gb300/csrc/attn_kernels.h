@@ -29,7 +29,8 @@ struct KvPrep {
   uint16_t* ksl;     // bf16 digit slices [rows][4][DP]
   unsigned char* ktc;   // the same slices as tensor-core operand tiles (below)
   int ntk;           // key tiles of KTILE rows per (b, hk) in ktc
-  int* kmeta;        // [rows]: (F + 1024) | (fit << 16)
+  int* kmeta;        // [rows]: (F + 1024) | (fit << 16) | (low-limb count, or 15 for deep, << 17)
+  int2* klo;         // [rows][NLO] low limbs (d, X_lo) of rows outside the 26-bit window
   unsigned char* vtc;   // DP == 128: V as tensor-core operand digit planes (below), else null
   int* vcol;         // [B * Hkv][DP] largest V biased exponent per column over the range
   int* vint;         // [rows][DP] V fixed point, |Vint| < 2^23

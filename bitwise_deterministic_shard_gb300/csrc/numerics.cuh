@@ -280,6 +280,61 @@ __device__ float exact_dot_warp(const typename In<DT>::T* q, const typename In<D
 }
 
 // ---------------------------------------------------------------------------------------
+// Exact score of one pair by one thread, for a pair with a row outside its 26-bit window.
+// Both rows are read as 52-bit fixed point X = x 2^-(F - 26), F the row's 26-bit window
+// exponent (|X| < 2^52), and X is split into a signed high limb X >> 26 and a low limb in
+// [0, 2^26), exactly as the warp version above; the four limb-product sums are exact int64s
+// and the 128-bit total is rounded once.  A row that fits its 26-bit window has zero low
+// limbs, so QLO / KLO false drops the products that would vanish.  An element below the
+// 52-bit window sends the pair to the Kulisch fallback.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ bool limbs52(uint32_t u, int Flo, int& h, int& l) {
+  h = 0;
+  l = 0;
+  if (nonfinite_bits(u)) return true;   // counted where the row was converted; it adds nothing
+  const Split s = split_f32(u);
+  if (s.mant == 0u) return true;
+  const int sh = s.lsb - Flo;   // <= 28
+  long long X;
+  bool ok = true;
+  if (sh >= 0) {
+    X = (long long)((unsigned long long)s.mant << sh);
+  } else if (sh > -32) {
+    X = (long long)(s.mant >> (-sh));
+    ok = (s.mant & ((1u << (-sh)) - 1u)) == 0u;
+  } else {
+    X = 0;
+    ok = false;
+  }
+  if (s.neg) X = -X;
+  h = (int)(X >> 26);
+  l = (int)(X & 0x3FFFFFFll);
+  return ok;
+}
+
+template <int DT, bool QLO, bool KLO>
+__device__ __noinline__ float exact_dot_lane(const typename In<DT>::T* q, int Fq, const typename In<DT>::T* k, int Fk,
+                                             int D) {
+  long long shh = 0, shl = 0, slh = 0, sll = 0;
+  bool ok = true;
+  for (int d = 0; d < D; d++) {
+    int qh, ql, kh, kl;
+    ok &= limbs52(In<DT>::bits(q, d), Fq - 26, qh, ql);
+    ok &= limbs52(In<DT>::bits(k, d), Fk - 26, kh, kl);
+    shh += (long long)qh * kh;
+    if (KLO) shl += (long long)qh * kl;
+    if (QLO) slh += (long long)ql * kh;
+    if (QLO && KLO) sll += (long long)ql * kl;
+  }
+  if (!ok) return exact_dot_slow<DT>(q, k, D);
+  const __int128 T = (__int128)shh * ((__int128)1 << 52) + (__int128)(shl + slh) * (1ll << 26) + (__int128)sll;
+  if (T == 0) return 0.0f;
+  const int neg = T < 0;
+  const unsigned __int128 mag = neg ? (unsigned __int128)(-T) : (unsigned __int128)T;
+  return round_f32(mag, false, Fq + Fk - 52, neg);
+}
+
+// ---------------------------------------------------------------------------------------
 // Round a digit array (radix 2^32 int64, word k weighs 2^(32k + base), any carries) to
 // binary64, ties to even.  Values here lie in [2^-320, 2^192): normal binary64 range.
 // ---------------------------------------------------------------------------------------

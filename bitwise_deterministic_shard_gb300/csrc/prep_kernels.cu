@@ -70,12 +70,15 @@ __global__ void __launch_bounds__(256) prep_kv_kernel(const AttnArgs a, KvPrep p
   {
     const T* krow = (const T*)a.k + b * a.ks[0] + hk * a.ks[1] + (int64_t)j * a.ks[2];
     __shared__ int Fk_s[8];
-    __shared__ unsigned char fit_s[8];
+    __shared__ unsigned char fit_s[8], lon_s[8];
     uint16_t* ks = p.ksl + row * NSLICE * DP;
     row_slices<DT, DP>(krow, a.D, [&](int q, int d, uint16_t v) { ks[q * DP + d] = v; store_tc(q, d, v); },
-                       &Fk_s[warp], &fit_s[warp], nf, lane);
+                       &Fk_s[warp], &fit_s[warp], nf, lane, p.klo + row * NLO, &lon_s[warp]);
     __syncwarp();
-    if (lane == 0) p.kmeta[row] = (Fk_s[warp] + 1024) | ((int)fit_s[warp] << 16);
+    if (lane == 0) {
+      const int lon = lon_s[warp] == LO_DEEP ? KLO_DEEP : (int)lon_s[warp];
+      p.kmeta[row] = (Fk_s[warp] + 1024) | ((int)fit_s[warp] << 16) | (lon << 17);
+    }
   }
   if (p.do_v) {
     const T* vrow = (const T*)a.v + b * a.vs[0] + hk * a.vs[1] + (int64_t)j * a.vs[2];
@@ -136,8 +139,8 @@ size_t kv_prep_bytes(int B, int Hkv, int Skv, int D) {
   const int dp = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
   const size_t rows = (size_t)B * Hkv * Skv;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return up(rows * NSLICE * dp * 2) + up(rows * 4) + up((size_t)B * Hkv * dp * 4) + up(rows * dp * 4) +
-         up(rows * (dp / 32) * 4) + up(ktc_bytes(B, Hkv, Skv, dp)) + up(vtc_bytes(B, Hkv, Skv, dp));
+  return up(rows * NSLICE * dp * 2) + up(rows * 4) + up(rows * NLO * 8) + up((size_t)B * Hkv * dp * 4) +
+         up(rows * dp * 4) + up(rows * (dp / 32) * 4) + up(ktc_bytes(B, Hkv, Skv, dp)) + up(vtc_bytes(B, Hkv, Skv, dp));
 }
 
 KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v) {
@@ -152,6 +155,8 @@ KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v) {
   c += up(rows * NSLICE * dp * 2);
   p.kmeta = (int*)c;
   c += up(rows * 4);
+  p.klo = (int2*)c;
+  c += up(rows * NLO * 8);
   p.vcol = (int*)c;
   c += up((size_t)B * Hkv * dp * 4);
   p.vint = (int*)c;

@@ -97,12 +97,29 @@ __device__ __forceinline__ long long combine_diag(const float (&acc)[NDIAG][N], 
   return (long long)((unsigned long long)T - 0x4B400000ull * 0x10204081ull);
 }
 
+// Rows outside the 26-bit window.  Such a row's digit slices hold its truncated part
+// X_hi = trunc(x 2^-F); the rest is the low limb X_lo = (x 2^-F - X_hi) 2^26, an integer in
+// (-2^26, 2^26) whenever the element has no bit below 2^(F - 26).  In practice few elements
+// of a row have a low limb, so up to NLO of them are listed as (d, X_lo); a row with more,
+// or with bits below 2^(F - 26), is "deep" and its pairs take the general exact dot.
+constexpr int NLO = 4;
+constexpr unsigned char LO_DEEP = 0xFF;
+constexpr int KLO_DEEP = 15;   // the low-limb field of a deep key row's meta word
+
+// key meta word: window exponent, fit flag, low-limb count (or KLO_DEEP)
+__device__ __forceinline__ int kmeta_F(int mv) { return (mv & 0xFFFF) - 1024; }
+__device__ __forceinline__ int kmeta_fit(int mv) { return (mv >> 16) & 1; }
+__device__ __forceinline__ int kmeta_lon(int mv) { return (mv >> 17) & 15; }
+
 // Convert one row (one warp) to fixed point and hand its four digit slices to
 // store(slice, d, bf16 bits) for d in [0, DP) (zeros past D).  F_out / fit_out receive the
-// row's window exponent and whether every element fits the 26-bit window.
+// row's window exponent and whether every element fits the 26-bit window.  With lo_out,
+// the row's low limbs go to lo_out[0 .. NLO) and *lon_out receives their count (0 for a row
+// that fits) or LO_DEEP.
 template <int DT, int DP, class Store>
 __device__ __forceinline__ void row_slices(const typename In<DT>::T* src, int D, Store store, int* F_out,
-                                           unsigned char* fit_out, int& nf, int lane) {
+                                           unsigned char* fit_out, int& nf, int lane, int2* lo_out = nullptr,
+                                           unsigned char* lon_out = nullptr) {
   constexpr int PER = DP / 32;
   uint32_t bv[PER];
   int emax = 1;
@@ -116,33 +133,87 @@ __device__ __forceinline__ void row_slices(const typename In<DT>::T* src, int D,
   }
   emax = __reduce_max_sync(0xFFFFFFFFu, emax);
   const int F = emax - 152;
-  bool ok = true;
+  bool ok = true, deep = false;
+  int nlo = 0;
 #pragma unroll
   for (int t = 0; t < PER; t++) {
     Split s = split_f32(bv[t]);
     int sh = s.lsb - F;   // <= 2
-    int X = 0;
+    int X = 0, Xl = 0;
     if (s.mant != 0) {
       if (sh >= 0) {
         X = (int)(s.mant << sh);
-      } else if (sh > -32) {
-        X = (int)(s.mant >> (-sh));
-        ok = ok && ((s.mant & ((1u << (-sh)) - 1u)) == 0u);
       } else {
-        ok = false;
+        X = sh > -32 ? (int)(s.mant >> (-sh)) : 0;
+        const uint32_t rem = sh > -32 ? (s.mant & ((1u << (-sh)) - 1u)) : s.mant;
+        if (rem != 0u) {
+          ok = false;
+          const int sl = sh + 26;   // the remainder's lsb in units of 2^(F - 26)
+          if (sl >= 0)
+            Xl = (int)(rem << sl);   // < 2^26
+          else if (sl > -32 && (rem & ((1u << (-sl)) - 1u)) == 0u)
+            Xl = (int)(rem >> (-sl));
+          else
+            deep = true;
+        }
       }
-      if (s.neg) X = -X;
+      if (s.neg) {
+        X = -X;
+        Xl = -Xl;
+      }
     }
-    uint16_t sl[NSLICE];
-    slice4(X, sl);
+    uint16_t sl4[NSLICE];
+    slice4(X, sl4);
 #pragma unroll
-    for (int q = 0; q < NSLICE; q++) store(q, lane + 32 * t, sl[q]);
+    for (int q = 0; q < NSLICE; q++) store(q, lane + 32 * t, sl4[q]);
+    if (lo_out != nullptr) {
+      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, Xl != 0);
+      const int idx = nlo + __popc(bal & ((1u << lane) - 1u));
+      if (Xl != 0 && idx < NLO) lo_out[idx] = make_int2(lane + 32 * t, Xl);
+      nlo += __popc(bal);
+    }
   }
   ok = __all_sync(0xFFFFFFFFu, ok);
+  deep = __any_sync(0xFFFFFFFFu, deep) || nlo > NLO;
   if (lane == 0) {
     *F_out = F;
     *fit_out = ok ? 1 : 0;
+    if (lon_out != nullptr) *lon_out = ok ? 0 : (deep ? LO_DEEP : (unsigned char)nlo);
   }
+}
+
+// truncated 26-bit fixed point of one element, trunc(x 2^-F) (the value its digit slices hold)
+__device__ __forceinline__ int hi26(uint32_t u, int F) {
+  if (nonfinite_bits(u)) return 0;
+  const Split s = split_f32(u);
+  const int sh = s.lsb - F;
+  const int X = sh >= 0 ? (int)(s.mant << sh) : (sh > -32 ? (int)(s.mant >> (-sh)) : 0);
+  return s.neg ? -X : X;
+}
+
+// Exact score of a pair with a row outside its window (neither row deep), from the dot of
+// the truncated parts T_hh = sum_d Xq_hi Xk_hi (the tensor core's) and the rows' low limbs:
+//   x_q . x_k = 2^(Fq + Fk - 52) (T_hh 2^52 + (sum ql Xk_hi + sum Xq_hi kl) 2^26 + sum ql kl),
+// the cross sums over the listed elements only.  Rounded once to binary32.
+template <int DT>
+__device__ __noinline__ float dot_lo(long long Thh, const typename In<DT>::T* qrow, int Fq, const int2* qlo, int nq,
+                                        const typename In<DT>::T* krow, int Fk, const int2* klo, int nk) {
+  long long cross = 0, ll = 0;
+  for (int i = 0; i < nq; i++) {
+    const int2 e = qlo[i];
+    cross += (long long)e.y * hi26(In<DT>::bits(krow, e.x), Fk);
+  }
+  for (int i = 0; i < nk; i++) {
+    const int2 e = klo[i];
+    cross += (long long)hi26(In<DT>::bits(qrow, e.x), Fq) * e.y;
+    for (int i2 = 0; i2 < nq; i2++)
+      if (qlo[i2].x == e.x) ll += (long long)qlo[i2].y * e.y;
+  }
+  const __int128 T = (__int128)Thh * ((__int128)1 << 52) + (__int128)cross * (1ll << 26) + (__int128)ll;
+  if (T == 0) return 0.0f;
+  const int neg = T < 0;
+  const unsigned __int128 mag = neg ? (unsigned __int128)(-T) : (unsigned __int128)T;
+  return round_f32(mag, false, Fq + Fk - 52, neg);
 }
 
 // the same, stored as slice planes dst[q * plane + d]

@@ -114,8 +114,9 @@ def test_wide_exponent_inputs_take_the_exact_fallbacks(da, orc):
 @pytest.mark.parametrize("causal", [False, True])
 def test_rows_outside_the_fast_window_match_oracle(da, orc, causal):
     """Rows with one element 20 to 40 binades below the row maximum do not fit the 26-bit
-    fixed point of the tensor-core path; their pairs take the deferred one-warp exact dot
-    (52-bit window).  Every third Q and K row is made such a row."""
+    fixed point of the tensor-core path; their pairs take the deferred exact dot (52-bit
+    window, one warp or one thread per pair).  Every third Q and K row is made such a row,
+    so some pairs have both rows outside."""
     g = torch.Generator().manual_seed(70 + causal)
     Q, K, V = (torch.randn(1, 2, 150, 128, generator=g) for _ in range(3))
     for X in (Q, K):
