@@ -11,7 +11,9 @@
 // with the four query slices stacked along N (n = 16 sb + row).  The MMA of key slice sa
 // writes its accumulator at TMEM column offset 16 sa, so column 16 sb + row lands on
 // 16 (sa + sb) + row: the tensor core itself forms the seven diagonal sums
-// A_c = sum_{sa+sb=c} sum_d K_sa Q_sb (integers below 2^22, exact in f32).
+// A_c = sum_{sa+sb=c} sum_d K_sa Q_sb (integers below 2^22, exact in f32).  A pair with a
+// row outside its 26-bit window adds the row's low limbs to that truncated dot (dot_lo,
+// score_tc.cuh); a pair with a deep row takes the per-thread exact dot.
 //
 // PV.  Every weight w >= 2^-56 is held as W = w 2^79, an integer below 2^80, split into
 // ten base-256 digits W_s (bytes, exact in f16); V is fixed point per column, |Vint| < 2^23,
@@ -19,24 +21,35 @@
 // The ten weight digit planes of a 16-key block lie next to each other along N (n = 16 s +
 // row, MN-major), so one MMA of M = 128 value columns x N = 160 x K = 16 multiplies V digit
 // t by all ten; written at column offset 16 t it adds V_t W_s into the diagonal sum
-// P_c (c = s + t) at column 16 c + row.  Three MMAs per 16 keys, plus one with an all-ones
-// A operand whose rows all receive DEN's digit sums sum_k W_s.  A product is at most
+// P_c (c = s + t) at column 16 c + row: three MMAs per 16 keys.  A product is at most
 // 255 * 128 and a diagonal holds at most 3 per key, so over one 128-key tile every partial
 // sum is an integer below 128 * 3 * 32640 < 2^24: exact.  After each tile the compute warps
-// fold sum_c P_c 2^(8c) into three radix-2^32 int64 digits per (row, column) and the DEN
-// planes into int32 sums, then zero the accumulators.  The weight digit planes are
-// double-buffered, so the PV MMAs of one tile run while the next tile's weights are
-// computed.  Products outside the window (w < 2^-56, or a V element below its column
-// window) are added with exact int64 atomics into the output digits.
+// fold sum_c P_c 2^(8c) into three radix-2^32 int64 digits per (row, column) and zero the
+// accumulators.  The weight digit planes and the PV accumulators are double-buffered, so
+// the PV MMAs of one tile run while the next tile's weights are computed and the tile before
+// is folded in.
+//
+// DEN.  The same planes read as an MN-major A operand (M = 8 digits x 16 rows) times a block
+// of ones give sum_k W_s for digits 0-7 in TMEM lane 16 s + row; these sums grow by at most
+// 255 per key, so they stay exact for ACC_TP_MAX_TILES tiles and are read once per pass.
+// Digits 8-9 (below 2^16 per key) are summed with one warp reduction per row.
+//
+// Products outside the window are added with exact int64 atomics into the output digits by
+// the warp that owns the pair, so the compute warps share no per-tile state and never wait
+// for each other within a pass; the output rows are cleared when the pass starts and the
+// epilogue adds onto them.  Weights 2^-112 <= w < 2^-56 are integers W' = w 2^135 < 2^79:
+// per row, the warp sums W' Vint over its keys exactly (three 32-bit words of W') and adds
+// the sums, so a row costs twelve atomics per lane and tile however many such weights it
+// has.  V elements below their column window (Vint = 0 there) are kept in a per-warp list of
+// (key, the four weights) and their products added after the tiles; smaller weights take
+// whole-product atomics.
 //
 // Roles: warp 16 copies (lane 0: key operand steps, 4-stage ring; lane 1: V digit blocks,
-// 3-stage ring), warp 17 lane 0 issues the score MMAs, warp 18 lane 0 the PV and DEN MMAs.
-// Warps 0-15 read the score diagonals, compute weights, write the weight digit planes and
-// drain the PV accumulators; each zeroes the TMEM it read before releasing it, so every MMA
-// accumulates.  Every mbarrier wait is bounded; one that gives up sets DA_STATUS_TIMEOUT,
-// and a failed wait in the compute warps only skips work so every named barrier is still
-// passed.  The three int64 state digits stay exact for up to ACC_TP_MAX_TILES key tiles per
-// pass; longer key ranges take the integer-pipe kernel.
+// NVB-stage ring), warps 17 and 19 (lane 0) issue the score MMAs of alternate steps, warp 18
+// lane 0 the PV and DEN MMAs.  Warps 0-15 read the score diagonals, compute weights, write the weight digit
+// planes and drain the PV accumulators; each zeroes the TMEM it read before releasing it,
+// so every MMA accumulates.  Every mbarrier wait is bounded; one that gives up sets
+// DA_STATUS_TIMEOUT, and a failed wait in the compute warps only skips work.
 #include "numerics.cuh"
 #include "score_tc.cuh"
 #include "tc5.cuh"
@@ -45,13 +58,16 @@
 namespace detattn {
 
 struct AccTpLayout {
-  static constexpr int DP = 128, BM = 16, NDS = DP / 16, NSK = 4, NVB = 3, NCW = 16;
-  static constexpr int LOADW = NCW, SISS = NCW + 1, PISS = NCW + 2, THREADS = 32 * (NCW + 3);
+  static constexpr int DP = 128, BM = 16, NDS = DP / 16, NSK = 4, NVB = 4, NCW = 16;
+  // warps: NCW compute, the loader, score issuer 0, the PV issuer, score issuer 1 (the two
+  // score issuers take alternate 16-dimension steps and sit on different SM sub-partitions)
+  static constexpr int LOADW = NCW, SISS = NCW + 1, PISS = NCW + 2, SISS2 = NCW + 3, THREADS = 32 * (NCW + 4);
   static constexpr int NWP = 10, NVP = 3, NPD = NWP + NVP - 1, NKB = KTILE / VKEYS;
   static constexpr int NQ = NSLICE * BM;                              // score MMA N: the stacked query slices
   static constexpr int NW16 = NWP * BM;                               // PV MMA N: the stacked weight digits
-  // TMEM columns: PV diagonals P_c at 16 c, DEN digit sums at 16 s, score diagonals at 16 c
-  static constexpr int PV_COL = 0, DEN_COL = PV_COL + NPD * BM, SC_COL = DEN_COL + NWP * BM, TCOLS = 512;
+  static constexpr int NDEN = 8;                                      // weight digits summed on the tensor cores
+  // TMEM columns: two PV buffers (diagonal P_c at 16 c), the score diagonals at 16 c, DEN
+  static constexpr int PV_COL = 0, PV_BUF = NPD * BM, SC_COL = 2 * PV_BUF, DEN_COL = SC_COL + NDIAG * BM, TCOLS = 512;
   static constexpr size_t q_step = (size_t)NQ * 32;                    // one B block: 64 rows (16 sb + r) x 16 bf16
   static constexpr size_t q_bytes = (size_t)NDS * q_step;
   static constexpr size_t k_off = q_bytes;                             // NSK key operand steps
@@ -59,28 +75,26 @@ struct AccTpLayout {
   static constexpr size_t w_blk = (size_t)BM * VKEYS * 2;              // one weight digit plane: 16 rows x 16 keys
   static constexpr size_t w_buf = (size_t)NKB * NWP * w_blk;           // one tile's weight digit planes [kb][s]
   static constexpr size_t w_off = v_off + (size_t)NVB * VP_BLOCK;      // two buffers
-  static constexpr size_t one_off = w_off + 2 * w_buf;                 // 128 x 16 f16 ones (DEN's A operand)
-  static constexpr size_t wf_off = one_off + (size_t)DP * 16 * 2;      // float [KTILE][BM] weights
-  static constexpr size_t ps_off = wf_off + (size_t)BM * KTILE * 4;    // uint16 pairs below 2^-56
-  static constexpr size_t bytes = ps_off + (size_t)KTILE * BM * 2;
-  static constexpr int NBAD = 1024;
-  static_assert(SC_COL + NDIAG * BM <= TCOLS, "TMEM columns");
+  static constexpr size_t one_off = w_off + 2 * w_buf;                 // 16 x 16 f16 ones: DEN's B operand
+  static constexpr size_t bytes = one_off + 16 * 16 * 2;
+  static_assert(DEN_COL + 16 <= TCOLS, "TMEM columns");
+  static_assert(NDEN * BM == 128, "the DEN MMA's A operand is eight digit planes");
   static_assert(NW16 <= 256 && NW16 % 16 == 0, "one PV MMA covers every weight digit");
-  static_assert(KTILE * (DP / 32) == 32 * NCW, "one V-bad word per compute thread");
   static_assert(bytes <= 213 * 1024, "shared memory budget (plus about 8 KB static)");
 };
 
-// one 16-key block: V digit t (A) times the ten stacked weight digits (B) into P_{s+t}, and
-// the ones block times the weight digits into the DEN sums
-__device__ __forceinline__ void pv_block_mmas(uint32_t tmem, const unsigned char* vblk, const unsigned char* wblk,
-                                              uint64_t ones, uint32_t idesc) {
+// one 16-key block: V digit t (A) times the ten stacked weight digits (B) into P_{s+t} of
+// the PV buffer at TMEM address pv; weight digits 0-7 (A, MN-major) times ones (B) into DEN
+__device__ __forceinline__ void pv_block_mmas(uint32_t pv, uint32_t den, const unsigned char* vblk,
+                                              const unsigned char* wblk, uint64_t ones, uint32_t idesc_pv,
+                                              uint32_t idesc_den) {
   using L = AccTpLayout;
   const uint64_t va = tc5::desc(tc5::smem_addr(vblk));
   const uint64_t wa = tc5::desc(tc5::smem_addr(wblk));
 #pragma unroll
   for (int t = 0; t < L::NVP; t++)   // descriptor start addresses advance in 16-byte units
-    tc5::mma_bf16(tmem + L::PV_COL + t * L::BM, va + (uint64_t)(t * (VP_BLOCK / 3) / 16), wa, idesc, 1u);
-  tc5::mma_bf16(tmem + L::DEN_COL, ones, wa, idesc, 1u);
+    tc5::mma_bf16(pv + t * L::BM, va + (uint64_t)(t * (VP_BLOCK / 3) / 16), wa, idesc_pv, 1u);
+  tc5::mma_bf16(den, wa, ones, idesc_den, 1u);
 }
 
 // two f16 values b0, b1 in [0, 255] from the pattern (0x64 b1 0x64 b0): (1024 + b) - 1024
@@ -112,24 +126,23 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   constexpr int NQ = L::NQ;
   constexpr uint32_t IDESC_S = tc5::idesc_bf16(KTILE, NQ);        // scores: 128 keys x (4 slices x 16 rows)
   constexpr uint32_t IDESC_P = tc5::idesc_f16(DP, L::NW16, true);   // PV: 128 columns x (10 digits x 16 rows)
+  constexpr uint32_t IDESC_D = tc5::idesc_f16(L::NDEN * BM, 16, false, true);   // DEN: (8 digits x 16 rows) x 16
   extern __shared__ __align__(1024) unsigned char smem_p[];
   unsigned char* Qs = smem_p;
   unsigned char* Kst = smem_p + L::k_off;
   unsigned char* Vst = smem_p + L::v_off;
   unsigned char* Wp = smem_p + L::w_off;
-  float* Wf = reinterpret_cast<float*>(smem_p + L::wf_off);
-  uint16_t* plist = reinterpret_cast<uint16_t*>(smem_p + L::ps_off);
-  __shared__ __align__(8) uint64_t kfull[NSK], kempty[NSK], sfull, sempty, vfull[NVB], vempty[NVB], wready[2], pvdone,
-      pvfree, fin;
+  __shared__ __align__(8) uint64_t kfull[NSK], kempty[NSK], sfull, sempty, vfull[NVB], vempty[NVB], wready[2],
+      pvdone[2], pvfree[2], fin;
   __shared__ uint32_t tmem_s;
   __shared__ int Fq[BM], Fv[DP];
   __shared__ unsigned char qfit[BM], qlon[BM];
   __shared__ int2 qlo[BM][NLO];
   __shared__ float mrow[BM];
   __shared__ long long denT[BM][3];
-  __shared__ uint32_t vmask[KTILE * NW];
-  __shared__ uint32_t badl[L::NBAD];
-  __shared__ int s_np[2], s_nbad[2], s_vany[2], s_zeroed;   // per tile parity
+  constexpr int NVBL = 16;   // per compute warp: keys with V elements outside their window, handled after the tiles
+  __shared__ float4 vbl_w[NCW][NVBL];
+  __shared__ int vbl_j[NCW][NVBL], vbl_n[NCW];
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -155,17 +168,19 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
       tc5::mbar_init(&vempty[s], 1);
     }
     for (int s = 0; s < 2; s++) tc5::mbar_init(&wready[s], NCW);
-    tc5::mbar_init(&sfull, 1);
+    tc5::mbar_init(&sfull, 2);   // one commit per score issuer
     tc5::mbar_init(&sempty, NCW);
-    tc5::mbar_init(&pvdone, 1);
-    tc5::mbar_init(&pvfree, NCW);
-    tc5::mbar_init(&fin, 2);   // the score issuer and the PV issuer
+    for (int s = 0; s < 2; s++) {
+      tc5::mbar_init(&pvdone[s], 1);
+      tc5::mbar_init(&pvfree[s], NCW);
+    }
+    tc5::mbar_init(&fin, 3);   // the score issuers and the PV issuer
     s_abort = 0;
     tc5::mbar_fence_init();
   }
   for (int d = tid; d < DP; d += L::THREADS)   // biased exponent in [1, 254]: |Vint| < 2^23, digit offsets in range
     Fv[d] = min(max(p.vcol[((int64_t)b * a.Hkv + hk) * DP + d], 1), 254) - 149;
-  for (int e = tid; e < DP * 16 / 2; e += L::THREADS)   // f16 1.0 pairs: DEN's all-ones A operand
+  for (int e = tid; e < 16 * 16 / 2; e += L::THREADS)   // f16 1.0 pairs: DEN's all-ones B operand
     reinterpret_cast<uint32_t*>(smem_p + L::one_off)[e] = 0x3C003C00u;
   tc5::fence_before();
   __syncthreads();
@@ -176,11 +191,10 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
   if (warp < NCW) {
 #pragma unroll
-    for (int c = 0; c < L::NPD; c++) tc5::st_zero_x4(lane_base + L::PV_COL + c * BM + rg * 4);
-#pragma unroll
-    for (int c = 0; c < NWP; c++) tc5::st_zero_x4(lane_base + L::DEN_COL + c * BM + rg * 4);
+    for (int c = 0; c < 2 * L::NPD; c++) tc5::st_zero_x4(lane_base + L::PV_COL + c * BM + rg * 4);
 #pragma unroll
     for (int c = 0; c < NDIAG; c++) tc5::st_zero_x4(lane_base + L::SC_COL + c * BM + rg * 4);
+    tc5::st_zero_x4(lane_base + L::DEN_COL + rg * 4);
     tc5::st_wait();
   }
   tc5::fence_before();
@@ -208,8 +222,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
     }
     for (int r = tid; r < BM; r += L::THREADS) mrow[r] = (q0 + r < a.Sq) ? a.m_in[rowbase + q0 + r] : 0.0f;
     for (int e = tid; e < BM * 3; e += L::THREADS) (&denT[0][0])[e] = 0;
-    if (tid < 2) { s_np[tid] = 0; s_nbad[tid] = 0; s_vany[tid] = 0; }
-    if (tid == 0) s_zeroed = 0;
+    for (int e = tid; e < NCW; e += L::THREADS) vbl_n[e] = 0;
     tc5::fence_async_smem();
     __syncthreads();
 
@@ -229,13 +242,13 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           tc5::bulk_g2s(Vst + sl * VP_BLOCK, vtc + (size_t)lb * VP_BLOCK, VP_BLOCK, &vfull[sl]);
         }
       }
-    } else if (warp == L::SISS) {   // ---------------- score MMAs ----------------
+    } else if (warp == L::SISS || warp == L::SISS2) {   // ---------------- score MMAs: steps ii, ii + 2, ... ----------------
       if (lane == 0)
-        for (int ls = 0; ls < nkt * NDS && !s_abort; ls++) {
+        for (int ls = warp == L::SISS ? 0 : 1; ls < nkt * NDS && !s_abort; ls += 2) {
           const uint32_t g = tc * NDS + ls, st = g % NSK, tt = tc + ls / NDS;
           const int k = ls % NDS;
           if (!tc5::mbar_wait(&kfull[st], (g / NSK) & 1, &s_abort, 32)) break;
-          if (k == 0 && tt >= 1 && !tc5::mbar_wait(&sempty, (tt - 1) & 1, &s_abort, 64)) break;
+          if (k < 2 && tt >= 1 && !tc5::mbar_wait(&sempty, (tt - 1) & 1, &s_abort, 64)) break;
           tc5::fence_after();
           const uint64_t ka = tc5::desc(tc5::smem_addr(Kst + st * KT_BLOCK));
           const uint64_t qa = tc5::desc(tc5::smem_addr(Qs + k * L::q_step));
@@ -243,24 +256,26 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           for (int sa = 0; sa < NSLICE; sa++)   // descriptor start addresses advance in 16-byte units
             tc5::mma_bf16(tmem + L::SC_COL + sa * BM, ka + (uint64_t)(sa * KTILE * 2), qa, IDESC_S, 1u);
           tc5::commit(&kempty[st]);
-          if (k == NDS - 1) tc5::commit(&sfull);
+          if (k >= NDS - 2) tc5::commit(&sfull);   // this issuer's last step of the tile
         }
     } else if (warp == L::PISS) {   // ---------------- PV and DEN MMAs ----------------
       if (lane == 0) {
         const uint64_t ones = tc5::desc(tc5::smem_addr(smem_p + L::one_off));
+        tc5::fence_after();   // the DEN accumulators were zeroed before the pass barrier
         for (int t = 0; t < nkt && !s_abort; t++) {
           const uint32_t tt = tc + t, bsel = tt & 1;
           if (!tc5::mbar_wait(&wready[bsel], (tt >> 1) & 1, &s_abort, 64)) break;   // weight digits of tile tt
-          if (tt >= 1 && !tc5::mbar_wait(&pvfree, (tt - 1) & 1, &s_abort, 64)) break;   // accumulators drained
+          if (tt >= 2 && !tc5::mbar_wait(&pvfree[bsel], ((tt - 2) >> 1) & 1, &s_abort, 64)) break;   // buffer drained
           tc5::fence_after();
           for (int kb = 0; kb < NKB && !s_abort; kb++) {
             const uint32_t g = tt * NKB + kb, sl = g % NVB;
             if (!tc5::mbar_wait(&vfull[sl], (g / NVB) & 1, &s_abort, 32)) break;
             tc5::fence_after();
-            pv_block_mmas(tmem, Vst + sl * VP_BLOCK, Wp + bsel * L::w_buf + (size_t)kb * NWP * L::w_blk, ones, IDESC_P);
+            pv_block_mmas(tmem + L::PV_COL + bsel * L::PV_BUF, tmem + L::DEN_COL, Vst + sl * VP_BLOCK,
+                          Wp + bsel * L::w_buf + (size_t)kb * NWP * L::w_blk, ones, IDESC_P, IDESC_D);
             tc5::commit(&vempty[sl]);
           }
-          tc5::commit(&pvdone);
+          tc5::commit(&pvdone[bsel]);
         }
       }
     } else {   // ---------------- compute warps ----------------
@@ -287,14 +302,15 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         tc5::fence_after();
         return ok;
       };
-      // fold the PV and DEN accumulators of one tile into the integer sums, zero them, release them
+      // fold the PV accumulators of one tile into the integer digits, zero them, release them
       auto drain = [&](uint32_t tt) {
-        if (warp_wait(&pvdone, tt & 1)) {
+        const uint32_t pvb = lane_base + L::PV_COL + (tt & 1) * L::PV_BUF + rg * 4;
+        if (warp_wait(&pvdone[tt & 1], (tt >> 1) & 1)) {
 #pragma unroll
           for (int g3 = 0; g3 < 3; g3++) {   // diagonals 4 g3 .. 4 g3 + 3 -> digit g3
             float pv[4][4];
 #pragma unroll
-            for (int c = 0; c < 4; c++) tc5::ld_x4(lane_base + L::PV_COL + (4 * g3 + c) * BM + rg * 4, pv[c]);
+            for (int c = 0; c < 4; c++) tc5::ld_x4(pvb + (4 * g3 + c) * BM, pv[c]);
             tc5::ld_wait();
 #pragma unroll
             for (int r = 0; r < 4; r++) {
@@ -304,66 +320,45 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
               acc[r][g3] += s;
             }
           }
-          // DEN: this warp folds planes quarter + 4 k (every lane holds the same sums); plane
-          // s weighs 2^(8 s) = 2^(32 k + 8 quarter) in units of 2^-79
-          float dv[3][4];
 #pragma unroll
-          for (int k = 0; k < 3; k++)
-            if (quarter + 4 * k < NWP) tc5::ld_x4(lane_base + L::DEN_COL + (quarter + 4 * k) * BM + rg * 4, dv[k]);
-          tc5::ld_wait();
-          if (lane == 0)
-#pragma unroll
-            for (int k = 0; k < 3; k++)
-              if (quarter + 4 * k < NWP)
-#pragma unroll
-                for (int r = 0; r < 4; r++) {
-                  const int sv = __float2int_rn(dv[k][r]);   // < 2^15
-                  if (sv) atomicAdd((unsigned long long*)&denT[rg * 4 + r][k], (unsigned long long)sv << (8 * quarter));
-                }
-#pragma unroll
-          for (int c = 0; c < L::NPD; c++) tc5::st_zero_x4(lane_base + L::PV_COL + c * BM + rg * 4);
-#pragma unroll
-          for (int c = 0; c < NWP; c++) tc5::st_zero_x4(lane_base + L::DEN_COL + c * BM + rg * 4);
+          for (int c = 0; c < L::NPD; c++) tc5::st_zero_x4(pvb + c * BM);
           tc5::st_wait();
         }
         tc5::fence_before();
         __syncwarp();
-        if (lane == 0) tc5::mbar_arrive(&pvfree);
+        if (lane == 0) tc5::mbar_arrive(&pvfree[tt & 1]);
       };
-      // key meta of this thread's key and V-bad word tid of tile t (zeros past the range)
-      auto tile_meta = [&](int t, int& mv, uint32_t& vb) {
+      // key meta and the V-bad words of this thread's key in tile t (zeros past the range)
+      auto tile_meta = [&](int t, int& mv, uint4& vb) {
         mv = 0;
-        vb = 0u;
+        vb = make_uint4(0u, 0u, 0u, 0u);
         if (t < nkt) {
-          const int kt = a.kv_lo + t * KTILE, r = tid / NW;
-          if (kt + dcol < hi) mv = p.kmeta[krow0 + kt + dcol];
-          if (kt + r < hi) vb = p.vbad[(krow0 + kt + r) * NW + tid % NW];
+          const int j = a.kv_lo + t * KTILE + dcol;
+          if (j < hi) {
+            mv = p.kmeta[krow0 + j];
+            vb = *reinterpret_cast<const uint4*>(p.vbad + (krow0 + j) * NW);
+          }
         }
       };
+      // this pass's output rows start at zero: out-of-window products are added atomically
+      if (!a.add_into) {
+        for (int64_t e = tid; e < (int64_t)nrows * NUM_NDIG * a.D; e += NCT) numb[(int64_t)q0 * NUM_NDIG * a.D + e] = 0;
+        for (int e = tid; e < nrows * DEN_NDIG; e += NCT) denb[(int64_t)q0 * DEN_NDIG + e] = 0;
+      }
+      tc5::bar_sync(1, NCT);
       int mv_n;
-      uint32_t vb_n;
+      uint4 vb_n;
       tile_meta(0, mv_n, vb_n);
       for (int t = 0; t < nkt; t++) {
-        const int kt = a.kv_lo + t * KTILE, cp = t & 1;
+        const int kt = a.kv_lo + t * KTILE;
         const uint32_t tt = tc + t, bsel = tt & 1;
         unsigned char* wbuf = Wp + bsel * L::w_buf;
         const int j = kt + dcol;
         const bool vj = j < hi;
         const int mv = mv_n;
-        const uint32_t vb = vb_n;
+        const uint4 vb = vb_n;
         tile_meta(t + 1, mv_n, vb_n);   // the next tile's, in flight meanwhile
         const int Fk = kmeta_F(mv), kf = kmeta_fit(mv);
-        if (tid == 0) { s_np[cp ^ 1] = 0; s_nbad[cp ^ 1] = 0; s_vany[cp ^ 1] = 0; }   // the next tile's counters
-        {   // V elements outside the column window (key tid / NW, word tid % NW)
-          uint32_t m = vb;
-          vmask[tid] = m;
-          if (m) s_vany[cp] = 1;
-          while (m) {
-            const int bit = __ffs(m) - 1, slot = atomicAdd(&s_nbad[cp], 1);
-            m &= m - 1;
-            if (slot < L::NBAD) badl[slot] = ((uint32_t)(tid / NW) << 16) | (uint32_t)((tid % NW) * 32 + bit);
-          }
-        }
         // ---- score diagonals of rows 4 rg .. 4 rg + 3 against this thread's key ----
         const bool ok = warp_wait(&sfull, tt & 1);
         float v[NDIAG][4];
@@ -383,45 +378,52 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         tc5::fence_before();
         __syncwarp();
         if (lane == 0) tc5::mbar_arrive(&sempty);
-        // ---- weights ----
+        // ---- weights: one straight-line evaluation per row (the four interleave); pairs it
+        // cannot take (a row outside its window, a score outside the normal range) go to `slow` ----
         float w[4];
-        uint32_t defer = 0;
+        uint32_t slow = 0;
 #pragma unroll
         for (int e = 0; e < 4; e++) {
           const int rl = rg * 4 + e, i = q0 + rl;
-          w[e] = 0.0f;
-          if (ok && vj && i < a.Sq && (!a.causal || j <= i)) {
-            if (qfit[rl] && kf) {
-              w[e] = weight_of(__fmul_rn(a.scale32, cr32_scaled(combine_diag(v, e), Fq[rl] + Fk)), mrow[rl]);
-            } else if (qlon[rl] != LO_DEEP && kmeta_lon(mv) != KLO_DEEP) {   // truncated dot + low limbs
-              const float dot = dot_lo<DT>(combine_diag(v, e), qbase + (int64_t)i * a.qs[2], Fq[rl], qlo[rl], qlon[rl],
-                                           kbase + (int64_t)j * a.ks[2], Fk, p.klo + (krow0 + j) * NLO, kmeta_lon(mv));
-              w[e] = weight_of(__fmul_rn(a.scale32, dot), mrow[rl]);
-            } else {
-              defer |= 1u << e;   // a deep row: the general exact dot below fills this pair
-            }
-          }
+          const bool valid = ok && vj && i < a.Sq && (!a.causal || j <= i);
+          bool sp;
+          const float c = cr32_scaled_nb(combine_diag(v, e), Fq[rl] + Fk, sp);
+          float x = __fsub_rn(__fmul_rn(a.scale32, c), mrow[rl]);
+          const bool fast = valid && qfit[rl] && kf && !sp;
+          if (fast && x != x) nf |= ST_NONFINITE;
+          if (fast && x > 0.0f) viol |= ST_VIOLATION;
+          x = x != x ? neg_inf() : (x > 0.0f ? 0.0f : x);
+          const float wf = exp32_det_nb(x);
+          w[e] = fast ? wf : 0.0f;
+          if (valid && !fast) slow |= 1u << e;
         }
-        // pairs with a deep row: each thread computes its own exactly
-        if (defer) {
-          const T* krow = kbase + (int64_t)j * a.ks[2];
+        if (slow) {
 #pragma unroll
           for (int e = 0; e < 4; e++)
-            if ((defer >> e) & 1u) {
-              const int rl = rg * 4 + e;
-              const T* qrow = qbase + (int64_t)(q0 + rl) * a.qs[2];
+            if ((slow >> e) & 1u) {
+              const int rl = rg * 4 + e, i = q0 + rl;
+              const T* qrow = qbase + (int64_t)i * a.qs[2];
+              const T* krow = kbase + (int64_t)j * a.ks[2];
               float dot;
-              if (!qfit[rl] && kf)
+              if (qfit[rl] && kf) {   // a score outside the normal range: the general rounding
+                w[e] = weight_of(__fmul_rn(a.scale32, cr32_scaled(combine_diag(v, e), Fq[rl] + Fk)), mrow[rl]);
+                continue;
+              } else if (qlon[rl] != LO_DEEP && kmeta_lon(mv) != KLO_DEEP) {   // truncated dot + low limbs
+                dot = dot_lo<DT>(combine_diag(v, e), qrow, Fq[rl], qlo[rl], qlon[rl], krow, Fk, p.klo + (krow0 + j) * NLO,
+                                 kmeta_lon(mv));
+              } else if (!qfit[rl] && kf) {   // a deep row: the general exact dot
                 dot = exact_dot_lane<DT, true, false>(qrow, Fq[rl], krow, Fk, a.D);
-              else if (qfit[rl])
+              } else if (qfit[rl]) {
                 dot = exact_dot_lane<DT, false, true>(qrow, Fq[rl], krow, Fk, a.D);
-              else
+              } else {
                 dot = exact_dot_lane<DT, true, true>(qrow, Fq[rl], krow, Fk, a.D);
+              }
               w[e] = weight_of(__fmul_rn(a.scale32, dot), mrow[rl]);
             }
         }
         // ---- weight digits: W = w 2^79 = x 2^(8 b0), x < 2^32; words[e][q] = bytes 4q .. 4q + 3 of W ----
         uint32_t words[4][3];
+        uint32_t tiny = 0;   // pairs with 0 < w < 2^-56: exact atomics below
 #pragma unroll
         for (int e = 0; e < 4; e++) {
           const uint32_t wb = __float_as_uint(w[e]);   // 0 <= w <= 1
@@ -433,16 +435,20 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
             b0 = sh >> 3;
             x = ((wb & 0x7FFFFFu) | 0x800000u) << (sh & 7);
           } else if (wb != 0u) {
-            plist[atomicAdd(&s_np[cp], 1)] = (uint16_t)(dcol * BM + rg * 4 + e);   // w < 2^-56: exact atomics
+            tiny |= 1u << e;
           }
           const uint64_t y = (uint64_t)x << (8 * (b0 & 3));
           const uint32_t lo = (uint32_t)y, hw = (uint32_t)(y >> 32);
           const bool low = b0 < 4;
           words[e][0] = low ? lo : 0u;
           words[e][1] = low ? hw : lo;
-          words[e][2] = low ? 0u : hw;
+          words[e][2] = low ? 0u : hw;   // digits 8 and 9: below 2^16
         }
-        *reinterpret_cast<float4*>(Wf + dcol * BM + rg * 4) = make_float4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int e = 0; e < 4; e++) {   // DEN digits 8-9: one exact warp sum per row (32 x 2^16 < 2^21)
+          const unsigned s89 = __reduce_add_sync(0xFFFFFFFFu, words[e][2]);
+          if (lane == 0 && s89) atomicAdd((unsigned long long*)&denT[rg * 4 + e][2], (unsigned long long)s89);
+        }
         {   // plane s of this key's 4 rows: 4 f16 values, contiguous in the MN-major block (one 8-byte store)
           unsigned char* wdst = wbuf + (size_t)(dcol / VKEYS) * NWP * L::w_blk + tc5::mn_off(rg * 4, dcol % VKEYS);
 #pragma unroll
@@ -468,85 +474,128 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         if (lane == 0) tc5::mbar_arrive(&wready[bsel]);
         // ---- the previous tile's PV products are done by now (or soon): fold them in ----
         if (t >= 1) drain(tt - 1);
-        // ---- products outside the window: exact int64 atomics into the output digits ----
-        tc5::bar_sync(1, NCT);   // lists, spill counters and the float weights complete
-        if (s_np[cp] > 0 || s_vany[cp]) {
-          if (!s_zeroed) {
-            if (!a.add_into) {
-              for (int64_t e = tid; e < (int64_t)nrows * NUM_NDIG * a.D; e += NCT)
-                numb[(int64_t)q0 * NUM_NDIG * a.D + e] = 0;
-              for (int e = tid; e < nrows * DEN_NDIG; e += NCT) denb[(int64_t)q0 * DEN_NDIG + e] = 0;
-            }
-            tc5::bar_sync(1, NCT);
-            if (tid == 0) s_zeroed = 1;
-          }
-          const int np = s_np[cp];
-          for (int e = warp; e < np; e += NCW) {
-            const int cl = plist[e] / BM, rl = plist[e] % BM;
-            const int i = q0 + rl, jj = kt + cl;
-            const uint32_t wb = __float_as_uint(Wf[cl * BM + rl]);
-            const Split sw = split_f32(wb);
-            long long* nrow = numb + (int64_t)i * NUM_NDIG * a.D;
-            for (int d = lane; d < a.D; d += 32) {
-              uint32_t u = In<DT>::bits(vbase + (int64_t)jj * a.vs[2], d);
-              if (nonfinite_bits(u)) continue;
-              Split sv = split_f32(u);
-              atomic_digits_add(nrow + d, a.D, NUM_E0, (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
-            }
-            if (lane == 0) atomic_digits_add(denb + (int64_t)i * DEN_NDIG, 1, DEN_E0, sw.mant, 0, sw.lsb);
-          }
-          const int nbad = s_nbad[cp];
-          for (int it = tid; it < min(nbad, L::NBAD) * BM; it += NCT) {   // one (element, row) product each
-            const int rl = it % BM;
-            const uint32_t ent = badl[it / BM];
-            const int cl = (int)(ent >> 16), d = (int)(ent & 0xFFFFu);
-            const uint32_t wb = __float_as_uint(Wf[cl * BM + rl]);
-            if (wb == 0u || (int)(wb >> 23) < 71) continue;   // zero, or already a pair spill
-            const Split sv = split_f32(In<DT>::bits(vbase + (int64_t)(kt + cl) * a.vs[2], d));
-            const Split sw = split_f32(wb);
-            atomic_digits_add(numb + (int64_t)(q0 + rl) * NUM_NDIG * a.D + d, a.D, NUM_E0,
-                              (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
-          }
-          if (nbad > L::NBAD) {   // list overflow: the elements past it, one thread per mask word
-            for (int e = tid; e < KTILE * NW; e += NCT) {
-              uint32_t m = vmask[e];
-              const int cl = e / NW, tw = e % NW, jj = kt + cl;
-              while (m) {
-                const int bit = __ffs(m) - 1;
-                m &= m - 1;
-                const int d = tw * 32 + bit;
-                bool listed = false;
-                for (int q = 0; q < L::NBAD && !listed; q++) listed = badl[q] == (((uint32_t)cl << 16) | (uint32_t)d);
-                if (listed) continue;
-                Split sv = split_f32(In<DT>::bits(vbase + (int64_t)jj * a.vs[2], d));
-                for (int rl = 0; rl < BM; rl++) {
-                  uint32_t wb = __float_as_uint(Wf[cl * BM + rl]);
-                  if (wb == 0u || (int)(wb >> 23) < 71) continue;
-                  Split sw = split_f32(wb);
-                  atomic_digits_add(numb + (int64_t)(q0 + rl) * NUM_NDIG * a.D + d, a.D, NUM_E0,
-                                    (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
+        // ---- this warp's products outside the window: exact int64 atomics into the output digits ----
+        if (__ballot_sync(0xFFFFFFFFu, tiny != 0)) {
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            uint32_t pend = __ballot_sync(0xFFFFFFFFu, (tiny >> e) & 1u);
+            if (!pend) continue;
+            const int rl = rg * 4 + e;
+            long long* nrow = numb + (int64_t)(q0 + rl) * NUM_NDIG * a.D;
+            long long sum[NW][3];
+#pragma unroll
+            for (int c = 0; c < NW; c++) sum[c][0] = sum[c][1] = sum[c][2] = 0;
+            for (; pend; pend &= pend - 1) {
+              const int src = __ffs(pend) - 1, jj = kt + 32 * quarter + src;
+              const uint32_t wb = __float_as_uint(__shfl_sync(0xFFFFFFFFu, w[e], src));
+              const Split sw = split_f32(wb);
+              if (lane == 0) atomic_digits_add(denb + (int64_t)(q0 + rl) * DEN_NDIG, 1, DEN_E0, sw.mant, 0, sw.lsb);
+              const int ex = (int)(wb >> 23);
+              if (ex >= 15) {   // W' = w 2^135 = x 2^(8 b0): words of W' against the prepared Vint
+                const int sh = ex - 15, b0 = sh >> 3;
+                const uint64_t y = (uint64_t)(((wb & 0x7FFFFFu) | 0x800000u) << (sh & 7)) << (8 * (b0 & 3));
+                const bool low = b0 < 4;
+                const long long w0 = low ? (long long)(uint32_t)y : 0, w1 = low ? (long long)(y >> 32) : (long long)(uint32_t)y,
+                                w2 = low ? 0 : (long long)(y >> 32);
+                const int* vrow = p.vint + (krow0 + jj) * DP;
+#pragma unroll
+                for (int c = 0; c < NW; c++) {   // |Vint| < 2^23, words < 2^32: 32 products stay below 2^60
+                  const long long vi = vrow[lane + 32 * c];
+                  sum[c][0] += vi * w0;
+                  sum[c][1] += vi * w1;
+                  sum[c][2] += vi * w2;
+                }
+              } else {   // w < 2^-112: the whole product w V_jd for every d
+                for (int d = lane; d < a.D; d += 32) {
+                  const uint32_t u = In<DT>::bits(vbase + (int64_t)jj * a.vs[2], d);
+                  if (nonfinite_bits(u)) continue;
+                  const Split sv = split_f32(u);
+                  atomic_digits_add(nrow + d, a.D, NUM_E0, (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
                 }
               }
             }
-          }
-        }
-        if ((t & 1023) == 1023) {   // carry the lower digits up
 #pragma unroll
-          for (int r = 0; r < 4; r++) {
-            long long c0 = acc[r][0] >> 32;
-            acc[r][0] -= c0 * (1ll << 32);
-            acc[r][1] += c0;
-            long long c1 = acc[r][1] >> 32;
-            acc[r][1] -= c1 * (1ll << 32);
-            acc[r][2] += c1;
+            for (int c = 0; c < NW; c++) {
+              const int d = lane + 32 * c;
+              if (d < a.D)
+#pragma unroll
+                for (int q = 0; q < 3; q++)
+                  if (sum[c][q] != 0)
+                    atomic_digits_add(nrow + d, a.D, NUM_E0,
+                                      sum[c][q] < 0 ? 0ull - (unsigned long long)sum[c][q] : (unsigned long long)sum[c][q],
+                                      sum[c][q] < 0, Fv[d] - 135 + 32 * q);
+            }
           }
         }
-        tc5::bar_sync(1, NCT);   // tile consumed: float weights, lists and V masks are free
+        {   // keys with V elements outside their column window: listed, their products added after the tiles
+          const bool bad = (vb.x | vb.y | vb.z | vb.w) != 0u && (w[0] != 0.0f || w[1] != 0.0f || w[2] != 0.0f || w[3] != 0.0f);
+          const uint32_t bm = __ballot_sync(0xFFFFFFFFu, bad);
+          if (bm) {
+            const int base = vbl_n[warp];
+            const int idx = base + __popc(bm & ((1u << lane) - 1u));
+            if (bad && idx < NVBL) {
+              vbl_w[warp][idx] = make_float4(w[0], w[1], w[2], w[3]);
+              vbl_j[warp][idx] = j;
+            }
+            __syncwarp();
+            if (lane == 0) vbl_n[warp] = base + __popc(bm);
+            if (bad && idx >= NVBL) {   // list full: this lane adds its products now
+              const uint32_t vw[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+              for (int tw = 0; tw < NW; tw++)
+                for (uint32_t m = vw[tw]; m; m &= m - 1) {
+                  const int d = tw * 32 + __ffs(m) - 1;
+                  const Split sv = split_f32(In<DT>::bits(vbase + (int64_t)j * a.vs[2], d));
+#pragma unroll
+                  for (int e = 0; e < 4; e++) {
+                    const uint32_t wb = __float_as_uint(w[e]);
+                    if (wb == 0u || (int)(wb >> 23) < 15) continue;   // zero, or a whole-product pair above
+                    const Split sw = split_f32(wb);
+                    atomic_digits_add(numb + (int64_t)(q0 + rg * 4 + e) * NUM_NDIG * a.D + d, a.D, NUM_E0,
+                                      (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
+                  }
+                }
+            }
+            __syncwarp();
+          }
+        }
       }
       if (nkt > 0) drain(tc + nkt - 1);
+      for (int li = 0; li < min(vbl_n[warp], NVBL); li++) {   // listed keys: products of their V elements below the window
+        const int jj = vbl_j[warp][li];
+        const float4 wl = vbl_w[warp][li];
+        const float wr[4] = {wl.x, wl.y, wl.z, wl.w};
+        const uint32_t* vbr = p.vbad + (krow0 + jj) * NW;
+        for (int tw = 0; tw < NW; tw++)
+          for (uint32_t m = vbr[tw]; m; m &= m - 1) {
+            const int d = tw * 32 + __ffs(m) - 1;
+            if (lane < 4) {
+              const uint32_t wb = __float_as_uint(wr[lane]);
+              if (wb != 0u && (int)(wb >> 23) >= 15) {   // smaller weights took whole products
+                const Split sv = split_f32(In<DT>::bits(vbase + (int64_t)jj * a.vs[2], d));
+                const Split sw = split_f32(wb);
+                atomic_digits_add(numb + (int64_t)(q0 + rg * 4 + lane) * NUM_NDIG * a.D + d, a.D, NUM_E0,
+                                  (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
+              }
+            }
+          }
+      }
+      // ---- DEN digits 0-7 from TMEM (lane 16 s + row; every column holds the same sum) ----
+      if (rg == 0) {
+        if (nkt > 0) {
+          const float dsum = tc5::ld_x1(lane_base + L::DEN_COL);
+          tc5::ld_wait();
+          const int sv = __float2int_rn(dsum);   // < 2^24
+          const int s = 2 * quarter + (lane >> 4), rl = lane & 15;
+          if (sv) atomicAdd((unsigned long long*)&denT[rl][s >> 2], (unsigned long long)sv << (8 * (s & 3)));
+          tc5::st_zero_x8(lane_base + L::DEN_COL);
+          tc5::st_zero_x8(lane_base + L::DEN_COL + 8);
+          tc5::st_wait();
+        }
+        tc5::fence_before();
+      }
       // ---- epilogue: canonical digits ----
-      tc5::bar_sync(1, NCT);   // denT and every spill atomic complete
-      const bool rmw = a.add_into || s_zeroed;
+      tc5::bar_sync(1, NCT);   // denT and every atomic of this pass complete
       const int d = dcol;
 #pragma unroll
       for (int r = 0; r < 4; r++) {
@@ -555,10 +604,9 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         long long* nrow = numb + (int64_t)i * NUM_NDIG * a.D;
         long long dg[NUM_NDIG + 3];
 #pragma unroll
-        for (int k = 0; k < NUM_NDIG + 3; k++) dg[k] = 0;
-        if (rmw)
+        for (int k = 0; k < NUM_NDIG; k++) dg[k] = __ldcg(nrow + (int64_t)k * a.D + d);
 #pragma unroll
-          for (int k = 0; k < NUM_NDIG; k++) dg[k] = __ldcg(nrow + (int64_t)k * a.D + d);
+        for (int k = NUM_NDIG; k < NUM_NDIG + 3; k++) dg[k] = 0;
         const int off = Fv[d] - 79 - NUM_E0;   // bit position of the accumulator's unit
         add_i64_at_tp(dg, acc[r][0], off);
         add_i64_at_tp(dg, acc[r][1], off + 32);
@@ -579,10 +627,9 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         long long* drow = denb + (int64_t)(q0 + rl) * DEN_NDIG;
         long long dg[DEN_NDIG + 3];
 #pragma unroll
-        for (int k = 0; k < DEN_NDIG + 3; k++) dg[k] = 0;
-        if (rmw)
+        for (int k = 0; k < DEN_NDIG; k++) dg[k] = __ldcg(drow + k);
 #pragma unroll
-          for (int k = 0; k < DEN_NDIG; k++) dg[k] = __ldcg(drow + k);
+        for (int k = DEN_NDIG; k < DEN_NDIG + 3; k++) dg[k] = 0;
         const int off = -79 - DEN_E0;   // W units
         add_i64_at_tp(dg, denT[rl][0], off);
         add_i64_at_tp(dg, denT[rl][1], off + 32);
@@ -603,7 +650,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
     tc += nkt;
     __syncthreads();
   }   // pass
-  if ((warp == L::SISS || warp == L::PISS) && lane == 0) {   // every MMA has completed before TMEM is released
+  if ((warp == L::SISS || warp == L::PISS || warp == L::SISS2) && lane == 0) {   // every MMA has completed before TMEM is released
     tc5::commit(&fin);
     tc5::mbar_wait(&fin, 0, &s_abort);
   }

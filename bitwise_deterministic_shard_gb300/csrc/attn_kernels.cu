@@ -68,10 +68,11 @@ __device__ __forceinline__ void load_k_tile(const KvPrep& p, int64_t rowbase, in
 // from above.  A pair whose bound does not exceed the row's running maximum (an exact score
 // already found for that row, shared in shared memory after every key tile) cannot change
 // the row maximum and skips the exact rounding;
-// all others take the exact path (int64 dot, cr32_scaled).  A pair outside the 26-bit
-// window is computed by its warp with the exact two-limb warp dot.  Every mbarrier wait is
-// bounded; a wait that gives up sets DA_STATUS_TIMEOUT and the CTA winds down, freeing its
-// TMEM.
+// all others take the exact path (int64 dot, cr32_scaled).  A pair with a row outside the
+// 26-bit window adds that row's few low limbs to the truncated dot (dot_lo, score_tc.cuh);
+// a pair with a deep row is computed by its warp with the exact two-limb warp dot.  Every
+// mbarrier wait is bounded; a wait that gives up sets DA_STATUS_TIMEOUT and the CTA winds
+// down, freeing its TMEM.
 // =======================================================================================
 template <int DP>
 struct RowmaxTcLayout {

@@ -56,7 +56,7 @@ cudaError_t launch_rowmax(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
 cudaError_t launch_accumulate(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
 cudaError_t launch_accumulate_tc(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // D <= 128
 cudaError_t launch_accumulate_tp(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // 64 < D <= 128
-constexpr int ACC_TP_MAX_TILES = 4096;   // key tiles per pass the tensor-PV kernel's state holds exactly
+constexpr int ACC_TP_MAX_TILES = 512;   // key tiles per pass the tensor-PV kernel's state holds exactly
 
 cudaError_t launch_compose_max(float* dst, const float* src, int64_t n, cudaStream_t st);
 cudaError_t launch_compose_add(long long* dst, const long long* src, int64_t n, cudaStream_t st);

@@ -78,6 +78,33 @@ __device__ __forceinline__ float exp32_det(float x) {
   return __fmul_rn(__fmul_rn(p, __uint_as_float((uint32_t)(k + 64 + 127) << 23)), 0x1p-64f);
 }
 
+// exp32_det without branches, for x <= 0 or x = -inf (not NaN): the same operations in the
+// same order as exp32_det, the special cases taken by selects, so the caller's independent
+// evaluations can interleave.
+__device__ __forceinline__ float exp32_det_nb(float x) {
+  const bool under = x < -104.0f;
+  const float xx = under ? 0.0f : x;
+  const float L2E = 0x1.715476p+0f, C1 = 0x1.62e4p-1f, C2 = 0x1.7f7d1cp-20f, MAGIC = 12582912.0f;
+  const float t = __fmul_rn(xx, L2E);
+  const float tr = __fadd_rn(t, MAGIC);
+  const int k = __float_as_int(tr) - 0x4B400000;
+  const float kf = __fsub_rn(tr, MAGIC);
+  const float r1 = __fmaf_rn(-kf, C1, xx);
+  const float r = __fmaf_rn(-kf, C2, r1);
+  float p = 0x1.a01a02p-13f;
+  p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);
+  p = __fmaf_rn(p, r, 0x1.111112p-7f);
+  p = __fmaf_rn(p, r, 0x1.555556p-5f);
+  p = __fmaf_rn(p, r, 0x1.555556p-3f);
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  const bool sub = k < -126;
+  const float res = __fmul_rn(p, __uint_as_float((uint32_t)(k + (sub ? 64 : 0) + 127) << 23));
+  const float out = sub ? __fmul_rn(res, 0x1p-64f) : res;
+  return under ? 0.0f : out;
+}
+
 // exact small-integer <-> binary32 conversions on the FP32/integer pipes (|v| <= 2^22)
 __device__ __forceinline__ int small_f2i(float f) { return __float_as_int(__fadd_rn(f, 12582912.0f)) - 0x4B400000; }
 __device__ __forceinline__ float small_i2f(int v) { return __fsub_rn(__int_as_float(0x4B400000 + v), 12582912.0f); }
@@ -149,6 +176,26 @@ __device__ __forceinline__ float cr32_scaled(long long T, int F) {
     bitsv = be >= 255 ? 0x7F800000u : (((uint32_t)be << 23) | ((uint32_t)n & 0x7FFFFFu));
   }
   return __uint_as_float(bitsv | (neg ? 0x80000000u : 0u));
+}
+
+// cr32_scaled without branches for results in the normal binary32 range: the top 24 bits of
+// |T| rounded to nearest-even on the round bit and the sticky bits below it.  *special is set
+// (and the result is meaningless) when T 2^F is nonzero and subnormal or beyond the largest
+// exponent; the caller then takes cr32_scaled.
+__device__ __forceinline__ float cr32_scaled_nb(long long T, int F, bool& special) {
+  const bool neg = T < 0;
+  const unsigned long long mag = neg ? 0ull - (unsigned long long)T : (unsigned long long)T;
+  const int lz = __clzll((long long)mag);   // 64 for T == 0
+  const int e = 63 - lz + F;                // 2^e <= |value| < 2^(e+1)
+  special = mag != 0ull && (e < -126 || e > 127);
+  const unsigned long long nrm = mag << (lz & 63);
+  const uint32_t hi = (uint32_t)(nrm >> 32), lo = (uint32_t)nrm;
+  uint32_t m = hi >> 8;   // 24 bits
+  const uint32_t rb = (hi >> 7) & 1u, st = ((hi & 0x7Fu) | lo) != 0u ? 1u : 0u;
+  m += rb & (st | (m & 1u));
+  const uint32_t carry = m >> 24;   // rounded up to 2^24
+  const uint32_t bitsv = ((uint32_t)(e + 127 + (int)carry) << 23) | ((m >> carry) & 0x7FFFFFu) | (neg ? 0x80000000u : 0u);
+  return mag == 0ull ? 0.0f : __uint_as_float(bitsv);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -317,14 +364,24 @@ __device__ __noinline__ float exact_dot_lane(const typename In<DT>::T* q, int Fq
                                              int D) {
   long long shh = 0, shl = 0, slh = 0, sll = 0;
   bool ok = true;
-  for (int d = 0; d < D; d++) {
-    int qh, ql, kh, kl;
-    ok &= limbs52(In<DT>::bits(q, d), Fq - 26, qh, ql);
-    ok &= limbs52(In<DT>::bits(k, d), Fk - 26, kh, kl);
-    shh += (long long)qh * kh;
-    if (KLO) shl += (long long)qh * kl;
-    if (QLO) slh += (long long)ql * kh;
-    if (QLO && KLO) sll += (long long)ql * kl;
+  constexpr int U = 16;   // elements loaded before any is used: the loads overlap
+  for (int d0 = 0; d0 < D; d0 += U) {
+    uint32_t qb[U], kb[U];
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      qb[u] = d0 + u < D ? In<DT>::bits(q, d0 + u) : 0u;
+      kb[u] = d0 + u < D ? In<DT>::bits(k, d0 + u) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      int qh, ql, kh, kl;
+      ok &= limbs52(qb[u], Fq - 26, qh, ql);
+      ok &= limbs52(kb[u], Fk - 26, kh, kl);
+      shh += (long long)qh * kh;
+      if (KLO) shl += (long long)qh * kl;
+      if (QLO) slh += (long long)ql * kh;
+      if (QLO && KLO) sll += (long long)ql * kl;
+    }
   }
   if (!ok) return exact_dot_slow<DT>(q, k, D);
   const __int128 T = (__int128)shh * ((__int128)1 << 52) + (__int128)(shl + slh) * (1ll << 26) + (__int128)sll;

@@ -42,9 +42,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn = fals
   return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn ? (1u << 16) : 0u) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(m >> 4) << 24);
 }
-// the same with f16 A and B
-__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool b_mn = false) {
-  return (1u << 4) | (b_mn ? (1u << 16) : 0u) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+// the same with f16 A and B (a_mn: A MN-major, the same core-matrix layout as an MN-major B)
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool b_mn = false, bool a_mn = false) {
+  return (1u << 4) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -145,6 +146,12 @@ __device__ __forceinline__ void ld_x2(uint32_t taddr, float& v0, float& v1) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(taddr));
   v0 = __uint_as_float(r0);
   v1 = __uint_as_float(r1);
+}
+// one 32-bit column of this thread's TMEM lane
+__device__ __forceinline__ float ld_x1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  return __uint_as_float(r);
 }
 // 4 consecutive 32-bit columns of this thread's TMEM lane
 __device__ __forceinline__ void ld_x4(uint32_t taddr, float (&v)[4]) {
