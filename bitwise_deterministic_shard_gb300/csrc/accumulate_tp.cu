@@ -34,19 +34,20 @@
 // 255 per key, so they stay exact for ACC_TP_MAX_TILES tiles and are read once per pass.
 // Digits 8-9 (below 2^16 per key) are summed with one warp reduction per row.
 //
-// Products outside the window are added with exact int64 atomics into the output digits by
-// the warp that owns the pair, so the compute warps share no per-tile state and never wait
-// for each other within a pass; the output rows are cleared when the pass starts and the
-// epilogue adds onto them.  Weights 2^-112 <= w < 2^-56 are integers W' = w 2^135 < 2^79:
+// Products outside the window are added with exact int64 atomics by the warp that owns the
+// pair, so the compute warps share no per-tile state and never wait for each other within a
+// pass.  They go to this SM's spill slot (attn_kernels.h), not to the output: the epilogue
+// adds the slot digits the pass touched (a bitmap in shared memory) and clears them, so every
+// output digit is written exactly once.  Weights 2^-112 <= w < 2^-56 are integers W' = w 2^135 < 2^79:
 // per row, the warp sums W' Vint over its keys exactly (three 32-bit words of W') and adds
 // the sums, so a row costs twelve atomics per lane and tile however many such weights it
 // has.  V elements below their column window (Vint = 0 there) are kept in a per-warp list of
 // (key, the four weights) and their products added after the tiles; smaller weights take
 // whole-product atomics.
 //
-// Roles: warp 16 copies (lane 0: key operand steps, 4-stage ring; lane 1: V digit blocks,
-// NVB-stage ring), warps 17 and 19 (lane 0) issue the score MMAs of alternate steps, warp 18
-// lane 0 the PV and DEN MMAs.  Warps 0-15 read the score diagonals, compute weights, write the weight digit
+// Roles (lane 0 of each control warp): warp 16 copies key operand steps (4-stage ring), warp
+// 17 issues the score MMAs, warp 18 the PV and DEN MMAs, warp 19 copies V digit blocks
+// (NVB-stage ring).  Warps 0-15 read the score diagonals, compute weights, write the weight digit
 // planes and drain the PV accumulators; each zeroes the TMEM it read before releasing it,
 // so every MMA accumulates.  Every mbarrier wait is bounded; one that gives up sets
 // DA_STATUS_TIMEOUT, and a failed wait in the compute warps only skips work.
@@ -59,9 +60,9 @@ namespace detattn {
 
 struct AccTpLayout {
   static constexpr int DP = 128, BM = 16, NDS = DP / 16, NSK = 4, NVB = 4, NCW = 16;
-  // warps: NCW compute, the loader, score issuer 0, the PV issuer, score issuer 1 (the two
-  // score issuers take alternate 16-dimension steps and sit on different SM sub-partitions)
-  static constexpr int LOADW = NCW, SISS = NCW + 1, PISS = NCW + 2, SISS2 = NCW + 3, THREADS = 32 * (NCW + 4);
+  // warps: NCW compute (four warpgroups) and the control warpgroup: key copies, score MMAs,
+  // PV and DEN MMAs, V copies (lane 0 of each)
+  static constexpr int LOADW = NCW, ISSW = NCW + 1, PISSW = NCW + 2, VLOADW = NCW + 3, THREADS = 32 * (NCW + 4);
   static constexpr int NWP = 10, NVP = 3, NPD = NWP + NVP - 1, NKB = KTILE / VKEYS;
   static constexpr int NQ = NSLICE * BM;                              // score MMA N: the stacked query slices
   static constexpr int NW16 = NWP * BM;                               // PV MMA N: the stacked weight digits
@@ -104,16 +105,39 @@ __device__ __forceinline__ uint32_t f16_pair_from_biased(uint32_t h) {
   return r;
 }
 
-__device__ __forceinline__ void add_i64_at_tp(long long* dg, long long X, int o) {
-  unsigned long long lo = (unsigned long long)X & 0xFFFFFFFFull;
-  long long hi = X >> 32;
-  int k = o >> 5, r = o & 31;
-  unsigned long long u = lo << r;
-  dg[k] += (long long)(u & 0xFFFFFFFFull);
-  dg[k + 1] += (long long)(u >> 32);
-  long long v = hi * (1ll << r);
-  dg[k + 1] += (long long)((unsigned long long)v & 0xFFFFFFFFull);
-  dg[k + 2] += v >> 32;
+// dg[k] (radix 2^32, int64 with lazy carries) += the digits of sign * M * 2^off, for every k
+// with a static index (the digit arrays stay in registers): digit k takes bits
+// [32 k - off, 32 k - off + 32) of M.
+template <int N>
+__device__ __forceinline__ void add_u128_at(long long (&dg)[N], unsigned __int128 M, bool neg, int off) {
+#pragma unroll
+  for (int k = 0; k < N; k++) {
+    const int sh = 32 * k - off;
+    unsigned long long c = 0;
+    if (sh >= 0 && sh < 128)
+      c = (unsigned long long)(M >> sh) & 0xFFFFFFFFull;
+    else if (sh < 0 && sh > -32)
+      c = (unsigned long long)(M << (-sh)) & 0xFFFFFFFFull;
+    dg[k] += neg ? -(long long)c : (long long)c;
+  }
+}
+
+// the signed radix-2^32 digits d0 + d1 2^32 + d2 2^64 (each |d| < 2^62) as sign and magnitude
+__device__ __forceinline__ void digits3_to_u128(long long d0, long long d1, long long d2, unsigned __int128& M, bool& neg) {
+  const __int128 X = (__int128)d0 + ((__int128)d1 << 32) + ((__int128)d2 << 64);
+  neg = X < 0;
+  M = neg ? (unsigned __int128)(-X) : (unsigned __int128)X;
+}
+
+// carry-normalize radix-2^32 digits with static indices: 0 .. N - 2 in [0, 2^32), the top signed
+template <int N>
+__device__ __forceinline__ void carry_digits(long long (&dg)[N]) {
+#pragma unroll
+  for (int k = 0; k < N - 1; k++) {
+    const long long c = dg[k] >> 32;
+    dg[k] -= c * 4294967296ll;
+    dg[k + 1] += c;
+  }
 }
 
 template <int DT>
@@ -143,19 +167,42 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   constexpr int NVBL = 16;   // per compute warp: keys with V elements outside their window, handled after the tiles
   __shared__ float4 vbl_w[NCW][NVBL];
   __shared__ int vbl_j[NCW][NVBL], vbl_n[NCW];
+  __shared__ uint32_t tbit[BM][NW];   // spill slot digits touched this pass: single columns, whole rows, DEN
+  __shared__ int trow[BM], tden[BM];
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.y, b = blockIdx.z, hk = h / (a.Hq / a.Hkv);
-  const T* qbase = (const T*)a.q + b * a.qs[0] + h * a.qs[1];
-  const T* kbase = (const T*)a.k + b * a.ks[0] + hk * a.ks[1];
-  const T* vbase = (const T*)a.v + b * a.vs[0] + hk * a.vs[1];
+  // Row, output and spill-slot addresses are recomputed where they are used (the block
+  // indices read through volatile moves, which the compiler does not hoist), so the compute
+  // warps do not hold them in registers across the tile loop.
+  auto cta_y = []() {
+    uint32_t v;
+    asm volatile("mov.u32 %0, %%ctaid.y;" : "=r"(v));
+    return (int64_t)v;
+  };
+  auto cta_z = []() {
+    uint32_t v;
+    asm volatile("mov.u32 %0, %%ctaid.z;" : "=r"(v));
+    return (int64_t)v;
+  };
+  auto qrow = [&](int i) { return (const T*)a.q + cta_z() * a.qs[0] + cta_y() * a.qs[1] + (int64_t)i * a.qs[2]; };
+  auto krow = [&](int j) {
+    return (const T*)a.k + cta_z() * a.ks[0] + (cta_y() / (a.Hq / a.Hkv)) * a.ks[1] + (int64_t)j * a.ks[2];
+  };
+  auto vrow = [&](int j) {
+    return (const T*)a.v + cta_z() * a.vs[0] + (cta_y() / (a.Hq / a.Hkv)) * a.vs[1] + (int64_t)j * a.vs[2];
+  };
+  auto out_row = [&](int i) { return (cta_z() * a.Hq + cta_y()) * a.Sq + i; };   // output row index
+  auto slot_num = [&](int rl) {   // this SM's spill slot: NUM digits of row rl, [15][DP]
+    uint32_t sm;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    return p.spill + (size_t)(sm < (uint32_t)SPILL_SLOTS ? sm : 0) * spill_slot_words(DP) + (size_t)rl * NUM_NDIG * DP;
+  };
+  auto slot_den = [&](int rl) { return slot_num(BM) + (size_t)rl * DEN_NDIG; };
   const int64_t krow0 = ((int64_t)b * a.Hkv + hk) * a.Skv;
   const unsigned char* ktc = p.ktc + (int64_t)(b * a.Hkv + hk) * p.ntk * NDS * KT_BLOCK;
   const unsigned char* vtc = p.vtc + (int64_t)(b * a.Hkv + hk) * p.ntk * NKB * VP_BLOCK;
-  const int64_t rowbase = ((int64_t)b * a.Hq + h) * a.Sq;
-  long long* numb = a.num + rowbase * NUM_NDIG * a.D;
-  long long* denb = a.den + rowbase * DEN_NDIG;
 
   if (warp == 0) tc5::tmem_alloc(&tmem_s, L::TCOLS);
   if (tid == 0) {
@@ -168,13 +215,13 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
       tc5::mbar_init(&vempty[s], 1);
     }
     for (int s = 0; s < 2; s++) tc5::mbar_init(&wready[s], NCW);
-    tc5::mbar_init(&sfull, 2);   // one commit per score issuer
+    tc5::mbar_init(&sfull, 1);
     tc5::mbar_init(&sempty, NCW);
     for (int s = 0; s < 2; s++) {
       tc5::mbar_init(&pvdone[s], 1);
       tc5::mbar_init(&pvfree[s], NCW);
     }
-    tc5::mbar_init(&fin, 3);   // the score issuers and the PV issuer
+    tc5::mbar_init(&fin, 2);   // the score issuer and the PV issuer
     s_abort = 0;
     tc5::mbar_fence_init();
   }
@@ -202,457 +249,506 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   tc5::fence_after();
 
   int nf = 0, viol = 0;
-  uint32_t tc = 0;   // key tiles of earlier passes
   const int ntq = (a.Sq + BM - 1) / BM;
   const int npass = (a.causal && (int)blockIdx.x != ntq - 1 - (int)blockIdx.x) ? 2 : 1;
-  for (int pass = 0; pass < npass; pass++) {
-    const int q0 = (pass == 0 ? ntq - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
-    const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
-    const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
-    const int nrows = min(BM, a.Sq - q0);
-    // ---- per pass: query slices (resident B operand of the scores), row maxima, cleared sums ----
-    for (int r = warp; r < BM; r += L::THREADS / 32) {
-      const int i = q0 + r;
-      row_slices<DT, DP>(
-          i < a.Sq ? qbase + (int64_t)i * a.qs[2] : nullptr, a.D,
-          [&](int q, int d, uint16_t v) {
-            *reinterpret_cast<uint16_t*>(Qs + (d >> 4) * L::q_step + tc5::canon_off(q * BM + r, d & 15)) = v;
-          },
-          &Fq[r], &qfit[r], nf, lane, qlo[r], &qlon[r]);
-    }
-    for (int r = tid; r < BM; r += L::THREADS) mrow[r] = (q0 + r < a.Sq) ? a.m_in[rowbase + q0 + r] : 0.0f;
-    for (int e = tid; e < BM * 3; e += L::THREADS) (&denT[0][0])[e] = 0;
-    for (int e = tid; e < NCW; e += L::THREADS) vbl_n[e] = 0;
-    tc5::fence_async_smem();
-    __syncthreads();
-
-    if (warp == L::LOADW) {   // ---------------- bulk copies ----------------
-      if (lane == 0) {   // key operand steps
-        for (int ls = 0; ls < nkt * NDS && !s_abort; ls++) {
-          const uint32_t g = tc * NDS + ls, st = g % NSK;
-          if (g >= NSK && !tc5::mbar_wait(&kempty[st], ((g / NSK) - 1) & 1, &s_abort, 64)) break;
-          tc5::mbar_expect_tx(&kfull[st], KT_BLOCK);
-          tc5::bulk_g2s(Kst + st * KT_BLOCK, ktc + (size_t)ls * KT_BLOCK, KT_BLOCK, &kfull[st]);
+  // Register split: the control warpgroup (copies, MMA issue) runs on 32 registers a thread,
+  // the four compute warpgroups on 112 (640 x 96 at launch = 128 x 32 + 512 x 112).  Each
+  // role runs its own pass loop; named barrier 2 opens a pass (query operand and per-pass
+  // state ready), barrier 3 closes it.
+  if (warp >= NCW) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 32;" ::: "memory");
+    uint32_t tc = 0;   // key tiles of earlier passes
+    for (int pass = 0; pass < npass; pass++) {
+      const int q0 = (pass == 0 ? ntq - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
+      const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
+      const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
+      tc5::bar_sync(2, L::THREADS);
+      if (warp == L::LOADW || warp == L::VLOADW) {   // ---------------- bulk copies ----------------
+        if (warp == L::LOADW && lane == 0) {   // key operand steps
+          for (int ls = 0; ls < nkt * NDS && !s_abort; ls++) {
+            const uint32_t g = tc * NDS + ls, st = g % NSK;
+            if (g >= NSK && !tc5::mbar_wait(&kempty[st], ((g / NSK) - 1) & 1, &s_abort, 64)) break;
+            tc5::mbar_expect_tx(&kfull[st], KT_BLOCK);
+            tc5::bulk_g2s(Kst + st * KT_BLOCK, ktc + (size_t)ls * KT_BLOCK, KT_BLOCK, &kfull[st]);
+          }
+        } else if (warp == L::VLOADW && lane == 0) {   // V digit blocks
+          for (int lb = 0; lb < nkt * NKB && !s_abort; lb++) {
+            const uint32_t g = tc * NKB + lb, sl = g % NVB;
+            if (g >= NVB && !tc5::mbar_wait(&vempty[sl], ((g / NVB) - 1) & 1, &s_abort, 64)) break;
+            tc5::mbar_expect_tx(&vfull[sl], VP_BLOCK);
+            tc5::bulk_g2s(Vst + sl * VP_BLOCK, vtc + (size_t)lb * VP_BLOCK, VP_BLOCK, &vfull[sl]);
+          }
         }
-      } else if (lane == 1) {   // V digit blocks
-        for (int lb = 0; lb < nkt * NKB && !s_abort; lb++) {
-          const uint32_t g = tc * NKB + lb, sl = g % NVB;
-          if (g >= NVB && !tc5::mbar_wait(&vempty[sl], ((g / NVB) - 1) & 1, &s_abort, 64)) break;
-          tc5::mbar_expect_tx(&vfull[sl], VP_BLOCK);
-          tc5::bulk_g2s(Vst + sl * VP_BLOCK, vtc + (size_t)lb * VP_BLOCK, VP_BLOCK, &vfull[sl]);
-        }
-      }
-    } else if (warp == L::SISS || warp == L::SISS2) {   // ---------------- score MMAs: steps ii, ii + 2, ... ----------------
-      if (lane == 0)
-        for (int ls = warp == L::SISS ? 0 : 1; ls < nkt * NDS && !s_abort; ls += 2) {
-          const uint32_t g = tc * NDS + ls, st = g % NSK, tt = tc + ls / NDS;
-          const int k = ls % NDS;
-          if (!tc5::mbar_wait(&kfull[st], (g / NSK) & 1, &s_abort, 32)) break;
-          if (k < 2 && tt >= 1 && !tc5::mbar_wait(&sempty, (tt - 1) & 1, &s_abort, 64)) break;
-          tc5::fence_after();
-          const uint64_t ka = tc5::desc(tc5::smem_addr(Kst + st * KT_BLOCK));
-          const uint64_t qa = tc5::desc(tc5::smem_addr(Qs + k * L::q_step));
-#pragma unroll
-          for (int sa = 0; sa < NSLICE; sa++)   // descriptor start addresses advance in 16-byte units
-            tc5::mma_bf16(tmem + L::SC_COL + sa * BM, ka + (uint64_t)(sa * KTILE * 2), qa, IDESC_S, 1u);
-          tc5::commit(&kempty[st]);
-          if (k >= NDS - 2) tc5::commit(&sfull);   // this issuer's last step of the tile
-        }
-    } else if (warp == L::PISS) {   // ---------------- PV and DEN MMAs ----------------
-      if (lane == 0) {
-        const uint64_t ones = tc5::desc(tc5::smem_addr(smem_p + L::one_off));
-        tc5::fence_after();   // the DEN accumulators were zeroed before the pass barrier
-        for (int t = 0; t < nkt && !s_abort; t++) {
-          const uint32_t tt = tc + t, bsel = tt & 1;
-          if (!tc5::mbar_wait(&wready[bsel], (tt >> 1) & 1, &s_abort, 64)) break;   // weight digits of tile tt
-          if (tt >= 2 && !tc5::mbar_wait(&pvfree[bsel], ((tt - 2) >> 1) & 1, &s_abort, 64)) break;   // buffer drained
-          tc5::fence_after();
-          for (int kb = 0; kb < NKB && !s_abort; kb++) {
-            const uint32_t g = tt * NKB + kb, sl = g % NVB;
-            if (!tc5::mbar_wait(&vfull[sl], (g / NVB) & 1, &s_abort, 32)) break;
+      } else {
+        if (warp == L::ISSW && lane == 0) {   // ---------------- score MMAs ----------------
+          for (int ls = 0; ls < nkt * NDS && !s_abort; ls++) {
+            const uint32_t g = tc * NDS + ls, st = g % NSK, tt = tc + ls / NDS;
+            const int k = ls % NDS;
+            if (!tc5::mbar_wait(&kfull[st], (g / NSK) & 1, &s_abort, 32)) break;
+            if (k == 0 && tt >= 1 && !tc5::mbar_wait(&sempty, (tt - 1) & 1, &s_abort, 64)) break;
             tc5::fence_after();
-            pv_block_mmas(tmem + L::PV_COL + bsel * L::PV_BUF, tmem + L::DEN_COL, Vst + sl * VP_BLOCK,
-                          Wp + bsel * L::w_buf + (size_t)kb * NWP * L::w_blk, ones, IDESC_P, IDESC_D);
-            tc5::commit(&vempty[sl]);
+            const uint64_t ka = tc5::desc(tc5::smem_addr(Kst + st * KT_BLOCK));
+            const uint64_t qa = tc5::desc(tc5::smem_addr(Qs + k * L::q_step));
+  #pragma unroll
+            for (int sa = 0; sa < NSLICE; sa++)   // descriptor start addresses advance in 16-byte units
+              tc5::mma_bf16(tmem + L::SC_COL + sa * BM, ka + (uint64_t)(sa * KTILE * 2), qa, IDESC_S, 1u);
+            tc5::commit(&kempty[st]);
+            if (k == NDS - 1) tc5::commit(&sfull);
           }
-          tc5::commit(&pvdone[bsel]);
+        } else if (warp == L::PISSW && lane == 0) {   // ---------------- PV and DEN MMAs ----------------
+          const uint64_t ones = tc5::desc(tc5::smem_addr(smem_p + L::one_off));
+          tc5::fence_after();   // the DEN accumulators were zeroed before the pass barrier
+          for (int t = 0; t < nkt && !s_abort; t++) {
+            const uint32_t tt = tc + t, bsel = tt & 1;
+            if (!tc5::mbar_wait(&wready[bsel], (tt >> 1) & 1, &s_abort, 64)) break;   // weight digits of tile tt
+            if (tt >= 2 && !tc5::mbar_wait(&pvfree[bsel], ((tt - 2) >> 1) & 1, &s_abort, 64)) break;   // buffer drained
+            tc5::fence_after();
+            for (int kb = 0; kb < NKB && !s_abort; kb++) {
+              const uint32_t g = tt * NKB + kb, sl = g % NVB;
+              if (!tc5::mbar_wait(&vfull[sl], (g / NVB) & 1, &s_abort, 32)) break;
+              tc5::fence_after();
+              pv_block_mmas(tmem + L::PV_COL + bsel * L::PV_BUF, tmem + L::DEN_COL, Vst + sl * VP_BLOCK,
+                            Wp + bsel * L::w_buf + (size_t)kb * NWP * L::w_blk, ones, IDESC_P, IDESC_D);
+              tc5::commit(&vempty[sl]);
+            }
+            tc5::commit(&pvdone[bsel]);
+          }
         }
       }
-    } else {   // ---------------- compute warps ----------------
-      // Weight phase: this thread's key is TMEM lane dcol (rows 4 rg .. 4 rg + 3).  Drain: it
-      // owns value column d = dcol; acc[r][k] is radix-2^32 digit k (lazily carried) in units
-      // of 2^(Fv[d] - 79).
-      const int dcol = 32 * quarter + lane;
-      long long acc[4][3];
-#pragma unroll
-      for (int r = 0; r < 4; r++)
-#pragma unroll
-        for (int k = 0; k < 3; k++) acc[r][k] = 0;
-      auto weight_of = [&](float sc, float m) -> float {
-        float x = __fsub_rn(sc, m);
-        if (x != x) { nf |= ST_NONFINITE; x = neg_inf(); }
-        if (x > 0.0f) { viol |= ST_VIOLATION; x = 0.0f; }
-        return exp32_det(x);
-      };
-      // lane 0 waits, the warp follows
-      auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-        bool ok = true;
-        if (lane == 0) ok = tc5::mbar_wait(bar, parity, &s_abort, 64);
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        tc5::fence_after();
-        return ok;
-      };
-      // fold the PV accumulators of one tile into the integer digits, zero them, release them
-      auto drain = [&](uint32_t tt) {
-        const uint32_t pvb = lane_base + L::PV_COL + (tt & 1) * L::PV_BUF + rg * 4;
-        if (warp_wait(&pvdone[tt & 1], (tt >> 1) & 1)) {
-#pragma unroll
-          for (int g3 = 0; g3 < 3; g3++) {   // diagonals 4 g3 .. 4 g3 + 3 -> digit g3
-            float pv[4][4];
-#pragma unroll
-            for (int c = 0; c < 4; c++) tc5::ld_x4(pvb + (4 * g3 + c) * BM, pv[c]);
+      tc += nkt;
+      tc5::bar_sync(3, L::THREADS);
+    }
+    if ((warp == L::ISSW || warp == L::PISSW) && lane == 0) {   // every MMA has completed before TMEM is released
+      tc5::commit(&fin);
+      tc5::mbar_wait(&fin, 0, &s_abort);
+    }
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 96;" ::: "memory");
+  } else {   // ---------------- compute warps ----------------
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 112;" ::: "memory");
+    uint32_t tc = 0;   // key tiles of earlier passes
+    for (int pass = 0; pass < npass; pass++) {
+      const int q0 = (pass == 0 ? ntq - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
+      const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
+      const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
+      const int nrows = min(BM, a.Sq - q0);
+      // ---- per pass: query slices (resident B operand of the scores), row maxima, cleared sums ----
+      for (int r = warp; r < BM; r += NCW) {
+        const int i = q0 + r;
+        row_slices<DT, DP>(
+            i < a.Sq ? qrow(i) : nullptr, a.D,
+            [&](int q, int d, uint16_t v) {
+              *reinterpret_cast<uint16_t*>(Qs + (d >> 4) * L::q_step + tc5::canon_off(q * BM + r, d & 15)) = v;
+            },
+            &Fq[r], &qfit[r], nf, lane, qlo[r], &qlon[r]);
+      }
+      for (int r = tid; r < BM; r += NCT) mrow[r] = (q0 + r < a.Sq) ? a.m_in[out_row(q0 + r)] : 0.0f;
+      for (int e = tid; e < BM * 3; e += NCT) (&denT[0][0])[e] = 0;
+      for (int e = tid; e < NCW; e += NCT) vbl_n[e] = 0;
+      for (int e = tid; e < BM * NW; e += NCT) (&tbit[0][0])[e] = 0;
+      for (int e = tid; e < BM; e += NCT) trow[e] = tden[e] = 0;
+      tc5::fence_async_smem();
+      tc5::bar_sync(2, L::THREADS);
+        // Weight phase: this thread's key is TMEM lane dcol (rows 4 rg .. 4 rg + 3).  Drain: it
+        // owns value column d = dcol; acc[r][k] is radix-2^32 digit k (lazily carried) in units
+        // of 2^(Fv[d] - 79).
+        const int dcol = 32 * quarter + lane;
+        long long acc[4][3];
+  #pragma unroll
+        for (int r = 0; r < 4; r++)
+  #pragma unroll
+          for (int k = 0; k < 3; k++) acc[r][k] = 0;
+        auto weight_of = [&](float sc, float m) -> float {
+          float x = __fsub_rn(sc, m);
+          if (x != x) { nf |= ST_NONFINITE; x = neg_inf(); }
+          if (x > 0.0f) { viol |= ST_VIOLATION; x = 0.0f; }
+          return exp32_det(x);
+        };
+        // lane 0 waits, the warp follows
+        auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+          bool ok = true;
+          if (lane == 0) ok = tc5::mbar_wait(bar, parity, &s_abort, 64);
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+          tc5::fence_after();
+          return ok;
+        };
+        // fold the PV accumulators of one tile into the integer digits, zero them, release them
+        auto drain = [&](uint32_t tt) {
+          const uint32_t pvb = lane_base + L::PV_COL + (tt & 1) * L::PV_BUF + rg * 4;
+          if (warp_wait(&pvdone[tt & 1], (tt >> 1) & 1)) {
+  #pragma unroll
+            for (int g3 = 0; g3 < 3; g3++) {   // diagonals 4 g3 .. 4 g3 + 3 -> digit g3
+              float pv[4][4];
+  #pragma unroll
+              for (int c = 0; c < 4; c++) tc5::ld_x4(pvb + (4 * g3 + c) * BM, pv[c]);
+              tc5::ld_wait();
+  #pragma unroll
+              for (int r = 0; r < 4; r++) {
+                long long s = 0;
+  #pragma unroll
+                for (int c = 0; c < 4; c++) s += (long long)__float2int_rn(pv[c][r]) * (1ll << (8 * c));   // |P_c| < 2^24
+                acc[r][g3] += s;
+              }
+            }
+  #pragma unroll
+            for (int c = 0; c < L::NPD; c++) tc5::st_zero_x4(pvb + c * BM);
+            tc5::st_wait();
+          }
+          tc5::fence_before();
+          __syncwarp();
+          if (lane == 0) tc5::mbar_arrive(&pvfree[tt & 1]);
+        };
+        // key meta and the V-bad words of this thread's key in tile t (zeros past the range)
+        auto tile_meta = [&](int t, int& mv, uint4& vb) {
+          mv = 0;
+          vb = make_uint4(0u, 0u, 0u, 0u);
+          if (t < nkt) {
+            const int j = a.kv_lo + t * KTILE + dcol;
+            if (j < hi) {
+              mv = p.kmeta[krow0 + j];
+              vb = *reinterpret_cast<const uint4*>(p.vbad + (krow0 + j) * NW);
+            }
+          }
+        };
+        int mv_n;
+        uint4 vb_n;
+        tile_meta(0, mv_n, vb_n);
+        for (int t = 0; t < nkt; t++) {
+          const int kt = a.kv_lo + t * KTILE;
+          const uint32_t tt = tc + t, bsel = tt & 1;
+          unsigned char* wbuf = Wp + bsel * L::w_buf;
+          const int j = kt + dcol;
+          const bool vj = j < hi;
+          const int mv = mv_n;
+          const uint4 vb = vb_n;
+          tile_meta(t + 1, mv_n, vb_n);   // the next tile's, in flight meanwhile
+          const int Fk = kmeta_F(mv), kf = kmeta_fit(mv);
+          // ---- score diagonals of rows 4 rg .. 4 rg + 3 against this thread's key ----
+          const bool ok = warp_wait(&sfull, tt & 1);
+          long long Tq[4];   // the exact dot of each row's (truncated) digits with this key's
+          if (ok) {
+            float v[NDIAG][4];
+  #pragma unroll
+            for (int c = 0; c < NDIAG; c++) tc5::ld_x4(lane_base + L::SC_COL + c * BM + rg * 4, v[c]);
             tc5::ld_wait();
-#pragma unroll
-            for (int r = 0; r < 4; r++) {
-              long long s = 0;
-#pragma unroll
-              for (int c = 0; c < 4; c++) s += (long long)__float2int_rn(pv[c][r]) * (1ll << (8 * c));   // |P_c| < 2^24
-              acc[r][g3] += s;
-            }
+  #pragma unroll
+            for (int e = 0; e < 4; e++) Tq[e] = combine_diag(v, e);
+  #pragma unroll
+            for (int c = 0; c < NDIAG; c++) tc5::st_zero_x4(lane_base + L::SC_COL + c * BM + rg * 4);
+            tc5::st_wait();
+          } else {
+  #pragma unroll
+            for (int e = 0; e < 4; e++) Tq[e] = 0;
           }
-#pragma unroll
-          for (int c = 0; c < L::NPD; c++) tc5::st_zero_x4(pvb + c * BM);
-          tc5::st_wait();
-        }
-        tc5::fence_before();
-        __syncwarp();
-        if (lane == 0) tc5::mbar_arrive(&pvfree[tt & 1]);
-      };
-      // key meta and the V-bad words of this thread's key in tile t (zeros past the range)
-      auto tile_meta = [&](int t, int& mv, uint4& vb) {
-        mv = 0;
-        vb = make_uint4(0u, 0u, 0u, 0u);
-        if (t < nkt) {
-          const int j = a.kv_lo + t * KTILE + dcol;
-          if (j < hi) {
-            mv = p.kmeta[krow0 + j];
-            vb = *reinterpret_cast<const uint4*>(p.vbad + (krow0 + j) * NW);
-          }
-        }
-      };
-      // this pass's output rows start at zero: out-of-window products are added atomically
-      if (!a.add_into) {
-        for (int64_t e = tid; e < (int64_t)nrows * NUM_NDIG * a.D; e += NCT) numb[(int64_t)q0 * NUM_NDIG * a.D + e] = 0;
-        for (int e = tid; e < nrows * DEN_NDIG; e += NCT) denb[(int64_t)q0 * DEN_NDIG + e] = 0;
-      }
-      tc5::bar_sync(1, NCT);
-      int mv_n;
-      uint4 vb_n;
-      tile_meta(0, mv_n, vb_n);
-      for (int t = 0; t < nkt; t++) {
-        const int kt = a.kv_lo + t * KTILE;
-        const uint32_t tt = tc + t, bsel = tt & 1;
-        unsigned char* wbuf = Wp + bsel * L::w_buf;
-        const int j = kt + dcol;
-        const bool vj = j < hi;
-        const int mv = mv_n;
-        const uint4 vb = vb_n;
-        tile_meta(t + 1, mv_n, vb_n);   // the next tile's, in flight meanwhile
-        const int Fk = kmeta_F(mv), kf = kmeta_fit(mv);
-        // ---- score diagonals of rows 4 rg .. 4 rg + 3 against this thread's key ----
-        const bool ok = warp_wait(&sfull, tt & 1);
-        float v[NDIAG][4];
-        if (ok) {
-#pragma unroll
-          for (int c = 0; c < NDIAG; c++) tc5::ld_x4(lane_base + L::SC_COL + c * BM + rg * 4, v[c]);
-          tc5::ld_wait();
-#pragma unroll
-          for (int c = 0; c < NDIAG; c++) tc5::st_zero_x4(lane_base + L::SC_COL + c * BM + rg * 4);
-          tc5::st_wait();
-        } else {
-#pragma unroll
-          for (int c = 0; c < NDIAG; c++)
-#pragma unroll
-            for (int e = 0; e < 4; e++) v[c][e] = 0.0f;
-        }
-        tc5::fence_before();
-        __syncwarp();
-        if (lane == 0) tc5::mbar_arrive(&sempty);
-        // ---- weights: one straight-line evaluation per row (the four interleave); pairs it
-        // cannot take (a row outside its window, a score outside the normal range) go to `slow` ----
-        float w[4];
-        uint32_t slow = 0;
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-          const int rl = rg * 4 + e, i = q0 + rl;
-          const bool valid = ok && vj && i < a.Sq && (!a.causal || j <= i);
-          bool sp;
-          const float c = cr32_scaled_nb(combine_diag(v, e), Fq[rl] + Fk, sp);
-          float x = __fsub_rn(__fmul_rn(a.scale32, c), mrow[rl]);
-          const bool fast = valid && qfit[rl] && kf && !sp;
-          if (fast && x != x) nf |= ST_NONFINITE;
-          if (fast && x > 0.0f) viol |= ST_VIOLATION;
-          x = x != x ? neg_inf() : (x > 0.0f ? 0.0f : x);
-          const float wf = exp32_det_nb(x);
-          w[e] = fast ? wf : 0.0f;
-          if (valid && !fast) slow |= 1u << e;
-        }
-        if (slow) {
-#pragma unroll
-          for (int e = 0; e < 4; e++)
-            if ((slow >> e) & 1u) {
-              const int rl = rg * 4 + e, i = q0 + rl;
-              const T* qrow = qbase + (int64_t)i * a.qs[2];
-              const T* krow = kbase + (int64_t)j * a.ks[2];
-              float dot;
-              if (qfit[rl] && kf) {   // a score outside the normal range: the general rounding
-                w[e] = weight_of(__fmul_rn(a.scale32, cr32_scaled(combine_diag(v, e), Fq[rl] + Fk)), mrow[rl]);
-                continue;
-              } else if (qlon[rl] != LO_DEEP && kmeta_lon(mv) != KLO_DEEP) {   // truncated dot + low limbs
-                dot = dot_lo<DT>(combine_diag(v, e), qrow, Fq[rl], qlo[rl], qlon[rl], krow, Fk, p.klo + (krow0 + j) * NLO,
-                                 kmeta_lon(mv));
-              } else if (!qfit[rl] && kf) {   // a deep row: the general exact dot
-                dot = exact_dot_lane<DT, true, false>(qrow, Fq[rl], krow, Fk, a.D);
-              } else if (qfit[rl]) {
-                dot = exact_dot_lane<DT, false, true>(qrow, Fq[rl], krow, Fk, a.D);
-              } else {
-                dot = exact_dot_lane<DT, true, true>(qrow, Fq[rl], krow, Fk, a.D);
-              }
-              w[e] = weight_of(__fmul_rn(a.scale32, dot), mrow[rl]);
-            }
-        }
-        // ---- weight digits: W = w 2^79 = x 2^(8 b0), x < 2^32; words[e][q] = bytes 4q .. 4q + 3 of W ----
-        uint32_t words[4][3];
-        uint32_t tiny = 0;   // pairs with 0 < w < 2^-56: exact atomics below
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-          const uint32_t wb = __float_as_uint(w[e]);   // 0 <= w <= 1
-          const int ex = (int)(wb >> 23);
-          uint32_t x = 0;
-          int b0 = 0;
-          if (ex >= 71) {
-            const int sh = ex - 71;   // <= 56
-            b0 = sh >> 3;
-            x = ((wb & 0x7FFFFFu) | 0x800000u) << (sh & 7);
-          } else if (wb != 0u) {
-            tiny |= 1u << e;
-          }
-          const uint64_t y = (uint64_t)x << (8 * (b0 & 3));
-          const uint32_t lo = (uint32_t)y, hw = (uint32_t)(y >> 32);
-          const bool low = b0 < 4;
-          words[e][0] = low ? lo : 0u;
-          words[e][1] = low ? hw : lo;
-          words[e][2] = low ? 0u : hw;   // digits 8 and 9: below 2^16
-        }
-#pragma unroll
-        for (int e = 0; e < 4; e++) {   // DEN digits 8-9: one exact warp sum per row (32 x 2^16 < 2^21)
-          const unsigned s89 = __reduce_add_sync(0xFFFFFFFFu, words[e][2]);
-          if (lane == 0 && s89) atomicAdd((unsigned long long*)&denT[rg * 4 + e][2], (unsigned long long)s89);
-        }
-        {   // plane s of this key's 4 rows: 4 f16 values, contiguous in the MN-major block (one 8-byte store)
-          unsigned char* wdst = wbuf + (size_t)(dcol / VKEYS) * NWP * L::w_blk + tc5::mn_off(rg * 4, dcol % VKEYS);
-#pragma unroll
-          for (int q = 0; q < 3; q++) {
-            const uint32_t a01[2] = {__byte_perm(words[0][q], words[1][q], 0x5140),    // bytes 0, 1 of rows 0, 1
-                                     __byte_perm(words[0][q], words[1][q], 0x7362)};   // bytes 2, 3
-            const uint32_t a23[2] = {__byte_perm(words[2][q], words[3][q], 0x5140),
-                                     __byte_perm(words[2][q], words[3][q], 0x7362)};
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-              const int s = 4 * q + k;
-              if (s < NWP) {
-                const uint32_t sel = (k & 1) ? 0x4342u : 0x4140u;   // (0x64, byte of row 1, 0x64, byte of row 0)
-                const uint32_t h01 = f16_pair_from_biased(__byte_perm(a01[k >> 1], 0x64646464u, sel));
-                const uint32_t h23 = f16_pair_from_biased(__byte_perm(a23[k >> 1], 0x64646464u, sel));
-                *reinterpret_cast<uint2*>(wdst + s * L::w_blk) = make_uint2(h01, h23);
-              }
-            }
-          }
-        }
-        tc5::fence_async_smem();   // the weight digit planes are read by the tensor cores
-        __syncwarp();
-        if (lane == 0) tc5::mbar_arrive(&wready[bsel]);
-        // ---- the previous tile's PV products are done by now (or soon): fold them in ----
-        if (t >= 1) drain(tt - 1);
-        // ---- this warp's products outside the window: exact int64 atomics into the output digits ----
-        if (__ballot_sync(0xFFFFFFFFu, tiny != 0)) {
-#pragma unroll
+          tc5::fence_before();
+          __syncwarp();
+          if (lane == 0) tc5::mbar_arrive(&sempty);
+          // ---- weights: one straight-line evaluation per row (the four interleave); pairs it
+          // cannot take (a row outside its window, a score outside the normal range) go to `slow` ----
+          float w[4];
+          uint32_t slow = 0;
+  #pragma unroll
           for (int e = 0; e < 4; e++) {
-            uint32_t pend = __ballot_sync(0xFFFFFFFFu, (tiny >> e) & 1u);
-            if (!pend) continue;
-            const int rl = rg * 4 + e;
-            long long* nrow = numb + (int64_t)(q0 + rl) * NUM_NDIG * a.D;
-            long long sum[NW][3];
-#pragma unroll
-            for (int c = 0; c < NW; c++) sum[c][0] = sum[c][1] = sum[c][2] = 0;
-            for (; pend; pend &= pend - 1) {
-              const int src = __ffs(pend) - 1, jj = kt + 32 * quarter + src;
-              const uint32_t wb = __float_as_uint(__shfl_sync(0xFFFFFFFFu, w[e], src));
-              const Split sw = split_f32(wb);
-              if (lane == 0) atomic_digits_add(denb + (int64_t)(q0 + rl) * DEN_NDIG, 1, DEN_E0, sw.mant, 0, sw.lsb);
-              const int ex = (int)(wb >> 23);
-              if (ex >= 15) {   // W' = w 2^135 = x 2^(8 b0): words of W' against the prepared Vint
-                const int sh = ex - 15, b0 = sh >> 3;
-                const uint64_t y = (uint64_t)(((wb & 0x7FFFFFu) | 0x800000u) << (sh & 7)) << (8 * (b0 & 3));
-                const bool low = b0 < 4;
-                const long long w0 = low ? (long long)(uint32_t)y : 0, w1 = low ? (long long)(y >> 32) : (long long)(uint32_t)y,
-                                w2 = low ? 0 : (long long)(y >> 32);
-                const int* vrow = p.vint + (krow0 + jj) * DP;
-#pragma unroll
-                for (int c = 0; c < NW; c++) {   // |Vint| < 2^23, words < 2^32: 32 products stay below 2^60
-                  const long long vi = vrow[lane + 32 * c];
-                  sum[c][0] += vi * w0;
-                  sum[c][1] += vi * w1;
-                  sum[c][2] += vi * w2;
+            const int rl = rg * 4 + e, i = q0 + rl;
+            const bool valid = ok && vj && i < a.Sq && (!a.causal || j <= i);
+            bool sp;
+            const float c = cr32_scaled_nb(Tq[e], Fq[rl] + Fk, sp);
+            float x = __fsub_rn(__fmul_rn(a.scale32, c), mrow[rl]);
+            const bool fast = valid && qfit[rl] && kf && !sp;
+            if (fast && x != x) nf |= ST_NONFINITE;
+            if (fast && x > 0.0f) viol |= ST_VIOLATION;
+            x = x != x ? neg_inf() : (x > 0.0f ? 0.0f : x);
+            const float wf = exp32_det_nb(x);
+            w[e] = fast ? wf : 0.0f;
+            if (valid && !fast) slow |= 1u << e;
+          }
+          if (slow) {
+  #pragma unroll
+            for (int e = 0; e < 4; e++)
+              if ((slow >> e) & 1u) {
+                const int rl = rg * 4 + e, i = q0 + rl;
+                const T* qr = qrow(i);
+                const T* kr = krow(j);
+                float dot;
+                if (qfit[rl] && kf) {   // a score outside the normal range: the general rounding
+                  w[e] = weight_of(__fmul_rn(a.scale32, cr32_scaled(Tq[e], Fq[rl] + Fk)), mrow[rl]);
+                  continue;
+                } else if (qlon[rl] != LO_DEEP && kmeta_lon(mv) != KLO_DEEP) {   // truncated dot + low limbs
+                  dot = dot_lo<DT>(Tq[e], qr, Fq[rl], qlo[rl], qlon[rl], kr, Fk, p.klo + (krow0 + j) * NLO, kmeta_lon(mv));
+                } else if (!qfit[rl] && kf) {   // a deep row: the general exact dot
+                  dot = exact_dot_lane<DT, true, false>(qr, Fq[rl], kr, Fk, a.D);
+                } else if (qfit[rl]) {
+                  dot = exact_dot_lane<DT, false, true>(qr, Fq[rl], kr, Fk, a.D);
+                } else {
+                  dot = exact_dot_lane<DT, true, true>(qr, Fq[rl], kr, Fk, a.D);
                 }
-              } else {   // w < 2^-112: the whole product w V_jd for every d
-                for (int d = lane; d < a.D; d += 32) {
-                  const uint32_t u = In<DT>::bits(vbase + (int64_t)jj * a.vs[2], d);
-                  if (nonfinite_bits(u)) continue;
-                  const Split sv = split_f32(u);
-                  atomic_digits_add(nrow + d, a.D, NUM_E0, (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
+                w[e] = weight_of(__fmul_rn(a.scale32, dot), mrow[rl]);
+              }
+          }
+          // ---- weight digits: W = w 2^79 = x 2^(8 b0), x < 2^32; words[e][q] = bytes 4q .. 4q + 3 of W ----
+          uint32_t words[4][3];
+          uint32_t tiny = 0;   // pairs with 0 < w < 2^-56: exact atomics below
+  #pragma unroll
+          for (int e = 0; e < 4; e++) {
+            const uint32_t wb = __float_as_uint(w[e]);   // 0 <= w <= 1
+            const int ex = (int)(wb >> 23);
+            uint32_t x = 0;
+            int b0 = 0;
+            if (ex >= 71) {
+              const int sh = ex - 71;   // <= 56
+              b0 = sh >> 3;
+              x = ((wb & 0x7FFFFFu) | 0x800000u) << (sh & 7);
+            } else if (wb != 0u) {
+              tiny |= 1u << e;
+            }
+            const uint64_t y = (uint64_t)x << (8 * (b0 & 3));
+            const uint32_t lo = (uint32_t)y, hw = (uint32_t)(y >> 32);
+            const bool low = b0 < 4;
+            words[e][0] = low ? lo : 0u;
+            words[e][1] = low ? hw : lo;
+            words[e][2] = low ? 0u : hw;   // digits 8 and 9: below 2^16
+          }
+  #pragma unroll
+          for (int e = 0; e < 4; e++) {   // DEN digits 8-9: one exact warp sum per row (32 x 2^16 < 2^21)
+            const unsigned s89 = __reduce_add_sync(0xFFFFFFFFu, words[e][2]);
+            if (lane == 0 && s89) atomicAdd((unsigned long long*)&denT[rg * 4 + e][2], (unsigned long long)s89);
+          }
+          {   // plane s of this key's 4 rows: 4 f16 values, contiguous in the MN-major block (one 8-byte store)
+            unsigned char* wdst = wbuf + (size_t)(dcol / VKEYS) * NWP * L::w_blk + tc5::mn_off(rg * 4, dcol % VKEYS);
+  #pragma unroll
+            for (int q = 0; q < 3; q++) {
+              const uint32_t a01[2] = {__byte_perm(words[0][q], words[1][q], 0x5140),    // bytes 0, 1 of rows 0, 1
+                                       __byte_perm(words[0][q], words[1][q], 0x7362)};   // bytes 2, 3
+              const uint32_t a23[2] = {__byte_perm(words[2][q], words[3][q], 0x5140),
+                                       __byte_perm(words[2][q], words[3][q], 0x7362)};
+  #pragma unroll
+              for (int k = 0; k < 4; k++) {
+                const int s = 4 * q + k;
+                if (s < NWP) {
+                  const uint32_t sel = (k & 1) ? 0x4342u : 0x4140u;   // (0x64, byte of row 1, 0x64, byte of row 0)
+                  const uint32_t h01 = f16_pair_from_biased(__byte_perm(a01[k >> 1], 0x64646464u, sel));
+                  const uint32_t h23 = f16_pair_from_biased(__byte_perm(a23[k >> 1], 0x64646464u, sel));
+                  *reinterpret_cast<uint2*>(wdst + s * L::w_blk) = make_uint2(h01, h23);
                 }
               }
             }
-#pragma unroll
-            for (int c = 0; c < NW; c++) {
-              const int d = lane + 32 * c;
-              if (d < a.D)
-#pragma unroll
-                for (int q = 0; q < 3; q++)
-                  if (sum[c][q] != 0)
-                    atomic_digits_add(nrow + d, a.D, NUM_E0,
-                                      sum[c][q] < 0 ? 0ull - (unsigned long long)sum[c][q] : (unsigned long long)sum[c][q],
-                                      sum[c][q] < 0, Fv[d] - 135 + 32 * q);
-            }
           }
-        }
-        {   // keys with V elements outside their column window: listed, their products added after the tiles
-          const bool bad = (vb.x | vb.y | vb.z | vb.w) != 0u && (w[0] != 0.0f || w[1] != 0.0f || w[2] != 0.0f || w[3] != 0.0f);
-          const uint32_t bm = __ballot_sync(0xFFFFFFFFu, bad);
-          if (bm) {
-            const int base = vbl_n[warp];
-            const int idx = base + __popc(bm & ((1u << lane) - 1u));
-            if (bad && idx < NVBL) {
-              vbl_w[warp][idx] = make_float4(w[0], w[1], w[2], w[3]);
-              vbl_j[warp][idx] = j;
-            }
-            __syncwarp();
-            if (lane == 0) vbl_n[warp] = base + __popc(bm);
-            if (bad && idx >= NVBL) {   // list full: this lane adds its products now
-              const uint32_t vw[4] = {vb.x, vb.y, vb.z, vb.w};
-#pragma unroll
-              for (int tw = 0; tw < NW; tw++)
-                for (uint32_t m = vw[tw]; m; m &= m - 1) {
-                  const int d = tw * 32 + __ffs(m) - 1;
-                  const Split sv = split_f32(In<DT>::bits(vbase + (int64_t)j * a.vs[2], d));
-#pragma unroll
-                  for (int e = 0; e < 4; e++) {
-                    const uint32_t wb = __float_as_uint(w[e]);
-                    if (wb == 0u || (int)(wb >> 23) < 15) continue;   // zero, or a whole-product pair above
-                    const Split sw = split_f32(wb);
-                    atomic_digits_add(numb + (int64_t)(q0 + rg * 4 + e) * NUM_NDIG * a.D + d, a.D, NUM_E0,
-                                      (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
+          tc5::fence_async_smem();   // the weight digit planes are read by the tensor cores
+          __syncwarp();
+          if (lane == 0) tc5::mbar_arrive(&wready[bsel]);
+          // ---- the previous tile's PV products are done by now (or soon): fold them in ----
+          if (t >= 1) drain(tt - 1);
+          // ---- this warp's products outside the window: exact int64 atomics into the output digits ----
+          if (__ballot_sync(0xFFFFFFFFu, tiny != 0)) {
+  #pragma unroll
+            for (int e = 0; e < 4; e++) {
+              uint32_t pend = __ballot_sync(0xFFFFFFFFu, (tiny >> e) & 1u);
+              if (!pend) continue;
+              const int rl = rg * 4 + e;
+              long long* nrow = slot_num(rl);
+              if (lane == 0) {
+                trow[rl] = 1;
+                tden[rl] = 1;
+              }
+              long long sum[NW][3];
+  #pragma unroll
+              for (int c = 0; c < NW; c++) sum[c][0] = sum[c][1] = sum[c][2] = 0;
+              for (; pend; pend &= pend - 1) {
+                const int src = __ffs(pend) - 1, jj = kt + 32 * quarter + src;
+                const uint32_t wb = __float_as_uint(__shfl_sync(0xFFFFFFFFu, w[e], src));
+                const Split sw = split_f32(wb);
+                if (lane == 0) atomic_digits_add(slot_den(rl), 1, DEN_E0, sw.mant, 0, sw.lsb);
+                const int ex = (int)(wb >> 23);
+                if (ex >= 15) {   // W' = w 2^135 = x 2^(8 b0): words of W' against the prepared Vint
+                  const int sh = ex - 15, b0 = sh >> 3;
+                  const uint64_t y = (uint64_t)(((wb & 0x7FFFFFu) | 0x800000u) << (sh & 7)) << (8 * (b0 & 3));
+                  const bool low = b0 < 4;
+                  const long long w0 = low ? (long long)(uint32_t)y : 0, w1 = low ? (long long)(y >> 32) : (long long)(uint32_t)y,
+                                  w2 = low ? 0 : (long long)(y >> 32);
+                  const int* vrow = p.vint + (krow0 + jj) * DP;
+  #pragma unroll
+                  for (int c = 0; c < NW; c++) {   // |Vint| < 2^23, words < 2^32: 32 products stay below 2^60
+                    const long long vi = vrow[lane + 32 * c];
+                    sum[c][0] += vi * w0;
+                    sum[c][1] += vi * w1;
+                    sum[c][2] += vi * w2;
+                  }
+                } else {   // w < 2^-112: the whole product w V_jd for every d
+                  for (int d = lane; d < a.D; d += 32) {
+                    const uint32_t u = In<DT>::bits(vrow(jj), d);
+                    if (nonfinite_bits(u)) continue;
+                    const Split sv = split_f32(u);
+                    atomic_digits_add(nrow + d, DP, NUM_E0, (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
                   }
                 }
-            }
-            __syncwarp();
-          }
-        }
-      }
-      if (nkt > 0) drain(tc + nkt - 1);
-      for (int li = 0; li < min(vbl_n[warp], NVBL); li++) {   // listed keys: products of their V elements below the window
-        const int jj = vbl_j[warp][li];
-        const float4 wl = vbl_w[warp][li];
-        const float wr[4] = {wl.x, wl.y, wl.z, wl.w};
-        const uint32_t* vbr = p.vbad + (krow0 + jj) * NW;
-        for (int tw = 0; tw < NW; tw++)
-          for (uint32_t m = vbr[tw]; m; m &= m - 1) {
-            const int d = tw * 32 + __ffs(m) - 1;
-            if (lane < 4) {
-              const uint32_t wb = __float_as_uint(wr[lane]);
-              if (wb != 0u && (int)(wb >> 23) >= 15) {   // smaller weights took whole products
-                const Split sv = split_f32(In<DT>::bits(vbase + (int64_t)jj * a.vs[2], d));
-                const Split sw = split_f32(wb);
-                atomic_digits_add(numb + (int64_t)(q0 + rg * 4 + lane) * NUM_NDIG * a.D + d, a.D, NUM_E0,
-                                  (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
+              }
+  #pragma unroll
+              for (int c = 0; c < NW; c++) {
+                const int d = lane + 32 * c;
+                if (d < a.D)
+  #pragma unroll
+                  for (int q = 0; q < 3; q++)
+                    if (sum[c][q] != 0)
+                      atomic_digits_add(nrow + d, DP, NUM_E0,
+                                        sum[c][q] < 0 ? 0ull - (unsigned long long)sum[c][q] : (unsigned long long)sum[c][q],
+                                        sum[c][q] < 0, Fv[d] - 135 + 32 * q);
               }
             }
           }
-      }
-      // ---- DEN digits 0-7 from TMEM (lane 16 s + row; every column holds the same sum) ----
-      if (rg == 0) {
-        if (nkt > 0) {
-          const float dsum = tc5::ld_x1(lane_base + L::DEN_COL);
-          tc5::ld_wait();
-          const int sv = __float2int_rn(dsum);   // < 2^24
-          const int s = 2 * quarter + (lane >> 4), rl = lane & 15;
-          if (sv) atomicAdd((unsigned long long*)&denT[rl][s >> 2], (unsigned long long)sv << (8 * (s & 3)));
-          tc5::st_zero_x8(lane_base + L::DEN_COL);
-          tc5::st_zero_x8(lane_base + L::DEN_COL + 8);
-          tc5::st_wait();
+          {   // keys with V elements outside their column window: listed, their products added after the tiles
+            const bool bad = (vb.x | vb.y | vb.z | vb.w) != 0u && (w[0] != 0.0f || w[1] != 0.0f || w[2] != 0.0f || w[3] != 0.0f);
+            const uint32_t bm = __ballot_sync(0xFFFFFFFFu, bad);
+            if (bm) {
+              const int base = vbl_n[warp];
+              const int idx = base + __popc(bm & ((1u << lane) - 1u));
+              if (bad && idx < NVBL) {
+                vbl_w[warp][idx] = make_float4(w[0], w[1], w[2], w[3]);
+                vbl_j[warp][idx] = j;
+              }
+              __syncwarp();
+              if (lane == 0) vbl_n[warp] = base + __popc(bm);
+              if (bad && idx >= NVBL) {   // list full: this lane adds its products now
+                const uint32_t vw[4] = {vb.x, vb.y, vb.z, vb.w};
+  #pragma unroll
+                for (int tw = 0; tw < NW; tw++)
+                  for (uint32_t m = vw[tw]; m; m &= m - 1) {
+                    const int d = tw * 32 + __ffs(m) - 1;
+                    const Split sv = split_f32(In<DT>::bits(vrow(j), d));
+  #pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                      const uint32_t wb = __float_as_uint(w[e]);
+                      if (wb == 0u || (int)(wb >> 23) < 15) continue;   // zero, or a whole-product pair above
+                      const Split sw = split_f32(wb);
+                      atomic_digits_add(slot_num(rg * 4 + e) + d, DP, NUM_E0,
+                                        (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
+                      atomicOr(&tbit[rg * 4 + e][d >> 5], 1u << (d & 31));
+                    }
+                  }
+              }
+              __syncwarp();
+            }
+          }
         }
-        tc5::fence_before();
-      }
-      // ---- epilogue: canonical digits ----
-      tc5::bar_sync(1, NCT);   // denT and every atomic of this pass complete
-      const int d = dcol;
-#pragma unroll
-      for (int r = 0; r < 4; r++) {
-        const int rl = rg * 4 + r, i = q0 + rl;
-        if (i >= a.Sq || d >= a.D) continue;
-        long long* nrow = numb + (int64_t)i * NUM_NDIG * a.D;
-        long long dg[NUM_NDIG + 3];
-#pragma unroll
-        for (int k = 0; k < NUM_NDIG; k++) dg[k] = __ldcg(nrow + (int64_t)k * a.D + d);
-#pragma unroll
-        for (int k = NUM_NDIG; k < NUM_NDIG + 3; k++) dg[k] = 0;
-        const int off = Fv[d] - 79 - NUM_E0;   // bit position of the accumulator's unit
-        add_i64_at_tp(dg, acc[r][0], off);
-        add_i64_at_tp(dg, acc[r][1], off + 32);
-        add_i64_at_tp(dg, acc[r][2], off + 64);
-        kul_carry(dg, NUM_NDIG + 3);
-        long long top = dg[NUM_NDIG + 2];
-        bool bad = false;
-        for (int k = NUM_NDIG + 1; k >= NUM_NDIG - 1; k--) {
-          if (top > (1ll << 30) || top < -(1ll << 30)) bad = true;
-          top = top * 4294967296ll + dg[k];
+        if (nkt > 0) drain(tc + nkt - 1);
+        if (lane < min(vbl_n[warp], NVBL)) {   // listed keys, one per lane: products of their V elements below the window
+          const int jj = vbl_j[warp][lane];
+          const float4 wl = vbl_w[warp][lane];
+          const float wr[4] = {wl.x, wl.y, wl.z, wl.w};
+          const uint4 vbr = *reinterpret_cast<const uint4*>(p.vbad + (krow0 + jj) * NW);
+          const uint32_t vw[4] = {vbr.x, vbr.y, vbr.z, vbr.w};
+  #pragma unroll
+          for (int tw = 0; tw < NW; tw++)
+            for (uint32_t m = vw[tw]; m; m &= m - 1) {
+              const int d = tw * 32 + __ffs(m) - 1;
+              const Split sv = split_f32(In<DT>::bits(vrow(jj), d));
+  #pragma unroll
+              for (int e = 0; e < 4; e++) {
+                const uint32_t wb = __float_as_uint(wr[e]);
+                if (wb == 0u || (int)(wb >> 23) < 15) continue;   // smaller weights took whole products
+                const Split sw = split_f32(wb);
+                atomic_digits_add(slot_num(rg * 4 + e) + d, DP, NUM_E0,
+                                  (unsigned long long)sw.mant * sv.mant, sv.neg, sw.lsb + sv.lsb);
+                atomicOr(&tbit[rg * 4 + e][d >> 5], 1u << (d & 31));
+              }
+            }
         }
-        if (bad) nf |= ST_HEADROOM;
-#pragma unroll
-        for (int k = 0; k < NUM_NDIG - 1; k++) nrow[(int64_t)k * a.D + d] = dg[k];
-        nrow[(int64_t)(NUM_NDIG - 1) * a.D + d] = top;
-      }
-      for (int rl = tid; rl < nrows; rl += NCT) {
-        long long* drow = denb + (int64_t)(q0 + rl) * DEN_NDIG;
-        long long dg[DEN_NDIG + 3];
-#pragma unroll
-        for (int k = 0; k < DEN_NDIG; k++) dg[k] = __ldcg(drow + k);
-#pragma unroll
-        for (int k = DEN_NDIG; k < DEN_NDIG + 3; k++) dg[k] = 0;
-        const int off = -79 - DEN_E0;   // W units
-        add_i64_at_tp(dg, denT[rl][0], off);
-        add_i64_at_tp(dg, denT[rl][1], off + 32);
-        add_i64_at_tp(dg, denT[rl][2], off + 64);
-        kul_carry(dg, DEN_NDIG + 3);
-        long long top = dg[DEN_NDIG + 2];
-        bool bad = false;
-        for (int k = DEN_NDIG + 1; k >= DEN_NDIG - 1; k--) {
-          if (top > (1ll << 30) || top < -(1ll << 30)) bad = true;
-          top = top * 4294967296ll + dg[k];
+        // ---- DEN digits 0-7 from TMEM (lane 16 s + row; every column holds the same sum) ----
+        if (rg == 0) {
+          if (nkt > 0) {
+            const float dsum = tc5::ld_x1(lane_base + L::DEN_COL);
+            tc5::ld_wait();
+            const int sv = __float2int_rn(dsum);   // < 2^24
+            const int s = 2 * quarter + (lane >> 4), rl = lane & 15;
+            if (sv) atomicAdd((unsigned long long*)&denT[rl][s >> 2], (unsigned long long)sv << (8 * (s & 3)));
+            tc5::st_zero_x8(lane_base + L::DEN_COL);
+            tc5::st_zero_x8(lane_base + L::DEN_COL + 8);
+            tc5::st_wait();
+          }
+          tc5::fence_before();
         }
-        if (bad) nf |= ST_HEADROOM;
+        // ---- epilogue: canonical digits ----
+        tc5::bar_sync(1, NCT);   // denT, the touched flags and every spill atomic of this pass complete
+        {
+          uint32_t sm;
+          asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+          if (sm >= (uint32_t)SPILL_SLOTS) nf |= ST_HEADROOM;   // no spill slot for this SM: products outside the windows are missing
+        }
+        const int d = dcol;
+  #pragma unroll
+        for (int r = 0; r < 4; r++) {
+          const int rl = rg * 4 + r, i = q0 + rl;
+          if (i >= a.Sq || d >= a.D) continue;
+          long long* nrow = a.num + out_row(i) * NUM_NDIG * a.D;
+          long long dg[NUM_NDIG + 3];
+  #pragma unroll
+          for (int k = 0; k < NUM_NDIG + 3; k++) dg[k] = 0;
+          if (a.add_into)
+  #pragma unroll
+            for (int k = 0; k < NUM_NDIG; k++) dg[k] = __ldcg(nrow + (int64_t)k * a.D + d);
+          if (trow[rl] || ((tbit[rl][d >> 5] >> (d & 31)) & 1u)) {   // this digit column of the slot was touched
+            long long* sp = slot_num(rl) + d;
+  #pragma unroll
+            for (int k = 0; k < NUM_NDIG; k++) {
+              dg[k] += __ldcg(sp + (size_t)k * DP);
+              sp[(size_t)k * DP] = 0;
+            }
+          }
+          {
+            unsigned __int128 M;
+            bool neg;
+            digits3_to_u128(acc[r][0], acc[r][1], acc[r][2], M, neg);
+            add_u128_at(dg, M, neg, Fv[d] - 79 - NUM_E0);   // the accumulator's unit is 2^(Fv - 79)
+          }
+          carry_digits(dg);
+          long long top = dg[NUM_NDIG + 2];
+          bool bad = false;
 #pragma unroll
-        for (int k = 0; k < DEN_NDIG - 1; k++) drow[k] = dg[k];
-        drow[DEN_NDIG - 1] = top;
-      }
+          for (int k = NUM_NDIG + 1; k >= NUM_NDIG - 1; k--) {
+            if (top > (1ll << 30) || top < -(1ll << 30)) bad = true;
+            top = top * 4294967296ll + dg[k];
+          }
+          if (bad) nf |= ST_HEADROOM;
+  #pragma unroll
+          for (int k = 0; k < NUM_NDIG - 1; k++) nrow[(int64_t)k * a.D + d] = dg[k];
+          nrow[(int64_t)(NUM_NDIG - 1) * a.D + d] = top;
+        }
+        for (int rl = tid; rl < nrows; rl += NCT) {
+          long long* drow = a.den + out_row(q0 + rl) * DEN_NDIG;
+          long long dg[DEN_NDIG + 3];
+  #pragma unroll
+          for (int k = 0; k < DEN_NDIG + 3; k++) dg[k] = 0;
+          if (a.add_into)
+  #pragma unroll
+            for (int k = 0; k < DEN_NDIG; k++) dg[k] = __ldcg(drow + k);
+          if (tden[rl])
+  #pragma unroll
+            for (int k = 0; k < DEN_NDIG; k++) {
+              dg[k] += __ldcg(slot_den(rl) + k);
+              slot_den(rl)[k] = 0;
+            }
+          {
+            unsigned __int128 M;
+            bool neg;
+            digits3_to_u128(denT[rl][0], denT[rl][1], denT[rl][2], M, neg);
+            add_u128_at(dg, M, neg, -79 - DEN_E0);   // W units
+          }
+          carry_digits(dg);
+          long long top = dg[DEN_NDIG + 2];
+          bool bad = false;
+#pragma unroll
+          for (int k = DEN_NDIG + 1; k >= DEN_NDIG - 1; k--) {
+            if (top > (1ll << 30) || top < -(1ll << 30)) bad = true;
+            top = top * 4294967296ll + dg[k];
+          }
+          if (bad) nf |= ST_HEADROOM;
+  #pragma unroll
+          for (int k = 0; k < DEN_NDIG - 1; k++) drow[k] = dg[k];
+          drow[DEN_NDIG - 1] = top;
+        }
+        __threadfence();   // the cleared slot digits reach L2 before the SM's next CTA adds into them
+          tc += nkt;
+      tc5::bar_sync(3, L::THREADS);
     }
-    tc += nkt;
-    __syncthreads();
-  }   // pass
-  if ((warp == L::SISS || warp == L::PISS || warp == L::SISS2) && lane == 0) {   // every MMA has completed before TMEM is released
-    tc5::commit(&fin);
-    tc5::mbar_wait(&fin, 0, &s_abort);
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
   }
   tc5::fence_before();
   __syncthreads();
@@ -666,6 +762,9 @@ template <int DT>
 static cudaError_t launch_acc_tp_t(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
   using L = AccTpLayout;
   cudaError_t e = cudaFuncSetAttribute(accumulate_tp_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
+  if (e != cudaSuccess) return e;
+  // the spill slots start clean (a CTA clears what it used; a kernel that gave up may not have)
+  e = cudaMemsetAsync(p.spill, 0, (size_t)SPILL_SLOTS * spill_slot_words(L::DP) * sizeof(long long), st);
   if (e != cudaSuccess) return e;
   const int nt = (a.Sq + L::BM - 1) / L::BM;
   dim3 grid(a.causal ? (nt + 1) / 2 : nt, a.Hq, a.B);

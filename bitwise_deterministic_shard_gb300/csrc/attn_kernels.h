@@ -31,6 +31,7 @@ struct KvPrep {
   int ntk;           // key tiles of KTILE rows per (b, hk) in ktc
   int* kmeta;        // [rows]: (F + 1024) | (fit << 16) | (low-limb count, or 15 for deep, << 17)
   int2* klo;         // [rows][NLO] low limbs (d, X_lo) of rows outside the 26-bit window
+  long long* spill;  // DP == 128 with V: SPILL_SLOTS per-SM scratch slots (below), zero between uses
   unsigned char* vtc;   // DP == 128: V as tensor-core operand digit planes (below), else null
   int* vcol;         // [B * Hkv][DP] largest V biased exponent per column over the range
   int* vint;         // [rows][DP] V fixed point, |Vint| < 2^23
@@ -47,6 +48,11 @@ constexpr int KT_BLOCK = 4 * KTILE * 16 * 2;
 // per block 3 planes = the balanced base-256 digits of Vint (each exact in f16), each a
 // 128 (d) x 16 (keys) operand block in the canonical K-major layout of tc5.cuh.
 constexpr int VKEYS = 16;
+// spill: one slot per SM (one tensor-PV CTA fits on an SM at a time), indexed by %smid: the
+// products outside the fixed-point windows of the CTA's 16 rows, [16][15][DP] NUM digits then
+// [16][6] DEN digits; the CTA's epilogue reads what it touched and clears it again
+constexpr int SPILL_SLOTS = 256, SPILL_ROWS = 16;
+__host__ __device__ constexpr size_t spill_slot_words(int dp) { return (size_t)SPILL_ROWS * (15 * dp + 6); }
 constexpr int VP_BLOCK = 3 * 128 * VKEYS * 2;
 size_t kv_prep_bytes(int B, int Hkv, int Skv, int D);
 KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v);

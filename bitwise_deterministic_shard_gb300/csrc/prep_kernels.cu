@@ -130,6 +130,8 @@ static size_t vtc_bytes(int B, int Hkv, int Skv, int dp) {
   return (size_t)B * Hkv * ntk * (KTILE / VKEYS) * VP_BLOCK;
 }
 
+static size_t spill_bytes(int dp) { return dp == 128 ? (size_t)SPILL_SLOTS * spill_slot_words(dp) * 8 : 0; }
+
 static size_t ktc_bytes(int B, int Hkv, int Skv, int dp) {
   const size_t ntk = (size_t)(Skv + KTILE - 1) / KTILE;
   return (size_t)B * Hkv * ntk * (dp / 16) * KT_BLOCK;
@@ -140,7 +142,8 @@ size_t kv_prep_bytes(int B, int Hkv, int Skv, int D) {
   const size_t rows = (size_t)B * Hkv * Skv;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   return up(rows * NSLICE * dp * 2) + up(rows * 4) + up(rows * NLO * 8) + up((size_t)B * Hkv * dp * 4) +
-         up(rows * dp * 4) + up(rows * (dp / 32) * 4) + up(ktc_bytes(B, Hkv, Skv, dp)) + up(vtc_bytes(B, Hkv, Skv, dp));
+         up(rows * dp * 4) + up(rows * (dp / 32) * 4) + up(ktc_bytes(B, Hkv, Skv, dp)) + up(vtc_bytes(B, Hkv, Skv, dp)) +
+         up(spill_bytes(dp));
 }
 
 KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v) {
@@ -167,6 +170,8 @@ KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v) {
   p.ntk = (Skv + KTILE - 1) / KTILE;
   c += up(ktc_bytes(B, Hkv, Skv, dp));
   p.vtc = dp == 128 ? (unsigned char*)c : nullptr;
+  c += up(vtc_bytes(B, Hkv, Skv, dp));
+  p.spill = dp == 128 ? (long long*)c : nullptr;
   return p;
 }
 
