@@ -38,6 +38,11 @@ METRIC = "exact attention MACs/s (S=4096,D=128,bf16) and % of binding INT/FP64 p
 UNIT = "MAC/s"
 
 
+# DRAM bytes (read + write) of one accumulate launch at the metric workload, from the ncu capture
+# summarised in profiles/ (4-head case scaled by 4: the traffic is per head); None until captured
+ACC_TRAFFIC_PER_LAUNCH = None
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -236,16 +241,17 @@ def run_ours(args, rank, world, local_rank):
     macs = w.attn_macs
     value = macs * world / (ms * 1e-3)
     e2e_val = macs * world / (statistics.mean(e2e_ms) * 1e-3)
-    # roofline of the dominant kernel (accumulate): integer multiply-add pipe
+    # roofline of the dominant kernel (accumulate): its MMAs on the tensor cores.  Per 128-key tile of
+    # 16 query rows it issues 32 score MMAs (M128 N64 K16), 24 PV MMAs (M128 N160 K16) and 8 DEN MMAs
+    # (M128 N16 K16): the integer digit decomposition of the exact products (16-bit operands).
     pk = _peaks()
     sm_clock = (ck or {}).get("sm_mhz") or pk.get("clocks_under_load", {}).get("sm_mhz_median") or 1447.0
-    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
-    # measured ceiling of exact 32x32->64 multiply-accumulates on this GPU: ~28 per clock per SM
-    imadw_per_clk_sm = 28.0
-    peak = n_sm * imadw_per_clk_sm * sm_clock * 1e6 / 1e12           # T multiply-adds / s at the sampled clock
     acc_ms = statistics.mean(k_acc)
-    acc_ops = w.pairs * 2 * w.D                                       # 2D PV multiply-adds per pair (integer pipe)
-    achieved = acc_ops / (acc_ms * 1e-3) / 1e12
+    tile_macs = 32 * 128 * 64 * 16 + 24 * 128 * 160 * 16 + 8 * 128 * 16 * 16
+    tiles = w.B * w.Hq * sum(-(-min(w.S, 16 * (qi + 1)) // 128) for qi in range(-(-w.S // 16)))
+    achieved = 2.0 * tile_macs * tiles / (acc_ms * 1e-3) / 1e12       # TFLOP/s
+    peak = pk.get("bf16_tflops") or 1900.0
+    peak_src = "measured burst bf16 (MEASURED_PEAKS.json)" if pk.get("bf16_tflops") else "fallback 1.9 PFLOP/s bf16"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
@@ -256,11 +262,12 @@ def run_ours(args, rank, world, local_rank):
                    "attn_macs_per_step": macs, "pairs_per_step": w.pairs},
         "method_macs_per_s": w.pairs * 3 * w.D * world / (ms * 1e-3),
         "kernels_ms": {"rowmax": statistics.mean(k_rowmax), "accumulate": acc_ms, "finalize": statistics.mean(k_fin)},
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "T int64 MAC/s",
-                     "frac": achieved / peak, "traffic": None,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": ACC_TRAFFIC_PER_LAUNCH if args.heads == 16 else None,
                      "kernel": "accumulate",
-                     "peak_basis": f"{n_sm} SMs x {imadw_per_clk_sm:g} exact 32x32->64 MACs/clk/SM (probed ceiling) x "
-                                   f"{sm_clock:g} MHz (sampled SM clock)"},
+                     "peak_basis": f"{peak_src}; f16 operands run at the bf16 rate; "
+                                   f"{tiles} key tiles x {tile_macs} MACs per launch",
+                     "sm_mhz": sm_clock},
         "clocks": ck,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": statistics.mean(e2e_ms)},

@@ -140,6 +140,40 @@ __device__ __forceinline__ void carry_digits(long long (&dg)[N]) {
   }
 }
 
+// Fold one tile's PV accumulators (12 diagonals x this thread's 4 rows, TMEM address pvb) into
+// the integer digits acc[r][g] (g: diagonals 4 g .. 4 g + 3), zero them and release the buffer.
+// A function rather than a lambda so that it is always inlined and acc stays in registers.
+__device__ __forceinline__ void drain_pv(long long (&acc)[4][3], uint32_t pvb, uint64_t* done, uint64_t* freeb,
+                                         uint32_t parity, volatile int* abort, int lane) {
+  using L = AccTpLayout;
+  bool ok = true;
+  if (lane == 0) ok = tc5::mbar_wait(done, parity, abort, 64);
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  tc5::fence_after();
+  if (ok) {
+#pragma unroll
+    for (int g3 = 0; g3 < 3; g3++) {
+      float pv[4][4];
+#pragma unroll
+      for (int c = 0; c < 4; c++) tc5::ld_x4(pvb + (4 * g3 + c) * L::BM, pv[c]);
+      tc5::ld_wait();
+#pragma unroll
+      for (int r = 0; r < 4; r++) {
+        long long s = 0;
+#pragma unroll
+        for (int c = 0; c < 4; c++) s += (long long)__float2int_rn(pv[c][r]) * (1ll << (8 * c));   // |P_c| < 2^24
+        acc[r][g3] += s;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < L::NPD; c++) tc5::st_zero_x4(pvb + c * L::BM);
+    tc5::st_wait();
+  }
+  tc5::fence_before();
+  __syncwarp();
+  if (lane == 0) tc5::mbar_arrive(freeb);
+}
+
 template <int DT>
 __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(const AttnArgs a, const KvPrep p) {
   using T = typename In<DT>::T;
@@ -373,29 +407,8 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         };
         // fold the PV accumulators of one tile into the integer digits, zero them, release them
         auto drain = [&](uint32_t tt) {
-          const uint32_t pvb = lane_base + L::PV_COL + (tt & 1) * L::PV_BUF + rg * 4;
-          if (warp_wait(&pvdone[tt & 1], (tt >> 1) & 1)) {
-  #pragma unroll
-            for (int g3 = 0; g3 < 3; g3++) {   // diagonals 4 g3 .. 4 g3 + 3 -> digit g3
-              float pv[4][4];
-  #pragma unroll
-              for (int c = 0; c < 4; c++) tc5::ld_x4(pvb + (4 * g3 + c) * BM, pv[c]);
-              tc5::ld_wait();
-  #pragma unroll
-              for (int r = 0; r < 4; r++) {
-                long long s = 0;
-  #pragma unroll
-                for (int c = 0; c < 4; c++) s += (long long)__float2int_rn(pv[c][r]) * (1ll << (8 * c));   // |P_c| < 2^24
-                acc[r][g3] += s;
-              }
-            }
-  #pragma unroll
-            for (int c = 0; c < L::NPD; c++) tc5::st_zero_x4(pvb + c * BM);
-            tc5::st_wait();
-          }
-          tc5::fence_before();
-          __syncwarp();
-          if (lane == 0) tc5::mbar_arrive(&pvfree[tt & 1]);
+          drain_pv(acc, lane_base + L::PV_COL + (tt & 1) * L::PV_BUF + rg * 4, &pvdone[tt & 1], &pvfree[tt & 1],
+                   (tt >> 1) & 1, &s_abort, lane);
         };
         // key meta and the V-bad words of this thread's key in tile t (zeros past the range)
         auto tile_meta = [&](int t, int& mv, uint4& vb) {
