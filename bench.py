@@ -39,8 +39,9 @@ UNIT = "MAC/s"
 
 
 # DRAM bytes (read + write) of one accumulate launch at the metric workload, from the ncu capture
-# summarised in profiles/ (4-head case scaled by 4: the traffic is per head); None until captured
-ACC_TRAFFIC_PER_LAUNCH = None
+# summarised in profiles/accumulate_tp_long_context_C3_H4.md (the 4-head case scaled by 4: the
+# traffic is per head); set to None whenever the kernel changes until it is captured again
+ACC_TRAFFIC_PER_LAUNCH = 4 * 466.6e6
 
 
 def _peaks():
@@ -119,7 +120,7 @@ def run_reference(args, rank, world):
     w = W.c3()
     Q, K, V = w.tensors("cpu")
     cores = os.cpu_count() or 1
-    rows_per_head = args.ref_rows
+    rows_per_head = args.ref_rows_step
     vals = []
     for s in range(args.warmup + args.steps):
         macs, dt, sample = oracle_sample(w, Q, K, V, rows_per_head, cores)
@@ -287,7 +288,10 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--ref-rows", type=int, default=16, help="oracle sample: query rows per head")
+    ap.add_argument("--ref-rows", type=int, default=3072,
+                    help="cpu_baseline sample: query rows per head (about 10-20 s of the oracle on 16 cores)")
+    ap.add_argument("--ref-rows-step", type=int, default=1024,
+                    help="--impl reference: query rows per head in each timed step (a few seconds each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=16, help="heads of the workload (16 = the metric workload)")
     args = ap.parse_args()
