@@ -84,7 +84,8 @@ struct RowmaxTcLayout {
   static constexpr size_t q_bytes = (size_t)NDS * q_step;
   static constexpr size_t k_off = q_bytes;
   static constexpr size_t bytes = k_off + (size_t)NST * KT_BLOCK;
-  static_assert(NSLICE * NSLICE * BM <= TCOLS, "TMEM columns");
+  static constexpr int SETC = NDIAG * BM;   // one set of diagonal sums: column BM c + row
+  static_assert(2 * SETC <= TCOLS, "TMEM columns");
   static_assert(bytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
   extern __shared__ __align__(1024) unsigned char smem_t[];
   unsigned char* Qs = smem_t;
   unsigned char* Kst = smem_t + L::k_off;
-  __shared__ __align__(8) uint64_t full[NST], empty[NST], tfull, tempty, fin;
+  __shared__ __align__(8) uint64_t full[NST], empty[NST], tfull[2], tempty[2], fin;
   __shared__ uint32_t tmem_s;
   __shared__ int Fq[BM], rkey[BM];
   __shared__ unsigned char qlon[BM];
@@ -134,8 +135,10 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
       tc5::mbar_init(&full[s], 1);
       tc5::mbar_init(&empty[s], 1);
     }
-    tc5::mbar_init(&tfull, NISS);
-    tc5::mbar_init(&tempty, NEPI);
+    for (int s = 0; s < 2; s++) {   // two diagonal sets: one tile's MMAs run while the epilogue reads the last
+      tc5::mbar_init(&tfull[s], NISS);
+      tc5::mbar_init(&tempty[s], NEPI);
+    }
     tc5::mbar_init(&fin, NISS);
     s_abort = 0;
     tc5::mbar_fence_init();
@@ -148,7 +151,7 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
   const uint32_t lbase = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (warp >> 2) * 8;
   if (warp < NEPI) {
 #pragma unroll
-    for (int g = 0; g < NSLICE * NSLICE; g++) tc5::st_zero_x8(lbase + g * BM);
+    for (int c = 0; c < 2 * NDIAG; c++) tc5::st_zero_x8(lbase + c * BM);
     tc5::st_wait();
   }
   tc5::fence_before();
@@ -193,16 +196,17 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
           const uint32_t g_step = g_base + ls, st = g_step % NST;
           const int k = (int)(ls % NDS);
           if (!tc5::mbar_wait(&full[st], (g_step / NST) & 1, &s_abort)) break;
-          if (k == (int)ii && tcount >= 1 && !tc5::mbar_wait(&tempty, (tcount - 1) & 1, &s_abort)) break;
+          const uint32_t set = tcount & 1;
+          if (k == (int)ii && tcount >= 2 && !tc5::mbar_wait(&tempty[set], ((tcount - 2) >> 1) & 1, &s_abort)) break;
           tc5::fence_after();
           const uint64_t ka = tc5::desc(tc5::smem_addr(Kst + st * KT_BLOCK));
           const uint64_t qa = tc5::desc(tc5::smem_addr(Qs + k * L::q_step));
 #pragma unroll
-          for (int sa = 0; sa < NSLICE; sa++)   // descriptor start addresses advance in 16-byte units
-            tc5::mma_bf16(tmem + sa * NQ, ka + (uint64_t)(sa * KTILE * 2), qa, IDESC, 1u);
+          for (int sa = 0; sa < NSLICE; sa++)   // D offset by BM per key slice: the diagonals add themselves
+            tc5::mma_bf16(tmem + set * L::SETC + sa * BM, ka + (uint64_t)(sa * KTILE * 2), qa, IDESC, 1u);
           tc5::commit(&empty[st]);
           if (k + NISS >= NDS) {   // this issuer's last step of the tile
-            tc5::commit(&tfull);
+            tc5::commit(&tfull[set]);
             tcount++;
           }
         }
@@ -217,34 +221,21 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
         const int j = a.kv_lo + t * KTILE + jl;
         const bool vj = j < hi;
         const int mv = vj ? p.kmeta[krow0 + j] : 0;
-        if (!__all_sync(0xFFFFFFFFu, tc5::mbar_wait(&tfull, tcount & 1, &s_abort, 128))) break;   // warp-uniform
+        const uint32_t set = tcount & 1;
+        bool tok = true;
+        if (lane == 0) tok = tc5::mbar_wait(&tfull[set], (tcount >> 1) & 1, &s_abort, 128);
+        if (!__shfl_sync(0xFFFFFFFFu, tok, 0)) break;   // warp-uniform
         tc5::fence_after();
         float v[NDIAG][8];   // diagonal sums of this thread's 8 rows, exact
 #pragma unroll
-        for (int rr = 0; rr < 8; rr += 4) {
-          float d[NSLICE][NSLICE][4];
+        for (int c = 0; c < NDIAG; c++) tc5::ld_x8(lbase + set * L::SETC + c * BM, v[c]);
+        tc5::ld_wait();
 #pragma unroll
-          for (int sa = 0; sa < NSLICE; sa++)
-#pragma unroll
-            for (int sb = 0; sb < NSLICE; sb++) tc5::ld_x4(lbase + sa * NQ + sb * BM + rr, d[sa][sb]);
-          tc5::ld_wait();
-#pragma unroll
-          for (int e = 0; e < 4; e++)
-#pragma unroll
-            for (int c = 0; c < NDIAG; c++) {
-              float acc = 0.0f;
-#pragma unroll
-              for (int sa = 0; sa < NSLICE; sa++)
-                if (c - sa >= 0 && c - sa < NSLICE) acc = __fadd_rn(acc, d[sa][c - sa][e]);
-              v[c][rr + e] = acc;
-            }
-        }
-#pragma unroll
-        for (int g = 0; g < NSLICE * NSLICE; g++) tc5::st_zero_x8(lbase + g * BM);
+        for (int c = 0; c < NDIAG; c++) tc5::st_zero_x8(lbase + set * L::SETC + c * BM);
         tc5::st_wait();
         tc5::fence_before();
         __syncwarp();
-        if (lane == 0) tc5::mbar_arrive(&tempty);
+        if (lane == 0) tc5::mbar_arrive(&tempty[set]);
         tcount++;
         float thr[8];   // the rows' running maxima so far (exact scores)
 #pragma unroll
