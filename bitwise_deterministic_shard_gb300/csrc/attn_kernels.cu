@@ -90,7 +90,8 @@ struct RowmaxTcLayout {
 };
 
 // true when the score RN32(scale * RN32(T 2^E)) cannot exceed `bound` and is finite
-__device__ __forceinline__ bool score_below(const float (&v)[NDIAG][8], int r, int E, float scale, float bound) {
+template <int N>
+__device__ __forceinline__ bool score_below(const float (&v)[NDIAG][N], int r, int E, float scale, float bound) {
   if (E < -126 || E > 127) return false;
   float t = v[NDIAG - 1][r], m = fabsf(v[NDIAG - 1][r]);
 #pragma unroll
@@ -226,10 +227,40 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
         if (lane == 0) tok = tc5::mbar_wait(&tfull[set], (tcount >> 1) & 1, &s_abort, 128);
         if (!__shfl_sync(0xFFFFFFFFu, tok, 0)) break;   // warp-uniform
         tc5::fence_after();
-        float v[NDIAG][8];   // diagonal sums of this thread's 8 rows, exact
+        float thr[8];   // the rows' running maxima so far (exact scores)
 #pragma unroll
-        for (int c = 0; c < NDIAG; c++) tc5::ld_x8(lbase + set * L::SETC + c * BM, v[c]);
-        tc5::ld_wait();
+        for (int r = 0; r < 8; r++) thr[r] = fmaxf(mrun[r], key_float(rkey[rg * 8 + r]));
+        const int Fk = kmeta_F(mv), kf = kmeta_fit(mv);
+        uint32_t defer = 0;   // rows whose pair with this key needs the exact fallback
+#pragma unroll
+        for (int hf = 0; hf < 2; hf++) {   // rows 4 hf .. 4 hf + 3: half the diagonal sums live at a time
+          float v[NDIAG][4];   // diagonal sums of these 4 rows, exact
+#pragma unroll
+          for (int c = 0; c < NDIAG; c++) tc5::ld_x4(lbase + set * L::SETC + c * BM + 4 * hf, v[c]);
+          tc5::ld_wait();
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            const int r = 4 * hf + e, rl = rg * 8 + r, i = q0 + rl;
+            if (vj && i < a.Sq && (!a.causal || j <= i)) {
+              if (qfit[rl] && kf) {
+                const int E = Fq[rl] + Fk;
+                if (!score_below(v, e, E, a.scale32, thr[r])) {
+                  const float sc = __fmul_rn(a.scale32, cr32_scaled(combine_diag(v, e), E));
+                  if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
+                  mrun[r] = sc > mrun[r] ? sc : mrun[r];
+                }
+              } else if (qlon[rl] != LO_DEEP && kmeta_lon(mv) != KLO_DEEP) {   // truncated dot + low limbs
+                const float sc = __fmul_rn(
+                    a.scale32, dot_lo<DT>(combine_diag(v, e), qbase + (int64_t)i * a.qs[2], Fq[rl], qlo[rl], qlon[rl],
+                                          kbase + (int64_t)j * a.ks[2], Fk, p.klo + (krow0 + j) * NLO, kmeta_lon(mv)));
+                if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
+                mrun[r] = sc > mrun[r] ? sc : mrun[r];
+              } else {
+                defer |= 1u << rl;   // a deep row: the warp's exact dot below
+              }
+            }
+          }
+        }
 #pragma unroll
         for (int c = 0; c < NDIAG; c++) tc5::st_zero_x8(lbase + set * L::SETC + c * BM);
         tc5::st_wait();
@@ -237,33 +268,6 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
         __syncwarp();
         if (lane == 0) tc5::mbar_arrive(&tempty[set]);
         tcount++;
-        float thr[8];   // the rows' running maxima so far (exact scores)
-#pragma unroll
-        for (int r = 0; r < 8; r++) thr[r] = fmaxf(mrun[r], key_float(rkey[rg * 8 + r]));
-        const int Fk = kmeta_F(mv), kf = kmeta_fit(mv);
-        uint32_t defer = 0;   // rows whose pair with this key needs the exact fallback
-#pragma unroll
-        for (int r = 0; r < 8; r++) {
-          const int rl = rg * 8 + r, i = q0 + rl;
-          if (vj && i < a.Sq && (!a.causal || j <= i)) {
-            if (qfit[rl] && kf) {
-              const int E = Fq[rl] + Fk;
-              if (!score_below(v, r, E, a.scale32, thr[r])) {
-                const float sc = __fmul_rn(a.scale32, cr32_scaled(combine_diag(v, r), E));
-                if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
-                mrun[r] = sc > mrun[r] ? sc : mrun[r];
-              }
-            } else if (qlon[rl] != LO_DEEP && kmeta_lon(mv) != KLO_DEEP) {   // truncated dot + low limbs
-              const float sc = __fmul_rn(
-                  a.scale32, dot_lo<DT>(combine_diag(v, r), qbase + (int64_t)i * a.qs[2], Fq[rl], qlo[rl], qlon[rl],
-                                        kbase + (int64_t)j * a.ks[2], Fk, p.klo + (krow0 + j) * NLO, kmeta_lon(mv)));
-              if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
-              mrun[r] = sc > mrun[r] ? sc : mrun[r];
-            } else {
-              defer |= 1u << rl;   // a deep row: the warp's exact dot below
-            }
-          }
-        }
         // deferred pairs of this warp, one at a time with the whole warp
         for (uint32_t pend = __ballot_sync(0xFFFFFFFFu, defer != 0); pend; pend = __ballot_sync(0xFFFFFFFFu, defer != 0)) {
           const int src = __ffs(pend) - 1;
