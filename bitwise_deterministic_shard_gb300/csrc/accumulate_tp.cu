@@ -45,9 +45,9 @@
 // (key, the four weights) and their products added after the tiles; smaller weights take
 // whole-product atomics.
 //
-// Roles (lane 0 of each control warp): warp 16 copies key operand steps (4-stage ring), warp
-// 17 issues the score MMAs, warp 18 the PV and DEN MMAs, warp 19 copies V digit blocks
-// (NVB-stage ring).  Warps 0-15 read the score diagonals, compute weights, write the weight digit
+// Roles: warp 16 copies key operand steps (lane 0, 4-stage ring) and V digit blocks (lane 1,
+// NVB-stage ring), warps 17 and 19 (lane 0) issue the score MMAs of alternate 16-dimension
+// steps, warp 18 (lane 0) the PV and DEN MMAs.  Warps 0-15 read the score diagonals, compute weights, write the weight digit
 // planes and drain the PV accumulators; each zeroes the TMEM it read before releasing it,
 // so every MMA accumulates.  Every mbarrier wait is bounded; one that gives up sets
 // DA_STATUS_TIMEOUT, and a failed wait in the compute warps only skips work.
@@ -60,9 +60,9 @@ namespace detattn {
 
 struct AccTpLayout {
   static constexpr int DP = 128, BM = 16, NDS = DP / 16, NSK = 4, NVB = 4, NCW = 16;
-  // warps: NCW compute (four warpgroups) and the control warpgroup: key copies, score MMAs,
-  // PV and DEN MMAs, V copies (lane 0 of each)
-  static constexpr int LOADW = NCW, ISSW = NCW + 1, PISSW = NCW + 2, VLOADW = NCW + 3, THREADS = 32 * (NCW + 4);
+  // warps: NCW compute (four warpgroups) and the control warpgroup: copies (lane 0 key steps,
+  // lane 1 V blocks), score MMAs of even steps, PV and DEN MMAs, score MMAs of odd steps
+  static constexpr int LOADW = NCW, ISSW = NCW + 1, PISSW = NCW + 2, ISSW2 = NCW + 3, THREADS = 32 * (NCW + 4);
   static constexpr int NWP = 10, NVP = 3, NPD = NWP + NVP - 1, NKB = KTILE / VKEYS;
   static constexpr int NQ = NSLICE * BM;                              // score MMA N: the stacked query slices
   static constexpr int NW16 = NWP * BM;                               // PV MMA N: the stacked weight digits
@@ -249,13 +249,13 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
       tc5::mbar_init(&vempty[s], 1);
     }
     for (int s = 0; s < 2; s++) tc5::mbar_init(&wready[s], NCW);
-    tc5::mbar_init(&sfull, 1);
+    tc5::mbar_init(&sfull, 2);   // one commit per score issuer
     tc5::mbar_init(&sempty, NCW);
     for (int s = 0; s < 2; s++) {
       tc5::mbar_init(&pvdone[s], 1);
       tc5::mbar_init(&pvfree[s], NCW);
     }
-    tc5::mbar_init(&fin, 2);   // the score issuer and the PV issuer
+    tc5::mbar_init(&fin, 3);   // the score issuers and the PV issuer
     s_abort = 0;
     tc5::mbar_fence_init();
   }
@@ -297,15 +297,15 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
       const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
       const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
       tc5::bar_sync(2, L::THREADS);
-      if (warp == L::LOADW || warp == L::VLOADW) {   // ---------------- bulk copies ----------------
-        if (warp == L::LOADW && lane == 0) {   // key operand steps
+      if (warp == L::LOADW) {   // ---------------- bulk copies ----------------
+        if (lane == 0) {   // key operand steps
           for (int ls = 0; ls < nkt * NDS && !s_abort; ls++) {
             const uint32_t g = tc * NDS + ls, st = g % NSK;
             if (g >= NSK && !tc5::mbar_wait(&kempty[st], ((g / NSK) - 1) & 1, &s_abort, 64)) break;
             tc5::mbar_expect_tx(&kfull[st], KT_BLOCK);
             tc5::bulk_g2s(Kst + st * KT_BLOCK, ktc + (size_t)ls * KT_BLOCK, KT_BLOCK, &kfull[st]);
           }
-        } else if (warp == L::VLOADW && lane == 0) {   // V digit blocks
+        } else if (lane == 1) {   // V digit blocks
           for (int lb = 0; lb < nkt * NKB && !s_abort; lb++) {
             const uint32_t g = tc * NKB + lb, sl = g % NVB;
             if (g >= NVB && !tc5::mbar_wait(&vempty[sl], ((g / NVB) - 1) & 1, &s_abort, 64)) break;
@@ -314,12 +314,12 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           }
         }
       } else {
-        if (warp == L::ISSW && lane == 0) {   // ---------------- score MMAs ----------------
-          for (int ls = 0; ls < nkt * NDS && !s_abort; ls++) {
+        if ((warp == L::ISSW || warp == L::ISSW2) && lane == 0) {   // ---------------- score MMAs: alternate steps ----------------
+          for (int ls = warp == L::ISSW ? 0 : 1; ls < nkt * NDS && !s_abort; ls += 2) {
             const uint32_t g = tc * NDS + ls, st = g % NSK, tt = tc + ls / NDS;
             const int k = ls % NDS;
             if (!tc5::mbar_wait(&kfull[st], (g / NSK) & 1, &s_abort, 32)) break;
-            if (k == 0 && tt >= 1 && !tc5::mbar_wait(&sempty, (tt - 1) & 1, &s_abort, 64)) break;
+            if (k < 2 && tt >= 1 && !tc5::mbar_wait(&sempty, (tt - 1) & 1, &s_abort, 64)) break;
             tc5::fence_after();
             const uint64_t ka = tc5::desc(tc5::smem_addr(Kst + st * KT_BLOCK));
             const uint64_t qa = tc5::desc(tc5::smem_addr(Qs + k * L::q_step));
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
             for (int sa = 0; sa < NSLICE; sa++)   // descriptor start addresses advance in 16-byte units
               tc5::mma_bf16(tmem + L::SC_COL + sa * BM, ka + (uint64_t)(sa * KTILE * 2), qa, IDESC_S, 1u);
             tc5::commit(&kempty[st]);
-            if (k == NDS - 1) tc5::commit(&sfull);
+            if (k >= NDS - 2) tc5::commit(&sfull);   // this issuer's last step of the tile
           }
         } else if (warp == L::PISSW && lane == 0) {   // ---------------- PV and DEN MMAs ----------------
           const uint64_t ones = tc5::desc(tc5::smem_addr(smem_p + L::one_off));
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
       tc += nkt;
       tc5::bar_sync(3, L::THREADS);
     }
-    if ((warp == L::ISSW || warp == L::PISSW) && lane == 0) {   // every MMA has completed before TMEM is released
+    if ((warp == L::ISSW || warp == L::PISSW || warp == L::ISSW2) && lane == 0) {   // every MMA has completed before TMEM is released
       tc5::commit(&fin);
       tc5::mbar_wait(&fin, 0, &s_abort);
     }
