@@ -41,7 +41,7 @@ UNIT = "MAC/s"
 # DRAM bytes (read + write) of one accumulate launch at the metric workload, from the ncu capture
 # summarised in profiles/accumulate_tp_long_context_C3_H4.md (the 4-head case scaled by 4: the
 # traffic is per head); set to None whenever the kernel changes until it is captured again
-ACC_TRAFFIC_PER_LAUNCH = 4 * 466.6e6
+ACC_TRAFFIC_PER_LAUNCH = 4 * 468.5e6
 
 
 def _peaks():
