@@ -491,3 +491,73 @@ def dce_forward(logits, targets, splits=None):
     den = normalize_den(compose_add([dce_denom_digits(X, m, a, b)[0] for a, b in bounds]))
     loss, denom, _ = dce_finalize(den, X, targets, m)
     return loss, denom, m, den
+
+
+# ----------------------------------------------------------------------------------------
+# det-cross-entropy: backward and reductions ("API": cross_entropy(logits, targets,
+# reduction) with a deterministic dLogits; "Method": the gradient softmax(x_i) -
+# onehot(t_i)).  The pages fix the gradient's value and that it reuses forward's
+# (loss, rowmax, denom); they do not print its rounding sequence.  Reading: each step is
+# one IEEE rounding of its exact result, in this order:
+#   w_iv = exp32_det(RN32(x_iv - m_i))                  (the forward's weights)
+#   p_iv = RN32(RN64(w_iv / denom_i))                   (denom_i = RN64(den_i), f64)
+#   g_iv = RN32(p_iv - [v == t_i])
+#   dLogits_iv = RN32(go_i * g_iv)
+# with go_i the upstream gradient of loss_i: grad[i] ("none"), grad ("sum"),
+# RN32(RN64(grad / N)) ("mean").  A target outside [0, V) subtracts nothing.
+# Reductions: "sum" = RN32(RN64(S)), "mean" = RN32(RN64(RN64(S) / N)), S the exact sum of
+# the f32 losses (a NaN loss makes the result NaN).
+# ----------------------------------------------------------------------------------------
+
+def dce_go(grad, N: int, reduction: str) -> np.ndarray:
+    """Per-row upstream gradient go_i of the loss for the given reduction."""
+    g = np.asarray(grad, dtype=np.float32).reshape(-1)
+    if reduction == "none":
+        return g.astype(np.float32)
+    if reduction == "sum":
+        return np.full(N, g[0], dtype=np.float32)
+    if reduction == "mean":
+        return np.full(N, np.float32(float(g[0]) / N), dtype=np.float32)
+    raise ValueError(reduction)
+
+
+def dce_backward(logits, targets, m, denom, go) -> np.ndarray:
+    """dLogits (float32 [N, V]) of the cross-entropy loss, in the reading above."""
+    X = decode(logits)
+    N, Vn = X.shape
+    out = np.zeros((N, Vn), dtype=np.float32)
+    one = np.float32(1.0)
+    for i in range(N):
+        mi = float(m[i])
+        d64 = float(denom[i])
+        t = int(targets[i])
+        gi = np.float32(go[i])
+        for v in range(Vn):
+            x = float(X[i, v])
+            if np.isfinite(x) and np.isfinite(mi):
+                xr = rn32(Fraction(x) - Fraction(mi))
+            else:
+                xr = float(np.float32(x) - np.float32(mi))   # IEEE inf / NaN arithmetic
+            if xr > 0:
+                xr = 0.0                                      # above the rowmax: clamped as in forward
+            w = exp32_det(xr)
+            p = np.float32(w / d64)             # Python float division is RN64; np.float32 is RN32
+            g = p - one if v == t else p        # float32 arithmetic: one RN32
+            out[i, v] = gi * g
+    return out
+
+
+def dce_reduce(loss, reduction: str) -> np.float32:
+    """sum / mean of the f32 losses through their exact sum."""
+    L = np.asarray(loss, dtype=np.float32).reshape(-1)
+    if np.isnan(L).any():
+        return np.float32(np.nan)
+    if np.isinf(L).any():
+        return np.float32(np.sum(L.astype(np.float64)))   # +inf, or NaN for +inf and -inf
+    S = sum((Fraction(float(x)) for x in L), Fraction(0))
+    s64 = rn64(S)
+    if reduction == "sum":
+        return np.float32(s64)
+    if reduction == "mean":
+        return np.float32(s64 / len(L))
+    raise ValueError(reduction)
