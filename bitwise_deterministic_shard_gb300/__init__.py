@@ -76,8 +76,11 @@ def lib():
         L.dce_rowmax.argtypes = [M, _I64, _I64, _P, _P, _P]
         L.dce_denom_digits.argtypes = [M, _P, _I64, _I64, _P, _I32, _P, _P]
         L.dce_finalize.argtypes = [_P, M, _P, _P, _P, _P, _P, _P]
+        L.dce_backward.argtypes = [M, _P, _P, _P, _P, _I32, _P, _P, _P]
+        L.dce_reduce.argtypes = [_P, _I64, _I32, _P, _P]
         for f in ("da_rowmax", "da_accumulate", "da_compose_max", "da_compose_add", "da_normalize", "da_finalize",
-                  "da_det_attn", "da_det_attn_sharded", "dce_rowmax", "dce_denom_digits", "dce_finalize"):
+                  "da_det_attn", "da_det_attn_sharded", "dce_rowmax", "dce_denom_digits", "dce_finalize",
+                  "dce_backward", "dce_reduce"):
             getattr(L, f).restype = C.c_int
         _lib = L
     return _lib
@@ -320,6 +323,67 @@ def dce_forward(logits, targets, splits=None, status=None):
         den = dce_denom_digits(logits, m, a, b, den=den, add_into=k > 0, status=status)
     loss, denom = dce_finalize(den, logits, targets, m, status=status)
     return loss, denom, m, den
+
+
+_REDUCTIONS = {"none": 0, "sum": 1, "mean": 2}
+
+
+def dce_backward(logits, targets, m, denom, grad, reduction="none", status=None):
+    """Deterministic dLogits of the cross-entropy loss from forward's state (m, denom):
+    RN32(go_i * RN32(RN32(RN64(w / denom_i)) - onehot)), w = exp32_det(RN32(x - m_i));
+    go_i = grad[i] ("none"), grad ("sum"), RN32(RN64(grad / N)) ("mean").  Returns a tensor
+    shaped like logits, of its dtype."""
+    M, keep = _matrix(logits)
+    red = _REDUCTIONS[reduction]
+    grad = grad.to(torch.float32).reshape(-1).contiguous()
+    if grad.numel() != (M.rows if red == 0 else 1):
+        raise DetAttnError("grad must have one entry per row for reduction='none', else one entry")
+    targets = targets.to(torch.int64).contiguous()
+    out = torch.empty((M.rows, M.cols), dtype=logits.dtype, device=logits.device)
+    _check(lib().dce_backward(C.byref(M), _ptr(targets), _ptr(m), _ptr(denom), _ptr(grad), red, _ptr(out),
+                              _ptr(status), _stream()), "dce_backward")
+    return out
+
+
+def dce_reduce(loss, reduction="mean"):
+    """sum / mean of the f32 losses through their exact (Kulisch) sum, independent of the
+    rows' order: RN32(RN64(S)) / RN32(RN64(RN64(S) / N))."""
+    loss = loss.to(torch.float32).contiguous()
+    out = torch.empty((), dtype=torch.float32, device=loss.device)
+    _check(lib().dce_reduce(_ptr(loss), loss.numel(), _REDUCTIONS[reduction], _ptr(out), _stream()), "dce_reduce")
+    return out
+
+
+def forward(logits, targets, splits=None, status=None):
+    """Fused cross-entropy forward (det-cross-entropy "API": forward): (loss [N], rowmax [N],
+    denom [N]), the state the backward reuses.  Vocab splits compose by max and digit add."""
+    loss, denom, m, den = dce_forward(logits, targets, splits=splits, status=status)
+    return loss, m, denom
+
+
+class _CrossEntropy(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, logits, targets, reduction, splits, status):
+        loss, m, denom = forward(logits, targets, splits=splits, status=status)
+        ctx.save_for_backward(logits, targets, m, denom)
+        ctx.reduction, ctx.status = reduction, status
+        return loss if reduction == "none" else dce_reduce(loss, reduction)
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        logits, targets, m, denom = ctx.saved_tensors
+        g = dce_backward(logits, targets, m, denom, grad_out.detach(), ctx.reduction, status=ctx.status)
+        return g, None, None, None, None
+
+
+def cross_entropy(logits, targets, reduction="mean", splits=None, status=None):
+    """Bitwise-deterministic cross-entropy with autograd (det-cross-entropy "API":
+    cross_entropy(logits, targets, reduction)).  Loss and dLogits are the same bytes for any
+    vocab split (splits: column counts summing to V) and any run.  logits: [N, V] f32 or bf16
+    on the GPU; targets: [N] integer."""
+    if reduction not in _REDUCTIONS:
+        raise DetAttnError("reduction must be 'none', 'sum' or 'mean'")
+    return _CrossEntropy.apply(logits, targets, reduction, splits, status)
 
 
 STATIC_MAX_ROWS = 65536

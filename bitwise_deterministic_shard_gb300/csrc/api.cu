@@ -311,4 +311,26 @@ DA_EXPORT int dce_finalize(const int64_t* den, const da_matrix* logits, const in
   return launched(launch_dce_finalize(a, (cudaStream_t)stream));
 }
 
+DA_EXPORT int dce_backward(const da_matrix* logits, const int64_t* targets, const float* m, const double* denom,
+                           const float* grad, int reduction, void* dlogits, int32_t* dev_status, da_stream_t stream) {
+  int e = check_matrix(logits);
+  if (e) return e;
+  if (reduction < 0 || reduction > 2) return DA_EINVAL;
+  if (logits->rows == 0 || logits->cols == 0) return DA_OK;
+  if (!targets || !m || !denom || !grad || !dlogits) return DA_EINVAL;
+  if (!aligned(targets, 8) || !aligned(m, 4) || !aligned(denom, 8) || !aligned(grad, 4) ||
+      !aligned(dlogits, logits->dtype == 0 ? 4 : 2))
+    return DA_EALIGN;
+  DceArgs a = make_dce(logits);
+  a.targets = targets; a.m_in = m; a.denom = (double*)denom; a.status = dev_status;
+  return launched(launch_dce_backward(a, grad, reduction, dlogits, (cudaStream_t)stream));
+}
+
+DA_EXPORT int dce_reduce(const float* loss, int64_t rows, int reduction, float* out, da_stream_t stream) {
+  if (rows < 0 || (reduction != 1 && reduction != 2)) return DA_EINVAL;
+  if ((!loss && rows > 0) || !out) return DA_EINVAL;
+  if (!aligned(loss, 4) || !aligned(out, 4)) return DA_EALIGN;
+  return launched(launch_dce_reduce(loss, rows, reduction, out, (cudaStream_t)stream));
+}
+
 }  // extern "C"

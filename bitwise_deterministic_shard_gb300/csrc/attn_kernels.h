@@ -86,6 +86,8 @@ struct DceArgs {
 };
 cudaError_t launch_dce_rowmax(const DceArgs& a, cudaStream_t st);
 cudaError_t launch_dce_denom(const DceArgs& a, cudaStream_t st);
+cudaError_t launch_dce_backward(const DceArgs& a, const float* grad, int reduction, void* dlogits, cudaStream_t st);
+cudaError_t launch_dce_reduce(const float* loss, int64_t N, int reduction, float* out, cudaStream_t st);
 cudaError_t launch_dce_finalize(const DceArgs& a, cudaStream_t st);
 
 }  // namespace detattn

@@ -1,5 +1,5 @@
 // det-cross-entropy kernels for sm_103a: vocab-range rowmax, exact denominator digits,
-// finalize to (loss, denom).
+// finalize to (loss, denom), the backward dLogits and the exact loss reductions.
 //
 // Page "det-cross-entropy", section "Method": m_i = max_v x_iv (order-invariant), then
 // den_i = sum_v exp(x_iv - m_i) in a Kulisch long accumulator of signed int64 digits;
@@ -10,6 +10,7 @@
 // One CTA streams one row of logits with 16-byte loads (HBM-bound: 4 B per f32 logit,
 // 2 B per bf16 logit) and keeps six int64 digits per thread; the CTA sum of digits is
 // exact, so the reduction order does not matter.
+#include <cuda_bf16.h>
 #include "numerics.cuh"
 #include "attn_kernels.h"
 
@@ -150,6 +151,109 @@ __global__ void dce_finalize_kernel(const DceArgs a) {
     a.loss[i] = __double2float_rn(__dadd_rn(log64_det(d64), diff));
   }
   report(a.status, st);
+}
+
+// Backward (page "det-cross-entropy", "API": cross_entropy with a deterministic dLogits;
+// "Method": the gradient softmax(x_i) - onehot(t_i)), one IEEE rounding per step:
+//   p = RN32(RN64(exp32_det(RN32(x - m)) / denom)),  g = RN32(p - [v == t]),
+//   dLogits = RN32(go * g),  go = grad[i] ("none"), grad[0] ("sum"), RN32(RN64(grad[0] / N))
+// ("mean").  A logit above the rowmax is clamped like the forward's (violation flag); NaN
+// propagates.  Streaming: 2 B or 4 B read and 2 B or 4 B written per logit; one CTA covers
+// BW_CHUNK columns of one row, consecutive threads consecutive columns.
+constexpr int BW_THREADS = 256, BW_CHUNK = 2048;
+
+template <int DT>
+__global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs a, const float* grad, int reduction,
+                                                                  void* dlogits) {
+  using T = typename In<DT>::T;
+  const int64_t nch = (a.V + BW_CHUNK - 1) / BW_CHUNK;
+  const int64_t i = blockIdx.x / nch, c0 = (blockIdx.x % nch) * BW_CHUNK;
+  const T* row = (const T*)a.x + i * a.rs;
+  const float m = a.m_in[i];
+  const double d64 = a.denom[i];
+  const int64_t t = a.targets[i];
+  float go = reduction == 0 ? grad[i] : grad[0];
+  if (reduction == 2) go = __double2float_rn(__ddiv_rn((double)go, (double)a.N));
+  int st = 0;
+#pragma unroll 4
+  for (int k = 0; k < BW_CHUNK / BW_THREADS; k++) {
+    const int64_t v = c0 + k * BW_THREADS + threadIdx.x;
+    if (v >= a.V) break;
+    float x = __fsub_rn(__uint_as_float(In<DT>::bits(row, v)), m);
+    if (x > 0.0f) {
+      st |= ST_VIOLATION;
+      x = 0.0f;
+    }
+    const float p = __double2float_rn(__ddiv_rn((double)exp32_det(x), d64));
+    const float g = v == t ? __fsub_rn(p, 1.0f) : p;
+    const float o = __fmul_rn(go, g);
+    if constexpr (DT == 0)
+      ((float*)dlogits)[i * a.V + v] = o;
+    else
+      ((__nv_bfloat16*)dlogits)[i * a.V + v] = __float2bfloat16_rn(o);
+  }
+  report(a.status, st);
+}
+
+// Loss reductions: S = the exact sum of the f32 losses (Kulisch words of 2^(32k - 320)),
+// "sum" = RN32(RN64(S)), "mean" = RN32(RN64(RN64(S) / N)); a NaN loss gives NaN, infinite
+// losses their IEEE sum.  One CTA: per-thread words, combined by exact shared-memory adds.
+__global__ void __launch_bounds__(256) dce_reduce_kernel(const float* loss, int64_t N, int reduction, float* out) {
+  __shared__ long long tot[KW];
+  __shared__ int flags;   // 1 NaN, 2 +inf, 4 -inf
+  for (int k = threadIdx.x; k < KW; k += blockDim.x) tot[k] = 0;
+  if (threadIdx.x == 0) flags = 0;
+  __syncthreads();
+  long long acc[KW];
+#pragma unroll
+  for (int k = 0; k < KW; k++) acc[k] = 0;
+  int fl = 0;
+  for (int64_t i = threadIdx.x; i < N; i += blockDim.x) {
+    const uint32_t u = __float_as_uint(loss[i]);
+    if (nonfinite_bits(u)) {
+      fl |= (u & 0x7FFFFFu) ? 1 : ((u >> 31) ? 4 : 2);
+      continue;
+    }
+    const Split s = split_f32(u);
+    kul_add(acc, s.mant, s.neg, s.lsb);
+    if ((i / blockDim.x) % 1024 == 1023) kul_carry(acc, KW);   // keep the words far from overflow
+  }
+  kul_carry(acc, KW);
+#pragma unroll
+  for (int k = 0; k < KW; k++)
+    if (acc[k]) atomicAdd((unsigned long long*)&tot[k], (unsigned long long)acc[k]);
+  if (fl) atomicOr(&flags, fl);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float r;
+    if (flags & 1 || (flags & 6) == 6) {
+      r = __int_as_float(0x7FC00000);
+    } else if (flags) {
+      r = __int_as_float(flags & 2 ? 0x7F800000 : 0xFF800000);
+    } else {
+      long long w[KW];
+#pragma unroll
+      for (int k = 0; k < KW; k++) w[k] = tot[k];
+      double s64 = digits_rn64<KW>(w, -320);
+      if (reduction == 2) s64 = __ddiv_rn(s64, (double)N);
+      r = s64 == s64 ? __double2float_rn(s64) : __int_as_float(0x7FC00000);   // 0 / 0: the canonical NaN
+    }
+    *out = r;
+  }
+}
+
+cudaError_t launch_dce_backward(const DceArgs& a, const float* grad, int reduction, void* dlogits, cudaStream_t st) {
+  if (a.N <= 0 || a.V <= 0) return cudaSuccess;
+  const int64_t blocks = a.N * ((a.V + BW_CHUNK - 1) / BW_CHUNK);
+  if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidValue;
+  if (a.dtype == 0) dce_backward_kernel<0><<<(unsigned)blocks, BW_THREADS, 0, st>>>(a, grad, reduction, dlogits);
+  else dce_backward_kernel<1><<<(unsigned)blocks, BW_THREADS, 0, st>>>(a, grad, reduction, dlogits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dce_reduce(const float* loss, int64_t N, int reduction, float* out, cudaStream_t st) {
+  dce_reduce_kernel<<<1, 256, 0, st>>>(loss, N, reduction, out);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_dce_rowmax(const DceArgs& a, cudaStream_t st) {

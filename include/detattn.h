@@ -176,6 +176,27 @@ int dce_denom_digits(const da_matrix* logits, const float* m, int64_t v_lo, int6
 int dce_finalize(const int64_t* den, const da_matrix* logits, const int64_t* targets, const float* m, float* loss,
                  double* denom, int32_t* dev_status, da_stream_t stream);
 
+/* det-cross-entropy "API", the deterministic dLogits of cross_entropy ("Method": the
+ * gradient softmax(x_i) - onehot(t_i)), from forward's state (rowmax m, denom; targets):
+ *   p = RN32(RN64(exp32_det(RN32(logits[i, v] - m[i])) / denom[i])),
+ *   g = RN32(p - [v == targets[i]]),  dlogits[i, v] = RN32(go_i * g),
+ * go_i = grad[i] for reduction 0 ("none", grad: device f32 [rows]), grad[0] for 1 ("sum"),
+ * RN32(RN64(grad[0] / rows)) for 2 ("mean") (grad: device f32 [1]).  The pages fix the
+ * value; the rounding sequence is this library's reading.  dlogits: device [rows, cols],
+ * contiguous, of the logits' dtype (bf16 logits: the f32 value rounded to nearest even).
+ * A logit above m sets DA_STATUS_ROWMAX_VIOLATION and is clamped as in the forward; a
+ * target outside [0, cols) subtracts nothing.  Bit-identical for any vocab split of the
+ * forward (its m and denom are). */
+int dce_backward(const da_matrix* logits, const int64_t* targets, const float* m, const double* denom,
+                 const float* grad, int reduction, void* dlogits, int32_t* dev_status, da_stream_t stream);
+
+/* det-cross-entropy "API", the loss reduction of cross_entropy: with S the exact sum of the
+ * rows f32 losses (a Kulisch accumulator), reduction 1 ("sum") gives RN32(RN64(S)), 2
+ * ("mean") RN32(RN64(RN64(S) / rows)); a NaN loss gives NaN, infinite losses their IEEE
+ * sum; rows == 0 gives 0 ("sum") or NaN ("mean", 0 / 0), and loss may then be null.
+ * loss: device f32 [rows]; out: device f32 [1].  Independent of the rows' order. */
+int dce_reduce(const float* loss, int64_t rows, int reduction, float* out, da_stream_t stream);
+
 /* Static-scratch variant of the cross-entropy forward, for callers that cannot allocate
  * device memory: code that runs where cudaMalloc is not allowed or not wanted, such as a
  * host framework whose device memory is owned by another allocator, an embedded runtime

@@ -559,5 +559,7 @@ def dce_reduce(loss, reduction: str) -> np.float32:
     if reduction == "sum":
         return np.float32(s64)
     if reduction == "mean":
+        if len(L) == 0:
+            return np.float32(np.nan)                     # 0 / 0: IEEE division gives NaN
         return np.float32(s64 / len(L))
     raise ValueError(reduction)

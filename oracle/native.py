@@ -242,3 +242,20 @@ class DCE:
         tg = np.asarray(targets, dtype=np.int64)[rows]
         loss, denom, st = self.finalize(den, tg, m, rows)
         return loss, denom, m, den, st
+
+
+def dce_backward_many(logits, targets, m, denom, go) -> np.ndarray:
+    """The cross-entropy dLogits of oracle.exact.dce_backward, vectorized over whole rows:
+    numpy float32 subtraction and multiplication round once each, float64 division once,
+    and the weights come from this module's C exp32_det (equal to the exact one)."""
+    from .exact import decode
+    X = decode(logits).astype(np.float32)
+    N, V = X.shape
+    xr = X - np.asarray(m, dtype=np.float32)[:, None]
+    xr = np.where(xr > 0, np.float32(0), xr).astype(np.float32)
+    w = exp32_det_many(xr.reshape(-1)).reshape(N, V).astype(np.float32)
+    p = (w.astype(np.float64) / np.asarray(denom, dtype=np.float64)[:, None]).astype(np.float32)
+    t = np.asarray(targets, dtype=np.int64)
+    hit = (np.arange(V)[None, :] == t[:, None])
+    g = np.where(hit, p - np.float32(1), p).astype(np.float32)
+    return (np.asarray(go, dtype=np.float32)[:, None] * g).astype(np.float32)

@@ -99,3 +99,19 @@ def test_reductions_are_exact_sums():
     assert abs(float(E.dce_reduce(L, "mean")) - float(exact) / 1000) <= 2.0 ** -23 * float(exact) / 1000
     perm = g.permutation(1000)
     assert E.dce_reduce(L[perm], "mean") == E.dce_reduce(L, "mean")
+
+
+def test_vectorized_backward_equals_exact(oracle_native):
+    g = torch.Generator().manual_seed(34)
+    x = (torch.randn(5, 203, generator=g) * 4).to(torch.bfloat16)
+    t = torch.tensor([0, 202, 17, -3, 99])
+    loss, denom, m, st = forward_state(oracle_native, x, t)
+    go = np.array([1.0, -0.5, 2.0, 0.25, 3.0], dtype=np.float32)
+    a = E.dce_backward(x, t.numpy(), m, denom, go)
+    b = oracle_native.dce_backward_many(x, t.numpy(), m, denom, go)
+    assert np.array_equal(a, b)
+
+
+def test_reduce_of_no_losses():
+    assert E.dce_reduce(np.zeros(0, np.float32), "sum") == 0
+    assert np.isnan(E.dce_reduce(np.zeros(0, np.float32), "mean"))
