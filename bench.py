@@ -136,6 +136,80 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_dce(args, dev, stream):
+    """The cross-entropy rows of the path on the vocab-sharded workload (N4096 x V128256 f32
+    logits, resident in HBM; 2.1 GB, larger than L2, so no flush): per step the forward
+    (dce_rowmax, dce_denom_digits, dce_finalize), the mean reduction and the backward
+    (dce_backward), each bracketed by CUDA events on the launching stream.  HBM roofline per
+    kernel: algorithmic bytes (logits read once per kernel; the backward also writes dLogits)
+    over its event time."""
+    import bitwise_deterministic_shard_gb300 as da
+    L = da.lib()
+    w = W.c5()
+    x, t = w.tensors(dev)
+    M, _keep = da._matrix(x)
+    N, V = w.N, w.V
+    m = torch.empty(N, dtype=torch.float32, device=dev)
+    den = torch.empty(N, 6, dtype=torch.int64, device=dev)
+    loss = torch.empty(N, dtype=torch.float32, device=dev)
+    denom = torch.empty(N, dtype=torch.float64, device=dev)
+    red = torch.empty((), dtype=torch.float32, device=dev)
+    one = torch.ones(1, dtype=torch.float32, device=dev)
+    dx = torch.empty_like(x)
+    sp = C.c_void_p(stream.cuda_stream)
+
+    def ptr(a):
+        return C.c_void_p(a.data_ptr())
+
+    def step(ev):
+        ev[0].record(stream)
+        assert L.dce_rowmax(C.byref(M), 0, V, ptr(m), None, sp) == 0
+        ev[1].record(stream)
+        assert L.dce_denom_digits(C.byref(M), ptr(m), 0, V, ptr(den), 0, None, sp) == 0
+        ev[2].record(stream)
+        assert L.dce_finalize(ptr(den), C.byref(M), ptr(t), ptr(m), ptr(loss), ptr(denom), None, sp) == 0
+        assert L.dce_reduce(ptr(loss), N, 2, ptr(red), sp) == 0
+        ev[3].record(stream)
+        assert L.dce_backward(C.byref(M), ptr(t), ptr(m), ptr(denom), ptr(one), 2, ptr(dx), None, sp) == 0
+        ev[4].record(stream)
+
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for _ in range(args.warmup):
+        step(mk())
+    torch.cuda.synchronize()
+    evs = [mk() for _ in range(args.steps)]
+    for e in evs:
+        step(e)
+    torch.cuda.synchronize()
+    ms = lambda a, b: statistics.mean(e[a].elapsed_time(e[b]) for e in evs)
+    k = {"rowmax": ms(0, 1), "denom_digits": ms(1, 2), "finalize_reduce": ms(2, 3), "backward": ms(3, 4)}
+    step_ms = ms(0, 4)
+    nbytes = N * V * x.element_size()
+    traffic = {"rowmax": nbytes, "denom_digits": nbytes, "backward": 2 * nbytes}
+    peak = _peaks().get("hbm_gbs") or 6800.0
+    roof = {kk: {"achieved_gbs": b / (k[kk] * 1e-3) / 1e9, "frac": b / (k[kk] * 1e-3) / 1e9 / peak,
+                 "bytes": b} for kk, b in traffic.items()}
+    out = {"workload": w.name, "tokens_per_s": N / (step_ms * 1e-3), "ms_per_step": step_ms,
+           "kernels_ms": k, "hbm_roofline": roof, "hbm_peak_gbs": peak,
+           "peak_basis": "measured copy bandwidth (MEASURED_PEAKS.json)" if _peaks().get("hbm_gbs")
+           else "fallback 6.8 TB/s", "gpu_launches_per_step": 5}
+    if not args.no_cpu_baseline:
+        from oracle import native
+        from oracle import exact as E
+        native.build()
+        rows = 512
+        xs, ts = x[:rows].cpu(), t[:rows].cpu()
+        t0 = time.perf_counter()
+        rl, rd, rm, rden, st = native.DCE(xs).forward(ts.numpy())
+        native.dce_backward_many(xs, ts.numpy(), rm, rd, E.dce_go(np.ones(1, np.float32), N, "mean")[:rows])
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": rows / dt, "unit": "tokens/s", "cores": native.default_threads(),
+                               "kind": "oracle",
+                               "sample": f"{rows} tokens x {V} logits: forward (exact C) and backward (numpy)",
+                               "seconds": dt}
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import bitwise_deterministic_shard_gb300 as da
     da.lib()
@@ -239,6 +313,7 @@ def run_ours(args, rank, world, local_rank):
 
     if rank != 0:
         return
+    dce = run_dce(args, dev, stream)
     macs = w.attn_macs
     value = macs * world / (ms * 1e-3)
     e2e_val = macs * world / (statistics.mean(e2e_ms) * 1e-3)
@@ -272,7 +347,8 @@ def run_ours(args, rank, world, local_rank):
         "clocks": ck,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": statistics.mean(e2e_ms)},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 6 * args.steps,   # per step: key prep, rowmax, V columns, key+V prep, accumulate, finalize
+        "dce": dce,
         "wall_s_timed_region": wall,
     }
     if not args.no_cpu_baseline:

@@ -12,6 +12,7 @@
 // exact, so the reduction order does not matter.
 #include <cuda_bf16.h>
 #include "numerics.cuh"
+#include "divide.cuh"
 #include "attn_kernels.h"
 
 namespace detattn {
@@ -160,17 +161,29 @@ __global__ void dce_finalize_kernel(const DceArgs a) {
 // ("mean").  A logit above the rowmax is clamped like the forward's (violation flag); NaN
 // propagates.  Streaming: 2 B or 4 B read and 2 B or 4 B written per logit; one CTA covers
 // BW_CHUNK columns of one row, consecutive threads consecutive columns.
-constexpr int BW_THREADS = 256, BW_CHUNK = 2048;
+constexpr int BW_THREADS = 256, BW_CHUNK = 8192;
 
 template <int DT>
 __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs a, const float* grad, int reduction,
                                                                   void* dlogits) {
   using T = typename In<DT>::T;
+  __shared__ idiv::Divisor sdiv;
+  __shared__ int sslow;
   const int64_t nch = (a.V + BW_CHUNK - 1) / BW_CHUNK;
   const int64_t i = blockIdx.x / nch, c0 = (blockIdx.x % nch) * BW_CHUNK;
   const T* row = (const T*)a.x + i * a.rs;
   const float m = a.m_in[i];
   const double d64 = a.denom[i];
+  if (threadIdx.x == 0) {   // the row's divisor, once per CTA: RN64(w / d64) on the integer pipe
+    uint64_t dm;
+    int de;
+    const bool ok = d64 > 0.0 && idiv::split_f64((uint64_t)__double_as_longlong(d64), dm, de);
+    sslow = !ok;   // zero, subnormal, negative, infinite or NaN denominators divide in binary64
+    if (ok) sdiv = idiv::make_divisor(dm, de);
+  }
+  __syncthreads();
+  const idiv::Divisor Dv = sdiv;
+  const bool slow = sslow;
   const int64_t t = a.targets[i];
   float go = reduction == 0 ? grad[i] : grad[0];
   if (reduction == 2) go = __double2float_rn(__ddiv_rn((double)go, (double)a.N));
@@ -184,7 +197,19 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
       st |= ST_VIOLATION;
       x = 0.0f;
     }
-    const float p = __double2float_rn(__ddiv_rn((double)exp32_det(x), d64));
+    const float w = exp32_det(x);
+    float p;
+    if (!slow && w > 0.0f) {
+      uint64_t mw, q;
+      int ew, E;
+      idiv::split_f32_53(__float_as_uint(w), mw, ew);
+      idiv::div_rn64(mw, ew, Dv, q, E);
+      p = __uint_as_float(idiv::rn32_bits(q, E, false));
+    } else if (!slow && w == 0.0f) {
+      p = 0.0f;   // +0 / a positive denominator
+    } else {
+      p = __double2float_rn(__ddiv_rn((double)w, d64));   // NaN weight or a special denominator
+    }
     const float g = v == t ? __fsub_rn(p, 1.0f) : p;
     const float o = __fmul_rn(go, g);
     if constexpr (DT == 0)

@@ -1,0 +1,65 @@
+// Host driver for the integer-pipe division helpers of the CUDA kernels (divide.cuh): prints
+// seeded random and edge-case inputs with the helpers' results, which test_divide_host.py
+// checks against exact rational arithmetic.
+#include <cstdio>
+#include <cstdint>
+#include <cstring>
+#include <cstdlib>
+#include "divide.cuh"
+using namespace detattn::idiv;
+static uint64_t s = 88172645463325252ull;
+static uint64_t rnd() { s ^= s << 13; s ^= s >> 7; s ^= s << 17; return s; }
+int main(int argc, char** argv) {
+  int mode = atoi(argv[1]); long n = atol(argv[2]);
+  if (mode == 0) {   // div_rn64 + rn32
+    for (long i = 0; i < n; i++) {
+      uint64_t mn = (rnd() >> 11) | (1ull << 52), md = (rnd() >> 11) | (1ull << 52);
+      int pick = rnd() % 8;
+      if (pick == 0) md = 1ull << 52;
+      if (pick == 1) mn = md;
+      if (pick == 2) mn = (1ull << 53) - 1 - (rnd() % 4);
+      if (pick == 3) md = (1ull << 53) - 1 - (rnd() % 4);
+      if (pick == 4) { md = (1ull << 52) | (rnd() % 8); mn = md * 3 / 2; if (mn >> 53) mn >>= 1; mn |= 1ull<<52; }
+      int en = (int)(rnd() % 600) - 300, ed = (int)(rnd() % 300) - 150;
+      Divisor D = make_divisor(md, ed);
+      uint64_t q; int E; div_rn64(mn, en, D, q, E);
+      uint32_t f = rn32_bits(q, E, rnd() & 1);
+      printf("%llu %d %llu %d %llu %d %u\n", (unsigned long long)mn, en, (unsigned long long)md, ed, (unsigned long long)q, E, f);
+    }
+  } else if (mode == 1) {   // rn32 on random q53 and wide exponents
+    for (long i = 0; i < n; i++) {
+      uint64_t q = (rnd() >> 11) | (1ull << 52);
+      if (rnd() % 4 == 0) q = (q & ~((1ull << 29) - 1)) | (1ull << 28) | ((rnd()%2) ? 0 : 1);
+      int E = (int)(rnd() % 500) - 260;
+      bool neg = rnd() & 1;
+      printf("%llu %d %d %u\n", (unsigned long long)q, E, (int)neg, rn32_bits(q, E, neg));
+    }
+  } else if (mode == 2) {   // digits
+    for (long i = 0; i < n; i++) {
+      long long a[15];
+      int kind = rnd() % 4;
+      for (int k = 0; k < 15; k++) {
+        long long v = (long long)(rnd() >> 30) - (1ll << 33);
+        if (kind == 1 && k < 13) v = (rnd() % 3 == 0) ? (long long)(rnd() >> 32) : 0;
+        if (kind == 2) v = (k == (int)(rnd() % 15)) ? (long long)(rnd() >> 32) : 0;
+        if (kind == 3 && k > 10) v = 0;
+        a[k] = v;
+      }
+      if (kind == 1) { a[13] = 0; a[14] = (rnd() % 2) ? 1 : -1; }
+      if (kind == 2) a[14] = 0;
+      for (int k = 0; k < 15; k++) printf("%lld ", a[k]);
+      bool neg; uint64_t m; int e;
+      bool nz = digits_split_rn64<15>(a, -320, neg, m, e);
+      printf("| %d %d %llu %d\n", (int)nz, (int)neg, (unsigned long long)m, e);
+    }
+  } else if (mode == 3) {   // f32 split
+    for (long i = 0; i < n; i++) {
+      uint32_t b = (uint32_t)rnd() & 0x7FFFFFFFu;
+      if ((b >> 23) == 0xFF) b &= 0x7F7FFFFFu;
+      if (i < 30) b = (uint32_t)(1u << i);
+      if (b == 0) b = 1;
+      uint64_t m; int e; split_f32_53(b, m, e);
+      printf("%u %llu %d\n", b, (unsigned long long)m, e);
+    }
+  }
+}

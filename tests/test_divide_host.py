@@ -1,0 +1,70 @@
+"""The integer-pipe division helpers that the finalize kernels use (csrc/divide.cuh), compiled
+for the host with g++ and checked against exact rational arithmetic: RN64 of a quotient of two
+binary64 magnitudes (division by an invariant integer with a precomputed reciprocal), RN32 of
+a binary64 given as mantissa and exponent (normal, subnormal, overflow), RN64 of a Kulisch
+digit value, and the binary32 split.  CPython's int / int is correctly rounded and numpy's
+float32 conversion rounds to nearest even, so both serve as the exact references here."""
+import math
+import os
+import shutil
+import struct
+import subprocess
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "..", "bitwise_deterministic_shard_gb300", "csrc")
+
+
+@pytest.fixture(scope="module")
+def drv(tmp_path_factory):
+    cxx = shutil.which("g++")
+    if cxx is None:
+        pytest.skip("g++ not available")
+    exe = str(tmp_path_factory.mktemp("divide") / "drv")
+    subprocess.run([cxx, "-O2", "-std=c++17", "-I", CSRC, os.path.join(HERE, "divide_driver.cpp"), "-o", exe],
+                   check=True)
+
+    def run(mode, n):
+        return subprocess.run([exe, str(mode), str(n)], capture_output=True, text=True, check=True).stdout.splitlines()
+    return run
+
+
+def test_div_rn64_is_correctly_rounded(drv):
+    for line in drv(0, 60000):
+        mn, en, md, ed, q, E, f = map(int, line.split())
+        k = en - ed
+        val = (mn << k) / md if k >= 0 else mn / (md << -k)
+        m, e = math.frexp(val)
+        assert (q, E) == (int(m * 2 ** 53), e - 53), line
+
+
+def test_rn32_of_binary64(drv):
+    for line in drv(1, 60000):
+        q, E, neg, f = map(int, line.split())
+        x = math.ldexp(q, E) * (-1 if neg else 1)
+        with np.errstate(over="ignore"):
+            ref = struct.unpack("<I", struct.pack("<f", np.float32(x)))[0]
+        assert ref == f, line
+
+
+def test_digits_rn64(drv):
+    for line in drv(2, 20000):
+        a, r = line.split("|")
+        a = list(map(int, a.split()))
+        nz, neg, m, e = map(int, r.split())
+        S = sum(Fraction(v) * Fraction(2) ** (-320 + 32 * k) for k, v in enumerate(a))
+        if S == 0:
+            assert nz == 0, line
+            continue
+        mm, ee = math.frexp(abs(float(S)))
+        assert (nz, neg, m, e) == (1, int(S < 0), int(mm * 2 ** 53), ee - 53), line
+
+
+def test_f32_split(drv):
+    for line in drv(3, 20000):
+        b, m, e = map(int, line.split())
+        x = struct.unpack("<f", struct.pack("<I", b))[0]
+        assert 2 ** 52 <= m < 2 ** 53 and Fraction(m) * Fraction(2) ** e == Fraction(x), line
