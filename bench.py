@@ -2,8 +2,9 @@
 
 Metric: exact attention MACs/s on the long-context causal workload (B1 H16 S4096 D128
 bf16, 1% of K rows x8), MACs = B * Hq * P * 2D with P the unmasked (query, key) pairs.
-A step is one pass of the whole attention path through the C ABI: rowmax over all keys,
-exact accumulate (NUM/DEN digits, canonical), finalize to f32 - the kernels of det_attn.
+A step is one pass of the whole attention path through the C ABI, the calls det_attn makes:
+da_rowmax over all keys, then da_accumulate_finalize (exact NUM/DEN sums, normalized, rounded
+and divided in the tensor-PV kernel's epilogue: the output is f32, no digits are stored).
 Inputs are resident in HBM when the timed region starts; L2 is flushed (a 512 MiB write)
 between timed steps, outside the per-step CUDA events.
 
@@ -41,7 +42,7 @@ UNIT = "MAC/s"
 # DRAM bytes (read + write) of one accumulate launch at the metric workload, from the ncu capture
 # summarised in profiles/accumulate_tp_long_context_C3_H4.md (the 4-head case scaled by 4: the
 # traffic is per head); set to None whenever the kernel changes until it is captured again
-ACC_TRAFFIC_PER_LAUNCH = 4 * 468.5e6
+ACC_TRAFFIC_PER_LAUNCH = 4 * 88.41e6
 
 
 def _peaks():
@@ -146,6 +147,9 @@ def run_dce(args, dev, stream):
     import bitwise_deterministic_shard_gb300 as da
     L = da.lib()
     w = W.c5()
+    if args.dce_rows != w.N:                   # smaller case of the same kernels (profiling)
+        w.name = w.name.replace(f"N{w.N}", f"N{args.dce_rows}")
+        w.N = args.dce_rows
     x, t = w.tensors(dev)
     M, _keep = da._matrix(x)
     N, V = w.N, w.V
@@ -230,8 +234,6 @@ def run_ours(args, rank, world, local_rank):
     kvws = torch.empty(L.da_kv_workspace_bytes(P.ref()), dtype=torch.uint8, device=dev)
     rows = w.B * w.Hq * w.S
     m = torch.empty(rows, dtype=torch.float32, device=dev)
-    num = torch.empty(rows, 15, w.D, dtype=torch.int64, device=dev)
-    den = torch.empty(rows, 6, dtype=torch.int64, device=dev)
     out = torch.empty(w.B, w.Hq, w.S, w.D, dtype=torch.float32, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     sp = C.c_void_p(stream.cuda_stream)
@@ -245,18 +247,16 @@ def run_ours(args, rank, world, local_rank):
         assert L.da_rowmax(P.ref(), 0, w.S, ptr(m), ptr(kvws), kvws.numel(), sp) == 0
         if ev:
             ev[1].record(stream)
-        assert L.da_accumulate(P.ref(), ptr(m), 0, w.S, ptr(num), ptr(den), 0, ptr(kvws), kvws.numel(), sp) == 0
+        # accumulate over all keys with the global rowmax, finalized in the tensor-PV kernel's epilogue
+        assert L.da_accumulate_finalize(P.ref(), ptr(m), ptr(out), ptr(ws), ws.numel(), sp) == 0
         if ev:
             ev[2].record(stream)
-        assert L.da_finalize(ptr(num), ptr(den), w.B, w.Hq, w.S, w.D, ptr(out), None, sp) == 0
-        if ev:
-            ev[3].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = Clocks(local_rank) if rank == 0 else None
     time.sleep(0.3)
     if world > 1:
@@ -273,8 +273,7 @@ def run_ours(args, rank, world, local_rank):
     ck = clocks.stop() if clocks else None
     k_rowmax = [e[0].elapsed_time(e[1]) for e in evs]
     k_acc = [e[1].elapsed_time(e[2]) for e in evs]
-    k_fin = [e[2].elapsed_time(e[3]) for e in evs]
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
     ms = statistics.mean(step_ms)
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -337,7 +336,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "flushed between timed steps (512 MiB write, outside the step events)",
                    "attn_macs_per_step": macs, "pairs_per_step": w.pairs},
         "method_macs_per_s": w.pairs * 3 * w.D * world / (ms * 1e-3),
-        "kernels_ms": {"rowmax": statistics.mean(k_rowmax), "accumulate": acc_ms, "finalize": statistics.mean(k_fin)},
+        "kernels_ms": {"rowmax": statistics.mean(k_rowmax), "accumulate_finalize": acc_ms},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": ACC_TRAFFIC_PER_LAUNCH if args.heads == 16 else None,
                      "kernel": "accumulate",
@@ -347,7 +346,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": ck,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": statistics.mean(e2e_ms)},
-        "gpu_launches": 6 * args.steps,   # per step: key prep, rowmax, V columns, key+V prep, accumulate, finalize
+        "gpu_launches": 5 * args.steps,   # per step: key prep, rowmax, V columns, key+V prep, accumulate
         "dce": dce,
         "wall_s_timed_region": wall,
     }
@@ -370,6 +369,8 @@ def main():
                     help="--impl reference: query rows per head in each timed step (a few seconds each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=16, help="heads of the workload (16 = the metric workload)")
+    ap.add_argument("--dce-rows", type=int, default=4096,
+                    help="tokens of the cross-entropy leg (4096 = the vocab-sharded workload)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -72,6 +72,7 @@ def lib():
         L.da_workspace_bytes.argtypes = [D, _I32]
         L.da_workspace_bytes.restype = C.c_size_t
         L.da_det_attn.argtypes = [D, _P, _P, C.c_size_t, _P]
+        L.da_accumulate_finalize.argtypes = [D, _P, _P, _P, C.c_size_t, _P]
         L.da_det_attn_sharded.argtypes = [D, _P, _I32, _P, _P, _P, C.c_size_t, _P]
         L.dce_rowmax.argtypes = [M, _I64, _I64, _P, _P, _P]
         L.dce_denom_digits.argtypes = [M, _P, _I64, _I64, _P, _I32, _P, _P]
@@ -79,7 +80,7 @@ def lib():
         L.dce_backward.argtypes = [M, _P, _P, _P, _P, _I32, _P, _P, _P]
         L.dce_reduce.argtypes = [_P, _I64, _I32, _P, _P]
         for f in ("da_rowmax", "da_accumulate", "da_compose_max", "da_compose_add", "da_normalize", "da_finalize",
-                  "da_det_attn", "da_det_attn_sharded", "dce_rowmax", "dce_denom_digits", "dce_finalize",
+                  "da_det_attn", "da_det_attn_sharded", "da_accumulate_finalize", "dce_rowmax", "dce_denom_digits", "dce_finalize",
                   "dce_backward", "dce_reduce"):
             getattr(L, f).restype = C.c_int
         _lib = L
@@ -180,6 +181,21 @@ def det_attn(Q, K, V, causal=False, scale=None, out=None, workspace=None, status
     out = torch.empty(P.B, P.Hq, P.Sq, P.D, dtype=torch.float32, device=P.device) if out is None else out
     ws = _workspace(P, 1, workspace)
     _check(lib().da_det_attn(P.ref(), _ptr(out), _ptr(ws), ws.numel(), _stream()), "det_attn")
+    return out
+
+
+def accumulate_finalize(Q, K, V, rowmax, causal=False, scale=None, out=None, workspace=None, status=None):
+    """Pass 2 and finalize over all keys with the global rowmax: the f32 output [B, Hq, Sq, D],
+    equal bit for bit to finalize(*accumulate(Q, K, V, rowmax, 0, Skv)); the tensor-PV kernel
+    finalizes in its epilogue, so the NUM digits are never stored."""
+    P = _Problem(Q, K, V, causal, scale, status)
+    _cuda(rowmax, "rowmax")
+    if rowmax.dtype != torch.float32 or rowmax.numel() != P.B * P.Hq * P.Sq:
+        raise DetAttnError("rowmax must be f32 [B, Hq, Sq]")
+    out = torch.empty(P.B, P.Hq, P.Sq, P.D, dtype=torch.float32, device=P.device) if out is None else out
+    ws = _workspace(P, 1, workspace)
+    _check(lib().da_accumulate_finalize(P.ref(), _ptr(rowmax.contiguous()), _ptr(out), _ptr(ws), ws.numel(),
+                                        _stream()), "accumulate_finalize")
     return out
 
 

@@ -53,6 +53,7 @@
 // DA_STATUS_TIMEOUT, and a failed wait in the compute warps only skips work.
 #include "numerics.cuh"
 #include "score_tc.cuh"
+#include "divide.cuh"
 #include "tc5.cuh"
 #include "attn_kernels.h"
 
@@ -203,6 +204,9 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   __shared__ int vbl_j[NCW][NVBL], vbl_n[NCW];
   __shared__ uint32_t tbit[BM][NW];   // spill slot digits touched this pass: single columns, whole rows, DEN
   __shared__ int trow[BM], tden[BM];
+  __shared__ idiv::Divisor fdiv[BM];   // fused finalize: each row's RN64(DEN) prepared as a divisor
+  __shared__ double fden64[BM];
+  __shared__ int fslow[BM];
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -685,12 +689,62 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
           if (sm >= (uint32_t)SPILL_SLOTS) nf |= ST_HEADROOM;   // no spill slot for this SM: products outside the windows are missing
         }
+        // canonical DEN digits of row rl: this pass's sum, the spill slot's (cleared after), the
+        // stored digits with add_into; headroom checked
+        auto den_digits = [&](int rl, long long (&t)[DEN_NDIG]) {
+          const long long* drow = a.den + out_row(q0 + rl) * DEN_NDIG;
+          long long dg[DEN_NDIG + 3];
+  #pragma unroll
+          for (int k = 0; k < DEN_NDIG + 3; k++) dg[k] = 0;
+          if (a.add_into)
+  #pragma unroll
+            for (int k = 0; k < DEN_NDIG; k++) dg[k] = __ldcg(drow + k);
+          if (tden[rl])
+  #pragma unroll
+            for (int k = 0; k < DEN_NDIG; k++) {
+              dg[k] += __ldcg(slot_den(rl) + k);
+              slot_den(rl)[k] = 0;
+            }
+          {
+            unsigned __int128 M;
+            bool neg;
+            digits3_to_u128(denT[rl][0], denT[rl][1], denT[rl][2], M, neg);
+            add_u128_at(dg, M, neg, -79 - DEN_E0);   // W units
+          }
+          carry_digits(dg);
+          long long top = dg[DEN_NDIG + 2];
+          bool bad = false;
+#pragma unroll
+          for (int k = DEN_NDIG + 1; k >= DEN_NDIG - 1; k--) {
+            if (top > (1ll << 30) || top < -(1ll << 30)) bad = true;
+            top = top * 4294967296ll + dg[k];
+          }
+          if (bad) nf |= ST_HEADROOM;
+  #pragma unroll
+          for (int k = 0; k < DEN_NDIG - 1; k++) t[k] = dg[k];
+          t[DEN_NDIG - 1] = top;
+        };
+        const bool fused = a.out != nullptr;   // finalize here: o = RN32(RN64(RN64(NUM) / RN64(DEN)))
+        if (fused) {
+          for (int rl = tid; rl < nrows; rl += NCT) {
+            long long t[DEN_NDIG];
+            den_digits(rl, t);
+            bool neg;
+            uint64_t mm;
+            int ee;
+            const bool nz = idiv::digits_split_rn64<DEN_NDIG>(t, DEN_E0, neg, mm, ee);
+            fslow[rl] = !nz || neg;   // a zero or negative DEN divides in binary64 (IEEE NaN / inf)
+            fden64[rl] = nz ? idiv::make_f64(neg, mm, ee) : 0.0;
+            if (nz && !neg) fdiv[rl] = idiv::make_divisor(mm, ee);
+          }
+          tc5::bar_sync(1, NCT);
+        }
         const int d = dcol;
   #pragma unroll
         for (int r = 0; r < 4; r++) {
           const int rl = rg * 4 + r, i = q0 + rl;
           if (i >= a.Sq || d >= a.D) continue;
-          long long* nrow = a.num + out_row(i) * NUM_NDIG * a.D;
+          long long* nrow = a.num + out_row(i) * NUM_NDIG * a.D;   // unused when fused
           long long dg[NUM_NDIG + 3];
   #pragma unroll
           for (int k = 0; k < NUM_NDIG + 3; k++) dg[k] = 0;
@@ -720,43 +774,39 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
             top = top * 4294967296ll + dg[k];
           }
           if (bad) nf |= ST_HEADROOM;
+          if (fused) {
+            long long t[NUM_NDIG];
   #pragma unroll
-          for (int k = 0; k < NUM_NDIG - 1; k++) nrow[(int64_t)k * a.D + d] = dg[k];
-          nrow[(int64_t)(NUM_NDIG - 1) * a.D + d] = top;
-        }
-        for (int rl = tid; rl < nrows; rl += NCT) {
-          long long* drow = a.den + out_row(q0 + rl) * DEN_NDIG;
-          long long dg[DEN_NDIG + 3];
-  #pragma unroll
-          for (int k = 0; k < DEN_NDIG + 3; k++) dg[k] = 0;
-          if (a.add_into)
-  #pragma unroll
-            for (int k = 0; k < DEN_NDIG; k++) dg[k] = __ldcg(drow + k);
-          if (tden[rl])
-  #pragma unroll
-            for (int k = 0; k < DEN_NDIG; k++) {
-              dg[k] += __ldcg(slot_den(rl) + k);
-              slot_den(rl)[k] = 0;
-            }
-          {
-            unsigned __int128 M;
+            for (int k = 0; k < NUM_NDIG - 1; k++) t[k] = dg[k];
+            t[NUM_NDIG - 1] = top;
             bool neg;
-            digits3_to_u128(denT[rl][0], denT[rl][1], denT[rl][2], M, neg);
-            add_u128_at(dg, M, neg, -79 - DEN_E0);   // W units
-          }
-          carry_digits(dg);
-          long long top = dg[DEN_NDIG + 2];
-          bool bad = false;
-#pragma unroll
-          for (int k = DEN_NDIG + 1; k >= DEN_NDIG - 1; k--) {
-            if (top > (1ll << 30) || top < -(1ll << 30)) bad = true;
-            top = top * 4294967296ll + dg[k];
-          }
-          if (bad) nf |= ST_HEADROOM;
+            uint64_t mm;
+            int ee;
+            const bool nz = idiv::digits_split_rn64<NUM_NDIG>(t, NUM_E0, neg, mm, ee);
+            float o = 0.0f;   // RN64(NUM) = +0 over a positive DEN
+            if (fslow[rl]) {
+              o = __double2float_rn(__ddiv_rn(nz ? idiv::make_f64(neg, mm, ee) : 0.0, fden64[rl]));
+            } else if (nz) {
+              uint64_t qq;
+              int EE;
+              idiv::div_rn64(mm, ee, fdiv[rl], qq, EE);
+              o = __uint_as_float(idiv::rn32_bits(qq, EE, neg));
+            }
+            a.out[out_row(i) * a.D + d] = o;
+          } else {
   #pragma unroll
-          for (int k = 0; k < DEN_NDIG - 1; k++) drow[k] = dg[k];
-          drow[DEN_NDIG - 1] = top;
+            for (int k = 0; k < NUM_NDIG - 1; k++) nrow[(int64_t)k * a.D + d] = dg[k];
+            nrow[(int64_t)(NUM_NDIG - 1) * a.D + d] = top;
+          }
         }
+        if (!fused)
+          for (int rl = tid; rl < nrows; rl += NCT) {
+            long long t[DEN_NDIG];
+            den_digits(rl, t);
+            long long* drow = a.den + out_row(q0 + rl) * DEN_NDIG;
+  #pragma unroll
+            for (int k = 0; k < DEN_NDIG; k++) drow[k] = t[k];
+          }
         __threadfence();   // the cleared slot digits reach L2 before the SM's next CTA adds into them
           tc += nkt;
       tc5::bar_sync(3, L::THREADS);

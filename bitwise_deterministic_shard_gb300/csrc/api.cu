@@ -202,6 +202,36 @@ DA_EXPORT size_t da_workspace_bytes(const da_attn_desc* desc, int nsplits) {
   return ws_layout(desc, nsplits).total;
 }
 
+DA_EXPORT int da_accumulate_finalize(const da_attn_desc* desc, const float* m, float* out, void* ws, size_t ws_bytes,
+                                     da_stream_t stream) {
+  int e = check_desc(desc);
+  if (e) return e;
+  if (desc->q.B * desc->q.S == 0) return DA_OK;
+  if (!m || !out) return DA_EINVAL;
+  if (!aligned(m, 4) || !aligned(out, 4)) return DA_EALIGN;
+  WsLayout w = ws_layout(desc, 1);
+  if (!ws || ws_bytes < w.total) return DA_EWORKSPACE;
+  if (!aligned(ws, 256)) return DA_EALIGN;
+  char* base = (char*)ws;
+  int64_t* num = (int64_t*)(base + w.num);
+  int64_t* den = (int64_t*)(base + w.den);
+  void* kv = base + w.kv;
+  const size_t kvb = ws_bytes - w.kv;
+  if ((e = check_kv_ws(desc, kv, kvb))) return e;
+  AttnArgs a = make_args(desc);
+  a.kv_lo = 0; a.kv_hi = (int)desc->k.S;
+  a.m_in = m; a.num = (long long*)num; a.den = (long long*)den; a.add_into = 0;
+  KvPrep p = kv_prep_layout(kv, a.B, a.Hkv, a.Skv, a.D, 1);
+  if (accumulate_is_tp(a, p)) {   // finalize in the epilogue: no NUM digits in device memory
+    a.out = out;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (launch_kv_prep(a, p, st) != cudaSuccess) return DA_ECUDA;
+    return launched(launch_accumulate(a, p, st));
+  }
+  if ((e = da_accumulate(desc, m, 0, desc->k.S, num, den, 0, kv, kvb, stream))) return e;
+  return da_finalize(num, den, desc->q.B, desc->q.H, desc->q.S, desc->q.D, out, desc->dev_status, stream);
+}
+
 DA_EXPORT int da_det_attn(const da_attn_desc* desc, float* out, void* ws, size_t ws_bytes, da_stream_t stream) {
   int e = check_desc(desc);
   if (e) return e;
@@ -210,15 +240,10 @@ DA_EXPORT int da_det_attn(const da_attn_desc* desc, float* out, void* ws, size_t
   WsLayout w = ws_layout(desc, 1);
   if (!ws || ws_bytes < w.total) return DA_EWORKSPACE;
   if (!aligned(ws, 256)) return DA_EALIGN;
-  char* base = (char*)ws;
-  float* m = (float*)(base + w.m);
-  int64_t* num = (int64_t*)(base + w.num);
-  int64_t* den = (int64_t*)(base + w.den);
-  void* kv = base + w.kv;
-  const size_t kvb = ws_bytes - w.kv;
-  if ((e = da_rowmax(desc, 0, desc->k.S, m, kv, kvb, stream))) return e;
-  if ((e = da_accumulate(desc, m, 0, desc->k.S, num, den, 0, kv, kvb, stream))) return e;
-  return da_finalize(num, den, desc->q.B, desc->q.H, desc->q.S, desc->q.D, out, desc->dev_status, stream);
+  float* m = (float*)((char*)ws + w.m);
+  void* kv = (char*)ws + w.kv;
+  if ((e = da_rowmax(desc, 0, desc->k.S, m, kv, ws_bytes - w.kv, stream))) return e;
+  return da_accumulate_finalize(desc, m, out, ws, ws_bytes, stream);
 }
 
 DA_EXPORT int da_det_attn_sharded(const da_attn_desc* desc, const int64_t* kv_splits, int nsplits, const int32_t* order,

@@ -752,10 +752,14 @@ cudaError_t launch_rowmax(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
   return launch_rowmax_t<1, 256>(a, p, st);
 }
 
+bool accumulate_is_tp(const AttnArgs& a, const KvPrep& p) {
+  return padded_d(a.D) == 128 && p.vtc != nullptr && (a.kv_hi - a.kv_lo + KTILE - 1) / KTILE <= ACC_TP_MAX_TILES;
+}
+
 cudaError_t launch_accumulate(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
   const int dp = padded_d(a.D);
-  if (dp == 128 && p.vtc != nullptr && (a.kv_hi - a.kv_lo + KTILE - 1) / KTILE <= ACC_TP_MAX_TILES)
-    return launch_accumulate_tp(a, p, st);
+  if (accumulate_is_tp(a, p)) return launch_accumulate_tp(a, p, st);
+  if (a.out) return cudaErrorInvalidValue;   // only the tensor-PV kernel finalizes in its epilogue
   if (dp <= 128) return launch_accumulate_tc(a, p, st);
   return a.dtype == 0 ? launch_accumulate_t<0, 256>(a, p, st) : launch_accumulate_t<1, 256>(a, p, st);
 }

@@ -21,6 +21,8 @@ struct AttnArgs {
   long long* den;                // [B, Hq, Sq, 6]
   int add_into;
   int* status;                   // device status word (may be null)
+  float* out;                    // non-null: the tensor-PV accumulate finalizes into out [B, Hq, Sq, D]
+                                 // instead of writing digits (one key range, add_into == 0)
 };
 
 // Prepared keys/values of one call's key range (prep_kernels.cu), rows indexed as
@@ -63,6 +65,7 @@ cudaError_t launch_accumulate(const AttnArgs& a, const KvPrep& p, cudaStream_t s
 cudaError_t launch_accumulate_tc(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // D <= 128
 cudaError_t launch_accumulate_tp(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // 64 < D <= 128
 constexpr int ACC_TP_MAX_TILES = 512;   // key tiles per pass the tensor-PV kernel's state holds exactly
+bool accumulate_is_tp(const AttnArgs& a, const KvPrep& p);   // launch_accumulate takes the tensor-PV kernel
 
 cudaError_t launch_compose_max(float* dst, const float* src, int64_t n, cudaStream_t st);
 cudaError_t launch_compose_add(long long* dst, const long long* src, int64_t n, cudaStream_t st);

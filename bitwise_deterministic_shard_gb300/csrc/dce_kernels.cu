@@ -73,8 +73,10 @@ __global__ void __launch_bounds__(256) dce_rowmax_kernel(const DceArgs a) {
   report(a.status, nf);
 }
 
+constexpr int DEN_THREADS = 256;   // one CTA per row, six resident per SM
+
 template <int DT>
-__global__ void __launch_bounds__(256) dce_denom_kernel(const DceArgs a) {
+__global__ void __launch_bounds__(DEN_THREADS, 6) dce_denom_kernel(const DceArgs a) {
   using T = typename In<DT>::T;
   const int64_t i = blockIdx.x;
   const T* row = (const T*)a.x + i * a.rs;
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(256) dce_denom_kernel(const DceArgs a) {
     float x = __fsub_rn(__uint_as_float(u), m);
     if (x != x) { st |= ST_NONFINITE; return; }
     if (x > 0.0f) { st |= ST_VIOLATION; x = 0.0f; }
-    const uint32_t wb = __float_as_uint(exp32_det(x));
+    const uint32_t wb = __float_as_uint(exp32_det_nb(x));   // x <= 0, not NaN
     if (wb == 0u) return;
     const int ex = (int)(wb >> 23);
     const uint32_t M = ex ? ((wb & 0x7FFFFFu) | 0x800000u) : wb;
@@ -110,7 +112,7 @@ __global__ void __launch_bounds__(256) dce_denom_kernel(const DceArgs a) {
   for (int k = 0; k < 6; k++)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dg[k] += __shfl_xor_sync(0xFFFFFFFFu, dg[k], o);
-  __shared__ long long wsum[8][6];
+  __shared__ long long wsum[DEN_THREADS / 32][6];
   if ((threadIdx.x & 31) == 0)
 #pragma unroll
     for (int k = 0; k < 6; k++) wsum[threadIdx.x >> 5][k] = dg[k];
@@ -121,7 +123,7 @@ __global__ void __launch_bounds__(256) dce_denom_kernel(const DceArgs a) {
 #pragma unroll
     for (int k = 0; k < 6; k++) {
       t[k] = a.add_into ? out[k] : 0;
-      for (int w = 0; w < 8; w++) t[k] += wsum[w][k];
+      for (int w = 0; w < DEN_THREADS / 32; w++) t[k] += wsum[w][k];
     }
     kul_carry(t, 6);
     if (t[5] > (1ll << 62) || t[5] < -(1ll << 62)) st |= ST_HEADROOM;
@@ -161,17 +163,18 @@ __global__ void dce_finalize_kernel(const DceArgs a) {
 // ("mean").  A logit above the rowmax is clamped like the forward's (violation flag); NaN
 // propagates.  Streaming: 2 B or 4 B read and 2 B or 4 B written per logit; one CTA covers
 // BW_CHUNK columns of one row, consecutive threads consecutive columns.
-constexpr int BW_THREADS = 256, BW_CHUNK = 8192;
+constexpr int BW_THREADS = 256, BW_PER = 32, BW_CHUNK = BW_THREADS * BW_PER, BW_BATCH = 8;
 
 template <int DT>
-__global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs a, const float* grad, int reduction,
-                                                                  void* dlogits) {
+__global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs a, const float* __restrict__ grad,
+                                                                  int reduction, void* __restrict__ dlogits) {
   using T = typename In<DT>::T;
   __shared__ idiv::Divisor sdiv;
   __shared__ int sslow;
   const int64_t nch = (a.V + BW_CHUNK - 1) / BW_CHUNK;
   const int64_t i = blockIdx.x / nch, c0 = (blockIdx.x % nch) * BW_CHUNK;
-  const T* row = (const T*)a.x + i * a.rs;
+  const T* __restrict__ row = (const T*)a.x + i * a.rs + c0;
+  const int nv = (int)(a.V - c0 < BW_CHUNK ? a.V - c0 : BW_CHUNK);
   const float m = a.m_in[i];
   const double d64 = a.denom[i];
   if (threadIdx.x == 0) {   // the row's divisor, once per CTA: RN64(w / d64) on the integer pipe
@@ -184,38 +187,45 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
   __syncthreads();
   const idiv::Divisor Dv = sdiv;
   const bool slow = sslow;
-  const int64_t t = a.targets[i];
+  const int64_t tg = a.targets[i] - c0;   // the target's column within this chunk (any value)
   float go = reduction == 0 ? grad[i] : grad[0];
   if (reduction == 2) go = __double2float_rn(__ddiv_rn((double)go, (double)a.N));
   int st = 0;
-#pragma unroll 4
-  for (int k = 0; k < BW_CHUNK / BW_THREADS; k++) {
-    const int64_t v = c0 + k * BW_THREADS + threadIdx.x;
-    if (v >= a.V) break;
-    float x = __fsub_rn(__uint_as_float(In<DT>::bits(row, v)), m);
-    if (x > 0.0f) {
-      st |= ST_VIOLATION;
-      x = 0.0f;
+  for (int k0 = 0; k0 < BW_PER; k0 += BW_BATCH) {
+    uint32_t u[BW_BATCH];
+#pragma unroll
+    for (int j = 0; j < BW_BATCH; j++) {   // the batch's loads first, all in flight together
+      const int v = (k0 + j) * BW_THREADS + threadIdx.x;
+      u[j] = v < nv ? In<DT>::bits(row, v) : 0u;
     }
-    const float w = exp32_det(x);
-    float p;
-    if (!slow && w > 0.0f) {
-      uint64_t mw, q;
-      int ew, E;
-      idiv::split_f32_53(__float_as_uint(w), mw, ew);
-      idiv::div_rn64(mw, ew, Dv, q, E);
-      p = __uint_as_float(idiv::rn32_bits(q, E, false));
-    } else if (!slow && w == 0.0f) {
-      p = 0.0f;   // +0 / a positive denominator
-    } else {
-      p = __double2float_rn(__ddiv_rn((double)w, d64));   // NaN weight or a special denominator
+#pragma unroll
+    for (int j = 0; j < BW_BATCH; j++) {
+      const int v = (k0 + j) * BW_THREADS + threadIdx.x;
+      if (v >= nv) continue;
+      float x = __fsub_rn(__uint_as_float(u[j]), m);
+      if (x > 0.0f) {
+        st |= ST_VIOLATION;
+        x = 0.0f;
+      }
+      const float w = x != x ? x : exp32_det_nb(x);
+      float p;
+      if (!slow && w > 0.0f) {
+        uint32_t mw;
+        int ew;
+        idiv::split_f32_24(__float_as_uint(w), mw, ew);
+        p = __uint_as_float(idiv::div_f32_rn32(mw, ew, Dv));
+      } else if (!slow && w == 0.0f) {
+        p = 0.0f;   // +0 / a positive denominator
+      } else {
+        p = __double2float_rn(__ddiv_rn((double)w, d64));   // NaN weight or a special denominator
+      }
+      const float g = v == tg ? __fsub_rn(p, 1.0f) : p;
+      const float o = __fmul_rn(go, g);
+      if constexpr (DT == 0)
+        ((float*)dlogits)[i * a.V + c0 + v] = o;
+      else
+        ((__nv_bfloat16*)dlogits)[i * a.V + c0 + v] = __float2bfloat16_rn(o);
     }
-    const float g = v == t ? __fsub_rn(p, 1.0f) : p;
-    const float o = __fmul_rn(go, g);
-    if constexpr (DT == 0)
-      ((float*)dlogits)[i * a.V + v] = o;
-    else
-      ((__nv_bfloat16*)dlogits)[i * a.V + v] = __float2bfloat16_rn(o);
   }
   report(a.status, st);
 }
@@ -290,8 +300,8 @@ cudaError_t launch_dce_rowmax(const DceArgs& a, cudaStream_t st) {
 
 cudaError_t launch_dce_denom(const DceArgs& a, cudaStream_t st) {
   if (a.N <= 0) return cudaSuccess;
-  if (a.dtype == 0) dce_denom_kernel<0><<<(unsigned)a.N, 256, 0, st>>>(a);
-  else dce_denom_kernel<1><<<(unsigned)a.N, 256, 0, st>>>(a);
+  if (a.dtype == 0) dce_denom_kernel<0><<<(unsigned)a.N, DEN_THREADS, 0, st>>>(a);
+  else dce_denom_kernel<1><<<(unsigned)a.N, DEN_THREADS, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -143,6 +143,56 @@ DA_HD double make_f64(bool neg, uint64_t m, int e) {
 #endif
 }
 
+// A nonzero binary32 magnitude as mw 2^ew with mw in [2^23, 2^24).
+DA_HD void split_f32_24(uint32_t bits, uint32_t& mw, int& ew) {
+  const int be = (int)((bits >> 23) & 0xFF);
+  if (be) {
+    mw = (bits & 0x7FFFFFu) | 0x800000u;
+    ew = be - 150;
+  } else {   // subnormal
+    const uint32_t f = bits & 0x7FFFFFu;
+#if defined(__CUDA_ARCH__)
+    const int sh = __clz(f) - 8;
+#else
+    const int sh = __builtin_clz(f) - 8;
+#endif
+    mw = f << sh;
+    ew = -149 - sh;
+  }
+}
+
+// RN32 bits of RN64(w / d) for w = mw 2^ew (mw in [2^23, 2^24)) and the prepared divisor.
+// The same 2-by-1 division as div_rn64 (u1 = mw 2^31, u0 = 0), with v u1 formed from two
+// 32 x 32 -> 64 products since mw has 24 bits, then both roundings.
+DA_HD uint32_t div_f32_rn32(uint32_t mw, int ew, const Divisor& D) {
+  const uint64_t A = (uint64_t)(uint32_t)D.v * mw, B = (D.v >> 32) * (uint64_t)mw;   // each < 2^56
+  const uint64_t Plo = A + (B << 32);                                                 // P = v mw, 88 bits
+  const uint64_t Phi = (B >> 32) + (Plo < A ? 1u : 0u);
+  const uint64_t q0 = Plo << 31;                                                      // (q1, q0) = P 2^31
+  uint64_t q1 = (Phi << 31) | (Plo >> 33);
+  q1 += ((uint64_t)mw << 31) + 1;                                                     // + u1 2^64, + 2^64
+  uint64_t r = 0 - q1 * D.dn;
+  if (r > q0) {
+    q1 -= 1;
+    r += D.dn;
+  }
+  if (r >= D.dn) {
+    q1 += 1;
+    r -= D.dn;
+  }
+  const uint64_t Q = q1;   // floor(mw 2^84 / md): 55 or 56 bits
+  const int s = (Q >> 55) ? 3 : 2;
+  uint64_t m = Q >> s;
+  const uint64_t rb = Q & ((1ull << s) - 1), half = 1ull << (s - 1);
+  if (rb > half || (rb == half && (r != 0 || (m & 1)))) m += 1;
+  int e = ew - 29 - D.e - 55 + s;
+  if (m >> 53) {
+    m >>= 1;
+    e += 1;
+  }
+  return rn32_bits(m, e, false);
+}
+
 // A binary64's magnitude as m 2^e with m in [2^52, 2^53); false for zero, subnormal,
 // infinity or NaN (the callers route those through their slow path).
 DA_HD bool split_f64(uint64_t bits, uint64_t& m, int& e) {

@@ -127,6 +127,16 @@ int da_rowmax(const da_attn_desc* desc, int64_t kv_lo, int64_t kv_hi, float* m, 
 int da_accumulate(const da_attn_desc* desc, const float* m, int64_t kv_lo, int64_t kv_hi, int64_t* num,
                   int64_t* den, int add_into, void* ws, size_t ws_bytes, da_stream_t stream);
 
+/* det-attn "Method", pass 2 and finalize over the whole key range in one call:
+ * out = RN32(RN64(RN64(NUM) / RN64(DEN))) for NUM/DEN over keys [0, Skv) with the global
+ * rowmax m (device f32 [B, Hq, Sq]).  out: device f32 [B, Hq, Sq, D], contiguous.  Equal bit
+ * for bit to da_accumulate(.., 0, Skv, .., add_into = 0) followed by da_finalize; where the
+ * tensor-PV kernel applies (64 < D <= 128, at most 65,536 keys) it finalizes in its epilogue
+ * and the NUM digits never reach device memory.  ws: at least da_workspace_bytes(desc, 1)
+ * (the digits are kept there on the other paths). */
+int da_accumulate_finalize(const da_attn_desc* desc, const float* m, float* out, void* ws, size_t ws_bytes,
+                           da_stream_t stream);
+
 /* det-attn "Method", shard composition: dst[i] = max(dst[i], src[i]) (f32, -0 -> +0). */
 int da_compose_max(float* dst, const float* src, int64_t n, da_stream_t stream);
 

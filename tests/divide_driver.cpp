@@ -52,6 +52,22 @@ int main(int argc, char** argv) {
       bool nz = digits_split_rn64<15>(a, -320, neg, m, e);
       printf("| %d %d %llu %d\n", (int)nz, (int)neg, (unsigned long long)m, e);
     }
+  } else if (mode == 4) {   // the binary32-numerator division against the generic one
+    for (long i = 0; i < n; i++) {
+      uint32_t b = (uint32_t)rnd() & 0x7FFFFFFFu;
+      if ((b >> 23) == 0xFF || b == 0) b = 0x3F800000u;
+      if (i % 5 == 0) b &= 0x807FFFFFu;   // subnormal
+      if (b == 0) b = 1;
+      uint64_t md = (rnd() >> 11) | (1ull << 52);
+      if (i % 7 == 0) md = 1ull << 52;
+      int ed = (int)(rnd() % 120) - 60;
+      Divisor D = make_divisor(md, ed);
+      uint32_t mw; int ew; split_f32_24(b, mw, ew);
+      uint64_t m53, q; int e53, E;
+      split_f32_53(b, m53, e53);
+      div_rn64(m53, e53, D, q, E);
+      printf("%u %llu %d %u %u\n", b, (unsigned long long)md, ed, div_f32_rn32(mw, ew, D), rn32_bits(q, E, false));
+    }
   } else if (mode == 3) {   // f32 split
     for (long i = 0; i < n; i++) {
       uint32_t b = (uint32_t)rnd() & 0x7FFFFFFFu;

@@ -68,3 +68,18 @@ def test_f32_split(drv):
         b, m, e = map(int, line.split())
         x = struct.unpack("<f", struct.pack("<I", b))[0]
         assert 2 ** 52 <= m < 2 ** 53 and Fraction(m) * Fraction(2) ** e == Fraction(x), line
+
+
+def test_binary32_numerator_division(drv):
+    """div_f32_rn32 (two 32 x 32 products) equals the generic division, and RN32(RN64(w / d))
+    computed exactly."""
+    for k, line in enumerate(drv(4, 60000)):
+        b, md, ed, fast, generic = map(int, line.split())
+        assert fast == generic, line
+        if k % 10 == 0:
+            w = Fraction(struct.unpack("<f", struct.pack("<I", b))[0])
+            d = Fraction(md) * Fraction(2) ** (ed)
+            q = w / d
+            q64 = q.numerator / q.denominator          # correctly rounded binary64
+            ref = struct.unpack("<I", struct.pack("<f", np.float32(q64)))[0]
+            assert fast == ref, line

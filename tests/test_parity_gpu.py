@@ -277,6 +277,37 @@ def test_strided_nhd_views(da, orc):
 
 
 @cuda
+@pytest.mark.parametrize("case", [
+    # (B, Hq, Hkv, S, D, dtype, causal, spread): D in (64, 128] takes the tensor-PV kernel,
+    # which finalizes in its epilogue; D = 64 takes the digits + finalize path
+    (1, 2, 2, 200, 128, torch.bfloat16, True, 1.0),
+    (2, 4, 2, 300, 128, torch.float32, False, 1.0),
+    (1, 2, 1, 150, 100, torch.bfloat16, True, 1.0),
+    (1, 2, 2, 170, 128, torch.bfloat16, False, 60.0),
+    (1, 2, 2, 90, 64, torch.bfloat16, False, 1.0),
+])
+def test_accumulate_finalize_equals_the_digit_path(da, orc, case):
+    """The fused pass 2 (NUM digits never stored) against accumulate + finalize, bit for
+    bit, and against the oracle."""
+    B, Hq, Hkv, S, D, dt, causal, spread = case
+    Q, K, V = W.random_attn(90 + S, B, Hq, Hkv, S, D, dt, causal, spread=spread)
+    if spread != 1.0:
+        K = K.clone()
+        K[0, 0, 5] *= 2 ** 40   # tiny weights for the other keys: the spill slots
+    Qd, Kd, Vd = Q.cuda(), K.cuda(), V.cuda()
+    st = da.new_status()
+    m = da.rowmax(Qd, Kd, causal=causal, status=st)
+    fused = da.accumulate_finalize(Qd, Kd, Vd, m, causal=causal, status=st)
+    num, den = da.accumulate(Qd, Kd, Vd, m, causal=causal, status=st)
+    ref = da.finalize(num, den)
+    torch.cuda.synchronize()
+    assert_bits_equal(fused, ref, "fused vs digits")
+    assert da.read_status(st) & ~1 == 0
+    _, _, _, out_o = orc.Attn(Q, K, V, causal=causal).forward_rows()
+    assert_bits_equal(fused.reshape(-1, D), out_o, "fused vs oracle")
+
+
+@cuda
 def test_empty_and_edge_ranges(da, orc):
     Q, K, V = W.random_attn(45, 1, 2, 2, 50, 32, torch.bfloat16, False)
     Qd, Kd, Vd = Q.cuda(), K.cuda(), V.cuda()
