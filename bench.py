@@ -129,9 +129,14 @@ def run_reference(args, rank, world):
             vals.append(macs / dt)
     v = statistics.median(vals)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup,
+            "ms_per_step": w.attn_macs / v * 1e3,   # one whole step of the workload at the sampled rate
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "S": w.S, "D": w.D, "causal": True},
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": True,
+                       "input_dtype": "bf16", "parallelism": "single GPU" if world == 1 else f"replicas x{world}",
+                       "l2": "host oracle on sampled query rows (no device cache involved)",
+                       "attn_macs_per_step": w.attn_macs, "pairs_per_step": w.pairs},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

@@ -179,5 +179,9 @@ def test_c5_backward_sampled_rows(da, orc):
     go = E.dce_go(np.ones(1, dtype=np.float32), w.N, "mean")[: len(rows)]
     want = _want(orc, xs, ts, rm, rd, go, torch.float32)
     _assert_same(grads[0][1][torch.from_numpy(rows).cuda()], want, "C5 sampled dLogits")
-    ref = torch.nn.functional.cross_entropy(x.double(), t)
-    assert abs(float(grads[0][0]) - float(ref)) < 1e-5
+    # the det-cross-entropy page's match to torch: loss within 1.9e-6, gradient within 1.2e-10
+    x64 = x.double().requires_grad_(True)
+    ref = torch.nn.functional.cross_entropy(x64, t)
+    ref.backward()
+    assert abs(float(grads[0][0]) - float(ref)) < 1.9e-6
+    assert float((grads[0][1].double() - x64.grad).abs().max()) < 1.2e-10
