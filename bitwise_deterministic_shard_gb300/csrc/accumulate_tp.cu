@@ -45,6 +45,14 @@
 // (key, the four weights) and their products added after the tiles; smaller weights take
 // whole-product atomics.
 //
+// Epilogue.  Per pass the compute warps add the spill slot's touched digits and carry the
+// sums into canonical digits, then either store NUM / DEN digits (accumulate), or, when the
+// call covers the whole key range (AttnArgs::out, no add_into), finalize in place: each row's
+// DEN is rounded to binary64 and prepared as an integer divisor (divide.cuh), and every
+// (row, column) gets o = RN32(RN64(RN64(NUM) / RN64(DEN))) on the integer pipe; only the f32
+// output reaches device memory (page "det-attn", section "Method": finalize rounds and
+// divides).
+//
 // Roles: warp 16 copies key operand steps (lane 0, 4-stage ring) and V digit blocks (lane 1,
 // NVB-stage ring), warps 17 and 19 (lane 0) issue the score MMAs of alternate 16-dimension
 // steps, warp 18 (lane 0) the PV and DEN MMAs.  Warps 0-15 read the score diagonals, compute weights, write the weight digit

@@ -130,3 +130,52 @@ def test_dropped_top_digit_in_finalize_is_caught(monkeypatch):
     monkeypatch.setattr(E, "finalize_value", bad)
     Q, K, V = W.random_attn(36, 1, 1, 1, 6, 4, torch.float32, False)
     assert not _agrees_with_naive_out(E.det_attn(Q, K, V), Q, K, V)
+
+
+# ---------------------------------------------------------------- cross-entropy backward
+
+def _dce_backward_agrees_with_torch(oracle_native, reduction) -> bool:
+    g = torch.Generator().manual_seed(41)
+    x = torch.randn(10, 200, generator=g) * 2
+    t = torch.randint(0, 200, (10,), generator=g)
+    loss, denom, m, den, st = oracle_native.DCE(x).forward(t.numpy())
+    up = torch.rand(10 if reduction == "none" else 1, generator=g).float() + 0.5
+    grad = E.dce_backward(x, t.numpy(), m, denom, E.dce_go(up.numpy(), 10, reduction))
+    x64 = x.double().requires_grad_(True)
+    torch.nn.functional.cross_entropy(x64, t, reduction=reduction).backward(
+        up.double() if reduction == "none" else up.double()[0])
+    return bool(np.max(np.abs(grad - x64.grad.numpy())) < 2.0 ** -20)
+
+
+def test_unmutated_backward_passes(oracle_native):
+    for reduction in ("none", "sum", "mean"):
+        assert _dce_backward_agrees_with_torch(oracle_native, reduction)
+
+
+def test_one_hot_at_the_wrong_column_is_caught(monkeypatch, oracle_native):
+    orig = E.dce_backward
+
+    def bad(logits, targets, m, denom, go):
+        return orig(logits, (np.asarray(targets) + 1) % np.asarray(logits).shape[1], m, denom, go)
+    monkeypatch.setattr(E, "dce_backward", bad)
+    assert not _dce_backward_agrees_with_torch(oracle_native, "none")
+
+
+def test_mean_without_the_division_by_n_is_caught(monkeypatch, oracle_native):
+    orig = E.dce_go
+
+    def bad(grad, N, reduction):
+        return orig(grad, N, "sum" if reduction == "mean" else reduction)
+    monkeypatch.setattr(E, "dce_go", bad)
+    assert not _dce_backward_agrees_with_torch(oracle_native, "mean")
+
+
+def test_mean_over_n_minus_one_is_caught(monkeypatch):
+    def bad(loss, reduction):
+        L = np.asarray(loss, dtype=np.float32).reshape(-1)
+        S = sum((Fraction(float(v)) for v in L), Fraction(0))
+        return np.float32(float(S) / (len(L) - 1)) if reduction == "mean" else np.float32(float(S))
+    monkeypatch.setattr(E, "dce_reduce", bad)
+    # the printed-value pin of the reduction: mean of [1, 2, 4] is RN32(7/3) = 0x40155555
+    got = E.dce_reduce(np.array([1, 2, 4], np.float32), "mean")
+    assert np.float32(got).view(np.uint32) != np.uint32(0x40155555)
