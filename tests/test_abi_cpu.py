@@ -72,3 +72,27 @@ def test_argument_checks_reject_before_any_launch(libpath):
     assert L.da_kv_workspace_bytes(ctypes.byref(d)) > 0
     assert L.da_det_attn_sharded(ctypes.byref(d), (ctypes.c_int64 * 2)(4, 4), 2, None, None, None, 0, None) == 1
     assert L.da_normalize(None, 4, 7, 1, None, None) == 1                  # ndig must be 15 or 6
+
+
+def test_new_entry_points_reject_before_any_launch(libpath):
+    """da_accumulate_finalize, dce_backward and dce_reduce validate on the host first."""
+    import bitwise_deterministic_shard_gb300 as da
+    L = da.lib()
+    d = da._Desc()
+    for t in (d.q, d.k, d.v):
+        t.ptr = 4096
+        t.dtype, t.B, t.H, t.S, t.D = 1, 1, 2, 8, 128
+        t.stride[3] = 1
+    assert L.da_accumulate_finalize(None, None, None, None, 0, None) == 1        # null descriptor
+    assert L.da_accumulate_finalize(ctypes.byref(d), None, None, None, 0, None) == 1   # null m / out
+    assert L.da_accumulate_finalize(ctypes.byref(d), 4096, 8192, None, 0, None) == 5   # no workspace
+    M = da._Matrix()
+    M.ptr, M.dtype, M.rows, M.cols, M.row_stride = 4096, 0, 4, 10, 10
+    assert L.dce_backward(ctypes.byref(M), None, None, None, None, 3, None, None, None) == 1    # reduction 0..2
+    assert L.dce_backward(ctypes.byref(M), None, None, None, None, 0, None, None, None) == 1    # null pointers
+    M.row_stride = 5
+    assert L.dce_backward(ctypes.byref(M), 8, 4, 8, 4, 0, 4, None, None) == 2                   # row stride < cols
+    assert L.dce_reduce(None, 4, 0, None, None) == 1                                             # "none" is not a reduction
+    assert L.dce_reduce(None, -1, 1, 4096, None) == 1
+    assert L.dce_reduce(None, 4, 2, 4096, None) == 1                                             # null losses
+    assert L.dce_reduce(4098, 4, 2, 4096, None) == 4                                             # misaligned
