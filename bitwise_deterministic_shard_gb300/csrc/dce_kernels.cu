@@ -13,26 +13,31 @@
 #include <cuda_bf16.h>
 #include "numerics.cuh"
 #include "divide.cuh"
+#include "den_acc.cuh"
 #include "attn_kernels.h"
 
 namespace detattn {
 
 // visit every element of row[v_lo, v_hi) owned by this thread: scalar head up to a 16-byte
-// boundary, 16-byte vectors, scalar tail
-template <int DT, typename F>
-__device__ __forceinline__ void for_row(const typename In<DT>::T* row, int64_t v_lo, int64_t v_hi, F&& f) {
+// boundary, 16-byte vectors, scalar tail; group() runs before each vector or scalar element
+template <int DT, typename F, typename G>
+__device__ __forceinline__ void for_row(const typename In<DT>::T* row, int64_t v_lo, int64_t v_hi, F&& f, G&& group) {
   using T = typename In<DT>::T;
   constexpr int VEC = 16 / sizeof(T);
   const uintptr_t addr = reinterpret_cast<uintptr_t>(row + v_lo);
   int64_t head = (int64_t)(((16 - (addr & 15)) & 15) / sizeof(T));
   if (((addr & 15) % sizeof(T)) != 0) head = v_hi - v_lo;   // unaligned element pointer: scalar only
   const int64_t hend = min(v_hi, v_lo + head);
-  for (int64_t v = v_lo + threadIdx.x; v < hend; v += blockDim.x) f(In<DT>::bits(row, v));
+  for (int64_t v = v_lo + threadIdx.x; v < hend; v += blockDim.x) {
+    group();
+    f(In<DT>::bits(row, v));
+  }
   const int64_t nvec = (v_hi - hend) / VEC;
   const uint4* vp = reinterpret_cast<const uint4*>(row + hend);
   for (int64_t k = threadIdx.x; k < nvec; k += blockDim.x) {
     uint4 q = __ldg(vp + k);
     uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    group();
     if constexpr (DT == 0) {
 #pragma unroll
       for (int t = 0; t < 4; t++) f(w[t]);
@@ -44,7 +49,10 @@ __device__ __forceinline__ void for_row(const typename In<DT>::T* row, int64_t v
       }
     }
   }
-  for (int64_t v = hend + nvec * VEC + threadIdx.x; v < v_hi; v += blockDim.x) f(In<DT>::bits(row, v));
+  for (int64_t v = hend + nvec * VEC + threadIdx.x; v < v_hi; v += blockDim.x) {
+    group();
+    f(In<DT>::bits(row, v));
+  }
 }
 
 template <int DT>
@@ -58,7 +66,7 @@ __global__ void __launch_bounds__(256) dce_rowmax_kernel(const DceArgs a) {
     if (nonfinite_bits(u)) { nf = ST_NONFINITE; return; }
     float x = __uint_as_float(u);
     mx = x > mx ? x : mx;
-  });
+  }, [] {});
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
   __shared__ float wm[8];
@@ -81,33 +89,18 @@ __global__ void __launch_bounds__(DEN_THREADS, 6) dce_denom_kernel(const DceArgs
   const int64_t i = blockIdx.x;
   const T* row = (const T*)a.x + i * a.rs;
   const float m = a.m_in[i];
-  long long d0 = 0, d1 = 0, d2 = 0, d3 = 0, d4 = 0, d5 = 0;   // word k weighs 2^(32k - 160)
+  DenAcc A;   // exact: a private word for w >= 2^-31, digit words for the rest (den_acc.cuh)
+  den_init(A);
   int st = 0;
   for_row<DT>(row, a.v_lo, a.v_hi, [&](uint32_t u) {
     if (nonfinite_bits(u)) { st |= ST_NONFINITE; return; }
     float x = __fsub_rn(__uint_as_float(u), m);
     if (x != x) { st |= ST_NONFINITE; return; }
     if (x > 0.0f) { st |= ST_VIOLATION; x = 0.0f; }
-    const uint32_t wb = __float_as_uint(exp32_det_nb(x));   // x <= 0, not NaN
-    if (wb == 0u) return;
-    const int ex = (int)(wb >> 23);
-    const uint32_t M = ex ? ((wb & 0x7FFFFFu) | 0x800000u) : wb;
-    const int pos = (ex ? ex : 1) + 10;        // bit position of M's unit above 2^-160
-    const int k = pos >> 5;
-    const unsigned long long ch = (unsigned long long)M << (pos & 31);
-    const long long c0 = (long long)(ch & 0xFFFFFFFFull), c1 = (long long)(ch >> 32);
-    if (k >= 3) {                               // w >= 2^-74: the common case
-      const bool k4 = (k == 4);
-      d3 += k4 ? 0 : c0;
-      d4 += k4 ? c0 : c1;
-      d5 += k4 ? c1 : 0;
-    } else {
-      if (k == 0) { d0 += c0; d1 += c1; }
-      else if (k == 1) { d1 += c0; d2 += c1; }
-      else { d2 += c0; d3 += c1; }
-    }
-  });
-  long long dg[6] = {d0, d1, d2, d3, d4, d5};
+    den_add(A, __float_as_uint(exp32_det_nb(x)));   // x <= 0, not NaN
+  }, [&] { den_guard(A); });
+  den_flush(A);
+  long long dg[6] = {A.d[0], A.d[1], A.d[2], A.d[3], A.d[4], A.d[5]};
 #pragma unroll
   for (int k = 0; k < 6; k++)
 #pragma unroll
