@@ -18,13 +18,17 @@ Sources (page title, section):
   * "det-attn", section "Correctness" and "Requirements and limits": causal and
     non-causal, MHA and GQA, f32 and bf16 inputs, D <= 256, f32 output.
   * "det-cross-entropy" model card, sections "Usage", "API", "Method": per-token
-    rowmax over a vocab range, exact denominator digits, finalize to (loss, denom).
+    rowmax over a vocab range, exact denominator digits, finalize to (loss, denom); the
+    gradient softmax(x_i) - onehot(t_i) from the forward's state and the loss reductions
+    "none" / "sum" / "mean" of cross_entropy.
 
 The pages leave the roundings open.  The readings taken here (score = correctly rounded
 f32 of the exact dot, then one f32 multiply by the scale; a fixed f32 exp routine; digits
 in radix 2**32; finalize rounds NUM and DEN to f64, divides, rounds to f32) are the
 numerical contract the CUDA path must meet bit for bit.  Parity status: pinned (see
-tests/test_oracle_pins.py); nothing in this module is "parity unpinned".
+tests/test_oracle_pins.py, tests/test_dce_backward_oracle.py and tests/test_golden.py;
+tests/test_oracle_mutations.py shows the pins reject planted slips); nothing in this
+module is "parity unpinned".
 """
 from __future__ import annotations
 

@@ -3,7 +3,9 @@
 The C oracle computes the same definition as oracle/exact.py, independently written, fast
 enough for whole rows of the full-size workloads.  build() compiles it with the host C
 compiler; -ffp-contract=off keeps every binary32/binary64 operation a single IEEE
-operation (no fused multiply-add unless the source writes fmaf).
+operation (no fused multiply-add unless the source writes fmaf).  dce_backward_many is the
+cross-entropy gradient of oracle/exact.py vectorized with numpy on top of the C exp32_det
+(pinned equal to the exact rational version in tests/test_dce_backward_oracle.py).
 """
 from __future__ import annotations
 
