@@ -6,7 +6,8 @@ at every world size.  Here each gloo rank owns a contiguous KV shard, computes i
 rowmax and digits with the oracle, and the ranks combine them with all_reduce(MAX) and
 all_reduce(SUM) on int64 - the collectives a multi-GPU deployment would run.  The result
 must equal the fused single-process result bit for bit, in either rank order.  A missing
-or duplicated shard must change it (failure detection by comparison).
+or duplicated shard must change it (failure detection by comparison).  The vocab-parallel
+cross-entropy (page "det-cross-entropy") is composed the same way at the end of the file.
 """
 import os
 import socket
@@ -96,3 +97,66 @@ def test_missing_or_duplicated_shard_is_detected(fused):
     dup = native.finalize(native.normalize(n0 + n1 + n1, -320)[0], native.normalize(d0 + d1 + d1, -160)[0])
     assert not np.array_equal(missing, fused[3])
     assert not np.array_equal(dup, fused[3])
+
+
+# ------------------------------------------------ vocab-parallel cross-entropy (gloo, 2 ranks)
+#
+# Page "det-cross-entropy", sections "Usage" and "Method": a vocab-parallel LM head keeps a
+# column range of the logits per rank; the rowmax composes by max, the denominator digits by
+# int64 addition, and finalize gives the loss; the gradient softmax - onehot of each rank's
+# columns needs only the global rowmax and denominator.
+
+def _dce_case():
+    g = torch.Generator().manual_seed(78)
+    x = torch.randn(24, 3001, generator=g) * 2
+    t = torch.randint(0, 3001, (24,), generator=g)
+    return x, t
+
+
+def _dce_worker(rank, world, port, splits, outq):
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from oracle import native
+    from oracle import exact as E
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    x, t = _dce_case()
+    D = native.DCE(x)
+    bounds = np.cumsum([0] + splits)
+    lo, hi = int(bounds[rank]), int(bounds[rank + 1])
+    m, _ = D.rowmax(lo, hi, nthreads=1)
+    mt = torch.from_numpy(m.copy())
+    dist.all_reduce(mt, op=dist.ReduceOp.MAX)
+    den, _ = D.denom_digits(mt.numpy(), lo, hi, nthreads=1)
+    dt_ = torch.from_numpy(den.copy())
+    dist.all_reduce(dt_, op=dist.ReduceOp.SUM)
+    denc, _ = native.normalize(dt_.numpy(), -160)
+    loss, denom, st = D.finalize(denc, t.numpy(), mt.numpy())
+    go = E.dce_go(np.ones(1, np.float32), 24, "mean")
+    grad = native.dce_backward_many(x[:, lo:hi], t.numpy() - lo, mt.numpy(), denom, go)
+    parts = [None] * world
+    dist.all_gather_object(parts, grad)
+    if rank == 0:
+        outq.put((loss, denom, np.concatenate(parts, axis=1), st))
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("splits", [[1500, 1501], [1, 3000]])
+def test_gloo_vocab_parallel_cross_entropy_equals_single_process(splits):
+    from oracle import native
+    from oracle import exact as E
+    ctx = mp.get_context("spawn")
+    q = ctx.SimpleQueue()
+    port = _free_port()
+    procs = [ctx.Process(target=_dce_worker, args=(r, 2, port, splits, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    loss, denom, grad, st = q.get()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    x, t = _dce_case()
+    rl, rd, rm, rden, st1 = native.DCE(x).forward(t.numpy())
+    want = native.dce_backward_many(x, t.numpy(), rm, rd, E.dce_go(np.ones(1, np.float32), 24, "mean"))
+    assert st == 0
+    assert np.array_equal(loss.view(np.uint32), rl.view(np.uint32)) and np.array_equal(denom, rd)
+    assert np.array_equal(grad.view(np.uint32), want.view(np.uint32))
