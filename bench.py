@@ -40,7 +40,7 @@ UNIT = "MAC/s"
 
 
 # DRAM bytes (read + write) of one accumulate launch at the metric workload, from the ncu capture
-# summarised in profiles/accumulate_tp_long_context_C3_H4.md (the 4-head case scaled by 4: the
+# summarised in profiles/accumulate_tp_long_context_causal_S4096_H4.md (the 4-head case scaled by 4: the
 # traffic is per head); set to None whenever the kernel changes until it is captured again
 ACC_TRAFFIC_PER_LAUNCH = 4 * 88.41e6
 
@@ -118,7 +118,7 @@ def oracle_sample(w, Q, K, V, rows_per_head: int, nthreads: int):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    w = W.c3()
+    w = W.long_context_causal()
     Q, K, V = w.tensors("cpu")
     cores = os.cpu_count() or 1
     rows_per_head = args.ref_rows_step
@@ -151,7 +151,7 @@ def run_dce(args, dev, stream):
     over its event time."""
     import bitwise_deterministic_shard_gb300 as da
     L = da.lib()
-    w = W.c5()
+    w = W.vocab_sharded_ce()
     if args.dce_rows != w.N:                   # smaller case of the same kernels (profiling)
         w.name = w.name.replace(f"N{w.N}", f"N{args.dce_rows}")
         w.N = args.dce_rows
@@ -225,7 +225,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
-    w = W.c3()
+    w = W.long_context_causal()
     if args.heads != w.Hq:                     # smaller case of the same kernels (profiling)
         w.Hq = w.Hkv = args.heads
         w.name = w.name.replace("H16", f"H{args.heads}")

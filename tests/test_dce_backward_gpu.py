@@ -159,10 +159,10 @@ def test_backward_argument_errors(da):
 
 
 @cuda
-def test_c5_backward_sampled_rows(da, orc):
+def test_vocab_sharded_backward_sampled_rows(da, orc):
     """The N4096 x V128256 f32 vocab-sharded workload: mean-reduced cross-entropy and its
     dLogits, split-invariant, and sampled rows against the oracle."""
-    w = W.c5()
+    w = W.vocab_sharded_ce()
     x, t = w.tensors("cuda")
     grads = []
     for sp in (w.splits[0], w.splits[-1]):
@@ -178,7 +178,7 @@ def test_c5_backward_sampled_rows(da, orc):
     rl, rd, rm, rden, st = orc.DCE(xs).forward(ts.numpy())
     go = E.dce_go(np.ones(1, dtype=np.float32), w.N, "mean")[: len(rows)]
     want = _want(orc, xs, ts, rm, rd, go, torch.float32)
-    _assert_same(grads[0][1][torch.from_numpy(rows).cuda()], want, "C5 sampled dLogits")
+    _assert_same(grads[0][1][torch.from_numpy(rows).cuda()], want, "vocab-sharded sampled dLogits")
     # the det-cross-entropy page's match to torch: loss within 1.9e-6, gradient within 1.2e-10
     x64 = x.double().requires_grad_(True)
     ref = torch.nn.functional.cross_entropy(x64, t)

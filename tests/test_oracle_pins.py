@@ -201,10 +201,10 @@ def _naive64(Q, K, V, causal, scale):
     return torch.softmax(s, -1) @ V
 
 
-def test_c1_agrees_with_naive_float64_attention(oracle_native):
+def test_tiny_exact_agrees_with_naive_float64_attention(oracle_native):
     """North-star agreement: the exact result equals a naive float64 softmax attention to
     1e-6 absolute on the tiny f32 workload."""
-    w = W.c1()
+    w = W.tiny_exact()
     Q, K, V = w.tensors()
     A = oracle_native.Attn(Q, K, V, w.causal, w.scale)
     _, _, _, out = A.forward_rows()
@@ -329,8 +329,8 @@ def test_python_sharded_equals_fused_all_orders():
                               fused.view(np.uint32))
 
 
-def test_c1_sharded_all_24_orders_equal_fused(oracle_native):
-    w = W.c1()
+def test_tiny_exact_sharded_all_24_orders_equal_fused(oracle_native):
+    w = W.tiny_exact()
     Q, K, V = w.tensors()
     A = oracle_native.Attn(Q, K, V, w.causal, w.scale)
     m0, n0, d0, o0 = A.forward_rows()

@@ -157,12 +157,12 @@ def test_extreme_digit_patterns_match_oracle(da, orc, D):
 
 
 @cuda
-def test_c1_fused_and_all_24_orders(da, orc):
-    w = W.c1()
+def test_tiny_exact_fused_and_all_24_orders(da, orc):
+    w = W.tiny_exact()
     Q, K, V = w.tensors("cuda")
     fused = da.det_attn(Q, K, V, causal=w.causal, scale=w.scale)
     _, _, _, ref = orc.Attn(Q.cpu(), K.cpu(), V.cpu(), w.causal, w.scale).forward_rows()
-    assert_bits_equal(fused.reshape(-1, w.D), ref, "C1 fused vs oracle")
+    assert_bits_equal(fused.reshape(-1, w.D), ref, "tiny fused vs oracle")
     for sp, order in w.splits:
         out = da.det_attn_sharded(Q, K, V, sp, causal=w.causal, scale=w.scale, order=order)
         assert torch.equal(out, fused), order
@@ -173,21 +173,21 @@ def test_c1_fused_and_all_24_orders(da, orc):
 
 
 @cuda
-def test_c2_gqa_causal_splits_and_oracle(da, orc):
-    w = W.c2()
+def test_gqa_causal_splits_and_oracle(da, orc):
+    w = W.gqa_causal()
     Q, K, V = w.tensors("cuda")
     fused = da.det_attn(Q, K, V, causal=True)
     torch.cuda.synchronize()
     _, _, _, ref = orc.Attn(Q.cpu(), K.cpu(), V.cpu(), True).forward_rows()
-    assert_bits_equal(fused.reshape(-1, w.D), ref, "C2 fused vs oracle")
+    assert_bits_equal(fused.reshape(-1, w.D), ref, "GQA causal fused vs oracle")
     for sp, order in w.splits:
         out = da.det_attn_sharded(Q, K, V, sp, causal=True, order=order)
         assert torch.equal(out, fused), (sp, order)
 
 
 @cuda
-def test_c3_ring_steps_and_sampled_oracle(da, orc):
-    w = W.c3()
+def test_long_context_ring_steps_and_sampled_oracle(da, orc):
+    w = W.long_context_causal()
     Q, K, V = w.tensors("cuda")
     st = da.new_status()
     fused = da.det_attn(Q, K, V, causal=True, status=st)
@@ -199,18 +199,18 @@ def test_c3_ring_steps_and_sampled_oracle(da, orc):
     fl = flat_rows(1, w.Hq, w.S, rows)
     _, _, _, ref = A.forward_rows(rows=fl)
     got = fused.reshape(-1, w.D)[torch.from_numpy(fl).cuda()]
-    assert_bits_equal(got, ref, "C3 sampled rows vs oracle")
+    assert_bits_equal(got, ref, "long-context sampled rows vs oracle")
     for sp, order in w.splits:
         out = da.det_attn_sharded(Q, K, V, sp, causal=True, order=order)
         assert torch.equal(out, fused), len(sp)
 
 
 @cuda
-def test_c4_unequal_splits_and_sampled_oracle(da, orc):
+def test_large_noncausal_unequal_splits_and_sampled_oracle(da, orc):
     """Large non-causal workload at full size (B1 H56 S37810 D128 bf16; S is no tile
     multiple): the fused call, the 32 unequal random splits composed in a random order,
     and sampled rows (4 per head plus the last row) against the oracle."""
-    w = W.c4()
+    w = W.large_noncausal()
     Q, K, V = w.tensors("cuda")
     st = da.new_status()
     fused = da.det_attn(Q, K, V, status=st)
@@ -229,14 +229,14 @@ def test_c4_unequal_splits_and_sampled_oracle(da, orc):
     A = orc.Attn(Q.cpu(), K.cpu(), V.cpu(), False)
     _, _, _, ref = A.forward_rows(rows=fl)
     got = fused.reshape(-1, w.D)[torch.from_numpy(fl).cuda()]
-    assert_bits_equal(got, ref, "C4 sampled rows vs oracle")
+    assert_bits_equal(got, ref, "large non-causal sampled rows vs oracle")
 
 
 @cuda
-def test_c3_shard_digits_compose_to_fused_digits(da):
+def test_long_context_shard_digits_compose_to_fused_digits(da):
     """accumulate per shard into separate arrays + compose_add + normalize equals the
     fused digits (det-attn "Method": an int64 add of digit arrays)."""
-    w = W.c3()
+    w = W.long_context_causal()
     Q, K, V = w.tensors("cuda")
     Q, K, V = Q[:, :4, :1024], K[:, :4, :1024], V[:, :4, :1024]
     m = da.rowmax(Q, K, causal=True)
@@ -258,7 +258,7 @@ def test_c3_shard_digits_compose_to_fused_digits(da):
 
 @cuda
 def test_repeat_runs_bitwise_identical(da):
-    w = W.c3()
+    w = W.long_context_causal()
     Q, K, V = w.tensors("cuda")
     a = da.det_attn(Q, K, V, causal=True)
     b = da.det_attn(Q, K, V, causal=True)
@@ -379,8 +379,8 @@ def test_dce_small_matches_oracle(da, orc, dt):
 
 
 @cuda
-def test_c5_vocab_splits_and_oracle(da, orc):
-    w = W.c5()
+def test_vocab_sharded_splits_and_oracle(da, orc):
+    w = W.vocab_sharded_ce()
     x, t = w.tensors("cuda")
     base = da.dce_forward(x, t)
     for sp in w.splits[1:]:
@@ -390,7 +390,7 @@ def test_c5_vocab_splits_and_oracle(da, orc):
     rows = np.arange(0, w.N, 8, dtype=np.int64)
     D = orc.DCE(x.cpu())
     rl, rd, rm, rden, st = D.forward(t.cpu().numpy(), rows=rows)
-    assert_bits_equal(base[0][torch.from_numpy(rows).cuda()], rl, "C5 loss")
+    assert_bits_equal(base[0][torch.from_numpy(rows).cuda()], rl, "vocab-sharded loss")
     assert torch.equal(base[1][torch.from_numpy(rows).cuda()].cpu(), torch.from_numpy(rd))
     ref = torch.nn.functional.cross_entropy(x.double(), t, reduction="none")
     assert float((base[0].double() - ref).abs().max()) < 2e-6

@@ -63,7 +63,7 @@ def equal_splits(S: int, n: int) -> list:
     return [base + (1 if i < rem else 0) for i in range(n)]
 
 
-def _c2_splits():
+def _gqa_causal_splits():
     r = random.Random(2)
     out = []
     for n in (4, 8):
@@ -75,7 +75,7 @@ def _c2_splits():
     return out
 
 
-def _c4_splits():
+def _large_noncausal_splits():
     r = random.Random(4)
     cuts = sorted(r.sample(range(1, 37810), 31))
     b = [0] + cuts + [37810]
@@ -85,27 +85,27 @@ def _c4_splits():
     return [(sp, order)]
 
 
-def c1():
+def tiny_exact():
     import itertools
     perms = [([32] * 4, list(p)) for p in itertools.permutations(range(4))]
     return AttnWorkload("tiny exact check B1 H2 S128 D64 f32", 1, 2, 2, 128, 64, torch.float32, False, 0,
                         scale=0.125, splits=perms)
 
 
-def c2():
+def gqa_causal():
     return AttnWorkload("GQA causal B2 Hq8 Hkv2 S1024 D128 bf16", 2, 8, 2, 1024, 128, torch.bfloat16, True, 2,
-                        splits=_c2_splits())
+                        splits=_gqa_causal_splits())
 
 
-def c3():
+def long_context_causal():
     return AttnWorkload("long-context causal B1 H16 S4096 D128 bf16, 1% of K rows x8", 1, 16, 16, 4096, 128,
                         torch.bfloat16, True, 3, big_k_frac=0.01,
                         splits=[(equal_splits(4096, n), list(range(n))) for n in (1, 2, 4, 8, 16, 32)])
 
 
-def c4():
+def large_noncausal():
     return AttnWorkload("large non-causal B1 H56 S37810 D128 bf16", 1, 56, 56, 37810, 128, torch.bfloat16, False, 4,
-                        splits=_c4_splits())
+                        splits=_large_noncausal_splits())
 
 
 @dataclass
@@ -125,7 +125,7 @@ class DCEWorkload:
         return logits.to(device), targets.to(device)
 
 
-def c5():
+def vocab_sharded_ce():
     return DCEWorkload("vocab-sharded cross-entropy N4096 V128256 f32", 4096, 128256, torch.float32, 5,
                        splits=[equal_splits(128256, n) for n in (1, 2, 4, 8)])
 
