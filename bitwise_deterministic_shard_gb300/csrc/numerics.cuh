@@ -477,17 +477,29 @@ __device__ __forceinline__ void atomic_digits_add(long long* dg, int64_t stride,
 }
 
 // acc += a * b exactly: one 32x32 -> 64-bit signed multiply-add (mad.wide.s32)
+// (The #else branches let host tests compile this header with a host C++ compiler; device
+// code always takes the PTX.)
 __device__ __forceinline__ void mad_wide(long long& acc, int a, int b) {
+#if defined(__CUDA_ARCH__)
   asm("mad.wide.s32 %0, %1, %2, %0;" : "+l"(acc) : "r"(a), "r"(b));
+#else
+  acc += (long long)a * b;
+#endif
 }
 
 // 16-byte asynchronous global -> shared copy (zero-filled when src_bytes == 0)
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+#if defined(__CUDA_ARCH__)
   const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sa), "l"(gmem), "r"(src_bytes));
+#else
+  for (int b = 0; b < 16; b++) ((unsigned char*)smem)[b] = b < src_bytes ? ((const unsigned char*)gmem)[b] : 0;
+#endif
 }
 __device__ __forceinline__ void cp_async_wait_all() {
+#if defined(__CUDA_ARCH__)
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+#endif
 }
 
 // order-preserving int key of a binary32 (not NaN): key(a) < key(b) iff a < b, with -0 < +0
