@@ -60,3 +60,6 @@ inline int __all_sync(unsigned, int p) { return p; }
 inline int __reduce_max_sync(unsigned, int v) { return v; }
 inline unsigned __reduce_add_sync(unsigned, unsigned v) { return v; }
 inline void __syncwarp(unsigned = 0xFFFFFFFFu) {}
+inline unsigned __ballot_sync(unsigned, int p) { return p ? 1u : 0u; }
+inline int __any_sync(unsigned, int p) { return p; }
+inline int __popc(unsigned x) { return __builtin_popcount(x); }

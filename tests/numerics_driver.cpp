@@ -5,10 +5,16 @@
 //   mode 2: 15 int64 digits    -> digits_rn64<15>(digits, -320)            (binary64)
 //   mode 3: 6 int64 digits     -> digits_rn64<6>(digits, -160)             (binary64)
 //   mode 4: binary64 d         -> log64_det(d)                             (binary64)
+//   mode 5: int32 X            -> slice4(X): four bf16 bit patterns
+//   mode 6: 7 binary32 A_c     -> combine_diag: int64 sum_c 2^(7c) A_c
+//   mode 7: (uint32 u, int32 F) -> hi26(u, F)
+//   mode 8: records for dot_lo (see below)                                  (binary32 bits)
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <vector>
 #include "numerics.cuh"
+#include "score_tc.cuh"
 using namespace detattn;
 
 template <class T>
@@ -55,6 +61,45 @@ int main(int argc, char** argv) {
     for (double d : read_all<double>()) {
       const double r = log64_det(d);
       fwrite(&r, 8, 1, stdout);
+    }
+  } else if (mode == 5) {
+    for (int X : read_all<int>()) {
+      uint16_t s[NSLICE];
+      slice4(X, s);
+      fwrite(s, 2, NSLICE, stdout);
+    }
+  } else if (mode == 6) {
+    const std::vector<float> in = read_all<float>();
+    for (size_t i = 0; i + NDIAG <= in.size(); i += NDIAG) {
+      float acc[NDIAG][1];
+      for (int c = 0; c < NDIAG; c++) acc[c][0] = in[i + c];
+      const long long T = combine_diag<1>(acc, 0);
+      fwrite(&T, 8, 1, stdout);
+    }
+  } else if (mode == 7) {
+    const std::vector<int> in = read_all<int>();
+    for (size_t i = 0; i + 1 < in.size(); i += 2) {
+      const int r = hi26((uint32_t)in[i], in[i + 1]);
+      fwrite(&r, 4, 1, stdout);
+    }
+  } else if (mode == 8) {
+    // record: int32 D, Fq, Fk, nq, nk; int64 Thh; D binary32 q; D binary32 k; nq (d, lo); nk (d, lo)
+    const std::vector<int> in = read_all<int>();
+    size_t i = 0;
+    while (i + 7 <= in.size()) {
+      const int D = in[i], Fq = in[i + 1], Fk = in[i + 2], nq = in[i + 3], nk = in[i + 4];
+      long long Thh;
+      memcpy(&Thh, &in[i + 5], 8);
+      i += 7;
+      const float* q = reinterpret_cast<const float*>(&in[i]);
+      const float* k = reinterpret_cast<const float*>(&in[i + D]);
+      i += 2 * D;
+      const int2* ql = reinterpret_cast<const int2*>(&in[i]);
+      i += 2 * nq;
+      const int2* kl = reinterpret_cast<const int2*>(&in[i]);
+      i += 2 * nk;
+      const uint32_t r = __float_as_uint(dot_lo<0>(Thh, q, Fq, ql, nq, k, Fk, kl, nk));
+      fwrite(&r, 4, 1, stdout);
     }
   }
   return 0;

@@ -87,3 +87,105 @@ def test_log64_det_equals_the_oracle(drv, oracle_native):
                         np.array([1.0, 2.0, 1.5, np.sqrt(2.0), 2.0 ** 31, np.nextafter(1.0, 2.0)])])
     got = drv(4, d, np.float64, 1)[:, 0]
     assert np.array_equal(got.view(np.uint64), oracle_native.log64_det_many(d).view(np.uint64))
+
+
+# ------------------------------------------------------- the exact score on the tensor cores
+# (csrc/score_tc.cuh): a row's 26-bit fixed point X split into four balanced base-128 bf16
+# slices; the seven diagonal sums A_c of slice products (what the MMAs accumulate, exact in
+# f32) recombined into the int64 dot; rows outside the window corrected by their low limbs.
+
+def _bf16_to_int(bits):
+    return np.array(bits, dtype=np.uint32).__lshift__(16).view(np.float32).astype(np.int64)
+
+
+def test_slices_recompose_the_fixed_point(drv):
+    rng = np.random.default_rng(55)
+    X = np.concatenate([rng.integers(-(2 ** 26) + 1, 2 ** 26, 200_000),
+                        [0, 1, -1, 63, 64, -64, -65, 2 ** 26 - 1, -(2 ** 26) + 1]]).astype(np.int32)
+    s = _bf16_to_int(drv(5, X, np.uint16, 4).astype(np.uint32))
+    assert np.all(np.abs(s) <= 64)
+    assert np.array_equal(s[:, 0] + s[:, 1] * 2 ** 7 + s[:, 2] * 2 ** 14 + s[:, 3] * 2 ** 21, X.astype(np.int64))
+
+
+def test_diagonal_sums_recombine_to_the_exact_dot(drv):
+    """Slices of random 26-bit rows (D = 128 and 256), the seven diagonal sums formed exactly,
+    handed to combine_diag as the f32 values the tensor core holds: the int64 dot."""
+    rng = np.random.default_rng(56)
+    A_all, dots = [], []
+    for D in (128, 256):
+        for _ in range(40):
+            q = rng.integers(-(2 ** 26) + 1, 2 ** 26, D).astype(np.int32)
+            k = rng.integers(-(2 ** 26) + 1, 2 ** 26, D).astype(np.int32)
+            if rng.random() < 0.3:
+                q[rng.random(D) < 0.5] = 0
+            sq = _bf16_to_int(drv(5, q, np.uint16, 4).astype(np.uint32))
+            sk = _bf16_to_int(drv(5, k, np.uint16, 4).astype(np.uint32))
+            A = [sum(int((sq[:, a] * sk[:, c - a]).sum()) for a in range(4) if 0 <= c - a < 4) for c in range(7)]
+            assert max(abs(v) for v in A) <= 2 ** 22
+            A_all.append(A)
+            dots.append(int((q.astype(object) * k.astype(object)).sum()))
+    T = drv(6, np.array(A_all, dtype=np.float32), np.int64, 1)[:, 0]
+    assert [int(t) for t in T] == dots
+
+
+def test_hi26_truncates_toward_zero(drv):
+    rng = np.random.default_rng(57)
+    x = (rng.standard_normal(50_000) * np.exp2(rng.integers(-40, 40, 50_000))).astype(np.float32)
+    F = rng.integers(-180, 40, 50_000).astype(np.int32)
+    emax = ((x.view(np.uint32) >> 23) & 0xFF).astype(np.int64)
+    F = np.maximum(F, emax - 152).astype(np.int32)              # windows a row can have (|X| < 2^26)
+    pairs = np.stack([x.view(np.int32), F], axis=1)
+    got = drv(7, pairs, np.int32, 1)[:, 0]
+    for xi, fi, g in zip(x.tolist(), F.tolist(), got.tolist()):
+        v = Fraction(xi) / Fraction(2) ** fi
+        assert g == (int(v) if v >= 0 else -int(-v)), (xi, fi)
+
+
+def _row_limbs(x, F):
+    """(X_hi, listed low limbs) of a row in window F per the score_tc.cuh definitions, or None
+    for a deep row."""
+    hi, lo = [], []
+    for d, xv in enumerate(x.tolist()):
+        v = Fraction(xv) / Fraction(2) ** F
+        h = int(v) if v >= 0 else -int(-v)
+        r = (v - h) * 2 ** 26
+        if r.denominator != 1:
+            return None
+        hi.append(h)
+        if r:
+            lo.append((d, int(r)))
+    return (hi, lo) if len(lo) <= 4 else None
+
+
+def test_low_limb_correction_gives_the_exact_score(drv):
+    """bf16-valued rows (8 significant bits) with a few elements scaled 2^-19 .. 2^-24 below
+    the rest, so that their low bits fall under the 26-bit window as listed low limbs."""
+    rng = np.random.default_rng(58)
+    recs, want = [], []
+    D = 128
+
+    def bf16_row():
+        r = rng.standard_normal(D).astype(np.float32)
+        r = (r.view(np.uint32) & 0xFFFF0000).view(np.float32)
+        idx = rng.choice(D, rng.integers(0, 5), replace=False)
+        r[idx] = r[idx] * np.exp2(-rng.integers(19, 25, len(idx))).astype(np.float32)
+        return r
+
+    for _ in range(4000):
+        if len(recs) >= 300:
+            break
+        q, k = bf16_row(), bf16_row()
+        Fq = int(((q.view(np.uint32) >> 23) & 0xFF).max()) - 152
+        Fk = int(((k.view(np.uint32) >> 23) & 0xFF).max()) - 152
+        lq, lk = _row_limbs(q, Fq), _row_limbs(k, Fk)
+        if lq is None or lk is None:
+            continue
+        Thh = sum(a * b for a, b in zip(lq[0], lk[0]))
+        head = np.array([D, Fq, Fk, len(lq[1]), len(lk[1])], np.int32).tobytes() + np.int64(Thh).tobytes()
+        body = q.tobytes() + k.tobytes() + np.array(lq[1] + lk[1], np.int32).reshape(-1).tobytes()
+        recs.append(head + body)
+        exact = sum((Fraction(a) * Fraction(b) for a, b in zip(q.tolist(), k.tolist())), Fraction(0))
+        want.append(int(np.float32(E.rn32(exact)).view(np.uint32)))
+    assert len(recs) >= 100
+    got = drv(8, np.frombuffer(b"".join(recs), np.uint8), np.uint32, 1)[:, 0]
+    assert got.tolist() == want
