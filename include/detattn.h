@@ -156,8 +156,10 @@ int da_finalize(const int64_t* num, const int64_t* den, int64_t B, int64_t Hq, i
 /* Bytes of workspace da_det_attn (nsplits <= 1) or da_det_attn_sharded needs. */
 size_t da_workspace_bytes(const da_attn_desc* desc, int nsplits);
 
-/* det-attn "API", det_attn: rowmax over all keys, accumulate, finalize.  out: device f32
- * [B, Hq, Sq, D] contiguous; ws: device workspace of at least da_workspace_bytes(desc, 1). */
+/* det-attn "API", det_attn: rowmax over all keys, then da_accumulate_finalize (accumulate and
+ * finalize; for 64 < D <= 128 in one kernel that writes only the output).  out: device f32
+ * [B, Hq, Sq, D] contiguous; ws: device workspace of at least da_workspace_bytes(desc, 1).
+ * Bit-identical to da_det_attn_sharded for every split and order. */
 int da_det_attn(const da_attn_desc* desc, float* out, void* ws, size_t ws_bytes, da_stream_t stream);
 
 /* det-attn "API", det_attn_sharded: the keys split into nsplits contiguous shards of
