@@ -54,7 +54,7 @@ def lib():
     if _lib is None:
         if not os.path.exists(LIB_PATH):
             raise DetAttnError(f"{LIB_PATH} is missing: build it with "
-                               "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+                               "`python -m bitwise_deterministic_shard_gb300.build` (needs nvcc)")
         L = C.CDLL(LIB_PATH)
         L.da_abi_version.restype = C.c_int
         L.da_status_string.argtypes = [C.c_int]
