@@ -296,10 +296,19 @@ def dce_rowmax(logits, v_lo=0, v_hi=None, out=None, status=None):
     return m
 
 
+def _vec(t, dtype, n, name):
+    """A per-row input: a CUDA tensor of the given dtype and element count, made contiguous."""
+    _cuda(t, name)
+    if t.dtype != dtype or t.numel() != n:
+        raise DetAttnError(f"{name} must be a {dtype} tensor of {n} elements")
+    return t.contiguous()
+
+
 def dce_denom_digits(logits, m, v_lo=0, v_hi=None, den=None, add_into=False, status=None):
     """Exact denominator digits over [v_lo, v_hi) with the global rowmax m
     (det-cross-entropy "API": denom_digits); int64 [N, 6]."""
     M, keep = _matrix(logits)
+    m = _vec(m, torch.float32, M.rows, "rowmax")
     v_hi = M.cols if v_hi is None else v_hi
     den = torch.empty(M.rows, DEN_NDIG, dtype=torch.int64, device=logits.device) if den is None else den
     _check(lib().dce_denom_digits(C.byref(M), _ptr(m), v_lo, v_hi, _ptr(den), 1 if add_into else 0, _ptr(status),
@@ -310,9 +319,11 @@ def dce_denom_digits(logits, m, v_lo=0, v_hi=None, den=None, add_into=False, sta
 def dce_finalize(den, logits, targets, m, status=None):
     """(loss f32 [N], denom f64 [N]) from composed digits (det-cross-entropy "API": finalize)."""
     M, keep = _matrix(logits)
+    den = _vec(den, torch.int64, M.rows * DEN_NDIG, "den")
+    m = _vec(m, torch.float32, M.rows, "rowmax")
+    targets = _vec(targets.to(torch.int64), torch.int64, M.rows, "targets")
     loss = torch.empty(M.rows, dtype=torch.float32, device=logits.device)
     denom = torch.empty(M.rows, dtype=torch.float64, device=logits.device)
-    targets = targets.to(torch.int64).contiguous()
     _check(lib().dce_finalize(_ptr(den), C.byref(M), _ptr(targets), _ptr(m), _ptr(loss), _ptr(denom), _ptr(status),
                               _stream()), "dce_finalize")
     return loss, denom
@@ -350,11 +361,15 @@ def dce_backward(logits, targets, m, denom, grad, reduction="none", status=None)
     go_i = grad[i] ("none"), grad ("sum"), RN32(RN64(grad / N)) ("mean").  Returns a tensor
     shaped like logits, of its dtype."""
     M, keep = _matrix(logits)
+    if reduction not in _REDUCTIONS:
+        raise DetAttnError("reduction must be 'none', 'sum' or 'mean'")
     red = _REDUCTIONS[reduction]
     grad = grad.to(torch.float32).reshape(-1).contiguous()
     if grad.numel() != (M.rows if red == 0 else 1):
         raise DetAttnError("grad must have one entry per row for reduction='none', else one entry")
-    targets = targets.to(torch.int64).contiguous()
+    targets = _vec(targets.to(torch.int64), torch.int64, M.rows, "targets")
+    m = _vec(m, torch.float32, M.rows, "rowmax")
+    denom = _vec(denom, torch.float64, M.rows, "denom")
     out = torch.empty((M.rows, M.cols), dtype=logits.dtype, device=logits.device)
     _check(lib().dce_backward(C.byref(M), _ptr(targets), _ptr(m), _ptr(denom), _ptr(grad), red, _ptr(out),
                               _ptr(status), _stream()), "dce_backward")
@@ -364,6 +379,9 @@ def dce_backward(logits, targets, m, denom, grad, reduction="none", status=None)
 def dce_reduce(loss, reduction="mean"):
     """sum / mean of the f32 losses through their exact (Kulisch) sum, independent of the
     rows' order: RN32(RN64(S)) / RN32(RN64(RN64(S) / N))."""
+    _cuda(loss, "loss")
+    if reduction not in ("sum", "mean"):
+        raise DetAttnError("reduction must be 'sum' or 'mean'")
     loss = loss.to(torch.float32).contiguous()
     out = torch.empty((), dtype=torch.float32, device=loss.device)
     _check(lib().dce_reduce(_ptr(loss), loss.numel(), _REDUCTIONS[reduction], _ptr(out), _stream()), "dce_reduce")
@@ -416,8 +434,10 @@ def dce_forward_static(logits, targets, status=None):
     f.argtypes = [C.POINTER(_Matrix), _P, _P, _P, _P, _P]
     f.restype = C.c_int
     M, keep = _matrix(logits)
+    den = _vec(den, torch.int64, M.rows * DEN_NDIG, "den")
+    m = _vec(m, torch.float32, M.rows, "rowmax")
+    targets = _vec(targets.to(torch.int64), torch.int64, M.rows, "targets")
     loss = torch.empty(M.rows, dtype=torch.float32, device=logits.device)
     denom = torch.empty(M.rows, dtype=torch.float64, device=logits.device)
-    targets = targets.to(torch.int64).contiguous()
     _check(f(C.byref(M), _ptr(targets), _ptr(loss), _ptr(denom), _ptr(status), _stream()), "dce_forward_static")
     return loss, denom
