@@ -79,9 +79,10 @@ def lib():
         L.dce_finalize.argtypes = [_P, M, _P, _P, _P, _P, _P, _P]
         L.dce_backward.argtypes = [M, _P, _P, _P, _P, _I32, _P, _P, _P]
         L.dce_reduce.argtypes = [_P, _I64, _I32, _P, _P]
+        L.dce_forward_static.argtypes = [M, _P, _P, _P, _P, _P]
         for f in ("da_rowmax", "da_accumulate", "da_compose_max", "da_compose_add", "da_normalize", "da_finalize",
                   "da_det_attn", "da_det_attn_sharded", "da_accumulate_finalize", "dce_rowmax", "dce_denom_digits", "dce_finalize",
-                  "dce_backward", "dce_reduce"):
+                  "dce_backward", "dce_reduce", "dce_forward_static"):
             getattr(L, f).restype = C.c_int
         _lib = L
     return _lib
@@ -128,6 +129,30 @@ def _ptr(t):
     return None if t is None else C.c_void_p(t.data_ptr())
 
 
+def _sptr(status):
+    """Pointer of an optional device status word: a CUDA int32 tensor of at least one element."""
+    if status is None:
+        return None
+    _cuda(status, "status")
+    if status.dtype != torch.int32 or status.numel() < 1:
+        raise DetAttnError("status must be a CUDA int32 tensor (see new_status())")
+    return C.c_void_p(status.data_ptr())
+
+
+def _out(t, dtype, shape, device, name):
+    """A caller-supplied output (or in-place state): allocated when None, else checked for
+    device, dtype, element count and contiguity.  Never copied, since the kernels write it."""
+    n = 1
+    for x in shape:
+        n *= int(x)
+    if t is None:
+        return torch.empty(*shape, dtype=dtype, device=device)
+    _cuda(t, name)
+    if t.dtype != dtype or t.numel() != n or not t.is_contiguous() or t.device != torch.device(device):
+        raise DetAttnError(f"{name} must be a contiguous {dtype} tensor of {n} elements on {device}")
+    return t
+
+
 class _Problem:
     """Keeps the tensors alive while their descriptor is in use."""
 
@@ -138,7 +163,7 @@ class _Problem:
         self.desc.q, self.desc.k, self.desc.v = _tensor(Q, "Q"), _tensor(K, "K"), _tensor(V, "V")
         self.desc.causal = 1 if causal else 0
         self.desc.scale = math.nan if scale is None else float(scale)
-        self.desc.dev_status = None if status is None else status.data_ptr()
+        self.desc.dev_status = _sptr(status)
         self.B, self.Hq, self.Sq, self.D = Q.shape
         self.Skv = K.shape[2]
         self.device = Q.device
@@ -178,7 +203,7 @@ def _kv_workspace(P: _Problem, ws):
 def det_attn(Q, K, V, causal=False, scale=None, out=None, workspace=None, status=None):
     """Fused deterministic attention (det-attn "API": det_attn); f32 output [B, Hq, Sq, D]."""
     P = _Problem(Q, K, V, causal, scale, status)
-    out = torch.empty(P.B, P.Hq, P.Sq, P.D, dtype=torch.float32, device=P.device) if out is None else out
+    out = _out(out, torch.float32, (P.B, P.Hq, P.Sq, P.D), P.device, "out")
     ws = _workspace(P, 1, workspace)
     _check(lib().da_det_attn(P.ref(), _ptr(out), _ptr(ws), ws.numel(), _stream()), "det_attn")
     return out
@@ -192,7 +217,7 @@ def accumulate_finalize(Q, K, V, rowmax, causal=False, scale=None, out=None, wor
     _cuda(rowmax, "rowmax")
     if rowmax.dtype != torch.float32 or rowmax.numel() != P.B * P.Hq * P.Sq:
         raise DetAttnError("rowmax must be f32 [B, Hq, Sq]")
-    out = torch.empty(P.B, P.Hq, P.Sq, P.D, dtype=torch.float32, device=P.device) if out is None else out
+    out = _out(out, torch.float32, (P.B, P.Hq, P.Sq, P.D), P.device, "out")
     ws = _workspace(P, 1, workspace)
     _check(lib().da_accumulate_finalize(P.ref(), _ptr(rowmax.contiguous()), _ptr(out), _ptr(ws), ws.numel(),
                                         _stream()), "accumulate_finalize")
@@ -207,7 +232,7 @@ def det_attn_sharded(Q, K, V, kv_splits, causal=False, scale=None, order=None, o
     n = len(kv_splits)
     splits = (C.c_int64 * n)(*[int(x) for x in kv_splits])
     ordv = None if order is None else (C.c_int32 * n)(*[int(x) for x in order])
-    out = torch.empty(P.B, P.Hq, P.Sq, P.D, dtype=torch.float32, device=P.device) if out is None else out
+    out = _out(out, torch.float32, (P.B, P.Hq, P.Sq, P.D), P.device, "out")
     ws = _workspace(P, n, workspace)
     _check(lib().da_det_attn_sharded(P.ref(), splits, n, ordv, _ptr(out), _ptr(ws), ws.numel(), _stream()),
            "det_attn_sharded")
@@ -219,7 +244,7 @@ def rowmax(Q, K, kv_lo=0, kv_hi=None, causal=False, scale=None, out=None, status
     Shards combine with compose_max (or torch.maximum)."""
     P = _Problem(Q, K, K, causal, scale, status)
     kv_hi = P.Skv if kv_hi is None else kv_hi
-    m = torch.empty(P.B, P.Hq, P.Sq, dtype=torch.float32, device=P.device) if out is None else out
+    m = _out(out, torch.float32, (P.B, P.Hq, P.Sq), P.device, "out")
     ws = _kv_workspace(P, workspace)
     _check(lib().da_rowmax(P.ref(), kv_lo, kv_hi, _ptr(m), _ptr(ws), ws.numel(), _stream()), "rowmax")
     return m
@@ -231,10 +256,11 @@ def accumulate(Q, K, V, m, kv_lo=0, kv_hi=None, causal=False, scale=None, num=No
     accumulate).  Returns (num int64 [B,Hq,Sq,15,D], den int64 [B,Hq,Sq,6]), canonical."""
     P = _Problem(Q, K, V, causal, scale, status)
     kv_hi = P.Skv if kv_hi is None else kv_hi
-    if num is None:
-        num = torch.empty(P.B, P.Hq, P.Sq, NUM_NDIG, P.D, dtype=torch.int64, device=P.device)
-    if den is None:
-        den = torch.empty(P.B, P.Hq, P.Sq, DEN_NDIG, dtype=torch.int64, device=P.device)
+    num = _out(num, torch.int64, (P.B, P.Hq, P.Sq, NUM_NDIG, P.D), P.device, "num")
+    den = _out(den, torch.int64, (P.B, P.Hq, P.Sq, DEN_NDIG), P.device, "den")
+    _cuda(m, "rowmax")
+    if m.dtype != torch.float32 or m.numel() != P.B * P.Hq * P.Sq:
+        raise DetAttnError("rowmax must be f32 [B, Hq, Sq]")
     m = m.contiguous()
     ws = _kv_workspace(P, workspace)
     _check(lib().da_accumulate(P.ref(), _ptr(m), kv_lo, kv_hi, _ptr(num), _ptr(den), 1 if add_into else 0,
@@ -242,34 +268,59 @@ def accumulate(Q, K, V, m, kv_lo=0, kv_hi=None, causal=False, scale=None, num=No
     return num, den
 
 
+def _inplace_pair(dst, src, dtype, what):
+    """dst and src of one composition: CUDA tensors of `dtype` on one device, equal element
+    counts, both contiguous (dst is written in place, so it cannot be copied)."""
+    _cuda(dst, f"{what} dst")
+    _cuda(src, f"{what} src")
+    if dst.dtype != dtype or src.dtype != dtype:
+        raise DetAttnError(f"{what}: dst and src must both be {dtype}")
+    if dst.numel() != src.numel():
+        raise DetAttnError(f"{what}: dst has {dst.numel()} elements, src {src.numel()}")
+    if dst.device != src.device:
+        raise DetAttnError(f"{what}: dst and src are on different devices")
+    if not dst.is_contiguous() or not src.is_contiguous():
+        raise DetAttnError(f"{what}: dst and src must be contiguous")
+
+
 def compose_max(dst, src):
     """dst = max(dst, src) elementwise (shard rowmax composition), in place."""
+    _inplace_pair(dst, src, torch.float32, "compose_max")
     _check(lib().da_compose_max(_ptr(dst), _ptr(src), dst.numel(), _stream()), "compose_max")
     return dst
 
 
 def compose_add(dst, src):
     """dst += src elementwise (int64 digit composition), in place."""
+    _inplace_pair(dst, src, torch.int64, "compose_add")
     _check(lib().da_compose_add(_ptr(dst), _ptr(src), dst.numel(), _stream()), "compose_add")
     return dst
 
 
 def normalize(digits, status=None):
     """Canonical form, in place, of NUM [..., 15, D] or DEN [..., 6] digit arrays."""
+    _cuda(digits, "digits")
+    if digits.dtype != torch.int64 or not digits.is_contiguous() or digits.dim() < 1:
+        raise DetAttnError("digits must be a contiguous int64 tensor")
     if digits.shape[-1] == DEN_NDIG and (digits.dim() < 2 or digits.shape[-2] != NUM_NDIG):
         nrows, ndig, inner = digits.numel() // DEN_NDIG, DEN_NDIG, 1
     else:
         ndig, inner = digits.shape[-2], digits.shape[-1]
         nrows = digits.numel() // (ndig * inner)
-    _check(lib().da_normalize(_ptr(digits), nrows, ndig, inner, _ptr(status), _stream()), "normalize")
+    _check(lib().da_normalize(_ptr(digits), nrows, ndig, inner, _sptr(status), _stream()), "normalize")
     return digits
 
 
 def finalize(num, den, out=None, status=None):
     """Digits -> f32 output (det-attn "API": finalize): RN32(RN64(RN64(NUM)/RN64(DEN)))."""
+    _cuda(num, "num")
+    if num.dim() != 5 or num.shape[3] != NUM_NDIG:
+        raise DetAttnError("num must be int64 [B, Hq, Sq, 15, D]")
     B, H, S, _, D = num.shape
-    out = torch.empty(B, H, S, D, dtype=torch.float32, device=num.device) if out is None else out
-    _check(lib().da_finalize(_ptr(num), _ptr(den), B, H, S, D, _ptr(out), _ptr(status), _stream()), "finalize")
+    num = _out(num, torch.int64, tuple(num.shape), num.device, "num")
+    den = _out(den, torch.int64, (B, H, S, DEN_NDIG), num.device, "den")
+    out = _out(out, torch.float32, (B, H, S, D), num.device, "out")
+    _check(lib().da_finalize(_ptr(num), _ptr(den), B, H, S, D, _ptr(out), _sptr(status), _stream()), "finalize")
     return out
 
 
@@ -291,8 +342,8 @@ def dce_rowmax(logits, v_lo=0, v_hi=None, out=None, status=None):
     """Per-token max over the vocab range [v_lo, v_hi) (det-cross-entropy "API": rowmax)."""
     M, keep = _matrix(logits)
     v_hi = M.cols if v_hi is None else v_hi
-    m = torch.empty(M.rows, dtype=torch.float32, device=logits.device) if out is None else out
-    _check(lib().dce_rowmax(C.byref(M), v_lo, v_hi, _ptr(m), _ptr(status), _stream()), "dce_rowmax")
+    m = _out(out, torch.float32, (M.rows,), logits.device, "out")
+    _check(lib().dce_rowmax(C.byref(M), v_lo, v_hi, _ptr(m), _sptr(status), _stream()), "dce_rowmax")
     return m
 
 
@@ -310,8 +361,13 @@ def dce_denom_digits(logits, m, v_lo=0, v_hi=None, den=None, add_into=False, sta
     M, keep = _matrix(logits)
     m = _vec(m, torch.float32, M.rows, "rowmax")
     v_hi = M.cols if v_hi is None else v_hi
-    den = torch.empty(M.rows, DEN_NDIG, dtype=torch.int64, device=logits.device) if den is None else den
-    _check(lib().dce_denom_digits(C.byref(M), _ptr(m), v_lo, v_hi, _ptr(den), 1 if add_into else 0, _ptr(status),
+    if den is None:
+        den = torch.empty(M.rows, DEN_NDIG, dtype=torch.int64, device=logits.device)
+    else:   # written in place (and read with add_into): checked, never copied
+        _cuda(den, "den")
+        if den.dtype != torch.int64 or den.numel() != M.rows * DEN_NDIG or not den.is_contiguous():
+            raise DetAttnError(f"den must be a contiguous torch.int64 tensor of {M.rows * DEN_NDIG} elements")
+    _check(lib().dce_denom_digits(C.byref(M), _ptr(m), v_lo, v_hi, _ptr(den), 1 if add_into else 0, _sptr(status),
                                   _stream()), "dce_denom_digits")
     return den
 
@@ -324,7 +380,7 @@ def dce_finalize(den, logits, targets, m, status=None):
     targets = _vec(targets.to(torch.int64), torch.int64, M.rows, "targets")
     loss = torch.empty(M.rows, dtype=torch.float32, device=logits.device)
     denom = torch.empty(M.rows, dtype=torch.float64, device=logits.device)
-    _check(lib().dce_finalize(_ptr(den), C.byref(M), _ptr(targets), _ptr(m), _ptr(loss), _ptr(denom), _ptr(status),
+    _check(lib().dce_finalize(_ptr(den), C.byref(M), _ptr(targets), _ptr(m), _ptr(loss), _ptr(denom), _sptr(status),
                               _stream()), "dce_finalize")
     return loss, denom
 
@@ -372,7 +428,7 @@ def dce_backward(logits, targets, m, denom, grad, reduction="none", status=None)
     denom = _vec(denom, torch.float64, M.rows, "denom")
     out = torch.empty((M.rows, M.cols), dtype=logits.dtype, device=logits.device)
     _check(lib().dce_backward(C.byref(M), _ptr(targets), _ptr(m), _ptr(denom), _ptr(grad), red, _ptr(out),
-                              _ptr(status), _stream()), "dce_backward")
+                              _sptr(status), _stream()), "dce_backward")
     return out
 
 
@@ -429,15 +485,10 @@ def dce_forward_static(logits, targets, status=None):
     digits live in a fixed device array of STATIC_MAX_ROWS rows inside the library; only
     loss and denom are returned in new tensors here).  Equal bit for bit to dce_forward
     without splits.  Calls that overlap on the GPU race on the shared array."""
-    L = lib()
-    f = L.dce_forward_static
-    f.argtypes = [C.POINTER(_Matrix), _P, _P, _P, _P, _P]
-    f.restype = C.c_int
     M, keep = _matrix(logits)
-    den = _vec(den, torch.int64, M.rows * DEN_NDIG, "den")
-    m = _vec(m, torch.float32, M.rows, "rowmax")
     targets = _vec(targets.to(torch.int64), torch.int64, M.rows, "targets")
     loss = torch.empty(M.rows, dtype=torch.float32, device=logits.device)
     denom = torch.empty(M.rows, dtype=torch.float64, device=logits.device)
-    _check(f(C.byref(M), _ptr(targets), _ptr(loss), _ptr(denom), _ptr(status), _stream()), "dce_forward_static")
+    _check(lib().dce_forward_static(C.byref(M), _ptr(targets), _ptr(loss), _ptr(denom), _sptr(status), _stream()),
+           "dce_forward_static")
     return loss, denom

@@ -224,6 +224,9 @@ int dce_reduce(const float* loss, int64_t rows, int reduction, float* out, da_st
  *   - Every GPU that loads the library holds the array until the process exits.  The
  *     first call on a device looks up the array's device address (once per device, with
  *     that device current); make that first call before any stream capture.
+ *   - The looked-up address is kept for the life of the process: do not use the library
+ *     across a cudaDeviceReset (or anything else that destroys and recreates the device's
+ *     primary context), since the kept address would then be stale.
  *   - Every call shares the one array: calls whose work overlaps on the GPU (different
  *     streams, or several host threads) race on it.  Serialize them.  Each call overwrites
  *     every scratch entry it reads, so no clearing is needed between calls. */

@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
-def test_static_scratch_forward_matches_allocating_path_twice():
+def test_static_scratch_forward_matches_allocating_path_twice(oracle_native):
     import bitwise_deterministic_shard_gb300 as da
     g = torch.Generator().manual_seed(91)
     cases = [((torch.randn(300, 5000, generator=g) * 2).float(), 5000),
@@ -27,6 +27,9 @@ def test_static_scratch_forward_matches_allocating_path_twice():
         assert da.read_status(st) == 0
         assert torch.equal(loss, ref_loss)   # the contract fixes every rounding: zero tolerance
         assert torch.equal(denom, ref_denom)
+        o_loss, o_denom, _, _, _ = oracle_native.DCE(x).forward(t.cpu().numpy())
+        assert torch.equal(loss.cpu(), torch.from_numpy(o_loss))
+        assert torch.equal(denom.cpu(), torch.from_numpy(o_denom))
 
 
 @pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
