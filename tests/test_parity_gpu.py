@@ -5,7 +5,8 @@ the CUDA kernels share no code; both take their inputs from workloads/.  Every f
 point output is compared with torch.equal / bit patterns (the contract fixes every
 rounding, so the tolerance is zero); digits are compared exactly.  Sizes: small cases that
 span several tiles with ragged tails, every workload of the det-attn and det-cross-entropy
-pages at full size (sampled rows for the oracle where full rows would take minutes),
+pages at full size (every row of the long-context and cross-entropy workloads; sampled and
+out-of-window rows of the large non-causal one, whose full oracle run would take hours),
 and the edge cases (empty key ranges, one key, GQA, strided views, f32 and bf16).
 """
 import itertools
@@ -185,21 +186,40 @@ def test_gqa_causal_splits_and_oracle(da, orc):
         assert torch.equal(out, fused), (sp, order)
 
 
+def rows_outside_window(X):
+    """Indices of the rows of X ([rows, D] float32 values) that do not fit the 26-bit
+    fixed-point window of the tensor-core score path: some element is not a multiple of
+    2^(emax - 152), emax the row's largest biased exponent.  Such rows take the exact
+    low-limb or general dot, so the tests pick them out on purpose."""
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    e = (X.view(np.uint32) >> 23) & 0xFF
+    F = np.maximum(e.max(axis=1), 1).astype(np.int64) - 152
+    scaled = X.astype(np.float64) * np.exp2(-F.astype(np.float64))[:, None]
+    return np.nonzero((scaled != np.floor(scaled)).any(axis=1))[0]
+
+
 @cuda
-def test_long_context_ring_steps_and_sampled_oracle(da, orc):
+def test_long_context_ring_steps_and_full_oracle(da, orc):
+    """The metric workload at full size: every one of the 65,536 query rows against the
+    oracle (rowmax and output), so the rare exact paths (rows outside the fixed-point window,
+    rows whose maximum comes from a x8 key and their spill-slot products, several CTAs per
+    SM in turn) are checked under full-size contention; then ring steps 1 to 32 against the
+    fused result."""
     w = W.long_context_causal()
     Q, K, V = w.tensors("cuda")
     st = da.new_status()
+    m = da.rowmax(Q, K, causal=True, status=st)
     fused = da.det_attn(Q, K, V, causal=True, status=st)
     torch.cuda.synchronize()
     assert da.read_status(st) == 0
-    rng = random.Random(3)
-    rows = [(0, h, i) for h in range(w.Hq) for i in rng.sample(range(w.S), 8)] + [(0, 0, w.S - 1), (0, 15, 0)]
     A = orc.Attn(Q.cpu(), K.cpu(), V.cpu(), True)
-    fl = flat_rows(1, w.Hq, w.S, rows)
-    _, _, _, ref = A.forward_rows(rows=fl)
-    got = fused.reshape(-1, w.D)[torch.from_numpy(fl).cuda()]
-    assert_bits_equal(got, ref, "long-context sampled rows vs oracle")
+    m_o, _, _, ref = A.forward_rows()
+    assert_bits_equal(m.reshape(-1), m_o, "long-context rowmax vs oracle (all rows)")
+    assert_bits_equal(fused.reshape(-1, w.D), ref, "long-context output vs oracle (all rows)")
+    # the rare paths really occur in this workload
+    assert len(rows_outside_window(Q.float().cpu().reshape(-1, w.D).numpy())) > 0
+    Kb = K.float().cpu().reshape(w.Hkv, w.S, w.D).abs().amax(dim=2)
+    assert int((Kb > 8).sum()) > 0
     for sp, order in w.splits:
         out = da.det_attn_sharded(Q, K, V, sp, causal=True, order=order)
         assert torch.equal(out, fused), len(sp)
@@ -208,8 +228,9 @@ def test_long_context_ring_steps_and_sampled_oracle(da, orc):
 @cuda
 def test_large_noncausal_unequal_splits_and_sampled_oracle(da, orc):
     """Large non-causal workload at full size (B1 H56 S37810 D128 bf16; S is no tile
-    multiple): the fused call, the 32 unequal random splits composed in a random order,
-    and sampled rows (4 per head plus the last row) against the oracle."""
+    multiple): the fused call, the 32 unequal random splits composed in a random order, and
+    against the oracle sampled rows (4 per head, the last row) plus up to 64 query rows that
+    lie outside the fixed-point window (picked deterministically from the inputs)."""
     w = W.large_noncausal()
     Q, K, V = w.tensors("cuda")
     st = da.new_status()
@@ -226,10 +247,13 @@ def test_large_noncausal_unequal_splits_and_sampled_oracle(da, orc):
     rng = random.Random(4)
     rows = [(0, h, i) for h in range(w.Hq) for i in rng.sample(range(w.S), 4)] + [(0, w.Hq - 1, w.S - 1)]
     fl = flat_rows(1, w.Hq, w.S, rows)
+    wide = rows_outside_window(Q.float().cpu().reshape(-1, w.D).numpy())
+    assert len(wide) > 0
+    fl = np.unique(np.concatenate([fl, wide[np.linspace(0, len(wide) - 1, min(64, len(wide))).astype(np.int64)]]))
     A = orc.Attn(Q.cpu(), K.cpu(), V.cpu(), False)
     _, _, _, ref = A.forward_rows(rows=fl)
     got = fused.reshape(-1, w.D)[torch.from_numpy(fl).cuda()]
-    assert_bits_equal(got, ref, "large non-causal sampled rows vs oracle")
+    assert_bits_equal(got, ref, "large non-causal sampled and out-of-window rows vs oracle")
 
 
 @cuda
@@ -387,11 +411,12 @@ def test_vocab_sharded_splits_and_oracle(da, orc):
         got = da.dce_forward(x, t, splits=sp)
         for a, b in zip(base, got):
             assert torch.equal(a, b), len(sp)
-    rows = np.arange(0, w.N, 8, dtype=np.int64)
     D = orc.DCE(x.cpu())
-    rl, rd, rm, rden, st = D.forward(t.cpu().numpy(), rows=rows)
-    assert_bits_equal(base[0][torch.from_numpy(rows).cuda()], rl, "vocab-sharded loss")
-    assert torch.equal(base[1][torch.from_numpy(rows).cuda()].cpu(), torch.from_numpy(rd))
+    rl, rd, rm, rden, st = D.forward(t.cpu().numpy())                  # every token
+    assert_bits_equal(base[2], rm, "vocab-sharded rowmax")
+    assert torch.equal(base[3].cpu(), torch.from_numpy(rden)), "vocab-sharded denominator digits"
+    assert_bits_equal(base[0], rl, "vocab-sharded loss")
+    assert torch.equal(base[1].cpu(), torch.from_numpy(rd))
     ref = torch.nn.functional.cross_entropy(x.double(), t, reduction="none")
     assert float((base[0].double() - ref).abs().max()) < 2e-6
 
