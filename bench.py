@@ -39,10 +39,11 @@ METRIC = "exact attention MACs/s (S=4096,D=128,bf16) and % of binding INT/FP64 p
 UNIT = "MAC/s"
 
 
-# DRAM bytes (read + write) of one accumulate launch at the metric workload, from the ncu capture
-# summarised in profiles/accumulate_tp_long_context_causal_S4096_H4.md (the 4-head case scaled by 4: the
-# traffic is per head); set to None whenever the kernel changes until it is captured again
-ACC_TRAFFIC_PER_LAUNCH = 4 * 88.41e6
+# DRAM bytes (read + write) of one accumulate launch at the metric workload: dram__bytes_read.sum +
+# dram__bytes_write.sum of the 4-head case of the same kernel (`python bench.py --heads 4 --dce-rows 256
+# --steps 1 --warmup 1 --no-cpu-baseline` under ncu, -k regex:accumulate_tp -s 1 -c 1) scaled by 4 (the
+# traffic is per head).  None whenever the kernel has changed since that capture.
+ACC_TRAFFIC_PER_LAUNCH = None
 
 
 def _peaks():
@@ -122,15 +123,17 @@ def run_reference(args, rank, world):
     Q, K, V = w.tensors("cpu")
     cores = os.cpu_count() or 1
     rows_per_head = args.ref_rows_step
-    vals = []
+    vals, secs = [], []
     for s in range(args.warmup + args.steps):
         macs, dt, sample = oracle_sample(w, Q, K, V, rows_per_head, cores)
         if s >= args.warmup:
             vals.append(macs / dt)
+            secs.append(dt)
     v = statistics.median(vals)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup,
-            "ms_per_step": w.attn_macs / v * 1e3,   # one whole step of the workload at the sampled rate
+            "ms_per_step": statistics.median(secs) * 1e3,   # one timed step = one sample of the workload
+            "ms_per_full_workload_extrapolated": w.attn_macs / v * 1e3,
             "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": True,
@@ -249,11 +252,13 @@ def run_ours(args, rank, world, local_rank):
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        assert L.da_rowmax(P.ref(), 0, w.S, ptr(m), ptr(kvws), kvws.numel(), sp) == 0
+        # pass 1: keys and values prepared once, rowmax, every exact score kept in the workspace's cache
+        assert L.da_rowmax_cached(P.ref(), ptr(m), ptr(ws), ws.numel(), sp) == 0
         if ev:
             ev[1].record(stream)
-        # accumulate over all keys with the global rowmax, finalized in the tensor-PV kernel's epilogue
-        assert L.da_accumulate_finalize(P.ref(), ptr(m), ptr(out), ptr(ws), ws.numel(), sp) == 0
+        # pass 2: the exact sums from the cached scores with the global rowmax, finalized in the
+        # tensor-PV kernel's epilogue (the calls da_det_attn makes)
+        assert L.da_accumulate_finalize_cached(P.ref(), ptr(m), ptr(out), ptr(ws), ws.numel(), sp) == 0
         if ev:
             ev[2].record(stream)
 
@@ -302,6 +307,7 @@ def run_ours(args, rank, world, local_rank):
         flush.zero_()
         e2e_step()
     torch.cuda.synchronize()
+    macs_step = w.attn_macs
     e2e_ms = []
     for _ in range(args.steps):
         flush.zero_()
@@ -315,23 +321,73 @@ def run_ours(args, rank, world, local_rank):
     h2d = (Qh.numel() + Kh.numel() + Vh.numel()) * Qh.element_size()
     d2h = out.numel() * 4
 
+    # --- the sharded path on the same workload: ring steps 1..32 as equal kv_splits through
+    # da_det_attn_sharded (every shard's rowmax, compose_max, accumulate into one digit array, finalize)
+    sharded = {}
+    if not args.no_sharded:
+        for splits, order in w.splits:
+            n = len(splits)
+            wsn = torch.empty(L.da_workspace_bytes(P.ref(), n), dtype=torch.uint8, device=dev)
+            spv = (C.c_int64 * n)(*splits)
+            ordv = (C.c_int32 * n)(*order)
+            outs = torch.empty_like(out)
+
+            def sh_step():
+                assert L.da_det_attn_sharded(P.ref(), spv, n, ordv, ptr(outs), ptr(wsn), wsn.numel(), sp) == 0
+
+            flush.zero_()
+            sh_step()
+            ts = []
+            for _ in range(max(1, args.steps // 3)):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                sh_step()
+                b.record(stream)
+                b.synchronize()
+                ts.append(a.elapsed_time(b))
+            torch.cuda.synchronize()
+            assert torch.equal(outs, out), f"sharded ({n} splits) differs from the fused output"
+            t_med = statistics.median(ts)
+            sharded[str(n)] = {"ms": t_med, "macs_per_s": macs_step / (t_med * 1e-3), "bit_identical_to_fused": True}
+            del wsn
     if rank != 0:
         return
     dce = run_dce(args, dev, stream)
     macs = w.attn_macs
     value = macs * world / (ms * 1e-3)
     e2e_val = macs * world / (statistics.mean(e2e_ms) * 1e-3)
-    # roofline of the dominant kernel (accumulate): its MMAs on the tensor cores.  Per 128-key tile of
-    # 16 query rows it issues 32 score MMAs (M128 N64 K16), 24 PV MMAs (M128 N160 K16) and 8 DEN MMAs
-    # (M128 N16 K16): the integer digit decomposition of the exact products (16-bit operands).
+    # Roofline of the dominant kernel (accumulate + finalize), on the algorithmic basis: per unmasked
+    # (query, key) pair, D score multiply-adds and D PV multiply-adds (exact), 2 flop each, over the
+    # kernel's event time, against the measured dense bf16 tensor peak (the exact products run on the
+    # tensor cores as integer digit products).  Two further views of the same kernel:
+    #  - mma_util: the MMA work the kernel actually issues for its digit decomposition (per 128-key tile
+    #    of 16 query rows: 24 PV MMAs M128 N160 K16 and 8 DEN MMAs M128 N16 K16, plus 32 score MMAs
+    #    M128 N64 K16 when the scores are recomputed instead of read from pass 1's cache) against the
+    #    same peak;
+    #  - int_pipe: the exact multiply-adds per second against the integer pipe's rate of exact
+    #    32 x 32 -> 64-bit multiply-adds, measured by the library's probe kernel in this run (the metric's
+    #    "% of binding INT pipe peak"; FP64 is not used on the path).
     pk = _peaks()
     sm_clock = (ck or {}).get("sm_mhz") or pk.get("clocks_under_load", {}).get("sm_mhz_median") or 1447.0
     acc_ms = statistics.mean(k_acc)
-    tile_macs = 32 * 128 * 64 * 16 + 24 * 128 * 160 * 16 + 8 * 128 * 16 * 16
+    alg_macs = w.pairs * 2 * w.D                                         # per launch
+    achieved = 2.0 * alg_macs / (acc_ms * 1e-3) / 1e12                   # TFLOP/s
+    cached = L.da_score_cache_bytes(P.ref()) > 0
+    tile_macs = (0 if cached else 32 * 128 * 64 * 16) + 24 * 128 * 160 * 16 + 8 * 128 * 16 * 16
     tiles = w.B * w.Hq * sum(-(-min(w.S, 16 * (qi + 1)) // 128) for qi in range(-(-w.S // 16)))
-    achieved = 2.0 * tile_macs * tiles / (acc_ms * 1e-3) / 1e12       # TFLOP/s
+    mma_tflops = 2.0 * tile_macs * tiles / (acc_ms * 1e-3) / 1e12
     peak = pk.get("bf16_tflops") or 1900.0
     peak_src = "measured burst bf16 (MEASURED_PEAKS.json)" if pk.get("bf16_tflops") else "fallback 1.9 PFLOP/s bf16"
+    int_rate = da.probe_int_mac_rate()
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    int_pipe = {"achieved_exact_macs_per_s": alg_macs / (acc_ms * 1e-3),
+                "method_exact_macs_per_s": w.pairs * 3 * w.D / (acc_ms * 1e-3),
+                "peak_exact_macs_per_s": int_rate,
+                "peak_per_clock_per_sm": int_rate / (n_sm * sm_clock * 1e6),
+                "frac": alg_macs / (acc_ms * 1e-3) / int_rate,
+                "peak_basis": "mad.wide.s32 (exact 32 x 32 -> 64-bit multiply-add) issue rate over all SMs, "
+                              "measured by da_probe_int_mac in this run"}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
@@ -342,16 +398,21 @@ def run_ours(args, rank, world, local_rank):
                    "attn_macs_per_step": macs, "pairs_per_step": w.pairs},
         "method_macs_per_s": w.pairs * 3 * w.D * world / (ms * 1e-3),
         "kernels_ms": {"rowmax": statistics.mean(k_rowmax), "accumulate_finalize": acc_ms},
+        "score_cache_bytes": int(L.da_score_cache_bytes(P.ref())),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": ACC_TRAFFIC_PER_LAUNCH if args.heads == 16 else None,
                      "kernel": "accumulate",
-                     "peak_basis": f"{peak_src}; f16 operands run at the bf16 rate; "
-                                   f"{tiles} key tiles x {tile_macs} MACs per launch",
-                     "sm_mhz": sm_clock},
+                     "algorithmic": f"{w.pairs} unmasked pairs x 2D exact multiply-adds x 2 flop per launch",
+                     "peak_basis": peak_src, "sm_mhz": sm_clock,
+                     "mma_util": {"achieved": mma_tflops, "frac": mma_tflops / peak,
+                                  "basis": f"{tiles} key tiles x {tile_macs} bf16/f16 MACs per launch "
+                                           "(the digit decomposition the kernel issues)"},
+                     "int_pipe": int_pipe},
+        "sharded": sharded,
         "clocks": ck,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": statistics.mean(e2e_ms)},
-        "gpu_launches": 5 * args.steps,   # per step: key prep, rowmax, V columns, key+V prep, accumulate
+        "gpu_launches": 4 * args.steps,   # per step: V columns, key + V prep, rowmax (storing scores), accumulate
         "dce": dce,
         "wall_s_timed_region": wall,
     }
@@ -360,6 +421,111 @@ def run_ours(args, rank, world, local_rank):
         line["cpu_baseline"] = {"value": macs_c / dt_c, "unit": UNIT, "cores": os.cpu_count() or 1, "kind": "oracle",
                                 "sample": sample, "seconds": dt_c}
     print(json.dumps(line), flush=True)
+
+
+def _sha(*ts) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for t in ts:
+        t = t.detach().cpu().contiguous()
+        h.update((t.view(torch.int16) if t.dtype == torch.bfloat16 else t).numpy().tobytes())
+    return h.hexdigest()
+
+
+def _time_ms(fn, stream, flush, reps):
+    fn()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def run_configs(args):
+    """One JSON line per workload of the pages: fused and sharded device times (CUDA events, L2
+    flushed between calls), exact attention MACs/s, the oracle's host time and core count, SHA-256
+    of the inputs and the output, and parity against the oracle (every row where the oracle
+    finishes in seconds; sampled rows on the large non-causal workload)."""
+    import bitwise_deterministic_shard_gb300 as da
+    from oracle import native
+    native.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    cores = native.default_threads()
+    for w in (W.tiny_exact(), W.gqa_causal(), W.long_context_causal(), W.large_noncausal()):
+        Qh, Kh, Vh = w.tensors("cpu")
+        Q, K, V = Qh.to(dev), Kh.to(dev), Vh.to(dev)
+        ws = torch.empty(da.workspace_bytes(Q, K, V, w.causal, w.scale, max(len(s) for s, _ in w.splits)),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty(w.B, w.Hq, w.S, w.D, dtype=torch.float32, device=dev)
+        reps = 2 if w.S > 10000 else 5
+        fused_ms = _time_ms(lambda: da.det_attn(Q, K, V, w.causal, w.scale, out=out, workspace=ws), stream, flush,
+                            reps)
+        fused = out.clone()
+        sh = {}
+        outs = torch.empty_like(out)
+        for sp, order in w.splits:
+            key = f"{len(sp)} splits"
+            t = _time_ms(lambda: da.det_attn_sharded(Q, K, V, sp, w.causal, w.scale, order=order, out=outs,
+                                                     workspace=ws), stream, flush, 1 if w.S > 10000 else 2)
+            assert torch.equal(outs, fused), (w.name, len(sp), order)
+            sh.setdefault(key, []).append(t)
+        sharded = {k: {"compositions": len(v), "median_ms": statistics.median(v),
+                       "macs_per_s": w.attn_macs / (statistics.median(v) * 1e-3), "bit_identical_to_fused": True}
+                   for k, v in sh.items()}
+        A = native.Attn(Qh, Kh, Vh, w.causal, w.scale)
+        if w.S > 10000:   # 64 rows per head (spread over the sequence) plus the last 50 rows of head 0
+            rows = sorted({h * w.S + int(i) for h in range(w.Hq) for i in np.linspace(0, w.S - 1, 64)} |
+                          {w.S - 1 - i for i in range(50)})
+            rows = np.asarray(rows, dtype=np.int64)
+        else:
+            rows = native.all_rows(w.B, w.Hq, w.S)
+        keys = (rows % w.S) + 1 if w.causal else np.full(len(rows), w.S)
+        t0 = time.perf_counter()
+        _, _, _, ref = A.forward_rows(rows=rows)
+        dt = time.perf_counter() - t0
+        got = fused.reshape(-1, w.D)[torch.from_numpy(rows).to(dev)].cpu().numpy()
+        equal = bool(np.array_equal(got.view(np.uint32), ref.view(np.uint32)))
+        o_macs = int(keys.sum()) * 2 * w.D
+        line = {"config": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": w.causal,
+                "dtype": str(w.dtype).replace("torch.", ""), "pairs": w.pairs, "attn_macs": w.attn_macs,
+                "fused_ms": fused_ms, "fused_macs_per_s": w.attn_macs / (fused_ms * 1e-3), "sharded": sharded,
+                "oracle": {"seconds": dt, "cores": cores, "rows": "all" if len(rows) == w.B * w.Hq * w.S
+                           else f"{len(rows)} sampled rows", "macs_per_s": o_macs / dt,
+                           "full_workload_seconds_extrapolated": w.attn_macs / (o_macs / dt)},
+                "sha256": {"inputs": _sha(Qh, Kh, Vh), "output": _sha(fused)},
+                "parity": ("bit-exact vs oracle" if equal else "MISMATCH") +
+                          (" (every row)" if len(rows) == w.B * w.Hq * w.S else f" ({len(rows)} rows)")}
+        print(json.dumps(line), flush=True)
+        del Q, K, V, ws, out, outs, fused
+        torch.cuda.empty_cache()
+    # vocab-sharded cross-entropy
+    w = W.vocab_sharded_ce()
+    xh, th = w.tensors("cpu")
+    x, t = xh.to(dev), th.to(dev)
+    base = da.dce_forward(x, t)
+    times = {}
+    for sp in w.splits:
+        times[f"{len(sp)} splits"] = _time_ms(lambda: da.dce_forward(x, t, splits=sp), stream, flush, 5)
+        got = da.dce_forward(x, t, splits=sp)
+        assert all(torch.equal(a_, b_) for a_, b_ in zip(base, got))
+    t0 = time.perf_counter()
+    rl, rd, rm, rden, _ = native.DCE(xh).forward(th.numpy())
+    dt = time.perf_counter() - t0
+    equal = bool(np.array_equal(base[0].cpu().numpy().view(np.uint32), rl.view(np.uint32)) and
+                 np.array_equal(base[1].cpu().numpy(), rd))
+    print(json.dumps({"config": w.name, "N": w.N, "V": w.V, "dtype": "float32",
+                      "forward_ms_by_splits": times, "tokens_per_s": {k: w.N / (v * 1e-3) for k, v in times.items()},
+                      "all_splits_bit_identical": True,
+                      "oracle": {"seconds": dt, "cores": cores, "rows": "all", "tokens_per_s": w.N / dt},
+                      "sha256": {"inputs": _sha(xh, th), "loss": _sha(base[0]), "denom": _sha(base[1])},
+                      "parity": "bit-exact vs oracle (every token)" if equal else "MISMATCH"}), flush=True)
 
 
 def main():
@@ -373,6 +539,9 @@ def main():
     ap.add_argument("--ref-rows-step", type=int, default=1024,
                     help="--impl reference: query rows per head in each timed step (a few seconds each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sharded", action="store_true", help="skip the sharded ring-step timings")
+    ap.add_argument("--configs", action="store_true",
+                    help="per-workload table (fused / sharded times, oracle, SHA-256, parity) instead of the step")
     ap.add_argument("--heads", type=int, default=16, help="heads of the workload (16 = the metric workload)")
     ap.add_argument("--dce-rows", type=int, default=4096,
                     help="tokens of the cross-entropy leg (4096 = the vocab-sharded workload)")
@@ -384,6 +553,9 @@ def main():
         torch.distributed.init_process_group("nccl")
     elif world > 1:
         torch.distributed.init_process_group("gloo")
+    if args.configs:
+        run_configs(args)
+        return
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)

@@ -72,6 +72,10 @@ def lib():
         L.da_workspace_bytes.argtypes = [D, _I32]
         L.da_workspace_bytes.restype = C.c_size_t
         L.da_det_attn.argtypes = [D, _P, _P, C.c_size_t, _P]
+        L.da_score_cache_bytes.argtypes = [D]
+        L.da_score_cache_bytes.restype = C.c_size_t
+        L.da_rowmax_cached.argtypes = [D, _P, _P, C.c_size_t, _P]
+        L.da_accumulate_finalize_cached.argtypes = [D, _P, _P, _P, C.c_size_t, _P]
         L.da_accumulate_finalize.argtypes = [D, _P, _P, _P, C.c_size_t, _P]
         L.da_det_attn_sharded.argtypes = [D, _P, _I32, _P, _P, _P, C.c_size_t, _P]
         L.dce_rowmax.argtypes = [M, _I64, _I64, _P, _P, _P]
@@ -80,9 +84,15 @@ def lib():
         L.dce_backward.argtypes = [M, _P, _P, _P, _P, _I32, _P, _P, _P]
         L.dce_reduce.argtypes = [_P, _I64, _I32, _P, _P]
         L.dce_forward_static.argtypes = [M, _P, _P, _P, _P, _P]
+        L.dce_finalize_shard.argtypes = [_P, M, _I64, _I64, _P, _P, _P, _P, _P, _P]
+        L.dce_backward_shard.argtypes = [M, _I64, _P, _P, _P, _P, _I32, _P, _P, _P]
+        L.da_probe_int_mac.argtypes = [_I64, _I32, _P, _P]
+        L.da_probe_int_mac_per_thread_iter.restype = C.c_int64
+        L.da_probe_bounded_wait.argtypes = [_P, _P]
         for f in ("da_rowmax", "da_accumulate", "da_compose_max", "da_compose_add", "da_normalize", "da_finalize",
                   "da_det_attn", "da_det_attn_sharded", "da_accumulate_finalize", "dce_rowmax", "dce_denom_digits", "dce_finalize",
-                  "dce_backward", "dce_reduce", "dce_forward_static"):
+                  "dce_backward", "dce_reduce", "dce_forward_static", "da_probe_int_mac", "da_probe_bounded_wait",
+                  "dce_finalize_shard", "dce_backward_shard", "da_rowmax_cached", "da_accumulate_finalize_cached"):
             getattr(L, f).restype = C.c_int
         _lib = L
     return _lib
@@ -209,6 +219,12 @@ def det_attn(Q, K, V, causal=False, scale=None, out=None, workspace=None, status
     return out
 
 
+def score_cache_bytes(Q, K, V, causal=False, scale=None) -> int:
+    """Bytes of the score cache det_attn keeps in its workspace (0 when it recomputes scores)."""
+    P = _Problem(Q, K, V, causal, scale)
+    return int(lib().da_score_cache_bytes(P.ref()))
+
+
 def accumulate_finalize(Q, K, V, rowmax, causal=False, scale=None, out=None, workspace=None, status=None):
     """Pass 2 and finalize over all keys with the global rowmax: the f32 output [B, Hq, Sq, D],
     equal bit for bit to finalize(*accumulate(Q, K, V, rowmax, 0, Skv)); the tensor-PV kernel
@@ -237,6 +253,63 @@ def det_attn_sharded(Q, K, V, kv_splits, causal=False, scale=None, order=None, o
     _check(lib().da_det_attn_sharded(P.ref(), splits, n, ordv, _ptr(out), _ptr(ws), ws.numel(), _stream()),
            "det_attn_sharded")
     return out
+
+
+def _all_reduce(t, op, group):
+    """In-place all-reduce over the process group: on the device with NCCL, through a host copy
+    with a CPU backend (gloo).  MAX of f32 and SUM of int64 are exact, so the result does not
+    depend on the reduction order."""
+    import torch.distributed as dist
+    if dist.get_backend(group) == "nccl":
+        dist.all_reduce(t, op=op, group=group)
+        return t
+    h = t.cpu()
+    dist.all_reduce(h, op=op, group=group)
+    t.copy_(h)
+    return t
+
+
+def det_attn_cp(Q, K, V, kv_lo, S_kv=None, causal=False, scale=None, group=None, status=None):
+    """Context-parallel det-attn (det-attn, introduction and "Method": the output is the same
+    whether the sequence lives on one device or is split over many).  This rank holds every
+    query row Q [B, Hq, Sq, D] and the keys and values [kv_lo, kv_lo + K.shape[2]) of a
+    sequence of S_kv keys (S_kv = Sq when causal).  The rank runs pass 1 over its keys, the
+    group takes the max all-reduce of the f32 rowmax; the rank runs pass 2 with that global
+    rowmax, the group sums the canonical int64 NUM / DEN digits (exact, any order); every
+    rank then normalizes and finalizes on its GPU.  The f32 output [B, Hq, Sq, D] equals
+    det_attn over the whole sequence bit for bit, for any split of the keys over the ranks.
+
+    The shard is presented to the kernels at its global key positions (causal masking uses
+    them); the kernels read key / value rows of their range only.  Collectives: NCCL on device
+    tensors, or any CPU backend through host copies."""
+    import torch.distributed as dist
+    P = _Problem(Q, K, V, causal, scale, status)
+    S_kv = P.Sq if S_kv is None else int(S_kv)
+    n_local = P.keep[1].shape[2]
+    kv_lo = int(kv_lo)
+    kv_hi = kv_lo + n_local
+    if P.keep[2].shape[2] != n_local or kv_lo < 0 or kv_hi > S_kv:
+        raise DetAttnError("the key / value shard must lie inside [0, S_kv) and K, V must hold the same rows")
+    for t, x in ((P.desc.k, P.keep[1]), (P.desc.v, P.keep[2])):
+        if n_local > 0:
+            t.ptr = x.data_ptr() - kv_lo * x.stride(2) * x.element_size()   # row kv_lo at the shard's first row
+        else:   # an empty shard holds no storage; the kernels read no key row of an empty range
+            t.ptr = P.keep[0].data_ptr()
+        t.S = S_kv
+    L = lib()
+    kvws = torch.empty(max(int(L.da_kv_workspace_bytes(P.ref())), 1), dtype=torch.uint8, device=P.device)
+    m = torch.empty(P.B, P.Hq, P.Sq, dtype=torch.float32, device=P.device)
+    _check(L.da_rowmax(P.ref(), kv_lo, kv_hi, _ptr(m), _ptr(kvws), kvws.numel(), _stream()), "rowmax")
+    _all_reduce(m, dist.ReduceOp.MAX, group)
+    num = torch.empty(P.B, P.Hq, P.Sq, NUM_NDIG, P.D, dtype=torch.int64, device=P.device)
+    den = torch.empty(P.B, P.Hq, P.Sq, DEN_NDIG, dtype=torch.int64, device=P.device)
+    _check(L.da_accumulate(P.ref(), _ptr(m), kv_lo, kv_hi, _ptr(num), _ptr(den), 0, _ptr(kvws), kvws.numel(),
+                           _stream()), "accumulate")
+    _all_reduce(num, dist.ReduceOp.SUM, group)
+    _all_reduce(den, dist.ReduceOp.SUM, group)
+    normalize(num, status, ndig=NUM_NDIG)
+    normalize(den, status, ndig=DEN_NDIG)
+    return finalize(num, den, status=status)
 
 
 def rowmax(Q, K, kv_lo=0, kv_hi=None, causal=False, scale=None, out=None, status=None, workspace=None):
@@ -297,16 +370,31 @@ def compose_add(dst, src):
     return dst
 
 
-def normalize(digits, status=None):
-    """Canonical form, in place, of NUM [..., 15, D] or DEN [..., 6] digit arrays."""
+def normalize(digits, status=None, ndig=None):
+    """Canonical form, in place, of NUM [..., 15, D] or DEN [..., 6] digit arrays.  ndig (15 or
+    6) names the kind; without it a 5-dimensional array is NUM [B, Hq, Sq, 15, D] and a 4- or
+    2-dimensional one DEN [B, Hq, Sq, 6] / [N, 6]."""
     _cuda(digits, "digits")
     if digits.dtype != torch.int64 or not digits.is_contiguous() or digits.dim() < 1:
         raise DetAttnError("digits must be a contiguous int64 tensor")
-    if digits.shape[-1] == DEN_NDIG and (digits.dim() < 2 or digits.shape[-2] != NUM_NDIG):
-        nrows, ndig, inner = digits.numel() // DEN_NDIG, DEN_NDIG, 1
+    if ndig is None:
+        if digits.dim() == 5:
+            ndig = NUM_NDIG
+        elif digits.dim() in (2, 4):
+            ndig = DEN_NDIG
+        else:
+            raise DetAttnError("pass ndig=15 (NUM) or ndig=6 (DEN) for this shape")
+    if ndig == NUM_NDIG:
+        if digits.dim() < 2 or digits.shape[-2] != NUM_NDIG:
+            raise DetAttnError("NUM digits must be laid out [..., 15, D]")
+        inner = digits.shape[-1]
+    elif ndig == DEN_NDIG:
+        if digits.shape[-1] != DEN_NDIG:
+            raise DetAttnError("DEN digits must be laid out [..., 6]")
+        inner = 1
     else:
-        ndig, inner = digits.shape[-2], digits.shape[-1]
-        nrows = digits.numel() // (ndig * inner)
+        raise DetAttnError("ndig must be 15 (NUM) or 6 (DEN)")
+    nrows = digits.numel() // (ndig * inner)
     _check(lib().da_normalize(_ptr(digits), nrows, ndig, inner, _sptr(status), _stream()), "normalize")
     return digits
 
@@ -476,6 +564,75 @@ def cross_entropy(logits, targets, reduction="mean", splits=None, status=None):
     return _CrossEntropy.apply(logits, targets, reduction, splits, status)
 
 
+def dce_forward_vp(logits, targets, v_base, v_total, group=None, status=None):
+    """Vocabulary-parallel cross-entropy forward (det-cross-entropy, "Usage": the vocabulary
+    sharded over ranks composes by max and digit add).  This rank holds logits [N, cols], the
+    columns [v_base, v_base + cols) of a vocabulary of v_total; targets [N] are global column
+    indices.  The group takes a max all-reduce of the rowmax and an int64 sum all-reduce of
+    the denominator digits; each rank finalizes the rows whose target it holds (the others
+    add +0) and a sum all-reduce of the f32 losses (one nonzero term per row) completes the
+    loss.  Returns (loss [N], rowmax [N], denom [N]), equal bit for bit on every rank to the
+    single-device forward over the whole vocabulary."""
+    import torch.distributed as dist
+    M, keep = _matrix(logits)
+    targets = _vec(targets.to(torch.int64), torch.int64, M.rows, "targets")
+    m = dce_rowmax(logits, status=status)
+    _all_reduce(m, dist.ReduceOp.MAX, group)
+    den = dce_denom_digits(logits, m, status=status)
+    _all_reduce(den, dist.ReduceOp.SUM, group)
+    normalize(den, status, ndig=DEN_NDIG)
+    loss = torch.empty(M.rows, dtype=torch.float32, device=logits.device)
+    denom = torch.empty(M.rows, dtype=torch.float64, device=logits.device)
+    _check(lib().dce_finalize_shard(_ptr(den), C.byref(M), int(v_base), int(v_total), _ptr(targets), _ptr(m),
+                                    _ptr(loss), _ptr(denom), _sptr(status), _stream()), "dce_finalize_shard")
+    _all_reduce(loss, dist.ReduceOp.SUM, group)
+    return loss, m, denom
+
+
+def dce_backward_vp(logits, targets, v_base, m, denom, grad, reduction="none", status=None):
+    """dLogits of this rank's vocabulary columns from the composed forward state (m, denom):
+    the same bytes as the matching columns of dce_backward over the whole vocabulary."""
+    M, keep = _matrix(logits)
+    if reduction not in _REDUCTIONS:
+        raise DetAttnError("reduction must be 'none', 'sum' or 'mean'")
+    red = _REDUCTIONS[reduction]
+    grad = grad.to(torch.float32).reshape(-1).contiguous()
+    if grad.numel() != (M.rows if red == 0 else 1):
+        raise DetAttnError("grad must have one entry per row for reduction='none', else one entry")
+    targets = _vec(targets.to(torch.int64), torch.int64, M.rows, "targets")
+    m = _vec(m, torch.float32, M.rows, "rowmax")
+    denom = _vec(denom, torch.float64, M.rows, "denom")
+    out = torch.empty((M.rows, M.cols), dtype=logits.dtype, device=logits.device)
+    _check(lib().dce_backward_shard(C.byref(M), int(v_base), _ptr(targets), _ptr(m), _ptr(denom), _ptr(grad), red,
+                                    _ptr(out), _sptr(status), _stream()), "dce_backward_shard")
+    return out
+
+
+class _CrossEntropyVP(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, logits, targets, v_base, v_total, reduction, group, status):
+        loss, m, denom = dce_forward_vp(logits, targets, v_base, v_total, group=group, status=status)
+        ctx.save_for_backward(logits, targets, m, denom)
+        ctx.v_base, ctx.reduction, ctx.status = v_base, reduction, status
+        return loss if reduction == "none" else dce_reduce(loss, reduction)
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        logits, targets, m, denom = ctx.saved_tensors
+        g = dce_backward_vp(logits, targets, ctx.v_base, m, denom, grad_out.detach(), ctx.reduction,
+                            status=ctx.status)
+        return g, None, None, None, None, None, None
+
+
+def cross_entropy_vp(logits, targets, v_base, v_total, reduction="mean", group=None, status=None):
+    """Vocabulary-parallel cross_entropy with autograd: the loss is the same bytes on every rank
+    as cross_entropy over the whole vocabulary, and each rank's dLogits are the same bytes as
+    that call's columns [v_base, v_base + cols)."""
+    if reduction not in _REDUCTIONS:
+        raise DetAttnError("reduction must be 'none', 'sum' or 'mean'")
+    return _CrossEntropyVP.apply(logits, targets, v_base, v_total, reduction, group, status)
+
+
 STATIC_MAX_ROWS = 65536
 
 
@@ -492,3 +649,31 @@ def dce_forward_static(logits, targets, status=None):
     _check(lib().dce_forward_static(C.byref(M), _ptr(targets), _ptr(loss), _ptr(denom), _sptr(status), _stream()),
            "dce_forward_static")
     return loss, denom
+
+
+def probe_bounded_wait(status=None):
+    """Run the bounded-wait probe (a wait nothing ends; it gives up after about 2 s and
+    reports STATUS_TIMEOUT); returns the status word after synchronizing."""
+    st = new_status() if status is None else status
+    _check(lib().da_probe_bounded_wait(_sptr(st), _stream()), "probe_bounded_wait")
+    torch.cuda.current_stream().synchronize()
+    return read_status(st)
+
+
+def probe_int_mac_rate(iters=4096, nblocks=None):
+    """Exact 32 x 32 -> 64-bit multiply-adds per second over the whole GPU (the integer
+    pipe's rate for exact products), timed with CUDA events on the current stream."""
+    dev = torch.cuda.current_device()
+    if nblocks is None:
+        nblocks = 4 * torch.cuda.get_device_properties(dev).multi_processor_count
+    sink = torch.zeros(1, dtype=torch.int64, device="cuda")
+    L = lib()
+    _check(L.da_probe_int_mac(16, nblocks, _ptr(sink), _stream()), "probe_int_mac")   # warm-up
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s = torch.cuda.current_stream()
+    a.record(s)
+    _check(L.da_probe_int_mac(iters, nblocks, _ptr(sink), _stream()), "probe_int_mac")
+    b.record(s)
+    b.synchronize()
+    macs = iters * nblocks * 512 * int(L.da_probe_int_mac_per_thread_iter())
+    return macs / (a.elapsed_time(b) * 1e-3)

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdetattn.so")
-SOURCES = ["attn_kernels.cu", "accumulate_tc.cu", "accumulate_tp.cu", "prep_kernels.cu", "digit_kernels.cu", "dce_kernels.cu", "api.cu", "static_scratch.cu"]
+SOURCES = ["attn_kernels.cu", "accumulate_tc.cu", "accumulate_tp.cu", "prep_kernels.cu", "digit_kernels.cu", "dce_kernels.cu", "api.cu", "static_scratch.cu", "probe_kernels.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-ftz=false", "-prec-div=true", "-prec-sqrt=true",
          "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]

@@ -67,8 +67,10 @@
 
 namespace detattn {
 
-struct AccTpLayout {
-  static constexpr int DP = 128, BM = 16, NDS = DP / 16, NSK = 4, NVB = 4, NCW = 16;
+// SC: the score-cache variant holds no query operand and no key ring; the V ring takes that room.
+template <bool SC>
+struct AccTpLayoutT {
+  static constexpr int DP = 128, BM = 16, NDS = DP / 16, NSK = 4, NVB = SC ? 10 : 4, NCW = 16;
   // warps: NCW compute (four warpgroups) and the control warpgroup: copies (lane 0 key steps,
   // lane 1 V blocks), score MMAs of even steps, PV and DEN MMAs, score MMAs of odd steps
   static constexpr int LOADW = NCW, ISSW = NCW + 1, PISSW = NCW + 2, ISSW2 = NCW + 3, THREADS = 32 * (NCW + 4);
@@ -79,9 +81,9 @@ struct AccTpLayout {
   // TMEM columns: two PV buffers (diagonal P_c at 16 c), the score diagonals at 16 c, DEN
   static constexpr int PV_COL = 0, PV_BUF = NPD * BM, SC_COL = 2 * PV_BUF, DEN_COL = SC_COL + NDIAG * BM, TCOLS = 512;
   static constexpr size_t q_step = (size_t)NQ * 32;                    // one B block: 64 rows (16 sb + r) x 16 bf16
-  static constexpr size_t q_bytes = (size_t)NDS * q_step;
+  static constexpr size_t q_bytes = SC ? 0 : (size_t)NDS * q_step;
   static constexpr size_t k_off = q_bytes;                             // NSK key operand steps
-  static constexpr size_t v_off = k_off + (size_t)NSK * KT_BLOCK;      // NVB V digit blocks
+  static constexpr size_t v_off = k_off + (SC ? 0 : (size_t)NSK * KT_BLOCK);   // NVB V digit blocks
   static constexpr size_t w_blk = (size_t)BM * VKEYS * 2;              // one weight digit plane: 16 rows x 16 keys
   static constexpr size_t w_buf = (size_t)NKB * NWP * w_blk;           // one tile's weight digit planes [kb][s]
   static constexpr size_t w_off = v_off + (size_t)NVB * VP_BLOCK;      // two buffers
@@ -92,6 +94,7 @@ struct AccTpLayout {
   static_assert(NW16 <= 256 && NW16 % 16 == 0, "one PV MMA covers every weight digit");
   static_assert(bytes <= 213 * 1024, "shared memory budget (plus about 8 KB static)");
 };
+using AccTpLayout = AccTpLayoutT<false>;
 
 // one 16-key block: V digit t (A) times the ten stacked weight digits (B) into P_{s+t} of
 // the PV buffer at TMEM address pv; weight digits 0-7 (A, MN-major) times ones (B) into DEN
@@ -152,6 +155,8 @@ __device__ __forceinline__ void carry_digits(long long (&dg)[N]) {
 // Fold one tile's PV accumulators (12 diagonals x this thread's 4 rows, TMEM address pvb) into
 // the integer digits acc[r][g] (g: diagonals 4 g .. 4 g + 3), zero them and release the buffer.
 // A function rather than a lambda so that it is always inlined and acc stays in registers.
+// ONE_WAIT: all twelve diagonal loads in flight before one wait (more registers live).
+template <bool ONE_WAIT>
 __device__ __forceinline__ void drain_pv(long long (&acc)[4][3], uint32_t pvb, uint64_t* done, uint64_t* freeb,
                                          uint32_t parity, volatile int* abort, int lane) {
   using L = AccTpLayout;
@@ -160,18 +165,34 @@ __device__ __forceinline__ void drain_pv(long long (&acc)[4][3], uint32_t pvb, u
   ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
   tc5::fence_after();
   if (ok) {
-#pragma unroll
-    for (int g3 = 0; g3 < 3; g3++) {
-      float pv[4][4];
-#pragma unroll
-      for (int c = 0; c < 4; c++) tc5::ld_x4(pvb + (4 * g3 + c) * L::BM, pv[c]);
-      tc5::ld_wait();
+    // sum_c P_c 2^(8c) over a group of four diagonals: |P_c| < 2^24 integers, converted exactly,
+    // combined by exact 32 x 32 -> 64 multiply-adds
+    auto fold = [&](const float (&pv)[4][4], int g3) {
 #pragma unroll
       for (int r = 0; r < 4; r++) {
-        long long s = 0;
+        long long s = (long long)__float2int_rn(pv[0][r]);
 #pragma unroll
-        for (int c = 0; c < 4; c++) s += (long long)__float2int_rn(pv[c][r]) * (1ll << (8 * c));   // |P_c| < 2^24
+        for (int c = 1; c < 4; c++) mad_wide(s, __float2int_rn(pv[c][r]), 1 << (8 * c));
         acc[r][g3] += s;
+      }
+    };
+    if constexpr (ONE_WAIT) {
+      float pv[3][4][4];
+#pragma unroll
+      for (int g3 = 0; g3 < 3; g3++)
+#pragma unroll
+        for (int c = 0; c < 4; c++) tc5::ld_x4(pvb + (4 * g3 + c) * L::BM, pv[g3][c]);
+      tc5::ld_wait();
+#pragma unroll
+      for (int g3 = 0; g3 < 3; g3++) fold(pv[g3], g3);
+    } else {
+#pragma unroll
+      for (int g3 = 0; g3 < 3; g3++) {
+        float pv[4][4];
+#pragma unroll
+        for (int c = 0; c < 4; c++) tc5::ld_x4(pvb + (4 * g3 + c) * L::BM, pv[c]);
+        tc5::ld_wait();
+        fold(pv, g3);
       }
     }
 #pragma unroll
@@ -183,10 +204,46 @@ __device__ __forceinline__ void drain_pv(long long (&acc)[4][3], uint32_t pvb, u
   if (lane == 0) tc5::mbar_arrive(freeb);
 }
 
+// The weight of one pair the straight-line evaluation cannot take (a row outside its 26-bit
+// window, or a score outside the normal binary32 range), with the status bits it raises.
+// Out of line and with scalar arguments only, so that its code does not raise the register
+// pressure of the compute warps' tile loop: only the rare calls pay for saving registers.
+struct SlowWeight {
+  float w;
+  int flags;
+};
 template <int DT>
+__device__ __noinline__ SlowWeight slow_pair_weight(long long Tq, const typename In<DT>::T* qr, int Fq, int qfit,
+                                                    const int2* qlo, int qlon, const typename In<DT>::T* kr, int Fk,
+                                                    int kf, const int2* klo, int klon, int D, float scale32, float m) {
+  float dot;
+  if (qfit && kf) {   // a score outside the normal range: the general rounding
+    dot = cr32_scaled(Tq, Fq + Fk);
+  } else if (qlon != LO_DEEP && klon != KLO_DEEP) {   // truncated dot + low limbs
+    dot = dot_lo<DT>(Tq, qr, Fq, qlo, qlon, kr, Fk, klo, klon);
+  } else if (!qfit && kf) {   // a deep row: the general exact dot
+    dot = exact_dot_lane<DT, true, false>(qr, Fq, kr, Fk, D);
+  } else if (qfit) {
+    dot = exact_dot_lane<DT, false, true>(qr, Fq, kr, Fk, D);
+  } else {
+    dot = exact_dot_lane<DT, true, true>(qr, Fq, kr, Fk, D);
+  }
+  SlowWeight r;
+  r.flags = 0;
+  float x = __fsub_rn(__fmul_rn(scale32, dot), m);
+  if (x != x) { r.flags |= ST_NONFINITE; x = neg_inf(); }
+  if (x > 0.0f) { r.flags |= ST_VIOLATION; x = 0.0f; }
+  r.w = exp32_det(x);
+  return r;
+}
+
+// SC: the scores come from the score cache (AttnArgs::scores, written by the rowmax kernel of
+// the same call) instead of the score MMAs: no key operand stream, no score issue, no
+// recombination or rounding; every other step is the same.
+template <int DT, bool SC>
 __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(const AttnArgs a, const KvPrep p) {
   using T = typename In<DT>::T;
-  using L = AccTpLayout;
+  using L = AccTpLayoutT<SC>;
   constexpr int DP = L::DP, BM = L::BM, NDS = L::NDS, NSK = L::NSK, NVB = L::NVB, NCW = L::NCW;
   constexpr int NKB = L::NKB, NWP = L::NWP, NW = DP / 32;
   constexpr int NCT = 32 * NCW;
@@ -310,7 +367,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
       const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
       tc5::bar_sync(2, L::THREADS);
       if (warp == L::LOADW) {   // ---------------- bulk copies ----------------
-        if (lane == 0) {   // key operand steps
+        if (lane == 0 && !SC) {   // key operand steps
           for (int ls = 0; ls < nkt * NDS && !s_abort; ls++) {
             const uint32_t g = tc * NDS + ls, st = g % NSK;
             if (g >= NSK && !tc5::mbar_wait(&kempty[st], ((g / NSK) - 1) & 1, &s_abort, 64)) break;
@@ -326,7 +383,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           }
         }
       } else {
-        if ((warp == L::ISSW || warp == L::ISSW2) && lane == 0) {   // ---------------- score MMAs: alternate steps ----------------
+        if ((warp == L::ISSW || warp == L::ISSW2) && lane == 0 && !SC) {   // ---------------- score MMAs: alternate steps ----------------
           for (int ls = warp == L::ISSW ? 0 : 1; ls < nkt * NDS && !s_abort; ls += 2) {
             const uint32_t g = tc * NDS + ls, st = g % NSK, tt = tc + ls / NDS;
             const int k = ls % NDS;
@@ -378,7 +435,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
       const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
       const int nrows = min(BM, a.Sq - q0);
       // ---- per pass: query slices (resident B operand of the scores), row maxima, cleared sums ----
-      for (int r = warp; r < BM; r += NCW) {
+      for (int r = warp; r < BM && !SC; r += NCW) {
         const int i = q0 + r;
         row_slices<DT, DP>(
             i < a.Sq ? qrow(i) : nullptr, a.D,
@@ -403,12 +460,6 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         for (int r = 0; r < 4; r++)
   #pragma unroll
           for (int k = 0; k < 3; k++) acc[r][k] = 0;
-        auto weight_of = [&](float sc, float m) -> float {
-          float x = __fsub_rn(sc, m);
-          if (x != x) { nf |= ST_NONFINITE; x = neg_inf(); }
-          if (x > 0.0f) { viol |= ST_VIOLATION; x = 0.0f; }
-          return exp32_det(x);
-        };
         // lane 0 waits, the warp follows
         auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
           bool ok = true;
@@ -419,8 +470,8 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         };
         // fold the PV accumulators of one tile into the integer digits, zero them, release them
         auto drain = [&](uint32_t tt) {
-          drain_pv(acc, lane_base + L::PV_COL + (tt & 1) * L::PV_BUF + rg * 4, &pvdone[tt & 1], &pvfree[tt & 1],
-                   (tt >> 1) & 1, &s_abort, lane);
+          drain_pv<SC>(acc, lane_base + L::PV_COL + (tt & 1) * L::PV_BUF + rg * 4, &pvdone[tt & 1], &pvfree[tt & 1],
+                       (tt >> 1) & 1, &s_abort, lane);
         };
         // key meta and the V-bad words of this thread's key in tile t (zeros past the range)
         auto tile_meta = [&](int t, int& mv, uint4& vb) {
@@ -429,7 +480,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           if (t < nkt) {
             const int j = a.kv_lo + t * KTILE + dcol;
             if (j < hi) {
-              mv = p.kmeta[krow0 + j];
+              if constexpr (!SC) mv = p.kmeta[krow0 + j];
               vb = *reinterpret_cast<const uint4*>(p.vbad + (krow0 + j) * NW);
             }
           }
@@ -437,6 +488,17 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         int mv_n;
         uint4 vb_n;
         tile_meta(0, mv_n, vb_n);
+        // score cache: this thread's key column of each block, rows 4 rg .. 4 rg + 3 (16 bytes),
+        // one tile ahead; the blocks of one query tile are consecutive
+        const float* sc_col = nullptr;
+        float4 sc_n = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        float mr[4];
+        if constexpr (SC) {
+          sc_col = a.scores + sc_block(a, b * a.Hq + h, q0 / SC_ROWS, 0) * SC_BLOCK + dcol * SC_ROWS + 4 * rg;
+          if (nkt > 0) sc_n = __ldcs(reinterpret_cast<const float4*>(sc_col));
+#pragma unroll
+          for (int e = 0; e < 4; e++) mr[e] = mrow[rg * 4 + e];
+        }
         for (int t = 0; t < nkt; t++) {
           const int kt = a.kv_lo + t * KTILE;
           const uint32_t tt = tc + t, bsel = tt & 1;
@@ -447,6 +509,24 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           const uint4 vb = vb_n;
           tile_meta(t + 1, mv_n, vb_n);   // the next tile's, in flight meanwhile
           const int Fk = kmeta_F(mv), kf = kmeta_fit(mv);
+          float w[4];
+          uint32_t slow = 0;
+          if constexpr (SC) {   // ---- weights from the cached exact scores ----
+            const float4 sv = sc_n;
+            if (t + 1 < nkt) sc_n = __ldcs(reinterpret_cast<const float4*>(sc_col + (size_t)(t + 1) * SC_BLOCK));
+            const float scs[4] = {sv.x, sv.y, sv.z, sv.w};
+  #pragma unroll
+            for (int e = 0; e < 4; e++) {
+              const int i = q0 + rg * 4 + e;
+              const bool valid = vj && i < a.Sq && (!a.causal || j <= i);
+              float x = __fsub_rn(scs[e], mr[e]);
+              if (valid && x != x) nf |= ST_NONFINITE;
+              if (valid && x > 0.0f) viol |= ST_VIOLATION;
+              x = x != x ? neg_inf() : (x > 0.0f ? 0.0f : x);
+              const float wf = exp32_det_nb(x);
+              w[e] = valid ? wf : 0.0f;
+            }
+          } else {
           // ---- score diagonals of rows 4 rg .. 4 rg + 3 against this thread's key ----
           const bool ok = warp_wait(&sfull, tt & 1);
           long long Tq[4];   // the exact dot of each row's (truncated) digits with this key's
@@ -469,8 +549,6 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           if (lane == 0) tc5::mbar_arrive(&sempty);
           // ---- weights: one straight-line evaluation per row (the four interleave); pairs it
           // cannot take (a row outside its window, a score outside the normal range) go to `slow` ----
-          float w[4];
-          uint32_t slow = 0;
   #pragma unroll
           for (int e = 0; e < 4; e++) {
             const int rl = rg * 4 + e, i = q0 + rl;
@@ -487,28 +565,18 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
             if (valid && !fast) slow |= 1u << e;
           }
           if (slow) {
-  #pragma unroll
             for (int e = 0; e < 4; e++)
               if ((slow >> e) & 1u) {
-                const int rl = rg * 4 + e, i = q0 + rl;
-                const T* qr = qrow(i);
-                const T* kr = krow(j);
-                float dot;
-                if (qfit[rl] && kf) {   // a score outside the normal range: the general rounding
-                  w[e] = weight_of(__fmul_rn(a.scale32, cr32_scaled(Tq[e], Fq[rl] + Fk)), mrow[rl]);
-                  continue;
-                } else if (qlon[rl] != LO_DEEP && kmeta_lon(mv) != KLO_DEEP) {   // truncated dot + low limbs
-                  dot = dot_lo<DT>(Tq[e], qr, Fq[rl], qlo[rl], qlon[rl], kr, Fk, p.klo + (krow0 + j) * NLO, kmeta_lon(mv));
-                } else if (!qfit[rl] && kf) {   // a deep row: the general exact dot
-                  dot = exact_dot_lane<DT, true, false>(qr, Fq[rl], kr, Fk, a.D);
-                } else if (qfit[rl]) {
-                  dot = exact_dot_lane<DT, false, true>(qr, Fq[rl], kr, Fk, a.D);
-                } else {
-                  dot = exact_dot_lane<DT, true, true>(qr, Fq[rl], kr, Fk, a.D);
-                }
-                w[e] = weight_of(__fmul_rn(a.scale32, dot), mrow[rl]);
+                const int rl = rg * 4 + e;
+                const SlowWeight r = slow_pair_weight<DT>(Tq[e], qrow(q0 + rl), Fq[rl], qfit[rl], qlo[rl], qlon[rl],
+                                                          krow(j), Fk, kf, p.klo + (krow0 + j) * NLO, kmeta_lon(mv),
+                                                          a.D, a.scale32, mrow[rl]);
+                w[e] = r.w;
+                nf |= r.flags & ST_NONFINITE;
+                viol |= r.flags & ST_VIOLATION;
               }
           }
+          }   // scores recomputed
           // ---- weight digits: W = w 2^79 = x 2^(8 b0), x < 2^32; words[e][q] = bytes 4q .. 4q + 3 of W ----
           uint32_t words[4][3];
           uint32_t tiny = 0;   // pairs with 0 < w < 2^-56: exact atomics below
@@ -752,6 +820,29 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         for (int r = 0; r < 4; r++) {
           const int rl = rg * 4 + r, i = q0 + rl;
           if (i >= a.Sq || d >= a.D) continue;
+          const bool touched = trow[rl] || ((tbit[rl][d >> 5] >> (d & 31)) & 1u);
+          if (fused && !a.add_into && !touched) {
+            // Fast path: NUM is exactly acc0 + acc1 2^32 + acc2 2^64 (|acc_k| < 2^62) in units of
+            // 2^(Fv - 79), so it rounds to binary64 from one 128-bit integer, with no canonical
+            // digits (well inside the NUM range: no headroom check needed)
+            const __int128 X = (__int128)acc[r][0] + (__int128)acc[r][1] * ((__int128)1 << 32) +
+                               (__int128)acc[r][2] * ((__int128)1 << 64);
+            bool neg;
+            uint64_t mm;
+            int ee;
+            const bool nz = idiv::i128_split_rn64(X, Fv[d] - 79, neg, mm, ee);
+            float o = 0.0f;   // RN64(NUM) = +0 over a positive DEN
+            if (fslow[rl]) {
+              o = __double2float_rn(__ddiv_rn(nz ? idiv::make_f64(neg, mm, ee) : 0.0, fden64[rl]));
+            } else if (nz) {
+              uint64_t qq;
+              int EE;
+              idiv::div_rn64(mm, ee, fdiv[rl], qq, EE);
+              o = __uint_as_float(idiv::rn32_bits(qq, EE, neg));
+            }
+            a.out[out_row(i) * a.D + d] = o;
+            continue;
+          }
           long long* nrow = a.num + out_row(i) * NUM_NDIG * a.D;   // unused when fused
           long long dg[NUM_NDIG + 3];
   #pragma unroll
@@ -759,7 +850,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           if (a.add_into)
   #pragma unroll
             for (int k = 0; k < NUM_NDIG; k++) dg[k] = __ldcg(nrow + (int64_t)k * a.D + d);
-          if (trow[rl] || ((tbit[rl][d >> 5] >> (d & 31)) & 1u)) {   // this digit column of the slot was touched
+          if (touched) {   // this digit column of the slot was touched
             long long* sp = slot_num(rl) + d;
   #pragma unroll
             for (int k = 0; k < NUM_NDIG; k++) {
@@ -829,22 +920,24 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   report(a.status, nf | viol);
 }
 
-template <int DT>
+template <int DT, bool SC>
 static cudaError_t launch_acc_tp_t(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
-  using L = AccTpLayout;
-  cudaError_t e = cudaFuncSetAttribute(accumulate_tp_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
+  using L = AccTpLayoutT<SC>;
+  cudaError_t e =
+      cudaFuncSetAttribute(accumulate_tp_kernel<DT, SC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
   if (e != cudaSuccess) return e;
   // the spill slots start clean (a CTA clears what it used; a kernel that gave up may not have)
   e = cudaMemsetAsync(p.spill, 0, (size_t)SPILL_SLOTS * spill_slot_words(L::DP) * sizeof(long long), st);
   if (e != cudaSuccess) return e;
   const int nt = (a.Sq + L::BM - 1) / L::BM;
   dim3 grid(a.causal ? (nt + 1) / 2 : nt, a.Hq, a.B);
-  accumulate_tp_kernel<DT><<<grid, L::THREADS, L::bytes, st>>>(a, p);
+  accumulate_tp_kernel<DT, SC><<<grid, L::THREADS, L::bytes, st>>>(a, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_accumulate_tp(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
-  return a.dtype == 0 ? launch_acc_tp_t<0>(a, p, st) : launch_acc_tp_t<1>(a, p, st);
+  if (a.scores) return a.dtype == 0 ? launch_acc_tp_t<0, true>(a, p, st) : launch_acc_tp_t<1, true>(a, p, st);
+  return a.dtype == 0 ? launch_acc_tp_t<0, false>(a, p, st) : launch_acc_tp_t<1, false>(a, p, st);
 }
 
 }  // namespace detattn

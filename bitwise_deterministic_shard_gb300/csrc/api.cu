@@ -61,10 +61,25 @@ int launched(cudaError_t e) { return e == cudaSuccess ? DA_OK : DA_ECUDA; }
 size_t round_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t m, m2, num, den, kv, total;
+  size_t m, m2, num, den, kv, sc, sc_bytes, total;
 };
 
 size_t kv_bytes(const da_attn_desc* d) { return kv_prep_bytes((int)d->k.B, (int)d->k.H, (int)d->k.S, (int)d->k.D); }
+
+// The score cache of the whole-range path (64 < D <= 128, at most ACC_TP_MAX_TILES key tiles,
+// causal only with Sq == Skv): bytes, or 0 when the path recomputes the scores instead (other
+// head dimensions, or a cache above kScoreCacheCap).
+constexpr size_t kScoreCacheCap = (size_t)16 << 30;
+size_t sc_bytes(const da_attn_desc* d, int* nkt = nullptr, int64_t* per_bh = nullptr) {
+  int n;
+  int64_t pb;
+  if (d->q.D <= 64 || d->q.D > 128 || (d->k.S + KTILE - 1) / KTILE > ACC_TP_MAX_TILES) return 0;
+  const size_t b = score_cache_bytes((int)d->q.B, (int)d->q.H, (int)d->q.S, (int)d->k.S, d->causal, &n, &pb);
+  if (b > kScoreCacheCap) return 0;
+  if (nkt) *nkt = n;
+  if (per_bh) *per_bh = pb;
+  return b;
+}
 
 WsLayout ws_layout(const da_attn_desc* d, int nsplits) {
   const size_t rows = (size_t)d->q.B * d->q.H * d->q.S;
@@ -74,7 +89,9 @@ WsLayout ws_layout(const da_attn_desc* d, int nsplits) {
   w.num = w.m2 + (nsplits > 1 ? round_up(rows * 4) : 0);
   w.den = w.num + round_up(rows * DA_NUM_NDIG * (size_t)d->q.D * 8);
   w.kv = w.den + round_up(rows * DA_DEN_NDIG * 8);
-  w.total = w.kv + round_up(kv_bytes(d));
+  w.sc = w.kv + round_up(kv_bytes(d));
+  w.sc_bytes = nsplits == 1 ? sc_bytes(d) : 0;
+  w.total = w.sc + round_up(w.sc_bytes);
   return w;
 }
 
@@ -98,6 +115,7 @@ DceArgs make_dce(const da_matrix* x) {
   DceArgs a;
   std::memset(&a, 0, sizeof(a));
   a.x = x->ptr; a.dtype = x->dtype; a.N = x->rows; a.V = x->cols; a.rs = x->row_stride;
+  a.v_base = 0; a.v_total = x->cols;
   return a;
 }
 
@@ -107,7 +125,7 @@ DceArgs make_dce(const da_matrix* x) {
 
 extern "C" {
 
-DA_EXPORT int da_abi_version(void) { return 2; }
+DA_EXPORT int da_abi_version(void) { return 3; }
 
 DA_EXPORT const char* da_status_string(int code) {
   switch (code) {
@@ -232,6 +250,55 @@ DA_EXPORT int da_accumulate_finalize(const da_attn_desc* desc, const float* m, f
   return da_finalize(num, den, desc->q.B, desc->q.H, desc->q.S, desc->q.D, out, desc->dev_status, stream);
 }
 
+DA_EXPORT size_t da_score_cache_bytes(const da_attn_desc* desc) {
+  if (check_desc(desc)) return 0;
+  return sc_bytes(desc);
+}
+
+DA_EXPORT int da_rowmax_cached(const da_attn_desc* desc, float* m, void* ws, size_t ws_bytes, da_stream_t stream) {
+  int e = check_desc(desc);
+  if (e) return e;
+  if (desc->q.B * desc->q.S == 0) return DA_OK;
+  if (!m) return DA_EINVAL;
+  if (!aligned(m, 4)) return DA_EALIGN;
+  WsLayout w = ws_layout(desc, 1);
+  if (!ws || ws_bytes < w.total) return DA_EWORKSPACE;
+  if (!aligned(ws, 256)) return DA_EALIGN;
+  char* base = (char*)ws;
+  if (!w.sc_bytes) return da_rowmax(desc, 0, desc->k.S, m, base + w.kv, ws_bytes - w.kv, stream);
+  AttnArgs a = make_args(desc);
+  a.kv_lo = 0; a.kv_hi = (int)desc->k.S; a.m_out = m;
+  a.scores = (float*)(base + w.sc);
+  sc_bytes(desc, &a.sc_nkt, &a.sc_per_bh);
+  KvPrep p = kv_prep_layout(base + w.kv, a.B, a.Hkv, a.Skv, a.D, 1);   // keys and values, once for both passes
+  cudaStream_t st = (cudaStream_t)stream;
+  if (launch_kv_prep(a, p, st) != cudaSuccess) return DA_ECUDA;
+  return launched(launch_rowmax(a, p, st));
+}
+
+DA_EXPORT int da_accumulate_finalize_cached(const da_attn_desc* desc, const float* m, float* out, void* ws,
+                                            size_t ws_bytes, da_stream_t stream) {
+  int e = check_desc(desc);
+  if (e) return e;
+  if (desc->q.B * desc->q.S == 0) return DA_OK;
+  if (!m || !out) return DA_EINVAL;
+  if (!aligned(m, 4) || !aligned(out, 4)) return DA_EALIGN;
+  WsLayout w = ws_layout(desc, 1);
+  if (!ws || ws_bytes < w.total) return DA_EWORKSPACE;
+  if (!aligned(ws, 256)) return DA_EALIGN;
+  if (!w.sc_bytes) return da_accumulate_finalize(desc, m, out, ws, ws_bytes, stream);
+  char* base = (char*)ws;
+  AttnArgs a = make_args(desc);
+  a.kv_lo = 0; a.kv_hi = (int)desc->k.S;
+  a.m_in = m; a.out = out; a.add_into = 0;
+  a.num = (long long*)(base + w.num); a.den = (long long*)(base + w.den);
+  a.scores = (float*)(base + w.sc);
+  sc_bytes(desc, &a.sc_nkt, &a.sc_per_bh);
+  KvPrep p = kv_prep_layout(base + w.kv, a.B, a.Hkv, a.Skv, a.D, 1);   // prepared by da_rowmax_cached
+  if (!accumulate_is_tp(a, p)) return DA_EINVAL;
+  return launched(launch_accumulate(a, p, (cudaStream_t)stream));
+}
+
 DA_EXPORT int da_det_attn(const da_attn_desc* desc, float* out, void* ws, size_t ws_bytes, da_stream_t stream) {
   int e = check_desc(desc);
   if (e) return e;
@@ -241,9 +308,8 @@ DA_EXPORT int da_det_attn(const da_attn_desc* desc, float* out, void* ws, size_t
   if (!ws || ws_bytes < w.total) return DA_EWORKSPACE;
   if (!aligned(ws, 256)) return DA_EALIGN;
   float* m = (float*)((char*)ws + w.m);
-  void* kv = (char*)ws + w.kv;
-  if ((e = da_rowmax(desc, 0, desc->k.S, m, kv, ws_bytes - w.kv, stream))) return e;
-  return da_accumulate_finalize(desc, m, out, ws, ws_bytes, stream);
+  if ((e = da_rowmax_cached(desc, m, ws, ws_bytes, stream))) return e;
+  return da_accumulate_finalize_cached(desc, m, out, ws, ws_bytes, stream);
 }
 
 DA_EXPORT int da_det_attn_sharded(const da_attn_desc* desc, const int64_t* kv_splits, int nsplits, const int32_t* order,
@@ -348,6 +414,38 @@ DA_EXPORT int dce_backward(const da_matrix* logits, const int64_t* targets, cons
     return DA_EALIGN;
   DceArgs a = make_dce(logits);
   a.targets = targets; a.m_in = m; a.denom = (double*)denom; a.status = dev_status;
+  return launched(launch_dce_backward(a, grad, reduction, dlogits, (cudaStream_t)stream));
+}
+
+DA_EXPORT int dce_finalize_shard(const int64_t* den, const da_matrix* logits, int64_t v_base, int64_t v_total,
+                                 const int64_t* targets, const float* m, float* loss, double* denom,
+                                 int32_t* dev_status, da_stream_t stream) {
+  int e = check_matrix(logits);
+  if (e) return e;
+  if (v_base < 0 || v_total < 1 || v_base > v_total || logits->cols > v_total - v_base) return DA_EINVAL;
+  if (logits->rows == 0) return DA_OK;
+  if (!den || !targets || !m || !loss || !denom) return DA_EINVAL;
+  if (!aligned(den, 8) || !aligned(targets, 8) || !aligned(m, 4) || !aligned(loss, 4) || !aligned(denom, 8))
+    return DA_EALIGN;
+  DceArgs a = make_dce(logits);
+  a.den = (long long*)den; a.targets = targets; a.m_in = m; a.loss = loss; a.denom = denom; a.status = dev_status;
+  a.v_base = v_base; a.v_total = v_total;
+  return launched(launch_dce_finalize(a, (cudaStream_t)stream));
+}
+
+DA_EXPORT int dce_backward_shard(const da_matrix* logits, int64_t v_base, const int64_t* targets, const float* m,
+                                 const double* denom, const float* grad, int reduction, void* dlogits,
+                                 int32_t* dev_status, da_stream_t stream) {
+  int e = check_matrix(logits);
+  if (e) return e;
+  if (v_base < 0 || reduction < 0 || reduction > 2) return DA_EINVAL;
+  if (logits->rows == 0 || logits->cols == 0) return DA_OK;
+  if (!targets || !m || !denom || !grad || !dlogits) return DA_EINVAL;
+  if (!aligned(targets, 8) || !aligned(m, 4) || !aligned(denom, 8) || !aligned(grad, 4) ||
+      !aligned(dlogits, logits->dtype == 0 ? 4 : 2))
+    return DA_EALIGN;
+  DceArgs a = make_dce(logits);
+  a.targets = targets; a.m_in = m; a.denom = (double*)denom; a.status = dev_status; a.v_base = v_base;
   return launched(launch_dce_backward(a, grad, reduction, dlogits, (cudaStream_t)stream));
 }
 

@@ -105,7 +105,10 @@ __device__ __forceinline__ bool score_below(const float (&v)[NDIAG][N], int r, i
   return fmaxf(s1, s2) <= bound && fminf(s1, s2) >= -3.4028235e38f;
 }
 
-template <int DT, int DP>
+// STORE: the score-cache variant (AttnArgs::scores).  Every valid pair's exact score is
+// rounded (no filter) and written to its cache block; the row maximum is the maximum of
+// those exact scores, so both variants produce the same rowmax.
+template <int DT, int DP, bool STORE>
 __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kernel(const AttnArgs a, const KvPrep p) {
   using T = typename In<DT>::T;
   using L = RowmaxTcLayout<DP>;
@@ -228,16 +231,58 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
         if (!__shfl_sync(0xFFFFFFFFu, tok, 0)) break;   // warp-uniform
         tc5::fence_after();
         float thr[8];   // the rows' running maxima so far (exact scores)
+        if constexpr (!STORE) {
 #pragma unroll
-        for (int r = 0; r < 8; r++) thr[r] = fmaxf(mrun[r], key_float(rkey[rg * 8 + r]));
+          for (int r = 0; r < 8; r++) thr[r] = fmaxf(mrun[r], key_float(rkey[rg * 8 + r]));
+        }
         const int Fk = kmeta_F(mv), kf = kmeta_fit(mv);
         uint32_t defer = 0;   // rows whose pair with this key needs the exact fallback
+        // score cache: this thread's 8 rows lie in query tile qt16 (rows rr0 .. rr0 + 7 of it);
+        // under causal masking that tile may have one key tile fewer than the 32-row tile
+        const int qt16 = q0 / SC_ROWS + (rg >> 1), rr0 = (rg & 1) * 8;
+        bool sc_ok = false;
+        float* sc_blk = nullptr;
+        if constexpr (STORE) {
+          const int hi16 = a.causal ? min(a.kv_hi, qt16 * SC_ROWS + SC_ROWS) : a.kv_hi;
+          sc_ok = qt16 * SC_ROWS < a.Sq && t * KTILE < hi16 - a.kv_lo;
+          if (sc_ok) sc_blk = a.scores + sc_block(a, b * a.Hq + h, qt16, t) * SC_BLOCK + jl * SC_ROWS + rr0;
+        }
 #pragma unroll
         for (int hf = 0; hf < 2; hf++) {   // rows 4 hf .. 4 hf + 3: half the diagonal sums live at a time
           float v[NDIAG][4];   // diagonal sums of these 4 rows, exact
 #pragma unroll
           for (int c = 0; c < NDIAG; c++) tc5::ld_x4(lbase + set * L::SETC + c * BM + 4 * hf, v[c]);
           tc5::ld_wait();
+          if constexpr (STORE) {   // every valid pair: its exact score, rounded once, into the cache
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+              const int r = 4 * hf + e, rl = rg * 8 + r, i = q0 + rl;
+              float sc = 0.0f;
+              if (vj && i < a.Sq && (!a.causal || j <= i)) {
+                if (qfit[rl] && kf) {
+                  const int E = Fq[rl] + Fk;
+                  const long long T = combine_diag(v, e);
+                  bool special;
+                  float c = cr32_scaled_nb(T, E, special);
+                  if (special) c = cr32_scaled(T, E);   // subnormal or overflowing: the general rounding
+                  sc = __fmul_rn(a.scale32, c);
+                } else if (qlon[rl] != LO_DEEP && kmeta_lon(mv) != KLO_DEEP) {   // truncated dot + low limbs
+                  sc = __fmul_rn(a.scale32, dot_lo<DT>(combine_diag(v, e), qbase + (int64_t)i * a.qs[2], Fq[rl],
+                                                        qlo[rl], qlon[rl], kbase + (int64_t)j * a.ks[2], Fk,
+                                                        p.klo + (krow0 + j) * NLO, kmeta_lon(mv)));
+                } else {
+                  defer |= 1u << rl;   // a deep row: the warp's exact dot below stores it
+                }
+                if (!((defer >> rl) & 1u)) {
+                  if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
+                  mrun[r] = sc > mrun[r] ? sc : mrun[r];
+                }
+              }
+              o[e] = sc;
+            }
+            if (sc_ok) *reinterpret_cast<float4*>(sc_blk + 4 * hf) = make_float4(o[0], o[1], o[2], o[3]);
+          } else {
 #pragma unroll
           for (int e = 0; e < 4; e++) {
             const int r = 4 * hf + e, rl = rg * 8 + r, i = q0 + rl;
@@ -260,6 +305,7 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
               }
             }
           }
+          }   // filter
         }
 #pragma unroll
         for (int c = 0; c < NDIAG; c++) tc5::st_zero_x8(lbase + set * L::SETC + c * BM);
@@ -278,12 +324,17 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
                                                                   kbase + (int64_t)jj * a.ks[2], a.D, lane));
           if (!(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
           if (lane == 0 && sc == sc) atomicMax(&rkey[rl], float_key(sc));
+          if constexpr (STORE) {   // the lane that owns the key stored the pair's placeholder: overwrite it
+            if (lane == src && sc_ok) sc_blk[rl - rg * 8] = sc;
+          }
           if (lane == src) defer &= defer - 1;
         }
+        if constexpr (!STORE) {
 #pragma unroll
-        for (int r = 0; r < 8; r++) {   // publish this tile's maxima
-          const int km = __reduce_max_sync(0xFFFFFFFFu, float_key(mrun[r]));
-          if (lane == 0 && key_float(km) > thr[r]) atomicMax(&rkey[rg * 8 + r], km);
+          for (int r = 0; r < 8; r++) {   // publish this tile's maxima
+            const int km = __reduce_max_sync(0xFFFFFFFFu, float_key(mrun[r]));
+            if (lane == 0 && key_float(km) > thr[r]) atomicMax(&rkey[rg * 8 + r], km);
+          }
         }
       }
 #pragma unroll
@@ -713,16 +764,40 @@ __global__ void __launch_bounds__(256, AccCfg<DP>::MINB) accumulate_kernel(const
 // ---------------------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------------------
-template <int DT, int DP>
+template <int DT, int DP, bool STORE>
 static cudaError_t launch_rowmax_t(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
   using L = RowmaxTcLayout<DP>;
   const size_t smem = L::bytes;
-  cudaError_t e = cudaFuncSetAttribute(rowmax_tc_kernel<DT, DP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(rowmax_tc_kernel<DT, DP, STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int nt = (a.Sq + L::BM - 1) / L::BM;
   dim3 grid(a.causal ? (nt + 1) / 2 : nt, a.Hq, a.B);
-  rowmax_tc_kernel<DT, DP><<<grid, L::THREADS, smem, st>>>(a, p);
+  rowmax_tc_kernel<DT, DP, STORE><<<grid, L::THREADS, smem, st>>>(a, p);
   return cudaGetLastError();
+}
+
+template <int DT, int DP>
+static cudaError_t launch_rowmax_t(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
+  if constexpr (DP == 128) {
+    if (a.scores) return launch_rowmax_t<DT, DP, true>(a, p, st);
+  }
+  return launch_rowmax_t<DT, DP, false>(a, p, st);
+}
+
+size_t score_cache_bytes(int B, int Hq, int Sq, int Skv, int causal, int* sc_nkt, int64_t* sc_per_bh) {
+  const int64_t nqt = (Sq + SC_ROWS - 1) / SC_ROWS;
+  int64_t per_bh;
+  *sc_nkt = (Skv + KTILE - 1) / KTILE;
+  if (causal) {
+    if (Sq != Skv) return 0;
+    const int64_t q = nqt - 1, g = q >> 3, r = q & 7;
+    per_bh = nqt == 0 ? 0 : q + 4 * g * (g - 1) + r * g + (Sq + KTILE - 1) / KTILE;
+  } else {
+    per_bh = nqt * *sc_nkt;
+  }
+  *sc_per_bh = per_bh;
+  return (size_t)B * Hq * per_bh * SC_BLOCK * sizeof(float);
 }
 
 template <int DT, int DP>

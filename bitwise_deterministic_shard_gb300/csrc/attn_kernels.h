@@ -23,7 +23,26 @@ struct AttnArgs {
   int* status;                   // device status word (may be null)
   float* out;                    // non-null: the tensor-PV accumulate finalizes into out [B, Hq, Sq, D]
                                  // instead of writing digits (one key range, add_into == 0)
+  float* scores;                 // non-null: the score cache (below); rowmax writes it, the tensor-PV
+                                 // accumulate reads it instead of recomputing the scores
+  int64_t sc_per_bh;             // score-cache blocks per (b, query head)
+  int sc_nkt;                    // non-causal: key tiles per query tile
 };
+
+// Score cache of one whole-range call (kv_lo = 0, kv_hi = Skv; causal needs Sq = Skv): the
+// exact score s_ij of every (query, key) pair of every processed tile, f32, in blocks of
+// SC_ROWS query rows x KTILE keys laid out [key][row], one block per (b, h, query tile of
+// SC_ROWS rows, key tile).  Causal: query tile q has ceil(min(Sq, SC_ROWS (q + 1)) / KTILE)
+// key tiles, so the tiles of query tiles below q (all full) number
+// q + 8 g (g - 1) / 2 + (q % 8) g with g = q / 8; non-causal: sc_nkt per query tile.
+constexpr int SC_ROWS = 16;
+__host__ __device__ inline int64_t sc_block(const AttnArgs& a, int bh, int qt, int kt) {
+  const int64_t g = qt >> 3, r = qt & 7;
+  const int64_t before = a.causal ? qt + 4 * g * (g - 1) + r * g : (int64_t)qt * a.sc_nkt;
+  return (int64_t)bh * a.sc_per_bh + before + kt;
+}
+constexpr int SC_BLOCK = SC_ROWS * 128;   // floats per block (KTILE keys)
+size_t score_cache_bytes(int B, int Hq, int Sq, int Skv, int causal, int* sc_nkt, int64_t* sc_per_bh);
 
 // Prepared keys/values of one call's key range (prep_kernels.cu), rows indexed as
 // (b * Hkv + hk) * Skv + j.
@@ -60,7 +79,7 @@ size_t kv_prep_bytes(int B, int Hkv, int Skv, int D);
 KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v);
 cudaError_t launch_kv_prep(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
 
-cudaError_t launch_rowmax(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
+cudaError_t launch_rowmax(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // a.scores: also store scores
 cudaError_t launch_accumulate(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
 cudaError_t launch_accumulate_tc(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // D <= 128
 cudaError_t launch_accumulate_tp(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // 64 < D <= 128
@@ -86,6 +105,9 @@ struct DceArgs {
   float* loss;
   double* denom;
   int* status;
+  // vocabulary shards: the matrix holds columns [v_base, v_base + V) of a vocabulary of v_total
+  // columns (0 and V for a whole vocabulary); targets are global column indices
+  int64_t v_base, v_total;
 };
 cudaError_t launch_dce_rowmax(const DceArgs& a, cudaStream_t st);
 cudaError_t launch_dce_denom(const DceArgs& a, cudaStream_t st);

@@ -137,12 +137,17 @@ __global__ void dce_finalize_kernel(const DceArgs a) {
     const double d64 = digits_rn64<DEN_NDIG>(e, DEN_E0);
     a.denom[i] = d64;
     const int64_t t = a.targets[i];
-    if (t < 0 || t >= a.V) {
+    if (t < 0 || t >= a.v_total) {
       st |= ST_BAD_TARGET;
       a.loss[i] = __int_as_float(0x7FC00000);
       continue;
     }
-    const double xt = (double)__uint_as_float(In<DT>::bits((const T*)a.x + i * a.rs, t));
+    const int64_t c = t - a.v_base;   // the target's column in this matrix
+    if (c < 0 || c >= a.V) {          // another vocabulary shard holds it: this shard adds +0
+      a.loss[i] = 0.0f;
+      continue;
+    }
+    const double xt = (double)__uint_as_float(In<DT>::bits((const T*)a.x + i * a.rs, c));
     const double diff = __dsub_rn((double)a.m_in[i], xt);
     a.loss[i] = __double2float_rn(__dadd_rn(log64_det(d64), diff));
   }
@@ -180,7 +185,7 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
   __syncthreads();
   const idiv::Divisor Dv = sdiv;
   const bool slow = sslow;
-  const int64_t tg = a.targets[i] - c0;   // the target's column within this chunk (any value)
+  const int64_t tg = a.targets[i] - a.v_base - c0;   // the target's column within this chunk (any value)
   float go = reduction == 0 ? grad[i] : grad[0];
   if (reduction == 2) go = __double2float_rn(__ddiv_rn((double)go, (double)a.N));
   int st = 0;

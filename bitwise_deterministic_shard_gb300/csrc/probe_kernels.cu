@@ -1,0 +1,84 @@
+// Measurement and self-test entry points that sit beside the method (include/detattn.h,
+// "probes"): they compute nothing of the attention or cross-entropy path.
+//
+// da_probe_int_mac: the issue rate of exact 32 x 32 -> 64-bit integer multiply-adds
+// (mad.wide.s32) over the whole GPU, the unit of exact arithmetic the integer pipe offers.
+// The benchmark divides the path's exact multiply-adds per second by this rate to state
+// the fraction of the integer pipe's peak that the path reaches.
+//
+// da_probe_bounded_wait: one warp waits on an mbarrier phase that nothing completes, through
+// the same bounded wait (tc5.cuh) every pipelined kernel of the library uses.  The wait gives
+// up after its time limit, the kernel returns normally and reports DA_STATUS_TIMEOUT in the
+// status word, so the caller's context stays usable: the timeout path is exercised without
+// a fault or a hang.
+#include "../../include/detattn.h"
+#include "numerics.cuh"
+#include "tc5.cuh"
+
+namespace detattn {
+
+constexpr int PROBE_ACC = 8;   // independent accumulators per thread (hides the multiply latency)
+constexpr int PROBE_UNROLL = 4;
+
+__global__ void __launch_bounds__(512) probe_int_mac_kernel(long long iters, long long* sink) {
+  long long acc[PROBE_ACC];
+  int a[PROBE_ACC];
+#pragma unroll
+  for (int k = 0; k < PROBE_ACC; k++) {
+    acc[k] = threadIdx.x + k;
+    a[k] = (int)(0x9E3779B1u * (threadIdx.x * PROBE_ACC + k + 1));
+  }
+  const int b = (int)(blockIdx.x * 2654435761u) | 1;
+  for (long long it = 0; it < iters; it++) {
+#pragma unroll
+    for (int u = 0; u < PROBE_UNROLL; u++)
+#pragma unroll
+      for (int k = 0; k < PROBE_ACC; k++) asm volatile("mad.wide.s32 %0, %1, %2, %0;" : "+l"(acc[k]) : "r"(a[k]), "r"(b));
+  }
+  long long s = 0;
+#pragma unroll
+  for (int k = 0; k < PROBE_ACC; k++) s ^= acc[k];
+  if (s == 0x7FFFFFFFFFFFFFFFll) sink[0] = s;   // keeps the chain alive; practically never stored
+}
+
+__global__ void probe_bounded_wait_kernel(int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    tc5::mbar_init(&bar, 1);   // one arrival would complete phase 0; none comes
+    abort_flag = 0;
+    tc5::mbar_fence_init();
+  }
+  __syncthreads();
+  bool ok = true;
+  if (threadIdx.x == 0) ok = tc5::mbar_wait(&bar, 0, &abort_flag, 1000);
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  if (!ok && threadIdx.x == 0) report(status, ST_TIMEOUT);
+}
+
+}  // namespace detattn
+
+#define DA_EXPORT __attribute__((visibility("default")))
+
+extern "C" {
+
+DA_EXPORT int da_probe_int_mac(int64_t iters, int nblocks, int64_t* sink, da_stream_t stream) {
+  if (iters < 0 || nblocks < 1 || nblocks > (1 << 20)) return DA_EINVAL;
+  if (!sink) return DA_EINVAL;
+  if (reinterpret_cast<uintptr_t>(sink) % 8) return DA_EALIGN;
+  detattn::probe_int_mac_kernel<<<nblocks, 512, 0, (cudaStream_t)stream>>>(iters, (long long*)sink);
+  return cudaGetLastError() == cudaSuccess ? DA_OK : DA_ECUDA;
+}
+
+DA_EXPORT int64_t da_probe_int_mac_per_thread_iter(void) {
+  return (int64_t)detattn::PROBE_ACC * detattn::PROBE_UNROLL;
+}
+
+DA_EXPORT int da_probe_bounded_wait(int32_t* dev_status, da_stream_t stream) {
+  if (!dev_status) return DA_EINVAL;
+  if (reinterpret_cast<uintptr_t>(dev_status) % 4) return DA_EALIGN;
+  detattn::probe_bounded_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((int*)dev_status);
+  return cudaGetLastError() == cudaSuccess ? DA_OK : DA_ECUDA;
+}
+
+}  // extern "C"

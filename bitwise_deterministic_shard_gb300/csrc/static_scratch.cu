@@ -71,6 +71,8 @@ extern "C" __attribute__((visibility("default"))) int dce_forward_static(const d
   a.rs = logits->row_stride;
   a.v_lo = 0;
   a.v_hi = logits->cols;
+  a.v_base = 0;
+  a.v_total = logits->cols;
   a.m_in = m;
   a.m_out = m;
   a.den = den;

@@ -156,11 +156,28 @@ int da_finalize(const int64_t* num, const int64_t* den, int64_t B, int64_t Hq, i
 /* Bytes of workspace da_det_attn (nsplits <= 1) or da_det_attn_sharded needs. */
 size_t da_workspace_bytes(const da_attn_desc* desc, int nsplits);
 
-/* det-attn "API", det_attn: rowmax over all keys, then da_accumulate_finalize (accumulate and
- * finalize; for 64 < D <= 128 in one kernel that writes only the output).  out: device f32
- * [B, Hq, Sq, D] contiguous; ws: device workspace of at least da_workspace_bytes(desc, 1).
- * Bit-identical to da_det_attn_sharded for every split and order. */
+/* det-attn "API", det_attn: da_rowmax_cached, then da_accumulate_finalize_cached (below).
+ * out: device f32 [B, Hq, Sq, D] contiguous; ws: device workspace of at least
+ * da_workspace_bytes(desc, 1).  Bit-identical to da_det_attn_sharded for every split and
+ * order. */
 int da_det_attn(const da_attn_desc* desc, float* out, void* ws, size_t ws_bytes, da_stream_t stream);
+
+/* The two passes of det_attn (det-attn "Method": a max-reduce, then the exact sums with the
+ * global rowmax) over all keys, with the score cache.  The score of a pair is a fixed function
+ * of its query and key rows, so pass 1 can hand every exact score it computes to pass 2:
+ * for 64 < D <= 128 (at most 65,536 keys, and a cache of at most 16 GiB) da_rowmax_cached
+ * prepares keys and values once, writes m (device f32 [B, Hq, Sq]) and stores every score it
+ * rounds in the workspace's cache; da_accumulate_finalize_cached then reads the scores
+ * instead of recomputing them and writes the f32 output, bit for bit what
+ * da_accumulate_finalize gives.  Otherwise they are da_rowmax over [0, Skv) and
+ * da_accumulate_finalize.  Both take the workspace of da_workspace_bytes(desc, 1); the
+ * second call reads what the first left in it, so issue them in this order on one stream
+ * with the same descriptor and workspace.  da_score_cache_bytes: the cache's share of that
+ * workspace (0 when the scores are recomputed). */
+size_t da_score_cache_bytes(const da_attn_desc* desc);
+int da_rowmax_cached(const da_attn_desc* desc, float* m, void* ws, size_t ws_bytes, da_stream_t stream);
+int da_accumulate_finalize_cached(const da_attn_desc* desc, const float* m, float* out, void* ws, size_t ws_bytes,
+                                  da_stream_t stream);
 
 /* det-attn "API", det_attn_sharded: the keys split into nsplits contiguous shards of
  * kv_splits[k] keys (host array, sum = Skv, entries >= 0), visited in the order
@@ -202,6 +219,24 @@ int dce_finalize(const int64_t* den, const da_matrix* logits, const int64_t* tar
 int dce_backward(const da_matrix* logits, const int64_t* targets, const float* m, const double* denom,
                  const float* grad, int reduction, void* dlogits, int32_t* dev_status, da_stream_t stream);
 
+/* Vocabulary-parallel forms (det-cross-entropy, "Usage": the vocabulary sharded over ranks
+ * composes by a max and a digit add; the logit of a row's target lives on one shard).
+ * logits holds columns [v_base, v_base + cols) of a vocabulary of v_total columns; targets
+ * are global column indices; den, m and denom are the composed (global) values.
+ *   dce_finalize_shard: denom as dce_finalize; loss_i = the full loss for a row whose target
+ *   lies in this shard, +0 for a row whose target lies in another shard, NaN with
+ *   DA_STATUS_BAD_TARGET for a target outside [0, v_total).  Summing the shards' losses
+ *   (exactly one term is nonzero) gives dce_finalize's loss over the whole vocabulary.
+ *   DA_EINVAL unless 0 <= v_base and v_base + cols <= v_total.
+ *   dce_backward_shard: the dLogits columns of this shard (as dce_backward; the one-hot is
+ *   subtracted where the target falls in the shard). */
+int dce_finalize_shard(const int64_t* den, const da_matrix* logits, int64_t v_base, int64_t v_total,
+                       const int64_t* targets, const float* m, float* loss, double* denom, int32_t* dev_status,
+                       da_stream_t stream);
+int dce_backward_shard(const da_matrix* logits, int64_t v_base, const int64_t* targets, const float* m,
+                       const double* denom, const float* grad, int reduction, void* dlogits, int32_t* dev_status,
+                       da_stream_t stream);
+
 /* det-cross-entropy "API", the loss reduction of cross_entropy: with S the exact sum of the
  * rows f32 losses (a Kulisch accumulator), reduction 1 ("sum") gives RN32(RN64(S)), 2
  * ("mean") RN32(RN64(RN64(S) / rows)); a NaN loss gives NaN, infinite losses their IEEE
@@ -233,6 +268,24 @@ int dce_reduce(const float* loss, int64_t rows, int reduction, float* out, da_st
 #define DA_STATIC_MAX_ROWS 65536
 int dce_forward_static(const da_matrix* logits, const int64_t* targets, float* loss, double* denom,
                        int32_t* dev_status, da_stream_t stream);
+
+/* ---- Probes.  Neither computes anything of the method, and the pages have no counterpart
+ * of them: one measures a hardware rate the benchmark reports against, one exercises the
+ * bounded-wait path of the pipelined kernels. ---- */
+
+/* Issue rate of exact 32 x 32 -> 64-bit integer multiply-adds (mad.wide.s32): nblocks CTAs of
+ * 512 threads each run iters iterations of da_probe_int_mac_per_thread_iter() independent
+ * multiply-adds per thread.  Time the launch on `stream` to get the GPU's rate; sink:
+ * device int64 [1], written only in a practically unreachable case (it keeps the chain
+ * live).  DA_EINVAL for iters < 0, nblocks outside [1, 2^20] or a null sink. */
+int da_probe_int_mac(int64_t iters, int nblocks, int64_t* sink, da_stream_t stream);
+int64_t da_probe_int_mac_per_thread_iter(void);
+
+/* One warp waits on an mbarrier phase that nothing completes, through the bounded wait the
+ * pipelined kernels use (it gives up after about 2 s).  The kernel then ends normally and
+ * ORs DA_STATUS_TIMEOUT into *dev_status (device int32, required): the caller reads the
+ * status, and the context stays usable.  Exercises the timeout path without a fault. */
+int da_probe_bounded_wait(int32_t* dev_status, da_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def _declared():
     txt = open(os.path.join(ROOT, "include", "detattn.h")).read()
     txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char\s*\*|const char\s*\*)\s*\**\s*(\w+)\s*\(", txt, flags=re.M)
+    names = re.findall(r"^\s*(?:const\s+)?(?:int64_t|int|size_t|char\s*\*|const char\s*\*)\s*\**\s*(\w+)\s*\(", txt, flags=re.M)
     return sorted(set(names))
 
 
@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(libpath):
 def test_host_only_calls(libpath):
     lib = ctypes.CDLL(libpath)
     lib.da_status_string.restype = ctypes.c_char_p
-    assert lib.da_abi_version() == 2
+    assert lib.da_abi_version() == 3
     assert lib.da_status_string(0) == b"ok"
     assert lib.da_status_string(5).startswith(b"workspace")
 
@@ -96,3 +96,15 @@ def test_new_entry_points_reject_before_any_launch(libpath):
     assert L.dce_reduce(None, -1, 1, 4096, None) == 1
     assert L.dce_reduce(None, 4, 2, 4096, None) == 1                                             # null losses
     assert L.dce_reduce(4098, 4, 2, 4096, None) == 4                                             # misaligned
+
+
+def test_probe_arguments_rejected_before_any_launch(libpath):
+    import bitwise_deterministic_shard_gb300 as da
+    L = da.lib()
+    assert L.da_probe_int_mac(-1, 4, None, None) == 1
+    assert L.da_probe_int_mac(8, 0, None, None) == 1
+    assert L.da_probe_int_mac(8, 4, None, None) == 1                        # null sink
+    assert L.da_probe_int_mac(8, 4, ctypes.c_void_p(4100), None) == 4      # misaligned sink
+    assert L.da_probe_bounded_wait(None, None) == 1
+    assert L.da_probe_int_mac_per_thread_iter() == 32
+    assert "da_probe_int_mac_per_thread_iter" in _declared()

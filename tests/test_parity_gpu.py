@@ -430,3 +430,16 @@ def test_dce_bad_target(da):
     torch.cuda.synchronize()
     assert da.read_status(st) & da.STATUS_BAD_TARGET
     assert torch.isnan(loss[1]) and torch.isnan(loss[2]) and not torch.isnan(loss[0])
+
+
+@cuda
+def test_bounded_wait_gives_up_and_reports_timeout(da, orc):
+    """A kernel waits on an mbarrier phase that nothing completes, through the bounded wait
+    every pipelined kernel uses: the wait gives up after its limit, the status word carries
+    STATUS_TIMEOUT, and the context stays usable for the next call."""
+    st = da.new_status()
+    assert da.probe_bounded_wait(st) == da.STATUS_TIMEOUT
+    Q, K, V = W.random_attn(49, 1, 2, 2, 40, 128, torch.bfloat16, True)
+    out = da.det_attn(Q.cuda(), K.cuda(), V.cuda(), causal=True)
+    _, _, _, ref = orc.Attn(Q, K, V, True).forward_rows()
+    assert_bits_equal(out.reshape(-1, 128), ref, "after a timed-out wait")
