@@ -67,10 +67,11 @@
 
 namespace detattn {
 
-// SC: the score-cache variant holds no query operand and no key ring; the V ring takes that room.
+// SC: the score-cache variant holds no query operand and no key ring (a deeper V ring measured
+// slower, so the room stays unused).
 template <bool SC>
 struct AccTpLayoutT {
-  static constexpr int DP = 128, BM = 16, NDS = DP / 16, NSK = 4, NVB = SC ? 10 : 4, NCW = 16;
+  static constexpr int DP = 128, BM = 16, NDS = DP / 16, NSK = 4, NVB = 4, NCW = 16;
   // warps: NCW compute (four warpgroups) and the control warpgroup: copies (lane 0 key steps,
   // lane 1 V blocks), score MMAs of even steps, PV and DEN MMAs, score MMAs of odd steps
   static constexpr int LOADW = NCW, ISSW = NCW + 1, PISSW = NCW + 2, ISSW2 = NCW + 3, THREADS = 32 * (NCW + 4);
@@ -554,7 +555,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
             const int rl = rg * 4 + e, i = q0 + rl;
             const bool valid = ok && vj && i < a.Sq && (!a.causal || j <= i);
             bool sp;
-            const float c = cr32_scaled_nb(Tq[e], Fq[rl] + Fk, sp);
+            const float c = cr32_scaled_cvt(Tq[e], Fq[rl] + Fk, sp);
             float x = __fsub_rn(__fmul_rn(a.scale32, c), mrow[rl]);
             const bool fast = valid && qfit[rl] && kf && !sp;
             if (fast && x != x) nf |= ST_NONFINITE;
@@ -821,28 +822,6 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           const int rl = rg * 4 + r, i = q0 + rl;
           if (i >= a.Sq || d >= a.D) continue;
           const bool touched = trow[rl] || ((tbit[rl][d >> 5] >> (d & 31)) & 1u);
-          if (fused && !a.add_into && !touched) {
-            // Fast path: NUM is exactly acc0 + acc1 2^32 + acc2 2^64 (|acc_k| < 2^62) in units of
-            // 2^(Fv - 79), so it rounds to binary64 from one 128-bit integer, with no canonical
-            // digits (well inside the NUM range: no headroom check needed)
-            const __int128 X = (__int128)acc[r][0] + (__int128)acc[r][1] * ((__int128)1 << 32) +
-                               (__int128)acc[r][2] * ((__int128)1 << 64);
-            bool neg;
-            uint64_t mm;
-            int ee;
-            const bool nz = idiv::i128_split_rn64(X, Fv[d] - 79, neg, mm, ee);
-            float o = 0.0f;   // RN64(NUM) = +0 over a positive DEN
-            if (fslow[rl]) {
-              o = __double2float_rn(__ddiv_rn(nz ? idiv::make_f64(neg, mm, ee) : 0.0, fden64[rl]));
-            } else if (nz) {
-              uint64_t qq;
-              int EE;
-              idiv::div_rn64(mm, ee, fdiv[rl], qq, EE);
-              o = __uint_as_float(idiv::rn32_bits(qq, EE, neg));
-            }
-            a.out[out_row(i) * a.D + d] = o;
-            continue;
-          }
           long long* nrow = a.num + out_row(i) * NUM_NDIG * a.D;   // unused when fused
           long long dg[NUM_NDIG + 3];
   #pragma unroll

@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
                   const int E = Fq[rl] + Fk;
                   const long long T = combine_diag(v, e);
                   bool special;
-                  float c = cr32_scaled_nb(T, E, special);
+                  float c = cr32_scaled_cvt(T, E, special);
                   if (special) c = cr32_scaled(T, E);   // subnormal or overflowing: the general rounding
                   sc = __fmul_rn(a.scale32, c);
                 } else if (qlon[rl] != LO_DEEP && kmeta_lon(mv) != KLO_DEEP) {   // truncated dot + low limbs

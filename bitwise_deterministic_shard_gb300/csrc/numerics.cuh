@@ -198,6 +198,20 @@ __device__ __forceinline__ float cr32_scaled_nb(long long T, int F, bool& specia
   return mag == 0ull ? 0.0f : __uint_as_float(bitsv);
 }
 
+// cr32_scaled_nb through the hardware's correctly rounded 64-bit integer -> binary32
+// conversion (cvt.rn.f32.s64, issued on the FP64 pipe, which the score kernels otherwise leave
+// idle): RN32(T) times 2^F, exact when that product is a normal binary32, so equal to
+// RN32(T 2^F) there (rounding to 24 bits commutes with an exact power-of-two scale; a value
+// whose 24-bit rounding reaches 2^-126 also rounds to 2^-126 on the subnormal grid).
+// *special is set when T is nonzero and the scaled result is not normal, or F lies outside
+// [-126, 127]; the caller then takes cr32_scaled.
+__device__ __forceinline__ float cr32_scaled_cvt(long long T, int F, bool& special) {
+  const float f = __ll2float_rn(T);
+  const int be = (int)((__float_as_uint(f) >> 23) & 0xFFu) + F;
+  special = T != 0 && (be < 1 || be > 254 || F < -126 || F > 127);
+  return __fmul_rn(f, __uint_as_float((uint32_t)(min(max(F, -126), 127) + 127) << 23));
+}
+
 // ---------------------------------------------------------------------------------------
 // Kulisch accumulator in radix 2^32 (int64 words with lazy carries); word k weighs
 // 2^(32k - 320).  Used by the exact fallback dot and by digit conversions.

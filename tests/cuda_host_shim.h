@@ -31,6 +31,7 @@ inline double __dadd_rn(double a, double b) { return a + b; }
 inline double __dsub_rn(double a, double b) { return a - b; }
 inline double __ddiv_rn(double a, double b) { return a / b; }
 inline double __ull2double_rn(unsigned long long x) { return (double)x; }
+inline float __ll2float_rn(long long x) { return (float)x; }   // IEEE conversion, round to nearest even
 inline float __double2float_rn(double x) { return (float)x; }
 inline float __uint_as_float(uint32_t u) { return da_bitcast<float>(u); }
 inline uint32_t __float_as_uint(float f) { return da_bitcast<uint32_t>(f); }

@@ -1,7 +1,8 @@
 // Host driver for the device numerics of the CUDA path (csrc/numerics.cuh, compiled for the
 // host through cuda_host_shim.h): reads raw inputs from stdin, writes raw outputs to stdout.
 //   mode 0: binary32 x        -> exp32_det(x), exp32_det_nb(x)            (binary32 bits)
-//   mode 1: (int64 T, int32 F) -> cr32_scaled(T, F), cr32_scaled_nb(T, F) (bits), special flag
+//   mode 1: (int64 T, int32 F) -> cr32_scaled(T, F), cr32_scaled_nb(T, F) (bits), its special flag,
+//           cr32_scaled_cvt(T, F) (bits), its special flag
 //   mode 2: 15 int64 digits    -> digits_rn64<15>(digits, -320)            (binary64)
 //   mode 3: 6 int64 digits     -> digits_rn64<6>(digits, -160)             (binary64)
 //   mode 4: binary64 d         -> log64_det(d)                             (binary64)
@@ -35,11 +36,12 @@ int main(int argc, char** argv) {
   } else if (mode == 1) {
     const std::vector<long long> in = read_all<long long>();   // pairs (T, F)
     for (size_t i = 0; i + 1 < in.size(); i += 2) {
-      bool sp = false;
+      bool sp = false, sc = false;
       const int F = (int)in[i + 1];
-      const uint32_t r[3] = {__float_as_uint(cr32_scaled(in[i], F)), __float_as_uint(cr32_scaled_nb(in[i], F, sp)),
-                             sp ? 1u : 0u};
-      fwrite(r, 4, 3, stdout);
+      const uint32_t nb = __float_as_uint(cr32_scaled_nb(in[i], F, sp));
+      const uint32_t cv = __float_as_uint(cr32_scaled_cvt(in[i], F, sc));
+      const uint32_t r[5] = {__float_as_uint(cr32_scaled(in[i], F)), nb, sp ? 1u : 0u, cv, sc ? 1u : 0u};
+      fwrite(r, 4, 5, stdout);
     }
   } else if (mode == 2 || mode == 3) {
     const std::vector<long long> in = read_all<long long>();

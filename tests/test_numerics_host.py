@@ -55,13 +55,29 @@ def test_cr32_scaled_is_the_correctly_rounded_binary32(drv):
     T = np.where(rng.random(n) < 0.5, -mag, mag)
     T[:6] = [0, 1, -1, 2 ** 62, -(2 ** 62), 0x1000001]
     F = rng.integers(-200, 120, n).astype(np.int64)
+    # the edges of the normal range: values just below / at / above 2^-126 and 2^128, ties included
+    edge_T, edge_F = [], []
+    for t in (2 ** 24 - 1, 2 ** 24, 2 ** 24 + 1, 2 ** 25 - 1, 2 ** 25 + 1, 2 ** 26 - 2, 3 * 2 ** 23,
+              2 ** 40 - 2 ** 15, 2 ** 40 + 2 ** 16 + 1, 2 ** 62 - 1):
+        top = t.bit_length() - 1
+        for f in (-126 - top - 1, -126 - top, -126 - top + 1, 127 - top - 1, 127 - top, 127 - top + 1):
+            for sgn in (1, -1):
+                edge_T.append(sgn * t)
+                edge_F.append(f)
+    T = np.concatenate([T, np.asarray(edge_T, dtype=np.int64)])
+    F = np.concatenate([F, np.asarray(edge_F, dtype=np.int64)])
     pairs = np.stack([T, F], axis=1).astype(np.int64)
-    got = drv(1, pairs, np.uint32, 3)
-    for (t, f), (a, b, sp) in zip(pairs.tolist(), got.tolist()):
+    got = drv(1, pairs, np.uint32, 5)
+    n_cvt = 0
+    for (t, f), (a, b, sp, c, sc) in zip(pairs.tolist(), got.tolist()):
         want = np.float32(E.rn32(Fraction(t) * Fraction(2) ** f)).view(np.uint32)
         assert a == want, (t, f)
         if not sp:
             assert b == a, (t, f)                                           # fast twin where it claims the result
+        if not sc:
+            assert c == a, (t, f)                                           # conversion twin likewise
+            n_cvt += 1
+    assert n_cvt > len(pairs) // 3                                         # and it claims most of them
 
 
 def test_digits_to_binary64(drv):
