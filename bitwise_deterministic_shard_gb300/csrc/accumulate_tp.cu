@@ -67,8 +67,8 @@
 
 namespace detattn {
 
-// SC: the score-cache variant holds no query operand and no key ring (a deeper V ring measured
-// slower, so the room stays unused).
+// SC: the score-cache variant holds no query operand and no key ring; that room holds the
+// epilogue's element list (a deeper V ring there measured slower).
 template <bool SC>
 struct AccTpLayoutT {
   static constexpr int DP = 128, BM = 16, NDS = DP / 16, NSK = 4, NVB = 4, NCW = 16;
@@ -89,13 +89,24 @@ struct AccTpLayoutT {
   static constexpr size_t w_buf = (size_t)NKB * NWP * w_blk;           // one tile's weight digit planes [kb][s]
   static constexpr size_t w_off = v_off + (size_t)NVB * VP_BLOCK;      // two buffers
   static constexpr size_t one_off = w_off + 2 * w_buf;                 // 16 x 16 f16 ones: DEN's B operand
-  static constexpr size_t bytes = one_off + 16 * 16 * 2;
+  // SC: the epilogue's list of elements that need canonical digits (every element of a pass at
+  // most), in the room the query operand and key ring leave unused
+  static constexpr size_t e_off = one_off + 16 * 16 * 2;
+  static constexpr size_t bytes = e_off + (SC ? (size_t)BM * DP * 32 : 0);
   static_assert(DEN_COL + 16 <= TCOLS, "TMEM columns");
   static_assert(NDEN * BM == 128, "the DEN MMA's A operand is eight digit planes");
   static_assert(NW16 <= 256 && NW16 % 16 == 0, "one PV MMA covers every weight digit");
   static_assert(bytes <= 213 * 1024, "shared memory budget (plus about 8 KB static)");
 };
 using AccTpLayout = AccTpLayoutT<false>;
+
+// an element of the score-cache variant's epilogue that needs canonical digits: row, column and
+// its three register digits
+struct EpiElem {
+  int rl, d;
+  long long a0, a1, a2;
+};
+static_assert(sizeof(EpiElem) <= 32, "element list entry");
 
 // one 16-key block: V digit t (A) times the ten stacked weight digits (B) into P_{s+t} of
 // the PV buffer at TMEM address pv; weight digits 0-7 (A, MN-major) times ones (B) into DEN
@@ -262,6 +273,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   __shared__ uint32_t tmem_s;
   __shared__ int Fq[BM], Fv[DP];
   __shared__ unsigned char qfit[BM], qlon[BM];
+  __shared__ int elist_n;   // SC epilogue: elements listed for canonical digits
   __shared__ int2 qlo[BM][NLO];
   __shared__ float mrow[BM];
   __shared__ long long denT[BM][3];
@@ -447,6 +459,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
       }
       for (int r = tid; r < BM; r += NCT) mrow[r] = (q0 + r < a.Sq) ? a.m_in[out_row(q0 + r)] : 0.0f;
       for (int e = tid; e < BM * 3; e += NCT) (&denT[0][0])[e] = 0;
+      if (tid == 0) elist_n = 0;
       for (int e = tid; e < NCW; e += NCT) vbl_n[e] = 0;
       for (int e = tid; e < BM * NW; e += NCT) (&tbit[0][0])[e] = 0;
       for (int e = tid; e < BM; e += NCT) trow[e] = tden[e] = 0;
@@ -816,21 +829,60 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           }
           tc5::bar_sync(1, NCT);
         }
+        // a pass with no key adds nothing: with canonical digits already there, leave them
+        const bool keep = nkt == 0 && a.add_into && a.canon_in && !fused;
         const int d = dcol;
+        if constexpr (SC) {
+          // Finalized whole range.  Phase 1: an element whose column of the spill slot was not
+          // touched holds NUM = X 2^(Fv - 79) exactly in its three register digits and is rounded
+          // from that 128-bit integer; the others are listed.  Phase 2: all compute threads share
+          // the listed elements (canonical digits), so a few touched columns or rows do not hold
+          // whole warps on the long path.
+          EpiElem* elist = reinterpret_cast<EpiElem*>(smem_p + L::e_off);
   #pragma unroll
-        for (int r = 0; r < 4; r++) {
-          const int rl = rg * 4 + r, i = q0 + rl;
-          if (i >= a.Sq || d >= a.D) continue;
-          const bool touched = trow[rl] || ((tbit[rl][d >> 5] >> (d & 31)) & 1u);
+          for (int r = 0; r < 4; r++) {
+            const int rl = rg * 4 + r, i = q0 + rl;
+            if (i >= a.Sq || d >= a.D) continue;
+            if (trow[rl] || ((tbit[rl][d >> 5] >> (d & 31)) & 1u)) {
+              const int k = atomicAdd(&elist_n, 1);
+              elist[k] = EpiElem{rl, d, acc[r][0], acc[r][1], acc[r][2]};
+              continue;
+            }
+            const __int128 X = (__int128)acc[r][0] + (__int128)acc[r][1] * ((__int128)1 << 32) +
+                               (__int128)acc[r][2] * ((__int128)1 << 64);
+            bool neg;
+            uint64_t mm;
+            int ee;
+            const bool nz = idiv::i128_split_rn64(X, Fv[d] - 79, neg, mm, ee);
+            float o = 0.0f;   // RN64(NUM) = +0 over a positive DEN
+            if (fslow[rl]) {
+              o = __double2float_rn(__ddiv_rn(nz ? idiv::make_f64(neg, mm, ee) : 0.0, fden64[rl]));
+            } else if (nz) {
+              uint64_t qq;
+              int EE;
+              idiv::div_rn64(mm, ee, fdiv[rl], qq, EE);
+              o = __uint_as_float(idiv::rn32_bits(qq, EE, neg));
+            }
+            a.out[out_row(i) * a.D + d] = o;
+          }
+          tc5::bar_sync(1, NCT);
+        }
+        // canonical digits of one element (row rl, column dd, register digits a0..a2): the stored
+        // digits with add_into, the spill slot's touched digits (cleared after), the register
+        // digits; then stored, or finalized
+        auto canonical = [&](int rl, int dd, long long a0, long long a1, long long a2) {
+          const int i = q0 + rl;
+          if (i >= a.Sq || dd >= a.D || keep) return;
+          const bool touched = trow[rl] || ((tbit[rl][dd >> 5] >> (dd & 31)) & 1u);
           long long* nrow = a.num + out_row(i) * NUM_NDIG * a.D;   // unused when fused
           long long dg[NUM_NDIG + 3];
   #pragma unroll
           for (int k = 0; k < NUM_NDIG + 3; k++) dg[k] = 0;
           if (a.add_into)
   #pragma unroll
-            for (int k = 0; k < NUM_NDIG; k++) dg[k] = __ldcg(nrow + (int64_t)k * a.D + d);
+            for (int k = 0; k < NUM_NDIG; k++) dg[k] = __ldcg(nrow + (int64_t)k * a.D + dd);
           if (touched) {   // this digit column of the slot was touched
-            long long* sp = slot_num(rl) + d;
+            long long* sp = slot_num(rl) + dd;
   #pragma unroll
             for (int k = 0; k < NUM_NDIG; k++) {
               dg[k] += __ldcg(sp + (size_t)k * DP);
@@ -840,8 +892,8 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           {
             unsigned __int128 M;
             bool neg;
-            digits3_to_u128(acc[r][0], acc[r][1], acc[r][2], M, neg);
-            add_u128_at(dg, M, neg, Fv[d] - 79 - NUM_E0);   // the accumulator's unit is 2^(Fv - 79)
+            digits3_to_u128(a0, a1, a2, M, neg);
+            add_u128_at(dg, M, neg, Fv[dd] - 79 - NUM_E0);   // the accumulator's unit is 2^(Fv - 79)
           }
           carry_digits(dg);
           long long top = dg[NUM_NDIG + 2];
@@ -870,14 +922,21 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
               idiv::div_rn64(mm, ee, fdiv[rl], qq, EE);
               o = __uint_as_float(idiv::rn32_bits(qq, EE, neg));
             }
-            a.out[out_row(i) * a.D + d] = o;
+            a.out[out_row(i) * a.D + dd] = o;
           } else {
   #pragma unroll
-            for (int k = 0; k < NUM_NDIG - 1; k++) nrow[(int64_t)k * a.D + d] = dg[k];
-            nrow[(int64_t)(NUM_NDIG - 1) * a.D + d] = top;
+            for (int k = 0; k < NUM_NDIG - 1; k++) nrow[(int64_t)k * a.D + dd] = dg[k];
+            nrow[(int64_t)(NUM_NDIG - 1) * a.D + dd] = top;
           }
+        };
+        if constexpr (SC) {
+          const EpiElem* el = reinterpret_cast<const EpiElem*>(smem_p + L::e_off);
+          for (int e = tid; e < elist_n; e += NCT) canonical(el[e].rl, el[e].d, el[e].a0, el[e].a1, el[e].a2);
+        } else {
+  #pragma unroll
+          for (int r = 0; r < 4; r++) canonical(rg * 4 + r, d, acc[r][0], acc[r][1], acc[r][2]);
         }
-        if (!fused)
+        if (!fused && !keep)
           for (int rl = tid; rl < nrows; rl += NCT) {
             long long t[DEN_NDIG];
             den_digits(rl, t);

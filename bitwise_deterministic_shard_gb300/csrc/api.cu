@@ -121,6 +121,10 @@ DceArgs make_dce(const da_matrix* x) {
 
 }  // namespace
 
+// da_accumulate with the internal canon_in flag (the sharded composition's own digits)
+int accumulate_range(const da_attn_desc* desc, const float* m, int64_t kv_lo, int64_t kv_hi, int64_t* num,
+                     int64_t* den, int add_into, int canon_in, void* ws, size_t ws_bytes, da_stream_t stream);
+
 #define DA_EXPORT __attribute__((visibility("default")))
 
 extern "C" {
@@ -164,6 +168,13 @@ DA_EXPORT int da_rowmax(const da_attn_desc* desc, int64_t kv_lo, int64_t kv_hi, 
 
 DA_EXPORT int da_accumulate(const da_attn_desc* desc, const float* m, int64_t kv_lo, int64_t kv_hi, int64_t* num,
                             int64_t* den, int add_into, void* ws, size_t ws_bytes, da_stream_t stream) {
+  return accumulate_range(desc, m, kv_lo, kv_hi, num, den, add_into, 0, ws, ws_bytes, stream);
+}
+
+}  // extern "C"
+
+int accumulate_range(const da_attn_desc* desc, const float* m, int64_t kv_lo, int64_t kv_hi, int64_t* num,
+                     int64_t* den, int add_into, int canon_in, void* ws, size_t ws_bytes, da_stream_t stream) {
   int e = check_desc(desc);
   if (e) return e;
   if (kv_lo < 0 || kv_hi < kv_lo || kv_hi > desc->k.S) return DA_EINVAL;
@@ -174,11 +185,14 @@ DA_EXPORT int da_accumulate(const da_attn_desc* desc, const float* m, int64_t kv
   AttnArgs a = make_args(desc);
   a.kv_lo = (int)kv_lo; a.kv_hi = (int)kv_hi;
   a.m_in = m; a.num = (long long*)num; a.den = (long long*)den; a.add_into = add_into ? 1 : 0;
+  a.canon_in = canon_in;
   KvPrep p = kv_prep_layout(ws, a.B, a.Hkv, a.Skv, a.D, 1);
   cudaStream_t st = (cudaStream_t)stream;
   if (launch_kv_prep(a, p, st) != cudaSuccess) return DA_ECUDA;
   return launched(launch_accumulate(a, p, st));
 }
+
+extern "C" {
 
 DA_EXPORT int da_compose_max(float* dst, const float* src, int64_t n, da_stream_t stream) {
   if (n < 0) return DA_EINVAL;
@@ -353,10 +367,12 @@ DA_EXPORT int da_det_attn_sharded(const da_attn_desc* desc, const int64_t* kv_sp
     if ((e = da_rowmax(desc, lo[s], hi[s], k == 0 ? m : m2, kv, kvb, stream))) return e;
     if (k > 0 && (e = da_compose_max(m, m2, rows, stream))) return e;
   }
-  // pass 2: shard digits with the global rowmax, composed by integer add (a sum reduce)
+  // pass 2: shard digits with the global rowmax, composed by integer add (a sum reduce); the
+  // digits already there are this call's own canonical digits, so a row with no key in a shard
+  // (causal masking) is left as it is
   for (int k = 0; k < nsplits; k++) {
     const int s = ord[k];
-    if ((e = da_accumulate(desc, m, lo[s], hi[s], num, den, k == 0 ? 0 : 1, kv, kvb, stream))) return e;
+    if ((e = accumulate_range(desc, m, lo[s], hi[s], num, den, k == 0 ? 0 : 1, 1, kv, kvb, stream))) return e;
   }
   return da_finalize(num, den, desc->q.B, desc->q.H, desc->q.S, desc->q.D, out, desc->dev_status, stream);
 }

@@ -20,6 +20,8 @@ struct AttnArgs {
   long long* num;                // [B, Hq, Sq, 15, D]
   long long* den;                // [B, Hq, Sq, 6]
   int add_into;
+  int canon_in;                  // with add_into: the digits already there are canonical, so a row with
+                                 // no key in [kv_lo, kv_hi) may be left as it is (no read-modify-write)
   int* status;                   // device status word (may be null)
   float* out;                    // non-null: the tensor-PV accumulate finalizes into out [B, Hq, Sq, D]
                                  // instead of writing digits (one key range, add_into == 0)

@@ -276,5 +276,30 @@ DA_HD bool digits_split_rn64(long long (&a)[N], int base, bool& neg, uint64_t& m
   return true;
 }
 
+// RN64 of X 2^lsb for a signed 128-bit integer X as a sign and m 2^e with m in [2^52, 2^53)
+// (the caller keeps X 2^lsb inside the normal binary64 range); false when X is zero.  The same
+// rounding as digits_split_rn64, for a value held in one 128-bit word.
+DA_HD bool i128_split_rn64(__int128 X, int lsb, bool& neg, uint64_t& m, int& e) {
+  if (X == 0) return false;
+  neg = X < 0;
+  const unsigned __int128 M = neg ? (unsigned __int128)0 - (unsigned __int128)X : (unsigned __int128)X;
+  const uint64_t hi = (uint64_t)(M >> 64), lo = (uint64_t)M;
+  const int lz = hi ? clz64(hi) : 64 + clz64(lo);
+  const unsigned __int128 W = M << lz;   // top bit at 127
+  const uint64_t t64 = (uint64_t)(W >> 64);
+  const bool sticky = (uint64_t)W != 0;
+  uint64_t mm = t64 >> 11;
+  const uint64_t rb = t64 & 0x7FF;
+  if (rb > 0x400 || (rb == 0x400 && (sticky || (mm & 1)))) mm += 1;
+  int ee = (127 - lz) - 52 + lsb;
+  if (mm >> 53) {
+    mm >>= 1;
+    ee += 1;
+  }
+  m = mm;
+  e = ee;
+  return true;
+}
+
 }  // namespace idiv
 }  // namespace detattn

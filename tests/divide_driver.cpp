@@ -68,6 +68,21 @@ int main(int argc, char** argv) {
       div_rn64(m53, e53, D, q, E);
       printf("%u %llu %d %u %u\n", b, (unsigned long long)md, ed, div_f32_rn32(mw, ew, D), rn32_bits(q, E, false));
     }
+  } else if (mode == 5) {   // RN64 of three lazy radix-2^32 digits as one 128-bit integer
+    for (long i = 0; i < n; i++) {
+      long long d[3];
+      int kind = rnd() % 4;
+      for (int k = 0; k < 3; k++) d[k] = (long long)(rnd() >> 2) - (1ll << 61);   // |d| < 2^62
+      if (kind == 1) d[2] = 0;
+      if (kind == 2) { d[1] = 0; d[2] = 0; d[0] = (long long)(rnd() >> 40) - (1ll << 23); }
+      if (kind == 3) { d[0] = (long long)(rnd() % 3) << 40; d[1] = -(long long)(rnd() % 2); d[2] = (long long)(rnd() % 2); }
+      if (i == 0) { d[0] = 0; d[1] = 0; d[2] = 0; }
+      int lsb = (int)(rnd() % 200) - 180;
+      __int128 X = (__int128)d[0] + (__int128)d[1] * ((__int128)1 << 32) + (__int128)d[2] * ((__int128)1 << 64);
+      bool neg = false; uint64_t m = 0; int e = 0;
+      bool nz = i128_split_rn64(X, lsb, neg, m, e);
+      printf("%lld %lld %lld %d | %d %d %llu %d\n", d[0], d[1], d[2], lsb, (int)nz, (int)neg, (unsigned long long)m, e);
+    }
   } else if (mode == 3) {   // f32 split
     for (long i = 0; i < n; i++) {
       uint32_t b = (uint32_t)rnd() & 0x7FFFFFFFu;

@@ -84,3 +84,18 @@ def test_binary32_numerator_division(drv):
             ref = struct.unpack("<I", struct.pack("<f", np.float32(q64)))[0]
             assert fast == ref, line
 
+
+def test_i128_rn64(drv):
+    """RN64 of d0 + d1 2^32 + d2 2^64 (three lazy radix-2^32 digits as one 128-bit integer)
+    times 2^lsb, the tensor-PV epilogue's form for the elements that touched no spill digit,
+    against CPython's correctly rounded int -> float conversion."""
+    for line in drv(5, 20000):
+        a, r = line.split("|")
+        d0, d1, d2, lsb = map(int, a.split())
+        nz, neg, m, e = map(int, r.split())
+        X = d0 + (d1 << 32) + (d2 << 64)
+        if X == 0:
+            assert nz == 0, line
+            continue
+        mm, ee = math.frexp(float(abs(X)))               # int -> float rounds to nearest even
+        assert (nz, neg, m, e) == (1, int(X < 0), int(mm * 2 ** 53), ee - 53 + lsb), line
