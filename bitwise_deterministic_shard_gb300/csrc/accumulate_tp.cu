@@ -122,10 +122,11 @@ __device__ __forceinline__ void pv_block_mmas(uint32_t pv, uint32_t den, const u
   tc5::mma_bf16(den, wa, ones, idesc_den, 1u);
 }
 
-// two f16 values b0, b1 in [0, 255] from the pattern (0x64 b1 0x64 b0): (1024 + b) - 1024
-__device__ __forceinline__ uint32_t f16_pair_from_biased(uint32_t h) {
+// two f16 values b0, b1 in [0, 255] from the pattern (0x64 b1 0x64 b0): (1024 + b) - 1024; with
+// bal, (1024 + b) - 1152 = b - 128 (a balanced digit)
+__device__ __forceinline__ uint32_t f16_pair_from_biased(uint32_t h, bool bal = false) {
   uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64006400u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(bal ? 0x64806480u : 0x64006400u));
   return r;
 }
 
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   unsigned char* Vst = smem_p + L::v_off;
   unsigned char* Wp = smem_p + L::w_off;
   __shared__ __align__(8) uint64_t kfull[NSK], kempty[NSK], sfull, sempty, vfull[NVB], vempty[NVB], wready[2],
-      pvdone[2], pvfree[2], fin;
+      pvdone[2], pvfree[2], wfree[2], fin;
   __shared__ uint32_t tmem_s;
   __shared__ int Fq[BM], Fv[DP];
   __shared__ unsigned char qfit[BM], qlon[BM];
@@ -336,6 +337,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
     for (int s = 0; s < 2; s++) {
       tc5::mbar_init(&pvdone[s], 1);
       tc5::mbar_init(&pvfree[s], NCW);
+      tc5::mbar_init(&wfree[s], 1);   // SC: the MMAs that read weight-plane buffer s have completed
     }
     tc5::mbar_init(&fin, 3);   // the score issuers and the PV issuer
     s_abort = 0;
@@ -374,6 +376,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   if (warp >= NCW) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 32;" ::: "memory");
     uint32_t tc = 0;   // key tiles of earlier passes
+    uint32_t pc = 0;   // SC: PV buffer pairs of earlier passes
     for (int pass = 0; pass < npass; pass++) {
       const int q0 = (pass == 0 ? ntq - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
       const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
@@ -416,18 +419,26 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           tc5::fence_after();   // the DEN accumulators were zeroed before the pass barrier
           for (int t = 0; t < nkt && !s_abort; t++) {
             const uint32_t tt = tc + t, bsel = tt & 1;
+            // SC: PV sums of two tiles share one buffer (a pair: tiles 2 m and 2 m + 1 of the pass)
+            const bool first = !SC || (t & 1) == 0, last = !SC || (t & 1) == 1 || t == nkt - 1;
+            const uint32_t pb = SC ? (pc & 1) : bsel;
+            const uint32_t pidx = SC ? pc : tt;   // pair (tile) index of the buffer's uses
             if (!tc5::mbar_wait(&wready[bsel], (tt >> 1) & 1, &s_abort, 64)) break;   // weight digits of tile tt
-            if (tt >= 2 && !tc5::mbar_wait(&pvfree[bsel], ((tt - 2) >> 1) & 1, &s_abort, 64)) break;   // buffer drained
+            if (first && pidx >= 2 && !tc5::mbar_wait(&pvfree[pb], ((pidx - 2) >> 1) & 1, &s_abort, 64)) break;   // buffer drained
             tc5::fence_after();
             for (int kb = 0; kb < NKB && !s_abort; kb++) {
               const uint32_t g = tt * NKB + kb, sl = g % NVB;
               if (!tc5::mbar_wait(&vfull[sl], (g / NVB) & 1, &s_abort, 32)) break;
               tc5::fence_after();
-              pv_block_mmas(tmem + L::PV_COL + bsel * L::PV_BUF, tmem + L::DEN_COL, Vst + sl * VP_BLOCK,
+              pv_block_mmas(tmem + L::PV_COL + pb * L::PV_BUF, tmem + L::DEN_COL, Vst + sl * VP_BLOCK,
                             Wp + bsel * L::w_buf + (size_t)kb * NWP * L::w_blk, ones, IDESC_P, IDESC_D);
               tc5::commit(&vempty[sl]);
             }
-            tc5::commit(&pvdone[bsel]);
+            if (SC) tc5::commit(&wfree[bsel]);   // weight-plane buffer bsel may be rewritten once these complete
+            if (last) {
+              tc5::commit(&pvdone[pb]);
+              if (SC) pc++;
+            }
           }
         }
       }
@@ -442,6 +453,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   } else {   // ---------------- compute warps ----------------
     asm volatile("setmaxnreg.inc.sync.aligned.u32 112;" ::: "memory");
     uint32_t tc = 0;   // key tiles of earlier passes
+    uint32_t pcd = 0;   // SC: the next PV buffer pair to drain (pairs of earlier passes included)
     for (int pass = 0; pass < npass; pass++) {
       const int q0 = (pass == 0 ? ntq - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
       const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
@@ -482,7 +494,8 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           tc5::fence_after();
           return ok;
         };
-        // fold the PV accumulators of one tile into the integer digits, zero them, release them
+        // fold the PV accumulators of one tile (SC: of one pair of tiles) into the integer digits,
+        // zero them, release them
         auto drain = [&](uint32_t tt) {
           drain_pv<SC>(acc, lane_base + L::PV_COL + (tt & 1) * L::PV_BUF + rg * 4, &pvdone[tt & 1], &pvfree[tt & 1],
                        (tt >> 1) & 1, &s_abort, lane);
@@ -614,12 +627,33 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
             words[e][1] = low ? hw : lo;
             words[e][2] = low ? 0u : hw;   // digits 8 and 9: below 2^16
           }
+          if constexpr (SC) {
+            // Balanced digits: W + sum_{s<9} 128 256^s, byte s minus 128 for s < 9 (in [-128, 127],
+            // carries included), byte 9 as is (at most 129): the same W, products at most
+            // 129 * 128, so two tiles of PV sums stay below 2^24 (the drains run every two tiles).
   #pragma unroll
-          for (int e = 0; e < 4; e++) {   // DEN digits 8-9: one exact warp sum per row (32 x 2^16 < 2^21)
-            const unsigned s89 = __reduce_add_sync(0xFFFFFFFFu, words[e][2]);
-            if (lane == 0 && s89) atomicAdd((unsigned long long*)&denT[rg * 4 + e][2], (unsigned long long)s89);
+            for (int e = 0; e < 4; e++) {
+              const uint64_t lo64 = ((uint64_t)words[e][1] << 32) | words[e][0];
+              const uint64_t b64 = lo64 + 0x8080808080808080ull;
+              words[e][0] = (uint32_t)b64;
+              words[e][1] = (uint32_t)(b64 >> 32);
+              words[e][2] += 0x80u + (b64 < lo64 ? 1u : 0u);   // below 2^16 + 2^8
+            }
+  #pragma unroll
+            for (int e = 0; e < 4; e++) {   // DEN digits 8-9: (byte 8 - 128) + 256 byte 9, one exact warp sum per row
+              const int s89 = __reduce_add_sync(0xFFFFFFFFu, (int)(words[e][2] & 0xFFFFu) - 128);
+              if (lane == 0 && s89) atomicAdd((unsigned long long*)&denT[rg * 4 + e][2], (unsigned long long)(long long)s89);
+            }
+          } else {
+  #pragma unroll
+            for (int e = 0; e < 4; e++) {   // DEN digits 8-9: one exact warp sum per row (32 x 2^16 < 2^21)
+              const unsigned s89 = __reduce_add_sync(0xFFFFFFFFu, words[e][2]);
+              if (lane == 0 && s89) atomicAdd((unsigned long long*)&denT[rg * 4 + e][2], (unsigned long long)s89);
+            }
           }
-          {   // plane s of this key's 4 rows: 4 f16 values, contiguous in the MN-major block (one 8-byte store)
+          // SC: the buffer's previous tile (tt - 2) may still be read by its PV MMAs (drains run per pair)
+          const bool wok = !SC || tt < 2 || warp_wait(&wfree[bsel], ((tt - 2) >> 1) & 1);
+          if (wok) {   // plane s of this key's 4 rows: 4 f16 values, contiguous in the MN-major block (one 8-byte store)
             unsigned char* wdst = wbuf + (size_t)(dcol / VKEYS) * NWP * L::w_blk + tc5::mn_off(rg * 4, dcol % VKEYS);
   #pragma unroll
             for (int q = 0; q < 3; q++) {
@@ -632,8 +666,9 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
                 const int s = 4 * q + k;
                 if (s < NWP) {
                   const uint32_t sel = (k & 1) ? 0x4342u : 0x4140u;   // (0x64, byte of row 1, 0x64, byte of row 0)
-                  const uint32_t h01 = f16_pair_from_biased(__byte_perm(a01[k >> 1], 0x64646464u, sel));
-                  const uint32_t h23 = f16_pair_from_biased(__byte_perm(a23[k >> 1], 0x64646464u, sel));
+                  const bool bal = SC && s < NWP - 1;   // digits 0-8 balanced, digit 9 as is
+                  const uint32_t h01 = f16_pair_from_biased(__byte_perm(a01[k >> 1], 0x64646464u, sel), bal);
+                  const uint32_t h23 = f16_pair_from_biased(__byte_perm(a23[k >> 1], 0x64646464u, sel), bal);
                   *reinterpret_cast<uint2*>(wdst + s * L::w_blk) = make_uint2(h01, h23);
                 }
               }
@@ -642,8 +677,12 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           tc5::fence_async_smem();   // the weight digit planes are read by the tensor cores
           __syncwarp();
           if (lane == 0) tc5::mbar_arrive(&wready[bsel]);
-          // ---- the previous tile's PV products are done by now (or soon): fold them in ----
-          if (t >= 1) drain(tt - 1);
+          // ---- the previous tile's (SC: pair's) PV products are done by now (or soon): fold them in ----
+          if constexpr (SC) {
+            if (t >= 2 && (t & 1) == 0) drain(pcd++);   // the pair of tiles t - 2, t - 1
+          } else {
+            if (t >= 1) drain(tt - 1);
+          }
           // ---- this warp's products outside the window: exact int64 atomics into the output digits ----
           if (__ballot_sync(0xFFFFFFFFu, tiny != 0)) {
   #pragma unroll
@@ -735,7 +774,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
             }
           }
         }
-        if (nkt > 0) drain(tc + nkt - 1);
+        if (nkt > 0) drain(SC ? pcd++ : tc + nkt - 1);
         if (lane < min(vbl_n[warp], NVBL)) {   // listed keys, one per lane: products of their V elements below the window
           const int jj = vbl_j[warp][lane];
           const float4 wl = vbl_w[warp][lane];
