@@ -446,6 +446,143 @@ def _time_ms(fn, stream, flush, reps):
     return statistics.median(ts)
 
 
+KERNEL_CALLS = ("rowmax", "accumulate_digits", "compose_max", "compose_add", "normalize", "finalize",
+                "rowmax_d64", "accumulate_d64", "rowmax_d256", "accumulate_d256",
+                "dce_rowmax", "dce_denom_digits", "dce_finalize", "dce_reduce", "dce_backward")
+
+
+def run_kernels(args):
+    """One JSON line per C-ABI call, each timed alone with CUDA events on the launching stream
+    (L2 flushed before each timed call; median of --steps calls after --warmup): the
+    device kernels it launches, its algorithmic bytes (inputs read once, outputs written once)
+    or flops, and the achieved rate against the measured peak.  Attention calls run on the
+    long-context causal shape (S4096, --heads heads; D = 64 and 256 variants of the same shape
+    for the integer-pipe kernels), the digit calls on that shape's NUM/DEN digits, the
+    cross-entropy calls on --dce-rows tokens of the vocab-sharded shape (V128256 f32)."""
+    import bitwise_deterministic_shard_gb300 as da
+    want = KERNEL_CALLS if args.kernels == "all" else tuple(args.kernels.split(","))
+    bad = [k for k in want if k not in KERNEL_CALLS]
+    if bad:
+        raise SystemExit(f"unknown kernel call(s) {bad}; choose from {', '.join(KERNEL_CALLS)}")
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    pk = _peaks()
+    hbm = pk.get("hbm_gbs") or 6800.0
+    tfl = pk.get("bf16_tflops") or 1900.0
+
+    def emit(call, launches, workload, ms, nbytes=None, flops=None, note=None):
+        line = {"call": call, "kernels": launches, "workload": workload, "ms": ms}
+        if nbytes is not None:
+            line.update({"algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9,
+                         "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm})
+        if flops is not None:
+            line.update({"algorithmic_flops": flops, "achieved_tflops": flops / (ms * 1e-3) / 1e12,
+                         "bf16_frac": flops / (ms * 1e-3) / 1e12 / tfl})
+        if note:
+            line["note"] = note
+        print(json.dumps(line), flush=True)
+
+    def timed(fn):
+        for _ in range(max(args.warmup - 1, 0)):
+            fn()
+        return _time_ms(fn, stream, flush, args.steps)
+
+    def attn(D, heads):
+        w = W.long_context_causal()
+        w.D, w.Hq, w.Hkv = D, heads, heads
+        w.name = f"long-context causal B1 H{heads} S4096 D{D} bf16, 1% of K rows x8"
+        Q, K, V = w.tensors(dev)
+        ws = torch.empty(da.workspace_bytes(Q, K, V, True), dtype=torch.uint8, device=dev)
+        return w, Q, K, V, ws
+
+    attn_calls = [k for k in want if not k.startswith("dce_")]
+    if attn_calls:
+        w, Q, K, V, ws = attn(128, args.heads)
+        rows = w.B * w.Hq * w.S
+        io = (Q.numel() + K.numel() + V.numel()) * 2
+        m = da.rowmax(Q, K, causal=True, workspace=ws)
+        if "rowmax" in want:
+            t = timed(lambda: da.rowmax(Q, K, causal=True, out=m, workspace=ws))
+            emit("rowmax", ["prep_kv_kernel", "rowmax_tc_kernel"], w.name, t, flops=w.pairs * w.D * 2,
+                 note="flops: the pages' score work, P x D multiply-adds x 2")
+        num = torch.empty(w.B, w.Hq, w.S, da.NUM_NDIG, w.D, dtype=torch.int64, device=dev)
+        den = torch.empty(w.B, w.Hq, w.S, da.DEN_NDIG, dtype=torch.int64, device=dev)
+        da.accumulate(Q, K, V, m, causal=True, num=num, den=den, workspace=ws)
+        if "accumulate_digits" in want:
+            t = timed(lambda: da.accumulate(Q, K, V, m, causal=True, num=num, den=den, workspace=ws))
+            emit("accumulate_digits", ["prep_vcol_kernel", "prep_kv_kernel", "accumulate_tp_kernel"], w.name, t,
+                 flops=w.pairs * 2 * w.D * 2, note="flops: P x 2D exact multiply-adds x 2; NUM/DEN digits written")
+        digit_bytes = num.numel() * 8
+        if "compose_max" in want:
+            m2 = m.clone()
+            t = timed(lambda: da.compose_max(m2, m))
+            emit("compose_max", ["compose_max_kernel"], w.name + ": rowmax f32", t, nbytes=3 * m.numel() * 4,
+                 note="input fits in L2: launch-bound")
+        if "compose_add" in want or "normalize" in want:
+            num2 = num.clone()
+            if "compose_add" in want:
+                t = timed(lambda: da.compose_add(num2, num))
+                emit("compose_add", ["compose_add_kernel"], w.name + ": NUM digits", t, nbytes=3 * digit_bytes)
+            if "normalize" in want:
+                t = timed(lambda: da.normalize(num2))
+                emit("normalize", ["normalize_kernel"], w.name + ": NUM digits", t, nbytes=2 * digit_bytes)
+            del num2
+        if "finalize" in want:
+            out = torch.empty(w.B, w.Hq, w.S, w.D, dtype=torch.float32, device=dev)
+            t = timed(lambda: da.finalize(num, den, out=out))
+            emit("finalize", ["finalize_kernel"], w.name + ": NUM/DEN digits to f32", t,
+                 nbytes=digit_bytes + den.numel() * 8 + out.numel() * 4)
+            del out
+        del num, den, Q, K, V, ws, m
+        torch.cuda.empty_cache()
+        for D, heads, acc_kernel in ((64, args.heads, "accumulate_tc_kernel"),
+                                     (256, max(1, args.heads // 4), "accumulate_kernel")):
+            if f"rowmax_d{D}" not in want and f"accumulate_d{D}" not in want:
+                continue
+            w, Q, K, V, ws = attn(D, heads)
+            m = da.rowmax(Q, K, causal=True, workspace=ws)
+            if f"rowmax_d{D}" in want:
+                t = timed(lambda: da.rowmax(Q, K, causal=True, out=m, workspace=ws))
+                emit(f"rowmax_d{D}", ["prep_kv_kernel", "rowmax_tc_kernel"], w.name, t, flops=w.pairs * w.D * 2)
+            if f"accumulate_d{D}" in want:
+                num = torch.empty(w.B, w.Hq, w.S, da.NUM_NDIG, w.D, dtype=torch.int64, device=dev)
+                den = torch.empty(w.B, w.Hq, w.S, da.DEN_NDIG, dtype=torch.int64, device=dev)
+                t = timed(lambda: da.accumulate(Q, K, V, m, causal=True, num=num, den=den, workspace=ws))
+                emit(f"accumulate_d{D}", ["prep_vcol_kernel", "prep_kv_kernel", acc_kernel], w.name, t,
+                     flops=w.pairs * 2 * w.D * 2)
+                del num, den
+            del Q, K, V, ws, m
+            torch.cuda.empty_cache()
+    dce_calls = [k for k in want if k.startswith("dce_")]
+    if dce_calls:
+        w = W.vocab_sharded_ce()
+        w.N = args.dce_rows
+        w.name = f"vocab-sharded cross-entropy N{w.N} V{w.V} f32"
+        x, tg = w.tensors(dev)
+        nb = x.numel() * 4
+        m = da.dce_rowmax(x)
+        den = da.dce_denom_digits(x, m)
+        loss, denom = da.dce_finalize(den, x, tg, m)
+        if "dce_rowmax" in want:
+            t = timed(lambda: da.dce_rowmax(x, out=m))
+            emit("dce_rowmax", ["dce_rowmax_kernel"], w.name, t, nbytes=nb + w.N * 4)
+        if "dce_denom_digits" in want:
+            t = timed(lambda: da.dce_denom_digits(x, m, den=den))
+            emit("dce_denom_digits", ["dce_denom_kernel"], w.name, t, nbytes=nb + w.N * (4 + 48))
+        if "dce_finalize" in want:
+            t = timed(lambda: da.dce_finalize(den, x, tg, m))
+            emit("dce_finalize", ["dce_finalize_kernel"], w.name, t, nbytes=w.N * (48 + 4 + 8 + 4 + 4 + 8),
+                 note="per token: DEN digits, rowmax, target, target logit read; loss, denom written")
+        if "dce_reduce" in want:
+            t = timed(lambda: da.dce_reduce(loss, "mean"))
+            emit("dce_reduce", ["dce_reduce_kernel"], w.name, t, nbytes=w.N * 4, note="launch-bound")
+        if "dce_backward" in want:
+            g = torch.ones((), dtype=torch.float32, device=dev)
+            t = timed(lambda: da.dce_backward(x, tg, m, denom, g, reduction="mean"))
+            emit("dce_backward", ["dce_backward_kernel"], w.name, t, nbytes=2 * nb + w.N * 16)
+
+
 def run_configs(args):
     """One JSON line per workload of the pages: fused and sharded device times (CUDA events, L2
     flushed between calls), exact attention MACs/s, the oracle's host time and core count, SHA-256
@@ -542,6 +679,9 @@ def main():
     ap.add_argument("--no-sharded", action="store_true", help="skip the sharded ring-step timings")
     ap.add_argument("--configs", action="store_true",
                     help="per-workload table (fused / sharded times, oracle, SHA-256, parity) instead of the step")
+    ap.add_argument("--kernels", nargs="?", const="all", default=None,
+                    help="time each C-ABI call alone instead of the step: 'all' or a comma list of "
+                         + ", ".join(KERNEL_CALLS))
     ap.add_argument("--heads", type=int, default=16, help="heads of the workload (16 = the metric workload)")
     ap.add_argument("--dce-rows", type=int, default=4096,
                     help="tokens of the cross-entropy leg (4096 = the vocab-sharded workload)")
@@ -555,6 +695,9 @@ def main():
         torch.distributed.init_process_group("gloo")
     if args.configs:
         run_configs(args)
+        return
+    if args.kernels:
+        run_kernels(args)
         return
     try:
         if args.impl == "reference":
