@@ -97,7 +97,14 @@ __global__ void __launch_bounds__(DEN_THREADS, 6) dce_denom_kernel(const DceArgs
     float x = __fsub_rn(__uint_as_float(u), m);
     if (x != x) { st |= ST_NONFINITE; return; }
     if (x > 0.0f) { st |= ST_VIOLATION; x = 0.0f; }
-    den_add(A, __float_as_uint(exp32_det_nb(x)));   // x <= 0, not NaN
+    // the weight's bits: exp32_det's p with k added to its exponent (exact for k >= -125),
+    // the full evaluation for the deepest weights (x < -86.6)
+    int k;
+    const uint32_t pbits = __float_as_uint(exp32_det_poly(x >= -104.0f ? x : 0.0f, k));
+    uint32_t wb;
+    if (x >= -104.0f && k >= -125) wb = pbits + ((uint32_t)k << 23);
+    else wb = __float_as_uint(exp32_det_nb(x));   // x <= 0, not NaN
+    den_add(A, wb);
   }, [&] { den_guard(A); });
   den_flush(A);
   long long dg[6] = {A.d[0], A.d[1], A.d[2], A.d[3], A.d[4], A.d[5]};
@@ -160,18 +167,25 @@ __global__ void dce_finalize_kernel(const DceArgs a) {
 //   dLogits = RN32(go * g),  go = grad[i] ("none"), grad[0] ("sum"), RN32(RN64(grad[0] / N))
 // ("mean").  A logit above the rowmax is clamped like the forward's (violation flag); NaN
 // propagates.  Streaming: 2 B or 4 B read and 2 B or 4 B written per logit; one CTA covers
-// BW_CHUNK columns of one row, consecutive threads consecutive columns.
+// BW_CHUNK columns of one row.  The quotient is rounded straight to binary32 from the row's
+// reciprocal (idiv::div_f32_rn32_direct) and divided exactly only when that rounding is not
+// certain (a quotient within about 2^-27 binary32 ulp of a half-way point, or a subnormal one).
 constexpr int BW_THREADS = 256, BW_PER = 32, BW_CHUNK = BW_THREADS * BW_PER, BW_BATCH = 8;
 
-template <int DT>
+// VEC: the row and the output row start on 16-byte boundaries and hold a whole number of
+// 16-byte vectors, so each thread moves its logits as 16-byte loads and stores (f32: 8 x 4,
+// bf16: 4 x 8), the loads all issued before the arithmetic.
+template <int DT, bool VEC>
 __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs a, const float* __restrict__ grad,
                                                                   int reduction, void* __restrict__ dlogits) {
   using T = typename In<DT>::T;
   __shared__ idiv::Divisor sdiv;
   __shared__ int sslow;
+  __shared__ float sgo;
   const int64_t nch = (a.V + BW_CHUNK - 1) / BW_CHUNK;
   const int64_t i = blockIdx.x / nch, c0 = (blockIdx.x % nch) * BW_CHUNK;
   const T* __restrict__ row = (const T*)a.x + i * a.rs + c0;
+  T* __restrict__ orow = (T*)dlogits + i * a.V + c0;
   const int nv = (int)(a.V - c0 < BW_CHUNK ? a.V - c0 : BW_CHUNK);
   const float m = a.m_in[i];
   const double d64 = a.denom[i];
@@ -181,32 +195,44 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
     const bool ok = d64 > 0.0 && idiv::split_f64((uint64_t)__double_as_longlong(d64), dm, de);
     sslow = !ok;   // zero, subnormal, negative, infinite or NaN denominators divide in binary64
     if (ok) sdiv = idiv::make_divisor(dm, de);
+    float g0 = reduction == 0 ? grad[i] : grad[0];
+    if (reduction == 2) g0 = __double2float_rn(__ddiv_rn((double)g0, (double)a.N));   // once per CTA
+    sgo = g0;
   }
   __syncthreads();
   const idiv::Divisor Dv = sdiv;
   const bool slow = sslow;
-  const int64_t tg = a.targets[i] - a.v_base - c0;   // the target's column within this chunk (any value)
-  float go = reduction == 0 ? grad[i] : grad[0];
-  if (reduction == 2) go = __double2float_rn(__ddiv_rn((double)go, (double)a.N));
+  const float go = sgo;
+  const int64_t tg64 = a.targets[i] - a.v_base - c0;   // the target's column within this chunk (any value)
+  const int tg = tg64 >= 0 && tg64 < nv ? (int)tg64 : -1;
   int st = 0;
-  for (int k0 = 0; k0 < BW_PER; k0 += BW_BATCH) {
-    uint32_t u[BW_BATCH];
-#pragma unroll
-    for (int j = 0; j < BW_BATCH; j++) {   // the batch's loads first, all in flight together
-      const int v = (k0 + j) * BW_THREADS + threadIdx.x;
-      u[j] = v < nv ? In<DT>::bits(row, v) : 0u;
+  // dLogits of the logit with bits u in column v of the chunk.  Fast path: the weight as
+  // exp32_det's p 2^k (exact for k >= -125: mantissa of p, exponent of p + k) and its quotient
+  // rounded straight from the row's reciprocal; the exact division and the special cases
+  // (NaN, deep or zero weights, special denominators, an uncertain rounding) otherwise.
+  auto one = [&](uint32_t u, int v) -> float {
+    float x = __fsub_rn(__uint_as_float(u), m);
+    if (x > 0.0f) {
+      st |= ST_VIOLATION;
+      x = 0.0f;
     }
-#pragma unroll
-    for (int j = 0; j < BW_BATCH; j++) {
-      const int v = (k0 + j) * BW_THREADS + threadIdx.x;
-      if (v >= nv) continue;
-      float x = __fsub_rn(__uint_as_float(u[j]), m);
-      if (x > 0.0f) {
-        st |= ST_VIOLATION;
-        x = 0.0f;
-      }
+    int k;
+    const float pp = exp32_det_poly(x >= -104.0f ? x : 0.0f, k);   // NaN x: NaN p, rejected below
+    const uint32_t pbits = __float_as_uint(pp);
+    const int bew = (int)(pbits >> 23) + k;                           // the weight's biased exponent
+    bool ok = !slow && x >= -104.0f && k >= -125;
+    uint32_t q = 0;
+    if (ok) {
+      const uint32_t mw = (pbits & 0x7FFFFFu) | 0x800000u;
+      bool sure;
+      q = idiv::div_f32_rn32_direct(mw, bew - 150, Dv, sure);
+      ok = sure;
+    }
+    float p;
+    if (ok) {
+      p = __uint_as_float(q);
+    } else {
       const float w = x != x ? x : exp32_det_nb(x);
-      float p;
       if (!slow && w > 0.0f) {
         uint32_t mw;
         int ew;
@@ -217,12 +243,56 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
       } else {
         p = __double2float_rn(__ddiv_rn((double)w, d64));   // NaN weight or a special denominator
       }
-      const float g = v == tg ? __fsub_rn(p, 1.0f) : p;
-      const float o = __fmul_rn(go, g);
-      if constexpr (DT == 0)
-        ((float*)dlogits)[i * a.V + c0 + v] = o;
-      else
-        ((__nv_bfloat16*)dlogits)[i * a.V + c0 + v] = __float2bfloat16_rn(o);
+    }
+    const float g = v == tg ? __fsub_rn(p, 1.0f) : p;
+    return __fmul_rn(go, g);
+  };
+  if constexpr (VEC) {
+    constexpr int EV = 16 / (int)sizeof(T), NV = BW_PER / EV;
+    const uint4* __restrict__ src = reinterpret_cast<const uint4*>(row);
+    uint4* __restrict__ dst = reinterpret_cast<uint4*>(orow);
+    uint4 q[NV];
+#pragma unroll
+    for (int k = 0; k < NV; k++) {   // every load in flight before the arithmetic
+      const int gv = k * BW_THREADS + threadIdx.x;
+      q[k] = gv * EV < nv ? __ldcs(src + gv) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < NV; k++) {
+      const int gv = k * BW_THREADS + threadIdx.x;
+      if (gv * EV >= nv) continue;   // nv is a multiple of EV here
+      const uint32_t wd[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int t = 0; t < 4; t++) {
+        if constexpr (DT == 0) {
+          o[t] = __float_as_uint(one(wd[t], gv * 4 + t));
+        } else {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(one(wd[t] << 16, gv * 8 + 2 * t),
+                                                         one(wd[t] & 0xFFFF0000u, gv * 8 + 2 * t + 1));
+          o[t] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+      }
+      __stcs(dst + gv, make_uint4(o[0], o[1], o[2], o[3]));
+    }
+  } else {
+    for (int k0 = 0; k0 < BW_PER; k0 += BW_BATCH) {
+      uint32_t u[BW_BATCH];
+#pragma unroll
+      for (int j = 0; j < BW_BATCH; j++) {   // the batch's loads first, all in flight together
+        const int v = (k0 + j) * BW_THREADS + threadIdx.x;
+        u[j] = v < nv ? In<DT>::bits(row, v) : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < BW_BATCH; j++) {
+        const int v = (k0 + j) * BW_THREADS + threadIdx.x;
+        if (v >= nv) continue;
+        const float o = one(u[j], v);
+        if constexpr (DT == 0)
+          ((float*)orow)[v] = o;
+        else
+          ((__nv_bfloat16*)orow)[v] = __float2bfloat16_rn(o);
+      }
     }
   }
   report(a.status, st);
@@ -279,8 +349,16 @@ cudaError_t launch_dce_backward(const DceArgs& a, const float* grad, int reducti
   if (a.N <= 0 || a.V <= 0) return cudaSuccess;
   const int64_t blocks = a.N * ((a.V + BW_CHUNK - 1) / BW_CHUNK);
   if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidValue;
-  if (a.dtype == 0) dce_backward_kernel<0><<<(unsigned)blocks, BW_THREADS, 0, st>>>(a, grad, reduction, dlogits);
-  else dce_backward_kernel<1><<<(unsigned)blocks, BW_THREADS, 0, st>>>(a, grad, reduction, dlogits);
+  const int esz = a.dtype == 0 ? 4 : 2;
+  const bool vec = (reinterpret_cast<uintptr_t>(a.x) & 15) == 0 && (reinterpret_cast<uintptr_t>(dlogits) & 15) == 0 &&
+                   (a.rs * esz) % 16 == 0 && (a.V * esz) % 16 == 0;
+  if (a.dtype == 0) {
+    if (vec) dce_backward_kernel<0, true><<<(unsigned)blocks, BW_THREADS, 0, st>>>(a, grad, reduction, dlogits);
+    else dce_backward_kernel<0, false><<<(unsigned)blocks, BW_THREADS, 0, st>>>(a, grad, reduction, dlogits);
+  } else {
+    if (vec) dce_backward_kernel<1, true><<<(unsigned)blocks, BW_THREADS, 0, st>>>(a, grad, reduction, dlogits);
+    else dce_backward_kernel<1, false><<<(unsigned)blocks, BW_THREADS, 0, st>>>(a, grad, reduction, dlogits);
+  }
   return cudaGetLastError();
 }
 

@@ -193,6 +193,32 @@ DA_HD uint32_t div_f32_rn32(uint32_t mw, int ew, const Divisor& D) {
   return rn32_bits(m, e, false);
 }
 
+// RN32 bits of RN64(w / d) straight from the reciprocal, for w = mw 2^ew (mw in [2^23, 2^24))
+// and the prepared divisor, when that is certain; ok = false asks for div_f32_rn32.
+// R = 2^64 + v = floor((2^128 - 1) / dn) lies in (2^128 / dn - 1 - 2^-63, 2^128 / dn), so
+// T = mw 2^128 / dn lies in (mw R, mw R + 2^24) and T' = T / 2^32 in (Y, Y + 1.01) with
+// Y = floor(mw R / 2^32) = mw 2^32 + mw v_hi + floor(mw v_lo / 2^32) (two 32 x 32 products;
+// 56 or 57 bits).  Y's top 32 bits yh (shifted right once when Y has 57 bits, the dropped bit
+// going to the top of yl) hold the 24 kept bits, yl the 32 below them; the rounding is
+// certain when yl is more than 64 from the half-way point 2^31: neither T''s uncertainty
+// (below 2 units of Y) nor the binary64 rounding before it (at most 8 units, which could only
+// matter by landing on the half-way point) can then change it.  Subnormal, zero and
+// overflowing results also take the exact path.  32-bit operations after the products.
+DA_HD uint32_t div_f32_rn32_direct(uint32_t mw, int ew, const Divisor& D, bool& ok) {
+  const uint64_t Y = ((uint64_t)mw << 32) + (uint64_t)mw * (uint32_t)(D.v >> 32) +
+                     (uint32_t)(((uint64_t)mw * (uint32_t)D.v) >> 32);
+  uint32_t yh = (uint32_t)(Y >> 32), yl = (uint32_t)Y;
+  int be = ew - D.e + 97;   // biased exponent of yh 2^(ew - D.e - 53) for yh in [2^23, 2^24)
+  if (yh >> 24) {
+    yl = (yl >> 1) | (yh << 31);
+    yh >>= 1;
+    be += 1;
+  }
+  ok = (uint32_t)((int32_t)(yl ^ 0x80000000u) + 64) > 128u && be >= 1 && be <= 253;   // |yl - 2^31| > 64
+  const uint32_t M = yh + (yl > 0x80000000u ? 1u : 0u);   // 2^24 carries into the exponent below
+  return ((uint32_t)(be - 1) << 23) + M;
+}
+
 // A binary64's magnitude as m 2^e with m in [2^52, 2^53); false for zero, subnormal,
 // infinity or NaN (the callers route those through their slow path).
 DA_HD bool split_f64(uint64_t bits, uint64_t& m, int& e) {

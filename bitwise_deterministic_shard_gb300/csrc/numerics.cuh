@@ -81,13 +81,26 @@ __device__ __forceinline__ float exp32_det(float x) {
 // exp32_det without branches, for x <= 0 or x = -inf (not NaN): the same operations in the
 // same order as exp32_det, the special cases taken by selects, so the caller's independent
 // evaluations can interleave.
+__device__ __forceinline__ float exp32_det_poly(float xx, int& k);
 __device__ __forceinline__ float exp32_det_nb(float x) {
   const bool under = x < -104.0f;
   const float xx = under ? 0.0f : x;
+  int k;
+  const float p = exp32_det_poly(xx, k);
+  const bool sub = k < -126;
+  const float res = __fmul_rn(p, __uint_as_float((uint32_t)(k + (sub ? 64 : 0) + 127) << 23));
+  const float out = sub ? __fmul_rn(res, 0x1p-64f) : res;
+  return under ? 0.0f : out;
+}
+
+// exp32_det's reduction and polynomial for -104 <= xx <= 0: returns p and k with
+// exp32_det(xx) = RN32(p 2^k).  p lies in (0.7, 1.5), so for k >= -125 the product is a
+// normal binary32 and exp32_det(xx) is p 2^k exactly (p's mantissa, p's exponent + k).
+__device__ __forceinline__ float exp32_det_poly(float xx, int& k) {
   const float L2E = 0x1.715476p+0f, C1 = 0x1.62e4p-1f, C2 = 0x1.7f7d1cp-20f, MAGIC = 12582912.0f;
   const float t = __fmul_rn(xx, L2E);
   const float tr = __fadd_rn(t, MAGIC);
-  const int k = __float_as_int(tr) - 0x4B400000;
+  k = __float_as_int(tr) - 0x4B400000;
   const float kf = __fsub_rn(tr, MAGIC);
   const float r1 = __fmaf_rn(-kf, C1, xx);
   const float r = __fmaf_rn(-kf, C2, r1);
@@ -99,10 +112,7 @@ __device__ __forceinline__ float exp32_det_nb(float x) {
   p = __fmaf_rn(p, r, 0.5f);
   p = __fmaf_rn(p, r, 1.0f);
   p = __fmaf_rn(p, r, 1.0f);
-  const bool sub = k < -126;
-  const float res = __fmul_rn(p, __uint_as_float((uint32_t)(k + (sub ? 64 : 0) + 127) << 23));
-  const float out = sub ? __fmul_rn(res, 0x1p-64f) : res;
-  return under ? 0.0f : out;
+  return p;
 }
 
 // exact small-integer <-> binary32 conversions on the FP32/integer pipes (|v| <= 2^22)

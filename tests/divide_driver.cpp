@@ -83,6 +83,37 @@ int main(int argc, char** argv) {
       bool nz = i128_split_rn64(X, lsb, neg, m, e);
       printf("%lld %lld %lld %d | %d %d %llu %d\n", d[0], d[1], d[2], lsb, (int)nz, (int)neg, (unsigned long long)m, e);
     }
+  } else if (mode == 6) {   // the direct binary32 quotient against the exact one
+    for (long i = 0; i < n; i++) {
+      uint32_t b;
+      uint64_t md = (rnd() >> 11) | (1ull << 52);
+      int ed = (int)(rnd() % 40) - 8;
+      const int kind = (int)(i % 4);
+      if (kind == 0) {   // weights exp-like in (0, 1]: exponent spread over [-40, 0]
+        b = ((uint32_t)(127 - (int)(rnd() % 41)) << 23) | ((uint32_t)rnd() & 0x7FFFFFu);
+      } else if (kind == 1) {   // any positive normal or subnormal binary32 (wide exponents)
+        b = (uint32_t)rnd() & 0x7FFFFFFFu;
+        if ((b >> 23) == 0xFF || b == 0) b = 0x3F800000u;
+        ed = (int)(rnd() % 400) - 200;
+      } else if (kind == 2) {   // quotients within about 2^-53 of a binary32 half-way point
+        b = ((uint32_t)(120 + (int)(rnd() % 8)) << 23) | ((uint32_t)rnd() & 0x7FFFFFu);
+        const uint32_t mw = (b & 0x7FFFFFu) | 0x800000u;
+        const uint64_t odd = ((rnd() >> 40) & 0x7FFFFFull) * 2 + 1 + (1ull << 24);   // 2M + 1, 25 bits
+        unsigned __int128 num = (unsigned __int128)(2ull * mw) << 52;
+        uint64_t q = (uint64_t)(num / odd);
+        if (!(q >> 52)) q = (uint64_t)((num << 1) / odd);
+        md = q + (uint64_t)(rnd() % 3) - 1;
+        if (!(md >> 52) || (md >> 53)) md = q;
+      } else {   // power-of-two and all-ones divisors
+        b = ((uint32_t)(100 + (int)(rnd() % 28)) << 23) | ((uint32_t)rnd() & 0x7FFFFFu);
+        md = (rnd() & 1) ? (1ull << 52) : ((1ull << 53) - 1);
+      }
+      Divisor D = make_divisor(md, ed);
+      uint32_t mw; int ew; split_f32_24(b, mw, ew);
+      bool ok = false;
+      const uint32_t fast = div_f32_rn32_direct(mw, ew, D, ok);
+      printf("%u %llu %d %d %u %u\n", b, (unsigned long long)md, ed, (int)ok, fast, div_f32_rn32(mw, ew, D));
+    }
   } else if (mode == 3) {   // f32 split
     for (long i = 0; i < n; i++) {
       uint32_t b = (uint32_t)rnd() & 0x7FFFFFFFu;

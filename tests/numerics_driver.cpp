@@ -1,6 +1,6 @@
 // Host driver for the device numerics of the CUDA path (csrc/numerics.cuh, compiled for the
 // host through cuda_host_shim.h): reads raw inputs from stdin, writes raw outputs to stdout.
-//   mode 0: binary32 x        -> exp32_det(x), exp32_det_nb(x)            (binary32 bits)
+//   mode 0: binary32 x        -> exp32_det(x), exp32_det_nb(x), p 2^k from exp32_det_poly (bits)
 //   mode 1: (int64 T, int32 F) -> cr32_scaled(T, F), cr32_scaled_nb(T, F) (bits), its special flag,
 //           cr32_scaled_cvt(T, F) (bits), its special flag
 //   mode 2: 15 int64 digits    -> digits_rn64<15>(digits, -320)            (binary64)
@@ -30,8 +30,16 @@ int main(int argc, char** argv) {
   const int mode = atoi(argv[1]);
   if (mode == 0) {
     for (float x : read_all<float>()) {
-      const uint32_t r[2] = {__float_as_uint(exp32_det(x)), x != x ? 0u : __float_as_uint(exp32_det_nb(x))};
-      fwrite(r, 4, 2, stdout);
+      // third: p 2^k assembled from exp32_det_poly's p and k (the bits of p with k added to its
+      // exponent) where k >= -125, else all ones
+      uint32_t pk = 0xFFFFFFFFu;
+      if (x == x && x >= -104.0f) {
+        int k;
+        const uint32_t pb = __float_as_uint(exp32_det_poly(x, k));
+        if (k >= -125) pk = pb + ((uint32_t)k << 23);
+      }
+      const uint32_t r[3] = {__float_as_uint(exp32_det(x)), x != x ? 0u : __float_as_uint(exp32_det_nb(x)), pk};
+      fwrite(r, 4, 3, stdout);
     }
   } else if (mode == 1) {
     const std::vector<long long> in = read_all<long long>();   // pairs (T, F)

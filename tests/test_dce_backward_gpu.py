@@ -52,7 +52,7 @@ def _assert_same(got, want, what):
 @cuda
 @pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("reduction", ["none", "sum", "mean"])
-@pytest.mark.parametrize("V", [1, 517, 5003])
+@pytest.mark.parametrize("V", [1, 12, 517, 4096, 5003, 8200])   # 12, 4096, 8200: 16-byte rows (vector path)
 def test_backward_matches_oracle(da, orc, dt, reduction, V):
     g = torch.Generator().manual_seed(60 + V)
     N = 37

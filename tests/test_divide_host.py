@@ -99,3 +99,29 @@ def test_i128_rn64(drv):
             continue
         mm, ee = math.frexp(float(abs(X)))               # int -> float rounds to nearest even
         assert (nz, neg, m, e) == (1, int(X < 0), int(mm * 2 ** 53), ee - 53 + lsb), line
+
+
+def test_direct_binary32_quotient(drv):
+    """div_f32_rn32_direct (the dLogits fast path): whenever it reports success its bits equal
+    the exact division's, and every fourth case is also checked against RN32(RN64(w / d))
+    computed with CPython's exact arithmetic.  Quotients within about 2^-53 of a binary32
+    half-way point must take the exact path, and for weights like the backward's
+    (exponents in [-40, 0], divisors of ordinary size) the fallback stays rare."""
+    taken = {0: [0, 0], 1: [0, 0], 2: [0, 0], 3: [0, 0]}
+    for k, line in enumerate(drv(6, 80000)):
+        b, md, ed, ok, fast, exact = map(int, line.split())
+        kind = k % 4
+        taken[kind][0] += 1
+        taken[kind][1] += ok
+        if ok:
+            assert fast == exact, line
+        if k % 4 == 0 or kind == 2:
+            w = Fraction(struct.unpack("<f", struct.pack("<I", b))[0])
+            q = w / (Fraction(md) * Fraction(2) ** ed)
+            q64 = q.numerator / q.denominator
+            assert exact == struct.unpack("<I", struct.pack("<f", np.float32(q64)))[0], line
+            if kind == 2 and ok:   # certain only when far from the half-way point
+                qf = Fraction(struct.unpack("<f", struct.pack("<I", fast))[0])
+                assert abs(q - qf) < Fraction(struct.unpack("<f", struct.pack("<I", fast + 1))[0]) - qf, line
+    assert taken[0][1] >= 0.999 * taken[0][0], taken      # exp-like weights: almost never the exact path
+    assert taken[2][1] <= 0.01 * taken[2][0], taken       # near half-way points: the exact path

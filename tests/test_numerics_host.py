@@ -40,12 +40,17 @@ def test_exp32_det_equals_the_oracle(drv, oracle_native):
         -rng.random(200_000) * 1e-3,                                        # near 0
         np.array([0.0, -0.0, -104.0, -103.97, -104.0001, -np.inf, -1e-45, -1.17549435e-38, np.nan]),
     ]).astype(np.float32)
-    got = drv(0, x, np.uint32, 2)
+    got = drv(0, x, np.uint32, 3)
     want = oracle_native.exp32_det_many(x).view(np.uint32)
     nan = np.isnan(x)
     assert np.array_equal(got[~nan, 0], want[~nan])
     assert np.all(np.isnan(got[nan, 0].view(np.float32)))
     assert np.array_equal(got[~nan, 1], got[~nan, 0])                      # the branch-free twin
+    # the split form the cross-entropy backward uses: exp32_det = p 2^k exactly for k >= -125,
+    # which holds for every x down to about -86.6 (so all but the deepest weights)
+    have = got[:, 2] != 0xFFFFFFFF
+    assert np.array_equal(got[have, 2], want[have])
+    assert np.all(have[~nan & (x >= -86.6)])
 
 
 def test_cr32_scaled_is_the_correctly_rounded_binary32(drv):
