@@ -97,14 +97,14 @@ __global__ void __launch_bounds__(DEN_THREADS, 6) dce_denom_kernel(const DceArgs
     float x = __fsub_rn(__uint_as_float(u), m);
     if (x != x) { st |= ST_NONFINITE; return; }
     if (x > 0.0f) { st |= ST_VIOLATION; x = 0.0f; }
-    // the weight's bits: exp32_det's p with k added to its exponent (exact for k >= -125),
-    // the full evaluation for the deepest weights (x < -86.6)
+    // the weight is exp32_det's p 2^k (exact for k >= -125): for w >= 2^-31 its mantissa goes
+    // straight into the private word (den_add's first case, without forming w); smaller
+    // weights take den_add with the full evaluation
     int k;
     const uint32_t pbits = __float_as_uint(exp32_det_poly(x >= -104.0f ? x : 0.0f, k));
-    uint32_t wb;
-    if (x >= -104.0f && k >= -125) wb = pbits + ((uint32_t)k << 23);
-    else wb = __float_as_uint(exp32_det_nb(x));   // x <= 0, not NaN
-    den_add(A, wb);
+    const int sh = (int)(pbits >> 23) + k - 96;
+    if (x >= -104.0f && sh >= 0) A.U += (uint64_t)((pbits & 0x7FFFFFu) | 0x800000u) << sh;
+    else den_add(A, __float_as_uint(exp32_det_nb(x)));   // x <= 0, not NaN
   }, [&] { den_guard(A); });
   den_flush(A);
   long long dg[6] = {A.d[0], A.d[1], A.d[2], A.d[3], A.d[4], A.d[5]};
