@@ -40,10 +40,11 @@ UNIT = "MAC/s"
 
 
 # DRAM bytes (read + write) of one accumulate launch at the metric workload: dram__bytes_read.sum +
-# dram__bytes_write.sum of the 4-head case of the same kernel (`python bench.py --heads 4 --dce-rows 256
-# --steps 1 --warmup 1 --no-cpu-baseline` under ncu, -k regex:accumulate_tp -s 1 -c 1) scaled by 4 (the
-# traffic is per head).  None whenever the kernel has changed since that capture.
-ACC_TRAFFIC_PER_LAUNCH = None
+# dram__bytes_write.sum (189.43 MB + 7.04 MB) of the 4-head case of the same kernel (`python bench.py
+# --heads 4 --dce-rows 256 --steps 1 --warmup 1 --no-cpu-baseline --no-sharded` under ncu, -k
+# regex:accumulate_tp -s 1 -c 1) scaled by 4 (the traffic is per head: the score cache, the V digit
+# planes and the output of each head).  None whenever the kernel has changed since that capture.
+ACC_TRAFFIC_PER_LAUNCH = 4 * (189_431_552 + 7_042_816)
 
 
 def _peaks():
@@ -358,20 +359,22 @@ def run_ours(args, rank, world, local_rank):
     value = macs * world / (ms * 1e-3)
     e2e_val = macs * world / (statistics.mean(e2e_ms) * 1e-3)
     # Roofline of the dominant kernel (accumulate + finalize), on the algorithmic basis: per unmasked
-    # (query, key) pair, D score multiply-adds and D PV multiply-adds (exact), 2 flop each, over the
-    # kernel's event time, against the measured dense bf16 tensor peak (the exact products run on the
-    # tensor cores as integer digit products).  Two further views of the same kernel:
+    # (query, key) pair, D exact PV multiply-adds, 2 flop each (the pair's D score multiply-adds run
+    # in pass 1, which hands the exact score over through the score cache), over the kernel's event
+    # time, against the measured dense bf16 tensor peak (the exact products run on the tensor cores
+    # as integer digit products).  Two further views:
     #  - mma_util: the MMA work the kernel actually issues for its digit decomposition (per 128-key tile
     #    of 16 query rows: 24 PV MMAs M128 N160 K16 and 8 DEN MMAs M128 N16 K16, plus 32 score MMAs
     #    M128 N64 K16 when the scores are recomputed instead of read from pass 1's cache) against the
     #    same peak;
-    #  - int_pipe: the exact multiply-adds per second against the integer pipe's rate of exact
-    #    32 x 32 -> 64-bit multiply-adds, measured by the library's probe kernel in this run (the metric's
-    #    "% of binding INT pipe peak"; FP64 is not used on the path).
+    #  - int_pipe: the whole path's exact multiply-adds per second (D score + D PV per pair, each once,
+    #    over the step time) against the integer pipe's rate of exact 32 x 32 -> 64-bit multiply-adds,
+    #    measured by the library's probe kernel in this run (the metric's "% of binding INT pipe peak":
+    #    what an exact integer-pipe implementation could reach at best).
     pk = _peaks()
     sm_clock = (ck or {}).get("sm_mhz") or pk.get("clocks_under_load", {}).get("sm_mhz_median") or 1447.0
     acc_ms = statistics.mean(k_acc)
-    alg_macs = w.pairs * 2 * w.D                                         # per launch
+    alg_macs = w.pairs * w.D                                             # per launch: PV
     achieved = 2.0 * alg_macs / (acc_ms * 1e-3) / 1e12                   # TFLOP/s
     cached = L.da_score_cache_bytes(P.ref()) > 0
     tile_macs = (0 if cached else 32 * 128 * 64 * 16) + 24 * 128 * 160 * 16 + 8 * 128 * 16 * 16
@@ -381,11 +384,11 @@ def run_ours(args, rank, world, local_rank):
     peak_src = "measured burst bf16 (MEASURED_PEAKS.json)" if pk.get("bf16_tflops") else "fallback 1.9 PFLOP/s bf16"
     int_rate = da.probe_int_mac_rate()
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
-    int_pipe = {"achieved_exact_macs_per_s": alg_macs / (acc_ms * 1e-3),
-                "method_exact_macs_per_s": w.pairs * 3 * w.D / (acc_ms * 1e-3),
+    int_pipe = {"achieved_exact_macs_per_s": macs / (ms * 1e-3),
                 "peak_exact_macs_per_s": int_rate,
                 "peak_per_clock_per_sm": int_rate / (n_sm * sm_clock * 1e6),
-                "frac": alg_macs / (acc_ms * 1e-3) / int_rate,
+                "frac": macs / (ms * 1e-3) / int_rate,
+                "basis": "the step's exact multiply-adds (D score + D PV per unmasked pair) over the step time",
                 "peak_basis": "mad.wide.s32 (exact 32 x 32 -> 64-bit multiply-add) issue rate over all SMs, "
                               "measured by da_probe_int_mac in this run"}
     line = {
@@ -396,13 +399,13 @@ def run_ours(args, rank, world, local_rank):
                    "input_dtype": "bf16", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (512 MiB write, outside the step events)",
                    "attn_macs_per_step": macs, "pairs_per_step": w.pairs},
-        "method_macs_per_s": w.pairs * 3 * w.D * world / (ms * 1e-3),
         "kernels_ms": {"rowmax": statistics.mean(k_rowmax), "accumulate_finalize": acc_ms},
         "score_cache_bytes": int(L.da_score_cache_bytes(P.ref())),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": ACC_TRAFFIC_PER_LAUNCH if args.heads == 16 else None,
                      "kernel": "accumulate",
-                     "algorithmic": f"{w.pairs} unmasked pairs x 2D exact multiply-adds x 2 flop per launch",
+                     "algorithmic": f"{w.pairs} unmasked pairs x D exact PV multiply-adds x 2 flop per launch "
+                                    "(the D score multiply-adds per pair run in pass 1)",
                      "peak_basis": peak_src, "sm_mhz": sm_clock,
                      "mma_util": {"achieved": mma_tflops, "frac": mma_tflops / peak,
                                   "basis": f"{tiles} key tiles x {tile_macs} bf16/f16 MACs per launch "
