@@ -854,6 +854,35 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
           t[DEN_NDIG - 1] = top;
         };
         const bool fused = a.out != nullptr;   // finalize here: o = RN32(RN64(RN64(NUM) / RN64(DEN)))
+        const int d = dcol;
+        // SC, phase 1a (needs no divisor, so it overlaps the divisors' preparation): an element
+        // whose column of the spill slot was not touched holds NUM = X 2^(Fv - 79) exactly in its
+        // three register digits; its RN64 comes from that 128-bit integer.  Touched elements are
+        // listed for phase 2.
+        uint64_t p1m[4];
+        int p1e[4];
+        uint32_t p1nz = 0, p1neg = 0, p1live = 0;
+        if constexpr (SC) {
+          EpiElem* elist = reinterpret_cast<EpiElem*>(smem_p + L::e_off);
+  #pragma unroll
+          for (int r = 0; r < 4; r++) {
+            p1m[r] = 0;
+            p1e[r] = 0;
+            const int rl = rg * 4 + r, i = q0 + rl;
+            if (i >= a.Sq || d >= a.D) continue;
+            if (trow[rl] || ((tbit[rl][d >> 5] >> (d & 31)) & 1u)) {
+              const int k = atomicAdd(&elist_n, 1);
+              elist[k] = EpiElem{rl, d, acc[r][0], acc[r][1], acc[r][2]};
+              continue;
+            }
+            const __int128 X = (__int128)acc[r][0] + (__int128)acc[r][1] * ((__int128)1 << 32) +
+                               (__int128)acc[r][2] * ((__int128)1 << 64);
+            bool neg;
+            if (idiv::i128_split_rn64(X, Fv[d] - 79, neg, p1m[r], p1e[r])) p1nz |= 1u << r;
+            if (neg) p1neg |= 1u << r;
+            p1live |= 1u << r;
+          }
+        }
         if (fused) {
           for (int rl = tid; rl < nrows; rl += NCT) {
             long long t[DEN_NDIG];
@@ -870,41 +899,20 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
         }
         // a pass with no key adds nothing: with canonical digits already there, leave them
         const bool keep = nkt == 0 && a.add_into && a.canon_in && !fused;
-        const int d = dcol;
-        if constexpr (SC) {
-          // Finalized whole range.  Phase 1: an element whose column of the spill slot was not
-          // touched holds NUM = X 2^(Fv - 79) exactly in its three register digits and is rounded
-          // from that 128-bit integer; the others are listed.  Phase 2: all compute threads share
-          // the listed elements (canonical digits), so a few touched columns or rows do not hold
-          // whole warps on the long path.
-          EpiElem* elist = reinterpret_cast<EpiElem*>(smem_p + L::e_off);
+        if constexpr (SC) {   // phase 1b: the untouched elements' quotients
   #pragma unroll
           for (int r = 0; r < 4; r++) {
-            const int rl = rg * 4 + r, i = q0 + rl;
-            if (i >= a.Sq || d >= a.D) continue;
-            if (trow[rl] || ((tbit[rl][d >> 5] >> (d & 31)) & 1u)) {
-              const int k = atomicAdd(&elist_n, 1);
-              elist[k] = EpiElem{rl, d, acc[r][0], acc[r][1], acc[r][2]};
-              continue;
-            }
-            const __int128 X = (__int128)acc[r][0] + (__int128)acc[r][1] * ((__int128)1 << 32) +
-                               (__int128)acc[r][2] * ((__int128)1 << 64);
-            bool neg;
-            uint64_t mm;
-            int ee;
-            const bool nz = idiv::i128_split_rn64(X, Fv[d] - 79, neg, mm, ee);
+            if (!((p1live >> r) & 1u)) continue;
+            const int rl = rg * 4 + r;
+            const bool nz = (p1nz >> r) & 1u, neg = (p1neg >> r) & 1u;
             float o = 0.0f;   // RN64(NUM) = +0 over a positive DEN
-            if (fslow[rl]) {
-              o = __double2float_rn(__ddiv_rn(nz ? idiv::make_f64(neg, mm, ee) : 0.0, fden64[rl]));
-            } else if (nz) {
-              uint64_t qq;
-              int EE;
-              idiv::div_rn64(mm, ee, fdiv[rl], qq, EE);
-              o = __uint_as_float(idiv::rn32_bits(qq, EE, neg));
-            }
-            a.out[out_row(i) * a.D + d] = o;
+            if (fslow[rl])
+              o = __double2float_rn(__ddiv_rn(nz ? idiv::make_f64(neg, p1m[r], p1e[r]) : 0.0, fden64[rl]));
+            else if (nz)
+              o = __uint_as_float(idiv::div_rn32(p1m[r], p1e[r], fdiv[rl], neg));
+            a.out[out_row(q0 + rl) * a.D + d] = o;
           }
-          tc5::bar_sync(1, NCT);
+          tc5::bar_sync(1, NCT);   // the element list is complete
         }
         // canonical digits of one element (row rl, column dd, register digits a0..a2): the stored
         // digits with add_into, the spill slot's touched digits (cleared after), the register
@@ -953,14 +961,10 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
             int ee;
             const bool nz = idiv::digits_split_rn64<NUM_NDIG>(t, NUM_E0, neg, mm, ee);
             float o = 0.0f;   // RN64(NUM) = +0 over a positive DEN
-            if (fslow[rl]) {
+            if (fslow[rl])
               o = __double2float_rn(__ddiv_rn(nz ? idiv::make_f64(neg, mm, ee) : 0.0, fden64[rl]));
-            } else if (nz) {
-              uint64_t qq;
-              int EE;
-              idiv::div_rn64(mm, ee, fdiv[rl], qq, EE);
-              o = __uint_as_float(idiv::rn32_bits(qq, EE, neg));
-            }
+            else if (nz)
+              o = __uint_as_float(idiv::div_rn32(mm, ee, fdiv[rl], neg));
             a.out[out_row(i) * a.D + dd] = o;
           } else {
   #pragma unroll

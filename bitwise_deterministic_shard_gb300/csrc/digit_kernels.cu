@@ -136,12 +136,8 @@ __global__ void __launch_bounds__(256) finalize_kernel(const long long* __restri
           uint64_t m;
           int en;
           o = 0.0f;   // RN64(NUM) = +0: +0 / DEN = +0
-          if (idiv::digits_split_rn64<NUM_NDIG>(a, NUM_E0, neg, m, en)) {
-            uint64_t q;
-            int E;
-            idiv::div_rn64(m, en, Dv, q, E);
-            o = __uint_as_float(idiv::rn32_bits(q, E, neg));
-          }
+          if (idiv::digits_split_rn64<NUM_NDIG>(a, NUM_E0, neg, m, en))
+            o = __uint_as_float(idiv::div_rn32(m, en, Dv, neg));
         }
         out[r * D + c] = o;
       }

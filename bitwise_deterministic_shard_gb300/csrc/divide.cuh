@@ -219,6 +219,36 @@ DA_HD uint32_t div_f32_rn32_direct(uint32_t mw, int ew, const Divisor& D, bool& 
   return ((uint32_t)(be - 1) << 23) + M;
 }
 
+// RN32 bits of RN64(n / d) straight from the reciprocal, for n = (-1)^neg mn 2^en (mn in
+// [2^52, 2^53)) and the prepared divisor, when that is certain; ok = false asks for div_rn64
+// and rn32_bits.  T = mn 2^128 / dn lies in (mn R, mn R + mn) with R = 2^64 + v, so T / 2^64
+// lies in (H, H + 2) for H = mn + floor(mn v / 2^64) (one 64 x 64 high product), which has 53
+// or 54 bits.  The 24 kept bits M and the s = 29 or 30 bits F below them decide the binary32
+// rounding unless F is within 64 of the half-way point: the binary64 rounding of the quotient
+// moves it by at most one unit of H, T''s uncertainty is below two.  Subnormal and
+// overflowing results also take the exact path.
+DA_HD uint32_t div_rn64_rn32_direct(uint64_t mn, int en, const Divisor& D, bool neg, bool& ok) {
+  const uint64_t H = mn + mul_hi(mn, D.v);
+  const int s = (H >> 53) ? 30 : 29;
+  const uint64_t M = H >> s, F = H & ((1ull << s) - 1), half = 1ull << (s - 1);
+  const int be = s + en - D.e + 97;   // biased exponent of M 2^(s + en - D.e - 53), M in [2^23, 2^24)
+  ok = F - half + 64 > 128 && be >= 1 && be <= 253;   // |F - half| > 64 (unsigned wrap below)
+  const uint32_t m = (uint32_t)M + (F > half ? 1u : 0u);   // 2^24 carries into the exponent below
+  return (neg ? 0x80000000u : 0u) | (((uint32_t)(be - 1) << 23) + m);
+}
+
+// RN32 bits of RN64(n / d), n = (-1)^neg mn 2^en: the direct rounding, the exact division when
+// that is not certain.
+DA_HD uint32_t div_rn32(uint64_t mn, int en, const Divisor& D, bool neg) {
+  bool ok;
+  const uint32_t r = div_rn64_rn32_direct(mn, en, D, neg, ok);
+  if (ok) return r;
+  uint64_t q;
+  int E;
+  div_rn64(mn, en, D, q, E);
+  return rn32_bits(q, E, neg);
+}
+
 // A binary64's magnitude as m 2^e with m in [2^52, 2^53); false for zero, subnormal,
 // infinity or NaN (the callers route those through their slow path).
 DA_HD bool split_f64(uint64_t bits, uint64_t& m, int& e) {

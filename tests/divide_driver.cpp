@@ -114,6 +114,33 @@ int main(int argc, char** argv) {
       const uint32_t fast = div_f32_rn32_direct(mw, ew, D, ok);
       printf("%u %llu %d %d %u %u\n", b, (unsigned long long)md, ed, (int)ok, fast, div_f32_rn32(mw, ew, D));
     }
+  } else if (mode == 7) {   // the direct binary32 rounding of a binary64 quotient against the exact one
+    for (long i = 0; i < n; i++) {
+      uint64_t mn = (rnd() >> 11) | (1ull << 52), md = (rnd() >> 11) | (1ull << 52);
+      int en = (int)(rnd() % 120) - 60, ed = (int)(rnd() % 120) - 60;
+      const int kind = (int)(i % 4);
+      if (kind == 1) {   // wide exponents: subnormal and overflowing quotients
+        en = (int)(rnd() % 600) - 300;
+        ed = (int)(rnd() % 300) - 150;
+      } else if (kind == 2) {   // quotients within about 2^-53 of a binary32 half-way point
+        const uint64_t odd = ((rnd() >> 40) & 0x7FFFFFull) * 2 + 1 + (1ull << 24);   // 2M + 1, 25 bits
+        unsigned __int128 num = (unsigned __int128)mn << 25;
+        uint64_t q = (uint64_t)(num / odd);
+        while (q >> 53) q >>= 1;
+        while (!(q >> 52)) q <<= 1;
+        md = q + (uint64_t)(rnd() % 5) - 2;
+        if (!(md >> 52) || (md >> 53)) md = q;
+      } else if (kind == 3) {   // exact quotients: power-of-two divisors, equal mantissas
+        if (rnd() & 1) md = 1ull << 52; else md = mn;
+      }
+      Divisor D = make_divisor(md, ed);
+      uint64_t q; int E; div_rn64(mn, en, D, q, E);
+      const bool neg = rnd() & 1;
+      bool ok = false;
+      const uint32_t fast = div_rn64_rn32_direct(mn, en, D, neg, ok);
+      printf("%llu %d %llu %d %d %d %u %u\n", (unsigned long long)mn, en, (unsigned long long)md, ed, (int)neg, (int)ok,
+             fast, rn32_bits(q, E, neg));
+    }
   } else if (mode == 3) {   // f32 split
     for (long i = 0; i < n; i++) {
       uint32_t b = (uint32_t)rnd() & 0x7FFFFFFFu;

@@ -125,3 +125,26 @@ def test_direct_binary32_quotient(drv):
                 assert abs(q - qf) < Fraction(struct.unpack("<f", struct.pack("<I", fast + 1))[0]) - qf, line
     assert taken[0][1] >= 0.999 * taken[0][0], taken      # exp-like weights: almost never the exact path
     assert taken[2][1] <= 0.01 * taken[2][0], taken       # near half-way points: the exact path
+
+
+def test_direct_binary32_of_binary64_quotient(drv):
+    """div_rn64_rn32_direct (the finalize epilogues' fast path): whenever it reports success its
+    bits equal rn32_bits(div_rn64(...)), which every fourth case also checks against
+    RN32(RN64(n / d)) from CPython's exact arithmetic; quotients within about 2^-53 of a binary32
+    half-way point must take the exact path, exact quotients must not."""
+    taken = [[0, 0] for _ in range(4)]
+    for k, line in enumerate(drv(7, 80000)):
+        mn, en, md, ed, neg, ok, fast, exact = map(int, line.split())
+        kind = k % 4
+        taken[kind][0] += 1
+        taken[kind][1] += ok
+        if ok:
+            assert fast == exact, line
+        if k % 4 == 0 or kind == 2:
+            q = Fraction(mn) * Fraction(2) ** en / (Fraction(md) * Fraction(2) ** ed)
+            q64 = q.numerator / q.denominator if abs(q) < 2 ** 1000 else float("inf")
+            ref = struct.unpack("<I", struct.pack("<f", np.float32(-q64 if neg else q64)))[0]
+            assert exact == ref, line
+    assert taken[0][1] == taken[0][0], taken     # ordinary quotients: always direct here
+    assert taken[2][1] == 0, taken               # near half-way points: always exact
+    assert taken[3][1] == taken[3][0], taken     # exact quotients are decided directly
