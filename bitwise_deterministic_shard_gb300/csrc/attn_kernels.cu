@@ -77,8 +77,13 @@ __device__ __forceinline__ void load_k_tile(const KvPrep& p, int64_t rowbase, in
 template <int DP>
 struct RowmaxTcLayout {
   static constexpr int BM = 32, NDS = DP / 16, NST = 8, TCOLS = 512, NEPI = 16, NISS = 2;
+  // warps: NEPI epilogue warps (four warpgroups) and one control warpgroup (the copy warp, NISS
+  // MMA issuers, one idle warp).  The control warpgroup runs on 32 registers a thread, the
+  // epilogue on 112 (640 x 96 at launch = 128 x 32 + 512 x 112); each role runs its own pass
+  // loop, opened by named barrier 2 (query operand ready) and closed by barrier 3.
   static constexpr int LOADER = NEPI, ISS0 = NEPI + 1;
-  static constexpr int THREADS = 32 * (NEPI + 1 + NISS);
+  static constexpr int THREADS = 32 * (NEPI + 4);
+  static_assert(NISS <= 2, "the control warpgroup holds the copy warp and the issuers");
   static_assert(NDS % NISS == 0, "issuers split the steps of a tile evenly");
   static constexpr size_t q_step = (size_t)NSLICE * BM * 32;   // one B block: 4 slices x BM rows x 16 bf16
   static constexpr size_t q_bytes = (size_t)NDS * q_step;
@@ -166,13 +171,58 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
   uint32_t g_base = 0, tcount = 0;   // ring steps of earlier passes; key tiles seen by this thread's role
   const int ntq = (a.Sq + BM - 1) / BM;
   const int npass = (a.causal && (int)blockIdx.x != ntq - 1 - (int)blockIdx.x) ? 2 : 1;
-  for (int pass = 0; pass < npass; pass++) {
-    const int q0 = (pass == 0 ? ntq - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
-    const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
-    const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
-    const uint32_t nsteps = (uint32_t)nkt * NDS;
+  if (warp >= NEPI) {   // ---------------- control warpgroup ----------------
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 32;" ::: "memory");
+    for (int pass = 0; pass < npass; pass++) {
+      const int q0 = (pass == 0 ? ntq - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
+      const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
+      const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
+      const uint32_t nsteps = (uint32_t)nkt * NDS;
+      tc5::bar_sync(2, L::THREADS);
+      if (warp == L::LOADER) {   // ---------------- bulk copies of the key operand tiles ----------------
+        if (lane == 0)
+          for (uint32_t ls = 0; ls < nsteps && !s_abort; ls++) {
+            const uint32_t g_step = g_base + ls, st = g_step % NST;
+            if (g_step >= NST && !tc5::mbar_wait(&empty[st], ((g_step / NST) - 1) & 1, &s_abort, 64)) break;
+            tc5::mbar_expect_tx(&full[st], KT_BLOCK);
+            tc5::bulk_g2s(Kst + st * KT_BLOCK, ktc + (size_t)ls * KT_BLOCK, KT_BLOCK, &full[st]);
+          }
+      } else if (warp < L::ISS0 + NISS) {   // ---------------- MMA issuers: steps ii, ii + NISS, ... ----------------
+        if (lane == 0) {
+          const uint32_t ii = warp - L::ISS0;
+          for (uint32_t ls = ii; ls < nsteps && !s_abort; ls += NISS) {
+            const uint32_t g_step = g_base + ls, st = g_step % NST;
+            const int k = (int)(ls % NDS);
+            if (!tc5::mbar_wait(&full[st], (g_step / NST) & 1, &s_abort)) break;
+            const uint32_t set = tcount & 1;
+            if (k == (int)ii && tcount >= 2 && !tc5::mbar_wait(&tempty[set], ((tcount - 2) >> 1) & 1, &s_abort)) break;
+            tc5::fence_after();
+            const uint64_t ka = tc5::desc(tc5::smem_addr(Kst + st * KT_BLOCK));
+            const uint64_t qa = tc5::desc(tc5::smem_addr(Qs + k * L::q_step));
+#pragma unroll
+            for (int sa = 0; sa < NSLICE; sa++)   // D offset by BM per key slice: the diagonals add themselves
+              tc5::mma_bf16(tmem + set * L::SETC + sa * BM, ka + (uint64_t)(sa * KTILE * 2), qa, IDESC, 1u);
+            tc5::commit(&empty[st]);
+            if (k + NISS >= NDS) {   // this issuer's last step of the tile
+              tc5::commit(&tfull[set]);
+              tcount++;
+            }
+          }
+        }
+      }
+      g_base += nsteps;
+      tc5::bar_sync(3, L::THREADS);
+    }
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 96;" ::: "memory");
+  } else {   // ---------------- epilogue warps: thread = key, 8 query rows ----------------
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 112;" ::: "memory");
+    for (int pass = 0; pass < npass; pass++) {
+      const int q0 = (pass == 0 ? ntq - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
+      const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
+      const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
+      const uint32_t nsteps = (uint32_t)nkt * NDS;
     // ---- query slices into the resident B operand ----
-    for (int r = warp; r < BM; r += L::THREADS / 32) {
+    for (int r = warp; r < BM; r += NEPI) {
       const int i = q0 + r;
       row_slices<DT, DP>(
           i < a.Sq ? qbase + (int64_t)i * a.qs[2] : nullptr, a.D,
@@ -181,43 +231,17 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
           },
           &Fq[r], &qfit[r], nf, lane, qlo[r], &qlon[r]);
     }
-    for (int r = tid; r < BM; r += L::THREADS) rkey[r] = float_key(neg_inf());
+    for (int r = tid; r < BM; r += NEPI * 32) rkey[r] = float_key(neg_inf());
     tc5::fence_async_smem();
-    __syncthreads();
-
-    if (warp == L::LOADER) {   // ---------------- bulk copies of the key operand tiles ----------------
-      if (lane == 0)
-        for (uint32_t ls = 0; ls < nsteps && !s_abort; ls++) {
-          const uint32_t g_step = g_base + ls, st = g_step % NST;
-          if (g_step >= NST && !tc5::mbar_wait(&empty[st], ((g_step / NST) - 1) & 1, &s_abort, 64)) break;
-          tc5::mbar_expect_tx(&full[st], KT_BLOCK);
-          tc5::bulk_g2s(Kst + st * KT_BLOCK, ktc + (size_t)ls * KT_BLOCK, KT_BLOCK, &full[st]);
-        }
-    } else if (warp >= L::ISS0) {   // ---------------- MMA issuers: steps ii, ii + NISS, ... ----------------
-      if (lane == 0) {
-        const uint32_t ii = warp - L::ISS0;
-        for (uint32_t ls = ii; ls < nsteps && !s_abort; ls += NISS) {
-          const uint32_t g_step = g_base + ls, st = g_step % NST;
-          const int k = (int)(ls % NDS);
-          if (!tc5::mbar_wait(&full[st], (g_step / NST) & 1, &s_abort)) break;
-          const uint32_t set = tcount & 1;
-          if (k == (int)ii && tcount >= 2 && !tc5::mbar_wait(&tempty[set], ((tcount - 2) >> 1) & 1, &s_abort)) break;
-          tc5::fence_after();
-          const uint64_t ka = tc5::desc(tc5::smem_addr(Kst + st * KT_BLOCK));
-          const uint64_t qa = tc5::desc(tc5::smem_addr(Qs + k * L::q_step));
-#pragma unroll
-          for (int sa = 0; sa < NSLICE; sa++)   // D offset by BM per key slice: the diagonals add themselves
-            tc5::mma_bf16(tmem + set * L::SETC + sa * BM, ka + (uint64_t)(sa * KTILE * 2), qa, IDESC, 1u);
-          tc5::commit(&empty[st]);
-          if (k + NISS >= NDS) {   // this issuer's last step of the tile
-            tc5::commit(&tfull[set]);
-            tcount++;
-          }
-        }
-      }
-    } else {   // ---------------- epilogue: thread = key, 8 query rows ----------------
+    tc5::bar_sync(2, L::THREADS);
+    {
       const int quarter = warp & 3, rg = warp >> 2;
       const int jl = 32 * quarter + lane;
+      // STORE: this thread's 8 rows all exist and fit their windows (then a tile whose keys all
+      // fit and lie at or below every one of these rows takes the short path below)
+      bool rows_clean = q0 + rg * 8 + 7 < a.Sq;
+#pragma unroll
+      for (int r = 0; r < 8; r++) rows_clean = rows_clean && qfit[rg * 8 + r];
       float mrun[8];
 #pragma unroll
       for (int r = 0; r < 8; r++) mrun[r] = neg_inf();
@@ -247,6 +271,35 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
           sc_ok = qt16 * SC_ROWS < a.Sq && t * KTILE < hi16 - a.kv_lo;
           if (sc_ok) sc_blk = a.scores + sc_block(a, b * a.Hq + h, qt16, t) * SC_BLOCK + jl * SC_ROWS + rr0;
         }
+        // short path (STORE): every pair of this warp's tile is valid and in its window, so each
+        // score is the combined dot rounded once; a subnormal or overflowing one takes the
+        // general rounding
+        const bool clean = STORE && __all_sync(0xFFFFFFFFu, rows_clean && vj && kf) &&
+                           (!a.causal || a.kv_lo + t * KTILE + KTILE - 1 <= q0 + rg * 8);
+        if (clean) {
+#pragma unroll
+          for (int hf = 0; hf < 2; hf++) {
+            float v[NDIAG][4];
+#pragma unroll
+            for (int c = 0; c < NDIAG; c++) tc5::ld_x4(lbase + set * L::SETC + c * BM + 4 * hf, v[c]);
+            tc5::ld_wait();
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+              const int r = 4 * hf + e, rl = rg * 8 + r;
+              const int E = Fq[rl] + Fk;
+              const long long T = combine_diag(v, e);
+              bool special;
+              float c = cr32_scaled_cvt(T, E, special);
+              if (special) c = cr32_scaled(T, E);
+              const float sc = __fmul_rn(a.scale32, c);
+              if (special && !(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
+              mrun[r] = sc > mrun[r] ? sc : mrun[r];
+              o[e] = sc;
+            }
+            if (sc_ok) *reinterpret_cast<float4*>(sc_blk + 4 * hf) = make_float4(o[0], o[1], o[2], o[3]);
+          }
+        } else
 #pragma unroll
         for (int hf = 0; hf < 2; hf++) {   // rows 4 hf .. 4 hf + 3: half the diagonal sums live at a time
           float v[NDIAG][4];   // diagonal sums of these 4 rows, exact
@@ -343,8 +396,7 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
         if (lane == 0) atomicMax(&rkey[rg * 8 + r], kmax);
       }
     }
-    g_base += nsteps;
-    __syncthreads();
+    tc5::bar_sync(1, NEPI * 32);   // every epilogue warp's maxima are in rkey
     if (tid < BM) {
       const int i = q0 + tid;
       float v = key_float(rkey[tid]);
@@ -353,8 +405,11 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
         a.m_out[((int64_t)b * a.Hq + h) * a.Sq + i] = v;
       }
     }
-  }   // pass
-  if (warp >= L::ISS0 && lane == 0) {   // every MMA issued has completed before TMEM is released
+    tc5::bar_sync(3, L::THREADS);
+    }
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
+  }
+  if (warp >= L::ISS0 && warp < L::ISS0 + NISS && lane == 0) {   // every MMA issued has completed before TMEM is released
     tc5::commit(&fin);
     tc5::mbar_wait(&fin, 0, &s_abort);
   }
