@@ -193,9 +193,9 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
           for (uint32_t ls = ii; ls < nsteps && !s_abort; ls += NISS) {
             const uint32_t g_step = g_base + ls, st = g_step % NST;
             const int k = (int)(ls % NDS);
-            if (!tc5::mbar_wait(&full[st], (g_step / NST) & 1, &s_abort)) break;
+            if (!tc5::mbar_wait(&full[st], (g_step / NST) & 1, &s_abort, 32)) break;
             const uint32_t set = tcount & 1;
-            if (k == (int)ii && tcount >= 2 && !tc5::mbar_wait(&tempty[set], ((tcount - 2) >> 1) & 1, &s_abort)) break;
+            if (k == (int)ii && tcount >= 2 && !tc5::mbar_wait(&tempty[set], ((tcount - 2) >> 1) & 1, &s_abort, 64)) break;
             tc5::fence_after();
             const uint64_t ka = tc5::desc(tc5::smem_addr(Kst + st * KT_BLOCK));
             const uint64_t qa = tc5::desc(tc5::smem_addr(Qs + k * L::q_step));
@@ -239,16 +239,25 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
       const int jl = 32 * quarter + lane;
       // STORE: this thread's 8 rows all exist and fit their windows (then a tile whose keys all
       // fit and lie at or below every one of these rows takes the short path below)
-      bool rows_clean = q0 + rg * 8 + 7 < a.Sq;
+      bool rows_clean = q0 + rg * 8 + 7 < a.Sq && fabsf(a.scale32) <= 1.0f;
+      int fqr[8], fqmin = 1 << 20, fqmax = -(1 << 20);
 #pragma unroll
-      for (int r = 0; r < 8; r++) rows_clean = rows_clean && qfit[rg * 8 + r];
+      for (int r = 0; r < 8; r++) {
+        rows_clean = rows_clean && qfit[rg * 8 + r];
+        fqr[r] = Fq[rg * 8 + r];
+        fqmin = min(fqmin, fqr[r]);
+        fqmax = max(fqmax, fqr[r]);
+      }
       float mrun[8];
 #pragma unroll
       for (int r = 0; r < 8; r++) mrun[r] = neg_inf();
+      // key meta words one tile ahead (the load's latency stays off the tile's path)
+      int mv_n = (nkt > 0 && a.kv_lo + jl < hi) ? p.kmeta[krow0 + a.kv_lo + jl] : 0;
       for (int t = 0; t < nkt; t++) {
         const int j = a.kv_lo + t * KTILE + jl;
         const bool vj = j < hi;
-        const int mv = vj ? p.kmeta[krow0 + j] : 0;
+        const int mv = mv_n;
+        mv_n = (t + 1 < nkt && j + KTILE < hi) ? p.kmeta[krow0 + j + KTILE] : 0;
         const uint32_t set = tcount & 1;
         bool tok = true;
         if (lane == 0) tok = tc5::mbar_wait(&tfull[set], (tcount >> 1) & 1, &s_abort, 128);
@@ -271,11 +280,14 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
           sc_ok = qt16 * SC_ROWS < a.Sq && t * KTILE < hi16 - a.kv_lo;
           if (sc_ok) sc_blk = a.scores + sc_block(a, b * a.Hq + h, qt16, t) * SC_BLOCK + jl * SC_ROWS + rr0;
         }
-        // short path (STORE): every pair of this warp's tile is valid and in its window, so each
-        // score is the combined dot rounded once; a subnormal or overflowing one takes the
-        // general rounding
-        const bool clean = STORE && __all_sync(0xFFFFFFFFu, rows_clean && vj && kf) &&
-                           (!a.causal || a.kv_lo + t * KTILE + KTILE - 1 <= q0 + rg * 8);
+        // short path (STORE): every row and every key of this warp's tile that takes part is in its
+        // window, and every E = Fq + Fk lies in [-126, 64]: then RN32(T) 2^E is a normal binary32
+        // for every nonzero T (|T| < 2^63), so the score is RN32(scale * RN32(T) 2^E) with no
+        // special case, and with |scale| <= 1 it is finite.  Masked pairs (a key past the range
+        // or, under causal masking, after the row) store 0 and leave the maximum alone.
+        const bool clean = STORE && __all_sync(0xFFFFFFFFu, rows_clean && (!vj || (kf && fqmin + Fk >= -126 && fqmax + Fk <= 64)));
+        const bool all_valid = a.kv_lo + t * KTILE + KTILE <= hi &&
+                               (!a.causal || a.kv_lo + t * KTILE + KTILE - 1 <= q0 + rg * 8);   // warp-uniform
         if (clean) {
 #pragma unroll
           for (int hf = 0; hf < 2; hf++) {
@@ -286,15 +298,12 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
             float o[4];
 #pragma unroll
             for (int e = 0; e < 4; e++) {
-              const int r = 4 * hf + e, rl = rg * 8 + r;
-              const int E = Fq[rl] + Fk;
-              const long long T = combine_diag(v, e);
-              bool special;
-              float c = cr32_scaled_cvt(T, E, special);
-              if (special) c = cr32_scaled(T, E);
-              const float sc = __fmul_rn(a.scale32, c);
-              if (special && !(fabsf(sc) <= 3.4028235e38f)) nf |= ST_NONFINITE;
-              mrun[r] = sc > mrun[r] ? sc : mrun[r];
+              const int r = 4 * hf + e;
+              const int E = fqr[r] + Fk;
+              const float c = __fmul_rn(__ll2float_rn(combine_diag(v, e)), __uint_as_float((uint32_t)(E + 127) << 23));
+              float sc = __fmul_rn(a.scale32, c);
+              if (!all_valid && !(vj && (!a.causal || j <= q0 + rg * 8 + r))) sc = 0.0f;   // masked (the row exists)
+              else mrun[r] = sc > mrun[r] ? sc : mrun[r];
               o[e] = sc;
             }
             if (sc_ok) *reinterpret_cast<float4*>(sc_blk + 4 * hf) = make_float4(o[0], o[1], o[2], o[3]);
