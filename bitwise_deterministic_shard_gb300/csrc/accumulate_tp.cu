@@ -869,12 +869,16 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
             p1m[r] = 0;
             p1e[r] = 0;
             const int rl = rg * 4 + r, i = q0 + rl;
-            if (i >= a.Sq || d >= a.D) continue;
-            if (trow[rl] || ((tbit[rl][d >> 5] >> (d & 31)) & 1u)) {
-              const int k = atomicAdd(&elist_n, 1);
-              elist[k] = EpiElem{rl, d, acc[r][0], acc[r][1], acc[r][2]};
-              continue;
+            const bool live = i < a.Sq && d < a.D;
+            const bool touched = live && (trow[rl] || ((tbit[rl][d >> 5] >> (d & 31)) & 1u));
+            const uint32_t tm = __ballot_sync(0xFFFFFFFFu, touched);   // one list slot reservation per warp and row
+            if (tm) {
+              int base = 0;
+              if (lane == 0) base = atomicAdd(&elist_n, __popc(tm));
+              base = __shfl_sync(0xFFFFFFFFu, base, 0);
+              if (touched) elist[base + __popc(tm & ((1u << lane) - 1u))] = EpiElem{rl, d, acc[r][0], acc[r][1], acc[r][2]};
             }
+            if (!live || touched) continue;
             const __int128 X = (__int128)acc[r][0] + (__int128)acc[r][1] * ((__int128)1 << 32) +
                                (__int128)acc[r][2] * ((__int128)1 << 64);
             bool neg;
