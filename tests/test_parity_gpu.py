@@ -443,3 +443,27 @@ def test_bounded_wait_gives_up_and_reports_timeout(da, orc):
     out = da.det_attn(Q.cuda(), K.cuda(), V.cuda(), causal=True)
     _, _, _, ref = orc.Attn(Q, K, V, True).forward_rows()
     assert_bits_equal(out.reshape(-1, 128), ref, "after a timed-out wait")
+
+
+@cuda
+@pytest.mark.parametrize("causal", [False, True])
+def test_score_cache_rare_paths_match_oracle(da, orc, causal):
+    """det_attn at D = 128 (score cache, tensor-PV accumulate, finalize in the epilogue) on the
+    inputs that reach its rare paths: a key far above the others (tiny weights for every
+    other key: the spill slot and the whole-row canonical path), V columns with one huge
+    element (the rest of the column falls below its fixed-point window: the listed V-bad
+    keys and the touched-column canonical path), and wide-exponent rows."""
+    Q, K, V = W.random_attn(311 + causal, 1, 2, 2, 300, 128, torch.bfloat16, causal, spread=20.0)
+    K, V = K.clone(), V.clone()
+    K[0, 0, 7] *= 2 ** 30
+    K[0, 1, 200] *= 2 ** 25
+    for d in (0, 17, 64, 127):
+        V[0, :, 11 + d, d] = 2.0 ** 30
+    st = da.new_status()
+    out = da.det_attn(Q.cuda(), K.cuda(), V.cuda(), causal=causal, status=st)
+    sh = da.det_attn_sharded(Q.cuda(), K.cuda(), V.cuda(), [100, 77, 123], causal=causal, order=[1, 2, 0], status=st)
+    torch.cuda.synchronize()
+    _, _, _, out_o = orc.Attn(Q, K, V, causal=causal).forward_rows()
+    assert da.read_status(st) & ~1 == 0
+    assert_bits_equal(out.reshape(-1, 128), out_o, "output")
+    assert_bits_equal(sh, out, "sharded vs fused")
