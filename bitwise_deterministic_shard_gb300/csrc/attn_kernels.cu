@@ -220,7 +220,6 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
       const int q0 = (pass == 0 ? ntq - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
       const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
       const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
-      const uint32_t nsteps = (uint32_t)nkt * NDS;
     // ---- query slices into the resident B operand ----
     for (int r = warp; r < BM; r += NEPI) {
       const int i = q0 + r;
