@@ -40,11 +40,11 @@ UNIT = "MAC/s"
 
 
 # DRAM bytes (read + write) of one accumulate launch at the metric workload: dram__bytes_read.sum +
-# dram__bytes_write.sum (189.43 MB + 7.04 MB) of the 4-head case of the same kernel (`python bench.py
+# dram__bytes_write.sum (189.20 MB + 6.43 MB) of the 4-head case of the same kernel (`python bench.py
 # --heads 4 --dce-rows 256 --steps 1 --warmup 1 --no-cpu-baseline --no-sharded` under ncu, -k
 # regex:accumulate_tp -s 1 -c 1) scaled by 4 (the traffic is per head: the score cache, the V digit
 # planes and the output of each head).  None whenever the kernel has changed since that capture.
-ACC_TRAFFIC_PER_LAUNCH = 4 * (189_431_552 + 7_042_816)
+ACC_TRAFFIC_PER_LAUNCH = 4 * (189_196_032 + 6_427_904)
 
 
 def _peaks():
