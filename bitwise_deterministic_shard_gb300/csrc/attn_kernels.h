@@ -49,7 +49,7 @@ size_t score_cache_bytes(int B, int Hq, int Sq, int Skv, int causal, int* sc_nkt
 // Prepared keys/values of one call's key range (prep_kernels.cu), rows indexed as
 // (b * Hkv + hk) * Skv + j.
 struct KvPrep {
-  uint16_t* ksl;     // bf16 digit slices [rows][4][DP]
+  uint16_t* ksl;     // bf16 digit slices [rows][4][DP] (DP == 256 only)
   unsigned char* ktc;   // the same slices as tensor-core operand tiles (below)
   int ntk;           // key tiles of KTILE rows per (b, hk) in ktc
   int* kmeta;        // [rows]: (F + 1024) | (fit << 16) | (low-limb count, or 15 for deep, << 17)

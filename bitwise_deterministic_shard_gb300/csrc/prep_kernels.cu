@@ -12,17 +12,19 @@
 
 namespace detattn {
 
-// column maxima of the V biased exponents over rows [lo, hi), atomically into vcol (zeroed)
+// column maxima of the V biased exponents over rows [lo, hi), atomically into vcol (zeroed);
+// VCOL_ROWS rows per CTA, so that a short range still spreads over many CTAs
+constexpr int VCOL_ROWS = 64;
 template <int DT>
 __global__ void __launch_bounds__(256) prep_vcol_kernel(const AttnArgs a, KvPrep p) {
   using T = typename In<DT>::T;
   const int hk = blockIdx.y, b = blockIdx.z;
   const T* vbase = (const T*)a.v + b * a.vs[0] + hk * a.vs[1];
   int* vcol = p.vcol + ((int64_t)b * a.Hkv + hk) * p.DP;
-  const int rows_per_block = 256;
-  const int j0 = a.kv_lo + blockIdx.x * rows_per_block, j1 = min(a.kv_hi, j0 + rows_per_block);
+  const int j0 = a.kv_lo + blockIdx.x * VCOL_ROWS, j1 = min(a.kv_hi, j0 + VCOL_ROWS);
   for (int d = threadIdx.x % 64; d < a.D; d += 64) {
     int em = 0;
+#pragma unroll 4
     for (int j = j0 + threadIdx.x / 64; j < j1; j += 4) {
       const uint32_t u = In<DT>::bits(vbase + (int64_t)j * a.vs[2], d);
       const int ex = (int)((u >> 23) & 0xFFu);
@@ -71,8 +73,12 @@ __global__ void __launch_bounds__(256) prep_kv_kernel(const AttnArgs a, KvPrep p
     const T* krow = (const T*)a.k + b * a.ks[0] + hk * a.ks[1] + (int64_t)j * a.ks[2];
     __shared__ int Fk_s[8];
     __shared__ unsigned char fit_s[8], lon_s[8];
-    uint16_t* ks = p.ksl + row * NSLICE * DP;
-    row_slices<DT, DP>(krow, a.D, [&](int q, int d, uint16_t v) { ks[q * DP + d] = v; store_tc(q, d, v); },
+    uint16_t* ks = p.ksl + row * NSLICE * DP;   // row-major slices: only the D = 256 kernel reads them
+    row_slices<DT, DP>(krow, a.D,
+                       [&](int q, int d, uint16_t v) {
+                         if constexpr (DP == 256) ks[q * DP + d] = v;
+                         store_tc(q, d, v);
+                       },
                        &Fk_s[warp], &fit_s[warp], nf, lane, p.klo + row * NLO, &lon_s[warp]);
     __syncwarp();
     if (lane == 0) {
@@ -141,7 +147,7 @@ size_t kv_prep_bytes(int B, int Hkv, int Skv, int D) {
   const int dp = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
   const size_t rows = (size_t)B * Hkv * Skv;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return up(rows * NSLICE * dp * 2) + up(rows * 4) + up(rows * NLO * 8) + up((size_t)B * Hkv * dp * 4) +
+  return up(dp == 256 ? rows * NSLICE * dp * 2 : 0) + up(rows * 4) + up(rows * NLO * 8) + up((size_t)B * Hkv * dp * 4) +
          up(rows * dp * 4) + up(rows * (dp / 32) * 4) + up(ktc_bytes(B, Hkv, Skv, dp)) + up(vtc_bytes(B, Hkv, Skv, dp)) +
          up(spill_bytes(dp));
 }
@@ -154,8 +160,8 @@ KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v) {
   KvPrep p;
   p.DP = dp;
   p.do_v = do_v;
-  p.ksl = (uint16_t*)c;
-  c += up(rows * NSLICE * dp * 2);
+  p.ksl = (uint16_t*)c;   // row-major key slices, for the D = 256 kernel only
+  c += up(dp == 256 ? rows * NSLICE * dp * 2 : 0);
   p.kmeta = (int*)c;
   c += up(rows * 4);
   p.klo = (int2*)c;
@@ -181,7 +187,7 @@ static cudaError_t launch_prep_t(const AttnArgs& a, const KvPrep& p, cudaStream_
   if (p.do_v) {   // the column exponents are read even when the range is empty
     cudaError_t e = cudaMemsetAsync(p.vcol, 0, sizeof(int) * (size_t)a.B * a.Hkv * DP, st);
     if (e != cudaSuccess) return e;
-    if (n > 0) prep_vcol_kernel<DT><<<dim3((n + 255) / 256, a.Hkv, a.B), 256, 0, st>>>(a, p);
+    if (n > 0) prep_vcol_kernel<DT><<<dim3((n + VCOL_ROWS - 1) / VCOL_ROWS, a.Hkv, a.B), 256, 0, st>>>(a, p);
   }
   const int padded = ((n + KTILE - 1) / KTILE) * KTILE;
   if (n > 0) prep_kv_kernel<DT, DP><<<dim3(padded / 8, a.Hkv, a.B), 256, 0, st>>>(a, p);
