@@ -72,6 +72,9 @@ def lib():
         L.da_workspace_bytes.argtypes = [D, _I32]
         L.da_workspace_bytes.restype = C.c_size_t
         L.da_det_attn.argtypes = [D, _P, _P, C.c_size_t, _P]
+        L.da_det_attn_host_workspace_bytes.argtypes = [D, _I32]
+        L.da_det_attn_host_workspace_bytes.restype = C.c_size_t
+        L.da_det_attn_host.argtypes = [D, _P, _I32, _P, C.c_size_t, _P]
         L.da_score_cache_bytes.argtypes = [D]
         L.da_score_cache_bytes.restype = C.c_size_t
         L.da_rowmax_cached.argtypes = [D, _P, _P, C.c_size_t, _P]
@@ -90,7 +93,7 @@ def lib():
         L.da_probe_int_mac_per_thread_iter.restype = C.c_int64
         L.da_probe_bounded_wait.argtypes = [_P, _P]
         for f in ("da_rowmax", "da_accumulate", "da_compose_max", "da_compose_add", "da_normalize", "da_finalize",
-                  "da_det_attn", "da_det_attn_sharded", "da_accumulate_finalize", "dce_rowmax", "dce_denom_digits", "dce_finalize",
+                  "da_det_attn", "da_det_attn_host", "da_det_attn_sharded", "da_accumulate_finalize", "dce_rowmax", "dce_denom_digits", "dce_finalize",
                   "dce_backward", "dce_reduce", "dce_forward_static", "da_probe_int_mac", "da_probe_bounded_wait",
                   "dce_finalize_shard", "dce_backward_shard", "da_rowmax_cached", "da_accumulate_finalize_cached"):
             getattr(L, f).restype = C.c_int
@@ -216,6 +219,54 @@ def det_attn(Q, K, V, causal=False, scale=None, out=None, workspace=None, status
     out = _out(out, torch.float32, (P.B, P.Hq, P.Sq, P.D), P.device, "out")
     ws = _workspace(P, 1, workspace)
     _check(lib().da_det_attn(P.ref(), _ptr(out), _ptr(ws), ws.numel(), _stream()), "det_attn")
+    return out
+
+
+def _host_tensor(t: torch.Tensor, name: str) -> _Tensor:
+    """Descriptor of a contiguous host [B, H, S, D] tensor (the host-buffer entry point)."""
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise DetAttnError(f"{name} must be a host (CPU) tensor for det_attn_host")
+    if t.dim() != 4 or not t.is_contiguous():
+        raise DetAttnError(f"{name} must be a contiguous [B, H, S, D] host tensor")
+    x = _Tensor()
+    x.ptr = t.data_ptr()
+    x.dtype = _dtype_code(t)
+    x.B, x.H, x.S, x.D = t.shape
+    for i in range(4):
+        x.stride[i] = t.stride(i)
+    return x
+
+
+def det_attn_host(Q, K, V, causal=False, scale=None, out=None, ngroups=4, workspace=None, status=None,
+                  device=None):
+    """det_attn on HOST tensors through da_det_attn_host: Q, K, V contiguous CPU tensors
+    [B, H, S, D] (pinned memory lets the copies overlap the kernels), the f32 output a CPU
+    tensor [B, Hq, Sq, D] (pinned when allocated here).  The copies and the kernels run in
+    `ngroups` groups of (batch, KV head) units on `device` (default: the current CUDA device);
+    the call returns when the output is in host memory.  Bit-identical to det_attn."""
+    desc = _Desc()
+    desc.q, desc.k, desc.v = _host_tensor(Q, "Q"), _host_tensor(K, "K"), _host_tensor(V, "V")
+    if int(ngroups) < 1:
+        raise DetAttnError("ngroups must be at least 1")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    desc.causal = 1 if causal else 0
+    desc.scale = math.nan if scale is None else float(scale)
+    desc.dev_status = _sptr(status)
+    B, Hq, Sq, D = Q.shape
+    if out is None:
+        out = torch.empty(B, Hq, Sq, D, dtype=torch.float32).pin_memory()
+    elif (out.device.type != "cpu" or out.dtype != torch.float32 or tuple(out.shape) != (B, Hq, Sq, D)
+          or not out.is_contiguous()):
+        raise DetAttnError("out must be a contiguous f32 host tensor [B, Hq, Sq, D]")
+    need = int(lib().da_det_attn_host_workspace_bytes(C.byref(desc), int(ngroups)))
+    if need == 0 and B * Sq > 0:
+        raise DetAttnError("det_attn_host: invalid shapes, dtypes or ngroups")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().da_det_attn_host(C.byref(desc), _ptr(out), int(ngroups), _ptr(workspace), need, _stream()),
+               "det_attn_host")
+        torch.cuda.current_stream().synchronize()
     return out
 
 

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/detattn.h: argument checks, workspace
 // layout, and the launch sequences of the fused and the KV-sharded paths (page
 // "det-attn", section "API"; page "det-cross-entropy", section "API").
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -324,6 +325,137 @@ DA_EXPORT int da_det_attn(const da_attn_desc* desc, float* out, void* ws, size_t
   float* m = (float*)((char*)ws + w.m);
   if ((e = da_rowmax_cached(desc, m, ws, ws_bytes, stream))) return e;
   return da_accumulate_finalize_cached(desc, m, out, ws, ws_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+bool dense(const da_tensor& t) {   // [B, H, S, D] contiguous
+  return t.stride[3] == 1 && t.stride[2] == t.D && t.stride[1] == t.S * t.D && t.stride[0] == t.H * t.S * t.D;
+}
+
+// det_attn with host buffers, split into groups of whole (batch, KV head) units: the flattened
+// units [u0, u1) are contiguous in Q, K, V and the output, and each group is an independent
+// det_attn problem (one batch of (u1 - u0) KV heads and their query heads).
+struct HostPlan {
+  int64_t units, per, ngroups;       // units = B * Hkv; per = units per group
+  size_t qb, kb, ob;                 // bytes of one unit's query rows, key (= value) rows, output rows
+  size_t q_off, k_off, v_off, o_off, w_off, w_bytes, total;
+};
+
+da_attn_desc group_desc(const da_attn_desc* d, const void* q, const void* k, const void* v, int64_t n) {
+  da_attn_desc g = *d;
+  const int64_t r = d->q.H / d->k.H;
+  auto set = [](da_tensor& t, const void* ptr, int64_t h) {
+    t.ptr = ptr;
+    t.B = 1;
+    t.H = h;
+    t.stride[3] = 1;
+    t.stride[2] = t.D;
+    t.stride[1] = t.S * t.D;
+    t.stride[0] = h * t.S * t.D;
+  };
+  set(g.q, q, n * r);
+  set(g.k, k, n);
+  set(g.v, v, n);
+  return g;
+}
+
+int host_plan(const da_attn_desc* d, int ngroups, HostPlan& p) {
+  int e = check_desc(d);
+  if (e) return e;
+  if (!dense(d->q) || !dense(d->k) || !dense(d->v)) return DA_ESHAPE;
+  if (ngroups < 1) return DA_EINVAL;
+  const int64_t r = d->q.H / d->k.H;
+  const size_t es = (size_t)elem_size(d->q.dtype);
+  p.units = d->q.B * d->k.H;
+  p.ngroups = p.units == 0 ? 0 : std::min<int64_t>(ngroups, p.units);
+  p.per = p.ngroups == 0 ? 0 : (p.units + p.ngroups - 1) / p.ngroups;
+  p.ngroups = p.per == 0 ? 0 : (p.units + p.per - 1) / p.per;
+  p.qb = (size_t)r * d->q.S * d->q.D * es;
+  p.kb = (size_t)d->k.S * d->k.D * es;
+  p.ob = (size_t)r * d->q.S * d->q.D * 4;
+  p.q_off = 0;
+  p.k_off = round_up(p.q_off + p.units * p.qb);
+  p.v_off = round_up(p.k_off + p.units * p.kb);
+  p.o_off = round_up(p.v_off + p.units * p.kb);
+  p.w_off = round_up(p.o_off + p.units * p.ob);
+  p.w_bytes = 0;
+  if (p.per > 0) {
+    const da_attn_desc g = group_desc(d, d->q.ptr, d->k.ptr, d->v.ptr, p.per);
+    p.w_bytes = ws_layout(&g, 1).total;
+  }
+  p.total = p.w_off + p.ngroups * round_up(p.w_bytes);   // one det_attn workspace per group
+  return DA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+DA_EXPORT size_t da_det_attn_host_workspace_bytes(const da_attn_desc* desc, int ngroups) {
+  HostPlan p;
+  return host_plan(desc, ngroups, p) ? 0 : p.total;
+}
+
+DA_EXPORT int da_det_attn_host(const da_attn_desc* desc, float* out, int ngroups, void* ws, size_t ws_bytes,
+                               da_stream_t stream) {
+  HostPlan p;
+  int e = host_plan(desc, ngroups, p);
+  if (e) return e;
+  if (desc->q.B * desc->q.S == 0) return DA_OK;
+  if (!out) return DA_EINVAL;
+  if (!ws || ws_bytes < p.total) return DA_EWORKSPACE;
+  if (!aligned(ws, 256)) return DA_EALIGN;
+  char* base = (char*)ws;
+  cudaStream_t st = (cudaStream_t)stream;
+  std::vector<cudaStream_t> gs;
+  std::vector<cudaEvent_t> ev;
+  auto event = [&]() {
+    cudaEvent_t x = nullptr;
+    if (cudaEventCreateWithFlags(&x, cudaEventDisableTiming) != cudaSuccess) return (cudaEvent_t) nullptr;
+    ev.push_back(x);
+    return x;
+  };
+  auto run = [&]() -> int {
+    cudaEvent_t start = event();
+    if (!start || cudaEventRecord(start, st) != cudaSuccess) return DA_ECUDA;
+    const char* qh = (const char*)desc->q.ptr;
+    const char* kh = (const char*)desc->k.ptr;
+    const char* vh = (const char*)desc->v.ptr;
+    for (int64_t g = 0; g < p.ngroups; g++) {
+      // one stream per group: its inputs up, its det_attn (own workspace), its output down;
+      // the groups' streams run side by side, so one group's copies overlap another's kernels
+      // and the kernels of several groups fill each other's tails
+      cudaStream_t s = nullptr;
+      if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return DA_ECUDA;
+      gs.push_back(s);
+      if (cudaStreamWaitEvent(s, start, 0) != cudaSuccess) return DA_ECUDA;
+      const int64_t u0 = g * p.per, n = std::min(p.per, p.units - u0);
+      char* qd = base + p.q_off + u0 * p.qb;
+      char* kd = base + p.k_off + u0 * p.kb;
+      char* vd = base + p.v_off + u0 * p.kb;
+      float* od = (float*)(base + p.o_off + u0 * p.ob);
+      if (cudaMemcpyAsync(qd, qh + u0 * p.qb, n * p.qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+          cudaMemcpyAsync(kd, kh + u0 * p.kb, n * p.kb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+          cudaMemcpyAsync(vd, vh + u0 * p.kb, n * p.kb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return DA_ECUDA;
+      const da_attn_desc gd = group_desc(desc, qd, kd, vd, n);
+      const int r = da_det_attn(&gd, od, base + p.w_off + g * round_up(p.w_bytes), p.w_bytes, (da_stream_t)s);
+      if (r) return r;
+      if (cudaMemcpyAsync((char*)out + u0 * p.ob, od, n * p.ob, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return DA_ECUDA;
+      cudaEvent_t done = event();
+      if (!done || cudaEventRecord(done, s) != cudaSuccess || cudaStreamWaitEvent(st, done, 0) != cudaSuccess)
+        return DA_ECUDA;
+    }
+    return DA_OK;
+  };
+  const int r = run();
+  for (cudaEvent_t x : ev) cudaEventDestroy(x);   // released once the work that uses them has run
+  for (cudaStream_t x : gs) cudaStreamDestroy(x);
+  return r;
 }
 
 DA_EXPORT int da_det_attn_sharded(const da_attn_desc* desc, const int64_t* kv_splits, int nsplits, const int32_t* order,

@@ -162,6 +162,25 @@ size_t da_workspace_bytes(const da_attn_desc* desc, int nsplits);
  * order. */
 int da_det_attn(const da_attn_desc* desc, float* out, void* ws, size_t ws_bytes, da_stream_t stream);
 
+/* det_attn with HOST buffers (the call of a program whose tensors live in host memory):
+ * desc's q, k, v point to host memory holding [B, H, S, D] contiguous tensors (strides
+ * D*S*H, D*S, D, 1), out to host f32 [B, Hq, Sq, D] contiguous.  The call copies the inputs
+ * to the device workspace, runs da_det_attn there and copies the output back, in ngroups
+ * groups of whole (batch, KV head) units (clamped to [1, B * Hkv]), each on an internal
+ * stream of its own that waits for the work already queued on `stream`: one group's copies
+ * overlap another's kernels, and the groups' kernels fill each other's tails.
+ * Pinned host memory lets the copies proceed asynchronously; pageable memory works but the
+ * driver stages it.  Returns once the work is queued; the output is in `out` when `stream`
+ * has run it (synchronize `stream`), and the inputs must stay valid until then.  ws: device
+ * workspace of at least da_det_attn_host_workspace_bytes(desc, ngroups) (the device copies
+ * of Q, K, V and the output, and a da_det_attn workspace per group), 256-byte aligned.
+ * Bit-identical to da_det_attn on device copies of the same tensors.  DA_ESHAPE for
+ * non-contiguous tensors, DA_EINVAL for ngroups < 1; da_det_attn_host_workspace_bytes
+ * returns 0 for an invalid descriptor. */
+size_t da_det_attn_host_workspace_bytes(const da_attn_desc* desc, int ngroups);
+int da_det_attn_host(const da_attn_desc* desc, float* out, int ngroups, void* ws, size_t ws_bytes,
+                     da_stream_t stream);
+
 /* The two passes of det_attn (det-attn "Method": a max-reduce, then the exact sums with the
  * global rowmax) over all keys, with the score cache.  The score of a pair is a fixed function
  * of its query and key rows, so pass 1 can hand every exact score it computes to pass 2:

@@ -150,3 +150,18 @@ def test_outputs_and_state_are_checked(nolib):
         da.dce_rowmax(torch.zeros(4, 10), out=torch.zeros(3))
     with pytest.raises(da.DetAttnError):
         da.det_attn(Q, Q, Q, status=torch.zeros(1, dtype=torch.int64))
+
+
+def test_det_attn_host_rejects_bad_host_tensors():
+    """The host-buffer entry point's binding checks its tensors before any CUDA call: host
+    memory, [B, H, S, D], contiguous; ngroups >= 1."""
+    import bitwise_deterministic_shard_gb300 as da
+    Q = torch.zeros(1, 2, 8, 16, dtype=torch.bfloat16)
+    with pytest.raises(da.DetAttnError):
+        da.det_attn_host(Q.transpose(2, 3), Q, Q, device="cuda:0")      # not contiguous
+    with pytest.raises(da.DetAttnError):
+        da.det_attn_host(Q[0], Q, Q, device="cuda:0")                    # not 4-dimensional
+    with pytest.raises(da.DetAttnError):
+        da.det_attn_host(Q, Q, Q, ngroups=0, device="cuda:0")
+    with pytest.raises(da.DetAttnError):
+        da.det_attn_host(Q.half(), Q.half(), Q.half(), device="cuda:0")  # f16 is not a supported dtype

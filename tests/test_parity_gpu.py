@@ -467,3 +467,25 @@ def test_score_cache_rare_paths_match_oracle(da, orc, causal):
     assert da.read_status(st) & ~1 == 0
     assert_bits_equal(out.reshape(-1, 128), out_o, "output")
     assert_bits_equal(sh, out, "sharded vs fused")
+
+
+@cuda
+@pytest.mark.parametrize("case", [
+    # (B, Hq, Hkv, S, D, dtype, causal, ngroups, pinned)
+    (2, 4, 2, 200, 128, torch.bfloat16, True, 3, True),
+    (1, 4, 4, 150, 128, torch.bfloat16, False, 8, False),
+    (1, 2, 1, 90, 64, torch.float32, True, 1, True),
+])
+def test_host_buffer_entry_point_equals_det_attn(da, case):
+    """da_det_attn_host (host inputs and output, copies overlapped with the kernels in groups of
+    (batch, KV head) units) against det_attn on device copies, bit for bit, for even and uneven
+    groups, pinned and pageable host memory, GQA and f32."""
+    B, Hq, Hkv, S, D, dt, causal, ngroups, pinned = case
+    Q, K, V = W.random_attn(500 + S, B, Hq, Hkv, S, D, dt, causal)
+    if pinned:
+        Q, K, V = Q.pin_memory(), K.pin_memory(), V.pin_memory()
+    got = da.det_attn_host(Q, K, V, causal=causal, ngroups=ngroups)
+    ref = da.det_attn(Q.cuda(), K.cuda(), V.cuda(), causal=causal)
+    torch.cuda.synchronize()
+    assert got.device.type == "cpu"
+    assert_bits_equal(got, ref.cpu(), "host entry point vs det_attn")
