@@ -93,18 +93,22 @@ __global__ void __launch_bounds__(DEN_THREADS, 6) dce_denom_kernel(const DceArgs
   den_init(A);
   int st = 0;
   for_row<DT>(row, a.v_lo, a.v_hi, [&](uint32_t u) {
-    if (nonfinite_bits(u)) { st |= ST_NONFINITE; return; }
+    // common case, one test: a finite logit at most about 21.5 below the maximum (x <= 0 and a
+    // weight w >= 2^-31).  The weight is exp32_det's p 2^k (exact for k >= -125), so its
+    // mantissa goes straight into the private word (den_add's first case, without forming w).
+    // A NaN or infinite logit, one above the maximum, or a smaller weight fails the test.
     float x = __fsub_rn(__uint_as_float(u), m);
+    int k;
+    const uint32_t pbits = __float_as_uint(exp32_det_poly(fmaxf(x, -104.0f), k));
+    const int sh = (int)(pbits >> 23) + k - 96;
+    if (x <= 0.0f && sh >= 0) {
+      A.U += (uint64_t)((pbits & 0x7FFFFFu) | 0x800000u) << sh;
+      return;
+    }
+    if (nonfinite_bits(u)) { st |= ST_NONFINITE; return; }
     if (x != x) { st |= ST_NONFINITE; return; }
     if (x > 0.0f) { st |= ST_VIOLATION; x = 0.0f; }
-    // the weight is exp32_det's p 2^k (exact for k >= -125): for w >= 2^-31 its mantissa goes
-    // straight into the private word (den_add's first case, without forming w); smaller
-    // weights take den_add with the full evaluation
-    int k;
-    const uint32_t pbits = __float_as_uint(exp32_det_poly(x >= -104.0f ? x : 0.0f, k));
-    const int sh = (int)(pbits >> 23) + k - 96;
-    if (x >= -104.0f && sh >= 0) A.U += (uint64_t)((pbits & 0x7FFFFFu) | 0x800000u) << sh;
-    else den_add(A, __float_as_uint(exp32_det_nb(x)));   // x <= 0, not NaN
+    den_add(A, __float_as_uint(exp32_det_nb(x)));   // x <= 0, not NaN
   }, [&] { den_guard(A); });
   den_flush(A);
   long long dg[6] = {A.d[0], A.d[1], A.d[2], A.d[3], A.d[4], A.d[5]};
