@@ -216,15 +216,13 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
   // (NaN, deep or zero weights, special denominators, an uncertain rounding) otherwise.
   auto one = [&](uint32_t u, int v) -> float {
     float x = __fsub_rn(__uint_as_float(u), m);
-    if (x > 0.0f) {
-      st |= ST_VIOLATION;
-      x = 0.0f;
-    }
+    // one test for the common case: x <= 0 (not NaN, not above the maximum) and k >= -125 (the
+    // weight p 2^k is exact and normal; this also rejects x below about -86.6 and -inf)
     int k;
-    const float pp = exp32_det_poly(x >= -104.0f ? x : 0.0f, k);   // NaN x: NaN p, rejected below
+    const float pp = exp32_det_poly(fmaxf(x, -104.0f), k);
     const uint32_t pbits = __float_as_uint(pp);
     const int bew = (int)(pbits >> 23) + k;                           // the weight's biased exponent
-    bool ok = !slow && x >= -104.0f && k >= -125;
+    bool ok = !slow && x <= 0.0f && k >= -125;
     uint32_t q = 0;
     if (ok) {
       const uint32_t mw = (pbits & 0x7FFFFFu) | 0x800000u;
@@ -236,6 +234,10 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
     if (ok) {
       p = __uint_as_float(q);
     } else {
+      if (x > 0.0f) {   // above the maximum: clamped as in the forward
+        st |= ST_VIOLATION;
+        x = 0.0f;
+      }
       const float w = x != x ? x : exp32_det_nb(x);
       if (!slow && w > 0.0f) {
         uint32_t mw;
