@@ -85,18 +85,19 @@ __device__ __forceinline__ void score_tile_mma(float (&acc)[NDIAG][4], const uin
 }
 
 // exact int64 dot sum_c 2^(7c) A_c from the 7 diagonal sums of output element e (f32
-// integers, |A_c| <= 2^22): v + 1.5 2^23 puts A_c in the low bits of the float's pattern,
-// and the patterns' common offset is folded into one constant (arithmetic mod 2^64)
+// integers, |A_c| <= 2^22): v + 1.5 2^23 puts A_c in the low bits of the float's pattern.
+// Summed as a shallow tree: pairs A_c + 128 A_(c+1) fit 32 bits, then three exact 64-bit
+// multiply-adds
 template <int N>
 __device__ __forceinline__ long long combine_diag(const float (&acc)[NDIAG][N], int e) {
-  int raw[NDIAG];
+  int A[NDIAG];
 #pragma unroll
-  for (int c = 0; c < NDIAG; c++) raw[c] = __float_as_int(__fadd_rn(acc[c][e], 12582912.0f));
-  const int hi = (raw[5] - 0x4B400000) + (raw[6] - 0x4B400000) * 128;   // |hi| < 2^30
-  long long T = (long long)((unsigned long long)(long long)hi << 35);
-#pragma unroll
-  for (int c = 0; c < 5; c++) mad_wide(T, raw[c], 1 << (7 * c));
-  return (long long)((unsigned long long)T - 0x4B400000ull * 0x10204081ull);
+  for (int c = 0; c < NDIAG; c++) A[c] = __float_as_int(__fadd_rn(acc[c][e], 12582912.0f)) - 0x4B400000;
+  const int s01 = A[0] + A[1] * 128, s23 = A[2] + A[3] * 128, s56 = A[5] + A[6] * 128;   // each below 2^30
+  long long lo = (long long)s01, hi = (long long)((unsigned long long)(long long)s56 << 35);
+  mad_wide(lo, s23, 1 << 14);   // s01 + 2^14 s23
+  mad_wide(hi, A[4], 1 << 28);  // 2^28 A_4 + 2^35 s56
+  return lo + hi;
 }
 
 // Rows outside the 26-bit window.  Such a row's digit slices hold its truncated part
