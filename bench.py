@@ -541,7 +541,7 @@ def run_kernels(args):
             del out
         del num, den, Q, K, V, ws, m
         torch.cuda.empty_cache()
-        for D, heads, acc_kernel in ((64, args.heads, "accumulate_tc_kernel"),
+        for D, heads, acc_kernel in ((64, args.heads, "accumulate_tp_kernel"),
                                      (256, max(1, args.heads // 4), "accumulate_kernel")):
             if f"rowmax_d{D}" not in want and f"accumulate_d{D}" not in want:
                 continue

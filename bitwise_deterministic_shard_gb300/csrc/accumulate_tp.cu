@@ -1,5 +1,5 @@
 // K2 with both products on the tensor cores (sm_103a): exact accumulate of NUM / DEN
-// digits for 64 < D <= 128.
+// digits for D <= 128 (head dimensions below 128 padded with zero columns).
 //
 // Page "det-attn", section "Method": NUM_id = sum_j exp(s_ij - rowmax_i) V_jd and
 // DEN_i = sum_j exp(s_ij - rowmax_i) are exact integer sums in fixed bins.

@@ -67,14 +67,14 @@ struct WsLayout {
 
 size_t kv_bytes(const da_attn_desc* d) { return kv_prep_bytes((int)d->k.B, (int)d->k.H, (int)d->k.S, (int)d->k.D); }
 
-// The score cache of the whole-range path (64 < D <= 128, at most ACC_TP_MAX_TILES key tiles,
+// The score cache of the whole-range path (D <= 128, at most ACC_TP_MAX_TILES key tiles,
 // causal only with Sq == Skv): bytes, or 0 when the path recomputes the scores instead (other
 // head dimensions, or a cache above kScoreCacheCap).
 constexpr size_t kScoreCacheCap = (size_t)16 << 30;
 size_t sc_bytes(const da_attn_desc* d, int* nkt = nullptr, int64_t* per_bh = nullptr) {
   int n;
   int64_t pb;
-  if (d->q.D <= 64 || d->q.D > 128 || (d->k.S + KTILE - 1) / KTILE > ACC_TP_MAX_TILES) return 0;
+  if (d->q.D > 128 || (d->k.S + KTILE - 1) / KTILE > ACC_TP_MAX_TILES) return 0;
   const size_t b = score_cache_bytes((int)d->q.B, (int)d->q.H, (int)d->q.S, (int)d->k.S, d->causal, &n, &pb);
   if (b > kScoreCacheCap) return 0;
   if (nkt) *nkt = n;

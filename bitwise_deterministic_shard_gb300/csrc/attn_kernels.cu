@@ -876,7 +876,10 @@ static cudaError_t launch_accumulate_t(const AttnArgs& a, const KvPrep& p, cudaS
   return cudaGetLastError();
 }
 
-static int padded_d(int D) { return D <= 64 ? 64 : (D <= 128 ? 128 : 256); }
+// D <= 128 runs on the 128-wide tensor-core kernels (the padding columns are zero: the exact
+// sums are unchanged, and the per-pair work, not the MMA width, sets their time), D <= 256 on
+// the 256-wide ones
+static int padded_d(int D) { return D <= 128 ? 128 : 256; }
 
 cudaError_t launch_rowmax(const AttnArgs& a, const KvPrep& p, cudaStream_t st) {
   const int dp = padded_d(a.D);

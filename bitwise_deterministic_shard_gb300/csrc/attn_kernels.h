@@ -84,7 +84,7 @@ cudaError_t launch_kv_prep(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
 cudaError_t launch_rowmax(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // a.scores: also store scores
 cudaError_t launch_accumulate(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
 cudaError_t launch_accumulate_tc(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // D <= 128
-cudaError_t launch_accumulate_tp(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // 64 < D <= 128
+cudaError_t launch_accumulate_tp(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // D <= 128
 constexpr int ACC_TP_MAX_TILES = 512;   // key tiles per pass the tensor-PV kernel's state holds exactly
 bool accumulate_is_tp(const AttnArgs& a, const KvPrep& p);   // launch_accumulate takes the tensor-PV kernel
 

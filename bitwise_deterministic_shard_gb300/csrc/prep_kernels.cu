@@ -144,7 +144,7 @@ static size_t ktc_bytes(int B, int Hkv, int Skv, int dp) {
 }
 
 size_t kv_prep_bytes(int B, int Hkv, int Skv, int D) {
-  const int dp = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
+  const int dp = D <= 128 ? 128 : 256;   // the kernels' padded width (attn_kernels.cu)
   const size_t rows = (size_t)B * Hkv * Skv;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   return up(dp == 256 ? rows * NSLICE * dp * 2 : 0) + up(rows * 4) + up(rows * NLO * 8) + up((size_t)B * Hkv * dp * 4) +
@@ -153,7 +153,7 @@ size_t kv_prep_bytes(int B, int Hkv, int Skv, int D) {
 }
 
 KvPrep kv_prep_layout(void* ws, int B, int Hkv, int Skv, int D, int do_v) {
-  const int dp = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
+  const int dp = D <= 128 ? 128 : 256;   // the kernels' padded width (attn_kernels.cu)
   const size_t rows = (size_t)B * Hkv * Skv;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   char* c = (char*)ws;

@@ -131,7 +131,7 @@ int da_accumulate(const da_attn_desc* desc, const float* m, int64_t kv_lo, int64
  * out = RN32(RN64(RN64(NUM) / RN64(DEN))) for NUM/DEN over keys [0, Skv) with the global
  * rowmax m (device f32 [B, Hq, Sq]).  out: device f32 [B, Hq, Sq, D], contiguous.  Equal bit
  * for bit to da_accumulate(.., 0, Skv, .., add_into = 0) followed by da_finalize; where the
- * tensor-PV kernel applies (64 < D <= 128, at most 65,536 keys) it finalizes in its epilogue
+ * tensor-PV kernel applies (D <= 128, at most 65,536 keys) it finalizes in its epilogue
  * and the NUM digits never reach device memory.  ws: at least da_workspace_bytes(desc, 1)
  * (the digits are kept there on the other paths). */
 int da_accumulate_finalize(const da_attn_desc* desc, const float* m, float* out, void* ws, size_t ws_bytes,
@@ -184,7 +184,7 @@ int da_det_attn_host(const da_attn_desc* desc, float* out, int ngroups, void* ws
 /* The two passes of det_attn (det-attn "Method": a max-reduce, then the exact sums with the
  * global rowmax) over all keys, with the score cache.  The score of a pair is a fixed function
  * of its query and key rows, so pass 1 can hand every exact score it computes to pass 2:
- * for 64 < D <= 128 (at most 65,536 keys, and a cache of at most 16 GiB) da_rowmax_cached
+ * for D <= 128 (at most 65,536 keys, and a cache of at most 16 GiB) da_rowmax_cached
  * prepares keys and values once, writes m (device f32 [B, Hq, Sq]) and stores every score it
  * rounds in the workspace's cache; da_accumulate_finalize_cached then reads the scores
  * instead of recomputing them and writes the f32 output, bit for bit what
