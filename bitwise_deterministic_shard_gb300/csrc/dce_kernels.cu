@@ -7,21 +7,28 @@
 // logsumexp - x_target.  The contract here: weights exp32_det(RN32(x - m)), digits in
 // radix 2^32 with E0 = -160, loss = RN32(RN64(log64_det(RN64(den)) + RN64(m - x_t))).
 //
-// One CTA streams one row of logits with 16-byte loads (HBM-bound: 4 B per f32 logit,
-// 2 B per bf16 logit) and keeps six int64 digits per thread; the CTA sum of digits is
-// exact, so the reduction order does not matter.
+// The denominator streams each row of logits with 16-byte loads (HBM-bound: 4 B per f32
+// logit, 2 B per bf16 logit), one CTA or one cluster of CTAs per row, six int64 digits per
+// thread; the sums of digits are exact, so the reduction order does not matter.  The
+// exponentials of adjacent logits are evaluated in pairs on the packed FP32 instructions.
 #include <cuda_bf16.h>
+#include <cooperative_groups.h>
 #include "numerics.cuh"
 #include "divide.cuh"
 #include "den_acc.cuh"
+#include "pack2.cuh"
 #include "attn_kernels.h"
 
 namespace detattn {
 
+namespace cg = cooperative_groups;
+
 // visit every element of row[v_lo, v_hi) owned by this thread: scalar head up to a 16-byte
-// boundary, 16-byte vectors, scalar tail; group() runs before each vector or scalar element
-template <int DT, typename F, typename G>
-__device__ __forceinline__ void for_row(const typename In<DT>::T* row, int64_t v_lo, int64_t v_hi, F&& f, G&& group) {
+// boundary, 16-byte vectors, scalar tail.  f(bits) takes one element, f2(bits, bits) the
+// adjacent pairs of a vector; group() runs before each vector or scalar element.
+template <int DT, typename F, typename F2, typename G>
+__device__ __forceinline__ void for_row2(const typename In<DT>::T* row, int64_t v_lo, int64_t v_hi, F&& f, F2&& f2,
+                                         G&& group) {
   using T = typename In<DT>::T;
   constexpr int VEC = 16 / sizeof(T);
   const uintptr_t addr = reinterpret_cast<uintptr_t>(row + v_lo);
@@ -34,25 +41,39 @@ __device__ __forceinline__ void for_row(const typename In<DT>::T* row, int64_t v
   }
   const int64_t nvec = (v_hi - hend) / VEC;
   const uint4* vp = reinterpret_cast<const uint4*>(row + hend);
-  for (int64_t k = threadIdx.x; k < nvec; k += blockDim.x) {
-    uint4 q = __ldg(vp + k);
-    uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  auto vec = [&](const uint4& q) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
     group();
     if constexpr (DT == 0) {
-#pragma unroll
-      for (int t = 0; t < 4; t++) f(w[t]);
+      f2(w[0], w[1]);
+      f2(w[2], w[3]);
     } else {
 #pragma unroll
-      for (int t = 0; t < 4; t++) {
-        f(w[t] << 16);
-        f(w[t] & 0xFFFF0000u);
-      }
+      for (int t = 0; t < 4; t++) f2(w[t] << 16, w[t] & 0xFFFF0000u);
     }
+  };
+  // NB vectors per thread in flight before their arithmetic (the loop body is long, so one
+  // load at a time would leave the memory system short of requests)
+  constexpr int NB = 3;
+  const int64_t step = blockDim.x;
+  int64_t k = threadIdx.x;
+  for (; k + (NB - 1) * step < nvec; k += NB * step) {
+    uint4 q[NB];
+#pragma unroll
+    for (int b = 0; b < NB; b++) q[b] = __ldg(vp + k + b * step);
+#pragma unroll
+    for (int b = 0; b < NB; b++) vec(q[b]);
   }
+  for (; k < nvec; k += step) vec(__ldg(vp + k));
   for (int64_t v = hend + nvec * VEC + threadIdx.x; v < v_hi; v += blockDim.x) {
     group();
     f(In<DT>::bits(row, v));
   }
+}
+
+template <int DT, typename F, typename G>
+__device__ __forceinline__ void for_row(const typename In<DT>::T* row, int64_t v_lo, int64_t v_hi, F&& f, G&& group) {
+  for_row2<DT>(row, v_lo, v_hi, f, [&](uint32_t u0, uint32_t u1) { f(u0); f(u1); }, group);
 }
 
 template <int DT>
@@ -81,35 +102,61 @@ __global__ void __launch_bounds__(256) dce_rowmax_kernel(const DceArgs a) {
   report(a.status, nf);
 }
 
-constexpr int DEN_THREADS = 256;   // one CTA per row, six resident per SM
+// A row is split over `parts` CTAs (1, 2, 4 or 8), one thread-block cluster per row; six
+// CTAs resident per SM.  Each CTA sums its share of the columns; the others' sums reach the
+// cluster's first CTA through distributed shared memory, and it adds them (integers: exact in
+// any order), carries and writes the row's digits.  Splitting the rows fills the GPU when the
+// rows are fewer than its CTA slots.
+constexpr int DEN_THREADS = 256, DEN_MAX_PARTS = 8;
 
 template <int DT>
-__global__ void __launch_bounds__(DEN_THREADS, 6) dce_denom_kernel(const DceArgs a) {
+__global__ void __launch_bounds__(DEN_THREADS, 6) dce_denom_kernel(const DceArgs a, int parts) {
   using T = typename In<DT>::T;
-  const int64_t i = blockIdx.x;
+  const int64_t i = blockIdx.x / parts;
+  const int c = (int)(blockIdx.x % parts);   // the CTA's rank in its cluster
   const T* row = (const T*)a.x + i * a.rs;
   const float m = a.m_in[i];
+  // this CTA's columns: equal shares of the range, each a multiple of 64 columns
+  const int64_t share = ((a.v_hi - a.v_lo + parts - 1) / parts + 63) / 64 * 64;
+  const int64_t c_lo = min(a.v_hi, a.v_lo + c * share), c_hi = min(a.v_hi, c_lo + share);
   DenAcc A;   // exact: a private word for w >= 2^-31, digit words for the rest (den_acc.cuh)
   den_init(A);
   int st = 0;
-  for_row<DT>(row, a.v_lo, a.v_hi, [&](uint32_t u) {
-    // common case, one test: a finite logit at most about 21.5 below the maximum (x <= 0 and a
-    // weight w >= 2^-31).  The weight is exp32_det's p 2^k (exact for k >= -125), so its
-    // mantissa goes straight into the private word (den_add's first case, without forming w).
-    // A NaN or infinite logit, one above the maximum, or a smaller weight fails the test.
-    float x = __fsub_rn(__uint_as_float(u), m);
-    int k;
-    const uint32_t pbits = __float_as_uint(exp32_det_poly(fmaxf(x, -104.0f), k));
+  // common case, one test: a finite logit at most about 21.5 below the maximum (x <= 0 and a
+  // weight w >= 2^-31).  The weight is exp32_det's p 2^k (exact for k >= -125), so its
+  // mantissa goes straight into the private word (den_add's first case, without forming w).
+  // A NaN or infinite logit, one above the maximum, or a smaller weight fails the test.
+  auto fast = [&](float x, float p, int k) -> bool {
+    const uint32_t pbits = __float_as_uint(p);
     const int sh = (int)(pbits >> 23) + k - 96;
     if (x <= 0.0f && sh >= 0) {
       A.U += (uint64_t)((pbits & 0x7FFFFFu) | 0x800000u) << sh;
-      return;
+      return true;
     }
+    return false;
+  };
+  auto general = [&](uint32_t u, float x) {
     if (nonfinite_bits(u)) { st |= ST_NONFINITE; return; }
     if (x != x) { st |= ST_NONFINITE; return; }
     if (x > 0.0f) { st |= ST_VIOLATION; x = 0.0f; }
     den_add(A, __float_as_uint(exp32_det_nb(x)));   // x <= 0, not NaN
-  }, [&] { den_guard(A); });
+  };
+  for_row2<DT>(row, c_lo, c_hi,
+               [&](uint32_t u) {
+                 const float x = __fsub_rn(__uint_as_float(u), m);
+                 int k;
+                 const float p = exp32_det_poly(fmaxf(x, -104.0f), k);
+                 if (!fast(x, p, k)) general(u, x);
+               },
+               [&](uint32_t u0, uint32_t u1) {   // two logits on the packed FP32 lanes
+                 float x0, x1, p0, p1;
+                 int k0, k1;
+                 f2::unpack(f2::sub(f2::pack(__uint_as_float(u0), __uint_as_float(u1)), f2::splat(m)), x0, x1);
+                 exp32_det_poly2(fmaxf(x0, -104.0f), fmaxf(x1, -104.0f), p0, p1, k0, k1);
+                 if (!fast(x0, p0, k0)) general(u0, x0);
+                 if (!fast(x1, p1, k1)) general(u1, x1);
+               },
+               [&] { den_guard(A); });
   den_flush(A);
   long long dg[6] = {A.d[0], A.d[1], A.d[2], A.d[3], A.d[4], A.d[5]};
 #pragma unroll
@@ -120,15 +167,37 @@ __global__ void __launch_bounds__(DEN_THREADS, 6) dce_denom_kernel(const DceArgs
   if ((threadIdx.x & 31) == 0)
 #pragma unroll
     for (int k = 0; k < 6; k++) wsum[threadIdx.x >> 5][k] = dg[k];
+  __shared__ long long psum[DEN_MAX_PARTS][6];   // the cluster's first CTA: the others' sums
   __syncthreads();
-  if (threadIdx.x == 0) {
-    long long t[6];
-    long long* out = a.den + i * DEN_NDIG;
+  long long t[6];
+  if (threadIdx.x == 0)
 #pragma unroll
     for (int k = 0; k < 6; k++) {
-      t[k] = a.add_into ? out[k] : 0;
+      t[k] = 0;
       for (int w = 0; w < DEN_THREADS / 32; w++) t[k] += wsum[w][k];
     }
+  if (parts > 1) {
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();   // every CTA of the cluster runs: the first one's psum may be written
+    if (threadIdx.x == 0 && c > 0) {
+      long long* dst = cl.map_shared_rank(&psum[c][0], 0);
+#pragma unroll
+      for (int k = 0; k < 6; k++) dst[k] = t[k];
+    }
+    cl.sync();   // the sums have landed
+    if (c > 0) {
+      report(a.status, st);
+      return;
+    }
+    if (threadIdx.x == 0)
+      for (int q = 1; q < parts; q++)
+#pragma unroll
+        for (int k = 0; k < 6; k++) t[k] += psum[q][k];
+  }
+  if (threadIdx.x == 0) {
+    long long* out = a.den + i * DEN_NDIG;
+#pragma unroll
+    for (int k = 0; k < 6; k++) t[k] += a.add_into ? out[k] : 0;
     kul_carry(t, 6);
     if (t[5] > (1ll << 62) || t[5] < -(1ll << 62)) st |= ST_HEADROOM;
 #pragma unroll
@@ -210,16 +279,14 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
   const int64_t tg64 = a.targets[i] - a.v_base - c0;   // the target's column within this chunk (any value)
   const int tg = tg64 >= 0 && tg64 < nv ? (int)tg64 : -1;
   int st = 0;
-  // dLogits of the logit with bits u in column v of the chunk.  Fast path: the weight as
-  // exp32_det's p 2^k (exact for k >= -125: mantissa of p, exponent of p + k) and its quotient
-  // rounded straight from the row's reciprocal; the exact division and the special cases
-  // (NaN, deep or zero weights, special denominators, an uncertain rounding) otherwise.
-  auto one = [&](uint32_t u, int v) -> float {
-    float x = __fsub_rn(__uint_as_float(u), m);
+  // fin: dLogits of the logit in column v of the chunk, from x = RN32(logit - m) and
+  // exp32_det_poly(max(x, -104)) = (pp, k).  Fast path: the weight as exp32_det's p 2^k (exact
+  // for k >= -125: mantissa of p, exponent of p + k) and its quotient rounded straight from the
+  // row's reciprocal; the exact division and the special cases (NaN, deep or zero weights,
+  // special denominators, an uncertain rounding) otherwise.
+  auto fin = [&](float x, float pp, int k, int v) -> float {
     // one test for the common case: x <= 0 (not NaN, not above the maximum) and k >= -125 (the
     // weight p 2^k is exact and normal; this also rejects x below about -86.6 and -inf)
-    int k;
-    const float pp = exp32_det_poly(fmaxf(x, -104.0f), k);
     const uint32_t pbits = __float_as_uint(pp);
     const int bew = (int)(pbits >> 23) + k;                           // the weight's biased exponent
     bool ok = !slow && x <= 0.0f && k >= -125;
@@ -253,6 +320,21 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
     const float g = v == tg ? __fsub_rn(p, 1.0f) : p;
     return __fmul_rn(go, g);
   };
+  auto one = [&](uint32_t u, int v) -> float {
+    const float x = __fsub_rn(__uint_as_float(u), m);
+    int k;
+    const float pp = exp32_det_poly(fmaxf(x, -104.0f), k);
+    return fin(x, pp, k, v);
+  };
+  // two adjacent logits (columns v, v + 1), their exponentials on the packed FP32 lanes
+  auto two = [&](uint32_t u0, uint32_t u1, int v, float& o0, float& o1) {
+    float x0, x1, p0, p1;
+    int k0, k1;
+    f2::unpack(f2::sub(f2::pack(__uint_as_float(u0), __uint_as_float(u1)), f2::splat(m)), x0, x1);
+    exp32_det_poly2(fmaxf(x0, -104.0f), fmaxf(x1, -104.0f), p0, p1, k0, k1);
+    o0 = fin(x0, p0, k0, v);
+    o1 = fin(x1, p1, k1, v + 1);
+  };
   if constexpr (VEC) {
     constexpr int EV = 16 / (int)sizeof(T), NV = BW_PER / EV;
     const uint4* __restrict__ src = reinterpret_cast<const uint4*>(row);
@@ -269,13 +351,20 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
       if (gv * EV >= nv) continue;   // nv is a multiple of EV here
       const uint32_t wd[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
       uint32_t o[4];
+      if constexpr (DT == 0) {
 #pragma unroll
-      for (int t = 0; t < 4; t++) {
-        if constexpr (DT == 0) {
-          o[t] = __float_as_uint(one(wd[t], gv * 4 + t));
-        } else {
-          const __nv_bfloat162 h = __floats2bfloat162_rn(one(wd[t] << 16, gv * 8 + 2 * t),
-                                                         one(wd[t] & 0xFFFF0000u, gv * 8 + 2 * t + 1));
+        for (int t = 0; t < 4; t += 2) {
+          float r0, r1;
+          two(wd[t], wd[t + 1], gv * 4 + t, r0, r1);
+          o[t] = __float_as_uint(r0);
+          o[t + 1] = __float_as_uint(r1);
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; t++) {
+          float r0, r1;
+          two(wd[t] << 16, wd[t] & 0xFFFF0000u, gv * 8 + 2 * t, r0, r1);
+          const __nv_bfloat162 h = __floats2bfloat162_rn(r0, r1);
           o[t] = *reinterpret_cast<const uint32_t*>(&h);
         }
       }
@@ -380,11 +469,38 @@ cudaError_t launch_dce_rowmax(const DceArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// CTAs per row: the fewest of 1, 2, 4, 8 that fill the GPU's CTA slots (six per SM) once, each
+// CTA keeping at least 4,096 columns.  Measured on the V128256 f32 rows: 256 rows run 1.4x
+// faster on clusters of 8; from about one row per slot on, splitting gains nothing (the
+// streaming CTAs of a partial last wave take the whole bandwidth).
+static int denom_parts(int64_t N, int64_t cols) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 1;
+  }
+  int p = 1;
+  while (p < DEN_MAX_PARTS && N * p < 6ll * sms && cols / (2 * p) >= 4096) p *= 2;
+  return p;
+}
+
 cudaError_t launch_dce_denom(const DceArgs& a, cudaStream_t st) {
   if (a.N <= 0) return cudaSuccess;
-  if (a.dtype == 0) dce_denom_kernel<0><<<(unsigned)a.N, DEN_THREADS, 0, st>>>(a);
-  else dce_denom_kernel<1><<<(unsigned)a.N, DEN_THREADS, 0, st>>>(a);
-  return cudaGetLastError();
+  const int parts = denom_parts(a.N, a.v_hi - a.v_lo);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.N * parts));
+  cfg.blockDim = dim3(DEN_THREADS);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)parts;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = parts > 1 ? 1 : 0;
+  return a.dtype == 0 ? cudaLaunchKernelEx(&cfg, dce_denom_kernel<0>, a, parts)
+                      : cudaLaunchKernelEx(&cfg, dce_denom_kernel<1>, a, parts);
 }
 
 cudaError_t launch_dce_finalize(const DceArgs& a, cudaStream_t st) {

@@ -11,14 +11,48 @@
 // up after its time limit, the kernel returns normally and reports DA_STATUS_TIMEOUT in the
 // status word, so the caller's context stays usable: the timeout path is exercised without
 // a fault or a hang.
+//
+// da_probe_exp_pairs: the packed two-lane exponential (pack2.cuh) against the scalar one, on
+// every binary32 bit pattern of a range; the cross-entropy kernels take the packed form for
+// two adjacent logits, so it must give the same bits for every argument.
 #include "../../include/detattn.h"
 #include "numerics.cuh"
+#include "pack2.cuh"
 #include "tc5.cuh"
 
 namespace detattn {
 
 constexpr int PROBE_ACC = 8;   // independent accumulators per thread (hides the multiply latency)
 constexpr int PROBE_UNROLL = 4;
+
+// Thread pairs (u, u + 1) of the range [lo, lo + count) (bit patterns, wrapping mod 2^32): x
+// is the binary32 with those bits, clamped as the kernels clamp (NaN -> -inf, then to
+// [-104, 0]).  Counts the patterns whose packed exp32_det_poly2 (p or k) differs from the
+// scalar exp32_det_poly in any bit.
+__global__ void __launch_bounds__(256) probe_exp_pairs_kernel(uint32_t lo, long long count,
+                                                              unsigned long long* mismatches) {
+  auto arg = [](uint32_t u) {
+    const float x = __uint_as_float(u);
+    return fmaxf(x != x ? neg_inf() : (x > 0.0f ? 0.0f : x), -104.0f);
+  };
+  unsigned long long bad = 0;
+  const long long npairs = (count + 1) / 2;
+  for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < npairs;
+       q += (long long)gridDim.x * blockDim.x) {
+    const uint32_t u0 = lo + (uint32_t)(2 * q);
+    const uint32_t u1 = 2 * q + 1 < count ? u0 + 1u : u0;
+    const float x0 = arg(u0), x1 = arg(u1);
+    float p0, p1;
+    int k0, k1, s0, s1;
+    exp32_det_poly2(x0, x1, p0, p1, k0, k1);
+    const float sp0 = exp32_det_poly(x0, s0), sp1 = exp32_det_poly(x1, s1);
+    const bool m0 = __float_as_uint(p0) != __float_as_uint(sp0) || k0 != s0;
+    const bool m1 = __float_as_uint(p1) != __float_as_uint(sp1) || k1 != s1;
+    bad += (unsigned long long)m0 + (unsigned long long)(m1 && u1 != u0);
+  }
+  for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xFFFFFFFFu, bad, o);
+  if ((threadIdx.x & 31) == 0 && bad) atomicAdd(mismatches, bad);
+}
 
 __global__ void __launch_bounds__(512) probe_int_mac_kernel(long long iters, long long* sink) {
   long long acc[PROBE_ACC];
@@ -61,6 +95,15 @@ __global__ void probe_bounded_wait_kernel(int* status) {
 #define DA_EXPORT __attribute__((visibility("default")))
 
 extern "C" {
+
+DA_EXPORT int da_probe_exp_pairs(uint32_t lo_bits, int64_t count, int64_t* mismatches, da_stream_t stream) {
+  if (count < 0 || count > (1ll << 32) || !mismatches) return DA_EINVAL;
+  if (reinterpret_cast<uintptr_t>(mismatches) % 8) return DA_EALIGN;
+  if (count == 0) return DA_OK;
+  detattn::probe_exp_pairs_kernel<<<1216, 256, 0, (cudaStream_t)stream>>>(lo_bits, (long long)count,
+                                                                          (unsigned long long*)mismatches);
+  return cudaGetLastError() == cudaSuccess ? DA_OK : DA_ECUDA;
+}
 
 DA_EXPORT int da_probe_int_mac(int64_t iters, int nblocks, int64_t* sink, da_stream_t stream) {
   if (iters < 0 || nblocks < 1 || nblocks > (1 << 20)) return DA_EINVAL;

@@ -302,8 +302,8 @@ def test_strided_nhd_views(da, orc):
 
 @cuda
 @pytest.mark.parametrize("case", [
-    # (B, Hq, Hkv, S, D, dtype, causal, spread): D in (64, 128] takes the tensor-PV kernel,
-    # which finalizes in its epilogue; D = 64 takes the digits + finalize path
+    # (B, Hq, Hkv, S, D, dtype, causal, spread): every D <= 128 takes the 128-wide tensor-PV
+    # kernel, which finalizes in its epilogue (the digit path stores NUM and finalizes apart)
     (1, 2, 2, 200, 128, torch.bfloat16, True, 1.0),
     (2, 4, 2, 300, 128, torch.float32, False, 1.0),
     (1, 2, 1, 150, 100, torch.bfloat16, True, 1.0),
@@ -403,6 +403,28 @@ def test_dce_small_matches_oracle(da, orc, dt):
 
 
 @cuda
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("N,V,splits", [
+    (64, 65613, [65613]),              # eight CTAs per row (one cluster), a ragged last share
+    (64, 65613, [30001, 35612]),       # four and eight per shard, shares off the 16-byte grid
+    (300, 40000, [40000]),             # four per row (152 SMs)
+])
+def test_dce_denominator_rows_split_over_clusters(da, orc, dt, N, V, splits):
+    """Few rows of many columns: the denominator splits each row over a cluster of CTAs and
+    adds their digit sums through distributed shared memory; digits, loss and denominator
+    equal the oracle's bit for bit."""
+    g = torch.Generator().manual_seed(51 + N)
+    x = (torch.randn(N, V, generator=g) * 2).to(dt)
+    t = torch.randint(0, V, (N,), generator=g)
+    loss, denom, m, den = da.dce_forward(x.cuda(), t.cuda(), splits=splits)
+    rl, rd, rm, rden, st = orc.DCE(x).forward(t.numpy(), splits=splits)
+    assert_bits_equal(m, rm, "m")
+    assert torch.equal(den.cpu(), torch.from_numpy(rden))
+    assert_bits_equal(loss, rl, "loss")
+    assert torch.equal(denom.cpu(), torch.from_numpy(rd))
+
+
+@cuda
 def test_vocab_sharded_splits_and_oracle(da, orc):
     w = W.vocab_sharded_ce()
     x, t = w.tensors("cuda")
@@ -430,6 +452,17 @@ def test_dce_bad_target(da):
     torch.cuda.synchronize()
     assert da.read_status(st) & da.STATUS_BAD_TARGET
     assert torch.isnan(loss[1]) and torch.isnan(loss[2]) and not torch.isnan(loss[0])
+
+
+@cuda
+def test_packed_exponential_equals_scalar_on_every_bit_pattern(da):
+    """The cross-entropy kernels take the exponentials of two adjacent logits at once on the
+    packed FP32 lanes; on all 2^32 binary32 bit patterns (clamped as the kernels clamp) the
+    packed polynomial value and exponent equal the scalar ones bit for bit (the scalar form is
+    the one the host tests pin to the oracle).  A packed multiply feeding a packed add, fused
+    by the compiler, fails this on 79 patterns."""
+    assert da.probe_exp_pairs(0, 1 << 32) == 0
+    assert da.probe_exp_pairs(0xC2D00000 - 7, 15) == 0   # an odd count around -104
 
 
 @cuda
