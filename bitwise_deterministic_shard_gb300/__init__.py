@@ -92,11 +92,11 @@ def lib():
         L.da_probe_int_mac.argtypes = [_I64, _I32, _P, _P]
         L.da_probe_int_mac_per_thread_iter.restype = C.c_int64
         L.da_probe_bounded_wait.argtypes = [_P, _P]
-        L.da_probe_exp_pairs.argtypes = [C.c_uint32, _I64, _P, _P]
+        L.da_probe_packed.argtypes = [_I32, C.c_uint32, _I64, _P, _P]
         for f in ("da_rowmax", "da_accumulate", "da_compose_max", "da_compose_add", "da_normalize", "da_finalize",
                   "da_det_attn", "da_det_attn_host", "da_det_attn_sharded", "da_accumulate_finalize", "dce_rowmax", "dce_denom_digits", "dce_finalize",
                   "dce_backward", "dce_reduce", "dce_forward_static", "da_probe_int_mac", "da_probe_bounded_wait",
-                  "da_probe_exp_pairs",
+                  "da_probe_packed",
                   "dce_finalize_shard", "dce_backward_shard", "da_rowmax_cached", "da_accumulate_finalize_cached"):
             getattr(L, f).restype = C.c_int
         _lib = L
@@ -713,11 +713,12 @@ def probe_bounded_wait(status=None):
     return read_status(st)
 
 
-def probe_exp_pairs(lo_bits, count):
+def probe_packed(which, lo_bits, count):
     """Number of binary32 bit patterns in [lo_bits, lo_bits + count) whose packed two-lane
-    exponential differs from the scalar one in any bit (0 expected)."""
+    result differs from the scalar one in any bit (0 expected): which 0 the exponential, 1 the
+    backward's quotient."""
     out = torch.zeros(1, dtype=torch.int64, device="cuda")
-    _check(lib().da_probe_exp_pairs(lo_bits & 0xFFFFFFFF, count, _ptr(out), _stream()), "probe_exp_pairs")
+    _check(lib().da_probe_packed(which, lo_bits & 0xFFFFFFFF, count, _ptr(out), _stream()), "probe_packed")
     return int(out.item())
 
 

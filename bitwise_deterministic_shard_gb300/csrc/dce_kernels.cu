@@ -15,6 +15,7 @@
 #include <cooperative_groups.h>
 #include "numerics.cuh"
 #include "divide.cuh"
+#include "fdiv.cuh"
 #include "den_acc.cuh"
 #include "pack2.cuh"
 #include "attn_kernels.h"
@@ -240,9 +241,10 @@ __global__ void dce_finalize_kernel(const DceArgs a) {
 //   dLogits = RN32(go * g),  go = grad[i] ("none"), grad[0] ("sum"), RN32(RN64(grad[0] / N))
 // ("mean").  A logit above the rowmax is clamped like the forward's (violation flag); NaN
 // propagates.  Streaming: 2 B or 4 B read and 2 B or 4 B written per logit; one CTA covers
-// BW_CHUNK columns of one row.  The quotient is rounded straight to binary32 from the row's
-// reciprocal (idiv::div_f32_rn32_direct) and divided exactly only when that rounding is not
-// certain (a quotient within about 2^-27 binary32 ulp of a half-way point, or a subnormal one).
+// BW_CHUNK columns of one row.  The quotient is rounded to binary32 on the FP32 pipe from the
+// row's split divisor with a residual certificate (fdiv.cuh) and divided exactly (integer
+// pipe, divide.cuh) only when that rounding is not certain (a quotient within about 2^-15
+// binary32 ulp of a half-way point, or a subnormal one).
 constexpr int BW_THREADS = 256, BW_PER = 32, BW_CHUNK = BW_THREADS * BW_PER, BW_BATCH = 8;
 
 // VEC: the row and the output row start on 16-byte boundaries and hold a whole number of
@@ -253,7 +255,8 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
                                                                   int reduction, void* __restrict__ dlogits) {
   using T = typename In<DT>::T;
   __shared__ idiv::Divisor sdiv;
-  __shared__ int sslow;
+  __shared__ fdiv::FpDivisor sfd;
+  __shared__ int sslow, sfast;
   __shared__ float sgo;
   const int64_t nch = (a.V + BW_CHUNK - 1) / BW_CHUNK;
   const int64_t i = blockIdx.x / nch, c0 = (blockIdx.x % nch) * BW_CHUNK;
@@ -262,44 +265,38 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
   const int nv = (int)(a.V - c0 < BW_CHUNK ? a.V - c0 : BW_CHUNK);
   const float m = a.m_in[i];
   const double d64 = a.denom[i];
-  if (threadIdx.x == 0) {   // the row's divisor, once per CTA: RN64(w / d64) on the integer pipe
+  if (threadIdx.x == 0) {   // the row's divisor, once per CTA: both forms
     uint64_t dm;
     int de;
     const bool ok = d64 > 0.0 && idiv::split_f64((uint64_t)__double_as_longlong(d64), dm, de);
     sslow = !ok;   // zero, subnormal, negative, infinite or NaN denominators divide in binary64
     if (ok) sdiv = idiv::make_divisor(dm, de);
+    sfast = fdiv::make_fp_divisor(d64, sfd);   // d in [2^-60, 2^60]: the FP32-pipe quotient
     float g0 = reduction == 0 ? grad[i] : grad[0];
     if (reduction == 2) g0 = __double2float_rn(__ddiv_rn((double)g0, (double)a.N));   // once per CTA
     sgo = g0;
   }
   __syncthreads();
   const idiv::Divisor Dv = sdiv;
-  const bool slow = sslow;
+  const fdiv::FpDivisor F = sfd;
+  const bool slow = sslow, fast = sfast;
   const float go = sgo;
   const int64_t tg64 = a.targets[i] - a.v_base - c0;   // the target's column within this chunk (any value)
   const int tg = tg64 >= 0 && tg64 < nv ? (int)tg64 : -1;
   int st = 0;
-  // fin: dLogits of the logit in column v of the chunk, from x = RN32(logit - m) and
-  // exp32_det_poly(max(x, -104)) = (pp, k).  Fast path: the weight as exp32_det's p 2^k (exact
-  // for k >= -125: mantissa of p, exponent of p + k) and its quotient rounded straight from the
-  // row's reciprocal; the exact division and the special cases (NaN, deep or zero weights,
-  // special denominators, an uncertain rounding) otherwise.
-  auto fin = [&](float x, float pp, int k, int v) -> float {
+  // fin: dLogits of the logit in column v of the chunk, from x = RN32(logit - m),
+  // exp32_det_poly(max(x, -104)) = (pp, k) and the FP32-pipe quotient of pp by the row's
+  // denominator (candidate bits qb, residual estimate dl; fdiv.cuh).  Fast path: the weight is
+  // exp32_det's pp 2^k (exact for k >= -125), so RN32(RN64(w / d)) is the certified quotient of
+  // pp times 2^k when that is a normal binary32.  The exact division and the special cases
+  // (NaN, deep or zero weights, special denominators, an uncertain rounding) otherwise.
+  auto fin = [&](float x, int k, uint32_t qb, float dl, int v) -> float {
     // one test for the common case: x <= 0 (not NaN, not above the maximum) and k >= -125 (the
     // weight p 2^k is exact and normal; this also rejects x below about -86.6 and -inf)
-    const uint32_t pbits = __float_as_uint(pp);
-    const int bew = (int)(pbits >> 23) + k;                           // the weight's biased exponent
-    bool ok = !slow && x <= 0.0f && k >= -125;
-    uint32_t q = 0;
-    if (ok) {
-      const uint32_t mw = (pbits & 0x7FFFFFu) | 0x800000u;
-      bool sure;
-      q = idiv::div_f32_rn32_direct(mw, bew - 150, Dv, sure);
-      ok = sure;
-    }
+    const int be = (int)(qb >> 23) + k;   // the quotient's biased exponent after the 2^k
     float p;
-    if (ok) {
-      p = __uint_as_float(q);
+    if (fast && x <= 0.0f && k >= -125 && be >= 1 && fdiv::certain(qb, dl)) {
+      p = __uint_as_float(qb + ((uint32_t)k << 23));
     } else {
       if (x > 0.0f) {   // above the maximum: clamped as in the forward
         st |= ST_VIOLATION;
@@ -324,16 +321,28 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
     const float x = __fsub_rn(__uint_as_float(u), m);
     int k;
     const float pp = exp32_det_poly(fmaxf(x, -104.0f), k);
-    return fin(x, pp, k, v);
+    const float q0 = __fmul_rn(pp, F.r);
+    const float e2 = __fmaf_rn(q0, -F.lo, __fmaf_rn(q0, -F.hi, pp));
+    const float q1 = __fmaf_rn(e2, F.r, q0);
+    return fin(x, k, __float_as_uint(q1), __fmaf_rn(e2, F.r, __fsub_rn(q0, q1)), v);
   };
-  // two adjacent logits (columns v, v + 1), their exponentials on the packed FP32 lanes
+  // two adjacent logits (columns v, v + 1): the exponentials and the quotients on the packed
+  // FP32 lanes (the same operations as `one`, lane by lane; q0 from scalar multiplies, as a
+  // packed multiply feeding the packed subtraction could be fused into it)
   auto two = [&](uint32_t u0, uint32_t u1, int v, float& o0, float& o1) {
+    using namespace f2;
     float x0, x1, p0, p1;
     int k0, k1;
-    f2::unpack(f2::sub(f2::pack(__uint_as_float(u0), __uint_as_float(u1)), f2::splat(m)), x0, x1);
+    unpack(sub(pack(__uint_as_float(u0), __uint_as_float(u1)), splat(m)), x0, x1);
     exp32_det_poly2(fmaxf(x0, -104.0f), fmaxf(x1, -104.0f), p0, p1, k0, k1);
-    o0 = fin(x0, p0, k0, v);
-    o1 = fin(x1, p1, k1, v + 1);
+    const u64 q0 = pack(__fmul_rn(p0, F.r), __fmul_rn(p1, F.r));
+    const u64 e2 = fma(q0, splat(-F.lo), fma(q0, splat(-F.hi), pack(p0, p1)));
+    const u64 q1 = fma(e2, splat(F.r), q0);
+    float qa, qb, da, db;
+    unpack(q1, qa, qb);
+    unpack(fma(e2, splat(F.r), sub(q0, q1)), da, db);
+    o0 = fin(x0, k0, __float_as_uint(qa), da, v);
+    o1 = fin(x1, k1, __float_as_uint(qb), db, v + 1);
   };
   if constexpr (VEC) {
     constexpr int EV = 16 / (int)sizeof(T), NV = BW_PER / EV;

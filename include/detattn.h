@@ -290,8 +290,8 @@ int dce_forward_static(const da_matrix* logits, const int64_t* targets, float* l
 
 /* ---- Probes.  None computes anything of the method, and the pages have no counterpart
  * of them: one measures a hardware rate the benchmark reports against, one exercises the
- * bounded-wait path of the pipelined kernels, one checks the packed two-lane form of the
- * exponential against the scalar form. ---- */
+ * bounded-wait path of the pipelined kernels, one checks the packed two-lane forms of the
+ * cross-entropy arithmetic against the scalar forms. ---- */
 
 /* Issue rate of exact 32 x 32 -> 64-bit integer multiply-adds (mad.wide.s32): nblocks CTAs of
  * 512 threads each run iters iterations of da_probe_int_mac_per_thread_iter() independent
@@ -302,14 +302,17 @@ int da_probe_int_mac(int64_t iters, int nblocks, int64_t* sink, da_stream_t stre
 int64_t da_probe_int_mac_per_thread_iter(void);
 
 /* The cross-entropy kernels evaluate the exponentials of two adjacent logits (page
- * "det-cross-entropy", section "Method": the weight exp32_det(RN32(x - m))) at once on the
- * packed FP32 instructions.  This runs the packed and the scalar device forms of the
- * reduction and polynomial on every binary32 bit pattern lo_bits, lo_bits + 1, ...,
- * lo_bits + count - 1 (mod 2^32; NaN taken as -inf, then clamped to [-104, 0] as the kernels
- * clamp) and adds to *mismatches (device int64 [1], 8-byte aligned, not cleared here) the
- * number of patterns whose polynomial value or exponent differ in any bit.
- * DA_EINVAL for count outside [0, 2^32] or a null pointer. */
-int da_probe_exp_pairs(uint32_t lo_bits, int64_t count, int64_t* mismatches, da_stream_t stream);
+ * "det-cross-entropy", section "Method": the weight exp32_det(RN32(x - m))), and the backward
+ * their quotients by the row's denominator, two at a time on the packed FP32 instructions.
+ * This runs the packed and the scalar device forms on every binary32 bit pattern lo_bits,
+ * lo_bits + 1, ..., lo_bits + count - 1 (mod 2^32) and adds to *mismatches (device int64 [1],
+ * 8-byte aligned, not cleared here) the number of patterns whose results differ in any bit.
+ * which 0: the reduction and polynomial of the exponential, the pattern read as x (NaN taken
+ * as -inf, then clamped to [-104, 0] as the kernels clamp).  which 1: the quotient candidate
+ * and its residual estimate, the pattern's low 24 bits giving p in [0.5, 2) and a hash of it
+ * the divisor in [1, 2^21).  DA_EINVAL for which outside {0, 1}, count outside [0, 2^32] or a
+ * null pointer. */
+int da_probe_packed(int which, uint32_t lo_bits, int64_t count, int64_t* mismatches, da_stream_t stream);
 
 /* One warp waits on an mbarrier phase that nothing completes, through the bounded wait the
  * pipelined kernels use (it gives up after about 2 s).  The kernel then ends normally and

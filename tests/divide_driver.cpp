@@ -2,10 +2,12 @@
 // seeded random and edge-case inputs with the helpers' results, which test_divide_host.py
 // checks against exact rational arithmetic.
 #include <cstdio>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <cstdlib>
 #include "divide.cuh"
+#include "fdiv.cuh"
 using namespace detattn::idiv;
 static uint64_t s = 88172645463325252ull;
 static uint64_t rnd() { s ^= s << 13; s ^= s >> 7; s ^= s << 17; return s; }
@@ -140,6 +142,37 @@ int main(int argc, char** argv) {
       const uint32_t fast = div_rn64_rn32_direct(mn, en, D, neg, ok);
       printf("%llu %d %llu %d %d %d %u %u\n", (unsigned long long)mn, en, (unsigned long long)md, ed, (int)neg, (int)ok,
              fast, rn32_bits(q, E, neg));
+    }
+  } else if (mode == 8) {   // the FP32-pipe quotient with its certificate against the exact one
+    auto f64 = [](uint64_t b) { double d; memcpy(&d, &b, 8); return d; };
+    auto b64 = [](double d) { uint64_t b; memcpy(&b, &d, 8); return b; };
+    auto f32 = [](uint32_t b) { float f; memcpy(&f, &b, 4); return f; };
+    for (long i = 0; i < n; i++) {
+      const int kind = (int)(i % 4);
+      uint32_t pb = (uint32_t)(126 + (int)(rnd() & 1)) << 23 | ((uint32_t)rnd() & 0x7FFFFFu);   // p in [0.5, 2)
+      double d;
+      if (kind == 0) {          // denominators of ordinary size, [1, 2^20)
+        d = f64(((uint64_t)(1023 + rnd() % 20) << 52) | (rnd() >> 12));
+      } else if (kind == 1) {   // the whole accepted range [2^-60, 2^60] and a little outside it
+        d = f64(((uint64_t)(1023 - 62 + rnd() % 125) << 52) | (rnd() >> 12));
+      } else if (kind == 2) {   // quotients within about 2^-53 of a binary32 half-way point
+        const int E = -(int)(rnd() % 20);
+        const uint64_t mid = (((rnd() >> 40) & 0x7FFFFFull) | 0x800000ull) * 2 + 1;   // 25 bits, odd
+        const double M = std::ldexp((double)mid, E - 24);
+        d = f64(b64(f32(pb) / M) + (rnd() % 5) - 2);
+      } else {                  // d a binary32 (d_lo = 0), a power of two, or p itself
+        const int c = (int)(rnd() % 3);
+        d = c == 0 ? (double)f32(((uint32_t)(127 + rnd() % 17) << 23) | ((uint32_t)rnd() & 0x7FFFFFu))
+                   : c == 1 ? std::ldexp(1.0, (int)(rnd() % 41) - 20) : (double)f32(pb);
+      }
+      detattn::fdiv::FpDivisor F;
+      bool ok = false;
+      uint32_t fast = 0;
+      if (detattn::fdiv::make_fp_divisor(d, F)) fast = detattn::fdiv::div_rn32(f32(pb), F, ok);
+      uint64_t md; int ed; split_f64(b64(d), md, ed);
+      Divisor D = make_divisor(md, ed);
+      uint32_t mw; int ew; split_f32_24(pb, mw, ew);
+      printf("%u %llu %d %u %u\n", pb, (unsigned long long)b64(d), (int)ok, fast, div_f32_rn32(mw, ew, D));
     }
   } else if (mode == 3) {   // f32 split
     for (long i = 0; i < n; i++) {

@@ -106,9 +106,11 @@ def test_probe_arguments_rejected_before_any_launch(libpath):
     assert L.da_probe_int_mac(8, 4, None, None) == 1                        # null sink
     assert L.da_probe_int_mac(8, 4, ctypes.c_void_p(4100), None) == 4      # misaligned sink
     assert L.da_probe_bounded_wait(None, None) == 1
-    assert L.da_probe_exp_pairs(0, -1, ctypes.c_void_p(4096), None) == 1
-    assert L.da_probe_exp_pairs(0, (1 << 32) + 1, ctypes.c_void_p(4096), None) == 1
-    assert L.da_probe_exp_pairs(0, 8, None, None) == 1
-    assert L.da_probe_exp_pairs(0, 8, ctypes.c_void_p(4100), None) == 4
+    assert L.da_probe_packed(0, 0, -1, ctypes.c_void_p(4096), None) == 1
+    assert L.da_probe_packed(0, 0, (1 << 32) + 1, ctypes.c_void_p(4096), None) == 1
+    assert L.da_probe_packed(2, 0, 8, ctypes.c_void_p(4096), None) == 1
+    assert L.da_probe_packed(-1, 0, 8, ctypes.c_void_p(4096), None) == 1
+    assert L.da_probe_packed(1, 0, 8, None, None) == 1
+    assert L.da_probe_packed(1, 0, 8, ctypes.c_void_p(4100), None) == 4
     assert L.da_probe_int_mac_per_thread_iter() == 32
     assert "da_probe_int_mac_per_thread_iter" in _declared()

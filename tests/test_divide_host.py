@@ -24,8 +24,8 @@ def drv(tmp_path_factory):
     if cxx is None:
         pytest.skip("g++ not available")
     exe = str(tmp_path_factory.mktemp("divide") / "drv")
-    subprocess.run([cxx, "-O2", "-std=c++17", "-I", CSRC, os.path.join(HERE, "divide_driver.cpp"), "-o", exe],
-                   check=True)
+    subprocess.run([cxx, "-O2", "-std=c++17", "-ffp-contract=off", "-I", CSRC, os.path.join(HERE, "divide_driver.cpp"),
+                    "-o", exe], check=True)
 
     def run(mode, n):
         return subprocess.run([exe, str(mode), str(n)], capture_output=True, text=True, check=True).stdout.splitlines()
@@ -148,3 +148,29 @@ def test_direct_binary32_of_binary64_quotient(drv):
     assert taken[0][1] == taken[0][0], taken     # ordinary quotients: always direct here
     assert taken[2][1] == 0, taken               # near half-way points: always exact
     assert taken[3][1] == taken[3][0], taken     # exact quotients are decided directly
+
+
+def test_fp32_pipe_quotient_with_certificate(drv):
+    """fdiv::div_rn32 (the dLogits fast path on the FP32 pipe): whenever its certificate holds,
+    its bits equal the exact division's (div_f32_rn32, itself pinned to exact rationals above),
+    and every fourth case plus every near-half-way case is also checked against
+    RN32(RN64(p / d)) from CPython's exact arithmetic.  Quotients within about 2^-53 of a
+    binary32 half-way point must fail the certificate; for ordinary denominators it fails
+    about once in 2^15 quotients."""
+    taken = [[0, 0] for _ in range(4)]
+    for k, line in enumerate(drv(8, 200000)):
+        pb, db, ok, fast, exact = map(int, line.split())
+        kind = k % 4
+        taken[kind][0] += 1
+        taken[kind][1] += ok
+        if ok:
+            assert fast == exact, line
+        if k % 4 == 0 or kind == 2:
+            p = Fraction(struct.unpack("<f", struct.pack("<I", pb))[0])
+            d = Fraction(struct.unpack("<d", struct.pack("<Q", db))[0])
+            q = p / d
+            q64 = q.numerator / q.denominator                  # RN64 of the exact quotient
+            assert exact == struct.unpack("<I", struct.pack("<f", np.float32(q64)))[0], line
+    assert taken[0][1] >= 0.999 * taken[0][0], taken        # ordinary denominators: rarely exact
+    assert taken[1][1] >= 0.95 * taken[1][0], taken         # the whole range (a few outside it)
+    assert taken[2][1] <= 0.001 * taken[2][0], taken        # near half-way points: never certified

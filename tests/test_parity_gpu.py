@@ -455,14 +455,16 @@ def test_dce_bad_target(da):
 
 
 @cuda
-def test_packed_exponential_equals_scalar_on_every_bit_pattern(da):
-    """The cross-entropy kernels take the exponentials of two adjacent logits at once on the
-    packed FP32 lanes; on all 2^32 binary32 bit patterns (clamped as the kernels clamp) the
-    packed polynomial value and exponent equal the scalar ones bit for bit (the scalar form is
-    the one the host tests pin to the oracle).  A packed multiply feeding a packed add, fused
-    by the compiler, fails this on 79 patterns."""
-    assert da.probe_exp_pairs(0, 1 << 32) == 0
-    assert da.probe_exp_pairs(0xC2D00000 - 7, 15) == 0   # an odd count around -104
+def test_packed_forms_equal_scalar_on_every_bit_pattern(da):
+    """The cross-entropy kernels take two adjacent logits at once on the packed FP32 lanes: on
+    all 2^32 binary32 bit patterns the packed exponential (reduction, polynomial, exponent;
+    arguments clamped as the kernels clamp) and the backward's packed quotient and residual
+    estimate equal the scalar forms bit for bit (the scalar forms are the ones the host tests
+    pin to the oracle and to exact rationals).  A packed multiply feeding a packed add, fused
+    by the compiler, fails the first on 79 patterns."""
+    assert da.probe_packed(0, 0, 1 << 32) == 0
+    assert da.probe_packed(0, 0xC2D00000 - 7, 15) == 0   # an odd count around -104
+    assert da.probe_packed(1, 0, 1 << 32) == 0
 
 
 @cuda
