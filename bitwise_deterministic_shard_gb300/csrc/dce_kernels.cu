@@ -123,15 +123,16 @@ __global__ void __launch_bounds__(DEN_THREADS, 6) dce_denom_kernel(const DceArgs
   DenAcc A;   // exact: a private word for w >= 2^-31, digit words for the rest (den_acc.cuh)
   den_init(A);
   int st = 0;
-  // common case, one test: a finite logit at most about 21.5 below the maximum (x <= 0 and a
-  // weight w >= 2^-31).  The weight is exp32_det's p 2^k (exact for k >= -125), so its
-  // mantissa goes straight into the private word (den_add's first case, without forming w).
-  // A NaN or infinite logit, one above the maximum, or a smaller weight fails the test.
+  // common case, one unsigned test on the bits of x = RN32(logit - m): x in [-21.4, -0].  Then
+  // the weight w = exp32_det(x) is at least 2^-31 (exp(-21.4) > 2^-31) and exp32_det's p 2^k
+  // (exact for k >= -125), so its mantissa goes straight into the private word, shifted by
+  // sh = (biased exponent of w) - 96 >= 0 (den_add's first case, without forming w).  NaN,
+  // infinite, above-maximum and +0 logits and smaller weights take the general handling; the
+  // packed evaluation runs on x unclamped, and its values are used only inside the range.
   auto fast = [&](float x, float p, int k) -> bool {
-    const uint32_t pbits = __float_as_uint(p);
-    const int sh = (int)(pbits >> 23) + k - 96;
-    if (x <= 0.0f && sh >= 0) {
-      A.U += (uint64_t)((pbits & 0x7FFFFFu) | 0x800000u) << sh;
+    if (__float_as_uint(x) - 0x80000000u <= 0x41AB3333u) {   // -21.4f = 0xC1AB3333
+      const uint32_t pbits = __float_as_uint(p);
+      A.U += (uint64_t)((pbits & 0x7FFFFFu) | 0x800000u) << ((int)(pbits >> 23) + k - 96);
       return true;
     }
     return false;
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(DEN_THREADS, 6) dce_denom_kernel(const DceArgs
                  float x0, x1, p0, p1;
                  int k0, k1;
                  f2::unpack(f2::sub(f2::pack(__uint_as_float(u0), __uint_as_float(u1)), f2::splat(m)), x0, x1);
-                 exp32_det_poly2(fmaxf(x0, -104.0f), fmaxf(x1, -104.0f), p0, p1, k0, k1);
+                 exp32_det_poly2(x0, x1, p0, p1, k0, k1);
                  if (!fast(x0, p0, k0)) general(u0, x0);
                  if (!fast(x1, p1, k1)) general(u1, x1);
                },
@@ -291,11 +292,12 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
   // pp times 2^k when that is a normal binary32.  The exact division and the special cases
   // (NaN, deep or zero weights, special denominators, an uncertain rounding) otherwise.
   auto fin = [&](float x, int k, uint32_t qb, float dl, int v) -> float {
-    // one test for the common case: x <= 0 (not NaN, not above the maximum) and k >= -125 (the
-    // weight p 2^k is exact and normal; this also rejects x below about -86.6 and -inf)
+    // the common case: x in [-86.5, -0] (one unsigned test on its bits: not NaN, not infinite,
+    // not above the maximum), so k >= -125 and the weight p 2^k is exact and normal; the
+    // exponential and the quotient were evaluated on x unclamped and are used only then
     const int be = (int)(qb >> 23) + k;   // the quotient's biased exponent after the 2^k
     float p;
-    if (fast && x <= 0.0f && k >= -125 && be >= 1 && fdiv::certain(qb, dl)) {
+    if (fast && __float_as_uint(x) - 0x80000000u <= 0x42AD0000u && be >= 1 && fdiv::certain(qb, dl)) {   // -86.5f
       p = __uint_as_float(qb + ((uint32_t)k << 23));
     } else {
       if (x > 0.0f) {   // above the maximum: clamped as in the forward
@@ -334,7 +336,7 @@ __global__ void __launch_bounds__(BW_THREADS) dce_backward_kernel(const DceArgs 
     float x0, x1, p0, p1;
     int k0, k1;
     unpack(sub(pack(__uint_as_float(u0), __uint_as_float(u1)), splat(m)), x0, x1);
-    exp32_det_poly2(fmaxf(x0, -104.0f), fmaxf(x1, -104.0f), p0, p1, k0, k1);
+    exp32_det_poly2(x0, x1, p0, p1, k0, k1);
     const u64 q0 = pack(__fmul_rn(p0, F.r), __fmul_rn(p1, F.r));
     const u64 e2 = fma(q0, splat(-F.lo), fma(q0, splat(-F.hi), pack(p0, p1)));
     const u64 q1 = fma(e2, splat(F.r), q0);

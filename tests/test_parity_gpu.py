@@ -356,6 +356,28 @@ def test_empty_and_edge_ranges(da, orc):
 
 
 @cuda
+@pytest.mark.parametrize("D", [64, 128])
+def test_key_ranges_at_and_beyond_the_tensor_pv_limit(da, orc, D):
+    """65,536 keys (512 key tiles) is the longest range the tensor-PV kernel takes, with the
+    score cache and the fused finalize; one key tile more sends the call to the integer-pipe
+    kernel (digits in device memory, then finalize).  Both, and a sharded call whose shards
+    lie on either side of the limit, equal the oracle bit for bit."""
+    g = torch.Generator().manual_seed(60 + D)
+    Sq = 24
+    for Skv in (65536, 65536 + 131):
+        Q = torch.randn(1, 1, Sq, D, generator=g).to(torch.bfloat16)
+        K = torch.randn(1, 1, Skv, D, generator=g).to(torch.bfloat16)
+        V = torch.randn(1, 1, Skv, D, generator=g).to(torch.bfloat16)
+        Qd, Kd, Vd = Q.cuda(), K.cuda(), V.cuda()
+        out = da.det_attn(Qd, Kd, Vd)
+        _, _, _, ref = orc.Attn(Q, K, V).forward_rows()
+        assert_bits_equal(out.reshape(-1, D), ref, f"{Skv} keys, D = {D}")
+        if Skv > 65536:
+            assert torch.equal(da.det_attn_sharded(Qd, Kd, Vd, [131, 65536]), out)
+            assert torch.equal(da.det_attn_sharded(Qd, Kd, Vd, [65536, 131]), out)
+
+
+@cuda
 def test_status_bits(da):
     Q, K, V = W.random_attn(47, 1, 1, 1, 40, 16, torch.bfloat16, False)
     Qd, Kd, Vd = Q.cuda(), K.cuda(), V.cuda()
