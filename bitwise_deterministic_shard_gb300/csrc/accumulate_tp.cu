@@ -698,8 +698,32 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
               long long sum[NW][3];
   #pragma unroll
               for (int c = 0; c < NW; c++) sum[c][0] = sum[c][1] = sum[c][2] = 0;
+              // SC: the Vint rows of up to TB pending keys at a time are staged in this warp's part of
+              // the element-list room (unused during the tile loop) by asynchronous copies issued
+              // together, so a row whose weights are nearly all tiny pays one memory latency per TB keys
+              constexpr int TB = 4;
+              int* stg = SC ? reinterpret_cast<int*>(smem_p + L::e_off) + warp * (TB * DP) : nullptr;
+              uint32_t staged = 0;   // the keys of the current batch (SC)
               for (; pend; pend &= pend - 1) {
                 const int src = __ffs(pend) - 1, jj = kt + 32 * quarter + src;
+                if constexpr (SC) {
+                  if (!((staged >> src) & 1u)) {   // a new batch: the next TB pending keys
+                    __syncwarp();                  // the previous batch's rows are read
+                    staged = 0;
+                    uint32_t q = pend;
+  #pragma unroll
+                    for (int u = 0; u < TB; u++) {
+                      if (q) {
+                        const int su = __ffs(q) - 1;
+                        staged |= 1u << su;
+                        cp_async16(stg + u * DP + 4 * lane, p.vint + (krow0 + kt + 32 * quarter + su) * DP + 4 * lane, 16);
+                        q &= q - 1;
+                      }
+                    }
+                    cp_async_wait_all();
+                    __syncwarp();
+                  }
+                }
                 const uint32_t wb = __float_as_uint(__shfl_sync(0xFFFFFFFFu, w[e], src));
                 const Split sw = split_f32(wb);
                 if (lane == 0) atomic_digits_add(slot_den(rl), 1, DEN_E0, sw.mant, 0, sw.lsb);
@@ -710,7 +734,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
                   const bool low = b0 < 4;
                   const long long w0 = low ? (long long)(uint32_t)y : 0, w1 = low ? (long long)(y >> 32) : (long long)(uint32_t)y,
                                   w2 = low ? 0 : (long long)(y >> 32);
-                  const int* vrow = p.vint + (krow0 + jj) * DP;
+                  const int* vrow = SC ? stg + __popc(staged & ((1u << src) - 1u)) * DP : p.vint + (krow0 + jj) * DP;
   #pragma unroll
                   for (int c = 0; c < NW; c++) {   // |Vint| < 2^23, words < 2^32: 32 products stay below 2^60
                     const long long vi = vrow[lane + 32 * c];
