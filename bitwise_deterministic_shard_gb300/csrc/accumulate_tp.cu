@@ -289,20 +289,22 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int h = blockIdx.y, b = blockIdx.z, hk = h / (a.Hq / a.Hkv);
-  // Row, output and spill-slot addresses are recomputed where they are used (the block
-  // indices read through volatile moves, which the compiler does not hoist), so the compute
-  // warps do not hold them in registers across the tile loop.
-  auto cta_y = []() {
-    uint32_t v;
-    asm volatile("mov.u32 %0, %%ctaid.y;" : "=r"(v));
-    return (int64_t)v;
-  };
-  auto cta_z = []() {
-    uint32_t v;
-    asm volatile("mov.u32 %0, %%ctaid.z;" : "=r"(v));
-    return (int64_t)v;
-  };
+  // This CTA's work item: query-tile pair (causal) or query tile bx of head h, batch b, taken
+  // from a.order when it is set (the heaviest items first), else in launch order.
+  const int ntq = (a.Sq + BM - 1) / BM;
+  const int nx = a.causal ? (ntq + 1) / 2 : ntq;
+  const int item = a.order ? __ldg(a.order + blockIdx.x) : (int)blockIdx.x;
+  const int bx = item % nx, h = (item / nx) % a.Hq, b = item / (nx * a.Hq), hk = h / (a.Hq / a.Hkv);
+  __shared__ int s_hb[2];
+  if (tid == 0) {
+    s_hb[0] = h;
+    s_hb[1] = b;
+  }
+  // Row, output and spill-slot addresses are recomputed where they are used (head and batch
+  // read back through volatile shared-memory loads, which the compiler does not hoist), so the
+  // compute warps do not hold them in registers across the tile loop.
+  auto cta_y = [&]() { return (int64_t)*reinterpret_cast<volatile int*>(&s_hb[0]); };
+  auto cta_z = [&]() { return (int64_t)*reinterpret_cast<volatile int*>(&s_hb[1]); };
   auto qrow = [&](int i) { return (const T*)a.q + cta_z() * a.qs[0] + cta_y() * a.qs[1] + (int64_t)i * a.qs[2]; };
   auto krow = [&](int j) {
     return (const T*)a.k + cta_z() * a.ks[0] + (cta_y() / (a.Hq / a.Hkv)) * a.ks[1] + (int64_t)j * a.ks[2];
@@ -367,8 +369,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   tc5::fence_after();
 
   int nf = 0, viol = 0;
-  const int ntq = (a.Sq + BM - 1) / BM;
-  const int npass = (a.causal && (int)blockIdx.x != ntq - 1 - (int)blockIdx.x) ? 2 : 1;
+  const int npass = (a.causal && bx != ntq - 1 - bx) ? 2 : 1;
   // Register split: the control warpgroup (copies, MMA issue) runs on 32 registers a thread,
   // the four compute warpgroups on 112 (640 x 96 at launch = 128 x 32 + 512 x 112).  Each
   // role runs its own pass loop; named barrier 2 opens a pass (query operand and per-pass
@@ -378,7 +379,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
     uint32_t tc = 0;   // key tiles of earlier passes
     uint32_t pc = 0;   // SC: PV buffer pairs of earlier passes
     for (int pass = 0; pass < npass; pass++) {
-      const int q0 = (pass == 0 ? ntq - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
+      const int q0 = (pass == 0 ? ntq - 1 - bx : bx) * BM;
       const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
       const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
       tc5::bar_sync(2, L::THREADS);
@@ -455,7 +456,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
     uint32_t tc = 0;   // key tiles of earlier passes
     uint32_t pcd = 0;   // SC: the next PV buffer pair to drain (pairs of earlier passes included)
     for (int pass = 0; pass < npass; pass++) {
-      const int q0 = (pass == 0 ? ntq - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
+      const int q0 = (pass == 0 ? ntq - 1 - bx : bx) * BM;
       const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
       const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
       const int nrows = min(BM, a.Sq - q0);
@@ -1039,8 +1040,66 @@ static cudaError_t launch_acc_tp_t(const AttnArgs& a, const KvPrep& p, cudaStrea
   e = cudaMemsetAsync(p.spill, 0, (size_t)SPILL_SLOTS * spill_slot_words(L::DP) * sizeof(long long), st);
   if (e != cudaSuccess) return e;
   const int nt = (a.Sq + L::BM - 1) / L::BM;
-  dim3 grid(a.causal ? (nt + 1) / 2 : nt, a.Hq, a.B);
-  accumulate_tp_kernel<DT, SC><<<grid, L::THREADS, L::bytes, st>>>(a, p);
+  const int64_t nitems = (int64_t)(a.causal ? (nt + 1) / 2 : nt) * a.Hq * a.B;   // one CTA per work item
+  accumulate_tp_kernel<DT, SC><<<(unsigned)nitems, L::THREADS, L::bytes, st>>>(a, p);
+  return cudaGetLastError();
+}
+
+// ---- work order ----
+// A work item whose rows have a rowmax far above the rest of their scores has most of its
+// weights below the 2^-56 window, and those take the exact per-pair path: such an item runs
+// several times longer than the others.  Launched late it leaves the GPU idle behind it, so the
+// items whose largest rowmax lies within 10 of the largest of the call go first.  The order
+// only schedules the same work: the output does not depend on it.
+static int tp_nx(const AttnArgs& a) {
+  const int nt = (a.Sq + AccTpLayout::BM - 1) / AccTpLayout::BM;
+  return a.causal ? (nt + 1) / 2 : nt;
+}
+
+__global__ void tp_item_keys_kernel(const AttnArgs a, int nx, int nitems, int* keys, int* gmax) {
+  constexpr int BM = AccTpLayout::BM;
+  const int it = blockIdx.x * blockDim.x + threadIdx.x;
+  if (it >= nitems) return;
+  const int ntq = (a.Sq + BM - 1) / BM;
+  const int bx = it % nx, h = (it / nx) % a.Hq, b = it / (nx * a.Hq);
+  const float* mr = a.m_in + ((int64_t)b * a.Hq + h) * a.Sq;
+  int key = float_key(neg_inf());
+  for (int pass = 0; pass < 2; pass++) {
+    const int qt = pass == 0 ? (a.causal ? ntq - 1 - bx : bx) : bx;
+    if (pass == 1 && (!a.causal || qt == ntq - 1 - bx)) break;
+    for (int i = qt * BM; i < min(a.Sq, qt * BM + BM); i++) {
+      const float m = mr[i];
+      if (m == m) key = max(key, float_key(m));
+    }
+  }
+  keys[it] = key;
+  atomicMax(gmax, key);
+}
+
+__global__ void tp_item_order_kernel(int nitems, const int* keys, int* counters, int* order) {
+  const int it = blockIdx.x * blockDim.x + threadIdx.x;
+  if (it >= nitems) return;
+  const int thr = float_key(__fsub_rn(key_float(counters[0]), 10.0f));
+  const int pos = keys[it] >= thr ? atomicAdd(&counters[1], 1) : nitems - 1 - atomicAdd(&counters[2], 1);
+  order[pos] = it;
+}
+
+size_t tp_order_bytes(const AttnArgs& a) {
+  const int64_t nitems = (int64_t)tp_nx(a) * a.Hq * a.B;
+  return 16 + (size_t)nitems * 8;
+}
+
+cudaError_t launch_tp_order(AttnArgs& a, void* ws, cudaStream_t st) {
+  const int64_t nitems = (int64_t)tp_nx(a) * a.Hq * a.B;
+  int* counters = (int*)ws;   // largest key (+0 to start), heavy and light positions taken
+  int* keys = counters + 4;
+  int* order = keys + nitems;
+  cudaError_t e = cudaMemsetAsync(counters, 0, 16, st);
+  if (e != cudaSuccess) return e;
+  const unsigned blocks = (unsigned)((nitems + 255) / 256);
+  tp_item_keys_kernel<<<blocks, 256, 0, st>>>(a, tp_nx(a), (int)nitems, keys, counters);
+  tp_item_order_kernel<<<blocks, 256, 0, st>>>((int)nitems, keys, counters, order);
+  a.order = order;
   return cudaGetLastError();
 }
 

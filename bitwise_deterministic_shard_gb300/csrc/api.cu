@@ -311,6 +311,9 @@ DA_EXPORT int da_accumulate_finalize_cached(const da_attn_desc* desc, const floa
   sc_bytes(desc, &a.sc_nkt, &a.sc_per_bh);
   KvPrep p = kv_prep_layout(base + w.kv, a.B, a.Hkv, a.Skv, a.D, 1);   // prepared by da_rowmax_cached
   if (!accumulate_is_tp(a, p)) return DA_EINVAL;
+  // the work order lives in the NUM digit room, which the fused finalize never writes
+  if (tp_order_bytes(a) <= w.den - w.num && (e = launched(launch_tp_order(a, base + w.num, (cudaStream_t)stream))))
+    return e;
   return launched(launch_accumulate(a, p, (cudaStream_t)stream));
 }
 

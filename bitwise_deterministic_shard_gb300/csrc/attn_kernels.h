@@ -29,6 +29,7 @@ struct AttnArgs {
                                  // accumulate reads it instead of recomputing the scores
   int64_t sc_per_bh;             // score-cache blocks per (b, query head)
   int sc_nkt;                    // non-causal: key tiles per query tile
+  const int* order;              // tensor-PV accumulate: its work items in this order (null: launch order)
 };
 
 // Score cache of one whole-range call (kv_lo = 0, kv_hi = Skv; causal needs Sq = Skv): the
@@ -85,6 +86,9 @@ cudaError_t launch_rowmax(const AttnArgs& a, const KvPrep& p, cudaStream_t st); 
 cudaError_t launch_accumulate(const AttnArgs& a, const KvPrep& p, cudaStream_t st);
 cudaError_t launch_accumulate_tc(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // D <= 128
 cudaError_t launch_accumulate_tp(const AttnArgs& a, const KvPrep& p, cudaStream_t st);   // D <= 128
+// the tensor-PV accumulate's work items, heaviest first, into ws (tp_order_bytes): a.order set
+size_t tp_order_bytes(const AttnArgs& a);
+cudaError_t launch_tp_order(AttnArgs& a, void* ws, cudaStream_t st);
 constexpr int ACC_TP_MAX_TILES = 512;   // key tiles per pass the tensor-PV kernel's state holds exactly
 bool accumulate_is_tp(const AttnArgs& a, const KvPrep& p);   // launch_accumulate takes the tensor-PV kernel
 
