@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "../../include/detattn.h"
@@ -341,6 +342,47 @@ bool dense(const da_tensor& t) {   // [B, H, S, D] contiguous
 // det_attn with host buffers, split into groups of whole (batch, KV head) units: the flattened
 // units [u0, u1) are contiguous in Q, K, V and the output, and each group is an independent
 // det_attn problem (one batch of (u1 - u0) KV heads and their query heads).
+// Streams for the host-buffer path's groups, created once per device and reused: creating
+// them on every call costs host time while the first groups' work already runs.  A call takes
+// what it needs and gives it back; calls from several host threads each get their own.
+struct StreamPool {
+  std::mutex mu;
+  std::vector<std::pair<int, cudaStream_t>> free;   // (device, stream)
+};
+StreamPool& stream_pool() {
+  static StreamPool* p = new StreamPool;   // never destroyed: streams outlive static destructors
+  return *p;
+}
+int take_streams(int n, std::vector<cudaStream_t>& out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DA_ECUDA;
+  StreamPool& p = stream_pool();
+  {
+    std::lock_guard<std::mutex> lk(p.mu);
+    for (size_t i = 0; i < p.free.size() && (int)out.size() < n;) {
+      if (p.free[i].first == dev) {
+        out.push_back(p.free[i].second);
+        p.free.erase(p.free.begin() + (long)i);
+      } else {
+        i++;
+      }
+    }
+  }
+  while ((int)out.size() < n) {
+    cudaStream_t s = nullptr;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return DA_ECUDA;
+    out.push_back(s);
+  }
+  return DA_OK;
+}
+void give_streams(const std::vector<cudaStream_t>& in) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return;
+  StreamPool& p = stream_pool();
+  std::lock_guard<std::mutex> lk(p.mu);
+  for (cudaStream_t s : in) p.free.emplace_back(dev, s);
+}
+
 struct HostPlan {
   int64_t units, per, ngroups;       // units = B * Hkv; per = units per group
   size_t qb, kb, ob;                 // bytes of one unit's query rows, key (= value) rows, output rows
@@ -424,40 +466,46 @@ DA_EXPORT int da_det_attn_host(const da_attn_desc* desc, float* out, int ngroups
   auto run = [&]() -> int {
     cudaEvent_t start = event();
     if (!start || cudaEventRecord(start, st) != cudaSuccess) return DA_ECUDA;
+    if (int r = take_streams((int)p.ngroups, gs)) return r;
     const char* qh = (const char*)desc->q.ptr;
     const char* kh = (const char*)desc->k.ptr;
     const char* vh = (const char*)desc->v.ptr;
+    // One stream per group: its inputs up, its det_attn (own workspace), its output down; the
+    // groups' streams run side by side, so one group's copies overlap another's kernels and the
+    // kernels of several groups fill each other's tails.  Every group's uploads are enqueued
+    // before any kernel, so the copy engines have them all from the start (chaining them one
+    // group after another measured slower).
     for (int64_t g = 0; g < p.ngroups; g++) {
-      // one stream per group: its inputs up, its det_attn (own workspace), its output down;
-      // the groups' streams run side by side, so one group's copies overlap another's kernels
-      // and the kernels of several groups fill each other's tails
-      cudaStream_t s = nullptr;
-      if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return DA_ECUDA;
-      gs.push_back(s);
-      if (cudaStreamWaitEvent(s, start, 0) != cudaSuccess) return DA_ECUDA;
       const int64_t u0 = g * p.per, n = std::min(p.per, p.units - u0);
-      char* qd = base + p.q_off + u0 * p.qb;
-      char* kd = base + p.k_off + u0 * p.kb;
-      char* vd = base + p.v_off + u0 * p.kb;
-      float* od = (float*)(base + p.o_off + u0 * p.ob);
-      if (cudaMemcpyAsync(qd, qh + u0 * p.qb, n * p.qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-          cudaMemcpyAsync(kd, kh + u0 * p.kb, n * p.kb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-          cudaMemcpyAsync(vd, vh + u0 * p.kb, n * p.kb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      if (cudaStreamWaitEvent(gs[g], start, 0) != cudaSuccess ||
+          cudaMemcpyAsync(base + p.q_off + u0 * p.qb, qh + u0 * p.qb, n * p.qb, cudaMemcpyHostToDevice, gs[g]) !=
+              cudaSuccess ||
+          cudaMemcpyAsync(base + p.k_off + u0 * p.kb, kh + u0 * p.kb, n * p.kb, cudaMemcpyHostToDevice, gs[g]) !=
+              cudaSuccess ||
+          cudaMemcpyAsync(base + p.v_off + u0 * p.kb, vh + u0 * p.kb, n * p.kb, cudaMemcpyHostToDevice, gs[g]) !=
+              cudaSuccess)
         return DA_ECUDA;
-      const da_attn_desc gd = group_desc(desc, qd, kd, vd, n);
-      const int r = da_det_attn(&gd, od, base + p.w_off + g * round_up(p.w_bytes), p.w_bytes, (da_stream_t)s);
+    }
+    for (int64_t g = 0; g < p.ngroups; g++) {
+      const int64_t u0 = g * p.per, n = std::min(p.per, p.units - u0);
+      float* od = (float*)(base + p.o_off + u0 * p.ob);
+      const da_attn_desc gd = group_desc(desc, base + p.q_off + u0 * p.qb, base + p.k_off + u0 * p.kb,
+                                         base + p.v_off + u0 * p.kb, n);
+      const int r = da_det_attn(&gd, od, base + p.w_off + g * round_up(p.w_bytes), p.w_bytes, (da_stream_t)gs[g]);
       if (r) return r;
-      if (cudaMemcpyAsync((char*)out + u0 * p.ob, od, n * p.ob, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      if (cudaMemcpyAsync((char*)out + u0 * p.ob, od, n * p.ob, cudaMemcpyDeviceToHost, gs[g]) != cudaSuccess)
         return DA_ECUDA;
       cudaEvent_t done = event();
-      if (!done || cudaEventRecord(done, s) != cudaSuccess || cudaStreamWaitEvent(st, done, 0) != cudaSuccess)
+      if (!done || cudaEventRecord(done, gs[g]) != cudaSuccess || cudaStreamWaitEvent(st, done, 0) != cudaSuccess)
         return DA_ECUDA;
     }
     return DA_OK;
   };
   const int r = run();
   for (cudaEvent_t x : ev) cudaEventDestroy(x);   // released once the work that uses them has run
-  for (cudaStream_t x : gs) cudaStreamDestroy(x);
+  if (r == DA_OK) give_streams(gs);               // their work is ordered before the caller's stream
+  else
+    for (cudaStream_t x : gs) cudaStreamDestroy(x);
   return r;
 }
 
