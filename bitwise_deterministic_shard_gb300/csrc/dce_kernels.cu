@@ -14,7 +14,6 @@
 #include <cuda_bf16.h>
 #include <cooperative_groups.h>
 #include "numerics.cuh"
-#include "divide.cuh"
 #include "fdiv.cuh"
 #include "den_acc.cuh"
 #include "pack2.cuh"
@@ -243,9 +242,10 @@ __global__ void dce_finalize_kernel(const DceArgs a) {
 // ("mean").  A logit above the rowmax is clamped like the forward's (violation flag); NaN
 // propagates.  Streaming: 2 B or 4 B read and 2 B or 4 B written per logit; one CTA covers
 // BW_CHUNK columns of one row.  The quotient is rounded to binary32 on the FP32 pipe from the
-// row's split divisor with a residual certificate (fdiv.cuh) and divided exactly (integer
-// pipe, divide.cuh) only when that rounding is not certain (a quotient within about 2^-15
-// binary32 ulp of a half-way point, or a subnormal one).
+// row's split divisor with a residual certificate (fdiv.cuh), and divided in binary64 only
+// when that rounding is not certain (a quotient within about 2^-15 binary32 ulp of a
+// half-way point, or a subnormal one) or the operands are special.  The divisor setup is a
+// few conversions for one thread of the CTA, with no division.
 // 16 logits a thread and eight CTAs an SM (32 registers): occupancy decides this kernel, whose
 // loads of a thread are all issued before its arithmetic (measured on the 4096 x V128256 f32
 // rows: 0.73 ms against 0.92 ms with 32 logits a thread at 64 registers)
@@ -258,9 +258,8 @@ template <int DT, bool VEC>
 __global__ void __launch_bounds__(BW_THREADS, BW_MINB) dce_backward_kernel(const DceArgs a, const float* __restrict__ grad,
                                                                   int reduction, void* __restrict__ dlogits) {
   using T = typename In<DT>::T;
-  __shared__ idiv::Divisor sdiv;
   __shared__ fdiv::FpDivisor sfd;
-  __shared__ int sslow, sfast;
+  __shared__ int sfast;
   __shared__ float sgo;
   const int64_t nch = (a.V + BW_CHUNK - 1) / BW_CHUNK;
   const int64_t i = blockIdx.x / nch, c0 = (blockIdx.x % nch) * BW_CHUNK;
@@ -269,21 +268,15 @@ __global__ void __launch_bounds__(BW_THREADS, BW_MINB) dce_backward_kernel(const
   const int nv = (int)(a.V - c0 < BW_CHUNK ? a.V - c0 : BW_CHUNK);
   const float m = a.m_in[i];
   const double d64 = a.denom[i];
-  if (threadIdx.x == 0) {   // the row's divisor, once per CTA: both forms
-    uint64_t dm;
-    int de;
-    const bool ok = d64 > 0.0 && idiv::split_f64((uint64_t)__double_as_longlong(d64), dm, de);
-    sslow = !ok;   // zero, subnormal, negative, infinite or NaN denominators divide in binary64
-    if (ok) sdiv = idiv::make_divisor(dm, de);
+  if (threadIdx.x == 0) {   // the row's divisor, once per CTA (a few conversions, no division)
     sfast = fdiv::make_fp_divisor(d64, sfd);   // d in [2^-60, 2^60]: the FP32-pipe quotient
     float g0 = reduction == 0 ? grad[i] : grad[0];
     if (reduction == 2) g0 = __double2float_rn(__ddiv_rn((double)g0, (double)a.N));   // once per CTA
     sgo = g0;
   }
   __syncthreads();
-  const idiv::Divisor Dv = sdiv;
   const fdiv::FpDivisor F = sfd;
-  const bool slow = sslow, fast = sfast;
+  const bool fast = sfast;
   const float go = sgo;
   const int64_t tg64 = a.targets[i] - a.v_base - c0;   // the target's column within this chunk (any value)
   const int tg = tg64 >= 0 && tg64 < nv ? (int)tg64 : -1;
@@ -292,8 +285,9 @@ __global__ void __launch_bounds__(BW_THREADS, BW_MINB) dce_backward_kernel(const
   // exp32_det_poly(max(x, -104)) = (pp, k) and the FP32-pipe quotient of pp by the row's
   // denominator (candidate bits qb, residual estimate dl; fdiv.cuh).  Fast path: the weight is
   // exp32_det's pp 2^k (exact for k >= -125), so RN32(RN64(w / d)) is the certified quotient of
-  // pp times 2^k when that is a normal binary32.  The exact division and the special cases
-  // (NaN, deep or zero weights, special denominators, an uncertain rounding) otherwise.
+  // pp times 2^k when that is a normal binary32.  Otherwise (NaN, deep or zero weights, special
+  // denominators, an uncertain rounding: rare) the binary64 division, correctly rounded, so
+  // RN32 of its result is the contract's quotient by definition.
   auto fin = [&](float x, int k, uint32_t qb, float dl, int v) -> float {
     // the common case: x in [-86.5, -0] (one unsigned test on its bits: not NaN, not infinite,
     // not above the maximum), so k >= -125 and the weight p 2^k is exact and normal; the
@@ -308,16 +302,7 @@ __global__ void __launch_bounds__(BW_THREADS, BW_MINB) dce_backward_kernel(const
         x = 0.0f;
       }
       const float w = x != x ? x : exp32_det_nb(x);
-      if (!slow && w > 0.0f) {
-        uint32_t mw;
-        int ew;
-        idiv::split_f32_24(__float_as_uint(w), mw, ew);
-        p = __uint_as_float(idiv::div_f32_rn32(mw, ew, Dv));
-      } else if (!slow && w == 0.0f) {
-        p = 0.0f;   // +0 / a positive denominator
-      } else {
-        p = __double2float_rn(__ddiv_rn((double)w, d64));   // NaN weight or a special denominator
-      }
+      p = __double2float_rn(__ddiv_rn((double)w, d64));
     }
     const float g = v == tg ? __fsub_rn(p, 1.0f) : p;
     return __fmul_rn(go, g);

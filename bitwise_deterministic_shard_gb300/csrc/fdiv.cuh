@@ -3,7 +3,7 @@
 // The cross-entropy gradient divides every weight of a row by the row's binary64
 // denominator (det-cross-entropy "Method": softmax(x_i) = w / denom, one RN64 and one RN32;
 // the quotient then feeds the binary32 gradient).  The divisor is split once per row into
-// d_hi = RN32(d), d_lo = RN32(d - d_hi) and r = RN32(RN64(1 / d_hi)); each quotient then
+// d_hi = RN32(d), d_lo = RN32(d - d_hi) and r = RN32(1 / d_hi); each quotient then
 // takes one multiply and five fused multiply-adds:
 //   q0 = RN(p r)                      (within about 2 units of 2^-24 of Q = p / d)
 //   e  = RN(p - q0 d_hi), e2 = RN(e - q0 d_lo)      (the residual p - q0 d)
@@ -47,7 +47,7 @@ DA_FD float sub_rn(float a, float b) { return __fsub_rn(a, b); }
 DA_FD uint32_t bits(float f) { return __float_as_uint(f); }
 DA_FD float from_bits(uint32_t u) { return __uint_as_float(u); }
 DA_FD float d2f_rn(double d) { return __double2float_rn(d); }
-DA_FD double inv_rn(double d) { return __ddiv_rn(1.0, d); }
+DA_FD float rcp_rn(float x) { return __frcp_rn(x); }   // correctly rounded, no FP64 instruction
 DA_FD double dsub_rn(double a, double b) { return __dsub_rn(a, b); }
 #else   // the host's IEEE operations (the host tests build with -ffp-contract=off)
 inline float fma_rn(float a, float b, float c) { return std::fmaf(a, b, c); }
@@ -64,7 +64,7 @@ inline float from_bits(uint32_t u) {
   return f;
 }
 inline float d2f_rn(double d) { return (float)d; }
-inline double inv_rn(double d) { return 1.0 / d; }
+inline float rcp_rn(float x) { return 1.0f / x; }
 inline double dsub_rn(double a, double b) { return a - b; }
 #endif
 
@@ -77,7 +77,7 @@ DA_FD bool make_fp_divisor(double d, FpDivisor& F) {
   if (!(d >= 0x1p-60 && d <= 0x1p60)) return false;
   F.hi = d2f_rn(d);
   F.lo = d2f_rn(dsub_rn(d, (double)F.hi));   // d - d_hi is exact (Sterbenz)
-  F.r = d2f_rn(inv_rn((double)F.hi));
+  F.r = rcp_rn(F.hi);   // within 2^-24 of 1 / d_hi, as the bound above takes it
   return true;
 }
 
