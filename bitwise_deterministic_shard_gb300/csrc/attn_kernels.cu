@@ -132,7 +132,14 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int h = blockIdx.y, b = blockIdx.z, hk = h / (a.Hq / a.Hkv);
+  // One query tile per CTA, the longest first: with causal masking tile q has q + 1 key
+  // tiles, and the blocks start roughly in index order, so the longest tiles of every head
+  // start first and the short ones fill the end of the launch (pairs of a long and a short
+  // tile, equal in work, left the last partial wave of the launch idle behind them).
+  const int ntq = (a.Sq + BM - 1) / BM, nbh = a.Hq * a.B;
+  const int tq = (int)blockIdx.x / nbh, bh = (int)blockIdx.x % nbh;
+  const int qtile = a.causal ? ntq - 1 - tq : tq;
+  const int h = bh % a.Hq, b = bh / a.Hq, hk = h / (a.Hq / a.Hkv);
   const T* qbase = (const T*)a.q + b * a.qs[0] + h * a.qs[1];
   const T* kbase = (const T*)a.k + b * a.ks[0] + hk * a.ks[1];
   const int64_t krow0 = ((int64_t)b * a.Hkv + hk) * a.Skv;
@@ -169,12 +176,11 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
 
   int nf = 0;
   uint32_t g_base = 0, tcount = 0;   // ring steps of earlier passes; key tiles seen by this thread's role
-  const int ntq = (a.Sq + BM - 1) / BM;
-  const int npass = (a.causal && (int)blockIdx.x != ntq - 1 - (int)blockIdx.x) ? 2 : 1;
+  const int npass = 1;
   if (warp >= NEPI) {   // ---------------- control warpgroup ----------------
     asm volatile("setmaxnreg.dec.sync.aligned.u32 32;" ::: "memory");
     for (int pass = 0; pass < npass; pass++) {
-      const int q0 = (pass == 0 ? ntq - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
+      const int q0 = qtile * BM;
       const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
       const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
       const uint32_t nsteps = (uint32_t)nkt * NDS;
@@ -217,7 +223,7 @@ __global__ void __launch_bounds__(RowmaxTcLayout<DP>::THREADS, 1) rowmax_tc_kern
   } else {   // ---------------- epilogue warps: thread = key, 8 query rows ----------------
     asm volatile("setmaxnreg.inc.sync.aligned.u32 112;" ::: "memory");
     for (int pass = 0; pass < npass; pass++) {
-      const int q0 = (pass == 0 ? ntq - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
+      const int q0 = qtile * BM;
       const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
       const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
     // ---- query slices into the resident B operand ----
@@ -835,8 +841,8 @@ static cudaError_t launch_rowmax_t(const AttnArgs& a, const KvPrep& p, cudaStrea
       cudaFuncSetAttribute(rowmax_tc_kernel<DT, DP, STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int nt = (a.Sq + L::BM - 1) / L::BM;
-  dim3 grid(a.causal ? (nt + 1) / 2 : nt, a.Hq, a.B);
-  rowmax_tc_kernel<DT, DP, STORE><<<grid, L::THREADS, smem, st>>>(a, p);
+  const int64_t nblocks = (int64_t)nt * a.Hq * a.B;   // one query tile per CTA
+  rowmax_tc_kernel<DT, DP, STORE><<<(unsigned)nblocks, L::THREADS, smem, st>>>(a, p);
   return cudaGetLastError();
 }
 
