@@ -143,6 +143,11 @@ DA_HD double make_f64(bool neg, uint64_t m, int e) {
 #endif
 }
 
+// The binary32-numerator routines below (split_f32_24, div_f32_rn32, div_f32_rn32_direct)
+// served the cross-entropy gradient before its quotient moved to the FP32 pipe (fdiv.cuh);
+// no kernel calls them now.  They stay as the host tests' exact integer reference for that
+// quotient (checked themselves against exact rationals).
+
 // A nonzero binary32 magnitude as mw 2^ew with mw in [2^23, 2^24).
 DA_HD void split_f32_24(uint32_t bits, uint32_t& mw, int& ew) {
   const int be = (int)((bits >> 23) & 0xFF);
