@@ -418,8 +418,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": statistics.mean(e2e_ms)},
         # per step: V columns, key + V prep, rowmax (storing scores), the work order (item keys,
-        # order), accumulate
-        "gpu_launches": 6 * args.steps,
+        # classes, placement), accumulate
+        "gpu_launches": 7 * args.steps,
         "dce": dce,
         "wall_s_timed_region": wall,
     }

@@ -290,10 +290,17 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // This CTA's work item: query-tile pair (causal) or query tile bx of head h, batch b, taken
-  // from a.order when it is set (the heaviest items first), else in launch order.
+  // from a.order when it is set (the heaviest items first; part 2 or 1: the pair's long or
+  // short tile alone; an unused slot ends the CTA at once), else in launch order.
   const int ntq = (a.Sq + BM - 1) / BM;
   const int nx = a.causal ? (ntq + 1) / 2 : ntq;
-  const int item = a.order ? __ldg(a.order + blockIdx.x) : (int)blockIdx.x;
+  int item = (int)blockIdx.x, part = 0;
+  if (a.order) {
+    const int v = __ldg(a.order + blockIdx.x);
+    if (v < 0) return;   // uniform over the CTA, before any barrier or TMEM allocation
+    item = v & 0x1FFFFFFF;
+    part = v >> 29;
+  }
   const int bx = item % nx, h = (item / nx) % a.Hq, b = item / (nx * a.Hq), hk = h / (a.Hq / a.Hkv);
   __shared__ int s_hb[2];
   if (tid == 0) {
@@ -369,7 +376,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
   tc5::fence_after();
 
   int nf = 0, viol = 0;
-  const int npass = (a.causal && bx != ntq - 1 - bx) ? 2 : 1;
+  const int npass = (part == 0 && a.causal && bx != ntq - 1 - bx) ? 2 : 1;
   // Register split: the control warpgroup (copies, MMA issue) runs on 32 registers a thread,
   // the four compute warpgroups on 112 (640 x 96 at launch = 128 x 32 + 512 x 112).  Each
   // role runs its own pass loop; named barrier 2 opens a pass (query operand and per-pass
@@ -379,7 +386,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
     uint32_t tc = 0;   // key tiles of earlier passes
     uint32_t pc = 0;   // SC: PV buffer pairs of earlier passes
     for (int pass = 0; pass < npass; pass++) {
-      const int q0 = (pass == 0 ? ntq - 1 - bx : bx) * BM;
+      const int q0 = (part == 1 || (part == 0 && pass == 1) ? bx : ntq - 1 - bx) * BM;
       const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
       const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
       tc5::bar_sync(2, L::THREADS);
@@ -456,7 +463,7 @@ __global__ void __launch_bounds__(AccTpLayout::THREADS, 1) accumulate_tp_kernel(
     uint32_t tc = 0;   // key tiles of earlier passes
     uint32_t pcd = 0;   // SC: the next PV buffer pair to drain (pairs of earlier passes included)
     for (int pass = 0; pass < npass; pass++) {
-      const int q0 = (pass == 0 ? ntq - 1 - bx : bx) * BM;
+      const int q0 = (part == 1 || (part == 0 && pass == 1) ? bx : ntq - 1 - bx) * BM;
       const int hi = a.causal ? min(a.kv_hi, q0 + BM) : a.kv_hi;
       const int nkt = hi > a.kv_lo ? (hi - a.kv_lo + KTILE - 1) / KTILE : 0;
       const int nrows = min(BM, a.Sq - q0);
@@ -1041,7 +1048,8 @@ static cudaError_t launch_acc_tp_t(const AttnArgs& a, const KvPrep& p, cudaStrea
   if (e != cudaSuccess) return e;
   const int nt = (a.Sq + L::BM - 1) / L::BM;
   const int64_t nitems = (int64_t)(a.causal ? (nt + 1) / 2 : nt) * a.Hq * a.B;   // one CTA per work item
-  accumulate_tp_kernel<DT, SC><<<(unsigned)nitems, L::THREADS, L::bytes, st>>>(a, p);
+  const int64_t nblocks = nitems + (a.order ? a.order_extra : 0);
+  accumulate_tp_kernel<DT, SC><<<(unsigned)nblocks, L::THREADS, L::bytes, st>>>(a, p);
   return cudaGetLastError();
 }
 
@@ -1076,30 +1084,72 @@ __global__ void tp_item_keys_kernel(const AttnArgs a, int nx, int nitems, int* k
   atomicMax(gmax, key);
 }
 
-__global__ void tp_item_order_kernel(int nitems, const int* keys, int* counters, int* order) {
+// Then the light items; last, split in two, the k pairs of each (b, h) with the largest bx
+// (their two tiles near the middle of the sequence, so the halves are near equal), long
+// halves before short ones, so the end of the launch is made of the smallest items (k = the
+// SMs over the heads, about one wave of halves).  Classes: 0 heavy, 1 light, 2 split.
+__global__ void tp_item_class_kernel(const AttnArgs a, int nx, int nitems, int ksplit, const int* keys, int* counters,
+                                     unsigned char* cls) {
   const int it = blockIdx.x * blockDim.x + threadIdx.x;
   if (it >= nitems) return;
+  const int ntq = (a.Sq + AccTpLayout::BM - 1) / AccTpLayout::BM, bx = it % nx;
   const int thr = float_key(__fsub_rn(key_float(counters[0]), 10.0f));
-  const int pos = keys[it] >= thr ? atomicAdd(&counters[1], 1) : nitems - 1 - atomicAdd(&counters[2], 1);
-  order[pos] = it;
+  const int c = keys[it] >= thr ? 0 : (a.causal && bx >= nx - ksplit && bx != ntq - 1 - bx ? 2 : 1);
+  cls[it] = (unsigned char)c;
+  atomicAdd(&counters[1 + c], 1);
+}
+
+__global__ void tp_item_place_kernel(int nitems, int nslots, const unsigned char* cls, int* counters, int* order) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= nslots) return;
+  const int nh = counters[1], nl = counters[2], ns = counters[3];
+  if (t >= nitems + ns) order[t] = -1;   // an unused slot (fewer pairs split than reserved)
+  if (t >= nitems) return;
+  const int c = cls[t];
+  if (c == 0) {
+    order[atomicAdd(&counters[4], 1)] = t;
+  } else if (c == 1) {
+    order[nh + atomicAdd(&counters[5], 1)] = t;
+  } else {
+    const int q = atomicAdd(&counters[6], 1);
+    order[nh + nl + q] = t | (1 << 30);        // the long tile
+    order[nh + nl + ns + q] = t | (1 << 29);   // the short tile
+  }
+}
+
+static int tp_ksplit(const AttnArgs& a) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 1;
+  }
+  if (!a.causal) return 0;
+  const int bh = a.Hq * a.B;
+  return min(tp_nx(a) / 4, (sms + bh - 1) / bh);
 }
 
 size_t tp_order_bytes(const AttnArgs& a) {
-  const int64_t nitems = (int64_t)tp_nx(a) * a.Hq * a.B;
-  return 16 + (size_t)nitems * 8;
+  const int64_t nitems = (int64_t)tp_nx(a) * a.Hq * a.B, nslots = nitems + (int64_t)tp_ksplit(a) * a.Hq * a.B;
+  return 32 + (size_t)nitems * 4 + (((size_t)nitems + 15) & ~(size_t)15) + (size_t)nslots * 4;
 }
 
 cudaError_t launch_tp_order(AttnArgs& a, void* ws, cudaStream_t st) {
   const int64_t nitems = (int64_t)tp_nx(a) * a.Hq * a.B;
-  int* counters = (int*)ws;   // largest key (+0 to start), heavy and light positions taken
-  int* keys = counters + 4;
-  int* order = keys + nitems;
-  cudaError_t e = cudaMemsetAsync(counters, 0, 16, st);
+  const int ksplit = tp_ksplit(a);
+  const int64_t nslots = nitems + (int64_t)ksplit * a.Hq * a.B;
+  int* counters = (int*)ws;   // largest key (+0 to start); heavy, light, split counts; their positions taken
+  int* keys = counters + 8;
+  unsigned char* cls = (unsigned char*)(keys + nitems);
+  int* order = (int*)(cls + ((nitems + 15) & ~(int64_t)15));
+  cudaError_t e = cudaMemsetAsync(counters, 0, 32, st);
   if (e != cudaSuccess) return e;
-  const unsigned blocks = (unsigned)((nitems + 255) / 256);
+  const unsigned blocks = (unsigned)((nitems + 255) / 256), sblocks = (unsigned)((nslots + 255) / 256);
   tp_item_keys_kernel<<<blocks, 256, 0, st>>>(a, tp_nx(a), (int)nitems, keys, counters);
-  tp_item_order_kernel<<<blocks, 256, 0, st>>>((int)nitems, keys, counters, order);
+  tp_item_class_kernel<<<blocks, 256, 0, st>>>(a, tp_nx(a), (int)nitems, ksplit, keys, counters, cls);
+  tp_item_place_kernel<<<sblocks, 256, 0, st>>>((int)nitems, (int)nslots, cls, counters, order);
   a.order = order;
+  a.order_extra = (int)(nslots - nitems);
   return cudaGetLastError();
 }
 

@@ -29,7 +29,10 @@ struct AttnArgs {
                                  // accumulate reads it instead of recomputing the scores
   int64_t sc_per_bh;             // score-cache blocks per (b, query head)
   int sc_nkt;                    // non-causal: key tiles per query tile
-  const int* order;              // tensor-PV accumulate: its work items in this order (null: launch order)
+  const int* order;              // tensor-PV accumulate: its work items in this order (null: launch order);
+                                 // an entry is a pair index, with bit 30 for its long tile alone or bit
+                                 // 29 for its short tile alone, or -1 for an unused slot
+  int order_extra;               // CTAs the order holds beyond one per pair (split pairs, unused slots)
 };
 
 // Score cache of one whole-range call (kv_lo = 0, kv_hi = Skv; causal needs Sq = Skv): the
