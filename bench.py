@@ -44,7 +44,7 @@ UNIT = "MAC/s"
 # --heads 4 --dce-rows 256 --steps 1 --warmup 1 --no-cpu-baseline --no-sharded` under ncu, -k
 # regex:accumulate_tp -s 1 -c 1) scaled by 4 (the traffic is per head: the score cache, the V digit
 # planes and the output of each head).  None whenever the kernel has changed since that capture.
-ACC_TRAFFIC_PER_LAUNCH = 4 * (189_347_840 + 7_944_704)
+ACC_TRAFFIC_PER_LAUNCH = 4 * (189_380_608 + 8_980_224)
 
 
 def _peaks():
