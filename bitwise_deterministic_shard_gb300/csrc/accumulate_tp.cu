@@ -1086,8 +1086,9 @@ __global__ void tp_item_keys_kernel(const AttnArgs a, int nx, int nitems, int* k
 
 // Then the light items; last, split in two, the k pairs of each (b, h) with the largest bx
 // (their two tiles near the middle of the sequence, so the halves are near equal), long
-// halves before short ones, so the end of the launch is made of the smallest items (k = the
-// SMs over the heads, about one wave of halves).  Classes: 0 heavy, 1 light, 2 split.
+// halves before short ones, so the end of the launch is made of the smallest items (k = half
+// the SMs over the heads: about one wave of halves, at most a quarter of the pairs).
+// Classes: 0 heavy, 1 light, 2 split.
 __global__ void tp_item_class_kernel(const AttnArgs a, int nx, int nitems, int ksplit, const int* keys, int* counters,
                                      unsigned char* cls) {
   const int it = blockIdx.x * blockDim.x + threadIdx.x;
@@ -1126,7 +1127,7 @@ static int tp_ksplit(const AttnArgs& a) {
   }
   if (!a.causal) return 0;
   const int bh = a.Hq * a.B;
-  return min(tp_nx(a) / 4, (sms + bh - 1) / bh);
+  return min(tp_nx(a) / 4, max(1, (sms + bh - 1) / bh / 2));
 }
 
 size_t tp_order_bytes(const AttnArgs& a) {
