@@ -73,6 +73,9 @@ CASES = [
     (1, 2, 2, 70, 256, torch.bfloat16, True),
     (1, 2, 1, 90, 64, torch.float32, False),
     (1, 2, 2, 66, 128, torch.float32, True),
+    # causal, 15 query tiles of 16 rows (ragged last tile): the pass-2 work order splits the
+    # pair beside the middle tile into two single-tile CTAs and leaves the middle one whole
+    (1, 2, 2, 235, 128, torch.bfloat16, True),
     (1, 1, 1, 1, 16, torch.bfloat16, False),
     (1, 2, 2, 65, 200, torch.float32, False),
 ]
