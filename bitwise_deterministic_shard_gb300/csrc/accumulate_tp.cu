@@ -1057,7 +1057,7 @@ static cudaError_t launch_acc_tp_t(const AttnArgs& a, const KvPrep& p, cudaStrea
 // A work item whose rows have a rowmax far above the rest of their scores has most of its
 // weights below the 2^-56 window, and those take the exact per-pair path: such an item runs
 // several times longer than the others.  Launched late it leaves the GPU idle behind it, so the
-// items whose largest rowmax lies within 10 of the largest of the call go first.  The order
+// items whose largest rowmax lies within 5 of the largest of the call go first.  The order
 // only schedules the same work: the output does not depend on it.
 static int tp_nx(const AttnArgs& a) {
   const int nt = (a.Sq + AccTpLayout::BM - 1) / AccTpLayout::BM;
@@ -1094,7 +1094,7 @@ __global__ void tp_item_class_kernel(const AttnArgs a, int nx, int nitems, int k
   const int it = blockIdx.x * blockDim.x + threadIdx.x;
   if (it >= nitems) return;
   const int ntq = (a.Sq + AccTpLayout::BM - 1) / AccTpLayout::BM, bx = it % nx;
-  const int thr = float_key(__fsub_rn(key_float(counters[0]), 10.0f));
+  const int thr = float_key(__fsub_rn(key_float(counters[0]), 5.0f));
   const int c = keys[it] >= thr ? 0 : (a.causal && bx >= nx - ksplit && bx != ntq - 1 - bx ? 2 : 1);
   cls[it] = (unsigned char)c;
   atomicAdd(&counters[1 + c], 1);
