@@ -1118,13 +1118,15 @@ __global__ void tp_item_place_kernel(int nitems, int nslots, const unsigned char
   }
 }
 
+static int current_device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 1;
+  return n;
+}
+
 static int tp_ksplit(const AttnArgs& a) {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      sms = 1;
-  }
+  static const int sms = current_device_sms();   // initialised once, safe under concurrent first calls
   if (!a.causal) return 0;
   const int bh = a.Hq * a.B;
   return min(tp_nx(a) / 4, max(1, (sms + bh - 1) / bh / 2));
